@@ -1,0 +1,176 @@
+// C ABI entry points of libkda (declared and documented in include/kda.h).
+//
+// Every call validates its arguments on the host and enqueues nothing when it
+// rejects them; no call allocates, frees or synchronises.  There is no
+// fallback path (cuLA PR #110, "feat(cp): add opt-in NVSHMEM CP state handoff",
+// §Supported configuration: request an error instead of fallback).
+#include <cstdint>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return KDA_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return KDA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Structural checks of a host plan (cheap, O(header)).
+bool plan_ok(const int32_t *plan)
+{
+    if (!plan) return false;
+    if (plan[KDA_PH_MAGIC] != KDA_PLAN_MAGIC || plan[KDA_PH_VERSION] != KDA_PLAN_VERSION) return false;
+    if (plan[KDA_PH_C] != KDA_CHUNK || plan[KDA_PH_T] < 1 || plan[KDA_PH_N] < 1 || plan[KDA_PH_S] < 1)
+        return false;
+    if (plan[KDA_PH_NPIECES] < plan[KDA_PH_S] || plan[KDA_PH_NCONT] < 0 || plan[KDA_PH_NFIN] < 0) return false;
+    if (plan[KDA_PH_TCONT] < 0 || plan[KDA_PH_TCONT] > plan[KDA_PH_T]) return false;
+    if (plan[KDA_PH_NITEMS] != plan[KDA_PH_NPIECES] + plan[KDA_PH_NCONT]) return false;
+    for (int i = KDA_PH_OFF_BOUNDS; i <= KDA_PH_OFF_FIN; ++i)
+        if (plan[i] < KDA_PLAN_HEADER_WORDS || plan[i] > plan[KDA_PH_TOTAL]) return false;
+    return true;
+}
+
+size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+bool layout(const int32_t *plan, int32_t H, size_t off[6])
+{
+    if (!plan_ok(plan) || H < 1) return false;
+    const size_t h = static_cast<size_t>(H), K = kda::KD, V = kda::VD;
+    const size_t sizes[5] = {
+        h * static_cast<size_t>(plan[KDA_PH_TCONT]) * K * 4,     // qhat
+        static_cast<size_t>(plan[KDA_PH_NFIN]) * h * K * K * 4,  // fin transitions
+        static_cast<size_t>(plan[KDA_PH_S]) * h * K * K * 4,     // A
+        static_cast<size_t>(plan[KDA_PH_S]) * h * K * V * 4,     // B
+        static_cast<size_t>(plan[KDA_PH_S]) * h * K * V * 4,     // S_in
+    };
+    size_t pos = 0;
+    for (int i = 0; i < 5; ++i) {
+        off[i] = pos;
+        pos = round256(pos + sizes[i]);
+    }
+    off[5] = pos;
+    return true;
+}
+
+bool inputs_ok(const void *q, const void *k, const void *v, const float *g, const float *beta,
+               const float *h0)
+{
+    if (!q || !k || !v || !g || !beta) return false;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta)) return false;
+    if (h0 && !aligned16(h0)) return false;
+    return true;
+}
+
+kda::Workspace carve(void *ws, const size_t off[6])
+{
+    char *b = static_cast<char *>(ws);
+    return kda::Workspace{reinterpret_cast<float *>(b + off[0]), reinterpret_cast<float *>(b + off[1]),
+                          reinterpret_cast<float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
+                          reinterpret_cast<float *>(b + off[4])};
+}
+
+// Bytes of the qhat + fin regions that the three-call path needs.
+size_t boundary_bytes(const size_t off[6]) { return off[2]; }
+
+}  // namespace
+
+extern "C" const char *kda_status_string(int status)
+{
+    switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KDA_ERR_WORKSPACE: return "buffer too small";
+    case KDA_ERR_CUDA: return "CUDA error";
+    case KDA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6])
+{
+    if (!off) return KDA_ERR_INVALID_ARG;
+    return layout(plan, H, off) ? KDA_OK : KDA_ERR_INVALID_ARG;
+}
+
+extern "C" size_t kda_workspace_bytes(const int32_t *plan, int32_t H)
+{
+    size_t off[6];
+    return layout(plan, H, off) ? off[5] : 0;
+}
+
+extern "C" int kda_segment_forward(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                   const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                   const float *g, const float *beta, const float *h0, float scale,
+                                   kda_bf16 *o, float *A, float *B, float *final_state,
+                                   void *ws, size_t ws_bytes, void *stream)
+{
+    size_t off[6];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
+    if (!o || !A || !B || !final_state || !aligned16(o) || !aligned16(A) || !aligned16(B) ||
+        !aligned16(final_state))
+        return KDA_ERR_INVALID_ARG;
+    if (boundary_bytes(off) > 0 && (!ws || !aligned16(ws))) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < boundary_bytes(off)) return KDA_ERR_WORKSPACE;
+    const kda::Workspace w = carve(ws, off);
+    return cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B,
+                                                 final_state, w.qhat, w.afin,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int kda_compose_summaries(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                     const float *A, const float *B, const float *h0, float *S_in,
+                                     void *stream)
+{
+    size_t off[6];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!A || !B || !S_in || !aligned16(A) || !aligned16(B) || !aligned16(S_in)) return KDA_ERR_INVALID_ARG;
+    if (h0 && !aligned16(h0)) return KDA_ERR_INVALID_ARG;
+    return cuda_status(kda::launch_compose(plan, plan_dev, H, A, B, h0, S_in, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int kda_apply_boundary(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                  const float *S_in, const void *ws, size_t ws_bytes, kda_bf16 *o,
+                                  float *final_state, void *stream)
+{
+    size_t off[6];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!S_in || !o || !final_state || !aligned16(S_in) || !aligned16(o) || !aligned16(final_state))
+        return KDA_ERR_INVALID_ARG;
+    if (boundary_bytes(off) > 0 && (!ws || !aligned16(ws))) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < boundary_bytes(off)) return KDA_ERR_WORKSPACE;
+    const kda::Workspace w = carve(const_cast<void *>(ws), off);
+    return cuda_status(kda::launch_boundary(plan, plan_dev, H, S_in, w.qhat, w.afin, o, final_state,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int kda_forward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                     const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                     const float *g, const float *beta, const float *h0, float scale,
+                                     kda_bf16 *o, float *final_state, void *ws, size_t ws_bytes,
+                                     void *stream)
+{
+    size_t off[6];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
+    if (!o || !final_state || !aligned16(o) || !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < off[5]) return KDA_ERR_WORKSPACE;
+    const kda::Workspace w = carve(ws, off);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, w.A, w.B,
+                                                   final_state, w.qhat, w.afin, s));
+    if (rc != KDA_OK) return rc;
+    rc = cuda_status(kda::launch_compose(plan, plan_dev, H, w.A, w.B, h0, w.S_in, s));
+    if (rc != KDA_OK) return rc;
+    return cuda_status(kda::launch_boundary(plan, plan_dev, H, w.S_in, w.qhat, w.afin, o, final_state, s));
+}

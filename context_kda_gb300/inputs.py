@@ -12,23 +12,29 @@ summary-workspace example of cuLA PR #136 ("feat(kda): add cuDNN
 concatenated-summary Kimi CP", §Latest cuDNN compatibility: CP64, H=32,
 K=V=128).  The pages publish no dataset; everything is drawn here.
 
-Recipe (seed 0, ``numpy.random.default_rng``, drawn in this order):
-  lengths (packed variable-length workload only): l_i = exp(U(ln 256, ln 8192)),
+Recipe (seed 0).  Every tensor has its own generator family, PCG64 seeded by
+``SeedSequence(seed, spawn_key=(tensor id, block))``; large tensors are drawn in
+blocks of 2^16 (token, head) rows, one generator per block, so the blocks can be
+drawn in parallel and the values do not depend on the thread count:
+  lengths (id 0; packed variable-length workload only): l_i = exp(U(ln 256, ln 8192)),
       rescaled to the requested total (floor, deficit given +1 each to the
       largest fractional parts, ties to the lower index);
-  q, k:  N(0,1) fp32, L2-normalised per (token, head) over K (norm taken in
-         fp64, no epsilon), rounded to bf16 (round-to-nearest-even);
-  v:     N(0,1) fp32 rounded to bf16;
-  g:     fp32 log-decay per key channel, U(lo, hi);
-  beta:  sigmoid(N(0,1)) in fp64, stored as fp32, one per (token, head);
-  h0:    optional fp32 N(0, std^2) initial state per sequence, [N,H,K,V].
+  q, k (ids 1, 2): N(0,1) fp32, L2-normalised per (token, head) over K (squared
+         norm accumulated in fp64, no epsilon; row times the fp32 reciprocal
+         norm), rounded to bf16 (round-to-nearest-even);
+  v (id 3): N(0,1) fp32 rounded to bf16;
+  g (id 4): fp32 log-decay per key channel, lo + (hi - lo) U(0,1);
+  beta (id 5): sigmoid(N(0,1)) in fp64, stored as fp32, one per (token, head);
+  h0 (id 6): optional fp32 N(0, std^2) initial state per sequence, [N,H,K,V].
 
 bf16 tensors are returned as ``uint16`` bit patterns; ``bf16_to_f32`` gives
 their exact fp32 values.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import math
+import os
 from dataclasses import dataclass, field
 from typing import Dict, List, Optional
 
@@ -37,6 +43,7 @@ import numpy as np
 K_DIM = 128
 V_DIM = 128
 CHUNK = 64
+_ROWS_PER_BLOCK = 1 << 16   # (token, head) rows drawn per independent block
 
 
 @dataclass(frozen=True)
@@ -59,6 +66,10 @@ class Workload:
         return int(sum(self.seqlens))
 
 
+def _block_rng(seed: int, tensor_id: int, block: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(tensor_id, block))))
+
+
 def draw_lengths(rng: np.random.Generator, count: int, lo: float, hi: float, total: int) -> List[int]:
     """Log-uniform lengths rescaled to sum exactly to ``total``."""
     raw = np.exp(rng.uniform(math.log(lo), math.log(hi), size=count))
@@ -74,8 +85,7 @@ def draw_lengths(rng: np.random.Generator, count: int, lo: float, hi: float, tot
 
 
 def _packed_lengths() -> tuple:
-    rng = np.random.default_rng(0)
-    return tuple(draw_lengths(rng, 24, 256.0, 8192.0, 65536))
+    return tuple(draw_lengths(_block_rng(0, 0, 0), 24, 256.0, 8192.0, 65536))
 
 
 def workloads() -> Dict[str, Workload]:
@@ -113,15 +123,33 @@ def bf16_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _l2_normalised_bf16(x: np.ndarray, block: int = 1 << 16) -> np.ndarray:
-    """Per-row L2 normalisation over the last axis (norm in fp64), then bf16."""
-    flat = x.reshape(-1, x.shape[-1])
-    out = np.empty(flat.shape, dtype=np.uint16)
-    for s in range(0, flat.shape[0], block):
-        blk = flat[s:s + block].astype(np.float64)
-        nrm = np.sqrt(np.einsum("ij,ij->i", blk, blk))
-        out[s:s + block] = f32_to_bf16_bits((blk / nrm[:, None]).astype(np.float32))
-    return out.reshape(x.shape)
+def _l2_normalised_bf16(x: np.ndarray) -> np.ndarray:
+    """Per-row L2 normalisation over the last axis (squared norm accumulated in fp64, the row
+    scaled by the fp32 reciprocal of the norm), then bf16."""
+    nrm = np.sqrt(np.einsum("ij,ij->i", x, x, dtype=np.float64))
+    return f32_to_bf16_bits(x * (1.0 / nrm).astype(np.float32)[:, None])
+
+
+def _draw_rows(seed: int, tensor_id: int, rows: int, width: int, kind: str) -> np.ndarray:
+    """rows x width array filled block by block; block b of 2^16 rows comes from its own
+    generator (seed, spawn key (tensor_id, b))."""
+    out = np.empty((rows, width), dtype=np.float32 if kind == "u01" else np.uint16)
+    nblk = (rows + _ROWS_PER_BLOCK - 1) // _ROWS_PER_BLOCK
+
+    def one(b):
+        lo, hi = b * _ROWS_PER_BLOCK, min(rows, (b + 1) * _ROWS_PER_BLOCK)
+        rng = _block_rng(seed, tensor_id, b)
+        if kind == "bf16n":      # N(0,1), L2-normalised per row, bf16
+            out[lo:hi] = _l2_normalised_bf16(rng.standard_normal((hi - lo, width), dtype=np.float32))
+        elif kind == "bf16":     # N(0,1), bf16
+            out[lo:hi] = f32_to_bf16_bits(rng.standard_normal((hi - lo, width), dtype=np.float32))
+        else:                    # U(0,1) fp32
+            out[lo:hi] = rng.random((hi - lo, width), dtype=np.float32)
+
+    workers = min(16, max(1, os.cpu_count() or 1), max(1, nblk))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(one, range(nblk)))
+    return out
 
 
 @dataclass
@@ -151,27 +179,27 @@ class Inputs:
 def make_inputs(seqlens, heads: int, segments: int, g_lo: float = -0.05, g_hi: float = -0.001,
                 h0_std: float = 0.0, seed: int = 0, K: int = K_DIM, V: int = V_DIM,
                 draw_lengths_spec: Optional[tuple] = None) -> Inputs:
-    """Draw q, k, v, g, beta (and h0) in the fixed order with ``default_rng(seed)``."""
-    rng = np.random.default_rng(seed)
+    """Draw lengths (when asked), q, k, v, g, beta and h0 from ``seed`` (recipe above)."""
     if draw_lengths_spec is not None:
         count, lo, hi, total = draw_lengths_spec
-        seqlens = draw_lengths(rng, count, lo, hi, total)
+        seqlens = draw_lengths(_block_rng(seed, 0, 0), count, lo, hi, total)
     seqlens = [int(x) for x in seqlens]
     T = int(sum(seqlens))
     H = int(heads)
     cu = np.zeros(len(seqlens) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(seqlens)
-    q = _l2_normalised_bf16(rng.standard_normal((T, H, K), dtype=np.float32))
-    k = _l2_normalised_bf16(rng.standard_normal((T, H, K), dtype=np.float32))
-    v = f32_to_bf16_bits(rng.standard_normal((T, H, V), dtype=np.float32))
-    u = rng.random((T, H, K), dtype=np.float32)
+    q = _draw_rows(seed, 1, T * H, K, "bf16n").reshape(T, H, K)
+    k = _draw_rows(seed, 2, T * H, K, "bf16n").reshape(T, H, K)
+    v = _draw_rows(seed, 3, T * H, V, "bf16").reshape(T, H, V)
+    u = _draw_rows(seed, 4, T * H, K, "u01").reshape(T, H, K)
     g = (np.float32(g_lo) + np.float32(g_hi - g_lo) * u).astype(np.float32)
     del u
-    logits = rng.standard_normal((T, H), dtype=np.float32).astype(np.float64)
+    logits = _block_rng(seed, 5, 0).standard_normal((T, H), dtype=np.float32).astype(np.float64)
     beta = (1.0 / (1.0 + np.exp(-logits))).astype(np.float32)
     h0 = None
     if h0_std > 0.0:
-        h0 = (rng.standard_normal((len(seqlens), H, K, V), dtype=np.float32) * np.float32(h0_std)).astype(np.float32)
+        h0 = (_block_rng(seed, 6, 0).standard_normal((len(seqlens), H, K, V), dtype=np.float32)
+              * np.float32(h0_std)).astype(np.float32)
     return Inputs(cu, q, k, v, g, beta, h0, int(segments), H)
 
 

@@ -1,0 +1,232 @@
+/*
+ * kda.h -- C ABI of libkda: segment-parallel Kimi Delta Attention (KDA) forward
+ * on one GB300 (sm_103a).
+ *
+ * KDA is a gated delta-rule linear attention with a K x V recurrent state per
+ * (sequence, head):
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,
+ * with BF16 q/k/v and an FP32 state (cuLA PR #110, "feat(cp): add opt-in
+ * NVSHMEM CP state handoff", §Supported configuration), g a per-token,
+ * per-key-channel natural-log decay and beta a per-token scalar.
+ *
+ * Context parallelism on one GPU.  A packed token stream is cut into
+ * contiguous segments that play the role of context-parallel ranks.  Each
+ * segment runs the recurrence locally and publishes an FP32 affine boundary
+ * summary of the state crossing its end, S_end = A S_start + B, with a
+ * transition A (K x K) and a state update B (K x V) (PR #110 §Motivation:
+ * affine recurrence state per producer; cuLA PR #136, "feat(kda): add cuDNN
+ * concatenated-summary Kimi CP", §Summary: preceding_transition /
+ * preceding_state_update).  Summaries compose in FP32 as
+ * (A2,B2) o (A1,B1) = (A2 A1, A2 B1 + B2) (PR #136 §Summary) to give each
+ * segment its true incoming state S_in, and the outputs of the piece that
+ * continues a sequence from an earlier segment are fixed up with
+ * o_t += S_in^T qhat_t, where qhat_t = scale P_t^T q_t and P_t is the
+ * transition from the segment start through token t.
+ *
+ * Call sequence (PR #136 §Walkthrough, sequence diagram: plan, then run):
+ *   kda_plan_segments          host, integer only, reusable across calls
+ *   kda_segment_forward        local chunkwise recurrence + summaries + qhat
+ *   kda_compose_summaries      scan of the summaries -> S_in per segment
+ *   kda_apply_boundary         fix-up of continuing outputs and final states
+ *   kda_forward_segmented      the three device steps above, in order
+ *
+ * Conventions shared by every entry point
+ *   - Fixed sizes: K = V = 128 (key and value head dimensions), chunk C = 64.
+ *   - Tensors are contiguous, packed-THD, row-major:
+ *       q, k  [T][H][K] bf16      v [T][H][V] bf16      o [T][H][V] bf16
+ *       g     [T][H][K] fp32      beta [T][H] fp32
+ *       h0, final_state [N][H][K][V] fp32 (state layout K x V, "non-transposed",
+ *           PR #110 §Supported configuration); h0 == NULL means zeros
+ *       A [S][H][K][K] fp32, B / S_in [S][H][K][V] fp32 (separate typed
+ *           tensors, PR #136 §Latest cuDNN compatibility)
+ *     bf16 is passed as its 16-bit pattern (kda_bf16).
+ *   - The chunkwise form takes exp(+-Gamma), Gamma being the decay summed
+ *     within a 64-token chunk; each channel's per-chunk sum must stay above
+ *     about -80 (fp32 range), e.g. g >= -1.25 per token.
+ *   - Device pointers must be 16-byte aligned.  The library never allocates
+ *     or frees memory, never synchronises, and enqueues all device work on
+ *     the caller's CUDA stream ('stream' is a cudaStream_t; NULL = legacy
+ *     default stream).
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     rejected call enqueues nothing.  There is no fallback path: an
+ *     unsupported request returns KDA_ERR_UNSUPPORTED (PR #110 §Supported
+ *     configuration: request an error instead of fallback; PR #136 §Latest
+ *     cuDNN compatibility: fail early).
+ *   - Launch failures return KDA_ERR_CUDA; kda_last_cuda_error() gives the
+ *     underlying cudaError_t value.
+ *   - Each call takes the host plan (to size its grids without reading device
+ *     memory) and a device copy of the same words (plan_dev), which the caller
+ *     uploads once.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kda_bf16;
+
+enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,   /* bad pointer, size, alignment or plan */
+    KDA_ERR_UNSUPPORTED = -2,   /* valid request outside what is built (e.g. chunk != 64) */
+    KDA_ERR_WORKSPACE = -3,     /* caller buffer too small */
+    KDA_ERR_CUDA = -4,          /* a CUDA launch or API call failed */
+    KDA_ERR_TIMEOUT = -5        /* a bounded device-side wait expired */
+};
+
+enum { KDA_HEAD_DIM_K = 128, KDA_HEAD_DIM_V = 128, KDA_CHUNK = 64 };
+
+/* Plan format v1 (int32 words).  Header words: */
+enum {
+    KDA_PLAN_MAGIC = 0x4B444131,
+    KDA_PLAN_VERSION = 1,
+    KDA_PLAN_HEADER_WORDS = 32,
+    KDA_PH_MAGIC = 0, KDA_PH_VERSION = 1, KDA_PH_TOTAL = 2, KDA_PH_T = 3, KDA_PH_N = 4,
+    KDA_PH_S = 5, KDA_PH_C = 6, KDA_PH_NPIECES = 7, KDA_PH_NCONT = 8, KDA_PH_TCONT = 9,
+    KDA_PH_NFIN = 10, KDA_PH_NCHUNKS = 11, KDA_PH_NITEMS = 12, KDA_PH_MAXPIECE = 13,
+    KDA_PH_OFF_BOUNDS = 14, KDA_PH_OFF_CU = 15, KDA_PH_OFF_SEGS = 16, KDA_PH_OFF_PIECES = 17,
+    KDA_PH_OFF_ITEMS = 18, KDA_PH_OFF_CHUNKS = 19, KDA_PH_OFF_CONT = 20, KDA_PH_OFF_FIN = 21
+};
+/* Sections (in this order after the header):
+ *   seg_bounds [S+1]; cu_seqlens [N+1];
+ *   segs   [S][4]: sequence holding the segment's first token, flags
+ *                  (1 = segment starts a sequence, 2 = a sequence starts inside
+ *                  the segment, so its transition A is exactly 0), first piece,
+ *                  piece count;
+ *   pieces [n][8]: start, len, sequence, segment, flags (1 FIRST: starts its
+ *                  sequence; 2 CONT: continues a sequence from an earlier
+ *                  segment; 4 SEG_LAST; 8 SEQ_END), cont index or -1, qhat row
+ *                  or -1, fin index or -1; in (segment, start) order;
+ *   items  [m][2]: piece, kind (0 state columns for every piece, 1 transition
+ *                  columns for CONT pieces), sorted by (-len, piece, kind);
+ *   chunks [c][4]: piece, start, len, index in piece (every C tokens from the
+ *                  piece start);
+ *   cont   [n_cont][4]: piece, segment, qhat row (running sum of CONT lengths),
+ *                  len;
+ *   fin    [n_fin][4]:  piece, sequence, segment, cont index, for CONT pieces
+ *                  that end their sequence. */
+enum { KDA_SEG_STARTS_SEQ = 1, KDA_SEG_HAS_RESET = 2 };
+enum { KDA_PIECE_FIRST = 1, KDA_PIECE_CONT = 2, KDA_PIECE_SEG_LAST = 4, KDA_PIECE_SEQ_END = 8 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kda_status_string(int status);
+
+/* cudaError_t value behind the most recent KDA_ERR_CUDA on this thread (0 if none). */
+int kda_last_cuda_error(void);
+
+/*
+ * kda_plan_segments -- packed-THD segment plan (host, integer work only).
+ * PR #136 §Walkthrough: CPU-only plan construction and validation for balanced
+ * or custom contiguous shards, checked against sequence boundaries and
+ * invalid inputs; the plan is reusable (PR #136 §Summary).
+ *
+ *   cu_seqlens   host int32 [num_seqs+1]: 0 = cu[0] < cu[1] < ... (zero-length
+ *                sequences are rejected); T = cu[num_seqs].
+ *   num_segments S >= 1.
+ *   seg_bounds   host int32 [S+1] strictly increasing from 0 to T, or NULL for
+ *                balanced segments b_j = floor(j T / S) (then S <= T).
+ *   chunk        must be 64 (else KDA_ERR_UNSUPPORTED).
+ *   plan         host int32 buffer of *plan_len words, caller-owned; NULL to
+ *                query the size only.
+ *   plan_len     in: capacity in words; out: words the plan needs.
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, or
+ * KDA_ERR_WORKSPACE (capacity too small; *plan_len holds the size needed).
+ * Deterministic: the same arguments give the same words.
+ */
+int kda_plan_segments(const int32_t *cu_seqlens, int32_t num_seqs, int32_t num_segments,
+                      const int32_t *seg_bounds, int32_t chunk, int32_t *plan, size_t *plan_len);
+
+/*
+ * kda_workspace_layout -- byte offsets of the regions of the device workspace
+ * for a plan and head count.  off[0..5] = qhat, fin transitions, A, B, S_in,
+ * total.  Each region starts on a 256-byte boundary.
+ *   qhat   fp32 [H][T_cont][K]    transition-seen queries of continuing tokens
+ *   fin    fp32 [n_fin][H][K][K]  transitions of continuing pieces that end a sequence
+ *   A      fp32 [S][H][K][K]      (used by kda_forward_segmented)
+ *   B      fp32 [S][H][K][V]      (used by kda_forward_segmented)
+ *   S_in   fp32 [S][H][K][V]      (used by kda_forward_segmented)
+ * The three-call path uses only the qhat and fin regions; A, B and S_in are
+ * then caller tensors.  Returns KDA_OK or KDA_ERR_INVALID_ARG.
+ */
+int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6]);
+
+/* kda_workspace_bytes -- total device workspace bytes (off[5] above); 0 if the
+ * plan or H is invalid.  The summary part, A + B, is S*H*(K*K + K*V)*4 bytes:
+ * 256 MiB at S = 64, H = 32, K = V = 128 (PR #136 §Latest cuDNN compatibility). */
+size_t kda_workspace_bytes(const int32_t *plan, int32_t H);
+
+/*
+ * kda_segment_forward -- local chunkwise forward of every piece of every
+ * segment, plus the segment summaries (PR #110 §Motivation; PR #136 §Summary).
+ *   q, k, v, g, beta   inputs as above (device).
+ *   h0                 device fp32 [N][H][K][V] or NULL (zeros).
+ *   scale              query scale (1.0 for the plain recurrence).
+ *   o      out  bf16 [T][H][V]: exact outputs for pieces that start their
+ *               sequence; for continuing pieces the output of the local run
+ *               from a zero state (completed by kda_apply_boundary).
+ *   A      out  fp32 [S][H][K][K]: the segment's transition; exactly 0 when a
+ *               sequence starts inside the segment.
+ *   B      out  fp32 [S][H][K][V]: the state at the segment end when the
+ *               segment starts from a zero state (exact where the segment's
+ *               last piece starts its sequence).
+ *   final_state out fp32 [N][H][K][V]: exact for sequences whose last piece
+ *               starts the sequence; local (zero-start) end state otherwise
+ *               (completed by kda_apply_boundary).
+ *   ws, ws_bytes  device workspace; its qhat and fin regions are written.
+ */
+int kda_segment_forward(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                        const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                        const float *g, const float *beta, const float *h0, float scale,
+                        kda_bf16 *o, float *A, float *B, float *final_state,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * kda_compose_summaries -- incoming state of every segment, S_in, by composing
+ * the summaries in order (PR #136 §Summary: affine summary composition in
+ * FP32).  S_in[0] = h0 of the first sequence; S_in[j] = h0 of the sequence
+ * starting at b_j when one does; otherwise A[j-1] S_in[j-1] + B[j-1].
+ *   A, B   device fp32 summaries from kda_segment_forward.
+ *   h0     device fp32 [N][H][K][V] or NULL (zeros).
+ *   S_in   out device fp32 [S][H][K][V].
+ */
+int kda_compose_summaries(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                          const float *A, const float *B, const float *h0, float *S_in,
+                          void *stream);
+
+/*
+ * kda_apply_boundary -- fix-up from the incoming states: for every token t of
+ * a continuing piece in segment j, o_t = bf16(o_local,t + S_in[j]^T qhat_t);
+ * for every sequence that ends in a continuing piece of segment j,
+ * final = P_end S_in[j] + final_local.
+ *   S_in        device fp32 [S][H][K][V] from kda_compose_summaries.
+ *   ws          the workspace kda_segment_forward wrote (qhat and fin regions).
+ *   o           in/out bf16 [T][H][V].   final_state in/out fp32 [N][H][K][V].
+ */
+int kda_apply_boundary(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                       const float *S_in, const void *ws, size_t ws_bytes,
+                       kda_bf16 *o, float *final_state, void *stream);
+
+/*
+ * kda_forward_segmented -- the whole segmented forward: kda_segment_forward,
+ * kda_compose_summaries and kda_apply_boundary in order on 'stream', with A,
+ * B and S_in held in the workspace (kda_workspace_bytes(plan, H) bytes).
+ * Outputs o and final_state equal the monolithic recurrence of every sequence
+ * (PR #136 §Walkthrough: compared with a monolithic reference).
+ */
+int kda_forward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                          const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                          const float *g, const float *beta, const float *h0, float scale,
+                          kda_bf16 *o, float *final_state, void *ws, size_t ws_bytes,
+                          void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */
