@@ -1,0 +1,339 @@
+#!/usr/bin/env python3
+"""Throughput of the segmented KDA forward on GB300: one JSON line.
+
+A step is one pass of the whole hot path -- kda_segment_forward (chunk forward +
+summaries), kda_compose_summaries (scan) and kda_apply_boundary (fix-up) -- over
+one batch of the synthetic workload, inputs resident in HBM.  The L2 cache is
+flushed (a 256 MiB write) before every step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 is launched with torch.distributed.run: every rank runs its own copy of
+the workload (independent problems, no collective on the data path), so the
+value is the tokens of all ranks over the slowest rank's time ("weak" scaling).
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from context_kda_gb300.inputs import HEADLINE, bf16_to_f32, make_workload, workloads  # noqa: E402
+
+METRIC = "segmented KDA fwd tokens/sec (H=16,K=V=128) on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+K_DIM = V_DIM = 128
+CH = 64
+# algorithmic work per token-head (minimal counts): the state columns of the
+# chunk forward, and the transition columns a continuing token adds
+FLOPS_STATE = 6 * CH * K_DIM + 4 * CH * V_DIM + 6 * K_DIM * V_DIM          # 180,224
+FLOPS_TRANSITION = 6 * K_DIM * K_DIM + 2 * CH * K_DIM                      # 114,688
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12                      # 80.5: SMs x FP32 lanes x FMA x max clock
+CHUNK_KERNEL_SRC = os.path.join(ROOT, "context_kda_gb300", "csrc", "chunk_fwd.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "chunk_forward_t8192_h16_s4.md")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _profile_values(kernel_src):
+    """Figures recorded in the committed ncu summary, if it was taken on the current source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return {}
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(PROFILE_SUMMARY):
+        if line.startswith("- ") and ":" in line:
+            key, _, val = line[2:].partition(":")
+            vals[key.strip()] = val.strip().strip("`")
+    return vals if vals.get("kernel_source_sha256_16") == sha else {}
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[4:8]):
+                if p.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _oracle_pass(inp, nthreads):
+    import oracle
+    q, k, v = bf16_to_f32(inp.q), bf16_to_f32(inp.k), bf16_to_f32(inp.v)
+    t = time.perf_counter()
+    oracle.forward(inp.cu_seqlens, q, k, v, inp.g, inp.beta, h0=inp.h0, nthreads=nthreads, want_final=False)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(inp, budget_s=10.0, max_passes=8):
+    """The fp64 oracle (monolithic recurrence) on the host cores: full passes over the
+    workload until about budget_s seconds have been spent."""
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    times = []
+    while len(times) < max_passes and (not times or sum(times) < budget_s):
+        times.append(_oracle_pass(inp, cores))
+    tasks = inp.num_seqs * inp.heads
+    return {"value": inp.tokens / statistics.median(times), "unit": UNIT, "cores": min(cores, tasks),
+            "kind": "oracle",
+            "sample": f"full workload ({inp.tokens} tokens x {inp.heads} heads), fp64 token recurrence, "
+                      f"{len(times)} pass(es), median; OpenMP over {tasks} (sequence, head) tasks"}
+
+
+def _config(w, n):
+    return {"workload": w.name, "tokens": w.tokens, "heads": w.heads, "segments": w.segments,
+            "sequences": len(w.seqlens), "K": K_DIM, "V": V_DIM, "chunk": CH, "g_range": [w.g_lo, w.g_hi],
+            "h0_std": w.h0_std, "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas{n}"}
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = make_workload(w)
+    cores = len(os.sched_getaffinity(0))
+    # each step is one full pass of the oracle over the workload
+    for _ in range(args.warmup):
+        _oracle_pass(inp, cores)
+    times = [_oracle_pass(inp, cores) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = inp.tokens / (ms / 1e3)
+    tasks = inp.num_seqs * inp.heads
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, tasks), "kind": "oracle",
+                             "sample": f"full workload per step ({inp.tokens} tokens x {inp.heads} heads)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from context_kda_gb300 import binding as kda
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = make_workload(w)
+    T, H, N, S = inp.tokens, inp.heads, inp.num_seqs, inp.segments
+    to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt)
+    host = {"q": to(inp.q, torch.bfloat16), "k": to(inp.k, torch.bfloat16), "v": to(inp.v, torch.bfloat16),
+            "g": to(inp.g, torch.float32), "beta": to(inp.beta, torch.float32)}
+    if inp.h0 is not None:
+        host["h0"] = to(inp.h0, torch.float32)
+    d = {k_: v_.to(dev) for k_, v_ in host.items()}
+    h0 = d.get("h0")
+    plan = kda.kda_plan_segments(inp.cu_seqlens, S)
+    plan_dev = kda.upload_plan(plan, dev)
+    off = kda.kda_workspace_layout(plan, H)
+    ws = torch.empty(off[5], dtype=torch.uint8, device=dev)
+    A = ws[off[2]:off[3]].view(torch.float32)
+    B = ws[off[3]:off[4]].view(torch.float32)
+    S_in = ws[off[4]:off[5]].view(torch.float32)
+    o = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, H, K_DIM, V_DIM), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_cont, n_fin = int(plan[8]), int(plan[10])
+    launches_per_step = 2 + (1 if (n_cont + n_fin) > 0 else 0)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        kda.kda_segment_forward(plan, plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], h0, 1.0, o, A, B,
+                                fin, ws, stream)
+        if evs:
+            evs[1].record(stream)
+        kda.kda_compose_summaries(plan, plan_dev, H, A, B, h0, S_in, stream)
+        if evs:
+            evs[2].record(stream)
+        kda.kda_apply_boundary(plan, plan_dev, H, S_in, ws, o, fin, stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(1)
+            step(evsets[i])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evsets])  # ms
+    step_ms = float(np.mean(per.sum(axis=1)))
+    kern_ms = per.mean(axis=0)
+
+    # end to end through the public entry point: pinned host inputs in, outputs back, every step
+    pinned = {k_: v_.pin_memory() for k_, v_ in host.items()}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    f_host = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(v_.numel() * v_.element_size() for v_ in pinned.values())
+    d2h = o_host.numel() * o_host.element_size() + f_host.numel() * f_host.element_size()
+
+    def e2e_step():
+        for k_ in pinned:
+            d[k_].copy_(pinned[k_], non_blocking=True)
+        kda.kda_forward_segmented(plan, plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), 1.0,
+                                  o, fin, ws, stream)
+        o_host.copy_(o, non_blocking=True)
+        f_host.copy_(fin, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    t_step = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_step, op=dist.ReduceOp.MAX)
+    step_ms, e2e_ms = (float(x) for x in t_step.cpu())
+    if rank != 0:
+        return
+    peaks = _peaks()
+    T_cont = int(plan[9])
+    flops = T * H * FLOPS_STATE + T_cont * H * FLOPS_TRANSITION
+    achieved = flops / (kern_ms[0] / 1e3) / 1e12
+    prof = _profile_values(CHUNK_KERNEL_SRC)
+    traffic = float(prof["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in prof else None
+    shares = (kern_ms / kern_ms.sum()).tolist()
+    line = {
+        "metric": METRIC, "value": world * T / (step_ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 state", "data": "synthetic",
+        "config": _config(w, world),
+        "kernels_ms": {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]},
+        "kernel_shares": {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]},
+        "roofline": {"bound": "alu", "kernel": "chunk_forward", "achieved": achieved,
+                     "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_PEAK_TFLOPS,
+                     "traffic": traffic, "algorithmic_flops_per_launch": flops,
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz",
+                     "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": peaks["source"]},
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(workloads().keys()))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workloads()[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,113 @@
+"""Helpers shared by the GPU tests: move a drawn problem to the device, run the
+CUDA path through the C ABI, and compute the oracle's values for comparison.
+
+Tolerances (the same in every GPU test):
+  outputs  max_{t,h,v} |o_gpu - o_oracle| <= 2e-2 (bf16 outputs vs fp64 oracle)
+  states   per (segment or sequence, head) matrix:
+           ||x - y||_F <= 1e-4 * max(||y||_F, 1e-6 * sqrt(K))
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from context_kda_gb300.inputs import bf16_to_f32
+
+O_TOL = 2e-2
+REL_TOL = 1e-4
+K = V = 128
+
+
+def rel_err(x, y):
+    """Largest per-matrix relative Frobenius error over the leading axes."""
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    x = x.reshape(-1, x.shape[-2] * x.shape[-1])
+    y = y.reshape(-1, y.shape[-2] * y.shape[-1])
+    num = np.linalg.norm(x - y, axis=1)
+    den = np.maximum(np.linalg.norm(y, axis=1), 1e-6 * np.sqrt(K))
+    return float(np.max(num / den)) if num.size else 0.0
+
+
+def to_device(inp, device="cuda"):
+    import torch
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(device)
+    return {
+        "q": t(inp.q, torch.bfloat16), "k": t(inp.k, torch.bfloat16), "v": t(inp.v, torch.bfloat16),
+        "g": t(inp.g, torch.float32), "beta": t(inp.beta, torch.float32),
+        "h0": None if inp.h0 is None else t(inp.h0, torch.float32),
+    }
+
+
+def plan_bounds(plan, S):
+    off = int(plan[14])
+    return [int(x) for x in plan[off:off + S + 1]]
+
+
+def gpu_forward(inp, scale=1.0, path="fused", seg_bounds=None, dev=None):
+    """Run the CUDA path; returns numpy o (fp32 of the bf16 bits), final, A, B, S_in."""
+    import torch
+    from context_kda_gb300 import binding as kda
+    dev = dev or to_device(inp)
+    T, H, N = inp.tokens, inp.heads, inp.num_seqs
+    S = inp.segments if seg_bounds is None else len(seg_bounds) - 1
+    plan = kda.kda_plan_segments(inp.cu_seqlens, S, seg_bounds)
+    plan_dev = kda.upload_plan(plan)
+    off = kda.kda_workspace_layout(plan, H)
+    ws = torch.empty(off[5], dtype=torch.uint8, device="cuda")
+    o = torch.empty((T, H, V), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((N, H, K, V), dtype=torch.float32, device="cuda")
+    if path == "fused":
+        kda.kda_forward_segmented(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                  dev["h0"], scale, o, fin, ws)
+        view = lambda a, shape: ws[a:a + 4 * int(np.prod(shape))].view(torch.float32).view(*shape)
+        A = view(off[2], (S, H, K, K))
+        B = view(off[3], (S, H, K, V))
+        S_in = view(off[4], (S, H, K, V))
+    else:
+        A = torch.empty((S, H, K, K), dtype=torch.float32, device="cuda")
+        B = torch.empty((S, H, K, V), dtype=torch.float32, device="cuda")
+        S_in = torch.empty((S, H, K, V), dtype=torch.float32, device="cuda")
+        kda.kda_segment_forward(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                dev["h0"], scale, o, A, B, fin, ws)
+        kda.kda_compose_summaries(plan, plan_dev, H, A, B, dev["h0"], S_in)
+        kda.kda_apply_boundary(plan, plan_dev, H, S_in, ws, o, fin)
+    torch.cuda.synchronize()
+    return {"o": o.float().cpu().numpy(), "final": fin.cpu().numpy(), "A": A.cpu().numpy(),
+            "B": B.cpu().numpy(), "S_in": S_in.cpu().numpy(), "plan": plan, "bounds": plan_bounds(plan, S),
+            "o_bits": o.view(torch.int16).cpu().numpy()}
+
+
+def f32_inputs(inp):
+    return bf16_to_f32(inp.q), bf16_to_f32(inp.k), bf16_to_f32(inp.v), inp.g, inp.beta
+
+
+def oracle_forward(inp, heads=None, scale=1.0):
+    q, k, v, g, b = f32_inputs(inp)
+    return oracle.forward(inp.cu_seqlens, q, k, v, g, b, h0=inp.h0, scale=scale, heads=heads)
+
+
+def oracle_segment(inp, bounds, j, h, want_s_in=True):
+    """(A_j, B_j, S_in[j]) of segment j, head h, straight from the definitions:
+    A_j/B_j from a zero-start run with the transition tracked (A_j = 0 when a sequence
+    starts inside the segment), S_in[j] from the monolithic run up to b_j."""
+    q, k, v, g, b = f32_inputs(inp)
+    cu = [int(x) for x in inp.cu_seqlens]
+    a, e = bounds[j], bounds[j + 1]
+    starts = [c for c in cu[:-1] if a <= c < e]
+    h0 = lambda s: None if inp.h0 is None else inp.h0[s, h].astype(np.float64)
+    if starts:
+        s_last = cu.index(max(starts))
+        r = oracle.run_range(max(starts), e, h, q, k, v, g, b, S0=h0(s_last), want_o=False)
+        A, B = np.zeros((K, K)), r["S"]
+    else:
+        r = oracle.run_range(a, e, h, q, k, v, g, b, S0=None, track_transition=True, want_o=False)
+        A, B = r["P"], r["S"]
+    S_in = None
+    if want_s_in:
+        s = max(i for i in range(len(cu) - 1) if cu[i] <= a)
+        if cu[s] == a:
+            S_in = np.zeros((K, V)) if inp.h0 is None else h0(s)
+        else:
+            S_in = oracle.run_range(cu[s], a, h, q, k, v, g, b, S0=h0(s), want_o=False)["S"]
+    return A, B, S_in

@@ -1,0 +1,134 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Workloads are the seeded synthetic problems of context_kda_gb300.inputs (shapes
+of cuLA PR #110, "feat(cp): add opt-in NVSHMEM CP state handoff",
+§Correctness / §Performance, and the CP64 packed case of cuLA PR #136,
+"feat(kda): add cuDNN concatenated-summary Kimi CP", §Latest cuDNN
+compatibility).  Small workloads are compared element by element on every
+head; the large ones on sampled heads (every token and state of those heads)
+and sampled segments.  Tolerances are in tests/harness.py.
+"""
+import numpy as np
+import pytest
+
+from context_kda_gb300.inputs import bf16_to_f32, make_inputs, make_workload, workloads
+from harness import O_TOL, REL_TOL, gpu_forward, oracle_forward, oracle_segment, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_outputs(res, inp, heads=None, scale=1.0):
+    o_ref, f_ref = oracle_forward(inp, heads=heads, scale=scale)
+    hs = list(range(inp.heads)) if heads is None else list(heads)
+    err = float(np.max(np.abs(res["o"][:, hs] - o_ref[:, hs])))
+    frel = rel_err(res["final"][:, hs], f_ref[:, hs])
+    assert err <= O_TOL, f"max|o - o_ref| = {err:.3e}"
+    assert frel <= REL_TOL, f"final-state rel = {frel:.3e}"
+    return err, frel
+
+
+def _check_segments(res, inp, pairs):
+    b = res["bounds"]
+    worst = 0.0
+    for j, h in pairs:
+        A, B, S_in = oracle_segment(inp, b, j, h)
+        ea, eb, es = rel_err(res["A"][j, h], A), rel_err(res["B"][j, h], B), rel_err(res["S_in"][j, h], S_in)
+        if np.all(A == 0):
+            assert np.all(res["A"][j, h] == 0), f"segment {j} head {h}: A must be exactly 0"
+        assert max(ea, eb, es) <= REL_TOL, f"segment {j} head {h}: A {ea:.2e} B {eb:.2e} S_in {es:.2e}"
+        worst = max(worst, ea, eb, es)
+    return worst
+
+
+@pytest.mark.parametrize("name", ["t1024_h4_s2", "t4096_h8_s4", "t8192_h16_s4"])
+def test_single_sequence_workloads_all_heads(name):
+    inp = make_workload(workloads()[name])
+    res = gpu_forward(inp)
+    _check_outputs(res, inp)
+    _check_segments(res, inp, [(j, h) for j in range(inp.segments) for h in range(inp.heads)])
+
+
+def test_packed_varlen_64_segments_sampled_heads():
+    inp = make_workload(workloads()["packed65536_h32_s64"])
+    res = gpu_forward(inp)
+    _check_outputs(res, inp, heads=[0, 31])
+    _check_segments(res, inp, [(j, h) for j in (0, 1, 17, 40, 63) for h in (0, 31)])
+
+
+@pytest.mark.parametrize("name", ["t32768_h32_s8", "t32768_h32_s64", "t131072_h32_s8", "t131072_h32_s64"])
+def test_long_context_sampled(name):
+    w = workloads()[name]
+    inp = make_workload(w)
+    res = gpu_forward(inp)
+    _check_outputs(res, inp, heads=[5])
+    _check_segments(res, inp, [(1, 5), (w.segments - 1, 5)])
+
+
+def test_three_call_path_matches_fused_bitwise():
+    inp = make_workload(workloads()["t4096_h8_s4"])
+    dev = to_device(inp)
+    a = gpu_forward(inp, path="fused", dev=dev)
+    b = gpu_forward(inp, path="split", dev=dev)
+    for key in ("o_bits", "final", "A", "B", "S_in"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_fresh_launches_are_bitwise_identical():
+    """Repeated launches agree exactly (cuLA PR #110 §Correctness: 3/3 fresh launches,
+    maximum absolute difference 0.0; fixture tests/golden/pages_correctness_shapes.txt)."""
+    inp = make_workload(workloads()["t4096_h8_s4"])
+    dev = to_device(inp)
+    runs = [gpu_forward(inp, dev=dev) for _ in range(3)]
+    for r in runs[1:]:
+        for key in ("o_bits", "final", "A", "B", "S_in"):
+            assert np.array_equal(r[key], runs[0][key]), key
+
+
+def test_one_segment_equals_many():
+    """The single-rank path (cuLA PR #136 §Summary by CodeRabbit: single-rank execution)
+    and the segmented path both match the oracle, and each other within tolerance."""
+    inp1 = make_inputs([1000], heads=3, segments=1, h0_std=0.2, seed=3)
+    inp7 = make_inputs([1000], heads=3, segments=7, h0_std=0.2, seed=3)
+    r1, r7 = gpu_forward(inp1), gpu_forward(inp7)
+    _check_outputs(r1, inp1)
+    _check_outputs(r7, inp7)
+    assert float(np.max(np.abs(r1["o"] - r7["o"]))) <= O_TOL
+    assert rel_err(r7["final"], r1["final"]) <= REL_TOL
+
+
+@pytest.mark.parametrize("seqlens,S,h0_std,scale", [
+    ([1], 1, 0.0, 1.0),                        # one token
+    ([63, 1, 65, 130], 3, 0.1, 1.0),          # ragged tails, a one-token sequence
+    ([200, 201, 50, 9, 300], 5, 0.3, 0.5),    # resets inside segments, continuing pieces ending mid-segment
+    ([700], 11, 0.0, 1.0),                     # non-64-aligned cuts
+    ([5, 5, 5, 5], 20, 0.1, 1.0),              # one-token segments crossing sequence starts
+])
+def test_edge_cases_all_heads(seqlens, S, h0_std, scale):
+    inp = make_inputs(seqlens, heads=2, segments=S, h0_std=h0_std, seed=11, g_lo=-0.2)
+    res = gpu_forward(inp, scale=scale)
+    _check_outputs(res, inp, scale=scale)
+    _check_segments(res, inp, [(j, h) for j in range(S) for h in range(2)])
+
+
+def test_custom_segment_bounds():
+    inp = make_inputs([130, 70, 300], heads=2, segments=4, h0_std=0.1, seed=12)
+    bounds = [0, 1, 129, 333, 500]
+    res = gpu_forward(inp, seg_bounds=bounds)
+    assert res["bounds"] == bounds
+    _check_outputs(res, inp)
+    _check_segments(res, inp, [(j, h) for j in range(4) for h in range(2)])
+
+
+def test_closed_form_static_state_on_gpu():
+    """beta = 0 and g = 0: the state stays h0, so o_t = h0^T q_t and final = h0."""
+    inp = make_inputs([257, 100], heads=2, segments=3, h0_std=0.5, seed=13)
+    inp.beta[:] = 0
+    inp.g[:] = 0
+    res = gpu_forward(inp)
+    q = bf16_to_f32(inp.q).astype(np.float64)
+    cu = inp.cu_seqlens
+    for s in range(inp.num_seqs):
+        for h in range(2):
+            want = q[cu[s]:cu[s + 1], h] @ inp.h0[s, h].astype(np.float64)
+            assert float(np.max(np.abs(res["o"][cu[s]:cu[s + 1], h] - want))) <= O_TOL
+            assert rel_err(res["final"][s, h], inp.h0[s, h]) <= REL_TOL
