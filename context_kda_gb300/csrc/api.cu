@@ -95,6 +95,10 @@ extern "C" const char *kda_status_string(int status)
 
 extern "C" int kda_last_cuda_error(void) { return g_last_cuda_error; }
 
+namespace kda {
+void record_cuda_error(int err) { g_last_cuda_error = err; }
+}  // namespace kda
+
 extern "C" int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6])
 {
     if (!off) return KDA_ERR_INVALID_ARG;

@@ -48,6 +48,9 @@ struct Workspace {
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
+// Records a cudaError_t for kda_last_cuda_error() on the calling thread.
+void record_cuda_error(int err);
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_dev, int H,
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,

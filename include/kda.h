@@ -225,6 +225,38 @@ int kda_forward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t 
                           kda_bf16 *o, float *final_state, void *ws, size_t ws_bytes,
                           void *stream);
 
+/*
+ * kda_forward_segmented_noalloc -- kda_forward_segmented without a caller
+ * workspace.  The pages have no counterpart to this entry point.
+ *
+ * For callers that cannot allocate device memory: code that is handed only its
+ * input and output buffers by a host framework that owns every device
+ * allocation (a plugin inside an inference engine, for instance), and code that
+ * must not call cudaMalloc in its steady-state loop because an allocation there
+ * can synchronise the device and stall other work.  The workspace lives in a
+ * fixed device array inside the library, KDA_NOALLOC_SCRATCH_BYTES (32 MiB)
+ * long, which every GPU that loads the library holds until the process exits.
+ *   - Arguments and results are those of kda_forward_segmented; the caller
+ *     still passes every input and output buffer.
+ *   - Returns KDA_ERR_WORKSPACE when kda_workspace_bytes(plan, H) exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES (e.g. T = 4096, H = 8, S = 4 needs about 18 MiB
+ *     and fits; T = 8192, H = 16, S = 4 does not).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Nothing is allocated, freed or cleared: every workspace region is fully
+ *     written before it is read within a call.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, other host
+ *     threads) race on it and must be serialised by the caller.
+ */
+enum { KDA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024 };
+
+int kda_forward_segmented_noalloc(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                  const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                  const float *g, const float *beta, const float *h0, float scale,
+                                  kda_bf16 *o, float *final_state, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
