@@ -1,61 +1,127 @@
-// Chunkwise KDA forward of one piece (segment x sequence), with the segment
-// summaries: state columns (outputs, state update B, final states) and
-// transition columns (qhat, transition A).
+// Chunkwise KDA forward of one piece (segment x sequence) on the tcgen05 tensor
+// cores, with the segment summaries: state columns (outputs, state update B,
+// final states) and transition columns (qhat, transition A).
 //
 // Algebra (per chunk of C = 64 rows, Gamma_r = cumulative g within the chunk):
 //   kt_r = exp(Gamma_r) k_r, kh_i = exp(-Gamma_i) k_i, kb_i = exp(Gamma_C - Gamma_i) k_i,
 //   qt_r = scale exp(Gamma_r) q_r,
-//   M[r,i] = beta_r (kt_r . kh_i) for i < r,   T = (I + M)^-1,
-//   W = T Diag(beta) Kt,   Ut = T Diag(beta) V,
-//   U = Ut - W S,   O = Qt S + ((Qt Kh^T) masked to i <= r) U,
-//   S' = Diag(exp Gamma_C) S + Kb^T U.
+//   M[r,i] = beta_r (kt_r . kh_i) for i < r,   T' = (I + M)^-1 Diag(beta),
+//   W = T' Kt,   Ut = T' V,
+//   U = Ut - W X,   O = Qt X + ((Qt Kh^T) masked to i <= r) U,
+//   X' = Diag(exp Gamma_C) X + Kb^T U.
 // This is the KDA gated delta rule (cuLA PR #110, "feat(cp): add opt-in NVSHMEM
 // CP state handoff", §Supported configuration: BF16 inputs, FP32 state) unrolled
-// over a chunk: writing u_r = beta_r (v_r - (Diag(exp g_r) S_{r-1})^T k_r) for
-// every row gives (I + M) U = Diag(beta) (V - Kt S).
+// over a chunk: writing u_r = beta_r (v_r - (Diag(exp g_r) X_{r-1})^T k_r) for
+// every row gives (I + M) U = Diag(beta) (V - Kt X).
 //
 // The transition columns run the same recurrence on P (K x K) with zero values
 // from P = I at the piece start, so their 'outputs' are qhat_t = scale P_t^T q_t
 // and their end state is the piece's transition (cuLA PR #136, "feat(kda): add
 // cuDNN concatenated-summary Kimi CP", §Summary: preceding_transition).
 //
-// This kernel keeps everything on the FP32 CUDA cores: one CTA per
-// (work item, head), 256 threads, the 128-column state slice in registers
-// (thread = column c, key half hf).
+// Mapping.  One CTA per (work item, head): 256 threads, 128 state columns c.
+// The state lives transposed in TMEM (lane c, column k) as an FP32 accumulator;
+// every contraction is a tcgen05.mma (M = 128, bf16 operands in shared memory,
+// FP32 accumulation in TMEM).  The contractions that feed the state and the
+// summaries (Kt Kh^T, W, Ut, W X, Kb^T U) use a three-term bf16 split
+// (hi*hi + hi*lo + lo*hi, ~2^-17 relative per product) so the FP32 state and
+// summaries stay within 1e-4; the output-only ones (Qt X, masked QK U) use one
+// term.  The 64 x 64 unit-triangular inverse is solved on the CUDA cores in
+// FP32 (16 x 16 blocks).
 #include "kda_internal.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int LDA = 132;  // row stride (floats) of 64 x 128 tiles, 16-byte aligned rows
-constexpr int LDH = 129;  // row stride of the kh / kb tile (odd: conflict-free column reads)
-constexpr int LDM = 65;   // row stride of 64 x 64 tiles
+using namespace tc;
 
-struct SmemV0 {
-    float kb[CH * LDA];   // beta * kt, then W
-    float kh[CH * LDH];   // kh, then kb (decay to chunk end)
-    float qt[CH * LDA];   // scaled qt
-    float vv[CH * LDA];   // beta * v, then Ut, then U
-    float rd[CH * LDA];   // Gamma, then T (stride LDM), then partial-sum exchange
-    float mt[CH * LDM];   // M
-    float qk[CH * LDM];   // masked Qt Kh^T
-    float bt[CH];         // beta
-    float gc[KD];         // exp(Gamma_C)
-};
+// ---- shared-memory map (bytes from the 16-byte aligned dynamic base) -----------------------------------
+constexpr uint32_t LBO_128P = 2064;  // 128-row tiles written column by column (padded chunks)
+constexpr uint32_t LBO_128 = 2048;   // 128-row tiles written row by row
+constexpr uint32_t LBO_64P = 1040;   // 64-row tiles written column by column
+constexpr uint32_t OFF_XT = 0;            // X^T hi | lo: rows c, cols k           (2 x 32768)
+constexpr uint32_t OFF_KQ = 65536;        // [Kt; Qt] hi | lo: rows r / 64+r, cols k (2 x 33024)
+constexpr uint32_t KQ_TILE = 33024;
+constexpr uint32_t OFF_R2 = OFF_KQ + 2 * KQ_TILE;  // 33280 bytes, reused:
+//   Kh hi | lo (rows i, cols k; 2 x 16640)  ->  M fp32 64x64 (16384) + T' hi | lo (rows r, cols i;
+//   2 x 8320 at +16640)  ->  V^T (rows v, cols r; 16384)  ->  -W hi | lo (rows r, cols k; 2 x 16640)
+constexpr uint32_t KH_TILE = 16640;
+constexpr uint32_t OFF_TP = OFF_R2 + 16640;
+constexpr uint32_t TP_TILE = 8320;
+constexpr uint32_t OFF_R3 = OFF_R2 + 33280;  // Kt^T hi | lo (rows k, cols r), then U^T hi | lo (rows c, cols r)
+constexpr uint32_t OFF_R4 = OFF_R3 + 32768;  // Kb^T hi | lo (rows k, cols r)
+constexpr uint32_t T64_TILE = 16384;         // 128 rows x 64 cols, LBO 2048
+constexpr uint32_t OFF_MISC = OFF_R4 + 32768;
+constexpr uint32_t OFF_BETA = OFF_MISC;          // 64 fp32
+constexpr uint32_t OFF_GC = OFF_MISC + 256;      // 128 fp32: exp(Gamma_C)
+constexpr uint32_t OFF_GSUM = OFF_MISC + 768;    // 2 x 128 fp32: per-half decay sums
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
+// QK (masked, bf16) reuses the Qt rows of the lo [Kt; Qt] tile once the first MMA is done;
+// T (fp32) reuses the Kt rows of the hi tile: row r at OFF_KQ + (r/4)*KQ-chunk + (r%4)*256.
+constexpr uint32_t OFF_QKL = OFF_KQ + KQ_TILE + 1024;
+constexpr uint32_t OFF_QT_HI = OFF_KQ + 1024;
+
+// ---- TMEM columns --------------------------------------------------------------------------
+constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols), later O^T
+constexpr uint32_t TM_W = 64;     // W^T
+constexpr uint32_t TM_U = 128;    // Ut^T, then U^T
+constexpr uint32_t TM_X = 256;    // X^T (128 cols)
+constexpr uint32_t TM_COLS = 512;
+
+__device__ int g_chunk_status;   // set to KDA_ERR_TIMEOUT when a bounded wait expires
+
+__device__ __forceinline__ float *t32_row(unsigned char *base, int r)
+{
+    return reinterpret_cast<float *>(base + OFF_KQ + (r >> 2) * LBO_128P + (r & 3) * 256);
+}
+__device__ __forceinline__ float *m32_at(unsigned char *base, int r, int i)
+{
+    return reinterpret_cast<float *>(base + OFF_R2 + r * 256 + ((((i >> 2) ^ (r & 15))) << 4) + (i & 3) * 4);
+}
+
+__device__ __forceinline__ void st_bf16(unsigned char *base, uint32_t off, uint16_t v)
+{
+    *reinterpret_cast<uint16_t *>(base + off) = v;
+}
+
+// Writes 8 consecutive bf16 (hi and lo of 8 fp32 values) as two 16-byte stores.
+__device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, const float *x)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint16_t h0, l0, h1, l1;
+        split_bf16(x[2 * p], h0, l0);
+        split_bf16(x[2 * p + 1], h1, l1);
+        h[p] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+        l[p] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+    }
+    *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 __global__ void __launch_bounds__(256, 1)
-chunk_forward_v0(const int32_t *__restrict__ plan, int H, const uint16_t *__restrict__ q,
+chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__restrict__ q,
                  const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta,
                  const float *__restrict__ h0, float scale, uint16_t *__restrict__ o,
                  float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
                  float *__restrict__ qhat, float *__restrict__ afin)
 {
-    extern __shared__ float4 smem_raw[];
-    SmemV0 &sm = *reinterpret_cast<SmemV0 *>(smem_raw);
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    unsigned char *const base = smem;
+    const uint32_t sbase = smem_u32(smem);
+    float *const s_beta = reinterpret_cast<float *>(base + OFF_BETA);
+    float *const s_gc = reinterpret_cast<float *>(base + OFF_GC);
+    float *const s_gsum = reinterpret_cast<float *>(base + OFF_GSUM);
+
     const PlanView pv{plan};
-    const int tid = threadIdx.x;
-    const int c = tid & 127, hf = tid >> 7;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hw = warp >> 2;          // TMEM lane quadrant, column half
     const int item = blockIdx.x / H, h = blockIdx.x % H;
     const int32_t *it = pv.item(item);
     const int p = it[0], kind = it[1];
@@ -63,266 +129,444 @@ chunk_forward_v0(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     const int start = pc[PC_START], len = pc[PC_LEN], seq = pc[PC_SEQ], seg = pc[PC_SEG];
     const int flags = pc[PC_FLAGS], row0 = pc[PC_ROW], fin = pc[PC_FIN];
     const int64_t T_cont = pv.T_cont();
+    const uint32_t mbar = smem_u32(&s_mbar);
 
-    // thread's slice of the state / transition: rows hf*64 + i, column c
-    float st[64];
-    if (kind == 0) {
-        const bool from_h0 = (flags & KDA_PIECE_FIRST) && h0 != nullptr;
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tbase = s_tmem;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
+    const int c_lane = quad * 32 + lane;                                     // state column of this thread
+    uint32_t phase = 0;
+    bool aborted = false;
+
+    auto wait_mma = [&]() {
+        if (!mbar_wait(mbar, phase & 1)) s_abort = 1;
+        ++phase;
+        fence_after();
+    };
+
+    // ---- piece start: X^T into TMEM (fp32) and its bf16 split into shared memory
+    {
+        const bool from_h0 = kind == 0 && (flags & KDA_PIECE_FIRST) && h0 != nullptr;
         const float *src = h0 + (static_cast<size_t>(seq) * H + h) * KD * VD;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) st[i] = from_h0 ? src[(hf * 64 + i) * VD + c] : 0.f;
-    } else {
+        for (int half = 0; half < 2; ++half) {
+            float x[32];
+            const int k0 = hw * 64 + half * 32;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) st[i] = (hf * 64 + i == c) ? 1.f : 0.f;
+            for (int j = 0; j < 32; ++j) {
+                const int kk = k0 + j;
+                x[j] = kind == 1 ? (kk == c_lane ? 1.f : 0.f) : (from_h0 ? src[kk * VD + c_lane] : 0.f);
+            }
+            tmem_st32(tl + TM_X + k0, x);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, LBO_128),
+                          base + OFF_XT + 32768 + cm_off(c_lane, k0 + 8 * m, LBO_128), x + 8 * m);
+        }
+        fence_before();
+        fence_async_smem();
+        __syncthreads();
     }
 
     const int nch = (len + CH - 1) / CH;
-    for (int ci = 0; ci < nch; ++ci) {
+    for (int ci = 0; ci < nch && !aborted; ++ci) {
         const int t0 = start + ci * CH;
         const int L = min(CH, len - ci * CH);
 
-        // ---- A1: cumulative decay per key channel (hf 0); beta * v and beta (hf 1)
-        if (hf == 0) {
-            float gam = 0.f;
-            for (int r = 0; r < CH; ++r) {
-                const float gv = (r < L) ? g[(static_cast<size_t>(t0 + r) * H + h) * KD + c] : 0.f;
-                gam += gv;
-                sm.rd[r * LDA + c] = gam;
-            }
-            sm.gc[c] = expf(gam);
-        } else {
-            for (int r = 0; r < CH; ++r) {
-                const float bv = (r < L) ? beta[static_cast<size_t>(t0 + r) * H + h] : 0.f;
-                float vv = 0.f;
-                if (kind == 0 && r < L) vv = bf16_bits_to_f32(v[(static_cast<size_t>(t0 + r) * H + h) * VD + c]);
-                sm.vv[r * LDA + c] = bv * vv;
-                if (c == 0) sm.bt[r] = bv;
-            }
-        }
-        __syncthreads();
-
-        // ---- A2: decayed keys and queries
-        for (int a = 0; a < 32; ++a) {
-            const int r = hf + 2 * a;
-            const float gam = sm.rd[r * LDA + c];
-            float kv = 0.f, qv = 0.f;
-            if (r < L) {
-                const size_t off = (static_cast<size_t>(t0 + r) * H + h) * KD + c;
-                kv = bf16_bits_to_f32(k[off]);
-                qv = bf16_bits_to_f32(q[off]);
-            }
-            const float e = expf(gam), ei = expf(-gam);
-            sm.kb[r * LDA + c] = sm.bt[r] * e * kv;
-            sm.kh[r * LDH + c] = ei * kv;
-            sm.qt[r * LDA + c] = scale * e * qv;
-        }
-        __syncthreads();
-
-        // ---- B: M = (beta Kt) Kh^T (strictly lower), QK = Qt Kh^T (lower incl. diagonal)
+        // ================= A: decayed keys / queries into operand tiles =================
         {
-            const int rb = tid >> 4, ib = tid & 15;
-            float am[4][4], aq[4][4];
+            const int kc = tid & 127, hr = tid >> 7;
+            float gam[32];
+            uint32_t kv[16], qv[16];
+            float acc = 0.f;
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) am[a][b] = aq[a][b] = 0.f;
-            for (int kk = 0; kk < KD; ++kk) {
-                float kr[4], qr[4], ki[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    kr[a] = sm.kb[(rb + 16 * a) * LDA + kk];
-                    qr[a] = sm.qt[(rb + 16 * a) * LDA + kk];
-                }
-#pragma unroll
-                for (int b = 0; b < 4; ++b) ki[b] = sm.kh[(ib + 16 * b) * LDH + kk];
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        am[a][b] = fmaf(kr[a], ki[b], am[a][b]);
-                        aq[a][b] = fmaf(qr[a], ki[b], aq[a][b]);
-                    }
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int r = rb + 16 * a, i = ib + 16 * b;
-                    sm.mt[r * LDM + i] = (i < r) ? am[a][b] : 0.f;
-                    sm.qk[r * LDM + i] = (i <= r) ? aq[a][b] : 0.f;
-                }
-        }
-        __syncthreads();
-
-        // ---- C: T = (I + M)^-1 by column-wise forward substitution (threads 0..63, one
-        //      column each, no barriers); meanwhile the others turn kh into kb in place.
-        if (tid < 64) {
-            const int j = tid;
-            float x[64];
-#pragma unroll
-            for (int r = 0; r < 64; ++r) {
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int i = 0; i + 1 < r; i += 2) {
-                    a0 = fmaf(sm.mt[r * LDM + i], x[i], a0);
-                    a1 = fmaf(sm.mt[r * LDM + i + 1], x[i + 1], a1);
-                }
-                if (r & 1) a0 = fmaf(sm.mt[r * LDM + r - 1], x[r - 1], a0);
-                x[r] = (r == j) ? 1.f : ((r < j) ? 0.f : -(a0 + a1));
-            }
-#pragma unroll
-            for (int r = 0; r < 64; ++r) sm.rd[r * LDM + j] = x[r];
-        } else {
-            for (int e = tid - 64; e < CH * KD; e += 192) {
-                const int r = e >> 7, kk = e & 127;
-                sm.kh[r * LDH + kk] *= sm.gc[kk];
-            }
-        }
-        __syncthreads();
-
-        // ---- D: W = T (beta Kt), Ut = T (beta V)
-        {
-            float w[32], u[32];
-#pragma unroll
-            for (int a = 0; a < 32; ++a) w[a] = u[a] = 0.f;
-            for (int i = 0; i < CH; ++i) {
-                const float kbv = sm.kb[i * LDA + c];
-                const float vbv = sm.vv[i * LDA + c];
-#pragma unroll
-                for (int a = 0; a < 32; ++a) {
-                    const float tv = sm.rd[(hf + 2 * a) * LDM + i];
-                    w[a] = fmaf(tv, kbv, w[a]);
-                    u[a] = fmaf(tv, vbv, u[a]);
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int a = 0; a < 32; ++a) {
-                sm.kb[(hf + 2 * a) * LDA + c] = w[a];
-                sm.vv[(hf + 2 * a) * LDA + c] = u[a];
-            }
-        }
-        __syncthreads();
-
-        // ---- E: U = Ut - W S   (partial over this thread's key half, exchanged through rd)
-        {
-            float part[64];
-#pragma unroll
-            for (int r = 0; r < 64; ++r) {
-                const float4 *wr = reinterpret_cast<const float4 *>(&sm.kb[r * LDA + hf * 64]);
-                float acc = 0.f;
-#pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 w4 = wr[i4];
-                    acc = fmaf(w4.x, st[4 * i4 + 0], acc);
-                    acc = fmaf(w4.y, st[4 * i4 + 1], acc);
-                    acc = fmaf(w4.z, st[4 * i4 + 2], acc);
-                    acc = fmaf(w4.w, st[4 * i4 + 3], acc);
-                }
-                part[r] = acc;
-            }
-            if (hf == 0) {
-#pragma unroll
-                for (int r = 32; r < 64; ++r) sm.rd[r * LDA + c] = part[r];
-            } else {
-#pragma unroll
-                for (int r = 0; r < 32; ++r) sm.rd[r * LDA + c] = part[r];
-            }
-            __syncthreads();
-            if (hf == 0) {
-#pragma unroll
-                for (int r = 0; r < 32; ++r) sm.vv[r * LDA + c] -= part[r] + sm.rd[r * LDA + c];
-            } else {
-#pragma unroll
-                for (int r = 32; r < 64; ++r) sm.vv[r * LDA + c] -= part[r] + sm.rd[r * LDA + c];
-            }
-        }
-        __syncthreads();
-
-        // ---- F: O = Qt S + (QK masked) U  -> outputs (state columns) or qhat (transition columns)
-        {
-            float part[64];
-#pragma unroll
-            for (int r = 0; r < 64; ++r) {
-                const float4 *qr = reinterpret_cast<const float4 *>(&sm.qt[r * LDA + hf * 64]);
-                float acc = 0.f;
-#pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 q4 = qr[i4];
-                    acc = fmaf(q4.x, st[4 * i4 + 0], acc);
-                    acc = fmaf(q4.y, st[4 * i4 + 1], acc);
-                    acc = fmaf(q4.z, st[4 * i4 + 2], acc);
-                    acc = fmaf(q4.w, st[4 * i4 + 3], acc);
-                }
-                part[r] = acc;
-            }
-            if (hf == 0) {
-#pragma unroll
-                for (int r = 32; r < 64; ++r) sm.rd[r * LDA + c] = part[r];
-            } else {
-#pragma unroll
-                for (int r = 0; r < 32; ++r) sm.rd[r * LDA + c] = part[r];
-            }
-            __syncthreads();
-#pragma unroll
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = hf * 32 + rr;
-                float acc = (hf == 0 ? part[rr] : part[32 + rr]) + sm.rd[r * LDA + c];
-                for (int i = 0; i <= r; ++i) acc = fmaf(sm.qk[r * LDM + i], sm.vv[i * LDA + c], acc);
+            for (int j = 0; j < 32; ++j) {
+                const int r = hr * 32 + j;
+                float gv = 0.f;
+                uint16_t kb16 = 0, qb16 = 0;
                 if (r < L) {
-                    if (kind == 0)
-                        o[(static_cast<size_t>(t0 + r) * H + h) * VD + c] = f32_to_bf16_bits(acc);
-                    else
-                        qhat[(static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) * KD + c] = acc;
+                    const size_t off = (static_cast<size_t>(t0 + r) * H + h) * KD + kc;
+                    gv = g[off];
+                    kb16 = k[off];
+                    qb16 = q[off];
+                }
+                acc += gv;
+                gam[j] = acc;
+                if (j & 1) {
+                    kv[j >> 1] |= static_cast<uint32_t>(kb16) << 16;
+                    qv[j >> 1] |= static_cast<uint32_t>(qb16) << 16;
+                } else {
+                    kv[j >> 1] = kb16;
+                    qv[j >> 1] = qb16;
+                }
+            }
+            s_gsum[hr * 128 + kc] = acc;
+            if (tid < 64) s_beta[tid] = (tid < L) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
+            __syncthreads();
+            const float off = hr ? s_gsum[kc] : 0.f;
+            const float gC = s_gsum[kc] + s_gsum[128 + kc];
+            if (hr == 0) s_gc[kc] = expf(gC);
+            float ktv[32], kbv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = hr * 32 + j;
+                const float G = off + gam[j];
+                const float e = expf(G), ei = expf(-G), eb = expf(gC - G);
+                const uint32_t kw = kv[j >> 1], qw = qv[j >> 1];
+                const float kf = __uint_as_float((j & 1) ? (kw & 0xFFFF0000u) : (kw << 16));
+                const float qf = __uint_as_float((j & 1) ? (qw & 0xFFFF0000u) : (qw << 16));
+                const float kt = e * kf, qt = scale * e * qf, kh = ei * kf;
+                ktv[j] = kt;
+                kbv[j] = eb * kf;
+                uint16_t hi, lo;
+                split_bf16(kt, hi, lo);
+                st_bf16(base, OFF_KQ + cm_off(r, kc, LBO_128P), hi);
+                st_bf16(base, OFF_KQ + KQ_TILE + cm_off(r, kc, LBO_128P), lo);
+                split_bf16(qt, hi, lo);
+                st_bf16(base, OFF_KQ + cm_off(64 + r, kc, LBO_128P), hi);
+                st_bf16(base, OFF_KQ + KQ_TILE + cm_off(64 + r, kc, LBO_128P), lo);
+                split_bf16(kh, hi, lo);
+                st_bf16(base, OFF_R2 + cm_off(r, kc, LBO_64P), hi);
+                st_bf16(base, OFF_R2 + KH_TILE + cm_off(r, kc, LBO_64P), lo);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r0 = hr * 32 + 8 * m;
+                st_split8(base + OFF_R3 + cm_off(kc, r0, LBO_128), base + OFF_R3 + T64_TILE + cm_off(kc, r0, LBO_128),
+                          ktv + 8 * m);
+                st_split8(base + OFF_R4 + cm_off(kc, r0, LBO_128), base + OFF_R4 + T64_TILE + cm_off(kc, r0, LBO_128),
+                          kbv + 8 * m);
+            }
+            fence_async_smem();
+            __syncthreads();
+        }
+
+        // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
+        if (tid == 0) {
+            fence_after();
+            const uint32_t id = idesc_bf16(128, 64);
+            const uint32_t aoff[3] = {0, 0, KQ_TILE}, boff[3] = {0, KH_TILE, 0};
+#pragma unroll
+            for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * LBO_128P, LBO_128P),
+                             sdesc(sbase + OFF_R2 + boff[ps] + kk * 2 * LBO_64P, LBO_64P), id, (ps | kk) != 0);
+            commit(mbar);
+        }
+        wait_mma();
+
+        // ================= C: M (fp32, beta-scaled, strictly lower) and masked QK (bf16) =====
+        {
+            float d[32];
+            tmem_ld32(tl + TM_D1 + hw * 32, d);
+            if (quad < 2) {
+                const int r = c_lane;
+                const float br = s_beta[r];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float4 m4;
+                    const int i0 = hw * 32 + 4 * j4;
+                    m4.x = (i0 + 0 < r) ? br * d[4 * j4 + 0] : 0.f;
+                    m4.y = (i0 + 1 < r) ? br * d[4 * j4 + 1] : 0.f;
+                    m4.z = (i0 + 2 < r) ? br * d[4 * j4 + 2] : 0.f;
+                    m4.w = (i0 + 3 < r) ? br * d[4 * j4 + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(m32_at(base, r, i0)) = m4;
+                }
+            } else {
+                const int r = c_lane - 64;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int p2 = 0; p2 < 4; ++p2) {
+                        const int i0 = hw * 32 + 8 * m + 2 * p2;
+                        const uint16_t a0 = f32_to_bf16_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f);
+                        const uint16_t a1 = f32_to_bf16_bits(i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                        w[p2] = static_cast<uint32_t>(a0) | (static_cast<uint32_t>(a1) << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(base + OFF_QKL + cm_off(r, hw * 32 + 8 * m, LBO_128P)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_before();
+            __syncthreads();
+            if (s_abort) aborted = true;
+        }
+        if (aborted) break;
+
+        // ================= D: T = (I + M)^-1 in 16 x 16 blocks (fp32, CUDA cores) =========
+        {
+            if (tid < 64) {   // diagonal blocks: column jj of block b by forward substitution
+                const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
+                float x[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int ii = 0; ii < rr; ++ii) s = fmaf(*m32_at(base, r0 + rr, r0 + ii), x[ii], s);
+                    x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -s);
+                }
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) t32_row(base, r0 + rr)[r0 + jj] = x[rr];
+            }
+            __syncthreads();
+            // off-diagonal blocks by distance d: Y = sum_{k=j}^{i-1} M_ik T_kj, T_ij = -T_ii Y
+            const int rr = tid >> 4, cc = tid & 15;
+#pragma unroll
+            for (int dd = 1; dd < 4; ++dd) {
+                float y[3];
+#pragma unroll
+                for (int bi = 0; bi < 3; ++bi) {
+                    y[bi] = 0.f;
+                    if (bi < 4 - dd) {
+                        const int i = bi + dd, j = bi;
+                        float s = 0.f;
+                        for (int kb = j; kb < i; ++kb)
+#pragma unroll
+                            for (int m = 0; m < 16; ++m)
+                                s = fmaf(*m32_at(base, 16 * i + rr, 16 * kb + m), t32_row(base, 16 * kb + m)[16 * j + cc], s);
+                        y[bi] = s;
+                    }
+                }
+                // Y_ij goes to the unused upper-triangle block (j, i) of M
+#pragma unroll
+                for (int bi = 0; bi < 3; ++bi)
+                    if (bi < 4 - dd) *m32_at(base, 16 * bi + rr, 16 * (bi + dd) + cc) = y[bi];
+                __syncthreads();
+#pragma unroll
+                for (int bi = 0; bi < 3; ++bi) {
+                    if (bi < 4 - dd) {
+                        const int i = bi + dd, j = bi;
+                        float s = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            s = fmaf(t32_row(base, 16 * i + rr)[16 * i + m], *m32_at(base, 16 * j + m, 16 * i + cc), s);
+                        t32_row(base, 16 * i + rr)[16 * j + cc] = -s;
+                    }
+                }
+                __syncthreads();
+            }
+            // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
+            {
+                const int r = tid >> 2, i0 = (tid & 3) * 16;
+                const float *tr = t32_row(base, r);
+                float tv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) tv[j] = (i0 + j <= r) ? tr[i0 + j] * s_beta[i0 + j] : 0.f;
+                st_split8(base + OFF_TP + cm_off(r, i0, LBO_64P), base + OFF_TP + TP_TILE + cm_off(r, i0, LBO_64P), tv);
+                st_split8(base + OFF_TP + cm_off(r, i0 + 8, LBO_64P),
+                          base + OFF_TP + TP_TILE + cm_off(r, i0 + 8, LBO_64P), tv + 8);
+            }
+            __syncthreads();   // M (fp32) is dead from here: V^T may overwrite it
+            if (kind == 0) {   // V^T (rows v, cols r), exact bf16
+                const int vc = tid & 127, hr = tid >> 7;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int p2 = 0; p2 < 4; ++p2) {
+                        uint32_t pair = 0;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = hr * 32 + 8 * m + 2 * p2 + e;
+                            uint16_t b16 = 0;
+                            if (r < L) b16 = v[(static_cast<size_t>(t0 + r) * H + h) * VD + vc];
+                            pair |= static_cast<uint32_t>(b16) << (16 * e);
+                        }
+                        w[p2] = pair;
+                    }
+                    *reinterpret_cast<uint4 *>(base + OFF_R2 + cm_off(vc, hr * 32 + 8 * m, LBO_128)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_async_smem();
+            __syncthreads();
+        }
+
+        // ================= E: W^T = Kt^T T'^T (3-term); Ut^T = V^T T'^T (2-term) =============
+        if (tid == 0) {
+            fence_after();
+            const uint32_t id = idesc_bf16(128, 64);
+            const uint32_t aoff[3] = {0, 0, T64_TILE}, boff[3] = {0, TP_TILE, 0};
+#pragma unroll
+            for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tbase + TM_W, sdesc(sbase + OFF_R3 + aoff[ps] + kk * 2 * LBO_128, LBO_128),
+                             sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * LBO_64P, LBO_64P), id, (ps | kk) != 0);
+            if (kind == 0) {
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tbase + TM_U, sdesc(sbase + OFF_R2 + kk * 2 * LBO_128, LBO_128),
+                                 sdesc(sbase + OFF_TP + ps * TP_TILE + kk * 2 * LBO_64P, LBO_64P), id, (ps | kk) != 0);
+            }
+            commit(mbar);
+        }
+        wait_mma();
+
+        // ================= F: -W (rows r, cols k) hi/lo; X^T *= exp(Gamma_C) in TMEM ==========
+        {
+            float d[32];
+            tmem_ld32(tl + TM_W + hw * 32, d);   // W^T[k = c_lane][r = hw*32 + j]
+            const int kc = c_lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = hw * 32 + j;
+                uint16_t hi, lo;
+                split_bf16(-d[j], hi, lo);
+                st_bf16(base, OFF_R2 + cm_off(r, kc, LBO_64P), hi);
+                st_bf16(base, OFF_R2 + KH_TILE + cm_off(r, kc, LBO_64P), lo);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int k0 = hw * 64 + half * 32;
+                float x[32];
+                tmem_ld32(tl + TM_X + k0, x);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];
+                tmem_st32(tl + TM_X + k0, x);
+            }
+            fence_before();
+            fence_async_smem();
+            __syncthreads();
+            if (s_abort) aborted = true;
+        }
+        if (aborted) break;
+
+        // ================= G: U^T = Ut^T - X^T W^T (3-term); O^T = X^T Qt^T (1-term) ==========
+        if (tid == 0) {
+            fence_after();
+            const uint32_t id = idesc_bf16(128, 64);
+            const uint32_t aoff[3] = {0, 0, 32768}, boff[3] = {0, KH_TILE, 0};
+#pragma unroll
+            for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_XT + aoff[ps] + kk * 2 * LBO_128, LBO_128),
+                             sdesc(sbase + OFF_R2 + boff[ps] + kk * 2 * LBO_64P, LBO_64P), id,
+                             (kind == 0) || ((ps | kk) != 0));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_XT + kk * 2 * LBO_128, LBO_128),
+                         sdesc(sbase + OFF_QT_HI + kk * 2 * LBO_128P, LBO_128P), id, kk != 0);
+            commit(mbar);
+        }
+        wait_mma();
+
+        // ================= H: U^T (rows c, cols r) hi/lo into shared memory ====================
+        {
+            float d[32];
+            tmem_ld32(tl + TM_U + hw * 32, d);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                st_split8(base + OFF_R3 + cm_off(c_lane, hw * 32 + 8 * m, LBO_128),
+                          base + OFF_R3 + T64_TILE + cm_off(c_lane, hw * 32 + 8 * m, LBO_128), d + 8 * m);
+            fence_before();
+            fence_async_smem();
+            __syncthreads();
+            if (s_abort) aborted = true;
+        }
+        if (aborted) break;
+
+        // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kb (3-term) ==================
+        if (tid == 0) {
+            fence_after();
+            const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_R3 + kk * 2 * LBO_128, LBO_128),
+                         sdesc(sbase + OFF_QKL + kk * 2 * LBO_128P, LBO_128P), id64, 1);
+            const uint32_t aoff[3] = {0, 0, T64_TILE}, boff[3] = {0, T64_TILE, 0};
+#pragma unroll
+            for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tbase + TM_X, sdesc(sbase + OFF_R3 + aoff[ps] + kk * 2 * LBO_128, LBO_128),
+                             sdesc(sbase + OFF_R4 + boff[ps] + kk * 2 * LBO_128, LBO_128), id128, 1);
+            commit(mbar);
+        }
+        wait_mma();
+
+        // ================= J: outputs (or qhat) to HBM; new X^T split into shared memory ========
+        {
+            float d[32];
+            tmem_ld32(tl + TM_D1 + hw * 32, d);   // O^T[c][r = hw*32 + j]
+            if (kind == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int r = hw * 32 + j;
+                    if (r < L) o[(static_cast<size_t>(t0 + r) * H + h) * VD + c_lane] = f32_to_bf16_bits(d[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int r = hw * 32 + j;
+                    if (r < L) qhat[(static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) * KD + c_lane] = d[j];
+                }
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int k0 = hw * 64 + half * 32;
+                float x[32];
+                tmem_ld32(tl + TM_X + k0, x);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, LBO_128),
+                              base + OFF_XT + 32768 + cm_off(c_lane, k0 + 8 * m, LBO_128), x + 8 * m);
+            }
+            fence_before();
+            fence_async_smem();
+            __syncthreads();
+            if (s_abort) aborted = true;
+        }
+    }
+
+    // ---- piece end: summaries and final states (X[k][c] from TMEM lane c, column k)
+    if (!aborted) {
+        const size_t mat = static_cast<size_t>(KD) * VD;
+        const bool seg_last = flags & KDA_PIECE_SEG_LAST, seq_end = flags & KDA_PIECE_SEQ_END;
+        float *dst0 = nullptr, *dst1 = nullptr;
+        if (kind == 0) {
+            if (seg_last) dst0 = B + (static_cast<size_t>(seg) * H + h) * mat;
+            if (seq_end) dst1 = fin_state + (static_cast<size_t>(seq) * H + h) * mat;
+            if (seg_last && (pv.seg(seg)[1] & KDA_SEG_HAS_RESET)) {
+                float *za = A + (static_cast<size_t>(seg) * H + h) * KD * KD;
+                for (int e = tid; e < KD * KD / 4; e += 256)
+                    reinterpret_cast<float4 *>(za)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        } else {
+            if (seg_last) dst0 = A + (static_cast<size_t>(seg) * H + h) * KD * KD;
+            if (seq_end) dst1 = afin + (static_cast<size_t>(fin) * H + h) * KD * KD;
+        }
+        if (dst0 || dst1) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int k0 = hw * 64 + half * 32;
+                float x[32];
+                tmem_ld32(tl + TM_X + k0, x);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (dst0) dst0[(k0 + j) * VD + c_lane] = x[j];
+                    if (dst1) dst1[(k0 + j) * VD + c_lane] = x[j];
                 }
             }
         }
-
-        // ---- G: S' = Diag(exp Gamma_C) S + Kb^T U
-        {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) st[i] *= sm.gc[hf * 64 + i];
-            for (int r = 0; r < L; ++r) {
-                const float ur = sm.vv[r * LDA + c];
-                const float *kbr = &sm.kh[r * LDH + hf * 64];
-#pragma unroll
-                for (int i = 0; i < 64; ++i) st[i] = fmaf(kbr[i], ur, st[i]);
-            }
-        }
-        __syncthreads();
+    } else if (tid == 0) {
+        atomicExch(&g_chunk_status, KDA_ERR_TIMEOUT);
     }
-
-    // ---- piece end: summaries and final states
-    const size_t mat = static_cast<size_t>(KD) * VD;
-    const bool seg_last = flags & KDA_PIECE_SEG_LAST, seq_end = flags & KDA_PIECE_SEQ_END;
-    if (kind == 0) {
-        if (seg_last) {
-            float *dst = B + (static_cast<size_t>(seg) * H + h) * mat;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(hf * 64 + i) * VD + c] = st[i];
-            if (pv.seg(seg)[1] & KDA_SEG_HAS_RESET) {
-                float *za = A + (static_cast<size_t>(seg) * H + h) * KD * KD;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) za[(hf * 64 + i) * KD + c] = 0.f;
-            }
-        }
-        if (seq_end) {
-            float *dst = fin_state + (static_cast<size_t>(seq) * H + h) * mat;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(hf * 64 + i) * VD + c] = st[i];
-        }
-    } else {
-        if (seg_last) {
-            float *dst = A + (static_cast<size_t>(seg) * H + h) * KD * KD;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(hf * 64 + i) * KD + c] = st[i];
-        }
-        if (seq_end) {
-            float *dst = afin + (static_cast<size_t>(fin) * H + h) * KD * KD;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(hf * 64 + i) * KD + c] = st[i];
-        }
-    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
 }  // namespace
@@ -334,14 +578,13 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
                                  float *qhat, float *afin, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
-    const size_t smem = sizeof(SmemV0);
-    cudaError_t err = cudaFuncSetAttribute(chunk_forward_v0, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+    cudaError_t err = cudaFuncSetAttribute(chunk_forward_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(SMEM_BYTES));
     if (err != cudaSuccess) return err;
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    chunk_forward_v0<<<static_cast<unsigned>(blocks), 256, smem, stream>>>(
+    chunk_forward_tc<<<static_cast<unsigned>(blocks), 256, SMEM_BYTES, stream>>>(
         plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B, final_state, qhat, afin);
     return cudaGetLastError();
 }
