@@ -61,6 +61,9 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
 // T (fp32) reuses the Kt rows of the hi tile: row r at OFF_KQ + (r/4)*KQ-chunk + (r%4)*256.
 constexpr uint32_t OFF_QKL = OFF_KQ + KQ_TILE + 1024;
 constexpr uint32_t OFF_QT_HI = OFF_KQ + 1024;
+// Raw rows of the next chunk, staged by bulk copies while the current chunk finishes:
+// v (bf16, 256 B/row) in R2, g (fp32, 512 B/row) in R3, q and k (bf16) in R4.
+constexpr uint32_t STG_V = OFF_R2, STG_G = OFF_R3, STG_Q = OFF_R4, STG_K = OFF_R4 + 16384;
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols), later O^T
@@ -111,6 +114,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ __align__(8) uint64_t s_ldbar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     unsigned char *const base = smem;
@@ -130,9 +134,11 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     const int flags = pc[PC_FLAGS], row0 = pc[PC_ROW], fin = pc[PC_FIN];
     const int64_t T_cont = pv.T_cont();
     const uint32_t mbar = smem_u32(&s_mbar);
+    const uint32_t ldbar = smem_u32(&s_ldbar);
 
     if (tid == 0) {
         mbar_init(mbar, 1);
+        mbar_init(ldbar, 1);
         s_abort = 0;
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
@@ -150,6 +156,29 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         ++phase;
         fence_after();
     };
+
+    // Stage the raw rows of chunk cn (q, k, g, and v for state columns) with one bulk copy
+    // per row and thread; beta of that chunk goes to a register.  Called by all threads.
+    uint32_t ld_phase = 0;
+    bool loads_pending = false;
+    float beta_next = 0.f;
+    auto issue_loads = [&](int cn) {
+        const int t0n = start + cn * CH;
+        const int Ln = min(CH, len - cn * CH);
+        if (tid == 0) mbar_arrive_expect_tx(ldbar, static_cast<uint32_t>(Ln) * (kind == 0 ? 1280u : 1024u));
+        __syncthreads();
+        const int arr = tid >> 6, r = tid & 63;
+        if (r < Ln && (arr != 2 || kind == 0)) {
+            const size_t row = static_cast<size_t>(t0n + r) * H + h;
+            if (arr == 0) bulk_g2s(sbase + STG_Q + r * 256, q + row * KD, 256, ldbar);
+            else if (arr == 1) bulk_g2s(sbase + STG_K + r * 256, k + row * KD, 256, ldbar);
+            else if (arr == 2) bulk_g2s(sbase + STG_V + r * 256, v + row * VD, 256, ldbar);
+            else bulk_g2s(sbase + STG_G + r * 512, g + row * KD, 512, ldbar);
+        }
+        if (tid < 64) beta_next = (tid < Ln) ? beta[static_cast<size_t>(t0n + tid) * H + h] : 0.f;
+        loads_pending = true;
+    };
+    issue_loads(0);
 
     // ---- piece start: X^T into TMEM (fp32) and its bf16 split into shared memory
     {
@@ -180,73 +209,83 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         const int t0 = start + ci * CH;
         const int L = min(CH, len - ci * CH);
 
-        // ================= A: decayed keys / queries into operand tiles =================
+        // ================= A: staged rows -> decayed keys / queries in operand tiles =========
+        uint32_t vv[16];   // this thread's v column (32 rows, bf16 pairs), kept for V^T in D
         {
+            if (!mbar_wait(ldbar, ld_phase & 1)) s_abort = 1;
+            ++ld_phase;
+            loads_pending = false;
             const int kc = tid & 127, hr = tid >> 7;
+            const float *sg = reinterpret_cast<const float *>(base + STG_G);
+            const uint16_t *sq = reinterpret_cast<const uint16_t *>(base + STG_Q);
+            const uint16_t *sk = reinterpret_cast<const uint16_t *>(base + STG_K);
+            const uint16_t *sv = reinterpret_cast<const uint16_t *>(base + STG_V);
             float gam[32];
             uint32_t kv[16], qv[16];
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int r = hr * 32 + j;
-                float gv = 0.f;
-                uint16_t kb16 = 0, qb16 = 0;
-                if (r < L) {
-                    const size_t off = (static_cast<size_t>(t0 + r) * H + h) * KD + kc;
-                    gv = g[off];
-                    kb16 = k[off];
-                    qb16 = q[off];
-                }
+                const bool ok = r < L;
+                const float gv = ok ? sg[r * 128 + kc] : 0.f;
+                const uint32_t kb16 = ok ? sk[r * 128 + kc] : 0u;
+                const uint32_t qb16 = ok ? sq[r * 128 + kc] : 0u;
+                const uint32_t vb16 = (ok && kind == 0) ? sv[r * 128 + kc] : 0u;
                 acc += gv;
                 gam[j] = acc;
                 if (j & 1) {
-                    kv[j >> 1] |= static_cast<uint32_t>(kb16) << 16;
-                    qv[j >> 1] |= static_cast<uint32_t>(qb16) << 16;
+                    kv[j >> 1] |= kb16 << 16;
+                    qv[j >> 1] |= qb16 << 16;
+                    vv[j >> 1] |= vb16 << 16;
                 } else {
                     kv[j >> 1] = kb16;
                     qv[j >> 1] = qb16;
+                    vv[j >> 1] = vb16;
                 }
             }
             s_gsum[hr * 128 + kc] = acc;
-            if (tid < 64) s_beta[tid] = (tid < L) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
-            __syncthreads();
+            if (tid < 64) s_beta[tid] = beta_next;
+            __syncthreads();   // staging consumed: R2, R3, R4 may be rewritten from here
             const float off = hr ? s_gsum[kc] : 0.f;
             const float gC = s_gsum[kc] + s_gsum[128 + kc];
             if (hr == 0) s_gc[kc] = expf(gC);
-            float ktv[32], kbv[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = hr * 32 + j;
-                const float G = off + gam[j];
-                const float e = expf(G), ei = expf(-G), eb = expf(gC - G);
-                const uint32_t kw = kv[j >> 1], qw = qv[j >> 1];
-                const float kf = __uint_as_float((j & 1) ? (kw & 0xFFFF0000u) : (kw << 16));
-                const float qf = __uint_as_float((j & 1) ? (qw & 0xFFFF0000u) : (qw << 16));
-                const float kt = e * kf, qt = scale * e * qf, kh = ei * kf;
-                ktv[j] = kt;
-                kbv[j] = eb * kf;
-                uint16_t hi, lo;
-                split_bf16(kt, hi, lo);
-                st_bf16(base, OFF_KQ + cm_off(r, kc, LBO_128P), hi);
-                st_bf16(base, OFF_KQ + KQ_TILE + cm_off(r, kc, LBO_128P), lo);
-                split_bf16(qt, hi, lo);
-                st_bf16(base, OFF_KQ + cm_off(64 + r, kc, LBO_128P), hi);
-                st_bf16(base, OFF_KQ + KQ_TILE + cm_off(64 + r, kc, LBO_128P), lo);
-                split_bf16(kh, hi, lo);
-                st_bf16(base, OFF_R2 + cm_off(r, kc, LBO_64P), hi);
-                st_bf16(base, OFF_R2 + KH_TILE + cm_off(r, kc, LBO_64P), lo);
-            }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
+                float ktv[8], kbv[8];
+#pragma unroll
+                for (int e8 = 0; e8 < 8; ++e8) {
+                    const int j = 8 * m + e8;
+                    const int r = hr * 32 + j;
+                    const float G = off + gam[j];
+                    const float e = expf(G), ei = expf(-G), eb = expf(gC - G);
+                    const uint32_t kw = kv[j >> 1], qw = qv[j >> 1];
+                    const float kf = __uint_as_float((j & 1) ? (kw & 0xFFFF0000u) : (kw << 16));
+                    const float qf = __uint_as_float((j & 1) ? (qw & 0xFFFF0000u) : (qw << 16));
+                    const float kt = e * kf, qt = scale * e * qf, kh = ei * kf;
+                    ktv[e8] = kt;
+                    kbv[e8] = eb * kf;
+                    uint16_t hi, lo;
+                    split_bf16(kt, hi, lo);
+                    st_bf16(base, OFF_KQ + cm_off(r, kc, LBO_128P), hi);
+                    st_bf16(base, OFF_KQ + KQ_TILE + cm_off(r, kc, LBO_128P), lo);
+                    split_bf16(qt, hi, lo);
+                    st_bf16(base, OFF_KQ + cm_off(64 + r, kc, LBO_128P), hi);
+                    st_bf16(base, OFF_KQ + KQ_TILE + cm_off(64 + r, kc, LBO_128P), lo);
+                    split_bf16(kh, hi, lo);
+                    st_bf16(base, OFF_R2 + cm_off(r, kc, LBO_64P), hi);
+                    st_bf16(base, OFF_R2 + KH_TILE + cm_off(r, kc, LBO_64P), lo);
+                }
                 const int r0 = hr * 32 + 8 * m;
                 st_split8(base + OFF_R3 + cm_off(kc, r0, LBO_128), base + OFF_R3 + T64_TILE + cm_off(kc, r0, LBO_128),
-                          ktv + 8 * m);
+                          ktv);
                 st_split8(base + OFF_R4 + cm_off(kc, r0, LBO_128), base + OFF_R4 + T64_TILE + cm_off(kc, r0, LBO_128),
-                          kbv + 8 * m);
+                          kbv);
             }
             fence_async_smem();
             __syncthreads();
+            if (s_abort) aborted = true;
         }
+        if (aborted) break;
 
         // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
         if (tid == 0) {
@@ -366,26 +405,12 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                           base + OFF_TP + TP_TILE + cm_off(r, i0 + 8, LBO_64P), tv + 8);
             }
             __syncthreads();   // M (fp32) is dead from here: V^T may overwrite it
-            if (kind == 0) {   // V^T (rows v, cols r), exact bf16
+            if (kind == 0) {   // V^T (rows v, cols r), exact bf16, from this thread's v column
                 const int vc = tid & 127, hr = tid >> 7;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int p2 = 0; p2 < 4; ++p2) {
-                        uint32_t pair = 0;
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int r = hr * 32 + 8 * m + 2 * p2 + e;
-                            uint16_t b16 = 0;
-                            if (r < L) b16 = v[(static_cast<size_t>(t0 + r) * H + h) * VD + vc];
-                            pair |= static_cast<uint32_t>(b16) << (16 * e);
-                        }
-                        w[p2] = pair;
-                    }
+                for (int m = 0; m < 4; ++m)
                     *reinterpret_cast<uint4 *>(base + OFF_R2 + cm_off(vc, hr * 32 + 8 * m, LBO_128)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
+                        make_uint4(vv[4 * m], vv[4 * m + 1], vv[4 * m + 2], vv[4 * m + 3]);
             }
             fence_async_smem();
             __syncthreads();
@@ -498,6 +523,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         wait_mma();
 
         // ================= J: outputs (or qhat) to HBM; new X^T split into shared memory ========
+        if (ci + 1 < nch) issue_loads(ci + 1);   // staging regions are free once I has completed
         {
             float d[32];
             tmem_ld32(tl + TM_D1 + hw * 32, d);   // O^T[c][r = hw*32 + j]
@@ -561,8 +587,9 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 }
             }
         }
-    } else if (tid == 0) {
-        atomicExch(&g_chunk_status, KDA_ERR_TIMEOUT);
+    } else {
+        if (loads_pending) mbar_wait(ldbar, ld_phase & 1);   // bounded: let staged copies land
+        if (tid == 0) atomicExch(&g_chunk_status, KDA_ERR_TIMEOUT);
     }
     fence_before();
     __syncthreads();
