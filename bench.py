@@ -40,7 +40,10 @@ CH = 64
 # chunk forward, and the transition columns a continuing token adds
 FLOPS_STATE = 6 * CH * K_DIM + 4 * CH * V_DIM + 6 * K_DIM * V_DIM          # 180,224
 FLOPS_TRANSITION = 6 * K_DIM * K_DIM + 2 * CH * K_DIM                      # 114,688
-FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12                      # 80.5: SMs x FP32 lanes x FMA x max clock
+# tensor work the chunk kernel issues per chunk and CTA (bf16 M=128 MMAs, split passes included)
+ISSUED_PER_CHUNK = {0: 2 * 128 * (3 * 64 * 128 + 3 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 128 + 64 * 128 + 64 * 64
+                                  + 3 * 128 * 64),
+                    1: 2 * 128 * (3 * 64 * 128 + 3 * 64 * 64 + 3 * 64 * 128 + 64 * 128 + 64 * 64 + 3 * 128 * 64)}
 CHUNK_KERNEL_SRC = os.path.join(ROOT, "context_kda_gb300", "csrc", "chunk_fwd.cu")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "chunk_forward_t8192_h16_s4.md")
 
@@ -281,6 +284,12 @@ def run_ours(args, w, rank, world, local_rank):
     T_cont = int(plan[9])
     flops = T * H * FLOPS_STATE + T_cont * H * FLOPS_TRANSITION
     achieved = flops / (kern_ms[0] / 1e3) / 1e12
+    items_off, pieces_off = int(plan[18]), int(plan[17])
+    issued = 0
+    for i in range(int(plan[12])):
+        pc, kind = int(plan[items_off + 2 * i]), int(plan[items_off + 2 * i + 1])
+        ln = int(plan[pieces_off + 8 * pc + 1])
+        issued += ((ln + CH - 1) // CH) * ISSUED_PER_CHUNK[kind] * H
     prof = _profile_values(CHUNK_KERNEL_SRC)
     traffic = float(prof["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in prof else None
     shares = (kern_ms / kern_ms.sum()).tolist()
@@ -291,11 +300,13 @@ def run_ours(args, w, rank, world, local_rank):
         "config": _config(w, world),
         "kernels_ms": {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]},
         "kernel_shares": {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]},
-        "roofline": {"bound": "alu", "kernel": "chunk_forward", "achieved": achieved,
-                     "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_PEAK_TFLOPS,
+        "roofline": {"bound": "tensor", "kernel": "chunk_forward", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "traffic": traffic, "algorithmic_flops_per_launch": flops,
-                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz",
-                     "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": peaks["source"]},
+                     "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                     "issued_tensor_flops_per_launch": issued,
+                     "issued_frac": issued / (kern_ms[0] / 1e3) / 1e12 / peaks["bf16_tflops"],
+                     "hbm_peak_gbs": peaks["hbm_gbs"]},
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

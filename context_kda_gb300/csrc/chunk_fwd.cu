@@ -22,12 +22,15 @@
 // Mapping.  One CTA per (work item, head): 256 threads, 128 state columns c.
 // The state lives transposed in TMEM (lane c, column k) as an FP32 accumulator;
 // every contraction is a tcgen05.mma (M = 128, bf16 operands in shared memory,
-// FP32 accumulation in TMEM).  The contractions that feed the state and the
+// FP32 accumulation in TMEM).  Operand tiles are written row by row with
+// 16-byte stores; the transposed operands (Kt^T, Kb^T, V^T, W) are the same
+// row-major tiles read MN-major.  The contractions that feed the state and the
 // summaries (Kt Kh^T, W, Ut, W X, Kb^T U) use a three-term bf16 split
 // (hi*hi + hi*lo + lo*hi, ~2^-17 relative per product) so the FP32 state and
 // summaries stay within 1e-4; the output-only ones (Qt X, masked QK U) use one
 // term.  The 64 x 64 unit-triangular inverse is solved on the CUDA cores in
-// FP32 (16 x 16 blocks).
+// FP32 (16 x 16 blocks).  Each chunk's raw rows are staged in shared memory
+// by bulk asynchronous copies issued while the previous chunk finishes.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -36,34 +39,31 @@ namespace {
 
 using namespace tc;
 
-// ---- shared-memory map (bytes from the 16-byte aligned dynamic base) -----------------------------------
-constexpr uint32_t LBO_128P = 2064;  // 128-row tiles written column by column (padded chunks)
-constexpr uint32_t LBO_128 = 2048;   // 128-row tiles written row by row
-constexpr uint32_t LBO_64P = 1040;   // 64-row tiles written column by column
-constexpr uint32_t OFF_XT = 0;            // X^T hi | lo: rows c, cols k           (2 x 32768)
-constexpr uint32_t OFF_KQ = 65536;        // [Kt; Qt] hi | lo: rows r / 64+r, cols k (2 x 33024)
-constexpr uint32_t KQ_TILE = 33024;
-constexpr uint32_t OFF_R2 = OFF_KQ + 2 * KQ_TILE;  // 33280 bytes, reused:
-//   Kh hi | lo (rows i, cols k; 2 x 16640)  ->  M fp32 64x64 (16384) + T' hi | lo (rows r, cols i;
-//   2 x 8320 at +16640)  ->  V^T (rows v, cols r; 16384)  ->  -W hi | lo (rows r, cols k; 2 x 16640)
-constexpr uint32_t KH_TILE = 16640;
-constexpr uint32_t OFF_TP = OFF_R2 + 16640;
-constexpr uint32_t TP_TILE = 8320;
-constexpr uint32_t OFF_R3 = OFF_R2 + 33280;  // Kt^T hi | lo (rows k, cols r), then U^T hi | lo (rows c, cols r)
-constexpr uint32_t OFF_R4 = OFF_R3 + 32768;  // Kb^T hi | lo (rows k, cols r)
-constexpr uint32_t T64_TILE = 16384;         // 128 rows x 64 cols, LBO 2048
-constexpr uint32_t OFF_MISC = OFF_R4 + 32768;
-constexpr uint32_t OFF_BETA = OFF_MISC;          // 64 fp32
-constexpr uint32_t OFF_GC = OFF_MISC + 256;      // 128 fp32: exp(Gamma_C)
-constexpr uint32_t OFF_GSUM = OFF_MISC + 768;    // 2 x 128 fp32: per-half decay sums
+// ---- shared-memory map (bytes from the 16-byte aligned dynamic base) ------------------------
+// Tiles are bf16, hi and lo halves back to back; CS = chunk-column stride (see tc.cuh).
+constexpr uint32_t OFF_XT = 0;        // X^T: rows c (128), cols k (128), CS 2048           2 x 32768
+constexpr uint32_t OFF_KQ = 65536;    // [Kt; Qt]: rows r / 64 + r, cols k, CS 2048          2 x 32768
+constexpr uint32_t OFF_KH = 131072;   // Kh: rows i (64), cols k, CS 1024                    2 x 16384
+//   then M (fp32 64 x 64) + T (fp32 64 x 64, at +16384); then -W read MN-major:
+//   rows k (128), cols r (64), CS 2048                                                   2 x 16384
+constexpr uint32_t OFF_KB = 163840;   // Kb: rows r (64), cols k, CS 1024                    2 x 16384
+constexpr uint32_t OFF_VT = 196608;   // V: rows r (64), cols v, CS 1024 (16384) + T': rows r, cols i,
+//   CS 1024 (2 x 8192 at +16384); then U^T: rows c (128), cols r (64), CS 2048          2 x 16384
+constexpr uint32_t OFF_MISC = 229376;
+constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
+constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: Gamma_C (log2-scaled), then exp(Gamma_C)
+constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
-// QK (masked, bf16) reuses the Qt rows of the lo [Kt; Qt] tile once the first MMA is done;
-// T (fp32) reuses the Kt rows of the hi tile: row r at OFF_KQ + (r/4)*KQ-chunk + (r%4)*256.
-constexpr uint32_t OFF_QKL = OFF_KQ + KQ_TILE + 1024;
-constexpr uint32_t OFF_QT_HI = OFF_KQ + 1024;
-// Raw rows of the next chunk, staged by bulk copies while the current chunk finishes:
-// v (bf16, 256 B/row) in R2, g (fp32, 512 B/row) in R3, q and k (bf16) in R4.
-constexpr uint32_t STG_V = OFF_R2, STG_G = OFF_R3, STG_Q = OFF_R4, STG_K = OFF_R4 + 16384;
+constexpr uint32_t T128 = 32768, T64 = 16384;
+constexpr uint32_t OFF_M32 = OFF_KH, OFF_T32 = OFF_KH + 16384;
+constexpr uint32_t OFF_TP = OFF_VT + 16384;          // T' hi | lo (8192 each)
+constexpr uint32_t OFF_QKL = OFF_KQ + T128 + 1024;   // masked QK (bf16) in the Qt rows of the lo tile
+constexpr uint32_t OFF_QT_HI = OFF_KQ + 1024;        // Qt rows of the hi tile
+// raw rows of the next chunk (bulk copies): q, k, v (bf16, 256 B/row) and g (fp32, 512 B/row); each
+// row pitch is padded by 16 B so that reading one 8-column piece of consecutive rows is conflict-free
+constexpr uint32_t PITCH_B = 272, PITCH_G = 528;
+constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 64 * PITCH_B, STG_V = OFF_KQ + 128 * PITCH_B;
+constexpr uint32_t STG_G = OFF_KH;   // 64 * 528 bytes: spills from the Kh region into the Kb region
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols), later O^T
@@ -72,23 +72,22 @@ constexpr uint32_t TM_U = 128;    // Ut^T, then U^T
 constexpr uint32_t TM_X = 256;    // X^T (128 cols)
 constexpr uint32_t TM_COLS = 512;
 
+constexpr float LOG2E = 1.4426950408889634f;
+
 __device__ int g_chunk_status;   // set to KDA_ERR_TIMEOUT when a bounded wait expires
 
-__device__ __forceinline__ float *t32_row(unsigned char *base, int r)
+// fp32 64 x 64 scratch with the 16-byte chunk index XOR-swizzled by the row
+__device__ __forceinline__ float *f32_at(unsigned char *base, uint32_t off, int r, int i)
 {
-    return reinterpret_cast<float *>(base + OFF_KQ + (r >> 2) * LBO_128P + (r & 3) * 256);
-}
-__device__ __forceinline__ float *m32_at(unsigned char *base, int r, int i)
-{
-    return reinterpret_cast<float *>(base + OFF_R2 + r * 256 + ((((i >> 2) ^ (r & 15))) << 4) + (i & 3) * 4);
+    return reinterpret_cast<float *>(base + off + r * 256 + (((i >> 2) ^ (r & 15)) << 4) + (i & 3) * 4);
 }
 
-__device__ __forceinline__ void st_bf16(unsigned char *base, uint32_t off, uint16_t v)
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 {
-    *reinterpret_cast<uint16_t *>(base + off) = v;
+    return static_cast<uint32_t>(f32_to_bf16_bits(a)) | (static_cast<uint32_t>(f32_to_bf16_bits(b)) << 16);
 }
 
-// Writes 8 consecutive bf16 (hi and lo of 8 fp32 values) as two 16-byte stores.
+// Writes 8 consecutive values as bf16 hi and lo (two 16-byte stores).
 __device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, const float *x)
 {
     uint32_t h[4], l[4];
@@ -102,6 +101,16 @@ __device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, 
     }
     *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 w, float *x)
+{
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        x[2 * p] = __uint_as_float(ww[p] << 16);
+        x[2 * p + 1] = __uint_as_float(ww[p] & 0xFFFF0000u);
+    }
 }
 
 __global__ void __launch_bounds__(256, 1)
@@ -170,10 +179,10 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         const int arr = tid >> 6, r = tid & 63;
         if (r < Ln && (arr != 2 || kind == 0)) {
             const size_t row = static_cast<size_t>(t0n + r) * H + h;
-            if (arr == 0) bulk_g2s(sbase + STG_Q + r * 256, q + row * KD, 256, ldbar);
-            else if (arr == 1) bulk_g2s(sbase + STG_K + r * 256, k + row * KD, 256, ldbar);
-            else if (arr == 2) bulk_g2s(sbase + STG_V + r * 256, v + row * VD, 256, ldbar);
-            else bulk_g2s(sbase + STG_G + r * 512, g + row * KD, 512, ldbar);
+            if (arr == 0) bulk_g2s(sbase + STG_Q + r * PITCH_B, q + row * KD, 256, ldbar);
+            else if (arr == 1) bulk_g2s(sbase + STG_K + r * PITCH_B, k + row * KD, 256, ldbar);
+            else if (arr == 2) bulk_g2s(sbase + STG_V + r * PITCH_B, v + row * VD, 256, ldbar);
+            else bulk_g2s(sbase + STG_G + r * PITCH_G, g + row * KD, 512, ldbar);
         }
         if (tid < 64) beta_next = (tid < Ln) ? beta[static_cast<size_t>(t0n + tid) * H + h] : 0.f;
         loads_pending = true;
@@ -196,8 +205,8 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             tmem_st32(tl + TM_X + k0, x);
 #pragma unroll
             for (int m = 0; m < 4; ++m)
-                st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, LBO_128),
-                          base + OFF_XT + 32768 + cm_off(c_lane, k0 + 8 * m, LBO_128), x + 8 * m);
+                st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
+                          base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
         }
         fence_before();
         fence_async_smem();
@@ -209,80 +218,79 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         const int t0 = start + ci * CH;
         const int L = min(CH, len - ci * CH);
 
-        // ================= A: staged rows -> decayed keys / queries in operand tiles =========
-        uint32_t vv[16];   // this thread's v column (32 rows, bf16 pairs), kept for V^T in D
+        // ================= A: staged rows -> decayed keys / queries / values in operand tiles =====
         {
             if (!mbar_wait(ldbar, ld_phase & 1)) s_abort = 1;
             ++ld_phase;
             loads_pending = false;
-            const int kc = tid & 127, hr = tid >> 7;
-            const float *sg = reinterpret_cast<const float *>(base + STG_G);
-            const uint16_t *sq = reinterpret_cast<const uint16_t *>(base + STG_Q);
-            const uint16_t *sk = reinterpret_cast<const uint16_t *>(base + STG_K);
-            const uint16_t *sv = reinterpret_cast<const uint16_t *>(base + STG_V);
-            float gam[32];
-            uint32_t kv[16], qv[16];
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = hr * 32 + j;
-                const bool ok = r < L;
-                const float gv = ok ? sg[r * 128 + kc] : 0.f;
-                const uint32_t kb16 = ok ? sk[r * 128 + kc] : 0u;
-                const uint32_t qb16 = ok ? sq[r * 128 + kc] : 0u;
-                const uint32_t vb16 = (ok && kind == 0) ? sv[r * 128 + kc] : 0u;
-                acc += gv;
-                gam[j] = acc;
-                if (j & 1) {
-                    kv[j >> 1] |= kb16 << 16;
-                    qv[j >> 1] |= qb16 << 16;
-                    vv[j >> 1] |= vb16 << 16;
-                } else {
-                    kv[j >> 1] = kb16;
-                    qv[j >> 1] = qb16;
-                    vv[j >> 1] = vb16;
+            // A1: log2-scaled cumulative decay per key channel, in place over the staged g
+            {
+                const int kc = tid & 127, hr = tid >> 7;
+                float *sg = reinterpret_cast<float *>(base + STG_G);
+                float acc = 0.f;
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int r = hr * 32 + j;
+                    acc += (r < L) ? sg[r * (PITCH_G / 4) + kc] * LOG2E : 0.f;
+                    sg[r * (PITCH_G / 4) + kc] = acc;
                 }
+                s_gsum[hr * 128 + kc] = acc;
+                if (tid < 64) s_beta[tid] = beta_next;
+                __syncthreads();
+                if (hr) {
+                    const float off = s_gsum[kc];
+#pragma unroll 8
+                    for (int j = 0; j < 32; ++j) sg[(32 + j) * (PITCH_G / 4) + kc] += off;
+                } else {
+                    s_gc[kc] = s_gsum[kc] + s_gsum[128 + kc];   // log2-scaled Gamma_C for now
+                }
+                __syncthreads();
             }
-            s_gsum[hr * 128 + kc] = acc;
-            if (tid < 64) s_beta[tid] = beta_next;
-            __syncthreads();   // staging consumed: R2, R3, R4 may be rewritten from here
-            const float off = hr ? s_gsum[kc] : 0.f;
-            const float gC = s_gsum[kc] + s_gsum[128 + kc];
-            if (hr == 0) s_gc[kc] = expf(gC);
+            // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
+            //     the lanes of a warp hold consecutive rows of one piece column
+            const int pr = tid & 63, pcg = tid >> 6;
+            float gam[4][8];
+            uint4 kw[4], qw[4], vw[4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float ktv[8], kbv[8];
+            for (int i = 0; i < 4; ++i) {
+                const int r = pr, c8 = (pcg + 4 * i) * 8;
+                const float4 *g4 = reinterpret_cast<const float4 *>(base + STG_G + r * PITCH_G + c8 * 4);
+                const float4 a = g4[0], b = g4[1];
+                gam[i][0] = a.x; gam[i][1] = a.y; gam[i][2] = a.z; gam[i][3] = a.w;
+                gam[i][4] = b.x; gam[i][5] = b.y; gam[i][6] = b.z; gam[i][7] = b.w;
+                const bool ok = r < L;
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                kw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_K + r * PITCH_B + c8 * 2) : z;
+                qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + r * PITCH_B + c8 * 2) : z;
+                vw[i] = (ok && kind == 0) ? *reinterpret_cast<const uint4 *>(base + STG_V + r * PITCH_B + c8 * 2) : z;
+            }
+            __syncthreads();   // staging consumed: every region may be rewritten from here
+            // A3: Kt, Qt (stacked), Kh, Kb as bf16 hi/lo and V as bf16, one row piece at a time
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = pr, c8 = (pcg + 4 * i) * 8;
+                float kf[8], qf[8], kt[8], qt[8], kh[8], kb[8];
+                bf16x8_to_f32(kw[i], kf);
+                bf16x8_to_f32(qw[i], qf);
 #pragma unroll
                 for (int e8 = 0; e8 < 8; ++e8) {
-                    const int j = 8 * m + e8;
-                    const int r = hr * 32 + j;
-                    const float G = off + gam[j];
-                    const float e = expf(G), ei = expf(-G), eb = expf(gC - G);
-                    const uint32_t kw = kv[j >> 1], qw = qv[j >> 1];
-                    const float kf = __uint_as_float((j & 1) ? (kw & 0xFFFF0000u) : (kw << 16));
-                    const float qf = __uint_as_float((j & 1) ? (qw & 0xFFFF0000u) : (qw << 16));
-                    const float kt = e * kf, qt = scale * e * qf, kh = ei * kf;
-                    ktv[e8] = kt;
-                    kbv[e8] = eb * kf;
-                    uint16_t hi, lo;
-                    split_bf16(kt, hi, lo);
-                    st_bf16(base, OFF_KQ + cm_off(r, kc, LBO_128P), hi);
-                    st_bf16(base, OFF_KQ + KQ_TILE + cm_off(r, kc, LBO_128P), lo);
-                    split_bf16(qt, hi, lo);
-                    st_bf16(base, OFF_KQ + cm_off(64 + r, kc, LBO_128P), hi);
-                    st_bf16(base, OFF_KQ + KQ_TILE + cm_off(64 + r, kc, LBO_128P), lo);
-                    split_bf16(kh, hi, lo);
-                    st_bf16(base, OFF_R2 + cm_off(r, kc, LBO_64P), hi);
-                    st_bf16(base, OFF_R2 + KH_TILE + cm_off(r, kc, LBO_64P), lo);
+                    const float G = gam[i][e8];
+                    const float e = exp2f(G), ei = exp2f(-G), eb = exp2f(s_gc[c8 + e8] - G);
+                    kt[e8] = e * kf[e8];
+                    qt[e8] = scale * e * qf[e8];
+                    kh[e8] = ei * kf[e8];
+                    kb[e8] = eb * kf[e8];
                 }
-                const int r0 = hr * 32 + 8 * m;
-                st_split8(base + OFF_R3 + cm_off(kc, r0, LBO_128), base + OFF_R3 + T64_TILE + cm_off(kc, r0, LBO_128),
-                          ktv);
-                st_split8(base + OFF_R4 + cm_off(kc, r0, LBO_128), base + OFF_R4 + T64_TILE + cm_off(kc, r0, LBO_128),
-                          kbv);
+                const uint32_t o_r = cm_off(r, c8, 2048), o_q = cm_off(64 + r, c8, 2048), o_64 = cm_off(r, c8, 1024);
+                st_split8(base + OFF_KQ + o_r, base + OFF_KQ + T128 + o_r, kt);
+                st_split8(base + OFF_KQ + o_q, base + OFF_KQ + T128 + o_q, qt);
+                st_split8(base + OFF_KH + o_64, base + OFF_KH + T64 + o_64, kh);
+                st_split8(base + OFF_KB + o_64, base + OFF_KB + T64 + o_64, kb);
+                if (kind == 0) *reinterpret_cast<uint4 *>(base + OFF_VT + o_64) = vw[i];
             }
             fence_async_smem();
             __syncthreads();
+            if (tid < 128) s_gc[tid] = exp2f(s_gc[tid]);   // exp(Gamma_C), read in F after barriers
             if (s_abort) aborted = true;
         }
         if (aborted) break;
@@ -291,13 +299,13 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         if (tid == 0) {
             fence_after();
             const uint32_t id = idesc_bf16(128, 64);
-            const uint32_t aoff[3] = {0, 0, KQ_TILE}, boff[3] = {0, KH_TILE, 0};
+            const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
 #pragma unroll
             for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * LBO_128P, LBO_128P),
-                             sdesc(sbase + OFF_R2 + boff[ps] + kk * 2 * LBO_64P, LBO_64P), id, (ps | kk) != 0);
+                    mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
+                             sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
             commit(mbar);
         }
         wait_mma();
@@ -317,7 +325,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     m4.y = (i0 + 1 < r) ? br * d[4 * j4 + 1] : 0.f;
                     m4.z = (i0 + 2 < r) ? br * d[4 * j4 + 2] : 0.f;
                     m4.w = (i0 + 3 < r) ? br * d[4 * j4 + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(m32_at(base, r, i0)) = m4;
+                    *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, r, i0)) = m4;
                 }
             } else {
                 const int r = c_lane - 64;
@@ -327,11 +335,9 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll
                     for (int p2 = 0; p2 < 4; ++p2) {
                         const int i0 = hw * 32 + 8 * m + 2 * p2;
-                        const uint16_t a0 = f32_to_bf16_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f);
-                        const uint16_t a1 = f32_to_bf16_bits(i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
-                        w[p2] = static_cast<uint32_t>(a0) | (static_cast<uint32_t>(a1) << 16);
+                        w[p2] = pack_bf16x2(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
                     }
-                    *reinterpret_cast<uint4 *>(base + OFF_QKL + cm_off(r, hw * 32 + 8 * m, LBO_128P)) =
+                    *reinterpret_cast<uint4 *>(base + OFF_QKL + cm_off(r, hw * 32 + 8 * m, 2048)) =
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
@@ -350,11 +356,11 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 for (int rr = 0; rr < 16; ++rr) {
                     float s = 0.f;
 #pragma unroll
-                    for (int ii = 0; ii < rr; ++ii) s = fmaf(*m32_at(base, r0 + rr, r0 + ii), x[ii], s);
+                    for (int ii = 0; ii < rr; ++ii) s = fmaf(*f32_at(base, OFF_M32, r0 + rr, r0 + ii), x[ii], s);
                     x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -s);
                 }
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) t32_row(base, r0 + rr)[r0 + jj] = x[rr];
+                for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
             }
             __syncthreads();
             // off-diagonal blocks by distance d: Y = sum_{k=j}^{i-1} M_ik T_kj, T_ij = -T_ii Y
@@ -371,14 +377,15 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                         for (int kb = j; kb < i; ++kb)
 #pragma unroll
                             for (int m = 0; m < 16; ++m)
-                                s = fmaf(*m32_at(base, 16 * i + rr, 16 * kb + m), t32_row(base, 16 * kb + m)[16 * j + cc], s);
+                                s = fmaf(*f32_at(base, OFF_M32, 16 * i + rr, 16 * kb + m),
+                                         *f32_at(base, OFF_T32, 16 * kb + m, 16 * j + cc), s);
                         y[bi] = s;
                     }
                 }
                 // Y_ij goes to the unused upper-triangle block (j, i) of M
 #pragma unroll
                 for (int bi = 0; bi < 3; ++bi)
-                    if (bi < 4 - dd) *m32_at(base, 16 * bi + rr, 16 * (bi + dd) + cc) = y[bi];
+                    if (bi < 4 - dd) *f32_at(base, OFF_M32, 16 * bi + rr, 16 * (bi + dd) + cc) = y[bi];
                 __syncthreads();
 #pragma unroll
                 for (int bi = 0; bi < 3; ++bi) {
@@ -387,70 +394,62 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                         float s = 0.f;
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            s = fmaf(t32_row(base, 16 * i + rr)[16 * i + m], *m32_at(base, 16 * j + m, 16 * i + cc), s);
-                        t32_row(base, 16 * i + rr)[16 * j + cc] = -s;
+                            s = fmaf(*f32_at(base, OFF_T32, 16 * i + rr, 16 * i + m),
+                                     *f32_at(base, OFF_M32, 16 * j + m, 16 * i + cc), s);
+                        *f32_at(base, OFF_T32, 16 * i + rr, 16 * j + cc) = -s;
                     }
                 }
                 __syncthreads();
             }
             // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
             {
-                const int r = tid >> 2, i0 = (tid & 3) * 16;
-                const float *tr = t32_row(base, r);
+                const int r = tid & 63, i0 = (tid >> 6) * 16;
                 float tv[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) tv[j] = (i0 + j <= r) ? tr[i0 + j] * s_beta[i0 + j] : 0.f;
-                st_split8(base + OFF_TP + cm_off(r, i0, LBO_64P), base + OFF_TP + TP_TILE + cm_off(r, i0, LBO_64P), tv);
-                st_split8(base + OFF_TP + cm_off(r, i0 + 8, LBO_64P),
-                          base + OFF_TP + TP_TILE + cm_off(r, i0 + 8, LBO_64P), tv + 8);
-            }
-            __syncthreads();   // M (fp32) is dead from here: V^T may overwrite it
-            if (kind == 0) {   // V^T (rows v, cols r), exact bf16, from this thread's v column
-                const int vc = tid & 127, hr = tid >> 7;
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    *reinterpret_cast<uint4 *>(base + OFF_R2 + cm_off(vc, hr * 32 + 8 * m, LBO_128)) =
-                        make_uint4(vv[4 * m], vv[4 * m + 1], vv[4 * m + 2], vv[4 * m + 3]);
+                for (int j = 0; j < 16; ++j)
+                    tv[j] = (i0 + j <= r) ? *f32_at(base, OFF_T32, r, i0 + j) * s_beta[i0 + j] : 0.f;
+                st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
+                st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),
+                          tv + 8);
             }
             fence_async_smem();
             __syncthreads();
         }
 
         // ================= E: W^T = Kt^T T'^T (3-term); Ut^T = V^T T'^T (2-term) =============
+        // Kt^T and V^T are the row-major Kt / V tiles read MN-major.
         if (tid == 0) {
             fence_after();
-            const uint32_t id = idesc_bf16(128, 64);
-            const uint32_t aoff[3] = {0, 0, T64_TILE}, boff[3] = {0, TP_TILE, 0};
+            const uint32_t id = idesc_bf16(128, 64, 1, 0);
+            const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, 8192, 0};
 #pragma unroll
             for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_W, sdesc(sbase + OFF_R3 + aoff[ps] + kk * 2 * LBO_128, LBO_128),
-                             sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * LBO_64P, LBO_64P), id, (ps | kk) != 0);
+                    mma_bf16(tbase + TM_W, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 256, 128, 2048),
+                             sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
             if (kind == 0) {
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tbase + TM_U, sdesc(sbase + OFF_R2 + kk * 2 * LBO_128, LBO_128),
-                                 sdesc(sbase + OFF_TP + ps * TP_TILE + kk * 2 * LBO_64P, LBO_64P), id, (ps | kk) != 0);
+                        mma_bf16(tbase + TM_U, sdesc(sbase + OFF_VT + kk * 256, 128, 1024),
+                                 sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
             }
             commit(mbar);
         }
         wait_mma();
 
-        // ================= F: -W (rows r, cols k) hi/lo; X^T *= exp(Gamma_C) in TMEM ==========
+        // ================= F: -W as an MN-major operand (rows k, cols r); X^T *= exp(Gamma_C) ===
         {
             float d[32];
             tmem_ld32(tl + TM_W + hw * 32, d);   // W^T[k = c_lane][r = hw*32 + j]
-            const int kc = c_lane;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = hw * 32 + j;
-                uint16_t hi, lo;
-                split_bf16(-d[j], hi, lo);
-                st_bf16(base, OFF_R2 + cm_off(r, kc, LBO_64P), hi);
-                st_bf16(base, OFF_R2 + KH_TILE + cm_off(r, kc, LBO_64P), lo);
+            for (int j = 0; j < 32; ++j) d[j] = -d[j];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
+                st_split8(base + OFF_KH + off, base + OFF_KH + T64 + off, d + 8 * m);
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -471,19 +470,19 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         // ================= G: U^T = Ut^T - X^T W^T (3-term); O^T = X^T Qt^T (1-term) ==========
         if (tid == 0) {
             fence_after();
-            const uint32_t id = idesc_bf16(128, 64);
-            const uint32_t aoff[3] = {0, 0, 32768}, boff[3] = {0, KH_TILE, 0};
+            const uint32_t idw = idesc_bf16(128, 64, 0, 1), idq = idesc_bf16(128, 64);
+            const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
 #pragma unroll
             for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_XT + aoff[ps] + kk * 2 * LBO_128, LBO_128),
-                             sdesc(sbase + OFF_R2 + boff[ps] + kk * 2 * LBO_64P, LBO_64P), id,
+                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_XT + aoff[ps] + kk * 2 * 2048, 2048),
+                             sdesc(sbase + OFF_KH + boff[ps] + kk * 256, 128, 2048), idw,
                              (kind == 0) || ((ps | kk) != 0));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_XT + kk * 2 * LBO_128, LBO_128),
-                         sdesc(sbase + OFF_QT_HI + kk * 2 * LBO_128P, LBO_128P), id, kk != 0);
+                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), idq, kk != 0);
             commit(mbar);
         }
         wait_mma();
@@ -493,9 +492,10 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             float d[32];
             tmem_ld32(tl + TM_U + hw * 32, d);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-                st_split8(base + OFF_R3 + cm_off(c_lane, hw * 32 + 8 * m, LBO_128),
-                          base + OFF_R3 + T64_TILE + cm_off(c_lane, hw * 32 + 8 * m, LBO_128), d + 8 * m);
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
+                st_split8(base + OFF_VT + off, base + OFF_VT + T64 + off, d + 8 * m);
+            }
             fence_before();
             fence_async_smem();
             __syncthreads();
@@ -503,21 +503,21 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         }
         if (aborted) break;
 
-        // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kb (3-term) ==================
+        // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kb (3-term, Kb read MN-major) ==
         if (tid == 0) {
             fence_after();
-            const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128);
+            const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_R3 + kk * 2 * LBO_128, LBO_128),
-                         sdesc(sbase + OFF_QKL + kk * 2 * LBO_128P, LBO_128P), id64, 1);
-            const uint32_t aoff[3] = {0, 0, T64_TILE}, boff[3] = {0, T64_TILE, 0};
+                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_VT + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_QKL + kk * 2 * 2048, 2048), id64, 1);
+            const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, T64, 0};
 #pragma unroll
             for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_X, sdesc(sbase + OFF_R3 + aoff[ps] + kk * 2 * LBO_128, LBO_128),
-                             sdesc(sbase + OFF_R4 + boff[ps] + kk * 2 * LBO_128, LBO_128), id128, 1);
+                    mma_bf16(tbase + TM_X, sdesc(sbase + OFF_VT + aoff[ps] + kk * 2 * 2048, 2048),
+                             sdesc(sbase + OFF_KB + boff[ps] + kk * 256, 128, 1024), id128, 1);
             commit(mbar);
         }
         wait_mma();
@@ -547,8 +547,8 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 tmem_ld32(tl + TM_X + k0, x);
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
-                    st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, LBO_128),
-                              base + OFF_XT + 32768 + cm_off(c_lane, k0 + 8 * m, LBO_128), x + 8 * m);
+                    st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
+                              base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
             }
             fence_before();
             fence_async_smem();

@@ -4,11 +4,12 @@
 //
 // Operand tiles live in shared memory in the no-swizzle canonical layout of
 // 8-row x 16-byte core matrices: element (row, col) of a bf16 tile is at byte
-//     (col / 8) * LBO + (row / 8) * 128 + (row % 8) * 16 + (col % 8) * 2,
-// i.e. row groups are 128 bytes apart (SBO = 128) and 8-column chunks along
-// the contraction dimension are LBO bytes apart.  An LBO of (rows/8)*128 + 16
-// pads each chunk column by 16 bytes so that writes of consecutive columns of
-// one row hit different banks.
+//     (col / 8) * CS + (row / 8) * 128 + (row % 8) * 16 + (col % 8) * 2,
+// i.e. 8-row groups are 128 bytes apart and 8-column chunks CS bytes apart.
+// Used K-major (rows = M or N index, cols = contraction index) the descriptor
+// takes LBO = CS, SBO = 128.  The same bytes read MN-major (rows = contraction
+// index, cols = M or N index) take LBO = 128, SBO = CS: a row-major tile of X
+// is then the operand X^T without any transposed write.
 #pragma once
 
 #include <stdint.h>
@@ -29,10 +30,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 accumulator, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, M x N.  a_mn / b_mn
+// select an MN-major operand (the M / N index contiguous within a core-matrix row);
+// otherwise the operand is K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn = 0, int b_mn = 0)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
