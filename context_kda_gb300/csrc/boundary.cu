@@ -36,13 +36,7 @@ __device__ __forceinline__ void split_store8(unsigned char *base, uint32_t off_h
 {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        uint16_t h0, l0, h1, l1;
-        split_bf16(x[2 * p], h0, l0);
-        split_bf16(x[2 * p + 1], h1, l1);
-        h[p] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-        l[p] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
-    }
+    for (int p = 0; p < 4; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], h[p], l[p]);
     *reinterpret_cast<uint4 *>(base + off_hi) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(base + off_lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -103,7 +97,7 @@ boundary_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ S
         float4 qv[16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int id = tid + 256 * i, r = id >> 4, kc = id & 15;
+            const int id = tid + 256 * i, r = id & 127, kc = id >> 7;   // lanes: consecutive rows
             const float4 *p4 = reinterpret_cast<const float4 *>(src + static_cast<size_t>(r) * KD + kc * 8);
             const bool ok = r < rows;
             qv[2 * i] = ok ? p4[0] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -116,7 +110,7 @@ boundary_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ S
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int id = tid + 256 * i, r = id >> 4, kc = id & 15;
+            const int id = tid + 256 * i, r = id & 127, kc = id >> 7;
             const uint32_t off = cm_off(r, kc * 8, LBO);
             split_store8(smem, OFF_A + off, OFF_A + TILE + off, reinterpret_cast<const float *>(&qv[2 * i]));
         }
@@ -164,8 +158,7 @@ boundary_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ S
                     for (int p = 0; p < 4; ++p) {
                         const float a0 = __uint_as_float(ww[p] << 16) + d[8 * m + 2 * p];
                         const float a1 = __uint_as_float(ww[p] & 0xFFFF0000u) + d[8 * m + 2 * p + 1];
-                        ww[p] = static_cast<uint32_t>(f32_to_bf16_bits(a0)) |
-                                (static_cast<uint32_t>(f32_to_bf16_bits(a1)) << 16);
+                        ww[p] = bf16x2_bits(a0, a1);
                     }
                     dst[m] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
                 }

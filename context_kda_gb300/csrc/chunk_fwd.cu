@@ -51,7 +51,7 @@ constexpr uint32_t OFF_VT = 196608;   // V: rows r (64), cols v, CS 1024 (16384)
 //   CS 1024 (2 x 8192 at +16384); then U^T: rows c (128), cols r (64), CS 2048          2 x 16384
 constexpr uint32_t OFF_MISC = 229376;
 constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
-constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: Gamma_C (log2-scaled), then exp(Gamma_C)
+constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
 constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
 constexpr uint32_t T128 = 32768, T64 = 16384;
@@ -82,23 +82,13 @@ __device__ __forceinline__ float *f32_at(unsigned char *base, uint32_t off, int 
     return reinterpret_cast<float *>(base + off + r * 256 + (((i >> 2) ^ (r & 15)) << 4) + (i & 3) * 4);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
-{
-    return static_cast<uint32_t>(f32_to_bf16_bits(a)) | (static_cast<uint32_t>(f32_to_bf16_bits(b)) << 16);
-}
 
 // Writes 8 consecutive values as bf16 hi and lo (two 16-byte stores).
 __device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, const float *x)
 {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        uint16_t h0, l0, h1, l1;
-        split_bf16(x[2 * p], h0, l0);
-        split_bf16(x[2 * p + 1], h1, l1);
-        h[p] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-        l[p] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
-    }
+    for (int p = 0; p < 4; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], h[p], l[p]);
     *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -242,7 +232,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll 8
                     for (int j = 0; j < 32; ++j) sg[(32 + j) * (PITCH_G / 4) + kc] += off;
                 } else {
-                    s_gc[kc] = s_gsum[kc] + s_gsum[128 + kc];   // log2-scaled Gamma_C for now
+                    s_gc[kc] = exp2f(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
                 }
                 __syncthreads();
             }
@@ -275,7 +265,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll
                 for (int e8 = 0; e8 < 8; ++e8) {
                     const float G = gam[i][e8];
-                    const float e = exp2f(G), ei = exp2f(-G), eb = exp2f(s_gc[c8 + e8] - G);
+                    const float e = exp2f(G), ei = exp2f(-G), eb = s_gc[c8 + e8] * ei;
                     kt[e8] = e * kf[e8];
                     qt[e8] = scale * e * qf[e8];
                     kh[e8] = ei * kf[e8];
@@ -290,7 +280,6 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             }
             fence_async_smem();
             __syncthreads();
-            if (tid < 128) s_gc[tid] = exp2f(s_gc[tid]);   // exp(Gamma_C), read in F after barriers
             if (s_abort) aborted = true;
         }
         if (aborted) break;
@@ -335,7 +324,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll
                     for (int p2 = 0; p2 < 4; ++p2) {
                         const int i0 = hw * 32 + 8 * m + 2 * p2;
-                        w[p2] = pack_bf16x2(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                        w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
                     }
                     *reinterpret_cast<uint4 *>(base + OFF_QKL + cm_off(r, hw * 32 + 8 * m, 2048)) =
                         make_uint4(w[0], w[1], w[2], w[3]);

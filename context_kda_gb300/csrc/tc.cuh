@@ -153,12 +153,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// bf16 split of an fp32 value: hi = bf16(x), lo = bf16(x - hi); hi + lo carries ~16 bits.
-__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo)
+// Two fp32 values rounded to a packed bf16 pair (a in the low half), one conversion instruction.
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
 {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    hi = __bfloat16_as_ushort(h);
-    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// bf16 split of a pair: hi = bf16(x), lo = bf16(x - hi), packed; hi + lo carries ~16 bits.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uint32_t &lo)
+{
+    hi = bf16x2_bits(a, b);
+    lo = bf16x2_bits(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
 
 }  // namespace tc
