@@ -352,43 +352,63 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
             }
             __syncthreads();
-            // off-diagonal blocks by distance d: Y = sum_{k=j}^{i-1} M_ik T_kj, T_ij = -T_ii Y
-            const int rr = tid >> 4, cc = tid & 15;
+            // off-diagonal blocks by distance dd: Y = sum_{k=j}^{i-1} M_ik T_kj, then T_ij = -T_ii Y.
+            // Thread -> block bi (j = bi, i = bi + dd), row rr, four adjacent columns c4..c4+3.
+            {
+                const int bi = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
 #pragma unroll
-            for (int dd = 1; dd < 4; ++dd) {
-                float y[3];
+                for (int dd = 1; dd < 4; ++dd) {
+                    const bool act = bi < 4 - dd;
+                    const int i = bi + dd, j = bi;
+                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (act) {
 #pragma unroll
-                for (int bi = 0; bi < 3; ++bi) {
-                    y[bi] = 0.f;
-                    if (bi < 4 - dd) {
-                        const int i = bi + dd, j = bi;
-                        float s = 0.f;
-                        for (int kb = j; kb < i; ++kb)
+                        for (int kb = 0; kb < 3; ++kb) {
+                            if (kb < dd) {
+                                const int kk = j + kb;
 #pragma unroll
-                            for (int m = 0; m < 16; ++m)
-                                s = fmaf(*f32_at(base, OFF_M32, 16 * i + rr, 16 * kb + m),
-                                         *f32_at(base, OFF_T32, 16 * kb + m, 16 * j + cc), s);
-                        y[bi] = s;
+                                for (int m4 = 0; m4 < 4; ++m4) {
+                                    const float4 mv = *reinterpret_cast<const float4 *>(
+                                        f32_at(base, OFF_M32, 16 * i + rr, 16 * kk + 4 * m4));
+                                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float4 tv = *reinterpret_cast<const float4 *>(
+                                            f32_at(base, OFF_T32, 16 * kk + 4 * m4 + e, 16 * j + c4));
+                                        y.x = fmaf(mm[e], tv.x, y.x);
+                                        y.y = fmaf(mm[e], tv.y, y.y);
+                                        y.z = fmaf(mm[e], tv.z, y.z);
+                                        y.w = fmaf(mm[e], tv.w, y.w);
+                                    }
+                                }
+                            }
+                        }
+                        // Y_ij goes to the unused upper-triangle block (j, i) of M
+                        *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, 16 * j + rr, 16 * i + c4)) = y;
                     }
-                }
-                // Y_ij goes to the unused upper-triangle block (j, i) of M
+                    __syncthreads();
+                    if (act) {
+                        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int bi = 0; bi < 3; ++bi)
-                    if (bi < 4 - dd) *f32_at(base, OFF_M32, 16 * bi + rr, 16 * (bi + dd) + cc) = y[bi];
-                __syncthreads();
+                        for (int m4 = 0; m4 < 4; ++m4) {
+                            const float4 tv = *reinterpret_cast<const float4 *>(
+                                f32_at(base, OFF_T32, 16 * i + rr, 16 * i + 4 * m4));
+                            const float tt[4] = {tv.x, tv.y, tv.z, tv.w};
 #pragma unroll
-                for (int bi = 0; bi < 3; ++bi) {
-                    if (bi < 4 - dd) {
-                        const int i = bi + dd, j = bi;
-                        float s = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            s = fmaf(*f32_at(base, OFF_T32, 16 * i + rr, 16 * i + m),
-                                     *f32_at(base, OFF_M32, 16 * j + m, 16 * i + cc), s);
-                        *f32_at(base, OFF_T32, 16 * i + rr, 16 * j + cc) = -s;
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 yv = *reinterpret_cast<const float4 *>(
+                                    f32_at(base, OFF_M32, 16 * j + 4 * m4 + e, 16 * i + c4));
+                                t.x = fmaf(tt[e], yv.x, t.x);
+                                t.y = fmaf(tt[e], yv.y, t.y);
+                                t.z = fmaf(tt[e], yv.z, t.z);
+                                t.w = fmaf(tt[e], yv.w, t.w);
+                            }
+                        }
+                        *reinterpret_cast<float4 *>(f32_at(base, OFF_T32, 16 * i + rr, 16 * j + c4)) =
+                            make_float4(-t.x, -t.y, -t.z, -t.w);
                     }
+                    __syncthreads();
                 }
-                __syncthreads();
             }
             // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
             {
@@ -514,20 +534,17 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         // ================= J: outputs (or qhat) to HBM; new X^T split into shared memory ========
         if (ci + 1 < nch) issue_loads(ci + 1);   // staging regions are free once I has completed
         {
+            // O^T[c][r] -> row-major O tile in the free V/U region, then 16-byte coalesced stores
             float d[32];
             tmem_ld32(tl + TM_D1 + hw * 32, d);   // O^T[c][r = hw*32 + j]
             if (kind == 0) {
+                uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_VT);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int r = hw * 32 + j;
-                    if (r < L) o[(static_cast<size_t>(t0 + r) * H + h) * VD + c_lane] = f32_to_bf16_bits(d[j]);
-                }
+                for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = f32_to_bf16_bits(d[j]);
             } else {
+                float *so = reinterpret_cast<float *>(base + OFF_VT);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int r = hw * 32 + j;
-                    if (r < L) qhat[(static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) * KD + c_lane] = d[j];
-                }
+                for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = d[j];
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -542,6 +559,24 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             fence_before();
             fence_async_smem();
             __syncthreads();
+            if (kind == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
+                    if (r < L)
+                        *reinterpret_cast<uint4 *>(o + (static_cast<size_t>(t0 + r) * H + h) * VD + c16 * 8) =
+                            *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 256 + c16 * 16);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int id = tid + 256 * i, r = id >> 5, c32 = id & 31;
+                    if (r < L)
+                        *reinterpret_cast<uint4 *>(qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) * KD +
+                                                   c32 * 4) =
+                            *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 512 + c32 * 16);
+                }
+            }
             if (s_abort) aborted = true;
         }
     }
