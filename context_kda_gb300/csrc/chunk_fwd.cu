@@ -31,6 +31,9 @@
 // term.  The 64 x 64 unit-triangular inverse is solved on the CUDA cores in
 // FP32 (16 x 16 blocks).  Each chunk's raw rows are staged in shared memory
 // by bulk asynchronous copies issued while the previous chunk finishes.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -54,16 +57,16 @@ constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
 constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
 constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
 constexpr uint32_t T128 = 32768, T64 = 16384;
 constexpr uint32_t OFF_M32 = OFF_KH, OFF_T32 = OFF_KH + 16384;
 constexpr uint32_t OFF_TP = OFF_VT + 16384;          // T' hi | lo (8192 each)
 constexpr uint32_t OFF_QKL = OFF_KQ + T128 + 1024;   // masked QK (bf16) in the Qt rows of the lo tile
 constexpr uint32_t OFF_QT_HI = OFF_KQ + 1024;        // Qt rows of the hi tile
-// raw rows of the next chunk (bulk copies): q, k, v (bf16, 256 B/row) and g (fp32, 512 B/row); each
-// row pitch is padded by 16 B so that reading one 8-column piece of consecutive rows is conflict-free
-constexpr uint32_t PITCH_B = 272, PITCH_G = 528;
-constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 64 * PITCH_B, STG_V = OFF_KQ + 128 * PITCH_B;
-constexpr uint32_t STG_G = OFF_KH;   // 64 * 528 bytes: spills from the Kh region into the Kb region
+// Raw rows of the next chunk, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of
+// 64 rows x 128 bytes): q, k, v as two 64-column boxes each, g as four 32-column boxes.
+constexpr uint32_t BOX = 8192;
+constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 * BOX, STG_G = OFF_KH;
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols), later O^T
@@ -109,15 +112,17 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                  const float *__restrict__ g, const float *__restrict__ beta,
                  const float *__restrict__ h0, float scale, uint16_t *__restrict__ o,
                  float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
-                 float *__restrict__ qhat, float *__restrict__ afin)
+                 float *__restrict__ qhat, float *__restrict__ afin,
+                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g)
 {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ __align__(8) uint64_t s_ldbar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    unsigned char *const base = smem;
-    const uint32_t sbase = smem_u32(smem);
+    unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(base);
     float *const s_beta = reinterpret_cast<float *>(base + OFF_BETA);
     float *const s_gc = reinterpret_cast<float *>(base + OFF_GC);
     float *const s_gsum = reinterpret_cast<float *>(base + OFF_GSUM);
@@ -156,23 +161,25 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         fence_after();
     };
 
-    // Stage the raw rows of chunk cn (q, k, g, and v for state columns) with one bulk copy
-    // per row and thread; beta of that chunk goes to a register.  Called by all threads.
+    // Stage the raw rows of chunk cn (q, k, g, and v for state columns) with tiled TMA copies
+    // issued by one thread; rows past the end of the tensor arrive as zeros, rows past the
+    // piece are masked when read.  beta of that chunk goes to a register.
     uint32_t ld_phase = 0;
     bool loads_pending = false;
     float beta_next = 0.f;
     auto issue_loads = [&](int cn) {
         const int t0n = start + cn * CH;
         const int Ln = min(CH, len - cn * CH);
-        if (tid == 0) mbar_arrive_expect_tx(ldbar, static_cast<uint32_t>(Ln) * (kind == 0 ? 1280u : 1024u));
-        __syncthreads();
-        const int arr = tid >> 6, r = tid & 63;
-        if (r < Ln && (arr != 2 || kind == 0)) {
-            const size_t row = static_cast<size_t>(t0n + r) * H + h;
-            if (arr == 0) bulk_g2s(sbase + STG_Q + r * PITCH_B, q + row * KD, 256, ldbar);
-            else if (arr == 1) bulk_g2s(sbase + STG_K + r * PITCH_B, k + row * KD, 256, ldbar);
-            else if (arr == 2) bulk_g2s(sbase + STG_V + r * PITCH_B, v + row * VD, 256, ldbar);
-            else bulk_g2s(sbase + STG_G + r * PITCH_G, g + row * KD, 512, ldbar);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(ldbar, (kind == 0 ? 6u : 4u) * BOX + 4u * BOX);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tma_load_3d(sbase + STG_Q + half * BOX, &tm_q, half * 64, h, t0n, ldbar);
+                tma_load_3d(sbase + STG_K + half * BOX, &tm_k, half * 64, h, t0n, ldbar);
+                if (kind == 0) tma_load_3d(sbase + STG_V + half * BOX, &tm_v, half * 64, h, t0n, ldbar);
+            }
+#pragma unroll
+            for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0n, ldbar);
         }
         if (tid < 64) beta_next = (tid < Ln) ? beta[static_cast<size_t>(t0n + tid) * H + h] : 0.f;
         loads_pending = true;
@@ -214,26 +221,27 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             ++ld_phase;
             loads_pending = false;
             // A1: log2-scaled cumulative decay per key channel, in place over the staged g
+            //     (32 rows per thread: load all, scan in registers, store once)
             {
                 const int kc = tid & 127, hr = tid >> 7;
-                float *sg = reinterpret_cast<float *>(base + STG_G);
+                unsigned char *gq = base + STG_G + (kc >> 5) * BOX + (kc & 3) * 4;
+                const int gch = (kc & 31) >> 2;
+                float gv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gv[j] = *reinterpret_cast<const float *>(gq + sw128(hr * 32 + j, gch));
                 float acc = 0.f;
-#pragma unroll 8
+#pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int r = hr * 32 + j;
-                    acc += (r < L) ? sg[r * (PITCH_G / 4) + kc] * LOG2E : 0.f;
-                    sg[r * (PITCH_G / 4) + kc] = acc;
+                    acc += (hr * 32 + j < L) ? gv[j] * LOG2E : 0.f;
+                    gv[j] = acc;
                 }
                 s_gsum[hr * 128 + kc] = acc;
                 if (tid < 64) s_beta[tid] = beta_next;
                 __syncthreads();
-                if (hr) {
-                    const float off = s_gsum[kc];
-#pragma unroll 8
-                    for (int j = 0; j < 32; ++j) sg[(32 + j) * (PITCH_G / 4) + kc] += off;
-                } else {
-                    s_gc[kc] = exp2f(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
-                }
+                const float off = hr ? s_gsum[kc] : 0.f;
+                if (hr == 0) s_gc[kc] = exp2f(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
                 __syncthreads();
             }
             // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
@@ -244,15 +252,18 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = pr, c8 = (pcg + 4 * i) * 8;
-                const float4 *g4 = reinterpret_cast<const float4 *>(base + STG_G + r * PITCH_G + c8 * 4);
-                const float4 a = g4[0], b = g4[1];
+                const unsigned char *gb = base + STG_G + (c8 >> 5) * BOX;
+                const int gch = (c8 & 31) >> 2;
+                const float4 a = *reinterpret_cast<const float4 *>(gb + sw128(r, gch));
+                const float4 b = *reinterpret_cast<const float4 *>(gb + sw128(r, gch + 1));
                 gam[i][0] = a.x; gam[i][1] = a.y; gam[i][2] = a.z; gam[i][3] = a.w;
                 gam[i][4] = b.x; gam[i][5] = b.y; gam[i][6] = b.z; gam[i][7] = b.w;
                 const bool ok = r < L;
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                kw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_K + r * PITCH_B + c8 * 2) : z;
-                qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + r * PITCH_B + c8 * 2) : z;
-                vw[i] = (ok && kind == 0) ? *reinterpret_cast<const uint4 *>(base + STG_V + r * PITCH_B + c8 * 2) : z;
+                const uint32_t bo = (c8 >> 6) * BOX + sw128(r, (c8 & 63) >> 3);
+                kw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_K + bo) : z;
+                qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + bo) : z;
+                vw[i] = (ok && kind == 0) ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
             }
             __syncthreads();   // staging consumed: every region may be rewritten from here
             // A3: Kt, Qt (stacked), Kh, Kb as bf16 hi/lo and V as bf16, one row piece at a time
@@ -622,6 +633,39 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 
 }  // namespace
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [T][H][128] tensor as a 3-D map (inner dim first) with a box of 'inner' x 1 x 64 rows.
+bool encode_rows(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
+                 uint32_t inner)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {128ull * elem, 128ull * elem * static_cast<cuuint64_t>(H)};
+    const cuuint32_t box[3] = {inner, 1, 64};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_dev, int H,
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const float *g, const float *beta, const float *h0, float scale,
@@ -629,14 +673,21 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
                                  float *qhat, float *afin, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
-    cudaError_t err = cudaFuncSetAttribute(chunk_forward_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_BYTES));
-    if (err != cudaSuccess) return err;
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    chunk_forward_tc<<<static_cast<unsigned>(blocks), 256, SMEM_BYTES, stream>>>(
-        plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B, final_state, qhat, afin);
+    CUtensorMap tq, tk, tv, tg;
+    const int T = pv.T();
+    if (!encode_rows(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
+        !encode_rows(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
+        !encode_rows(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
+        !encode_rows(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, 32))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(chunk_forward_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(SMEM_ALLOC));
+    if (err != cudaSuccess) return err;
+    chunk_forward_tc<<<static_cast<unsigned>(blocks), 256, SMEM_ALLOC, stream>>>(
+        plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B, final_state, qhat, afin, tq, tk, tv, tg);
     return cudaGetLastError();
 }
 

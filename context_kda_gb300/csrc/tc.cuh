@@ -100,6 +100,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void *src, uin
         : "memory");
 }
 
+// Tiled (tensor-map) TMA load of one 3-D box at coordinates (x, y, z) into shared memory,
+// completing its byte count on the mbarrier.  x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void *tmap, int x, int y, int z, uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst_smem), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
+// Byte offset of the 16-byte chunk 'ch' of row 'r' in a box whose rows are 128 bytes and which
+// was written with the 128-byte swizzle (chunk index XOR row mod 8, box 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(int r, int ch) { return static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4)); }
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
