@@ -69,9 +69,10 @@ constexpr uint32_t BOX = 8192;
 constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 * BOX, STG_G = OFF_KH;
 
 // ---- TMEM columns --------------------------------------------------------------------------
-constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols), later O^T
+constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols)
 constexpr uint32_t TM_W = 64;     // W^T
 constexpr uint32_t TM_U = 128;    // Ut^T, then U^T
+constexpr uint32_t TM_O = 192;    // O^T (64 cols)
 constexpr uint32_t TM_X = 256;    // X^T (128 cols)
 constexpr uint32_t TM_COLS = 512;
 
@@ -306,7 +307,22 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
                              sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
+            // O^T = X^T Qt^T (1-term): needs only the chunk-start state and Qt
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), id, kk != 0);
             commit(mbar);
+        }
+        // while the tensor core works: X^T *= exp(Gamma_C) in TMEM (the MMAs read X from smem)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int k0 = hw * 64 + half * 32;
+            float x[32];
+            tmem_ld32(tl + TM_X + k0, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];
+            tmem_st32(tl + TM_X + k0, x);
         }
         wait_mma();
 
@@ -423,11 +439,19 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             }
             // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
             {
-                const int r = tid & 63, i0 = (tid >> 6) * 16;
+                // lanes: 8 consecutive rows x four 16-column groups (conflict-free row-piece reads)
+                const int r = ((tid >> 5) << 3) | (tid & 7), i0 = ((tid >> 3) & 3) * 16;
                 float tv[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    tv[j] = (i0 + j <= r) ? *f32_at(base, OFF_T32, r, i0 + j) * s_beta[i0 + j] : 0.f;
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
+                    const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = i0 + 4 * m4 + e;
+                        tv[4 * m4 + e] = (i <= r) ? tt[e] * s_beta[i] : 0.f;
+                    }
+                }
                 st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
                 st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),
                           tv + 8);
@@ -460,7 +484,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         }
         wait_mma();
 
-        // ================= F: -W as an MN-major operand (rows k, cols r); X^T *= exp(Gamma_C) ===
+        // ================= F: -W as an MN-major operand (rows k, cols r) ============================
         {
             float d[32];
             tmem_ld32(tl + TM_W + hw * 32, d);   // W^T[k = c_lane][r = hw*32 + j]
@@ -471,15 +495,6 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
                 st_split8(base + OFF_KH + off, base + OFF_KH + T64 + off, d + 8 * m);
             }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int k0 = hw * 64 + half * 32;
-                float x[32];
-                tmem_ld32(tl + TM_X + k0, x);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];
-                tmem_st32(tl + TM_X + k0, x);
-            }
             fence_before();
             fence_async_smem();
             __syncthreads();
@@ -487,10 +502,10 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         }
         if (aborted) break;
 
-        // ================= G: U^T = Ut^T - X^T W^T (3-term); O^T = X^T Qt^T (1-term) ==========
+        // ================= G: U^T = Ut^T - X^T W^T (3-term) =========================================
         if (tid == 0) {
             fence_after();
-            const uint32_t idw = idesc_bf16(128, 64, 0, 1), idq = idesc_bf16(128, 64);
+            const uint32_t idw = idesc_bf16(128, 64, 0, 1);
             const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
 #pragma unroll
             for (int ps = 0; ps < 3; ++ps)
@@ -499,10 +514,6 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     mma_bf16(tbase + TM_U, sdesc(sbase + OFF_XT + aoff[ps] + kk * 2 * 2048, 2048),
                              sdesc(sbase + OFF_KH + boff[ps] + kk * 256, 128, 2048), idw,
                              (kind == 0) || ((ps | kk) != 0));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
-                         sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), idq, kk != 0);
             commit(mbar);
         }
         wait_mma();
@@ -529,7 +540,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_VT + kk * 2 * 2048, 2048),
+                mma_bf16(tbase + TM_O, sdesc(sbase + OFF_VT + kk * 2 * 2048, 2048),
                          sdesc(sbase + OFF_QKL + kk * 2 * 2048, 2048), id64, 1);
             const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, T64, 0};
 #pragma unroll
@@ -547,7 +558,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         {
             // O^T[c][r] -> row-major O tile in the free V/U region, then 16-byte coalesced stores
             float d[32];
-            tmem_ld32(tl + TM_D1 + hw * 32, d);   // O^T[c][r = hw*32 + j]
+            tmem_ld32(tl + TM_O + hw * 32, d);    // O^T[c][r = hw*32 + j]
             if (kind == 0) {
                 uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_VT);
 #pragma unroll
