@@ -236,6 +236,14 @@ def run_ours(args, w, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local_rank) as clk:
+        # the timed region is short, so clocks are sampled over a ~1 s soak of identical
+        # (untimed) steps right before it as well as during it
+        soak0 = time.perf_counter()
+        while time.perf_counter() - soak0 < args.clock_soak_s:
+            for _ in range(8):
+                flush.fill_(1)
+                step()
+            torch.cuda.synchronize(dev)
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(1)
@@ -310,7 +318,7 @@ def run_ours(args, w, rank, world, local_rank):
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window=f"{args.clock_soak_s:g} s soak of identical steps + timed region"),
         "wall_s_timed_region": wall,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -326,6 +334,7 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(workloads().keys()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-soak-s", type=float, default=1.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     rank = int(os.environ.get("RANK", "0"))
