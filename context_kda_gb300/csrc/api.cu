@@ -5,6 +5,7 @@
 // fallback path (cuLA PR #110, "feat(cp): add opt-in NVSHMEM CP state handoff",
 // §Supported configuration: request an error instead of fallback).
 #include <cstdint>
+#include <mutex>
 
 #include "kda_internal.cuh"
 
@@ -97,6 +98,47 @@ extern "C" int kda_last_cuda_error(void) { return g_last_cuda_error; }
 
 namespace kda {
 void record_cuda_error(int err) { g_last_cuda_error = err; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows)
+{
+    auto fn = tmap_encode_fn();
+    if (!fn || rows == 0) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {128ull * 4};
+    const cuuint32_t box[2] = {32, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
 }  // namespace kda
 
 extern "C" int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6])

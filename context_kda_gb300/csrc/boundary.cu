@@ -291,19 +291,6 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-int sm_count()
-{
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
-
 }  // namespace
 
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,

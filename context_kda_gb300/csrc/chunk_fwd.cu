@@ -30,10 +30,7 @@
 // summaries stay within 1e-4; the output-only ones (Qt X, masked QK U) use one
 // term.  The 64 x 64 unit-triangular inverse is solved on the CUDA cores in
 // FP32 (16 x 16 blocks).  Each chunk's raw rows are staged in shared memory
-// by bulk asynchronous copies issued while the previous chunk finishes.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+// by tiled TMA loads (128-byte swizzle) issued while the previous chunk finishes.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -646,25 +643,11 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // [T][H][128] tensor as a 3-D map (inner dim first) with a box of 'inner' x 1 x 64 rows.
 bool encode_rows(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
                  uint32_t inner)
 {
-    auto fn = encode_fn();
+    auto fn = tmap_encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     const cuuint64_t strides[2] = {128ull * elem, 128ull * elem * static_cast<cuuint64_t>(H)};

@@ -7,86 +7,250 @@
 //     S_in[0] = h0[first sequence],
 //     S_in[j] = h0[s]                            if sequence s starts at b_j,
 //             = B[j-1]                           if a sequence starts inside j-1,
-//             = A[j-1] S_in[j-1] + B[j-1]        otherwise.
-// The value columns are independent, so each CTA carries a 128 x 16 column
-// slice of one head's state through all segments (FP32 CUDA cores).
+//             = A[j-1] S_in[j-1] + B[j-1]        otherwise (a "step").
+// The value columns are independent, so each CTA carries a 32-column slice of
+// one head's state through all segments.  A step is one tcgen05 product
+// D = A[j-1] S_in[j-1] (M = 128 rows, N = 32, K = 128) with both operands split
+// into bf16 hi/lo and three products accumulated in FP32 in TMEM.
+//
+// All global traffic is tiled TMA with the 128-byte swizzle: each transition
+// arrives one step ahead and is split while the previous step's MMA runs; the
+// B (or h0) slice a step adds arrives in a 16 KiB buffer where the epilogue
+// forms S_in[j] in place, and one TMA store writes it out.  Thread 0 issues the
+// MMAs and the transition loads; thread 32 owns the slice loads and stores, so
+// neither waits on the other's copies.
 #include "kda_internal.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int NCOL = 16;        // value columns per CTA
-constexpr int LDS_A = KD + 4;   // padded row stride of the staged transition
+using namespace tc;
 
-__global__ void __launch_bounds__(256)
-compose_v0(const int32_t *__restrict__ plan, int H, const float *__restrict__ A,
-           const float *__restrict__ B, const float *__restrict__ h0, float *__restrict__ S_in)
+constexpr int NS = 32;                     // value columns per CTA
+constexpr int NC = NS / 2;                 // columns per epilogue thread
+constexpr uint32_t LBO_A = 2048;           // transition operand (rows r, cols k), K-major
+constexpr uint32_t TILE_A = 16 * LBO_A;
+constexpr uint32_t CS_S = 2048;            // state operand (rows k, cols c), read MN-major
+constexpr uint32_t SOP = NS / 8 * CS_S;
+constexpr uint32_t OFF_AOP = 0;                       // two buffers, each hi | lo
+constexpr uint32_t OFF_SOP = OFF_AOP + 4 * TILE_A;    // hi | lo
+constexpr uint32_t OFF_STG = OFF_SOP + 2 * SOP;       // fp32 transition, 4 swizzled boxes of 32 columns
+constexpr uint32_t OFF_BS = OFF_STG + 65536;          // fp32 slice, one swizzled box (B / h0 in, S_in out)
+constexpr uint32_t SMEM_BYTES = OFF_BS + 16384;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;    // room to align the base to 1024 bytes
+constexpr uint32_t TM_COLS = 32;
+
+__device__ int g_compose_status;
+
+enum { IN_SEED = 0, IN_UPDATE = 1, IN_STEP = 2 };
+
+__device__ __forceinline__ int in_kind(const PlanView &pv, int j)
 {
-    extern __shared__ float4 smem_raw[];
-    float *sA = reinterpret_cast<float *>(smem_raw);   // [KD][LDS_A]
-    float *sS = sA + KD * LDS_A;                        // [KD][NCOL]
-    const PlanView pv{plan};
-    const int tid = threadIdx.x;
-    const int ncb = VD / NCOL;
-    const int h = blockIdx.x / ncb, cb = blockIdx.x % ncb;
-    const int col0 = cb * NCOL;
+    if (j == 0 || (pv.seg(j)[1] & KDA_SEG_STARTS_SEQ)) return IN_SEED;
+    return (pv.seg(j - 1)[1] & KDA_SEG_HAS_RESET) ? IN_UPDATE : IN_STEP;
+}
+
+// First segment >= j whose incoming state is a step (S if none).
+__device__ __forceinline__ int next_step(const PlanView &pv, int j)
+{
     const int S = pv.S();
-    const size_t mat = static_cast<size_t>(KD) * VD;
-    // this thread's outputs: rows rg + 32 m (m < 4), columns 2 cp, 2 cp + 1
-    const int cp = tid & 7, rg = tid >> 3;
+    while (j < S && in_kind(pv, j) != IN_STEP) ++j;
+    return j;
+}
+
+__global__ void __launch_bounds__(256, 1)
+compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_constant__ CUtensorMap tm_A,
+           const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_h0,
+           const __grid_constant__ CUtensorMap tm_S)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t s_mbar, s_abar, s_bbar;
+    __shared__ uint32_t s_tmem;
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const PlanView pv{plan};
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int nsl = VD / NS;
+    const int h = blockIdx.x / nsl, col0 = (blockIdx.x % nsl) * NS;
+    const int S = pv.S();
+    const int r = quad * 32 + lane;   // state row held by this thread in the epilogue
+    const int cl = half * NC;         // its first column within the slice
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t mbar = smem_u32(&s_mbar), abar = smem_u32(&s_abar), bbar = smem_u32(&s_bbar);
+    const bool io = tid == 32;        // slice loads and stores
+
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_init(abar, 1);
+        mbar_init(bbar, 1);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tbase = s_tmem;
+    uint32_t a_phase = 0, b_phase = 0, mma_phase = 0;
+    bool ok = true, a_pending = false, b_pending = false;
+    int n_conv = 0, n_mma = 0;   // transitions split so far / steps issued so far
+
+    auto needs_vals = [&](int j) { return in_kind(pv, j) != IN_SEED || has_h0; };
+    auto fetch_A = [&](int step) {   // thread 0: transition of segment step-1, four 32-column boxes
+        const int y = ((step - 1) * H + h) * KD;
+        mbar_arrive_expect_tx(abar, 65536u);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tma_load_2d(sbase + OFF_STG + b * 16384, &tm_A, 32 * b, y, abar);
+    };
+    auto fetch_vals = [&](int j) {   // thread 32: the slice segment j's incoming state starts from
+        mbar_arrive_expect_tx(bbar, 16384u);
+        if (in_kind(pv, j) == IN_SEED)
+            tma_load_2d(sbase + OFF_BS, &tm_h0, col0, (pv.seg(j)[0] * H + h) * KD, bbar);
+        else
+            tma_load_2d(sbase + OFF_BS, &tm_B, col0, ((j - 1) * H + h) * KD, bbar);
+    };
+    // staged transition -> operand buffer b (rows r, cols k) as bf16 hi | lo; lanes take consecutive rows
+    auto convert_A = [&](int b) {
+        ok &= mbar_wait(abar, a_phase++ & 1);
+        a_pending = false;
+        const uint32_t base = OFF_AOP + static_cast<uint32_t>(b) * 2 * TILE_A;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int id = tid + 256 * i, rr = id & 127, kc = id >> 7;   // 8-column chunk kc of row rr
+            const unsigned char *box = smem + OFF_STG + (kc >> 2) * 16384;
+            const float4 x0 = *reinterpret_cast<const float4 *>(box + sw128(rr, (kc & 3) * 2));
+            const float4 x1 = *reinterpret_cast<const float4 *>(box + sw128(rr, (kc & 3) * 2 + 1));
+            uint32_t hi[4], lo[4];
+            split_bf16x2(x0.x, x0.y, hi[0], lo[0]);
+            split_bf16x2(x0.z, x0.w, hi[1], lo[1]);
+            split_bf16x2(x1.x, x1.y, hi[2], lo[2]);
+            split_bf16x2(x1.z, x1.w, hi[3], lo[3]);
+            const uint32_t off = cm_off(rr, kc * 8, LBO_A);
+            *reinterpret_cast<uint4 *>(smem + base + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(smem + base + TILE_A + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        ++n_conv;
+    };
+
+    {
+        const int s0 = next_step(pv, 1);
+        if (s0 < S) {
+            if (tid == 0) fetch_A(s0);
+            a_pending = true;
+        }
+        if (needs_vals(0)) {
+            if (io) fetch_vals(0);
+            b_pending = true;
+        }
+    }
 
     for (int j = 0; j < S; ++j) {
-        const int32_t *sg = pv.seg(j);
-        float *dst = S_in + (static_cast<size_t>(j) * H + h) * mat;
-        const bool reset = (j == 0) || (sg[1] & KDA_SEG_STARTS_SEQ);
-        if (reset) {
-            const float *src = h0 ? h0 + (static_cast<size_t>(sg[0]) * H + h) * mat : nullptr;
-            for (int e = tid; e < KD * NCOL; e += 256) {
-                const int r = e / NCOL, cc = e % NCOL;
-                sS[e] = src ? src[r * VD + col0 + cc] : 0.f;
+        const bool step = in_kind(pv, j) == IN_STEP;
+        float st[NC];
+        if (step) {
+            if (tid == 0) {
+                fence_after();
+                const uint32_t id = idesc_bf16(128, NS, 0, 1);
+                const uint32_t a_hi = sbase + OFF_AOP + static_cast<uint32_t>(n_mma & 1) * 2 * TILE_A;
+                const uint32_t s_hi = sbase + OFF_SOP;
+                const uint32_t aop[3] = {a_hi, a_hi, a_hi + TILE_A}, sop[3] = {s_hi, s_hi + SOP, s_hi};
+#pragma unroll
+                for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tbase, sdesc(aop[ps] + kk * 2 * LBO_A, LBO_A), sdesc(sop[ps] + kk * 256, 128, CS_S),
+                                 id, (ps | kk) != 0);
+                commit(mbar);
+            }
+            ++n_mma;
+            // split the next step's transition while this one runs
+            const int nxt = next_step(pv, j + 1);
+            if (nxt < S && n_conv == n_mma) {
+                convert_A(n_conv & 1);
+                fence_async_smem();
+                __syncthreads();   // staging read by all threads
+                const int nn = next_step(pv, nxt + 1);
+                if (nn < S) {
+                    if (tid == 0) fetch_A(nn);
+                    a_pending = true;
+                }
+            }
+            ok &= mbar_wait(mbar, mma_phase++ & 1);
+            fence_after();
+            float d[NC];
+            tmem_ld16(tbase + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(cl), d);
+#pragma unroll
+            for (int e = 0; e < NC; ++e) st[e] = d[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < NC; ++e) st[e] = 0.f;
+        }
+        // S_in[j] = (step ? D : 0) + (B[j-1] or h0 or 0), formed in the slice buffer
+        if (needs_vals(j)) {
+            ok &= mbar_wait(bbar, b_phase++ & 1);
+            b_pending = false;
+#pragma unroll
+            for (int m = 0; m < NC / 4; ++m) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(smem + OFF_BS + sw128(r, cl / 4 + m));
+                st[4 * m] += b4.x;
+                st[4 * m + 1] += b4.y;
+                st[4 * m + 2] += b4.z;
+                st[4 * m + 3] += b4.w;
             }
         } else {
-            const bool prev_reset = pv.seg(j - 1)[1] & KDA_SEG_HAS_RESET;
-            const float *Bp = B + (static_cast<size_t>(j - 1) * H + h) * mat;
-            if (prev_reset) {
-                for (int e = tid; e < KD * NCOL; e += 256) sS[e] = Bp[(e / NCOL) * VD + col0 + e % NCOL];
-            } else {
-                const float *Ap = A + (static_cast<size_t>(j - 1) * H + h) * KD * KD;
-                for (int e = tid; e < KD * KD / 4; e += 256) {
-                    const int r = e / (KD / 4), c4 = e % (KD / 4);
-                    const float4 a4 = reinterpret_cast<const float4 *>(Ap + r * KD)[c4];
-                    *reinterpret_cast<float4 *>(&sA[r * LDS_A + 4 * c4]) = a4;
-                }
-                __syncthreads();
-                float acc[4][2];
+            __syncthreads();   // the previous store has finished reading the buffer (thread 32 waited)
+        }
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = rg + 32 * m;
-                    acc[m][0] = Bp[r * VD + col0 + 2 * cp];
-                    acc[m][1] = Bp[r * VD + col0 + 2 * cp + 1];
-                }
-                for (int i = 0; i < KD; ++i) {
-                    const float2 s2 = *reinterpret_cast<const float2 *>(&sS[i * NCOL + 2 * cp]);
+        for (int m = 0; m < NC / 4; ++m)
+            *reinterpret_cast<float4 *>(smem + OFF_BS + sw128(r, cl / 4 + m)) =
+                make_float4(st[4 * m], st[4 * m + 1], st[4 * m + 2], st[4 * m + 3]);
+        bool fetch_after = false;
+        if (j + 1 < S && in_kind(pv, j + 1) == IN_STEP) {
+            if (n_conv == n_mma) {   // not split yet (no step ran since it was staged)
+                convert_A(n_conv & 1);
+                fetch_after = next_step(pv, j + 2) < S;
+            }
+            // S_in[j] -> state operand (rows k = r, cols c) as bf16 hi | lo
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float a = sA[(rg + 32 * m) * LDS_A + i];
-                        acc[m][0] = fmaf(a, s2.x, acc[m][0]);
-                        acc[m][1] = fmaf(a, s2.y, acc[m][1]);
-                    }
-                }
-                __syncthreads();
+            for (int m = 0; m < NC / 8; ++m) {
+                uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = rg + 32 * m;
-                    sS[r * NCOL + 2 * cp] = acc[m][0];
-                    sS[r * NCOL + 2 * cp + 1] = acc[m][1];
-                }
+                for (int p = 0; p < 4; ++p) split_bf16x2(st[8 * m + 2 * p], st[8 * m + 2 * p + 1], hi[p], lo[p]);
+                const uint32_t off = static_cast<uint32_t>((cl / 8 + m) * CS_S + (r >> 3) * 128 + (r & 7) * 16);
+                *reinterpret_cast<uint4 *>(smem + OFF_SOP + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(smem + OFF_SOP + SOP + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        __syncthreads();
-        for (int e = tid; e < KD * NCOL; e += 256) dst[(e / NCOL) * VD + col0 + e % NCOL] = sS[e];
+        fence_async_smem();
+        fence_before();
+        const bool all_ok = __syncthreads_and(ok);
+        if (io && all_ok) {
+            tma_store_2d(&tm_S, col0, (j * H + h) * KD, sbase + OFF_BS);
+            bulk_commit_group();
+            bulk_wait_read_all();   // the buffer is free again
+            if (j + 1 < S && needs_vals(j + 1)) fetch_vals(j + 1);
+        }
+        if (!all_ok) break;
+        if (j + 1 < S && needs_vals(j + 1)) b_pending = true;
+        if (fetch_after) {
+            if (tid == 0) fetch_A(next_step(pv, j + 2));
+            a_pending = true;
+        }
+    }
+    if (io) bulk_wait_all();
+    if (!__syncthreads_and(ok)) {
+        // a wait gave up: record it, and let copies and products still in flight land before the CTA exits
+        if (tid == 0) {
+            atomicExch(&g_compose_status, KDA_ERR_TIMEOUT);
+            if (a_pending) mbar_wait(abar, a_phase & 1);
+            mbar_wait(mbar, mma_phase & 1);
+        }
+        if (io && b_pending) mbar_wait(bbar, b_phase & 1);
         __syncthreads();
     }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
 }  // namespace
@@ -94,12 +258,23 @@ compose_v0(const int32_t *__restrict__ plan, int H, const float *__restrict__ A,
 cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
                            const float *B, const float *h0, float *S_in, cudaStream_t stream)
 {
-    const size_t smem = sizeof(float) * (KD * LDS_A + KD * NCOL);
-    cudaError_t err = cudaFuncSetAttribute(compose_v0, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+    const PlanView pv{plan_host};
+    const int S = pv.S();
+    if (S <= 0) return cudaSuccess;
+    const uint64_t rows = static_cast<uint64_t>(S) * H * KD;
+    CUtensorMap tA, tB, tH, tS;
+    if (!encode_f32_rows128(&tA, A, rows, KD) || !encode_f32_rows128(&tB, B, rows, KD) ||
+        !encode_f32_rows128(&tS, S_in, rows, KD))
+        return cudaErrorInvalidValue;
+    if (h0) {
+        if (!encode_f32_rows128(&tH, h0, static_cast<uint64_t>(pv.N()) * H * KD, KD)) return cudaErrorInvalidValue;
+    } else {
+        tH = tB;   // never read: no segment takes a seed from h0
+    }
+    cudaError_t err =
+        cudaFuncSetAttribute(compose_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    (void)plan_host;
-    compose_v0<<<H * (VD / NCOL), 256, smem, stream>>>(plan_dev, H, A, B, h0, S_in);
+    compose_tc<<<H * (VD / NS), 256, SMEM_ALLOC, stream>>>(plan_dev, H, h0 ? 1 : 0, tA, tB, tH, tS);
     return cudaGetLastError();
 }
 

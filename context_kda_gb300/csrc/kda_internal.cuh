@@ -1,6 +1,8 @@
 // Internal definitions shared by the libkda translation units (not installed).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -50,6 +52,16 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) { return __bfloat1
 
 // Records a cudaError_t for kda_last_cuda_error() on the calling thread.
 void record_cuda_error(int err);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
+
+// Tensor map of a row-major [rows][128] fp32 matrix with a box of 32 columns x box_rows
+// rows and the 128-byte swizzle (16-byte chunk c of box row r lands at chunk c ^ (r % 8)).
+bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_dev, int H,

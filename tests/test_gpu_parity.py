@@ -132,3 +132,13 @@ def test_closed_form_static_state_on_gpu():
             want = q[cu[s]:cu[s + 1], h] @ inp.h0[s, h].astype(np.float64)
             assert float(np.max(np.abs(res["o"][cu[s]:cu[s + 1], h] - want))) <= O_TOL
             assert rel_err(res["final"][s, h], inp.h0[s, h]) <= REL_TOL
+
+
+def test_wide_head_count_every_segment():
+    """More heads than one wave of 16-column composition slices holds (the 32-column
+    slices), with resets, continuing pieces and a random initial state: every head
+    and segment against the oracle."""
+    inp = make_inputs([300, 500, 77, 900], heads=24, segments=9, h0_std=0.1, seed=14)
+    res = gpu_forward(inp)
+    _check_outputs(res, inp)
+    _check_segments(res, inp, [(j, h) for j in range(9) for h in range(24)])
