@@ -16,9 +16,10 @@
 // All global traffic is tiled TMA with the 128-byte swizzle: each transition
 // arrives one step ahead and is split while the previous step's MMA runs; the
 // B (or h0) slice a step adds arrives in a 16 KiB buffer where the epilogue
-// forms S_in[j] in place, and one TMA store writes it out.  Thread 0 issues the
-// MMAs and the transition loads; thread 32 owns the slice loads and stores, so
-// neither waits on the other's copies.
+// forms S_in[j] in place, and one TMA store writes it out.  Eight warps split
+// operands and run the epilogue; a ninth warp issues the MMAs and the
+// transition loads, and a tenth owns the slice loads and stores, so neither
+// the split nor the copies wait on MMA issue.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -59,7 +60,10 @@ __device__ __forceinline__ int next_step(const PlanView &pv, int j)
     return j;
 }
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int NT = 320;                    // 8 worker warps + MMA warp + I/O warp
+constexpr int MMA_TID = 256, IO_TID = 288;
+
+__global__ void __launch_bounds__(NT, 1)
 compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_constant__ CUtensorMap tm_A,
            const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_h0,
            const __grid_constant__ CUtensorMap tm_S)
@@ -78,7 +82,9 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
     const int cl = half * NC;         // its first column within the slice
     const uint32_t sbase = smem_u32(smem);
     const uint32_t mbar = smem_u32(&s_mbar), abar = smem_u32(&s_abar), bbar = smem_u32(&s_bbar);
-    const bool io = tid == 32;        // slice loads and stores
+    const bool io = tid == IO_TID;           // slice loads and stores
+    const bool issuer = tid == MMA_TID;      // MMAs and transition loads
+    const bool worker = tid < 256;
 
     if (tid == 0) {
         mbar_init(mbar, 1);
@@ -95,13 +101,13 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
     int n_conv = 0, n_mma = 0;   // transitions split so far / steps issued so far
 
     auto needs_vals = [&](int j) { return in_kind(pv, j) != IN_SEED || has_h0; };
-    auto fetch_A = [&](int step) {   // thread 0: transition of segment step-1, four 32-column boxes
+    auto fetch_A = [&](int step) {   // issuer: transition of segment step-1, four 32-column boxes
         const int y = ((step - 1) * H + h) * KD;
         mbar_arrive_expect_tx(abar, 65536u);
 #pragma unroll
         for (int b = 0; b < 4; ++b) tma_load_2d(sbase + OFF_STG + b * 16384, &tm_A, 32 * b, y, abar);
     };
-    auto fetch_vals = [&](int j) {   // thread 32: the slice segment j's incoming state starts from
+    auto fetch_vals = [&](int j) {   // I/O thread: the slice segment j's incoming state starts from
         mbar_arrive_expect_tx(bbar, 16384u);
         if (in_kind(pv, j) == IN_SEED)
             tma_load_2d(sbase + OFF_BS, &tm_h0, col0, (pv.seg(j)[0] * H + h) * KD, bbar);
@@ -110,8 +116,11 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
     };
     // staged transition -> operand buffer b (rows r, cols k) as bf16 hi | lo; lanes take consecutive rows
     auto convert_A = [&](int b) {
-        ok &= mbar_wait(abar, a_phase++ & 1);
         a_pending = false;
+        ++n_conv;
+        const uint32_t par = a_phase++ & 1;   // every thread tracks the phases; workers wait
+        if (!worker) return;
+        ok &= mbar_wait(abar, par);
         const uint32_t base = OFF_AOP + static_cast<uint32_t>(b) * 2 * TILE_A;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -128,13 +137,12 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
             *reinterpret_cast<uint4 *>(smem + base + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4 *>(smem + base + TILE_A + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        ++n_conv;
     };
 
     {
         const int s0 = next_step(pv, 1);
         if (s0 < S) {
-            if (tid == 0) fetch_A(s0);
+            if (issuer) fetch_A(s0);
             a_pending = true;
         }
         if (needs_vals(0)) {
@@ -147,7 +155,7 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
         const bool step = in_kind(pv, j) == IN_STEP;
         float st[NC];
         if (step) {
-            if (tid == 0) {
+            if (issuer) {
                 fence_after();
                 const uint32_t id = idesc_bf16(128, NS, 0, 1);
                 const uint32_t a_hi = sbase + OFF_AOP + static_cast<uint32_t>(n_mma & 1) * 2 * TILE_A;
@@ -170,26 +178,30 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
                 __syncthreads();   // staging read by all threads
                 const int nn = next_step(pv, nxt + 1);
                 if (nn < S) {
-                    if (tid == 0) fetch_A(nn);
+                    if (issuer) fetch_A(nn);
                     a_pending = true;
                 }
             }
-            ok &= mbar_wait(mbar, mma_phase++ & 1);
-            fence_after();
-            float d[NC];
-            tmem_ld16(tbase + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(cl), d);
+            const uint32_t par = mma_phase++ & 1;
+            if (worker) {
+                ok &= mbar_wait(mbar, par);
+                fence_after();
+                float d[NC];
+                tmem_ld16(tbase + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(cl), d);
 #pragma unroll
-            for (int e = 0; e < NC; ++e) st[e] = d[e];
+                for (int e = 0; e < NC; ++e) st[e] = d[e];
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < NC; ++e) st[e] = 0.f;
         }
         // S_in[j] = (step ? D : 0) + (B[j-1] or h0 or 0), formed in the slice buffer
         if (needs_vals(j)) {
-            ok &= mbar_wait(bbar, b_phase++ & 1);
             b_pending = false;
+            const uint32_t par = b_phase++ & 1;
+            if (worker) ok &= mbar_wait(bbar, par);
 #pragma unroll
-            for (int m = 0; m < NC / 4; ++m) {
+            for (int m = 0; m < NC / 4 && worker; ++m) {
                 const float4 b4 = *reinterpret_cast<const float4 *>(smem + OFF_BS + sw128(r, cl / 4 + m));
                 st[4 * m] += b4.x;
                 st[4 * m + 1] += b4.y;
@@ -197,12 +209,14 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
                 st[4 * m + 3] += b4.w;
             }
         } else {
-            __syncthreads();   // the previous store has finished reading the buffer (thread 32 waited)
+            __syncthreads();   // the previous store has finished reading the buffer (the I/O thread waited)
         }
+        if (worker) {
 #pragma unroll
-        for (int m = 0; m < NC / 4; ++m)
-            *reinterpret_cast<float4 *>(smem + OFF_BS + sw128(r, cl / 4 + m)) =
-                make_float4(st[4 * m], st[4 * m + 1], st[4 * m + 2], st[4 * m + 3]);
+            for (int m = 0; m < NC / 4; ++m)
+                *reinterpret_cast<float4 *>(smem + OFF_BS + sw128(r, cl / 4 + m)) =
+                    make_float4(st[4 * m], st[4 * m + 1], st[4 * m + 2], st[4 * m + 3]);
+        }
         bool fetch_after = false;
         if (j + 1 < S && in_kind(pv, j + 1) == IN_STEP) {
             if (n_conv == n_mma) {   // not split yet (no step ran since it was staged)
@@ -211,7 +225,7 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
             }
             // S_in[j] -> state operand (rows k = r, cols c) as bf16 hi | lo
 #pragma unroll
-            for (int m = 0; m < NC / 8; ++m) {
+            for (int m = 0; m < NC / 8 && worker; ++m) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) split_bf16x2(st[8 * m + 2 * p], st[8 * m + 2 * p + 1], hi[p], lo[p]);
@@ -232,14 +246,14 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
         if (!all_ok) break;
         if (j + 1 < S && needs_vals(j + 1)) b_pending = true;
         if (fetch_after) {
-            if (tid == 0) fetch_A(next_step(pv, j + 2));
+            if (issuer) fetch_A(next_step(pv, j + 2));
             a_pending = true;
         }
     }
     if (io) bulk_wait_all();
     if (!__syncthreads_and(ok)) {
         // a wait gave up: record it, and let copies and products still in flight land before the CTA exits
-        if (tid == 0) {
+        if (issuer) {
             atomicExch(&g_compose_status, KDA_ERR_TIMEOUT);
             if (a_pending) mbar_wait(abar, a_phase & 1);
             mbar_wait(mbar, mma_phase & 1);
@@ -274,7 +288,7 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
     cudaError_t err =
         cudaFuncSetAttribute(compose_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    compose_tc<<<H * (VD / NS), 256, SMEM_ALLOC, stream>>>(plan_dev, H, h0 ? 1 : 0, tA, tB, tH, tS);
+    compose_tc<<<H * (VD / NS), NT, SMEM_ALLOC, stream>>>(plan_dev, H, h0 ? 1 : 0, tA, tB, tH, tS);
     return cudaGetLastError();
 }
 
