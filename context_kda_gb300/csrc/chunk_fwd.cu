@@ -6,8 +6,8 @@
 //   kt_r = exp(Gamma_r) k_r, kh_i = exp(-Gamma_i) k_i, kb_i = exp(Gamma_C - Gamma_i) k_i,
 //   qt_r = scale exp(Gamma_r) q_r,
 //   M[r,i] = beta_r (kt_r . kh_i) for i < r,   T' = (I + M)^-1 Diag(beta),
-//   W = T' Kt,   Ut = T' V,
-//   U = Ut - W X,   O = Qt X + ((Qt Kh^T) masked to i <= r) U,
+//   Ut = T' V,   U = Ut - T' (Kt X)   (= Ut - W X with W = T' Kt),
+//   O = Qt X + ((Qt Kh^T) masked to i <= r) U,
 //   X' = Diag(exp Gamma_C) X + Kb^T U.
 // This is the KDA gated delta rule (cuLA PR #110, "feat(cp): add opt-in NVSHMEM
 // CP state handoff", §Supported configuration: BF16 inputs, FP32 state) unrolled
@@ -25,11 +25,12 @@
 // FP32 accumulation in TMEM).  Operand tiles are written row by row with
 // 16-byte stores; the transposed operands (Kt^T, Kb^T, V^T, W) are the same
 // row-major tiles read MN-major.  The contractions that feed the state and the
-// summaries (Kt Kh^T, W, Ut, W X, Kb^T U) use a three-term bf16 split
+// summaries (Kt Kh^T, Kt X, Ut, T' (Kt X), Kb^T U) use a three-term bf16 split
 // (hi*hi + hi*lo + lo*hi, ~2^-17 relative per product) so the FP32 state and
 // summaries stay within 1e-4; the output-only ones (Qt X, masked QK U) use one
 // term.  The 64 x 64 unit-triangular inverse is solved on the CUDA cores in
-// FP32 (16 x 16 blocks).  Each chunk's raw rows are staged in shared memory
+// FP32 (16 x 16 blocks) while the tensor core forms Qt X and Kt X from the
+// chunk-start state.  Each chunk's raw rows are staged in shared memory
 // by tiled TMA loads (128-byte swizzle) issued while the previous chunk finishes.
 #include "kda_internal.cuh"
 #include "tc.cuh"
@@ -44,8 +45,8 @@ using namespace tc;
 constexpr uint32_t OFF_XT = 0;        // X^T: rows c (128), cols k (128), CS 2048           2 x 32768
 constexpr uint32_t OFF_KQ = 65536;    // [Kt; Qt]: rows r / 64 + r, cols k, CS 2048          2 x 32768
 constexpr uint32_t OFF_KH = 131072;   // Kh: rows i (64), cols k, CS 1024                    2 x 16384
-//   then M (fp32 64 x 64) + T (fp32 64 x 64, at +16384); then -W read MN-major:
-//   rows k (128), cols r (64), CS 2048                                                   2 x 16384
+//   then M (fp32 64 x 64) + T (fp32 64 x 64, at +16384); then -(Kt X)^T:
+//   rows c (128), cols i (64), CS 2048                                                   2 x 16384
 constexpr uint32_t OFF_KB = 163840;   // Kb: rows r (64), cols k, CS 1024                    2 x 16384
 constexpr uint32_t OFF_VT = 196608;   // V: rows r (64), cols v, CS 1024 (16384) + T': rows r, cols i,
 //   CS 1024 (2 x 8192 at +16384); then U^T: rows c (128), cols r (64), CS 2048          2 x 16384
@@ -67,7 +68,7 @@ constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols)
-constexpr uint32_t TM_W = 64;     // W^T
+constexpr uint32_t TM_KX = 64;    // (Kt X)^T
 constexpr uint32_t TM_U = 128;    // Ut^T, then U^T
 constexpr uint32_t TM_O = 192;    // O^T (64 cols)
 constexpr uint32_t TM_X = 256;    // X^T (128 cols)
@@ -117,6 +118,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ __align__(8) uint64_t s_ldbar;
+    __shared__ __align__(8) uint64_t s_mbar2;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -137,10 +139,12 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     const int64_t T_cont = pv.T_cont();
     const uint32_t mbar = smem_u32(&s_mbar);
     const uint32_t ldbar = smem_u32(&s_ldbar);
+    const uint32_t mbar2 = smem_u32(&s_mbar2);   // the state products issued with [KK; QK]
 
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(ldbar, 1);
+        mbar_init(mbar2, 1);
         s_abort = 0;
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
@@ -150,7 +154,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     const uint32_t tbase = s_tmem;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
     const int c_lane = quad * 32 + lane;                                     // state column of this thread
-    uint32_t phase = 0;
+    uint32_t phase = 0, phase2 = 0;
     bool aborted = false;
 
     auto wait_mma = [&]() {
@@ -304,12 +308,21 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
                              sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
-            // O^T = X^T Qt^T (1-term): needs only the chunk-start state and Qt
+            commit(mbar);
+            // O^T = X^T Qt^T (1-term) and (Kt X)^T = X^T Kt^T (3-term): need only the chunk-start
+            // state and the decayed rows; they run while the inverse is solved
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
                          sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), id, kk != 0);
-            commit(mbar);
+            const uint32_t xoff[3] = {0, 0, T128}, toff[3] = {0, T128, 0};
+#pragma unroll
+            for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + xoff[ps] + kk * 2 * 2048, 2048),
+                             sdesc(sbase + OFF_KQ + toff[ps] + kk * 2 * 2048, 2048), id, (ps | kk) != 0);
+            commit(mbar2);
         }
         // while the tensor core works: X^T *= exp(Gamma_C) in TMEM (the MMAs read X from smem)
 #pragma unroll
@@ -457,34 +470,24 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             __syncthreads();
         }
 
-        // ================= E: W^T = Kt^T T'^T (3-term); Ut^T = V^T T'^T (2-term) =============
-        // Kt^T and V^T are the row-major Kt / V tiles read MN-major.
-        if (tid == 0) {
+        // ================= E: U^T = Ut^T - (Kt X)^T T'^T; Ut^T = V^T T'^T (2-term, V^T the row-major
+        //                     V tile read MN-major), the product term 3-term from -(Kt X)^T in smem
+        if (tid == 0 && kind == 0) {
             fence_after();
             const uint32_t id = idesc_bf16(128, 64, 1, 0);
-            const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, 8192, 0};
 #pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
+            for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_W, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 256, 128, 2048),
-                             sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
-            if (kind == 0) {
-#pragma unroll
-                for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tbase + TM_U, sdesc(sbase + OFF_VT + kk * 256, 128, 1024),
-                                 sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
-            }
-            commit(mbar);
+                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_VT + kk * 256, 128, 1024),
+                             sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
         }
-        wait_mma();
-
-        // ================= F: -W as an MN-major operand (rows k, cols r) ============================
         {
+            if (!mbar_wait(mbar2, phase2 & 1)) s_abort = 1;
+            ++phase2;
+            fence_after();
             float d[32];
-            tmem_ld32(tl + TM_W + hw * 32, d);   // W^T[k = c_lane][r = hw*32 + j]
+            tmem_ld32(tl + TM_KX + hw * 32, d);   // (Kt X)^T[c = c_lane][i = hw*32 + j]
 #pragma unroll
             for (int j = 0; j < 32; ++j) d[j] = -d[j];
 #pragma unroll
@@ -498,18 +501,16 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             if (s_abort) aborted = true;
         }
         if (aborted) break;
-
-        // ================= G: U^T = Ut^T - X^T W^T (3-term) =========================================
         if (tid == 0) {
             fence_after();
-            const uint32_t idw = idesc_bf16(128, 64, 0, 1);
-            const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
+            const uint32_t id = idesc_bf16(128, 64);
+            const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, 8192, 0};
 #pragma unroll
             for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_XT + aoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_KH + boff[ps] + kk * 256, 128, 2048), idw,
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_KH + aoff[ps] + kk * 2 * 2048, 2048),
+                             sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id,
                              (kind == 0) || ((ps | kk) != 0));
             commit(mbar);
         }
