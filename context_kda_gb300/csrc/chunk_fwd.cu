@@ -3,12 +3,12 @@
 // final states) and transition columns (qhat, transition A).
 //
 // Algebra (per chunk of C = 64 rows, Gamma_r = cumulative g within the chunk):
-//   kt_r = exp(Gamma_r) k_r, kh_i = exp(-Gamma_i) k_i, kb_i = exp(Gamma_C - Gamma_i) k_i,
-//   qt_r = scale exp(Gamma_r) q_r,
+//   kt_r = exp(Gamma_r) k_r, kh_i = exp(-Gamma_i) k_i, qt_r = scale exp(Gamma_r) q_r,
 //   M[r,i] = beta_r (kt_r . kh_i) for i < r,   T' = (I + M)^-1 Diag(beta),
 //   Ut = T' V,   U = Ut - T' (Kt X)   (= Ut - W X with W = T' Kt),
 //   O = Qt X + ((Qt Kh^T) masked to i <= r) U,
-//   X' = Diag(exp Gamma_C) X + Kb^T U.
+//   X' = Diag(exp Gamma_C) (X + Kh^T U)   (= Diag(exp Gamma_C) X + Kb^T U with
+//        kb_i = exp(Gamma_C - Gamma_i) k_i).
 // This is the KDA gated delta rule (cuLA PR #110, "feat(cp): add opt-in NVSHMEM
 // CP state handoff", §Supported configuration: BF16 inputs, FP32 state) unrolled
 // over a chunk: writing u_r = beta_r (v_r - (Diag(exp g_r) X_{r-1})^T k_r) for
@@ -25,12 +25,12 @@
 // FP32 accumulation in TMEM).  Operand tiles are written row by row with
 // 16-byte stores; the transposed operands (Kt^T, Kb^T, V^T, W) are the same
 // row-major tiles read MN-major.  The contractions that feed the state and the
-// summaries (Kt Kh^T, Kt X, Ut, T' (Kt X), Kb^T U) use a three-term bf16 split
+// summaries (Kt Kh^T, Kt X, Ut, T' (Kt X), Kh^T U) use a three-term bf16 split
 // (hi*hi + hi*lo + lo*hi, ~2^-17 relative per product) so the FP32 state and
 // summaries stay within 1e-4; the output-only ones (Qt X, masked QK U) use one
 // term.  The 64 x 64 unit-triangular inverse is solved on the CUDA cores in
 // FP32 (16 x 16 blocks) while the tensor core forms Qt X and Kt X from the
-// chunk-start state.  Each chunk's raw rows are staged in shared memory
+// chunk-start state (issued by a warp the inverse leaves idle).  Each chunk's raw rows are staged in shared memory
 // by tiled TMA loads (128-byte swizzle) issued while the previous chunk finishes.
 #include "kda_internal.cuh"
 #include "tc.cuh"
@@ -44,10 +44,9 @@ using namespace tc;
 // Tiles are bf16, hi and lo halves back to back; CS = chunk-column stride (see tc.cuh).
 constexpr uint32_t OFF_XT = 0;        // X^T: rows c (128), cols k (128), CS 2048           2 x 32768
 constexpr uint32_t OFF_KQ = 65536;    // [Kt; Qt]: rows r / 64 + r, cols k, CS 2048          2 x 32768
-constexpr uint32_t OFF_KH = 131072;   // Kh: rows i (64), cols k, CS 1024                    2 x 16384
-//   then M (fp32 64 x 64) + T (fp32 64 x 64, at +16384); then -(Kt X)^T:
+constexpr uint32_t OFF_MT = 131072;   // M (fp32 64 x 64) + T (fp32 64 x 64, at +16384); then -(Kt X)^T:
 //   rows c (128), cols i (64), CS 2048                                                   2 x 16384
-constexpr uint32_t OFF_KB = 163840;   // Kb: rows r (64), cols k, CS 1024                    2 x 16384
+constexpr uint32_t OFF_KH = 163840;   // Kh: rows i (64), cols k, CS 1024                    2 x 16384
 constexpr uint32_t OFF_VT = 196608;   // V: rows r (64), cols v, CS 1024 (16384) + T': rows r, cols i,
 //   CS 1024 (2 x 8192 at +16384); then U^T: rows c (128), cols r (64), CS 2048          2 x 16384
 constexpr uint32_t OFF_MISC = 229376;
@@ -57,14 +56,14 @@ constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay 
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
 constexpr uint32_t T128 = 32768, T64 = 16384;
-constexpr uint32_t OFF_M32 = OFF_KH, OFF_T32 = OFF_KH + 16384;
+constexpr uint32_t OFF_M32 = OFF_MT, OFF_T32 = OFF_MT + 16384;
 constexpr uint32_t OFF_TP = OFF_VT + 16384;          // T' hi | lo (8192 each)
 constexpr uint32_t OFF_QKL = OFF_KQ + T128 + 1024;   // masked QK (bf16) in the Qt rows of the lo tile
 constexpr uint32_t OFF_QT_HI = OFF_KQ + 1024;        // Qt rows of the hi tile
 // Raw rows of the next chunk, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of
 // 64 rows x 128 bytes): q, k, v as two 64-column boxes each, g as four 32-column boxes.
 constexpr uint32_t BOX = 8192;
-constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 * BOX, STG_G = OFF_KH;
+constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 * BOX, STG_G = OFF_MT;
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols)
@@ -212,6 +211,33 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         __syncthreads();
     }
 
+    // O^T = X^T Qt^T (1-term) and (Kt X)^T = X^T Kt^T (3-term) need only the chunk-start state and
+    // the decayed rows: issued in two parts by the last thread, whose warp the inverse leaves idle
+    // (the issuing thread waits while the tensor core drains), committed to mbar2.
+    auto issue_state_products = [&](int part) {
+        fence_after();
+        const uint32_t id = idesc_bf16(128, 64);
+        const uint32_t xoff[3] = {0, 0, T128}, toff[3] = {0, T128, 0};
+        if (part == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), id, kk != 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_KQ + kk * 2 * 2048, 2048), id, kk != 0);
+        } else {
+#pragma unroll
+            for (int ps = 1; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + xoff[ps] + kk * 2 * 2048, 2048),
+                             sdesc(sbase + OFF_KQ + toff[ps] + kk * 2 * 2048, 2048), id, 1);
+            commit(mbar2);
+        }
+    };
+
     const int nch = (len + CH - 1) / CH;
     for (int ci = 0; ci < nch && !aborted; ++ci) {
         const int t0 = start + ci * CH;
@@ -268,27 +294,25 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 vw[i] = (ok && kind == 0) ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
             }
             __syncthreads();   // staging consumed: every region may be rewritten from here
-            // A3: Kt, Qt (stacked), Kh, Kb as bf16 hi/lo and V as bf16, one row piece at a time
+            // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16, one row piece at a time
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = pr, c8 = (pcg + 4 * i) * 8;
-                float kf[8], qf[8], kt[8], qt[8], kh[8], kb[8];
+                float kf[8], qf[8], kt[8], qt[8], kh[8];
                 bf16x8_to_f32(kw[i], kf);
                 bf16x8_to_f32(qw[i], qf);
 #pragma unroll
                 for (int e8 = 0; e8 < 8; ++e8) {
                     const float G = gam[i][e8];
-                    const float e = exp2f(G), ei = exp2f(-G), eb = s_gc[c8 + e8] * ei;
+                    const float e = exp2f(G), ei = exp2f(-G);
                     kt[e8] = e * kf[e8];
                     qt[e8] = scale * e * qf[e8];
                     kh[e8] = ei * kf[e8];
-                    kb[e8] = eb * kf[e8];
                 }
                 const uint32_t o_r = cm_off(r, c8, 2048), o_q = cm_off(64 + r, c8, 2048), o_64 = cm_off(r, c8, 1024);
                 st_split8(base + OFF_KQ + o_r, base + OFF_KQ + T128 + o_r, kt);
                 st_split8(base + OFF_KQ + o_q, base + OFF_KQ + T128 + o_q, qt);
                 st_split8(base + OFF_KH + o_64, base + OFF_KH + T64 + o_64, kh);
-                st_split8(base + OFF_KB + o_64, base + OFF_KB + T64 + o_64, kb);
                 if (kind == 0) *reinterpret_cast<uint4 *>(base + OFF_VT + o_64) = vw[i];
             }
             fence_async_smem();
@@ -309,30 +333,6 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
                              sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
             commit(mbar);
-            // O^T = X^T Qt^T (1-term) and (Kt X)^T = X^T Kt^T (3-term): need only the chunk-start
-            // state and the decayed rows; they run while the inverse is solved
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
-                         sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), id, kk != 0);
-            const uint32_t xoff[3] = {0, 0, T128}, toff[3] = {0, T128, 0};
-#pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + xoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_KQ + toff[ps] + kk * 2 * 2048, 2048), id, (ps | kk) != 0);
-            commit(mbar2);
-        }
-        // while the tensor core works: X^T *= exp(Gamma_C) in TMEM (the MMAs read X from smem)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int k0 = hw * 64 + half * 32;
-            float x[32];
-            tmem_ld32(tl + TM_X + k0, x);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];
-            tmem_st32(tl + TM_X + k0, x);
         }
         wait_mma();
 
@@ -375,6 +375,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 
         // ================= D: T = (I + M)^-1 in 16 x 16 blocks (fp32, CUDA cores) =========
         {
+            if (tid == 255) issue_state_products(0);
             if (tid < 64) {   // diagonal blocks: column jj of block b by forward substitution
                 const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
                 float x[16];
@@ -397,6 +398,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 for (int dd = 1; dd < 4; ++dd) {
                     const bool act = bi < 4 - dd;
                     const int i = bi + dd, j = bi;
+                    if (dd == 1 && tid == 255) issue_state_products(1);
                     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (act) {
 #pragma unroll
@@ -493,7 +495,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
-                st_split8(base + OFF_KH + off, base + OFF_KH + T64 + off, d + 8 * m);
+                st_split8(base + OFF_MT + off, base + OFF_MT + T64 + off, d + 8 * m);
             }
             fence_before();
             fence_async_smem();
@@ -509,7 +511,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_KH + aoff[ps] + kk * 2 * 2048, 2048),
+                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_MT + aoff[ps] + kk * 2 * 2048, 2048),
                              sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id,
                              (kind == 0) || ((ps | kk) != 0));
             commit(mbar);
@@ -532,7 +534,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         }
         if (aborted) break;
 
-        // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kb (3-term, Kb read MN-major) ==
+        // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kh (3-term, Kh read MN-major) ==
         if (tid == 0) {
             fence_after();
             const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
@@ -546,7 +548,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tbase + TM_X, sdesc(sbase + OFF_VT + aoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_KB + boff[ps] + kk * 256, 128, 1024), id128, 1);
+                             sdesc(sbase + OFF_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
             commit(mbar);
         }
         wait_mma();
@@ -570,7 +572,10 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             for (int half = 0; half < 2; ++half) {
                 const int k0 = hw * 64 + half * 32;
                 float x[32];
-                tmem_ld32(tl + TM_X + k0, x);
+                tmem_ld32(tl + TM_X + k0, x);   // X + Kh^T U
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];   // Diag(exp Gamma_C)
+                tmem_st32(tl + TM_X + k0, x);
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
                     st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
