@@ -104,7 +104,12 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 w, float *x)
     }
 }
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int NWORK = 256;        // worker threads (8 warps): operands, inverse, epilogues
+constexpr int NTHREADS = NWORK + 32;   // plus one warp whose lane 0 issues every MMA and TMA load
+constexpr int ISSUER = NWORK;
+enum { HO_A = 0, HO_D = 1, HO_E = 2, HO_H = 3 };   // worker -> issuer handoffs of a chunk
+
+__global__ void __launch_bounds__(NTHREADS, 1)
 chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__restrict__ q,
                  const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta,
@@ -118,8 +123,8 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ __align__(8) uint64_t s_ldbar;
     __shared__ __align__(8) uint64_t s_mbar2;
+    __shared__ __align__(8) uint64_t s_hbar[4];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_abort;
     unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(base);
     float *const s_beta = reinterpret_cast<float *>(base + OFF_BETA);
@@ -139,12 +144,13 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     const uint32_t mbar = smem_u32(&s_mbar);
     const uint32_t ldbar = smem_u32(&s_ldbar);
     const uint32_t mbar2 = smem_u32(&s_mbar2);   // the state products issued with [KK; QK]
+    const bool worker = tid < NWORK, issuer = tid == ISSUER;
 
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(ldbar, 1);
         mbar_init(mbar2, 1);
-        s_abort = 0;
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&s_hbar[i]), 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
     fence_before();
@@ -154,41 +160,42 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
     const int c_lane = quad * 32 + lane;                                     // state column of this thread
     uint32_t phase = 0, phase2 = 0;
-    bool aborted = false;
+    bool aborted = false;   // all workers agree on it (OR-reduced at barriers)
+    bool bad = false;       // a bounded wait of this thread gave up
 
     auto wait_mma = [&]() {
-        if (!mbar_wait(mbar, phase & 1)) s_abort = 1;
+        if (!mbar_wait(mbar, phase & 1)) bad = true;
         ++phase;
         fence_after();
     };
 
     // Stage the raw rows of chunk cn (q, k, g, and v for state columns) with tiled TMA copies
-    // issued by one thread; rows past the end of the tensor arrive as zeros, rows past the
-    // piece are masked when read.  beta of that chunk goes to a register.
+    // issued by the issuer thread; rows past the end of the tensor arrive as zeros, rows past the
+    // piece are masked when read.  beta of that chunk goes to a register of the first 64 workers.
     uint32_t ld_phase = 0;
-    bool loads_pending = false;
     float beta_next = 0.f;
-    auto issue_loads = [&](int cn) {
+    auto issue_tma = [&](int cn) {
+        const int t0n = start + cn * CH;
+        mbar_arrive_expect_tx(ldbar, (kind == 0 ? 6u : 4u) * BOX + 4u * BOX);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(sbase + STG_Q + half * BOX, &tm_q, half * 64, h, t0n, ldbar);
+            tma_load_3d(sbase + STG_K + half * BOX, &tm_k, half * 64, h, t0n, ldbar);
+            if (kind == 0) tma_load_3d(sbase + STG_V + half * BOX, &tm_v, half * 64, h, t0n, ldbar);
+        }
+#pragma unroll
+        for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0n, ldbar);
+    };
+    auto load_beta = [&](int cn) {
         const int t0n = start + cn * CH;
         const int Ln = min(CH, len - cn * CH);
-        if (tid == 0) {
-            mbar_arrive_expect_tx(ldbar, (kind == 0 ? 6u : 4u) * BOX + 4u * BOX);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tma_load_3d(sbase + STG_Q + half * BOX, &tm_q, half * 64, h, t0n, ldbar);
-                tma_load_3d(sbase + STG_K + half * BOX, &tm_k, half * 64, h, t0n, ldbar);
-                if (kind == 0) tma_load_3d(sbase + STG_V + half * BOX, &tm_v, half * 64, h, t0n, ldbar);
-            }
-#pragma unroll
-            for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0n, ldbar);
-        }
         if (tid < 64) beta_next = (tid < Ln) ? beta[static_cast<size_t>(t0n + tid) * H + h] : 0.f;
-        loads_pending = true;
     };
-    issue_loads(0);
+    if (issuer) issue_tma(0);
+    load_beta(0);
 
     // ---- piece start: X^T into TMEM (fp32) and its bf16 split into shared memory
-    {
+    if (worker) {
         const bool from_h0 = kind == 0 && (flags & KDA_PIECE_FIRST) && h0 != nullptr;
         const float *src = h0 + (static_cast<size_t>(seq) * H + h) * KD * VD;
 #pragma unroll
@@ -208,406 +215,425 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
         }
         fence_before();
         fence_async_smem();
-        __syncthreads();
     }
+    __syncthreads();
 
-    // O^T = X^T Qt^T (1-term) and (Kt X)^T = X^T Kt^T (3-term) need only the chunk-start state and
-    // the decayed rows: issued in two parts by the last thread, whose warp the inverse leaves idle
-    // (the issuing thread waits while the tensor core drains), committed to mbar2.
-    auto issue_state_products = [&](int part) {
-        fence_after();
+    // ---- MMA groups, issued by the issuer thread once the workers hand the operands over.
+    // [KK; QK] = [Kt; Qt] Kh^T (3-term) -> mbar
+    auto mma_kkqk = [&]() {
         const uint32_t id = idesc_bf16(128, 64);
+        const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
+#pragma unroll
+        for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
+        commit(mbar);
+    };
+    // O^T = X^T Qt^T (1-term) and (Kt X)^T = X^T Kt^T (3-term): only the chunk-start state and the
+    // decayed rows, so they run while the workers solve the inverse -> mbar2
+    auto mma_state = [&]() {
+        const uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
+                     sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), id, kk != 0);
         const uint32_t xoff[3] = {0, 0, T128}, toff[3] = {0, T128, 0};
-        if (part == 0) {
+#pragma unroll
+        for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
-                         sdesc(sbase + OFF_QT_HI + kk * 2 * 2048, 2048), id, kk != 0);
+                mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + xoff[ps] + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_KQ + toff[ps] + kk * 2 * 2048, 2048), id, (ps | kk) != 0);
+        commit(mbar2);
+    };
+    // Ut^T = V^T T'^T (2-term; V^T is the row-major V tile read MN-major), state columns only
+    auto mma_ut = [&]() {
+        const uint32_t id = idesc_bf16(128, 64, 1, 0);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
-                         sdesc(sbase + OFF_KQ + kk * 2 * 2048, 2048), id, kk != 0);
-        } else {
+        for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
-            for (int ps = 1; ps < 3; ++ps)
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + TM_U, sdesc(sbase + OFF_VT + kk * 256, 128, 1024),
+                         sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
+    };
+    // U^T (+)= -(Kt X)^T T'^T (3-term) -> mbar
+    auto mma_u = [&]() {
+        const uint32_t id = idesc_bf16(128, 64);
+        const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, 8192, 0};
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_KX, sdesc(sbase + OFF_XT + xoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_KQ + toff[ps] + kk * 2 * 2048, 2048), id, 1);
-            commit(mbar2);
-        }
+        for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + TM_U, sdesc(sbase + OFF_MT + aoff[ps] + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id, (kind == 0) || ((ps | kk) != 0));
+        commit(mbar);
+    };
+    // O^T += U^T QK^T (1-term); X^T += U^T Kh (3-term, Kh read MN-major) -> mbar
+    auto mma_out = [&]() {
+        const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tbase + TM_O, sdesc(sbase + OFF_VT + kk * 2 * 2048, 2048),
+                     sdesc(sbase + OFF_QKL + kk * 2 * 2048, 2048), id64, 1);
+        const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, T64, 0};
+#pragma unroll
+        for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + TM_X, sdesc(sbase + OFF_VT + aoff[ps] + kk * 2 * 2048, 2048),
+                         sdesc(sbase + OFF_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
+        commit(mbar);
+    };
+    // Workers hand a set of shared-memory operands over to the issuer: every writer fences its
+    // generic-proxy stores for the tensor core, the workers meet, and one of them arrives.
+    // Returns true when some worker's wait gave up (then nothing is handed over).
+    auto handoff = [&](int which) -> bool {
+        fence_async_smem();
+        fence_before();
+        const bool ab = bar_or1(NWORK, bad);
+        if (!ab && tid == 0) mbar_arrive(smem_u32(&s_hbar[which]));
+        return ab;
     };
 
     const int nch = (len + CH - 1) / CH;
-    for (int ci = 0; ci < nch && !aborted; ++ci) {
-        const int t0 = start + ci * CH;
-        const int L = min(CH, len - ci * CH);
+    if (worker) {
+        for (int ci = 0; ci < nch && !aborted; ++ci) {
+            const int t0 = start + ci * CH;
+            const int L = min(CH, len - ci * CH);
 
-        // ================= A: staged rows -> decayed keys / queries / values in operand tiles =====
-        {
-            if (!mbar_wait(ldbar, ld_phase & 1)) s_abort = 1;
-            ++ld_phase;
-            loads_pending = false;
-            // A1: log2-scaled cumulative decay per key channel, in place over the staged g
-            //     (32 rows per thread: load all, scan in registers, store once)
+            // ================= A: staged rows -> decayed keys / queries / values in operand tiles =====
             {
-                const int kc = tid & 127, hr = tid >> 7;
-                unsigned char *gq = base + STG_G + (kc >> 5) * BOX + (kc & 3) * 4;
-                const int gch = (kc & 31) >> 2;
-                float gv[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) gv[j] = *reinterpret_cast<const float *>(gq + sw128(hr * 32 + j, gch));
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc += (hr * 32 + j < L) ? gv[j] * LOG2E : 0.f;
-                    gv[j] = acc;
-                }
-                s_gsum[hr * 128 + kc] = acc;
-                if (tid < 64) s_beta[tid] = beta_next;
-                __syncthreads();
-                const float off = hr ? s_gsum[kc] : 0.f;
-                if (hr == 0) s_gc[kc] = exp2f(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
-#pragma unroll
-                for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
-                __syncthreads();
-            }
-            // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
-            //     the lanes of a warp hold consecutive rows of one piece column
-            const int pr = tid & 63, pcg = tid >> 6;
-            float gam[4][8];
-            uint4 kw[4], qw[4], vw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = pr, c8 = (pcg + 4 * i) * 8;
-                const unsigned char *gb = base + STG_G + (c8 >> 5) * BOX;
-                const int gch = (c8 & 31) >> 2;
-                const float4 a = *reinterpret_cast<const float4 *>(gb + sw128(r, gch));
-                const float4 b = *reinterpret_cast<const float4 *>(gb + sw128(r, gch + 1));
-                gam[i][0] = a.x; gam[i][1] = a.y; gam[i][2] = a.z; gam[i][3] = a.w;
-                gam[i][4] = b.x; gam[i][5] = b.y; gam[i][6] = b.z; gam[i][7] = b.w;
-                const bool ok = r < L;
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t bo = (c8 >> 6) * BOX + sw128(r, (c8 & 63) >> 3);
-                kw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_K + bo) : z;
-                qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + bo) : z;
-                vw[i] = (ok && kind == 0) ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
-            }
-            __syncthreads();   // staging consumed: every region may be rewritten from here
-            // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16, one row piece at a time
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = pr, c8 = (pcg + 4 * i) * 8;
-                float kf[8], qf[8], kt[8], qt[8], kh[8];
-                bf16x8_to_f32(kw[i], kf);
-                bf16x8_to_f32(qw[i], qf);
-#pragma unroll
-                for (int e8 = 0; e8 < 8; ++e8) {
-                    const float G = gam[i][e8];
-                    const float e = exp2f(G), ei = exp2f(-G);
-                    kt[e8] = e * kf[e8];
-                    qt[e8] = scale * e * qf[e8];
-                    kh[e8] = ei * kf[e8];
-                }
-                const uint32_t o_r = cm_off(r, c8, 2048), o_q = cm_off(64 + r, c8, 2048), o_64 = cm_off(r, c8, 1024);
-                st_split8(base + OFF_KQ + o_r, base + OFF_KQ + T128 + o_r, kt);
-                st_split8(base + OFF_KQ + o_q, base + OFF_KQ + T128 + o_q, qt);
-                st_split8(base + OFF_KH + o_64, base + OFF_KH + T64 + o_64, kh);
-                if (kind == 0) *reinterpret_cast<uint4 *>(base + OFF_VT + o_64) = vw[i];
-            }
-            fence_async_smem();
-            __syncthreads();
-            if (s_abort) aborted = true;
-        }
-        if (aborted) break;
-
-        // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
-        if (tid == 0) {
-            fence_after();
-            const uint32_t id = idesc_bf16(128, 64);
-            const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
-#pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
-            commit(mbar);
-        }
-        wait_mma();
-
-        // ================= C: M (fp32, beta-scaled, strictly lower) and masked QK (bf16) =====
-        {
-            float d[32];
-            tmem_ld32(tl + TM_D1 + hw * 32, d);
-            if (quad < 2) {
-                const int r = c_lane;
-                const float br = s_beta[r];
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float4 m4;
-                    const int i0 = hw * 32 + 4 * j4;
-                    m4.x = (i0 + 0 < r) ? br * d[4 * j4 + 0] : 0.f;
-                    m4.y = (i0 + 1 < r) ? br * d[4 * j4 + 1] : 0.f;
-                    m4.z = (i0 + 2 < r) ? br * d[4 * j4 + 2] : 0.f;
-                    m4.w = (i0 + 3 < r) ? br * d[4 * j4 + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, r, i0)) = m4;
-                }
-            } else {
-                const int r = c_lane - 64;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int p2 = 0; p2 < 4; ++p2) {
-                        const int i0 = hw * 32 + 8 * m + 2 * p2;
-                        w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                if (!mbar_wait(ldbar, ld_phase & 1)) bad = true;
+                ++ld_phase;
+                // A1: log2-scaled cumulative decay per key channel, in place over the staged g
+                //     (32 rows per thread: load all, scan in registers, store once)
+                {
+                    const int kc = tid & 127, hr = tid >> 7;
+                    unsigned char *gq = base + STG_G + (kc >> 5) * BOX + (kc & 3) * 4;
+                    const int gch = (kc & 31) >> 2;
+                    float gv[32];
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) gv[j] = *reinterpret_cast<const float *>(gq + sw128(hr * 32 + j, gch));
+                    float acc = 0.f;
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        acc += (hr * 32 + j < L) ? gv[j] * LOG2E : 0.f;
+                        gv[j] = acc;
                     }
-                    *reinterpret_cast<uint4 *>(base + OFF_QKL + cm_off(r, hw * 32 + 8 * m, 2048)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    s_gsum[hr * 128 + kc] = acc;
+                    if (tid < 64) s_beta[tid] = beta_next;
+                    bar_sync1(NWORK);
+                    const float off = hr ? s_gsum[kc] : 0.f;
+                    if (hr == 0) s_gc[kc] = exp2f(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
+                    bar_sync1(NWORK);
                 }
-            }
-            fence_before();
-            __syncthreads();
-            if (s_abort) aborted = true;
-        }
-        if (aborted) break;
-
-        // ================= D: T = (I + M)^-1 in 16 x 16 blocks (fp32, CUDA cores) =========
-        {
-            if (tid == 255) issue_state_products(0);
-            if (tid < 64) {   // diagonal blocks: column jj of block b by forward substitution
-                const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
-                float x[16];
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float s = 0.f;
-#pragma unroll
-                    for (int ii = 0; ii < rr; ++ii) s = fmaf(*f32_at(base, OFF_M32, r0 + rr, r0 + ii), x[ii], s);
-                    x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -s);
-                }
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
-            }
-            __syncthreads();
-            // off-diagonal blocks by distance dd: Y = sum_{k=j}^{i-1} M_ik T_kj, then T_ij = -T_ii Y.
-            // Thread -> block bi (j = bi, i = bi + dd), row rr, four adjacent columns c4..c4+3.
-            {
-                const int bi = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-#pragma unroll
-                for (int dd = 1; dd < 4; ++dd) {
-                    const bool act = bi < 4 - dd;
-                    const int i = bi + dd, j = bi;
-                    if (dd == 1 && tid == 255) issue_state_products(1);
-                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (act) {
-#pragma unroll
-                        for (int kb = 0; kb < 3; ++kb) {
-                            if (kb < dd) {
-                                const int kk = j + kb;
-#pragma unroll
-                                for (int m4 = 0; m4 < 4; ++m4) {
-                                    const float4 mv = *reinterpret_cast<const float4 *>(
-                                        f32_at(base, OFF_M32, 16 * i + rr, 16 * kk + 4 * m4));
-                                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float4 tv = *reinterpret_cast<const float4 *>(
-                                            f32_at(base, OFF_T32, 16 * kk + 4 * m4 + e, 16 * j + c4));
-                                        y.x = fmaf(mm[e], tv.x, y.x);
-                                        y.y = fmaf(mm[e], tv.y, y.y);
-                                        y.z = fmaf(mm[e], tv.z, y.z);
-                                        y.w = fmaf(mm[e], tv.w, y.w);
-                                    }
-                                }
-                            }
-                        }
-                        // Y_ij goes to the unused upper-triangle block (j, i) of M
-                        *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, 16 * j + rr, 16 * i + c4)) = y;
-                    }
-                    __syncthreads();
-                    if (act) {
-                        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int m4 = 0; m4 < 4; ++m4) {
-                            const float4 tv = *reinterpret_cast<const float4 *>(
-                                f32_at(base, OFF_T32, 16 * i + rr, 16 * i + 4 * m4));
-                            const float tt[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float4 yv = *reinterpret_cast<const float4 *>(
-                                    f32_at(base, OFF_M32, 16 * j + 4 * m4 + e, 16 * i + c4));
-                                t.x = fmaf(tt[e], yv.x, t.x);
-                                t.y = fmaf(tt[e], yv.y, t.y);
-                                t.z = fmaf(tt[e], yv.z, t.z);
-                                t.w = fmaf(tt[e], yv.w, t.w);
-                            }
-                        }
-                        *reinterpret_cast<float4 *>(f32_at(base, OFF_T32, 16 * i + rr, 16 * j + c4)) =
-                            make_float4(-t.x, -t.y, -t.z, -t.w);
-                    }
-                    __syncthreads();
-                }
-            }
-            // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
-            {
-                // lanes: 8 consecutive rows x four 16-column groups (conflict-free row-piece reads)
-                const int r = ((tid >> 5) << 3) | (tid & 7), i0 = ((tid >> 3) & 3) * 16;
-                float tv[16];
-#pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
-                    const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = i0 + 4 * m4 + e;
-                        tv[4 * m4 + e] = (i <= r) ? tt[e] * s_beta[i] : 0.f;
-                    }
-                }
-                st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
-                st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),
-                          tv + 8);
-            }
-            fence_async_smem();
-            __syncthreads();
-        }
-
-        // ================= E: U^T = Ut^T - (Kt X)^T T'^T; Ut^T = V^T T'^T (2-term, V^T the row-major
-        //                     V tile read MN-major), the product term 3-term from -(Kt X)^T in smem
-        if (tid == 0 && kind == 0) {
-            fence_after();
-            const uint32_t id = idesc_bf16(128, 64, 1, 0);
-#pragma unroll
-            for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_VT + kk * 256, 128, 1024),
-                             sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
-        }
-        {
-            if (!mbar_wait(mbar2, phase2 & 1)) s_abort = 1;
-            ++phase2;
-            fence_after();
-            float d[32];
-            tmem_ld32(tl + TM_KX + hw * 32, d);   // (Kt X)^T[c = c_lane][i = hw*32 + j]
-#pragma unroll
-            for (int j = 0; j < 32; ++j) d[j] = -d[j];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
-                st_split8(base + OFF_MT + off, base + OFF_MT + T64 + off, d + 8 * m);
-            }
-            fence_before();
-            fence_async_smem();
-            __syncthreads();
-            if (s_abort) aborted = true;
-        }
-        if (aborted) break;
-        if (tid == 0) {
-            fence_after();
-            const uint32_t id = idesc_bf16(128, 64);
-            const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, 8192, 0};
-#pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_U, sdesc(sbase + OFF_MT + aoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id,
-                             (kind == 0) || ((ps | kk) != 0));
-            commit(mbar);
-        }
-        wait_mma();
-
-        // ================= H: U^T (rows c, cols r) hi/lo into shared memory ====================
-        {
-            float d[32];
-            tmem_ld32(tl + TM_U + hw * 32, d);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
-                st_split8(base + OFF_VT + off, base + OFF_VT + T64 + off, d + 8 * m);
-            }
-            fence_before();
-            fence_async_smem();
-            __syncthreads();
-            if (s_abort) aborted = true;
-        }
-        if (aborted) break;
-
-        // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kh (3-term, Kh read MN-major) ==
-        if (tid == 0) {
-            fence_after();
-            const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tbase + TM_O, sdesc(sbase + OFF_VT + kk * 2 * 2048, 2048),
-                         sdesc(sbase + OFF_QKL + kk * 2 * 2048, 2048), id64, 1);
-            const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, T64, 0};
-#pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_X, sdesc(sbase + OFF_VT + aoff[ps] + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
-            commit(mbar);
-        }
-        wait_mma();
-
-        // ================= J: outputs (or qhat) to HBM; new X^T split into shared memory ========
-        if (ci + 1 < nch) issue_loads(ci + 1);   // staging regions are free once I has completed
-        {
-            // O^T[c][r] -> row-major O tile in the free V/U region, then 16-byte coalesced stores
-            float d[32];
-            tmem_ld32(tl + TM_O + hw * 32, d);    // O^T[c][r = hw*32 + j]
-            if (kind == 0) {
-                uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_VT);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = f32_to_bf16_bits(d[j]);
-            } else {
-                float *so = reinterpret_cast<float *>(base + OFF_VT);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = d[j];
-            }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int k0 = hw * 64 + half * 32;
-                float x[32];
-                tmem_ld32(tl + TM_X + k0, x);   // X + Kh^T U
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];   // Diag(exp Gamma_C)
-                tmem_st32(tl + TM_X + k0, x);
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
-                              base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
-            }
-            fence_before();
-            fence_async_smem();
-            __syncthreads();
-            if (kind == 0) {
-#pragma unroll
+                // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
+                //     the lanes of a warp hold consecutive rows of one piece column
+                const int pr = tid & 63, pcg = tid >> 6;
+                float gam[4][8];
+                uint4 kw[4], qw[4], vw[4];
+    #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
-                    if (r < L)
-                        *reinterpret_cast<uint4 *>(o + (static_cast<size_t>(t0 + r) * H + h) * VD + c16 * 8) =
-                            *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 256 + c16 * 16);
+                    const int r = pr, c8 = (pcg + 4 * i) * 8;
+                    const unsigned char *gb = base + STG_G + (c8 >> 5) * BOX;
+                    const int gch = (c8 & 31) >> 2;
+                    const float4 a = *reinterpret_cast<const float4 *>(gb + sw128(r, gch));
+                    const float4 b = *reinterpret_cast<const float4 *>(gb + sw128(r, gch + 1));
+                    gam[i][0] = a.x; gam[i][1] = a.y; gam[i][2] = a.z; gam[i][3] = a.w;
+                    gam[i][4] = b.x; gam[i][5] = b.y; gam[i][6] = b.z; gam[i][7] = b.w;
+                    const bool ok = r < L;
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t bo = (c8 >> 6) * BOX + sw128(r, (c8 & 63) >> 3);
+                    kw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_K + bo) : z;
+                    qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + bo) : z;
+                    vw[i] = (ok && kind == 0) ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int id = tid + 256 * i, r = id >> 5, c32 = id & 31;
-                    if (r < L)
-                        *reinterpret_cast<uint4 *>(qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) * KD +
-                                                   c32 * 4) =
-                            *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 512 + c32 * 16);
+                bar_sync1(NWORK);   // staging consumed: every region may be rewritten from here
+                // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16, one row piece at a time
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = pr, c8 = (pcg + 4 * i) * 8;
+                    float kf[8], qf[8], kt[8], qt[8], kh[8];
+                    bf16x8_to_f32(kw[i], kf);
+                    bf16x8_to_f32(qw[i], qf);
+    #pragma unroll
+                    for (int e8 = 0; e8 < 8; ++e8) {
+                        const float G = gam[i][e8];
+                        const float e = exp2f(G), ei = exp2f(-G);
+                        kt[e8] = e * kf[e8];
+                        qt[e8] = scale * e * qf[e8];
+                        kh[e8] = ei * kf[e8];
+                    }
+                    const uint32_t o_r = cm_off(r, c8, 2048), o_q = cm_off(64 + r, c8, 2048), o_64 = cm_off(r, c8, 1024);
+                    st_split8(base + OFF_KQ + o_r, base + OFF_KQ + T128 + o_r, kt);
+                    st_split8(base + OFF_KQ + o_q, base + OFF_KQ + T128 + o_q, qt);
+                    st_split8(base + OFF_KH + o_64, base + OFF_KH + T64 + o_64, kh);
+                    if (kind == 0) *reinterpret_cast<uint4 *>(base + OFF_VT + o_64) = vw[i];
+                }
+                aborted = handoff(HO_A);   // -> [KK; QK], then Qt X and Kt X
+            }
+            if (aborted) break;
+
+            // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
+            wait_mma();
+
+            // ================= C: M (fp32, beta-scaled, strictly lower) and masked QK (bf16) =====
+            {
+                float d[32];
+                tmem_ld32(tl + TM_D1 + hw * 32, d);
+                if (quad < 2) {
+                    const int r = c_lane;
+                    const float br = s_beta[r];
+    #pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float4 m4;
+                        const int i0 = hw * 32 + 4 * j4;
+                        m4.x = (i0 + 0 < r) ? br * d[4 * j4 + 0] : 0.f;
+                        m4.y = (i0 + 1 < r) ? br * d[4 * j4 + 1] : 0.f;
+                        m4.z = (i0 + 2 < r) ? br * d[4 * j4 + 2] : 0.f;
+                        m4.w = (i0 + 3 < r) ? br * d[4 * j4 + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, r, i0)) = m4;
+                    }
+                } else {
+                    const int r = c_lane - 64;
+    #pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        uint32_t w[4];
+    #pragma unroll
+                        for (int p2 = 0; p2 < 4; ++p2) {
+                            const int i0 = hw * 32 + 8 * m + 2 * p2;
+                            w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(base + OFF_QKL + cm_off(r, hw * 32 + 8 * m, 2048)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                fence_before();
+                aborted = bar_or1(NWORK, bad);
+            }
+            if (aborted) break;
+
+            // ================= D: T = (I + M)^-1 in 16 x 16 blocks (fp32, CUDA cores) =========
+            // Diagonal blocks t_b by forward substitution; then each 32 x 32 half as
+            // [t_0 0; -t_1 M_10 t_0  t_1], and the whole as [T_lo 0; -T_hi M_hi,lo T_lo  T_hi].
+            {
+                if (tid < 64) {   // column jj of diagonal block b; each solved entry updates all later rows
+                    const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
+                    float x[16], sacc[16];
+    #pragma unroll
+                    for (int rr = 0; rr < 16; ++rr) sacc[rr] = 0.f;
+    #pragma unroll
+                    for (int rr = 0; rr < 16; ++rr) {
+                        x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -sacc[rr]);
+    #pragma unroll
+                        for (int r2 = rr + 1; r2 < 16; ++r2)
+                            sacc[r2] = fmaf(*f32_at(base, OFF_M32, r0 + r2, r0 + rr), x[rr], sacc[r2]);
+                    }
+    #pragma unroll
+                    for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
+                }
+                bar_sync1(NWORK);
+                // Thread -> group g of 64 (one 16 x 16 output block), row rr, four adjacent columns c4..c4+3.
+                // Intermediate products Y_ij go to the unused upper-triangle block (j, i) of M.
+                const int g = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+                // y += A[ar + rr][ac + 0..15] * B[br + 0..15][bc + c4 .. c4 + 3]
+                auto blk_fma = [&](float4 &y, uint32_t offa, int ar, int ac, uint32_t offb, int br, int bc) {
+    #pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        const float4 av = *reinterpret_cast<const float4 *>(f32_at(base, offa, ar + rr, ac + 4 * m4));
+                        const float aa[4] = {av.x, av.y, av.z, av.w};
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 bv =
+                                *reinterpret_cast<const float4 *>(f32_at(base, offb, br + 4 * m4 + e, bc + c4));
+                            y.x = fmaf(aa[e], bv.x, y.x);
+                            y.y = fmaf(aa[e], bv.y, y.y);
+                            y.z = fmaf(aa[e], bv.z, y.z);
+                            y.w = fmaf(aa[e], bv.w, y.w);
+                        }
+                    }
+                };
+                const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                // halves: Y_10 = M_10 t_0, Y_32 = M_32 t_2 (groups 0, 1), then T_10, T_32 = -t_i Y
+                if (g < 2) {
+                    const int i = 1 + 2 * g, j = 2 * g;
+                    float4 y = z4;
+                    blk_fma(y, OFF_M32, 16 * i, 16 * j, OFF_T32, 16 * j, 16 * j);
+                    *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, 16 * j + rr, 16 * i + c4)) = y;
+                }
+                bar_sync1(NWORK);
+                if (g < 2) {
+                    const int i = 1 + 2 * g, j = 2 * g;
+                    float4 t = z4;
+                    blk_fma(t, OFF_T32, 16 * i, 16 * i, OFF_M32, 16 * j, 16 * i);
+                    *reinterpret_cast<float4 *>(f32_at(base, OFF_T32, 16 * i + rr, 16 * j + c4)) =
+                        make_float4(-t.x, -t.y, -t.z, -t.w);
+                }
+                bar_sync1(NWORK);
+                // whole: Y_ij = sum_{k=j..1} M_ik T_kj, then T_ij = -sum_{k=2..i} T_ik Y_kj (i = 2, 3; j = 0, 1)
+                {
+                    const int i = 2 + (g >> 1), j = g & 1;
+                    float4 y = z4;
+                    blk_fma(y, OFF_M32, 16 * i, 16 * j, OFF_T32, 16 * j, 16 * j);
+                    if (j == 0) blk_fma(y, OFF_M32, 16 * i, 16, OFF_T32, 16, 0);
+                    *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, 16 * j + rr, 16 * i + c4)) = y;
+                    bar_sync1(NWORK);
+                    float4 t = z4;
+                    blk_fma(t, OFF_T32, 16 * i, 32, OFF_M32, 16 * j, 32);
+                    if (i == 3) blk_fma(t, OFF_T32, 48, 48, OFF_M32, 16 * j, 48);
+                    *reinterpret_cast<float4 *>(f32_at(base, OFF_T32, 16 * i + rr, 16 * j + c4)) =
+                        make_float4(-t.x, -t.y, -t.z, -t.w);
+                    bar_sync1(NWORK);
+                }
+                // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
+                {
+                    // lanes: 8 consecutive rows x four 16-column groups (conflict-free row-piece reads)
+                    const int r = ((tid >> 5) << 3) | (tid & 7), i0 = ((tid >> 3) & 3) * 16;
+                    float tv[16];
+    #pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
+                        const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = i0 + 4 * m4 + e;
+                            tv[4 * m4 + e] = (i <= r) ? tt[e] * s_beta[i] : 0.f;
+                        }
+                    }
+                    st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
+                    st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),
+                              tv + 8);
+                }
+                aborted = handoff(HO_D);   // -> Ut^T = V^T T'^T
+            }
+            if (aborted) break;
+
+            // ================= E: U^T = Ut^T - (Kt X)^T T'^T; Ut^T = V^T T'^T (2-term, V^T the row-major
+            //                     V tile read MN-major), the product term 3-term from -(Kt X)^T in smem
+            {
+                if (!mbar_wait(mbar2, phase2 & 1)) bad = true;
+                ++phase2;
+                fence_after();
+                float d[32];
+                tmem_ld32(tl + TM_KX + hw * 32, d);   // (Kt X)^T[c = c_lane][i = hw*32 + j]
+    #pragma unroll
+                for (int j = 0; j < 32; ++j) d[j] = -d[j];
+    #pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
+                    st_split8(base + OFF_MT + off, base + OFF_MT + T64 + off, d + 8 * m);
+                }
+                aborted = handoff(HO_E);   // -> U^T += -(Kt X)^T T'^T
+            }
+            if (aborted) break;
+            wait_mma();
+
+            // ================= H: U^T (rows c, cols r) hi/lo into shared memory ====================
+            {
+                float d[32];
+                tmem_ld32(tl + TM_U + hw * 32, d);
+    #pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
+                    st_split8(base + OFF_VT + off, base + OFF_VT + T64 + off, d + 8 * m);
+                }
+                aborted = handoff(HO_H);   // -> O^T += U^T QK^T, X^T += U^T Kh
+            }
+            if (aborted) break;
+
+            // ================= I: O^T += U^T QK^T (1-term); X^T += U^T Kh (3-term, Kh read MN-major) ==
+            wait_mma();
+
+            // ================= J: outputs (or qhat) to HBM; new X^T split into shared memory ========
+            if (ci + 1 < nch) load_beta(ci + 1);   // the issuer stages the rows once I has completed
+            {
+                // O^T[c][r] -> row-major O tile in the free V/U region, then 16-byte coalesced stores
+                float d[32];
+                tmem_ld32(tl + TM_O + hw * 32, d);    // O^T[c][r = hw*32 + j]
+                if (kind == 0) {
+                    uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_VT);
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = f32_to_bf16_bits(d[j]);
+                } else {
+                    float *so = reinterpret_cast<float *>(base + OFF_VT);
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = d[j];
+                }
+    #pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int k0 = hw * 64 + half * 32;
+                    float x[32];
+                    tmem_ld32(tl + TM_X + k0, x);   // X + Kh^T U
+    #pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];   // Diag(exp Gamma_C)
+                    tmem_st32(tl + TM_X + k0, x);
+    #pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
+                                  base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
+                }
+                fence_before();
+                fence_async_smem();
+                aborted = bar_or1(NWORK, bad);
+                if (kind == 0) {
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
+                        if (r < L)
+                            *reinterpret_cast<uint4 *>(o + (static_cast<size_t>(t0 + r) * H + h) * VD + c16 * 8) =
+                                *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 256 + c16 * 16);
+                    }
+                } else {
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int id = tid + 256 * i, r = id >> 5, c32 = id & 31;
+                        if (r < L)
+                            *reinterpret_cast<uint4 *>(qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) * KD +
+                                                       c32 * 4) =
+                                *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 512 + c32 * 16);
+                    }
                 }
             }
-            if (s_abort) aborted = true;
+        }
+    } else if (issuer) {
+        // Issuer: for each chunk, wait for the workers' handoffs and issue the MMA groups; stage the
+        // next chunk's rows once the output products (the last readers of the staging regions) finish.
+        bool ok = true;
+        int last_tma = 0;
+        for (int ci = 0; ci < nch && ok; ++ci) {
+            const uint32_t par = ci & 1;
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
+            fence_after();
+            mma_kkqk();
+            mma_state();
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_D]), par))) break;
+            fence_after();
+            if (kind == 0) mma_ut();
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_E]), par))) break;
+            fence_after();
+            mma_u();
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_H]), par))) break;
+            fence_after();
+            mma_out();
+            if (ci + 1 < nch) {
+                // mbar phases per chunk: [KK; QK], U, outputs; the last is the one pending now
+                if (!(ok = mbar_wait(mbar, (3 * ci + 2) & 1))) break;
+                issue_tma(ci + 1);
+                last_tma = ci + 1;
+            }
+        }
+        if (!ok) {
+            atomicExch(&g_chunk_status, KDA_ERR_TIMEOUT);
+            mbar_wait(ldbar, last_tma & 1);   // bounded: let the last staged copy land
         }
     }
 
     // ---- piece end: summaries and final states (X[k][c] from TMEM lane c, column k)
-    if (!aborted) {
+    if (worker && !aborted) {
         const size_t mat = static_cast<size_t>(KD) * VD;
         const bool seg_last = flags & KDA_PIECE_SEG_LAST, seq_end = flags & KDA_PIECE_SEQ_END;
         float *dst0 = nullptr, *dst1 = nullptr;
@@ -636,9 +662,8 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 }
             }
         }
-    } else {
-        if (loads_pending) mbar_wait(ldbar, ld_phase & 1);   // bounded: let staged copies land
-        if (tid == 0) atomicExch(&g_chunk_status, KDA_ERR_TIMEOUT);
+    } else if (worker && tid == 0) {
+        atomicExch(&g_chunk_status, KDA_ERR_TIMEOUT);
     }
     fence_before();
     __syncthreads();
@@ -686,7 +711,7 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
     cudaError_t err = cudaFuncSetAttribute(chunk_forward_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    chunk_forward_tc<<<static_cast<unsigned>(blocks), 256, SMEM_ALLOC, stream>>>(
+    chunk_forward_tc<<<static_cast<unsigned>(blocks), NTHREADS, SMEM_ALLOC, stream>>>(
         plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B, final_state, qhat, afin, tq, tk, tv, tg);
     return cudaGetLastError();
 }

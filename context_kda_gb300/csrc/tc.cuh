@@ -84,6 +84,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
     }
 }
 
+// Plain one-count arrival (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
+// Named barrier 1 over the first 'count' threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync1(uint32_t count) { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); }
+
+// Named barrier 1 over the first 'count' threads with an OR reduction of v: every participant
+// gets the same answer.
+__device__ __forceinline__ bool bar_or1(uint32_t count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbarrier.cta.red.or.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // One-shot arrival that also announces 'bytes' of asynchronous copies on the barrier.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes)
 {
