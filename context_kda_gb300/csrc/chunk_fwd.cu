@@ -314,10 +314,10 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     unsigned char *gq = base + STG_G + (kc >> 5) * BOX + (kc & 3) * 4;
                     const int gch = (kc & 31) >> 2;
                     float gv[32];
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 32; ++j) gv[j] = *reinterpret_cast<const float *>(gq + sw128(hr * 32 + j, gch));
                     float acc = 0.f;
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         acc += (hr * 32 + j < L) ? gv[j] * LOG2E : 0.f;
                         gv[j] = acc;
@@ -326,8 +326,8 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     if (tid < 64) s_beta[tid] = beta_next;
                     bar_sync1(NWORK);
                     const float off = hr ? s_gsum[kc] : 0.f;
-                    if (hr == 0) s_gc[kc] = exp2f(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
-    #pragma unroll
+                    if (hr == 0) s_gc[kc] = ex2_ftz(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
+#pragma unroll
                     for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
                     bar_sync1(NWORK);
                 }
@@ -336,7 +336,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 const int pr = tid & 63, pcg = tid >> 6;
                 float gam[4][8];
                 uint4 kw[4], qw[4], vw[4];
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int r = pr, c8 = (pcg + 4 * i) * 8;
                     const unsigned char *gb = base + STG_G + (c8 >> 5) * BOX;
@@ -354,16 +354,16 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 }
                 bar_sync1(NWORK);   // staging consumed: every region may be rewritten from here
                 // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16, one row piece at a time
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int r = pr, c8 = (pcg + 4 * i) * 8;
                     float kf[8], qf[8], kt[8], qt[8], kh[8];
                     bf16x8_to_f32(kw[i], kf);
                     bf16x8_to_f32(qw[i], qf);
-    #pragma unroll
+#pragma unroll
                     for (int e8 = 0; e8 < 8; ++e8) {
                         const float G = gam[i][e8];
-                        const float e = exp2f(G), ei = exp2f(-G);
+                        const float e = ex2_ftz(G), ei = ex2_ftz(-G);
                         kt[e8] = e * kf[e8];
                         qt[e8] = scale * e * qf[e8];
                         kh[e8] = ei * kf[e8];
@@ -388,7 +388,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 if (quad < 2) {
                     const int r = c_lane;
                     const float br = s_beta[r];
-    #pragma unroll
+#pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         float4 m4;
                         const int i0 = hw * 32 + 4 * j4;
@@ -400,10 +400,10 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     }
                 } else {
                     const int r = c_lane - 64;
-    #pragma unroll
+#pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         uint32_t w[4];
-    #pragma unroll
+#pragma unroll
                         for (int p2 = 0; p2 < 4; ++p2) {
                             const int i0 = hw * 32 + 8 * m + 2 * p2;
                             w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
@@ -424,16 +424,16 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 if (tid < 64) {   // column jj of diagonal block b; each solved entry updates all later rows
                     const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
                     float x[16], sacc[16];
-    #pragma unroll
+#pragma unroll
                     for (int rr = 0; rr < 16; ++rr) sacc[rr] = 0.f;
-    #pragma unroll
+#pragma unroll
                     for (int rr = 0; rr < 16; ++rr) {
                         x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -sacc[rr]);
-    #pragma unroll
+#pragma unroll
                         for (int r2 = rr + 1; r2 < 16; ++r2)
                             sacc[r2] = fmaf(*f32_at(base, OFF_M32, r0 + r2, r0 + rr), x[rr], sacc[r2]);
                     }
-    #pragma unroll
+#pragma unroll
                     for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
                 }
                 bar_sync1(NWORK);
@@ -442,11 +442,11 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 const int g = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
                 // y += A[ar + rr][ac + 0..15] * B[br + 0..15][bc + c4 .. c4 + 3]
                 auto blk_fma = [&](float4 &y, uint32_t offa, int ar, int ac, uint32_t offb, int br, int bc) {
-    #pragma unroll
+#pragma unroll
                     for (int m4 = 0; m4 < 4; ++m4) {
                         const float4 av = *reinterpret_cast<const float4 *>(f32_at(base, offa, ar + rr, ac + 4 * m4));
                         const float aa[4] = {av.x, av.y, av.z, av.w};
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float4 bv =
                                 *reinterpret_cast<const float4 *>(f32_at(base, offb, br + 4 * m4 + e, bc + c4));
@@ -494,11 +494,11 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                     // lanes: 8 consecutive rows x four 16-column groups (conflict-free row-piece reads)
                     const int r = ((tid >> 5) << 3) | (tid & 7), i0 = ((tid >> 3) & 3) * 16;
                     float tv[16];
-    #pragma unroll
+#pragma unroll
                     for (int m4 = 0; m4 < 4; ++m4) {
                         const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
                         const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i = i0 + 4 * m4 + e;
                             tv[4 * m4 + e] = (i <= r) ? tt[e] * s_beta[i] : 0.f;
@@ -520,9 +520,9 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 fence_after();
                 float d[32];
                 tmem_ld32(tl + TM_KX + hw * 32, d);   // (Kt X)^T[c = c_lane][i = hw*32 + j]
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] = -d[j];
-    #pragma unroll
+#pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
                     st_split8(base + OFF_MT + off, base + OFF_MT + T64 + off, d + 8 * m);
@@ -536,7 +536,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             {
                 float d[32];
                 tmem_ld32(tl + TM_U + hw * 32, d);
-    #pragma unroll
+#pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
                     st_split8(base + OFF_VT + off, base + OFF_VT + T64 + off, d + 8 * m);
@@ -551,27 +551,36 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
             // ================= J: outputs (or qhat) to HBM; new X^T split into shared memory ========
             if (ci + 1 < nch) load_beta(ci + 1);   // the issuer stages the rows once I has completed
             {
-                // O^T[c][r] -> row-major O tile in the free V/U region, then 16-byte coalesced stores
+                // O^T[c][r] -> row-major O tile in the free V/U region, then 16-byte coalesced stores;
+                // the state half X^T[c][hw*64 .. +64) is read in the same batch
+                uint32_t od[32], xa[32], xb[32];
+                tmem_ld32_nowait(tl + TM_O + hw * 32, od);   // O^T[c][r = hw*32 + j]
+                tmem_ld32_nowait(tl + TM_X + hw * 64, xa);
+                tmem_ld32_nowait(tl + TM_X + hw * 64 + 32, xb);
+                tmem_wait_ld();
+                reg_fence32(od);
+                reg_fence32(xa);
+                reg_fence32(xb);
                 float d[32];
-                tmem_ld32(tl + TM_O + hw * 32, d);    // O^T[c][r = hw*32 + j]
+#pragma unroll
+                for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(od[j]);
                 if (kind == 0) {
                     uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_VT);
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = f32_to_bf16_bits(d[j]);
                 } else {
                     float *so = reinterpret_cast<float *>(base + OFF_VT);
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = d[j];
                 }
-    #pragma unroll
+#pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int k0 = hw * 64 + half * 32;
-                    float x[32];
-                    tmem_ld32(tl + TM_X + k0, x);   // X + Kh^T U
-    #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] *= s_gc[k0 + j];   // Diag(exp Gamma_C)
+                    float x[32];   // X + Kh^T U, then Diag(exp Gamma_C)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(half ? xb[j] : xa[j]) * s_gc[k0 + j];
                     tmem_st32(tl + TM_X + k0, x);
-    #pragma unroll
+#pragma unroll
                     for (int m = 0; m < 4; ++m)
                         st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
                                   base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
@@ -580,7 +589,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                 fence_async_smem();
                 aborted = bar_or1(NWORK, bad);
                 if (kind == 0) {
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
                         if (r < L)
@@ -588,7 +597,7 @@ chunk_forward_tc(const int32_t *__restrict__ plan, int H, const uint16_t *__rest
                                 *reinterpret_cast<const uint4 *>(base + OFF_VT + r * 256 + c16 * 16);
                     }
                 } else {
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int id = tid + 256 * i, r = id >> 5, c32 = id & 31;
                         if (r < L)
