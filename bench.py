@@ -40,10 +40,11 @@ CH = 64
 # chunk forward, and the transition columns a continuing token adds
 FLOPS_STATE = 6 * CH * K_DIM + 4 * CH * V_DIM + 6 * K_DIM * V_DIM          # 180,224
 FLOPS_TRANSITION = 6 * K_DIM * K_DIM + 2 * CH * K_DIM                      # 114,688
-# tensor work the chunk kernel issues per chunk and CTA (bf16 M=128 MMAs, split passes included)
-ISSUED_PER_CHUNK = {0: 2 * 128 * (3 * 64 * 128 + 3 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 128 + 64 * 128 + 64 * 64
-                                  + 3 * 128 * 64),
-                    1: 2 * 128 * (3 * 64 * 128 + 3 * 64 * 64 + 3 * 64 * 128 + 64 * 128 + 64 * 64 + 3 * 128 * 64)}
+# tensor work the chunk kernel issues per chunk and CTA (bf16 M=128 MMAs, split passes included):
+# [KK; QK] 3 x (N 64, K 128), Qt X 1 x (64, 128), Kt X 3 x (64, 128), Ut 2 x (64, 64) for state
+# columns, T'(Kt X) 3 x (64, 64), QK U 1 x (64, 64), Kh^T U 3 x (128, 64)
+_ISSUED_COMMON = 3 * 64 * 128 + 64 * 128 + 3 * 64 * 128 + 3 * 64 * 64 + 64 * 64 + 3 * 128 * 64
+ISSUED_PER_CHUNK = {0: 2 * 128 * (_ISSUED_COMMON + 2 * 64 * 64), 1: 2 * 128 * _ISSUED_COMMON}
 CHUNK_KERNEL_SRC = os.path.join(ROOT, "context_kda_gb300", "csrc", "chunk_fwd.cu")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "chunk_forward_t8192_h16_s4.md")
 
