@@ -40,12 +40,13 @@ CH = 64
 # chunk forward, and the transition columns a continuing token adds
 FLOPS_STATE = 6 * CH * K_DIM + 4 * CH * V_DIM + 6 * K_DIM * V_DIM          # 180,224
 FLOPS_TRANSITION = 6 * K_DIM * K_DIM + 2 * CH * K_DIM                      # 114,688
-# tensor work the chunk kernel issues per chunk and CTA (bf16 M=128 MMAs, split passes included):
-# [KK; QK] 3 x (N 64, K 128), Qt X 1 x (64, 128), Kt X 3 x (64, 128), Ut 2 x (64, 64) for state
-# columns, T'(Kt X) 3 x (64, 64), QK U 1 x (64, 64), Kh^T U 3 x (128, 64)
-_ISSUED_COMMON = 3 * 64 * 128 + 64 * 128 + 3 * 64 * 128 + 3 * 64 * 64 + 64 * 64 + 3 * 128 * 64
-ISSUED_PER_CHUNK = {0: 2 * 128 * (_ISSUED_COMMON + 2 * 64 * 64), 1: 2 * 128 * _ISSUED_COMMON}
-CHUNK_KERNEL_SRC = os.path.join(ROOT, "context_kda_gb300", "csrc", "chunk_fwd.cu")
+# tensor work the chunk stage issues (bf16 M=128 MMAs, split passes included), as 2 * 128 * N * K
+# per product: the preparation, once per (chunk, head): [KK; QK] 3 x (N 64, K 128), W 3 x (64, 64),
+# Ut 2 x (64, 64); the state pass, per chunk and work item: W X 3 x (64, 128), Qt X 1 x (64, 128),
+# QK U 1 x (64, 64), Kh^T U 3 x (128, 64)
+ISSUED_PREP_PER_CHUNK = 2 * 128 * (3 * 64 * 128 + 3 * 64 * 64 + 2 * 64 * 64)
+ISSUED_STATE_PER_CHUNK = 2 * 128 * (3 * 64 * 128 + 64 * 128 + 64 * 64 + 3 * 128 * 64)
+CHUNK_KERNEL_SRCS = [os.path.join(ROOT, "context_kda_gb300", "csrc", f) for f in ("chunk_prep.cu", "chunk_state.cu")]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "chunk_forward_t8192_h16_s4.md")
 
 
@@ -59,11 +60,14 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def _profile_values(kernel_src):
-    """Figures recorded in the committed ncu summary, if it was taken on the current source."""
+def _profile_values(kernel_srcs):
+    """Figures recorded in the committed ncu summary, if it was taken on the current sources."""
     if not os.path.exists(PROFILE_SUMMARY):
         return {}
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for src in kernel_srcs:
+        h.update(open(src, "rb").read())
+    sha = h.hexdigest()[:16]
     vals = {}
     for line in open(PROFILE_SUMMARY):
         if line.startswith("- ") and ":" in line:
@@ -203,10 +207,10 @@ def run_ours(args, w, rank, world, local_rank):
     plan = kda.kda_plan_segments(inp.cu_seqlens, S)
     plan_dev = kda.upload_plan(plan, dev)
     off = kda.kda_workspace_layout(plan, H)
-    ws = torch.empty(off[5], dtype=torch.uint8, device=dev)
-    A = ws[off[2]:off[3]].view(torch.float32)
-    B = ws[off[3]:off[4]].view(torch.float32)
-    S_in = ws[off[4]:off[5]].view(torch.float32)
+    ws = torch.empty(off[6], dtype=torch.uint8, device=dev)
+    A = ws[off[3]:off[4]].view(torch.float32)
+    B = ws[off[4]:off[5]].view(torch.float32)
+    S_in = ws[off[5]:off[6]].view(torch.float32)
     o = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((N, H, K_DIM, V_DIM), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
@@ -313,12 +317,12 @@ def run_ours(args, w, rank, world, local_rank):
     flops = T * H * FLOPS_STATE + T_cont * H * FLOPS_TRANSITION
     achieved = flops / (kern_ms[0] / 1e3) / 1e12
     items_off, pieces_off = int(plan[18]), int(plan[17])
-    issued = 0
+    issued = int(plan[11]) * H * ISSUED_PREP_PER_CHUNK   # every (chunk, head) is prepared once
     for i in range(int(plan[12])):
-        pc, kind = int(plan[items_off + 2 * i]), int(plan[items_off + 2 * i + 1])
+        pc = int(plan[items_off + 2 * i])
         ln = int(plan[pieces_off + 8 * pc + 1])
-        issued += ((ln + CH - 1) // CH) * ISSUED_PER_CHUNK[kind] * H
-    prof = _profile_values(CHUNK_KERNEL_SRC)
+        issued += ((ln + CH - 1) // CH) * ISSUED_STATE_PER_CHUNK * H
+    prof = _profile_values(CHUNK_KERNEL_SRCS)
     traffic = float(prof["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in prof else None
     shares = (kern_ms / kern_ms.sum()).tolist()
     line = {

@@ -102,9 +102,9 @@ def kda_plan_segments(cu_seqlens, num_segments: int, seg_bounds=None, chunk: int
 
 
 def kda_workspace_layout(plan, H: int):
-    """Byte offsets (qhat, fin, A, B, S_in, total) of the device workspace."""
+    """Byte offsets (qhat, fin, packages, A, B, S_in, total) of the device workspace."""
     p = _words(plan)
-    off = (ctypes.c_size_t * 6)()
+    off = (ctypes.c_size_t * 7)()
     _check("kda_workspace_layout", _lib.kda_workspace_layout(_hp(p), int(H), off))
     return tuple(int(x) for x in off)
 

@@ -39,23 +39,24 @@ bool plan_ok(const int32_t *plan)
 
 size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
-bool layout(const int32_t *plan, int32_t H, size_t off[6])
+bool layout(const int32_t *plan, int32_t H, size_t off[7])
 {
     if (!plan_ok(plan) || H < 1) return false;
     const size_t h = static_cast<size_t>(H), K = kda::KD, V = kda::VD;
-    const size_t sizes[5] = {
-        h * static_cast<size_t>(plan[KDA_PH_TCONT]) * K * 4,     // qhat
-        static_cast<size_t>(plan[KDA_PH_NFIN]) * h * K * K * 4,  // fin transitions
-        static_cast<size_t>(plan[KDA_PH_S]) * h * K * K * 4,     // A
-        static_cast<size_t>(plan[KDA_PH_S]) * h * K * V * 4,     // B
-        static_cast<size_t>(plan[KDA_PH_S]) * h * K * V * 4,     // S_in
+    const size_t sizes[6] = {
+        h * static_cast<size_t>(plan[KDA_PH_TCONT]) * K * 4,                 // qhat
+        static_cast<size_t>(plan[KDA_PH_NFIN]) * h * K * K * 4,              // fin transitions
+        static_cast<size_t>(plan[KDA_PH_NCHUNKS]) * h * KDA_PACKAGE_BYTES,   // chunk packages
+        static_cast<size_t>(plan[KDA_PH_S]) * h * K * K * 4,                 // A
+        static_cast<size_t>(plan[KDA_PH_S]) * h * K * V * 4,                 // B
+        static_cast<size_t>(plan[KDA_PH_S]) * h * K * V * 4,                 // S_in
     };
     size_t pos = 0;
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 6; ++i) {
         off[i] = pos;
         pos = round256(pos + sizes[i]);
     }
-    off[5] = pos;
+    off[6] = pos;
     return true;
 }
 
@@ -68,16 +69,18 @@ bool inputs_ok(const void *q, const void *k, const void *v, const float *g, cons
     return true;
 }
 
-kda::Workspace carve(void *ws, const size_t off[6])
+kda::Workspace carve(void *ws, const size_t off[7])
 {
     char *b = static_cast<char *>(ws);
     return kda::Workspace{reinterpret_cast<float *>(b + off[0]), reinterpret_cast<float *>(b + off[1]),
-                          reinterpret_cast<float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
-                          reinterpret_cast<float *>(b + off[4])};
+                          reinterpret_cast<unsigned char *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
+                          reinterpret_cast<float *>(b + off[4]), reinterpret_cast<float *>(b + off[5])};
 }
 
-// Bytes of the qhat + fin regions that the three-call path needs.
-size_t boundary_bytes(const size_t off[6]) { return off[2]; }
+// Bytes of the qhat + fin regions that kda_apply_boundary reads.
+size_t boundary_bytes(const size_t off[7]) { return off[2]; }
+// Bytes of the qhat + fin + package regions that kda_segment_forward uses.
+size_t segment_bytes(const size_t off[7]) { return off[3]; }
 
 }  // namespace
 
@@ -127,6 +130,20 @@ bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_rows_3d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
+                    uint32_t inner)
+{
+    auto fn = tmap_encode_fn();
+    if (!fn || T <= 0) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {128ull * elem, 128ull * elem * static_cast<cuuint64_t>(H)};
+    const cuuint32_t box[3] = {inner, 1, 64};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count()
 {
     static int cached[64] = {0};
@@ -141,7 +158,7 @@ int sm_count()
 }
 }  // namespace kda
 
-extern "C" int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6])
+extern "C" int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[7])
 {
     if (!off) return KDA_ERR_INVALID_ARG;
     return layout(plan, H, off) ? KDA_OK : KDA_ERR_INVALID_ARG;
@@ -149,8 +166,8 @@ extern "C" int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6
 
 extern "C" size_t kda_workspace_bytes(const int32_t *plan, int32_t H)
 {
-    size_t off[6];
-    return layout(plan, H, off) ? off[5] : 0;
+    size_t off[7];
+    return layout(plan, H, off) ? off[6] : 0;
 }
 
 extern "C" int kda_segment_forward(const int32_t *plan, const int32_t *plan_dev, int32_t H,
@@ -159,17 +176,17 @@ extern "C" int kda_segment_forward(const int32_t *plan, const int32_t *plan_dev,
                                    kda_bf16 *o, float *A, float *B, float *final_state,
                                    void *ws, size_t ws_bytes, void *stream)
 {
-    size_t off[6];
+    size_t off[7];
     if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
     if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
     if (!o || !A || !B || !final_state || !aligned16(o) || !aligned16(A) || !aligned16(B) ||
         !aligned16(final_state))
         return KDA_ERR_INVALID_ARG;
-    if (boundary_bytes(off) > 0 && (!ws || !aligned16(ws))) return KDA_ERR_INVALID_ARG;
-    if (ws_bytes < boundary_bytes(off)) return KDA_ERR_WORKSPACE;
+    if (segment_bytes(off) > 0 && (!ws || !aligned16(ws))) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < segment_bytes(off)) return KDA_ERR_WORKSPACE;
     const kda::Workspace w = carve(ws, off);
     return cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B,
-                                                 final_state, w.qhat, w.afin,
+                                                 final_state, w.qhat, w.afin, w.pkg,
                                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -177,7 +194,7 @@ extern "C" int kda_compose_summaries(const int32_t *plan, const int32_t *plan_de
                                      const float *A, const float *B, const float *h0, float *S_in,
                                      void *stream)
 {
-    size_t off[6];
+    size_t off[7];
     if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
     if (!A || !B || !S_in || !aligned16(A) || !aligned16(B) || !aligned16(S_in)) return KDA_ERR_INVALID_ARG;
     if (h0 && !aligned16(h0)) return KDA_ERR_INVALID_ARG;
@@ -188,7 +205,7 @@ extern "C" int kda_apply_boundary(const int32_t *plan, const int32_t *plan_dev, 
                                   const float *S_in, const void *ws, size_t ws_bytes, kda_bf16 *o,
                                   float *final_state, void *stream)
 {
-    size_t off[6];
+    size_t off[7];
     if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
     if (!S_in || !o || !final_state || !aligned16(S_in) || !aligned16(o) || !aligned16(final_state))
         return KDA_ERR_INVALID_ARG;
@@ -205,16 +222,16 @@ extern "C" int kda_forward_segmented(const int32_t *plan, const int32_t *plan_de
                                      kda_bf16 *o, float *final_state, void *ws, size_t ws_bytes,
                                      void *stream)
 {
-    size_t off[6];
+    size_t off[7];
     if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
     if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
     if (!o || !final_state || !aligned16(o) || !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
     if (!ws || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
-    if (ws_bytes < off[5]) return KDA_ERR_WORKSPACE;
+    if (ws_bytes < off[6]) return KDA_ERR_WORKSPACE;
     const kda::Workspace w = carve(ws, off);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int rc = cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, w.A, w.B,
-                                                   final_state, w.qhat, w.afin, s));
+                                                   final_state, w.qhat, w.afin, w.pkg, s));
     if (rc != KDA_OK) return rc;
     rc = cuda_status(kda::launch_compose(plan, plan_dev, H, w.A, w.B, h0, w.S_in, s));
     if (rc != KDA_OK) return rc;

@@ -1,0 +1,538 @@
+// Chunk-parallel preparation of the chunkwise KDA forward: everything about a 64-token chunk of
+// one head that does not depend on the state entering it.
+//
+// Algebra (per chunk of C = 64 rows, Gamma_r = cumulative g within the chunk):
+//   kt_r = exp(Gamma_r) k_r, kh_i = exp(-Gamma_i) k_i, qt_r = scale exp(Gamma_r) q_r,
+//   M[r,i] = beta_r (kt_r . kh_i) for i < r,   T' = (I + M)^-1 Diag(beta),
+//   W = T' Kt,   Ut = T' V,   QK = (Qt Kh^T) masked to i <= r.
+// The state pass then needs only these: with X the chunk-start state,
+//   U = Ut - W X,   O = Qt X + QK U,   X' = Diag(exp Gamma_C) (X + Kh^T U).
+// This is the KDA gated delta rule (cuLA PR #110, "feat(cp): add opt-in NVSHMEM CP state
+// handoff", §Supported configuration: BF16 inputs, FP32 state) unrolled over a chunk: writing
+// u_r = beta_r (v_r - (Diag(exp g_r) X_{r-1})^T k_r) for every row gives (I + M) U = Diag(beta)
+// (V - Kt X).  The intra-chunk transform runs once per (chunk, head) here, on all SMs, instead
+// of once per piece column set inside the serial pass.
+//
+// Mapping.  A persistent CTA per SM walks (chunk, head) units: 8 worker warps build the operand
+// tiles and solve the inverse on the CUDA cores; lane 0 of a ninth warp issues the tcgen05 MMAs
+// (M = 128, bf16 operands in shared memory, FP32 accumulators in TMEM) and the TMA loads that
+// stage the next unit's rows.  The products that feed the state (Kt Kh^T, W) use a three-term
+// bf16 split (hi*hi + hi*lo + lo*hi, ~2^-17 relative); Ut two terms (V is exact in bf16).
+// Results go straight from registers to the unit's package in the workspace with 16-byte
+// stores, each tile already in the layout the state pass's MMAs read.
+#include "kda_internal.cuh"
+#include "tc.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+// ---- shared-memory map (bytes from the 1024-byte aligned dynamic base) ------------------------
+constexpr uint32_t OFF_KQ = 0;        // [Kt; Qt]: rows r / 64 + r, cols k, CS 2048, hi | lo       2 x 32768
+constexpr uint32_t OFF_MT = 65536;    // M (fp32 64 x 64) + T (fp32 64 x 64, at +16384)
+constexpr uint32_t OFF_KH = 98304;    // Kh: rows i (64), cols k, CS 1024, hi | lo                2 x 16384
+constexpr uint32_t OFF_VT = 131072;   // V: rows r (64), cols v, CS 1024                            16384
+constexpr uint32_t OFF_TP = 147456;   // T': rows r, cols i, CS 1024, hi | lo                      2 x 8192
+constexpr uint32_t OFF_MISC = 163840;
+constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
+constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
+constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
+constexpr uint32_t T128 = 32768, T64 = 16384;
+constexpr uint32_t OFF_M32 = OFF_MT, OFF_T32 = OFF_MT + 16384;
+// Raw rows of a unit, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of 64 rows
+// x 128 bytes): q, k, v as two 64-column boxes each, g as four 32-column boxes.
+constexpr uint32_t BOX = 8192;
+constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 * BOX, STG_G = OFF_MT;
+
+// ---- TMEM columns --------------------------------------------------------------------------
+constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols)
+constexpr uint32_t TM_W = 64;     // W^T
+constexpr uint32_t TM_U = 128;    // Ut^T
+constexpr uint32_t TM_COLS = 256;
+
+constexpr int NWORK = 256;             // worker threads
+constexpr int NTHREADS = NWORK + 32;   // plus the issuer warp
+constexpr int ISSUER = NWORK;
+enum { HO_A = 0, HO_D = 1 };           // worker -> issuer handoffs of a unit
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ int g_prep_status;   // set to KDA_ERR_TIMEOUT when a bounded wait expires
+
+// fp32 64 x 64 scratch with the 16-byte chunk index XOR-swizzled by the row
+__device__ __forceinline__ float *f32_at(unsigned char *base, uint32_t off, int r, int i)
+{
+    return reinterpret_cast<float *>(base + off + r * 256 + (((i >> 2) ^ (r & 15)) << 4) + (i & 3) * 4);
+}
+
+// 8 consecutive values as bf16 hi and lo words (4 + 4 packed pairs).
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], h[p], l[p]);
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Writes 8 consecutive values as bf16 hi and lo (two 16-byte stores).
+__device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, const float *x)
+{
+    uint4 h, l;
+    split8(x, h, l);
+    *reinterpret_cast<uint4 *>(hi) = h;
+    *reinterpret_cast<uint4 *>(lo) = l;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 w, float *x)
+{
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        x[2 * p] = __uint_as_float(ww[p] << 16);
+        x[2 * p + 1] = __uint_as_float(ww[p] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const float *__restrict__ beta,
+              float scale, unsigned char *__restrict__ pkg, const __grid_constant__ CUtensorMap tm_q,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_g)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ __align__(8) uint64_t s_ldbar;
+    __shared__ __align__(8) uint64_t s_hbar[2];
+    __shared__ uint32_t s_tmem;
+    unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(base);
+    float *const s_beta = reinterpret_cast<float *>(base + OFF_BETA);
+    float *const s_gc = reinterpret_cast<float *>(base + OFF_GC);
+    float *const s_gsum = reinterpret_cast<float *>(base + OFF_GSUM);
+
+    const PlanView pv{plan};
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hw = warp >> 2;          // TMEM lane quadrant, column half
+    const bool worker = tid < NWORK, issuer = tid == ISSUER;
+    const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar);
+
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_init(ldbar, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s_hbar[i]), 1);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tbase = s_tmem;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
+    const int c_lane = quad * 32 + lane;                                     // TMEM lane of this thread
+
+    // unit u = head * n_chunks + chunk, so a head's chunks (and their packages, at
+    // pkg + u * KDA_PACKAGE_BYTES) are consecutive; each CTA takes a contiguous run of units
+    const int n_chunks = pv.n_chunks();
+    const long long u_begin = n_units * blockIdx.x / gridDim.x, u_end = n_units * (blockIdx.x + 1) / gridDim.x;
+    auto rows_of = [&](long long u, int &t0, int &L, int &h) {
+        const int32_t *cr = pv.chunk(static_cast<int>(u % n_chunks));
+        h = static_cast<int>(u / n_chunks);
+        t0 = cr[1];
+        L = cr[2];
+    };
+    // Rows of unit u (q, k, v, g) by tiled TMA copies; rows past the end of the tensor arrive as
+    // zeros, rows past the chunk are masked when read.
+    auto issue_tma = [&](long long u) {
+        int t0, L, h;
+        rows_of(u, t0, L, h);
+        mbar_arrive_expect_tx(ldbar, 10u * BOX);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(sbase + STG_Q + half * BOX, &tm_q, half * 64, h, t0, ldbar);
+            tma_load_3d(sbase + STG_K + half * BOX, &tm_k, half * 64, h, t0, ldbar);
+            tma_load_3d(sbase + STG_V + half * BOX, &tm_v, half * 64, h, t0, ldbar);
+        }
+#pragma unroll
+        for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0, ldbar);
+    };
+    float beta_next = 0.f;
+    auto load_beta = [&](long long u) {
+        if (u >= u_end || tid >= 64) return;
+        int t0, L, h;
+        rows_of(u, t0, L, h);
+        beta_next = (tid < L) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
+    };
+    if (issuer && u_begin < u_end) issue_tma(u_begin);
+    load_beta(u_begin);
+
+    bool aborted = false;   // all workers agree on it (OR-reduced at barriers)
+    bool bad = false;       // a bounded wait of this thread gave up
+    uint32_t phase = 0;
+    auto wait_mma = [&]() {
+        if (!mbar_wait(mbar, phase & 1)) bad = true;
+        ++phase;
+        fence_after();
+    };
+    // Workers hand their shared-memory operands over to the issuer (see the state pass).
+    auto handoff = [&](int which) -> bool {
+        fence_async_smem();
+        fence_before();
+        const bool ab = bar_or1(NWORK, bad);
+        if (!ab && tid == 0) mbar_arrive(smem_u32(&s_hbar[which]));
+        return ab;
+    };
+
+    if (worker) {
+        int n = 0;
+        for (long long u = u_begin; u < u_end && !aborted; ++u, ++n) {
+            int t0, L, h;
+            rows_of(u, t0, L, h);
+            (void)t0;
+            (void)h;
+            unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
+
+            // ================= A: staged rows -> decayed keys / queries / values =====================
+            {
+                if (!mbar_wait(ldbar, n & 1)) bad = true;
+                // A1: log2-scaled cumulative decay per key channel, in place over the staged g
+                //     (32 rows per thread: load all, scan in registers, store once)
+                {
+                    const int kc = tid & 127, hr = tid >> 7;
+                    unsigned char *gq = base + STG_G + (kc >> 5) * BOX + (kc & 3) * 4;
+                    const int gch = (kc & 31) >> 2;
+                    float gv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) gv[j] = *reinterpret_cast<const float *>(gq + sw128(hr * 32 + j, gch));
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        acc += (hr * 32 + j < L) ? gv[j] * LOG2E : 0.f;
+                        gv[j] = acc;
+                    }
+                    s_gsum[hr * 128 + kc] = acc;
+                    if (tid < 64) s_beta[tid] = beta_next;
+                    bar_sync1(NWORK);
+                    const float off = hr ? s_gsum[kc] : 0.f;
+                    if (hr == 0) {
+                        const float gcv = ex2_ftz(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
+                        s_gc[kc] = gcv;
+                        reinterpret_cast<float *>(pk + PK_GC)[kc] = gcv;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
+                    bar_sync1(NWORK);
+                }
+                load_beta(u + 1);   // s_beta holds this unit's values now
+                // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
+                //     the lanes of a warp hold consecutive rows of one piece column
+                const int pr = tid & 63, pcg = tid >> 6;
+                float gam[4][8];
+                uint4 kw[4], qw[4], vw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = pr, c8 = (pcg + 4 * i) * 8;
+                    const unsigned char *gb = base + STG_G + (c8 >> 5) * BOX;
+                    const int gch = (c8 & 31) >> 2;
+                    const float4 a = *reinterpret_cast<const float4 *>(gb + sw128(r, gch));
+                    const float4 b = *reinterpret_cast<const float4 *>(gb + sw128(r, gch + 1));
+                    gam[i][0] = a.x; gam[i][1] = a.y; gam[i][2] = a.z; gam[i][3] = a.w;
+                    gam[i][4] = b.x; gam[i][5] = b.y; gam[i][6] = b.z; gam[i][7] = b.w;
+                    const bool ok = r < L;
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t bo = (c8 >> 6) * BOX + sw128(r, (c8 & 63) >> 3);
+                    kw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_K + bo) : z;
+                    qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + bo) : z;
+                    vw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
+                }
+                bar_sync1(NWORK);   // staging consumed: every region may be rewritten from here
+                // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16 in shared memory; Qt hi and Kh
+                //     hi/lo also into the package (lanes hold consecutive rows: 512 contiguous bytes)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = pr, c8 = (pcg + 4 * i) * 8;
+                    float kf[8], qf[8], kt[8], qt[8], kh[8];
+                    bf16x8_to_f32(kw[i], kf);
+                    bf16x8_to_f32(qw[i], qf);
+#pragma unroll
+                    for (int e8 = 0; e8 < 8; ++e8) {
+                        const float G = gam[i][e8];
+                        const float e = ex2_ftz(G), ei = ex2_ftz(-G);
+                        kt[e8] = e * kf[e8];
+                        qt[e8] = scale * e * qf[e8];
+                        kh[e8] = ei * kf[e8];
+                    }
+                    const uint32_t o_r = cm_off(r, c8, 2048), o_q = cm_off(64 + r, c8, 2048), o_64 = cm_off(r, c8, 1024);
+                    uint4 hi, lo;
+                    split8(kt, hi, lo);
+                    *reinterpret_cast<uint4 *>(base + OFF_KQ + o_r) = hi;
+                    *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_r) = lo;
+                    split8(qt, hi, lo);
+                    *reinterpret_cast<uint4 *>(base + OFF_KQ + o_q) = hi;
+                    *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_q) = lo;
+                    *reinterpret_cast<uint4 *>(pk + PK_Q + o_64) = hi;
+                    split8(kh, hi, lo);
+                    *reinterpret_cast<uint4 *>(base + OFF_KH + o_64) = hi;
+                    *reinterpret_cast<uint4 *>(base + OFF_KH + T64 + o_64) = lo;
+                    *reinterpret_cast<uint4 *>(pk + PK_KH + o_64) = hi;
+                    *reinterpret_cast<uint4 *>(pk + PK_KH + T64 + o_64) = lo;
+                    *reinterpret_cast<uint4 *>(base + OFF_VT + o_64) = vw[i];
+                }
+                aborted = handoff(HO_A);   // -> [KK; QK]
+            }
+            if (aborted) break;
+
+            // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
+            wait_mma();
+
+            // ================= C: M (fp32, beta-scaled, strictly lower) and masked QK (bf16) =====
+            {
+                float d[32];
+                tmem_ld32(tl + TM_D1 + hw * 32, d);
+                if (quad < 2) {
+                    const int r = c_lane;
+                    const float br = s_beta[r];
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float4 m4;
+                        const int i0 = hw * 32 + 4 * j4;
+                        m4.x = (i0 + 0 < r) ? br * d[4 * j4 + 0] : 0.f;
+                        m4.y = (i0 + 1 < r) ? br * d[4 * j4 + 1] : 0.f;
+                        m4.z = (i0 + 2 < r) ? br * d[4 * j4 + 2] : 0.f;
+                        m4.w = (i0 + 3 < r) ? br * d[4 * j4 + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, r, i0)) = m4;
+                    }
+                } else {
+                    const int r = c_lane - 64;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int p2 = 0; p2 < 4; ++p2) {
+                            const int i0 = hw * 32 + 8 * m + 2 * p2;
+                            w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(pk + PK_QK + cm_off(r, hw * 32 + 8 * m, 1024)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                fence_before();
+                aborted = bar_or1(NWORK, bad);
+            }
+            if (aborted) break;
+
+        // ================= D: T = (I + M)^-1 in 16 x 16 blocks (fp32, CUDA cores) =========
+        // Diagonal blocks t_b by forward substitution; then each 32 x 32 half as
+        // [t_0 0; -t_1 M_10 t_0  t_1], and the whole as [T_lo 0; -T_hi M_hi,lo T_lo  T_hi].
+        {
+            if (tid < 64) {   // column jj of diagonal block b; each solved entry updates all later rows
+                const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
+                float x[16], sacc[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) sacc[rr] = 0.f;
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -sacc[rr]);
+#pragma unroll
+                    for (int r2 = rr + 1; r2 < 16; ++r2)
+                        sacc[r2] = fmaf(*f32_at(base, OFF_M32, r0 + r2, r0 + rr), x[rr], sacc[r2]);
+                }
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
+            }
+            bar_sync1(NWORK);
+            // Thread -> group g of 64 (one 16 x 16 output block), row rr, four adjacent columns c4..c4+3.
+            // Intermediate products Y_ij go to the unused upper-triangle block (j, i) of M.
+            const int g = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+            // y += A[ar + rr][ac + 0..15] * B[br + 0..15][bc + c4 .. c4 + 3]
+            auto blk_fma = [&](float4 &y, uint32_t offa, int ar, int ac, uint32_t offb, int br, int bc) {
+#pragma unroll
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(f32_at(base, offa, ar + rr, ac + 4 * m4));
+                    const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 bv =
+                            *reinterpret_cast<const float4 *>(f32_at(base, offb, br + 4 * m4 + e, bc + c4));
+                        y.x = fmaf(aa[e], bv.x, y.x);
+                        y.y = fmaf(aa[e], bv.y, y.y);
+                        y.z = fmaf(aa[e], bv.z, y.z);
+                        y.w = fmaf(aa[e], bv.w, y.w);
+                    }
+                }
+            };
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            // halves: Y_10 = M_10 t_0, Y_32 = M_32 t_2 (groups 0, 1), then T_10, T_32 = -t_i Y
+            if (g < 2) {
+                const int i = 1 + 2 * g, j = 2 * g;
+                float4 y = z4;
+                blk_fma(y, OFF_M32, 16 * i, 16 * j, OFF_T32, 16 * j, 16 * j);
+                *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, 16 * j + rr, 16 * i + c4)) = y;
+            }
+            bar_sync1(NWORK);
+            if (g < 2) {
+                const int i = 1 + 2 * g, j = 2 * g;
+                float4 t = z4;
+                blk_fma(t, OFF_T32, 16 * i, 16 * i, OFF_M32, 16 * j, 16 * i);
+                *reinterpret_cast<float4 *>(f32_at(base, OFF_T32, 16 * i + rr, 16 * j + c4)) =
+                    make_float4(-t.x, -t.y, -t.z, -t.w);
+            }
+            bar_sync1(NWORK);
+            // whole: Y_ij = sum_{k=j..1} M_ik T_kj, then T_ij = -sum_{k=2..i} T_ik Y_kj (i = 2, 3; j = 0, 1)
+            {
+                const int i = 2 + (g >> 1), j = g & 1;
+                float4 y = z4;
+                blk_fma(y, OFF_M32, 16 * i, 16 * j, OFF_T32, 16 * j, 16 * j);
+                if (j == 0) blk_fma(y, OFF_M32, 16 * i, 16, OFF_T32, 16, 0);
+                *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, 16 * j + rr, 16 * i + c4)) = y;
+                bar_sync1(NWORK);
+                float4 t = z4;
+                blk_fma(t, OFF_T32, 16 * i, 32, OFF_M32, 16 * j, 32);
+                if (i == 3) blk_fma(t, OFF_T32, 48, 48, OFF_M32, 16 * j, 48);
+                *reinterpret_cast<float4 *>(f32_at(base, OFF_T32, 16 * i + rr, 16 * j + c4)) =
+                    make_float4(-t.x, -t.y, -t.z, -t.w);
+                bar_sync1(NWORK);
+            }
+            // T' = T Diag(beta) as bf16 hi/lo (rows r, cols i), zero above the diagonal
+            {
+                // lanes: 8 consecutive rows x four 16-column groups (conflict-free row-piece reads)
+                const int r = ((tid >> 5) << 3) | (tid & 7), i0 = ((tid >> 3) & 3) * 16;
+                float tv[16];
+#pragma unroll
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
+                    const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = i0 + 4 * m4 + e;
+                        tv[4 * m4 + e] = (i <= r) ? tt[e] * s_beta[i] : 0.f;
+                    }
+                }
+                st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
+                st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),
+                          tv + 8);
+            }
+                aborted = handoff(HO_D);   // -> W^T = Kt^T T'^T, Ut^T = V^T T'^T
+            }
+            if (aborted) break;
+
+            // ================= E: W and Ut from TMEM into the package ================================
+            {
+                wait_mma();
+                uint32_t wd[32], ud[32];
+                tmem_ld32_nowait(tl + TM_W + hw * 32, wd);   // W^T[k = c_lane][r = hw*32 + j]
+                tmem_ld32_nowait(tl + TM_U + hw * 32, ud);   // Ut^T[c = c_lane][r = hw*32 + j]
+                tmem_wait_ld();
+                reg_fence32(wd);
+                reg_fence32(ud);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(wd[8 * m + e]);
+                    uint4 hi, lo;
+                    split8(x, hi, lo);
+                    const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
+                    *reinterpret_cast<uint4 *>(pk + PK_W + off) = hi;
+                    *reinterpret_cast<uint4 *>(pk + PK_W + T64 + off) = lo;
+                }
+                // Ut^T as [hw][m][c] float4 groups: a warp's store (and the state pass's load) of one
+                // group covers 512 contiguous bytes
+                float4 *ut = reinterpret_cast<float4 *>(pk + PK_U) + hw * 8 * 128 + c_lane;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    ut[m * 128] = make_float4(__uint_as_float(ud[4 * m]), __uint_as_float(ud[4 * m + 1]),
+                                        __uint_as_float(ud[4 * m + 2]), __uint_as_float(ud[4 * m + 3]));
+                fence_before();
+                aborted = bar_or1(NWORK, bad);
+            }
+        }
+    } else if (issuer) {
+        // Issuer: per unit, [KK; QK] once the operand tiles are in, then W and Ut once T' is; the
+        // next unit's rows are staged as soon as W (the last reader of the staging regions) is done.
+        bool ok = true;
+        int n = 0;
+        int last_n = 0;   // unit count of the last staged copy
+        for (long long u = u_begin; u < u_end && ok; ++u, ++n) {
+            const uint32_t par = n & 1;
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
+            fence_after();
+            {
+                const uint32_t id = idesc_bf16(128, 64);
+                const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
+#pragma unroll
+                for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
+                                 sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
+                commit(mbar);
+            }
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_D]), par))) break;
+            fence_after();
+            {
+                // W^T = Kt^T T'^T (3-term; Kt^T is the row-major Kt tile read MN-major)
+                const uint32_t id = idesc_bf16(128, 64, 1, 0);
+                const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, 8192, 0};
+#pragma unroll
+                for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tbase + TM_W, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 256, 128, 2048),
+                                 sdesc(sbase + OFF_TP + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
+                // Ut^T = V^T T'^T (2-term)
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tbase + TM_U, sdesc(sbase + OFF_VT + kk * 256, 128, 1024),
+                                 sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
+                commit(mbar);
+            }
+            if (u + 1 < u_end) {
+                // mbar phases per unit: [KK; QK], then W / Ut (pending now)
+                if (!(ok = mbar_wait(mbar, (2 * n + 1) & 1))) break;
+                issue_tma(u + 1);
+                last_n = n + 1;
+            }
+        }
+        if (!ok) {
+            atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+            mbar_wait(ldbar, last_n & 1);   // bounded: let the last staged copy land
+        }
+    }
+    if (worker && aborted && tid == 0) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0) tmem_dealloc(tbase, TM_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
+                              const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
+                              unsigned char *pkg, cudaStream_t stream)
+{
+    const PlanView pv{plan_host};
+    const long long n_units = static_cast<long long>(pv.n_chunks()) * H;
+    if (n_units <= 0) return cudaSuccess;
+    const int T = pv.T();
+    CUtensorMap tq, tk, tv, tg;
+    if (!encode_rows_3d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
+        !encode_rows_3d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
+        !encode_rows_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
+        !encode_rows_3d(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, 32))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(chunk_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(SMEM_ALLOC));
+    if (err != cudaSuccess) return err;
+    const long long grid = n_units < sm_count() ? n_units : sm_count();
+    chunk_prep_tc<<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(plan_dev, H, n_units, beta, scale,
+                                                                                 pkg, tq, tk, tv, tg);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

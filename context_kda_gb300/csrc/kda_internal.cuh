@@ -33,16 +33,36 @@ struct PlanView {
     __host__ __device__ const int32_t *item(int i) const { return w + w[KDA_PH_OFF_ITEMS] + 2 * i; }
     __host__ __device__ const int32_t *cont(int i) const { return w + w[KDA_PH_OFF_CONT] + 4 * i; }
     __host__ __device__ const int32_t *fin(int i) const { return w + w[KDA_PH_OFF_FIN] + 4 * i; }
+    __host__ __device__ int32_t n_chunks() const { return w[KDA_PH_NCHUNKS]; }
+    // chunk records: piece, start token, rows, index within the piece (pieces in order)
+    __host__ __device__ const int32_t *chunk(int i) const { return w + w[KDA_PH_OFF_CHUNKS] + 4 * i; }
 };
+
+// Chunk package: the operands one (chunk, head) hands from the preparation kernel to the state
+// pass, each tile in the shared-memory layout its MMA reads (byte offsets; bf16 tiles in the
+// no-swizzle core-matrix layout, hi then lo where split).
+enum : uint32_t {
+    PK_W = 0,          // W = T' Kt, read MN-major: rows k (128), cols r (64), CS 2048, hi | lo
+    PK_Q = 32768,      // Qt (scaled) hi, K-major: rows r (64), cols k (128), CS 1024
+    PK_P1_END = 49152,
+    PK_QK = 49152,     // masked Qt Kh^T, K-major: rows r (64), cols i (64), CS 1024
+    PK_KH = 57344,     // Kh, read MN-major: rows i (64), cols k (128), CS 1024, hi | lo
+    PK_GC = 90112,     // exp(Gamma_C), 128 fp32
+    PK_P2_END = 90624,
+    PK_U = 90624,      // Ut^T = (T' V)^T, fp32 (128 x 64) as float4 groups [r / 32][(r % 32) / 4][c]
+    PK_END = 123392
+};
+static_assert(static_cast<uint32_t>(PK_END) == static_cast<uint32_t>(KDA_PACKAGE_BYTES), "package size");
 
 // Piece record fields.
 enum { PC_START = 0, PC_LEN = 1, PC_SEQ = 2, PC_SEG = 3, PC_FLAGS = 4, PC_CONT = 5, PC_ROW = 6, PC_FIN = 7 };
 
 // Workspace regions resolved to typed device pointers.
 struct Workspace {
-    float *qhat;   // [H][T_cont][K]
-    float *afin;   // [n_fin][H][K][K]
-    float *A;      // [S][H][K][K]
+    float *qhat;          // [H][T_cont][K]
+    float *afin;          // [n_fin][H][K][K]
+    unsigned char *pkg;   // [H][n_chunks][KDA_PACKAGE_BYTES]
+    float *A;             // [S][H][K][K]
     float *B;      // [S][H][K][V]
     float *S_in;   // [S][H][K][V]
 };
@@ -63,12 +83,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 // rows and the 128-byte swizzle (16-byte chunk c of box row r lands at chunk c ^ (r % 8)).
 bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows);
 
+// Tensor map of a [T][H][128] tensor (inner dimension first) with a box of 'inner' columns x 1
+// head x 64 rows and the 128-byte swizzle; elem = element bytes.
+bool encode_rows_3d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
+                    uint32_t inner);
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_dev, int H,
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const float *g, const float *beta, const float *h0, float scale,
                                  uint16_t *o, float *A, float *B, float *final_state,
-                                 float *qhat, float *afin, cudaStream_t stream);
+                                 float *qhat, float *afin, unsigned char *pkg, cudaStream_t stream);
+cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
+                              const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
+                              unsigned char *pkg, cudaStream_t stream);
+cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
+                               const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
+                               float *qhat, float *afin, cudaStream_t stream);
 cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
                            const float *B, const float *h0, float *S_in, cudaStream_t stream);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,

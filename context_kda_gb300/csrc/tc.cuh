@@ -106,6 +106,17 @@ __device__ __forceinline__ bool bar_or1(uint32_t count, bool v)
     return r != 0;
 }
 
+// mbar_wait by lane 0 of the calling warp only, the result broadcast to the warp: the other
+// lanes do not poll the barrier (many pollers slow every mbarrier operation of the CTA, the TMA's
+// transaction updates included).  Call with the whole warp converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t mbar, uint32_t parity)
+{
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(mbar, parity) ? 1u : 0u;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // One-shot arrival that also announces 'bytes' of asynchronous copies on the barrier.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes)
 {

@@ -142,21 +142,27 @@ int kda_last_cuda_error(void);
 int kda_plan_segments(const int32_t *cu_seqlens, int32_t num_seqs, int32_t num_segments,
                       const int32_t *seg_bounds, int32_t chunk, int32_t *plan, size_t *plan_len);
 
+/* Bytes of one chunk package: the per-chunk operands that the chunk-parallel
+ * preparation hands to the serial state pass (see kda_segment_forward). */
+enum { KDA_PACKAGE_BYTES = 123392 };
+
 /*
  * kda_workspace_layout -- byte offsets of the regions of the device workspace
- * for a plan and head count.  off[0..5] = qhat, fin transitions, A, B, S_in,
- * total.  Each region starts on a 256-byte boundary.
+ * for a plan and head count.  off[0..6] = qhat, fin transitions, packages, A,
+ * B, S_in, total.  Each region starts on a 256-byte boundary.
  *   qhat   fp32 [H][T_cont][K]    transition-seen queries of continuing tokens
  *   fin    fp32 [n_fin][H][K][K]  transitions of continuing pieces that end a sequence
+ *   pkg    [H][n_chunks][KDA_PACKAGE_BYTES]  per-chunk operands (scratch)
  *   A      fp32 [S][H][K][K]      (used by kda_forward_segmented)
  *   B      fp32 [S][H][K][V]      (used by kda_forward_segmented)
  *   S_in   fp32 [S][H][K][V]      (used by kda_forward_segmented)
- * The three-call path uses only the qhat and fin regions; A, B and S_in are
- * then caller tensors.  Returns KDA_OK or KDA_ERR_INVALID_ARG.
+ * The three-call path uses the first off[3] bytes (qhat, fin, packages); A, B
+ * and S_in are then caller tensors.  kda_apply_boundary reads only qhat and fin
+ * (the first off[2] bytes).  Returns KDA_OK or KDA_ERR_INVALID_ARG.
  */
-int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[6]);
+int kda_workspace_layout(const int32_t *plan, int32_t H, size_t off[7]);
 
-/* kda_workspace_bytes -- total device workspace bytes (off[5] above); 0 if the
+/* kda_workspace_bytes -- total device workspace bytes (off[6] above); 0 if the
  * plan or H is invalid.  The summary part, A + B, is S*H*(K*K + K*V)*4 bytes:
  * 256 MiB at S = 64, H = 32, K = V = 128 (PR #136 §Latest cuDNN compatibility). */
 size_t kda_workspace_bytes(const int32_t *plan, int32_t H);
@@ -178,7 +184,14 @@ size_t kda_workspace_bytes(const int32_t *plan, int32_t H);
  *   final_state out fp32 [N][H][K][V]: exact for sequences whose last piece
  *               starts the sequence; local (zero-start) end state otherwise
  *               (completed by kda_apply_boundary).
- *   ws, ws_bytes  device workspace; its qhat and fin regions are written.
+ *   ws, ws_bytes  device workspace of at least off[3] bytes (kda_workspace_layout);
+ *               its qhat and fin regions are written, its package region is
+ *               scratch.
+ * Two kernels run on 'stream': a chunk-parallel preparation of every (chunk,
+ * head), which writes that chunk's operands (decayed queries and keys, the
+ * WY factors of the intra-chunk transform, the masked query-key scores) as a
+ * package, then the serial state pass of every piece, which reads them.
+ * Returns KDA_ERR_WORKSPACE when ws_bytes is short.
  */
 int kda_segment_forward(const int32_t *plan, const int32_t *plan_dev, int32_t H,
                         const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,

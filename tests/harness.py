@@ -54,16 +54,16 @@ def gpu_forward(inp, scale=1.0, path="fused", seg_bounds=None, dev=None):
     plan = kda.kda_plan_segments(inp.cu_seqlens, S, seg_bounds)
     plan_dev = kda.upload_plan(plan)
     off = kda.kda_workspace_layout(plan, H)
-    ws = torch.empty(off[5], dtype=torch.uint8, device="cuda")
+    ws = torch.empty(off[6], dtype=torch.uint8, device="cuda")
     o = torch.empty((T, H, V), dtype=torch.bfloat16, device="cuda")
     fin = torch.empty((N, H, K, V), dtype=torch.float32, device="cuda")
     if path == "fused":
         kda.kda_forward_segmented(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
                                   dev["h0"], scale, o, fin, ws)
         view = lambda a, shape: ws[a:a + 4 * int(np.prod(shape))].view(torch.float32).view(*shape)
-        A = view(off[2], (S, H, K, K))
-        B = view(off[3], (S, H, K, V))
-        S_in = view(off[4], (S, H, K, V))
+        A = view(off[3], (S, H, K, K))
+        B = view(off[4], (S, H, K, V))
+        S_in = view(off[5], (S, H, K, V))
     else:
         A = torch.empty((S, H, K, K), dtype=torch.float32, device="cuda")
         B = torch.empty((S, H, K, V), dtype=torch.float32, device="cuda")

@@ -115,10 +115,10 @@ def test_summary_workspace_matches_the_pages(kda):
     assert (w.segments, w.heads) == (S, H)
     plan = kda.kda_plan_segments(_cu(w.seqlens), S)
     off = kda.kda_workspace_layout(plan, H)
-    a_bytes, b_bytes = off[3] - off[2], off[4] - off[3]
+    a_bytes, b_bytes = off[4] - off[3], off[5] - off[4]
     assert a_bytes + b_bytes == want == 256 * 2 ** 20
     assert a_bytes == S * H * K * K * 4 and b_bytes == S * H * K * V * 4
-    assert kda.kda_workspace_bytes(plan, H) == off[5]
+    assert kda.kda_workspace_bytes(plan, H) == off[6]
     assert all(o % 256 == 0 for o in off)
 
 
