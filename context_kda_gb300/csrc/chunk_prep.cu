@@ -38,14 +38,18 @@ constexpr uint32_t OFF_MISC = 163840;
 constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
 constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
 constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 1792;
+// Raw rows of a unit, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of 64 rows
+// x 128 bytes): q, k, v as two 64-column boxes each in their own region (the next unit's copy is
+// issued once this unit's rows are in registers), g as four 32-column boxes over M / T (issued
+// once the inverse is done).
+constexpr uint32_t BOX = 8192;
+constexpr uint32_t OFF_SQKV = 166912;
+constexpr uint32_t STG_Q = OFF_SQKV, STG_K = OFF_SQKV + 2 * BOX, STG_V = OFF_SQKV + 4 * BOX, STG_G = OFF_MT;
+constexpr uint32_t SMEM_BYTES = OFF_SQKV + 6 * BOX;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
 constexpr uint32_t T128 = 32768, T64 = 16384;
 constexpr uint32_t OFF_M32 = OFF_MT, OFF_T32 = OFF_MT + 16384;
-// Raw rows of a unit, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of 64 rows
-// x 128 bytes): q, k, v as two 64-column boxes each, g as four 32-column boxes.
-constexpr uint32_t BOX = 8192;
-constexpr uint32_t STG_Q = OFF_KQ, STG_K = OFF_KQ + 2 * BOX, STG_V = OFF_KQ + 4 * BOX, STG_G = OFF_MT;
+static_assert(OFF_MISC + 1792 <= OFF_SQKV && OFF_SQKV % 1024 == 0, "staging region");
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols)
@@ -105,7 +109,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;
-    __shared__ __align__(8) uint64_t s_ldbar;
+    __shared__ __align__(8) uint64_t s_ldbar;    // q, k, v rows landed
+    __shared__ __align__(8) uint64_t s_gbar;     // g rows landed
     __shared__ __align__(8) uint64_t s_hbar[2];
     __shared__ uint32_t s_tmem;
     unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -118,11 +123,12 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;          // TMEM lane quadrant, column half
     const bool worker = tid < NWORK, issuer = tid == ISSUER;
-    const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar);
+    const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar), gbar = smem_u32(&s_gbar);
 
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(ldbar, 1);
+        mbar_init(gbar, 1);
         for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s_hbar[i]), 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
@@ -145,28 +151,38 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     };
     // Rows of unit u (q, k, v, g) by tiled TMA copies; rows past the end of the tensor arrive as
     // zeros, rows past the chunk are masked when read.
-    auto issue_tma = [&](long long u) {
+    auto issue_qkv = [&](long long u) {
         int t0, L, h;
         rows_of(u, t0, L, h);
-        mbar_arrive_expect_tx(ldbar, 10u * BOX);
+        mbar_arrive_expect_tx(ldbar, 6u * BOX);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             tma_load_3d(sbase + STG_Q + half * BOX, &tm_q, half * 64, h, t0, ldbar);
             tma_load_3d(sbase + STG_K + half * BOX, &tm_k, half * 64, h, t0, ldbar);
             tma_load_3d(sbase + STG_V + half * BOX, &tm_v, half * 64, h, t0, ldbar);
         }
-#pragma unroll
-        for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0, ldbar);
     };
-    float beta_next = 0.f;
-    auto load_beta = [&](long long u) {
-        if (u >= u_end || tid >= 64) return;
+    auto issue_g = [&](long long u) {
         int t0, L, h;
         rows_of(u, t0, L, h);
-        beta_next = (tid < L) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
+        mbar_arrive_expect_tx(gbar, 4u * BOX);
+#pragma unroll
+        for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0, gbar);
     };
-    if (issuer && u_begin < u_end) issue_tma(u_begin);
-    load_beta(u_begin);
+    // the next unit's rows and beta, fetched while the current one is processed
+    float beta_next = 0.f;
+    int L_next = 0;
+    auto load_next = [&](long long u) {
+        if (u >= u_end) return;
+        int t0, h;
+        rows_of(u, t0, L_next, h);
+        if (tid < 64) beta_next = (tid < L_next) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
+    };
+    if (issuer && u_begin < u_end) {
+        issue_qkv(u_begin);
+        issue_g(u_begin);
+    }
+    load_next(u_begin);
 
     bool aborted = false;   // all workers agree on it (OR-reduced at barriers)
     bool bad = false;       // a bounded wait of this thread gave up
@@ -188,15 +204,12 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     if (worker) {
         int n = 0;
         for (long long u = u_begin; u < u_end && !aborted; ++u, ++n) {
-            int t0, L, h;
-            rows_of(u, t0, L, h);
-            (void)t0;
-            (void)h;
+            const int L = L_next;
             unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
 
             // ================= A: staged rows -> decayed keys / queries / values =====================
             {
-                if (!mbar_wait(ldbar, n & 1)) bad = true;
+                if (!mbar_wait_warp(gbar, n & 1)) bad = true;
                 // A1: log2-scaled cumulative decay per key channel, in place over the staged g
                 //     (32 rows per thread: load all, scan in registers, store once)
                 {
@@ -225,9 +238,10 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                     for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
                     bar_sync1(NWORK);
                 }
-                load_beta(u + 1);   // s_beta holds this unit's values now
+                load_next(u + 1);   // s_beta holds this unit's values now
                 // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
                 //     the lanes of a warp hold consecutive rows of one piece column
+                if (!mbar_wait_warp(ldbar, n & 1)) bad = true;
                 const int pr = tid & 63, pcg = tid >> 6;
                 float gam[4][8];
                 uint4 kw[4], qw[4], vw[4];
@@ -454,10 +468,14 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         // next unit's rows are staged as soon as W (the last reader of the staging regions) is done.
         bool ok = true;
         int n = 0;
-        int last_n = 0;   // unit count of the last staged copy
+        int last_qkv = 0, last_g = 0;   // unit counts of the last staged copies
         for (long long u = u_begin; u < u_end && ok; ++u, ++n) {
             const uint32_t par = n & 1;
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
+            if (u + 1 < u_end) {   // this unit's q, k, v rows are in registers
+                issue_qkv(u + 1);
+                last_qkv = n + 1;
+            }
             fence_after();
             {
                 const uint32_t id = idesc_bf16(128, 64);
@@ -471,6 +489,10 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 commit(mbar);
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_D]), par))) break;
+            if (u + 1 < u_end) {   // M and T (over the g staging) are consumed
+                issue_g(u + 1);
+                last_g = n + 1;
+            }
             fence_after();
             {
                 // W^T = Kt^T T'^T (3-term; Kt^T is the row-major Kt tile read MN-major)
@@ -491,16 +513,11 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                                  sdesc(sbase + OFF_TP + ps * 8192 + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
                 commit(mbar);
             }
-            if (u + 1 < u_end) {
-                // mbar phases per unit: [KK; QK], then W / Ut (pending now)
-                if (!(ok = mbar_wait(mbar, (2 * n + 1) & 1))) break;
-                issue_tma(u + 1);
-                last_n = n + 1;
-            }
         }
         if (!ok) {
             atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
-            mbar_wait(ldbar, last_n & 1);   // bounded: let the last staged copy land
+            mbar_wait(ldbar, last_qkv & 1);   // bounded: let the last staged copies land
+            mbar_wait(gbar, last_g & 1);
         }
     }
     if (worker && aborted && tid == 0) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
