@@ -19,7 +19,9 @@
 // stage the next unit's rows.  The products that feed the state (Kt Kh^T, W) use a three-term
 // bf16 split (hi*hi + hi*lo + lo*hi, ~2^-17 relative); Ut two terms (V is exact in bf16).
 // Results go straight from registers to the unit's package in the workspace with 16-byte
-// stores, each tile already in the layout the state pass's MMAs read.
+// stores, each tile already in the layout the state pass's MMAs read.  A unit's W and Ut products
+// run while the workers start the next unit; the workers read them back from TMEM and store them
+// while they wait for the next unit's [KK; QK].
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -30,8 +32,9 @@ using namespace tc;
 
 // ---- shared-memory map (bytes from the 1024-byte aligned dynamic base) ------------------------
 constexpr uint32_t OFF_KQ = 0;        // [Kt; Qt]: rows r / 64 + r, cols k, CS 2048, hi | lo       2 x 32768
-constexpr uint32_t OFF_MT = 65536;    // M (fp32 64 x 64) + T (fp32 64 x 64, at +16384)
+constexpr uint32_t OFF_MT = 65536;    // g staging (four 32-column boxes)
 constexpr uint32_t OFF_KH = 98304;    // Kh: rows i (64), cols k, CS 1024, hi | lo                2 x 16384
+//   then (once [KK; QK] has read it) M (fp32 64 x 64) + T (fp32 64 x 64, at +16384)
 constexpr uint32_t OFF_VT = 131072;   // V: rows r (64), cols v, CS 1024                            16384
 constexpr uint32_t OFF_TP = 147456;   // T': rows r, cols i, CS 1024, hi | lo                      2 x 8192
 constexpr uint32_t OFF_MISC = 163840;
@@ -39,16 +42,15 @@ constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
 constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
 constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
 // Raw rows of a unit, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of 64 rows
-// x 128 bytes): q, k, v as two 64-column boxes each in their own region (the next unit's copy is
-// issued once this unit's rows are in registers), g as four 32-column boxes over M / T (issued
-// once the inverse is done).
+// x 128 bytes) into their own regions: q, k, v as two 64-column boxes each, g as four 32-column
+// boxes.  The next unit's copies are issued once this unit's rows are in registers.
 constexpr uint32_t BOX = 8192;
 constexpr uint32_t OFF_SQKV = 166912;
 constexpr uint32_t STG_Q = OFF_SQKV, STG_K = OFF_SQKV + 2 * BOX, STG_V = OFF_SQKV + 4 * BOX, STG_G = OFF_MT;
 constexpr uint32_t SMEM_BYTES = OFF_SQKV + 6 * BOX;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
 constexpr uint32_t T128 = 32768, T64 = 16384;
-constexpr uint32_t OFF_M32 = OFF_MT, OFF_T32 = OFF_MT + 16384;
+constexpr uint32_t OFF_M32 = OFF_KH, OFF_T32 = OFF_KH + 16384;
 static_assert(OFF_MISC + 1792 <= OFF_SQKV && OFF_SQKV % 1024 == 0, "staging region");
 
 // ---- TMEM columns --------------------------------------------------------------------------
@@ -201,6 +203,32 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         return ab;
     };
 
+    // W^T and Ut^T of a unit (already complete) from TMEM into its package, one at a time
+    auto store_w_ut = [&](long long u) {
+        unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
+        {
+            float x[32];
+            tmem_ld32(tl + TM_W + hw * 32, x);   // W^T[k = c_lane][r = hw*32 + j]
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                uint4 hi, lo;
+                split8(x + 8 * m, hi, lo);
+                const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
+                *reinterpret_cast<uint4 *>(pk + PK_W + off) = hi;
+                *reinterpret_cast<uint4 *>(pk + PK_W + T64 + off) = lo;
+            }
+        }
+        {
+            float x[32];
+            tmem_ld32(tl + TM_U + hw * 32, x);   // Ut^T[c = c_lane][r = hw*32 + j]
+            // Ut^T as [hw][m][c] float4 groups: a warp's store (and the state pass's load) of one
+            // group covers 512 contiguous bytes
+            float4 *ut = reinterpret_cast<float4 *>(pk + PK_U) + hw * 8 * 128 + c_lane;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) ut[m * 128] = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+        }
+    };
+
     if (worker) {
         int n = 0;
         for (long long u = u_begin; u < u_end && !aborted; ++u, ++n) {
@@ -261,7 +289,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                     qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + bo) : z;
                     vw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
                 }
-                bar_sync1(NWORK);   // staging consumed: every region may be rewritten from here
+                bar_sync1(NWORK);   // staging consumed
+                if (n > 0) wait_mma();   // the previous unit's W / Ut have read the operand tiles
                 // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16 in shared memory; Qt hi and Kh
                 //     hi/lo also into the package (lanes hold consecutive rows: 512 contiguous bytes)
 #pragma unroll
@@ -297,6 +326,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 aborted = handoff(HO_A);   // -> [KK; QK]
             }
             if (aborted) break;
+            if (n > 0) store_w_ut(u - 1);   // while [KK; QK] runs
 
             // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
             wait_mma();
@@ -430,51 +460,26 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             }
                 aborted = handoff(HO_D);   // -> W^T = Kt^T T'^T, Ut^T = V^T T'^T
             }
-            if (aborted) break;
 
-            // ================= E: W and Ut from TMEM into the package ================================
-            {
-                wait_mma();
-                uint32_t wd[32], ud[32];
-                tmem_ld32_nowait(tl + TM_W + hw * 32, wd);   // W^T[k = c_lane][r = hw*32 + j]
-                tmem_ld32_nowait(tl + TM_U + hw * 32, ud);   // Ut^T[c = c_lane][r = hw*32 + j]
-                tmem_wait_ld();
-                reg_fence32(wd);
-                reg_fence32(ud);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(wd[8 * m + e]);
-                    uint4 hi, lo;
-                    split8(x, hi, lo);
-                    const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
-                    *reinterpret_cast<uint4 *>(pk + PK_W + off) = hi;
-                    *reinterpret_cast<uint4 *>(pk + PK_W + T64 + off) = lo;
-                }
-                // Ut^T as [hw][m][c] float4 groups: a warp's store (and the state pass's load) of one
-                // group covers 512 contiguous bytes
-                float4 *ut = reinterpret_cast<float4 *>(pk + PK_U) + hw * 8 * 128 + c_lane;
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    ut[m * 128] = make_float4(__uint_as_float(ud[4 * m]), __uint_as_float(ud[4 * m + 1]),
-                                        __uint_as_float(ud[4 * m + 2]), __uint_as_float(ud[4 * m + 3]));
-                fence_before();
-                aborted = bar_or1(NWORK, bad);
-            }
+        }
+        if (!aborted && n > 0) {   // the last unit's W / Ut
+            wait_mma();
+            if (!bar_or1(NWORK, bad)) store_w_ut(u_end - 1);
+            else aborted = true;
         }
     } else if (issuer) {
-        // Issuer: per unit, [KK; QK] once the operand tiles are in, then W and Ut once T' is; the
-        // next unit's rows are staged as soon as W (the last reader of the staging regions) is done.
+        // Issuer: per unit, the next unit's rows and [KK; QK] once the operand tiles are in, then W
+        // and Ut once T' is.
         bool ok = true;
         int n = 0;
         int last_qkv = 0, last_g = 0;   // unit counts of the last staged copies
         for (long long u = u_begin; u < u_end && ok; ++u, ++n) {
             const uint32_t par = n & 1;
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
-            if (u + 1 < u_end) {   // this unit's q, k, v rows are in registers
+            if (u + 1 < u_end) {   // this unit's rows are in registers
                 issue_qkv(u + 1);
-                last_qkv = n + 1;
+                issue_g(u + 1);
+                last_qkv = last_g = n + 1;
             }
             fence_after();
             {
@@ -489,10 +494,6 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 commit(mbar);
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_D]), par))) break;
-            if (u + 1 < u_end) {   // M and T (over the g staging) are consumed
-                issue_g(u + 1);
-                last_g = n + 1;
-            }
             fence_after();
             {
                 // W^T = Kt^T T'^T (3-term; Kt^T is the row-major Kt tile read MN-major)
