@@ -216,7 +216,7 @@ def run_ours(args, w, rank, world, local_rank):
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     n_cont, n_fin = int(plan[8]), int(plan[10])
-    launches_per_step = 2 + (1 if (n_cont + n_fin) > 0 else 0)
+    launches_per_step = 3 + (1 if (n_cont + n_fin) > 0 else 0)   # prep, state, compose (+ fix-up)
 
     def step(evs=None):
         if evs:
