@@ -131,13 +131,13 @@ bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t
 }
 
 bool encode_rows_3d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
-                    uint32_t inner)
+                    uint32_t inner, uint32_t box_rows)
 {
     auto fn = tmap_encode_fn();
     if (!fn || T <= 0) return false;
     const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     const cuuint64_t strides[2] = {128ull * elem, 128ull * elem * static_cast<cuuint64_t>(H)};
-    const cuuint32_t box[3] = {inner, 1, 64};
+    const cuuint32_t box[3] = {inner, 1, box_rows};
     const cuuint32_t es[3] = {1, 1, 1};
     return fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

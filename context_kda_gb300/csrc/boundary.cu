@@ -16,8 +16,11 @@
 // qhat tile arrives by bulk copy into a staging buffer, is split likewise, and
 // D = Qhat S_in is formed on the tcgen05 tensor cores (M = N = K = 128, three
 // products accumulated in FP32 in TMEM).  The copy of the next item is issued
-// as soon as the staging buffer has been read, and the output rows are fetched
-// while the tensor core runs.
+// as soon as the staging buffer has been read.  A full 128-row output tile
+// moves through a shared-memory buffer by tiled TMA (128-byte swizzle): loaded
+// one unit ahead, updated in place by the epilogue, written back with one TMA
+// store.  Ragged tail tiles and final states are read and written by the
+// threads directly, so nothing outside a record is ever stored.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -33,7 +36,10 @@ constexpr uint32_t TILE_B = 32768, TILE_A = 16 * LBO_A;
 constexpr uint32_t OFF_B = 0;                      // S_in^T hi | lo
 constexpr uint32_t OFF_A = 2 * TILE_B;             // Qhat hi | lo
 constexpr uint32_t OFF_STG = OFF_A + 2 * TILE_A;   // fp32 staging: 128 rows x 512 bytes
-constexpr uint32_t SMEM_BYTES = OFF_STG + 65536;
+constexpr uint32_t OFF_OB = 197632;                // bf16 output tile: two swizzled 64-column boxes
+constexpr uint32_t SMEM_BYTES = OFF_OB + 32768;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
+static_assert(OFF_STG + 65536 <= OFF_OB && OFF_OB % 1024 == 0, "output tile buffer");
 constexpr uint32_t TM_COLS = 128;
 
 __device__ int g_boundary_status;
@@ -85,11 +91,12 @@ __device__ __forceinline__ void split_store4(unsigned char *base, uint32_t off_h
 __global__ void __launch_bounds__(256, 1)
 boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long long n_units,
             const float *__restrict__ S_in, const float *__restrict__ qhat, const float *__restrict__ afin,
-            uint16_t *__restrict__ o, float *__restrict__ final_state)
+            uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o)
 {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ __align__(8) uint64_t s_ldbar;
+    __shared__ __align__(8) uint64_t s_obar;   // output tile landed
     __shared__ uint32_t s_tmem;
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,8 +105,9 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     const long long u_begin = n_units * blockIdx.x / gridDim.x;
     const long long u_end = n_units * (blockIdx.x + 1) / gridDim.x;
     if (u_begin >= u_end) return;
+    unsigned char *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar);
+    const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar), obar = smem_u32(&s_obar);
     const float *stg = reinterpret_cast<const float *>(smem + OFF_STG);
 
     // cursor of the first unit
@@ -119,18 +127,27 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(ldbar, 1);
+        mbar_init(obar, 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tbase = s_tmem;
-    uint32_t ld_phase = 0, mma_phase = 0;
-    bool ok = true, pending = false;
+    uint32_t ld_phase = 0, mma_phase = 0, o_phase = 0;
+    bool ok = true, pending = false, o_pending = false;
 
     auto fetch_S = [&](int h, int seg) {
         mbar_arrive_expect_tx(ldbar, 65536u);
         bulk_g2s(sbase + OFF_STG, S_in + (static_cast<size_t>(seg) * H + h) * KD * VD, 65536u, ldbar);
+    };
+    // a unit whose output tile goes through the buffer: 128 continuing tokens
+    auto tiled = [&](const Rec &r, int tile) { return r.seq < 0 && r.rows_total - tile * TR >= TR; };
+    auto fetch_o = [&](const Rec &r, int tile, int h) {   // thread 0
+        mbar_arrive_expect_tx(obar, 32768u);
+        const int z = r.t_first + tile * TR;
+        tma_load_3d(sbase + OFF_OB, &tm_o, 0, h, z, obar);
+        tma_load_3d(sbase + OFF_OB + 16384, &tm_o, 64, h, z, obar);
     };
     auto fetch_tile = [&](const Rec &r, int tile) {
         const uint32_t rows = static_cast<uint32_t>(min(TR, r.rows_total - tile * TR));
@@ -142,6 +159,10 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     int key_h = -1, key_seg = -1;
     if (tid == 0) fetch_S(c.h, ri.seg);
     pending = true;
+    if (tiled(ri, c.tile)) {
+        if (tid == 0) fetch_o(ri, c.tile, c.h);
+        o_pending = true;
+    }
 
     for (long long u = u_begin; u < u_end; ++u) {
         if (c.h != key_h || ri.seg != key_seg) {
@@ -216,9 +237,11 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
         }
         pending = more;
 
-        // fetch this thread's destination row piece while the tensor core works
+        // fetch this thread's destination row piece while the tensor core works (units whose
+        // output tile is not in the buffer)
+        const bool tl_unit = tiled(ri, c.tile);
         const int r = quad * 32 + lane;
-        const bool live = r < rows;
+        const bool live = r < rows && !tl_unit;
         uint4 ow[8];
         float4 fw[16];
         uint4 *odst = nullptr;
@@ -252,6 +275,24 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
                 d[32 + j] = d1[j];
             }
         }
+        if (tl_unit) {   // output tile in the buffer: update in place (row r, this half's box)
+            ok &= mbar_wait(obar, o_phase++ & 1);
+            o_pending = false;
+            unsigned char *box = smem + OFF_OB + hw * 16384;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                uint4 *p = reinterpret_cast<uint4 *>(box + sw128(r, m));
+                const uint4 w4 = *p;
+                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+                uint32_t nw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    nw[q] = bf16x2_bits(__uint_as_float(ww[q] << 16) + d[8 * m + 2 * q],
+                                        __uint_as_float(ww[q] & 0xFFFF0000u) + d[8 * m + 2 * q + 1]);
+                *p = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+            }
+            fence_async_smem();
+        }
         if (live && ok) {
             if (odst) {
 #pragma unroll
@@ -273,14 +314,27 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
         }
         fence_before();
         if (!__syncthreads_and(ok)) break;
+        if (tid == 0 && (tl_unit || (more && tiled(nri, nc.tile)))) {
+            if (tl_unit) {   // write the tile back; the buffer is free once the store has read it
+                const int z = ri.t_first + c.tile * TR;
+                tma_store_3d(&tm_o, 0, c.h, z, sbase + OFF_OB);
+                tma_store_3d(&tm_o, 64, c.h, z, sbase + OFF_OB + 16384);
+                bulk_commit_group();
+                bulk_wait_read_all();
+            }
+            if (more && tiled(nri, nc.tile)) fetch_o(nri, nc.tile, nc.h);
+        }
+        if (more && tiled(nri, nc.tile)) o_pending = true;
         c = nc;
         ri = nri;
     }
+    if (tid == 0) bulk_wait_all();   // output tiles stored before the CTA exits
     if (!__syncthreads_and(ok)) {
         // a wait gave up: record it, and let any copy still in flight land before the CTA exits
         if (tid == 0) {
             atomicExch(&g_boundary_status, KDA_ERR_TIMEOUT);
             if (pending) mbar_wait(ldbar, ld_phase & 1);
+            if (o_pending) mbar_wait(obar, o_phase & 1);
             mbar_wait(mbar, mma_phase & 1);
         }
         __syncthreads();
@@ -304,11 +358,14 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
     if (per_head > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const long long n_units = per_head * H;
     const long long grid = n_units < sm_count() ? n_units : sm_count();
+    CUtensorMap to{};   // only full 128-row tiles use it, so T < 128 never reads it
+    if (pv.T() >= TR && !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, TR))
+        return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(boundary_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_BYTES));
+                                           static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    boundary_tc<<<static_cast<unsigned>(grid), 256, SMEM_BYTES, stream>>>(
-        plan_dev, H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state);
+    boundary_tc<<<static_cast<unsigned>(grid), 256, SMEM_ALLOC, stream>>>(
+        plan_dev, H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to);
     return cudaGetLastError();
 }
 

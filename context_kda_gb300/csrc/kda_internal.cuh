@@ -84,9 +84,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows);
 
 // Tensor map of a [T][H][128] tensor (inner dimension first) with a box of 'inner' columns x 1
-// head x 64 rows and the 128-byte swizzle; elem = element bytes.
+// head x box_rows rows and the 128-byte swizzle; elem = element bytes.
 bool encode_rows_3d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
-                    uint32_t inner);
+                    uint32_t inner, uint32_t box_rows = 64);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_dev, int H,

@@ -161,6 +161,14 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, uin
                  : "memory");
 }
 
+// Tiled TMA store of one 3-D box from shared memory to (x, y, z) (non-negative coordinates).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int x, int y, int z, uint32_t src_smem)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(src_smem)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
