@@ -110,17 +110,29 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar), obar = smem_u32(&s_obar);
     const float *stg = reinterpret_cast<const float *>(smem + OFF_STG);
 
-    // cursor of the first unit
+    // cursor of the first unit: each warp scans the records' tile counts 32 at a time (inclusive
+    // prefix sums over the lanes) and takes the first record whose running count passes the unit
     Cursor c{static_cast<int>(u_begin / units_per_head), 0, 0};
     {
         int rem = static_cast<int>(u_begin % units_per_head);
-        while (true) {
-            const int nt = rec_info(pv, H, c.h, c.rec).nt;
-            if (rem < nt) break;
-            rem -= nt;
-            ++c.rec;
+        for (int b = 0; b < n_rec; b += 32) {
+            const int i = b + lane;
+            const int nt = i >= n_rec ? 0 : (i < pv.n_cont() ? (pv.cont(i)[3] + TR - 1) / TR : 1);
+            int incl = nt;
+#pragma unroll
+            for (int sh = 1; sh < 32; sh <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, sh);
+                if (lane >= sh) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (rem < total) {
+                const int l = __ffs(__ballot_sync(0xffffffffu, incl > rem)) - 1;
+                c.rec = b + l;
+                c.tile = rem - __shfl_sync(0xffffffffu, incl - nt, l);
+                break;
+            }
+            rem -= total;
         }
-        c.tile = rem;
     }
     Rec ri = rec_info(pv, H, c.h, c.rec);
 

@@ -90,8 +90,12 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     const int flags = pc[PC_FLAGS], row0 = pc[PC_ROW], fin = pc[PC_FIN];
     const int64_t T_cont = pv.T_cont();
     const int nch = (len + CH - 1) / CH;
-    int c0 = 0;   // global index of the piece's first chunk (chunks are numbered piece by piece)
-    for (int i = 0; i < p; ++i) c0 += (pv.piece(i)[PC_LEN] + CH - 1) / CH;
+    // global index of the piece's first chunk (chunks are numbered piece by piece): each warp sums
+    // the earlier pieces' chunk counts, its lanes taking every 32nd piece
+    int c0 = 0;
+    for (int i = lane; i < p; i += 32) c0 += (pv.piece(i)[PC_LEN] + CH - 1) / CH;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) c0 += __shfl_xor_sync(0xffffffffu, c0, sh);
     auto pk_of = [&](int ci) {
         return pkg + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KDA_PACKAGE_BYTES;
     };
