@@ -44,7 +44,7 @@ bool layout(const int32_t *plan, int32_t H, size_t off[7])
     if (!plan_ok(plan) || H < 1) return false;
     const size_t h = static_cast<size_t>(H), K = kda::KD, V = kda::VD;
     const size_t sizes[6] = {
-        h * static_cast<size_t>(plan[KDA_PH_TCONT]) * K * 4,                 // qhat
+        h * static_cast<size_t>(plan[KDA_PH_TCONT]) * K * 2,                 // qhat (bf16)
         static_cast<size_t>(plan[KDA_PH_NFIN]) * h * K * K * 4,              // fin transitions
         static_cast<size_t>(plan[KDA_PH_NCHUNKS]) * h * KDA_PACKAGE_BYTES,   // chunk packages
         static_cast<size_t>(plan[KDA_PH_S]) * h * K * K * 4,                 // A
@@ -72,7 +72,7 @@ bool inputs_ok(const void *q, const void *k, const void *v, const float *g, cons
 kda::Workspace carve(void *ws, const size_t off[7])
 {
     char *b = static_cast<char *>(ws);
-    return kda::Workspace{reinterpret_cast<float *>(b + off[0]), reinterpret_cast<float *>(b + off[1]),
+    return kda::Workspace{reinterpret_cast<uint16_t *>(b + off[0]), reinterpret_cast<float *>(b + off[1]),
                           reinterpret_cast<unsigned char *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
                           reinterpret_cast<float *>(b + off[4]), reinterpret_cast<float *>(b + off[5])};
 }

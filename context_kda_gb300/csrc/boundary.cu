@@ -13,9 +13,10 @@
 // units share S_in[j].  The kernel is persistent: one CTA per SM takes a
 // contiguous run of units.  S_in[j] arrives by bulk copy and is split into a
 // bf16 hi/lo operand only when the run reaches a new (head, segment); each
-// qhat tile arrives by bulk copy into a staging buffer, is split likewise, and
-// D = Qhat S_in is formed on the tcgen05 tensor cores (M = N = K = 128, three
-// products accumulated in FP32 in TMEM).  The copy of the next item is issued
+// qhat tile (bf16) arrives by bulk copy into a staging buffer and is laid out
+// as the A operand, and D = Qhat S_in is formed on the tcgen05 tensor cores
+// (M = N = K = 128; qhat hi * S hi + qhat hi * S lo, FP32 in TMEM).  A final-
+// state transition (fp32) is split into hi/lo and takes the third product too.  The copy of the next item is issued
 // as soon as the staging buffer has been read.  A full 128-row output tile
 // moves through a shared-memory buffer by tiled TMA (128-byte swizzle): loaded
 // one unit ahead, updated in place by the epilogue, written back with one TMA
@@ -52,7 +53,7 @@ struct Cursor {
 
 struct Rec {
     int seg, seq, nt, rows_total, t_first;   // seq >= 0: final-state record
-    size_t src;                              // float offset of row 0 in qhat (or afin) for head h
+    size_t src;                              // element offset of row 0 in qhat (bf16) or afin (fp32), head h
 };
 
 __device__ __forceinline__ Rec rec_info(const PlanView &pv, int H, int h, int rec)
@@ -90,7 +91,7 @@ __device__ __forceinline__ void split_store4(unsigned char *base, uint32_t off_h
 
 __global__ void __launch_bounds__(256, 1)
 boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long long n_units,
-            const float *__restrict__ S_in, const float *__restrict__ qhat, const float *__restrict__ afin,
+            const float *__restrict__ S_in, const uint16_t *__restrict__ qhat, const float *__restrict__ afin,
             uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -163,9 +164,11 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     };
     auto fetch_tile = [&](const Rec &r, int tile) {
         const uint32_t rows = static_cast<uint32_t>(min(TR, r.rows_total - tile * TR));
-        const float *base = (r.seq < 0 ? qhat : afin) + r.src + static_cast<size_t>(tile) * TR * KD;
-        mbar_arrive_expect_tx(ldbar, rows * KD * 4);
-        bulk_g2s(sbase + OFF_STG, base, rows * KD * 4, ldbar);
+        const size_t e0 = r.src + static_cast<size_t>(tile) * TR * KD;
+        const void *base = r.seq < 0 ? static_cast<const void *>(qhat + e0) : static_cast<const void *>(afin + e0);
+        const uint32_t bytes = rows * KD * (r.seq < 0 ? 2u : 4u);
+        mbar_arrive_expect_tx(ldbar, bytes);
+        bulk_g2s(sbase + OFF_STG, base, bytes, ldbar);
     };
 
     int key_h = -1, key_seg = -1;
@@ -204,14 +207,26 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
         const int rows = min(TR, ri.rows_total - c.tile * TR);
         ok &= mbar_wait(ldbar, ld_phase++ & 1);
         pending = false;
-        // qhat tile (fp32 rows) -> operand (rows r, cols k) as bf16 hi/lo; rows past the record are zero
+        if (ri.seq < 0) {
+            // qhat tile (bf16 rows) -> operand (rows r, cols k); rows past the record are zero.  Lanes
+            // take consecutive 8-column pieces of a row.
+            const unsigned char *sb = smem + OFF_STG;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int id = tid + 256 * i, r = id >> 5, c4 = id & 31;   // lanes: consecutive 4-column pieces
-            const float4 x = r < rows ? *reinterpret_cast<const float4 *>(stg + r * KD + c4 * 4)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-            const uint32_t off = cm_off(r, c4 * 4, LBO_A);
-            split_store4(smem, OFF_A + off, OFF_A + TILE_A + off, x);
+            for (int i = 0; i < 8; ++i) {
+                const int id = tid + 256 * i, r = id >> 4, c8 = id & 15;
+                const uint4 x = r < rows ? *reinterpret_cast<const uint4 *>(sb + r * 256 + c8 * 16)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(smem + OFF_A + cm_off(r, c8 * 8, LBO_A)) = x;
+            }
+        } else {
+            // transition tile (fp32 rows) -> operand as bf16 hi/lo; lanes take consecutive 4-column pieces
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int id = tid + 256 * i, r = id >> 5, c4 = id & 31;
+                const float4 x = *reinterpret_cast<const float4 *>(stg + r * KD + c4 * 4);
+                const uint32_t off = cm_off(r, c4 * 4, LBO_A);
+                split_store4(smem, OFF_A + off, OFF_A + TILE_A + off, x);
+            }
         }
         fence_async_smem();
         fence_before();
@@ -239,8 +254,8 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
             }
             const uint32_t id = idesc_bf16(128, 128);
             const uint32_t aoff[3] = {0, 0, TILE_A}, boff[3] = {0, TILE_B, 0};
-#pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
+            const int terms = ri.seq < 0 ? 2 : 3;   // qhat is exact in bf16: no lo * hi product
+            for (int ps = 0; ps < terms; ++ps)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tbase, sdesc(sbase + OFF_A + aoff[ps] + kk * 2 * LBO_A, LBO_A),
@@ -360,7 +375,7 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
 }  // namespace
 
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
-                            const float *qhat, const float *afin, uint16_t *o, float *final_state,
+                            const uint16_t *qhat, const float *afin, uint16_t *o, float *final_state,
                             cudaStream_t stream)
 {
     const PlanView pv{plan_host};

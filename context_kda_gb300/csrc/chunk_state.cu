@@ -66,7 +66,7 @@ __device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, 
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ h0,
                const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o, float *__restrict__ A,
-               float *__restrict__ B, float *__restrict__ fin_state, float *__restrict__ qhat,
+               float *__restrict__ B, float *__restrict__ fin_state, uint16_t *__restrict__ qhat,
                float *__restrict__ afin)
 {
     extern __shared__ __align__(16) unsigned char base[];
@@ -238,36 +238,24 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 }
                 aborted = handoff(HO_X);   // -> next chunk's W X, Qt X (they overlap the stores below)
                 if (aborted) break;
-                // O^T[c][r] -> row-major O tile in the U^T region (free: its products have completed),
-                // then 16-byte coalesced stores
-                if (kind == 0) {
+                // O^T[c][r] -> row-major bf16 tile in the U^T region (free: its products have completed),
+                // then 16-byte coalesced stores: outputs for state columns, qhat for transition columns
+                {
                     uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_UT);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         so[(hw * 32 + j) * 128 + c_lane] = f32_to_bf16_bits(__uint_as_float(od[j]));
-                } else {
-                    float *so = reinterpret_cast<float *>(base + OFF_UT);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) so[(hw * 32 + j) * 128 + c_lane] = __uint_as_float(od[j]);
                 }
                 bar_sync1(NWORK);
-                if (kind == 0) {
+                uint16_t *const dst_row0 = kind == 0 ? o + (static_cast<size_t>(t0) * H + h) * VD
+                                                     : qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH) * KD;
+                const size_t row_stride = kind == 0 ? static_cast<size_t>(H) * VD : KD;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
-                        if (r < L)
-                            *reinterpret_cast<uint4 *>(o + (static_cast<size_t>(t0 + r) * H + h) * VD + c16 * 8) =
-                                *reinterpret_cast<const uint4 *>(base + OFF_UT + r * 256 + c16 * 16);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int id = tid + 256 * i, r = id >> 5, c32 = id & 31;
-                        if (r < L)
-                            *reinterpret_cast<uint4 *>(qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH + r) *
-                                                                  KD + c32 * 4) =
-                                *reinterpret_cast<const uint4 *>(base + OFF_UT + r * 512 + c32 * 16);
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
+                    if (r < L)
+                        *reinterpret_cast<uint4 *>(dst_row0 + r * row_stride + c16 * 8) =
+                            *reinterpret_cast<const uint4 *>(base + OFF_UT + r * 256 + c16 * 16);
                 }
                 bar_sync1(NWORK);   // the O tile is read before the next U^T overwrites it
             }
@@ -384,7 +372,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
 
 cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
                                const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
-                               float *qhat, float *afin, cudaStream_t stream)
+                               uint16_t *qhat, float *afin, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
@@ -403,7 +391,7 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const float *g, const float *beta, const float *h0, float scale,
                                  uint16_t *o, float *A, float *B, float *final_state,
-                                 float *qhat, float *afin, unsigned char *pkg, cudaStream_t stream)
+                                 uint16_t *qhat, float *afin, unsigned char *pkg, cudaStream_t stream)
 {
     cudaError_t err = launch_chunk_prep(plan_host, plan_dev, H, q, k, v, g, beta, scale, pkg, stream);
     if (err != cudaSuccess) return err;

@@ -59,7 +59,7 @@ enum { PC_START = 0, PC_LEN = 1, PC_SEQ = 2, PC_SEG = 3, PC_FLAGS = 4, PC_CONT =
 
 // Workspace regions resolved to typed device pointers.
 struct Workspace {
-    float *qhat;          // [H][T_cont][K]
+    uint16_t *qhat;       // [H][T_cont][K] bf16
     float *afin;          // [n_fin][H][K][K]
     unsigned char *pkg;   // [H][n_chunks][KDA_PACKAGE_BYTES]
     float *A;             // [S][H][K][K]
@@ -93,17 +93,17 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const float *g, const float *beta, const float *h0, float scale,
                                  uint16_t *o, float *A, float *B, float *final_state,
-                                 float *qhat, float *afin, unsigned char *pkg, cudaStream_t stream);
+                                 uint16_t *qhat, float *afin, unsigned char *pkg, cudaStream_t stream);
 cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                               const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
                               unsigned char *pkg, cudaStream_t stream);
 cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
                                const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
-                               float *qhat, float *afin, cudaStream_t stream);
+                               uint16_t *qhat, float *afin, cudaStream_t stream);
 cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
                            const float *B, const float *h0, float *S_in, cudaStream_t stream);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
-                            const float *qhat, const float *afin, uint16_t *o, float *final_state,
+                            const uint16_t *qhat, const float *afin, uint16_t *o, float *final_state,
                             cudaStream_t stream);
 
 }  // namespace kda
