@@ -13,13 +13,14 @@
 // preceding_transition).
 //
 // Mapping.  One CTA per (work item, head): 8 worker warps and an issuer warp.  The state lives
-// transposed in TMEM (lane c, column k) as an FP32 accumulator and, split into bf16 hi/lo, in
-// shared memory as the A operand of W X and Qt X.  Per chunk the chain is: (W X)^T = X^T W^T
-// (3-term) -> workers form U^T = Ut^T - (W X)^T and split it -> O^T += U^T QK^T (1-term),
-// X^T += U^T Kh (3-term) -> workers decay X and split it for the next chunk, then store O.
-// Qt X (1-term) runs right after W X.  The package arrives by bulk copies one chunk ahead
-// (W and Qt once Qt X has read the previous ones; QK, Kh and the decay double-buffered); Ut
-// goes straight into registers, also one chunk ahead.
+// transposed in TMEM (lane c, column k) twice: as an FP32 accumulator, and split into bf16 hi/lo
+// pairs as the A operand of W X and Qt X, which the tensor core reads from TMEM.  Per chunk the
+// chain is: (W X)^T = X^T W^T (3-term) -> workers form U^T = Ut^T - (W X)^T and split it into
+// TMEM -> O^T += U^T QK^T (1-term), X^T += U^T Kh (3-term) -> workers decay X and split it for
+// the next chunk, then stage O in shared memory for a tiled TMA store.  Qt X (1-term) runs right
+// after W X.  Both package parts are double-buffered and arrive by bulk copies issued one chunk
+// ahead; Ut goes straight into registers, also one chunk ahead.  Keeping both A operands in TMEM
+// leaves shared-memory bandwidth to the B operands and the copies.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -29,14 +30,15 @@ namespace {
 using namespace tc;
 
 // ---- shared-memory map (bytes from the dynamic base; bf16 tiles, hi then lo where split) ------
-constexpr uint32_t OFF_XT = 0;          // X^T: rows c (128), cols k (128), CS 2048, hi | lo   2 x 32768
-constexpr uint32_t OFF_P1 = 65536;      // package bytes [PK_W, PK_P1_END): W hi | lo, Qt hi   49152
+constexpr uint32_t P1_BYTES = PK_P1_END;          // package bytes [PK_W, PK_P1_END): W hi | lo, Qt hi
+constexpr uint32_t OFF_P1 = 0;                     // two buffers of P1_BYTES
 constexpr uint32_t P2_BYTES = PK_P2_END - PK_QK;   // QK, Kh hi | lo, exp(Gamma_C)          41472
-constexpr uint32_t OFF_P2 = OFF_P1 + PK_P1_END;    // two buffers of P2_BYTES
-constexpr uint32_t OFF_UT = OFF_P2 + 2 * P2_BYTES;  // U^T: rows c, cols r (64), CS 2048, hi | lo;
-                                                    // then the row-major O tile for the stores
-constexpr uint32_t SMEM_BYTES = OFF_UT + 32768;
-constexpr uint32_t T128 = 32768, T64 = 16384;
+constexpr uint32_t OFF_P2 = OFF_P1 + 2 * P1_BYTES;  // two buffers of P2_BYTES
+constexpr uint32_t OFF_OB = OFF_P2 + 2 * P2_BYTES;  // O tile: rows r (64), two 64-column boxes of
+                                                    // 128-byte rows, 128-byte swizzle     2 x 8192
+constexpr uint32_t SMEM_BYTES = OFF_OB + 16384;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // the base is rounded up to 1024 bytes
+constexpr uint32_t T64 = 16384;
 // offsets inside a P2 buffer
 constexpr uint32_t P2_QK = 0, P2_KH = PK_KH - PK_QK, P2_GC = PK_GC - PK_QK;
 
@@ -44,7 +46,11 @@ constexpr uint32_t P2_QK = 0, P2_KH = PK_KH - PK_QK, P2_GC = PK_GC - PK_QK;
 constexpr uint32_t TM_WX = 0;     // (W X)^T (64 cols)
 constexpr uint32_t TM_O = 64;     // O^T (64 cols)
 constexpr uint32_t TM_X = 128;    // X^T (128 cols)
-constexpr uint32_t TM_COLS = 256;
+constexpr uint32_t TM_XH = 256;   // X^T bf16 hi as packed pairs: column k/2 holds k, k + 1 (64 cols)
+constexpr uint32_t TM_XL = 320;   // X^T bf16 lo, the same way (64 cols)
+constexpr uint32_t TM_UH = 384;   // U^T bf16 hi as packed pairs: column r/2 holds r, r + 1 (32 cols)
+constexpr uint32_t TM_UL = 416;   // U^T bf16 lo (32 cols)
+constexpr uint32_t TM_COLS = 512;
 
 constexpr int NWORK = 256;             // worker threads
 constexpr int NTHREADS = NWORK + 32;   // plus the issuer warp
@@ -53,30 +59,32 @@ enum { HO_X = 0, HO_U = 1 };           // worker -> issuer handoffs of a chunk
 
 __device__ int g_state_status;   // set to KDA_ERR_TIMEOUT when a bounded wait expires
 
-// Writes 8 consecutive values as bf16 hi and lo (two 16-byte stores).
-__device__ __forceinline__ void st_split8(unsigned char *hi, unsigned char *lo, const float *x)
+// Splits 32 consecutive values (k0 .. k0 + 31 of this thread's TMEM lane) into packed bf16 hi / lo
+// pairs and stores them at columns k0 / 2 .. k0 / 2 + 15 of the hi and lo operand copies.
+__device__ __forceinline__ void tmem_st_split32(uint32_t t_hi, uint32_t t_lo, const float (&x)[32])
 {
-    uint32_t h[4], l[4];
+    uint32_t h[16], l[16];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], h[p], l[p]);
-    *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+    for (int p = 0; p < 16; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], h[p], l[p]);
+    tmem_st16_nowait(t_hi, h);
+    tmem_st16_nowait(t_lo, l);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ h0,
                const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o, float *__restrict__ A,
                float *__restrict__ B, float *__restrict__ fin_state, uint16_t *__restrict__ qhat,
-               float *__restrict__ afin)
+               float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
+               const __grid_constant__ CUtensorMap tm_q)
 {
-    extern __shared__ __align__(16) unsigned char base[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;      // W X, then the output / state products
-    __shared__ __align__(8) uint64_t s_mbar_o;    // Qt X (W and Qt read)
-    __shared__ __align__(8) uint64_t s_pbar1;     // package part 1 landed
+    __shared__ __align__(8) uint64_t s_pbar1[2];  // package part 1 landed, per buffer
     __shared__ __align__(8) uint64_t s_pbar2[2];  // package part 2 landed, per buffer
     __shared__ __align__(8) uint64_t s_hbar[2];   // worker -> issuer handoffs
     __shared__ uint32_t s_tmem;
-    const uint32_t sbase = smem_u32(base);
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;   // 128-byte swizzle atoms
+    unsigned char *const base = smem_raw + (sbase - smem_u32(smem_raw));
 
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -96,16 +104,14 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     for (int i = lane; i < p; i += 32) c0 += (pv.piece(i)[PC_LEN] + CH - 1) / CH;
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) c0 += __shfl_xor_sync(0xffffffffu, c0, sh);
-    auto pk_of = [&](int ci) {
-        return pkg + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KDA_PACKAGE_BYTES;
-    };
-    const uint32_t mbar = smem_u32(&s_mbar), mbar_o = smem_u32(&s_mbar_o), pbar1 = smem_u32(&s_pbar1);
+    const unsigned char *const pk0 = pkg + (static_cast<size_t>(h) * pv.n_chunks() + c0) * KDA_PACKAGE_BYTES;
+    auto pk_of = [&](int ci) { return pk0 + static_cast<size_t>(ci) * KDA_PACKAGE_BYTES; };
+    const uint32_t mbar = smem_u32(&s_mbar);
 
     if (tid == 0) {
         mbar_init(mbar, 1);
-        mbar_init(mbar_o, 1);
-        mbar_init(pbar1, 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s_pbar1[i]), 1);
             mbar_init(smem_u32(&s_pbar2[i]), 1);
             mbar_init(smem_u32(&s_hbar[i]), 1);
         }
@@ -120,8 +126,9 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
 
     // package parts by bulk copy (issuer thread)
     auto load_p1 = [&](int ci) {
-        mbar_arrive_expect_tx(pbar1, PK_P1_END);
-        bulk_g2s(sbase + OFF_P1, pk_of(ci) + PK_W, PK_P1_END, pbar1);
+        const uint32_t bar = smem_u32(&s_pbar1[ci & 1]);
+        mbar_arrive_expect_tx(bar, P1_BYTES);
+        bulk_g2s(sbase + OFF_P1 + (ci & 1) * P1_BYTES, pk_of(ci) + PK_W, P1_BYTES, bar);
     };
     auto load_p2 = [&](int ci) {
         const uint32_t bar = smem_u32(&s_pbar2[ci & 1]);
@@ -141,11 +148,10 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         ++phase;
         fence_after();
     };
-    // Workers hand a set of shared-memory operands over to the issuer: every writer fences its
-    // generic-proxy stores for the tensor core, the workers meet on named barrier 1 (OR-reducing
-    // their wait failures, so all of them take the same abort decision), and one of them arrives.
+    // Workers hand a set of TMEM operands over to the issuer: every writer has waited for its TMEM
+    // stores and fences them, the workers meet on named barrier 1 (OR-reducing their wait failures,
+    // so all of them take the same abort decision), and one of them arrives.
     auto handoff = [&](int which) -> bool {
-        fence_async_smem();
         fence_before();
         const bool ab = bar_or1(NWORK, bad);
         if (!ab && tid == 0) mbar_arrive(smem_u32(&s_hbar[which]));
@@ -162,7 +168,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     };
 
     if (worker) {
-        // ---- piece start: X^T into TMEM (fp32) and its bf16 split into shared memory
+        // ---- piece start: X^T into TMEM, fp32 and as its bf16 split
         {
             const bool from_h0 = kind == 0 && (flags & KDA_PIECE_FIRST) && h0 != nullptr;
             const float *src = h0 + (static_cast<size_t>(seq) * H + h) * KD * VD;
@@ -176,11 +182,9 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                     x[j] = kind == 1 ? (kk == c_lane ? 1.f : 0.f) : (from_h0 ? src[kk * VD + c_lane] : 0.f);
                 }
                 tmem_st32(tl + TM_X + k0, x);
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
-                              base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
+                tmem_st_split32(tl + TM_XH + k0 / 2, tl + TM_XL + k0 / 2, x);
             }
+            tmem_wait_st();
             load_ut(0);
             aborted = handoff(HO_X);   // -> W X, Qt X
         }
@@ -201,26 +205,22 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                     d[4 * m + 2] = u4.z - d[4 * m + 2];
                     d[4 * m + 3] = u4.w - d[4 * m + 3];
                 }
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
-                    st_split8(base + OFF_UT + off, base + OFF_UT + T64 + off, d + 8 * m);
-                }
+                tmem_st_split32(tl + TM_UH + hw * 16, tl + TM_UL + hw * 16, d);
+                tmem_wait_st();
+                if (tid == 0) bulk_wait_read_all();   // the previous O tile has left shared memory
                 aborted = handoff(HO_U);   // -> O^T += U^T QK^T, X^T += U^T Kh
             }
             if (aborted) break;
             load_ut(ci + 1);
 
-            // ================= outputs (or qhat) to HBM; new X^T split into shared memory =============
+            // ================= new X^T and its split into TMEM; outputs (or qhat) to HBM ==============
             wait_mma();
             {
-                // O^T and this thread's half of X^T (X + Kh^T U) in one batch of TMEM reads
-                uint32_t od[32], xa[32], xb[32];
-                tmem_ld32_nowait(tl + TM_O + hw * 32, od);   // O^T[c][r = hw*32 + j]
+                // this thread's half of X^T (X + Kh^T U) in one batch of TMEM reads
+                uint32_t xa[32], xb[32];
                 tmem_ld32_nowait(tl + TM_X + hw * 64, xa);
                 tmem_ld32_nowait(tl + TM_X + hw * 64 + 32, xb);
                 tmem_wait_ld();
-                reg_fence32(od);
                 reg_fence32(xa);
                 reg_fence32(xb);
                 const float *gc = reinterpret_cast<const float *>(base + OFF_P2 + (ci & 1) * P2_BYTES + P2_GC);
@@ -230,73 +230,91 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                     float x[32];   // Diag(exp Gamma_C) (X + Kh^T U)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(half ? xb[j] : xa[j]) * gc[k0 + j];
-                    tmem_st32(tl + TM_X + k0, x);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        st_split8(base + OFF_XT + cm_off(c_lane, k0 + 8 * m, 2048),
-                                  base + OFF_XT + T128 + cm_off(c_lane, k0 + 8 * m, 2048), x + 8 * m);
+                    tmem_st32_nowait(tl + TM_X + k0, reinterpret_cast<const uint32_t (&)[32]>(x));
+                    tmem_st_split32(tl + TM_XH + k0 / 2, tl + TM_XL + k0 / 2, x);
                 }
+                tmem_wait_st();
                 aborted = handoff(HO_X);   // -> next chunk's W X, Qt X (they overlap the stores below)
                 if (aborted) break;
-                // O^T[c][r] -> row-major bf16 tile in the U^T region (free: its products have completed),
-                // then 16-byte coalesced stores: outputs for state columns, qhat for transition columns
+                // O^T[c][r] -> bf16 tile of rows r in the TMA store layout (128-byte swizzle; the
+                // previous tile was read before the U^T handoff), then outputs (state columns) or
+                // qhat (transition columns) go out by tiled TMA stores; a ragged last chunk by 16-byte
+                // stores of its rows
                 {
-                    uint16_t *so = reinterpret_cast<uint16_t *>(base + OFF_UT);
+                    uint32_t od[32];
+                    tmem_ld32_nowait(tl + TM_O + hw * 32, od);   // O^T[c][r = hw*32 + j]
+                    tmem_wait_ld();
+                    reg_fence32(od);
+                    unsigned char *ob = base + OFF_OB + (c_lane >> 6) * 8192 + (c_lane & 7) * 2;
+                    const int ch = (c_lane & 63) >> 3;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        so[(hw * 32 + j) * 128 + c_lane] = f32_to_bf16_bits(__uint_as_float(od[j]));
+                        *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j, ch)) =
+                            f32_to_bf16_bits(__uint_as_float(od[j]));
                 }
+                fence_async_smem();
                 bar_sync1(NWORK);
-                uint16_t *const dst_row0 = kind == 0 ? o + (static_cast<size_t>(t0) * H + h) * VD
-                                                     : qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH) * KD;
-                const size_t row_stride = kind == 0 ? static_cast<size_t>(H) * VD : KD;
+                if (L == CH) {
+                    if (tid == 0) {
+                        if (kind == 0) {
+                            tma_store_3d(&tm_o, 0, h, t0, sbase + OFF_OB);
+                            tma_store_3d(&tm_o, 64, h, t0, sbase + OFF_OB + 8192);
+                        } else {
+                            const int row = static_cast<int>(static_cast<int64_t>(h) * T_cont + row0 + ci * CH);
+                            tma_store_3d(&tm_q, 0, 0, row, sbase + OFF_OB);
+                            tma_store_3d(&tm_q, 64, 0, row, sbase + OFF_OB + 8192);
+                        }
+                        bulk_commit_group();
+                    }
+                } else {
+                    uint16_t *const dst_row0 = kind == 0
+                                                   ? o + (static_cast<size_t>(t0) * H + h) * VD
+                                                   : qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH) * KD;
+                    const size_t row_stride = kind == 0 ? static_cast<size_t>(H) * VD : KD;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
-                    if (r < L)
-                        *reinterpret_cast<uint4 *>(dst_row0 + r * row_stride + c16 * 8) =
-                            *reinterpret_cast<const uint4 *>(base + OFF_UT + r * 256 + c16 * 16);
+                    for (int i = 0; i < 4; ++i) {
+                        const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
+                        if (r < L)
+                            *reinterpret_cast<uint4 *>(dst_row0 + r * row_stride + c16 * 8) =
+                                *reinterpret_cast<const uint4 *>(base + OFF_OB + (c16 >> 3) * 8192 + sw128(r, c16 & 7));
+                    }
                 }
-                bar_sync1(NWORK);   // the O tile is read before the next U^T overwrites it
             }
         }
     } else if (issuer) {
         // Issuer: per chunk, W X and Qt X once the state split is in, the output / state products
         // once U^T is; package parts are staged one chunk ahead.
         bool ok = true;
-        int n_p1 = nch > 0 ? 1 : 0, n_p2[2] = {nch > 0 ? 1 : 0, 0};
+        int n_p1[2] = {nch > 0 ? 1 : 0, 0}, n_p2[2] = {nch > 0 ? 1 : 0, 0};
         for (int ci = 0; ci < nch && ok; ++ci) {
             const uint32_t par = ci & 1;
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_X]), par))) break;
-            if (ci + 1 < nch) {   // its buffer's previous chunk (ci - 1) is fully consumed
+            if (ci + 1 < nch) {   // the buffers' previous chunk (ci - 1) is fully consumed
+                load_p1(ci + 1);
                 load_p2(ci + 1);
+                ++n_p1[(ci + 1) & 1];
                 ++n_p2[(ci + 1) & 1];
             }
-            if (!(ok = mbar_wait(pbar1, par))) break;
+            if (!(ok = mbar_wait(smem_u32(&s_pbar1[ci & 1]), (ci >> 1) & 1))) break;
             fence_after();
             {
-                // (W X)^T = X^T W^T (3-term; W read MN-major)
+                const uint32_t p1 = sbase + OFF_P1 + (ci & 1) * P1_BYTES;
+                // (W X)^T = X^T W^T (3-term; X^T from TMEM, W read MN-major)
                 const uint32_t idw = idesc_bf16(128, 64, 0, 1);
-                const uint32_t aoff[3] = {0, 0, T128}, boff[3] = {0, T64, 0};
+                const uint32_t aoff[3] = {TM_XH, TM_XH, TM_XL}, boff[3] = {0, T64, 0};
 #pragma unroll
                 for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tbase + TM_WX, sdesc(sbase + OFF_XT + aoff[ps] + kk * 2 * 2048, 2048),
-                                 sdesc(sbase + OFF_P1 + PK_W + boff[ps] + kk * 256, 128, 2048), idw, (ps | kk) != 0);
+                        mma_bf16_ta(tbase + TM_WX, tbase + aoff[ps] + kk * 8,
+                                    sdesc(p1 + PK_W + boff[ps] + kk * 256, 128, 2048), idw, (ps | kk) != 0);
                 commit(mbar);
                 // O^T = X^T Qt^T (1-term)
                 const uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase + TM_O, sdesc(sbase + OFF_XT + kk * 2 * 2048, 2048),
-                             sdesc(sbase + OFF_P1 + PK_Q + kk * 2 * 1024, 1024), id, kk != 0);
-                commit(mbar_o);
-            }
-            if (!(ok = mbar_wait(mbar_o, par))) break;
-            if (ci + 1 < nch) {   // W and Qt have been read
-                load_p1(ci + 1);
-                ++n_p1;
+                    mma_bf16_ta(tbase + TM_O, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id,
+                                kk != 0);
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
             if (!(ok = mbar_wait(smem_u32(&s_pbar2[ci & 1]), (ci >> 1) & 1))) break;
@@ -308,24 +326,25 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tbase + TM_O, sdesc(sbase + OFF_UT + kk * 2 * 2048, 2048),
-                             sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64, 1);
-                // X^T += U^T Kh (3-term; Kh read MN-major)
-                const uint32_t aoff[3] = {0, 0, T64}, boff[3] = {0, T64, 0};
+                    mma_bf16_ta(tbase + TM_O, tbase + TM_UH + kk * 8, sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64,
+                                1);
+                // X^T += U^T Kh (3-term; U^T from TMEM, Kh read MN-major)
+                const uint32_t aoff[3] = {TM_UH, TM_UH, TM_UL}, boff[3] = {0, T64, 0};
 #pragma unroll
                 for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tbase + TM_X, sdesc(sbase + OFF_UT + aoff[ps] + kk * 2 * 2048, 2048),
-                                 sdesc(s2 + P2_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
+                        mma_bf16_ta(tbase + TM_X, tbase + aoff[ps] + kk * 8,
+                                    sdesc(s2 + P2_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
                 commit(mbar);
             }
         }
         if (!ok) {   // a wait gave up: record it and let the staged copies land (bounded waits)
             atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
-            if (n_p1) mbar_wait(pbar1, (n_p1 - 1) & 1);
-            for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < 2; ++b) {
+                if (n_p1[b]) mbar_wait(smem_u32(&s_pbar1[b]), (n_p1[b] - 1) & 1);
                 if (n_p2[b]) mbar_wait(smem_u32(&s_pbar2[b]), (n_p2[b] - 1) & 1);
+            }
         }
     }
 
@@ -362,6 +381,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     } else if (worker && tid == 0) {
         atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
     }
+    if (tid == 0) bulk_wait_all();   // the last O tiles are written before shared memory goes away
     fence_before();
     __syncthreads();
     fence_after();
@@ -378,11 +398,22 @@ cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // full 64-row chunks leave by tiled TMA stores: outputs [T][H][V] and qhat rows [H * T_cont][K];
+    // a tensor shorter than one chunk has no full chunk, so its map stays unused
+    CUtensorMap to{}, tq{};
+    const long long q_rows = static_cast<long long>(H) * pv.T_cont();
+    if (pv.T() >= CH && !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, CH))
+        return cudaErrorInvalidValue;
+    if (q_rows >= CH) {
+        if (q_rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        if (!encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, CH))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t err = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_BYTES));
+                                           static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    chunk_state_tc<<<static_cast<unsigned>(blocks), NTHREADS, SMEM_BYTES, stream>>>(plan_dev, H, h0, pkg, o, A, B,
-                                                                                    final_state, qhat, afin);
+    chunk_state_tc<<<static_cast<unsigned>(blocks), NTHREADS, SMEM_ALLOC, stream>>>(
+        plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, to, tq);
     return cudaGetLastError();
 }
 
