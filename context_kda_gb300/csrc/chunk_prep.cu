@@ -145,17 +145,20 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     // pkg + u * KDA_PACKAGE_BYTES) are consecutive; each CTA takes a contiguous run of units
     const int n_chunks = pv.n_chunks();
     const long long u_begin = n_units * blockIdx.x / gridDim.x, u_end = n_units * (blockIdx.x + 1) / gridDim.x;
-    auto rows_of = [&](long long u, int &t0, int &L, int &h) {
-        const int32_t *cr = pv.chunk(static_cast<int>(u % n_chunks));
-        h = static_cast<int>(u / n_chunks);
-        t0 = cr[1];
-        L = cr[2];
+    // units are walked in order by (chunk, head) counters: no 64-bit division per unit
+    struct UnitPos {
+        int ch, h;
     };
-    // Rows of unit u (q, k, v, g) by tiled TMA copies; rows past the end of the tensor arrive as
+    const UnitPos pos_begin{static_cast<int>(u_begin % n_chunks), static_cast<int>(u_begin / n_chunks)};
+    auto advance = [&](UnitPos &q) {
+        if (++q.ch == n_chunks) {
+            q.ch = 0;
+            ++q.h;
+        }
+    };
+    // Rows of a unit (q, k, v, g) by tiled TMA copies; rows past the end of the tensor arrive as
     // zeros, rows past the chunk are masked when read.
-    auto issue_qkv = [&](long long u) {
-        int t0, L, h;
-        rows_of(u, t0, L, h);
+    auto issue_rows = [&](int t0, int h) {
         mbar_arrive_expect_tx(ldbar, 6u * BOX);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -163,10 +166,6 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             tma_load_3d(sbase + STG_K + half * BOX, &tm_k, half * 64, h, t0, ldbar);
             tma_load_3d(sbase + STG_V + half * BOX, &tm_v, half * 64, h, t0, ldbar);
         }
-    };
-    auto issue_g = [&](long long u) {
-        int t0, L, h;
-        rows_of(u, t0, L, h);
         mbar_arrive_expect_tx(gbar, 4u * BOX);
 #pragma unroll
         for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0, gbar);
@@ -174,15 +173,21 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     // the next unit's rows and beta, fetched while the current one is processed
     float beta_next = 0.f;
     int L_next = 0;
+    UnitPos wpos = pos_begin;   // workers: the unit load_next fetches
     auto load_next = [&](long long u) {
         if (u >= u_end) return;
-        int t0, h;
-        rows_of(u, t0, L_next, h);
+        const int32_t *cr = pv.chunk(wpos.ch);
+        const int t0 = cr[1], h = wpos.h;
+        L_next = cr[2];
         if (tid < 64) beta_next = (tid < L_next) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
+        advance(wpos);
     };
     if (issuer && u_begin < u_end) {
-        issue_qkv(u_begin);
-        issue_g(u_begin);
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_g) : "memory");
+        issue_rows(pv.chunk(pos_begin.ch)[1], pos_begin.h);
     }
     load_next(u_begin);
 
@@ -473,12 +478,16 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         bool ok = true;
         int n = 0;
         int last_qkv = 0, last_g = 0;   // unit counts of the last staged copies
+        UnitPos ipos = pos_begin;
+        advance(ipos);   // the unit whose rows are staged next
         for (long long u = u_begin; u < u_end && ok; ++u, ++n) {
             const uint32_t par = n & 1;
+            const bool more = u + 1 < u_end;
+            const int t0_next = more ? pv.chunk(ipos.ch)[1] : 0;   // read before the wait
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
-            if (u + 1 < u_end) {   // this unit's rows are in registers
-                issue_qkv(u + 1);
-                issue_g(u + 1);
+            if (more) {   // this unit's rows are in registers
+                issue_rows(t0_next, ipos.h);
+                advance(ipos);
                 last_qkv = last_g = n + 1;
             }
             fence_after();
