@@ -473,8 +473,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             else aborted = true;
         }
     } else if (issuer) {
-        // Issuer: per unit, the next unit's rows and [KK; QK] once the operand tiles are in, then W
-        // and Ut once T' is.
+        // Issuer: per unit, [KK; QK] and then the next unit's rows once the operand tiles are in, then
+        // W and Ut once T' is.
         bool ok = true;
         int n = 0;
         int last_qkv = 0, last_g = 0;   // unit counts of the last staged copies
@@ -485,11 +485,6 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             const bool more = u + 1 < u_end;
             const int t0_next = more ? pv.chunk(ipos.ch)[1] : 0;   // read before the wait
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
-            if (more) {   // this unit's rows are in registers
-                issue_rows(t0_next, ipos.h);
-                advance(ipos);
-                last_qkv = last_g = n + 1;
-            }
             fence_after();
             {
                 const uint32_t id = idesc_bf16(128, 64);
@@ -501,6 +496,11 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                         mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
                                  sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
                 commit(mbar);
+            }
+            if (more) {   // this unit's rows are in registers: stage the next unit's
+                issue_rows(t0_next, ipos.h);
+                advance(ipos);
+                last_qkv = last_g = n + 1;
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_D]), par))) break;
             fence_after();
