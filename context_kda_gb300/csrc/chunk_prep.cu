@@ -62,7 +62,7 @@ constexpr uint32_t TM_COLS = 256;
 constexpr int NWORK = 256;             // worker threads
 constexpr int NTHREADS = NWORK + 32;   // plus the issuer warp
 constexpr int ISSUER = NWORK;
-enum { HO_A = 0, HO_D = 1 };           // worker -> issuer handoffs of a unit
+enum { HO_A = 0, HO_D = 1, HO_S = 2 };  // worker -> issuer handoffs of a unit (HO_S: staging read)
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -113,7 +113,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ __align__(8) uint64_t s_ldbar;    // q, k, v rows landed
     __shared__ __align__(8) uint64_t s_gbar;     // g rows landed
-    __shared__ __align__(8) uint64_t s_hbar[2];
+    __shared__ __align__(8) uint64_t s_hbar[3];
     __shared__ uint32_t s_tmem;
     unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(base);
@@ -131,7 +131,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         mbar_init(mbar, 1);
         mbar_init(ldbar, 1);
         mbar_init(gbar, 1);
-        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s_hbar[i]), 1);
+        for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&s_hbar[i]), 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
     fence_before();
@@ -144,6 +144,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     // unit u = head * n_chunks + chunk, so a head's chunks (and their packages, at
     // pkg + u * KDA_PACKAGE_BYTES) are consecutive; each CTA takes a contiguous run of units
     const int n_chunks = pv.n_chunks();
+    const int32_t *const chunk_tab = pv.chunk(0);   // records of 4 words: piece, start, rows, index
     const long long u_begin = n_units * blockIdx.x / gridDim.x, u_end = n_units * (blockIdx.x + 1) / gridDim.x;
     // units are walked in order by (chunk, head) counters: no 64-bit division per unit
     struct UnitPos {
@@ -170,24 +171,30 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
 #pragma unroll
         for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0, gbar);
     };
-    // the next unit's rows and beta, fetched while the current one is processed
+    // the next unit's rows and beta, fetched while the current one is processed; its chunk record
+    // was read one call earlier, so no thread waits on the plan here
     float beta_next = 0.f;
     int L_next = 0;
     UnitPos wpos = pos_begin;   // workers: the unit load_next fetches
+    int rec_t0 = chunk_tab[4 * pos_begin.ch + 1], rec_L = chunk_tab[4 * pos_begin.ch + 2];
     auto load_next = [&](long long u) {
         if (u >= u_end) return;
-        const int32_t *cr = pv.chunk(wpos.ch);
-        const int t0 = cr[1], h = wpos.h;
-        L_next = cr[2];
+        const int t0 = rec_t0, h = wpos.h;
+        L_next = rec_L;
         if (tid < 64) beta_next = (tid < L_next) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
         advance(wpos);
+        if (u + 1 < u_end) {
+            const int32_t *cr = chunk_tab + 4 * wpos.ch;
+            rec_t0 = cr[1];
+            rec_L = cr[2];
+        }
     };
     if (issuer && u_begin < u_end) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_g) : "memory");
-        issue_rows(pv.chunk(pos_begin.ch)[1], pos_begin.h);
+        issue_rows(chunk_tab[4 * pos_begin.ch + 1], pos_begin.h);
     }
     load_next(u_begin);
 
@@ -294,7 +301,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                     qw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_Q + bo) : z;
                     vw[i] = ok ? *reinterpret_cast<const uint4 *>(base + STG_V + bo) : z;
                 }
-                bar_sync1(NWORK);   // staging consumed
+                bar_sync1(NWORK);   // staging consumed: the next unit's rows may land
+                if (tid == 0) mbar_arrive(smem_u32(&s_hbar[HO_S]));
                 if (n > 0) wait_mma();   // the previous unit's W / Ut have read the operand tiles
                 // A3: Kt, Qt (stacked), Kh as bf16 hi/lo and V as bf16 in shared memory; Qt hi and Kh
                 //     hi/lo also into the package (lanes hold consecutive rows: 512 contiguous bytes)
@@ -473,8 +481,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             else aborted = true;
         }
     } else if (issuer) {
-        // Issuer: per unit, [KK; QK] and then the next unit's rows once the operand tiles are in, then
-        // W and Ut once T' is.
+        // Issuer: per unit, the next unit's rows once the staged rows are read, [KK; QK] once the
+        // operand tiles are in, then W and Ut once T' is.
         bool ok = true;
         int n = 0;
         int last_qkv = 0, last_g = 0;   // unit counts of the last staged copies
@@ -483,7 +491,13 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         for (long long u = u_begin; u < u_end && ok; ++u, ++n) {
             const uint32_t par = n & 1;
             const bool more = u + 1 < u_end;
-            const int t0_next = more ? pv.chunk(ipos.ch)[1] : 0;   // read before the wait
+            const int t0_next = more ? chunk_tab[4 * ipos.ch + 1] : 0;   // read before the wait
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_S]), par))) break;
+            if (more) {   // this unit's rows are in registers: stage the next unit's
+                issue_rows(t0_next, ipos.h);
+                advance(ipos);
+                last_qkv = last_g = n + 1;
+            }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
             fence_after();
             {
@@ -496,11 +510,6 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                         mma_bf16(tbase + TM_D1, sdesc(sbase + OFF_KQ + aoff[ps] + kk * 2 * 2048, 2048),
                                  sdesc(sbase + OFF_KH + boff[ps] + kk * 2 * 1024, 1024), id, (ps | kk) != 0);
                 commit(mbar);
-            }
-            if (more) {   // this unit's rows are in registers: stage the next unit's
-                issue_rows(t0_next, ipos.h);
-                advance(ipos);
-                last_qkv = last_g = n + 1;
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_D]), par))) break;
             fence_after();

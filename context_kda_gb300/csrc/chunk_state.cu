@@ -44,12 +44,14 @@ constexpr uint32_t P2_QK = 0, P2_KH = PK_KH - PK_QK, P2_GC = PK_GC - PK_QK;
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_WX = 0;     // (W X)^T (64 cols)
-constexpr uint32_t TM_O = 64;     // O^T (64 cols)
+constexpr uint32_t TM_O0 = 64;    // O^T of even chunks (64 cols)
 constexpr uint32_t TM_X = 128;    // X^T (128 cols)
 constexpr uint32_t TM_XH = 256;   // X^T bf16 hi as packed pairs: column k/2 holds k, k + 1 (64 cols)
 constexpr uint32_t TM_XL = 320;   // X^T bf16 lo, the same way (64 cols)
 constexpr uint32_t TM_UH = 384;   // U^T bf16 hi as packed pairs: column r/2 holds r, r + 1 (32 cols)
 constexpr uint32_t TM_UL = 416;   // U^T bf16 lo (32 cols)
+constexpr uint32_t TM_O1 = 448;   // O^T of odd chunks (64 cols): a chunk's Qt X may start before the
+                                  // previous chunk's outputs have been read
 constexpr uint32_t TM_COLS = 512;
 
 constexpr int NWORK = 256;             // worker threads
@@ -78,7 +80,8 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                const __grid_constant__ CUtensorMap tm_q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t s_mbar;      // W X, then the output / state products
+    __shared__ __align__(8) uint64_t s_mbar;      // W X, then the state product
+    __shared__ __align__(8) uint64_t s_mbar_o;    // the output products of a chunk
     __shared__ __align__(8) uint64_t s_pbar1[2];  // package part 1 landed, per buffer
     __shared__ __align__(8) uint64_t s_pbar2[2];  // package part 2 landed, per buffer
     __shared__ __align__(8) uint64_t s_hbar[2];   // worker -> issuer handoffs
@@ -106,10 +109,11 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     for (int sh = 16; sh > 0; sh >>= 1) c0 += __shfl_xor_sync(0xffffffffu, c0, sh);
     const unsigned char *const pk0 = pkg + (static_cast<size_t>(h) * pv.n_chunks() + c0) * KDA_PACKAGE_BYTES;
     auto pk_of = [&](int ci) { return pk0 + static_cast<size_t>(ci) * KDA_PACKAGE_BYTES; };
-    const uint32_t mbar = smem_u32(&s_mbar);
+    const uint32_t mbar = smem_u32(&s_mbar), mbar_o = smem_u32(&s_mbar_o);
 
     if (tid == 0) {
         mbar_init(mbar, 1);
+        mbar_init(mbar_o, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_pbar1[i]), 1);
             mbar_init(smem_u32(&s_pbar2[i]), 1);
@@ -240,9 +244,11 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 // previous tile was read before the U^T handoff), then outputs (state columns) or
                 // qhat (transition columns) go out by tiled TMA stores; a ragged last chunk by 16-byte
                 // stores of its rows
+                if (!mbar_wait_warp(mbar_o, ci & 1)) bad = true;
+                fence_after();
                 {
                     uint32_t od[32];
-                    tmem_ld32_nowait(tl + TM_O + hw * 32, od);   // O^T[c][r = hw*32 + j]
+                    tmem_ld32_nowait(tl + ((ci & 1) ? TM_O1 : TM_O0) + hw * 32, od);   // O^T[c][r = hw*32 + j]
                     tmem_wait_ld();
                     reg_fence32(od);
                     unsigned char *ob = base + OFF_OB + (c_lane >> 6) * 8192 + (c_lane & 7) * 2;
@@ -288,13 +294,8 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         int n_p1[2] = {nch > 0 ? 1 : 0, 0}, n_p2[2] = {nch > 0 ? 1 : 0, 0};
         for (int ci = 0; ci < nch && ok; ++ci) {
             const uint32_t par = ci & 1;
+            const uint32_t t_o = tbase + ((ci & 1) ? TM_O1 : TM_O0);
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_X]), par))) break;
-            if (ci + 1 < nch) {   // the buffers' previous chunk (ci - 1) is fully consumed
-                load_p1(ci + 1);
-                load_p2(ci + 1);
-                ++n_p1[(ci + 1) & 1];
-                ++n_p2[(ci + 1) & 1];
-            }
             if (!(ok = mbar_wait(smem_u32(&s_pbar1[ci & 1]), (ci >> 1) & 1))) break;
             fence_after();
             {
@@ -313,8 +314,13 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 const uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(tbase + TM_O, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id,
-                                kk != 0);
+                    mma_bf16_ta(t_o, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id, kk != 0);
+            }
+            if (ci + 1 < nch) {   // the buffers' previous chunk (ci - 1) is fully consumed
+                load_p1(ci + 1);
+                load_p2(ci + 1);
+                ++n_p1[(ci + 1) & 1];
+                ++n_p2[(ci + 1) & 1];
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
             if (!(ok = mbar_wait(smem_u32(&s_pbar2[ci & 1]), (ci >> 1) & 1))) break;
@@ -322,13 +328,8 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
             {
                 const unsigned char *p2 = base + OFF_P2 + (ci & 1) * P2_BYTES;
                 const uint32_t s2 = smem_u32(p2);
-                // O^T += U^T QK^T (1-term)
                 const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ta(tbase + TM_O, tbase + TM_UH + kk * 8, sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64,
-                                1);
-                // X^T += U^T Kh (3-term; U^T from TMEM, Kh read MN-major)
+                // X^T += U^T Kh (3-term; U^T from TMEM, Kh read MN-major): the next chunk waits on it
                 const uint32_t aoff[3] = {TM_UH, TM_UH, TM_UL}, boff[3] = {0, T64, 0};
 #pragma unroll
                 for (int ps = 0; ps < 3; ++ps)
@@ -337,6 +338,11 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                         mma_bf16_ta(tbase + TM_X, tbase + aoff[ps] + kk * 8,
                                     sdesc(s2 + P2_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
                 commit(mbar);
+                // O^T += U^T QK^T (1-term)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ta(t_o, tbase + TM_UH + kk * 8, sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64, 1);
+                commit(mbar_o);
             }
         }
         if (!ok) {   // a wait gave up: record it and let the staged copies land (bounded waits)
