@@ -40,6 +40,14 @@ CH = 64
 # chunk forward, and the transition columns a continuing token adds
 FLOPS_STATE = 6 * CH * K_DIM + 4 * CH * V_DIM + 6 * K_DIM * V_DIM          # 180,224
 FLOPS_TRANSITION = 6 * K_DIM * K_DIM + 2 * CH * K_DIM                      # 114,688
+# algorithmic HBM bytes of the chunk forward: per token-head q, k, v (bf16), g (fp32), beta (fp32)
+# read and the bf16 output written; per continuing token-head the bf16 qhat written; per segment-head
+# the fp32 summaries A (K x K) and B (K x V) written; per sequence-head the fp32 final state written
+# and, when given, h0 read
+BYTES_TOKEN = 3 * K_DIM * 2 + K_DIM * 4 + 4 + V_DIM * 2                  # 1,540
+BYTES_CONT = K_DIM * 2                                                   # 256
+BYTES_SEGMENT = (K_DIM * K_DIM + K_DIM * V_DIM) * 4                      # 131,072
+BYTES_SEQ_STATE = K_DIM * V_DIM * 4                                      # 65,536
 # tensor work the chunk stage issues (bf16 M=128 MMAs, split passes included), as 2 * 128 * N * K
 # per product: the preparation, once per (chunk, head): [KK; QK] 3 x (N 64, K 128), W 3 x (64, 64),
 # Ut 2 x (64, 64); the state pass, per chunk and work item: W X 3 x (64, 128), Qt X 1 x (64, 128),
@@ -315,7 +323,15 @@ def run_ours(args, w, rank, world, local_rank):
     peaks = _peaks()
     T_cont = int(plan[9])
     flops = T * H * FLOPS_STATE + T_cont * H * FLOPS_TRANSITION
-    achieved = flops / (kern_ms[0] / 1e3) / 1e12
+    n_seq, n_seg = int(plan[4]), int(plan[5])
+    algo_bytes = (T * H * BYTES_TOKEN + T_cont * H * BYTES_CONT + n_seg * H * BYTES_SEGMENT
+                  + n_seq * H * BYTES_SEQ_STATE * (2 if w.h0_std > 0 else 1))
+    # the binding roof is the larger of bytes / HBM bandwidth and flops / tensor peak
+    t_hbm = algo_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    sec = kern_ms[0] / 1e3
+    achieved_gbs = algo_bytes / sec / 1e9
+    achieved_tflops = flops / sec / 1e12
     items_off, pieces_off = int(plan[18]), int(plan[17])
     issued = int(plan[11]) * H * ISSUED_PREP_PER_CHUNK   # every (chunk, head) is prepared once
     for i in range(int(plan[12])):
@@ -332,13 +348,18 @@ def run_ours(args, w, rank, world, local_rank):
         "config": _config(w, world),
         "kernels_ms": {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]},
         "kernel_shares": {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]},
-        "roofline": {"bound": "tensor", "kernel": "chunk_forward", "achieved": achieved,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                     "traffic": traffic, "algorithmic_flops_per_launch": flops,
-                     "peak_source": f"{peaks['source']} bf16 dense (burst)",
-                     "issued_tensor_flops_per_launch": issued,
-                     "issued_frac": issued / (kern_ms[0] / 1e3) / 1e12 / peaks["bf16_tflops"],
-                     "hbm_peak_gbs": peaks["hbm_gbs"]},
+        "roofline": ({"bound": "hbm", "kernel": "chunk_forward", "achieved": achieved_gbs,
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                      "peak_source": f"{peaks['source']} HBM copy"}
+                     if t_hbm >= t_tensor else
+                     {"bound": "tensor", "kernel": "chunk_forward", "achieved": achieved_tflops,
+                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved_tflops / peaks["bf16_tflops"],
+                      "peak_source": f"{peaks['source']} bf16 dense (burst)"})
+        | {"traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
+           "algorithmic_flops_per_launch": flops, "tensor_frac": achieved_tflops / peaks["bf16_tflops"],
+           "issued_tensor_flops_per_launch": issued,
+           "issued_frac": issued / sec / 1e12 / peaks["bf16_tflops"], "hbm_peak_gbs": peaks["hbm_gbs"],
+           "bf16_peak_tflops": peaks["bf16_tflops"]},
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "pipeline": "2 lanes: step i+1 uploads its inputs while step i computes and reads back"},
