@@ -15,13 +15,14 @@
 //
 // Mapping.  A persistent CTA per SM walks (chunk, head) units: 8 worker warps build the operand
 // tiles and solve the inverse on the CUDA cores; lane 0 of a ninth warp issues the tcgen05 MMAs
-// (M = 128, bf16 operands in shared memory, FP32 accumulators in TMEM) and the TMA loads that
-// stage the next unit's rows.  The products that feed the state (Kt Kh^T, W) use a three-term
+// (M = 128, bf16 operands in shared memory, FP32 accumulators in TMEM) and lane 0 of a tenth the
+// TMA loads that stage the next unit's rows.  The products that feed the state (Kt Kh^T, W) use a three-term
 // bf16 split (hi*hi + hi*lo + lo*hi, ~2^-17 relative); Ut two terms (V is exact in bf16).
 // Results go straight from registers to the unit's package in the workspace with 16-byte
 // stores, each tile already in the layout the state pass's MMAs read.  A unit's W and Ut products
-// run while the workers start the next unit; the workers read them back from TMEM and store them
-// while they wait for the next unit's [KK; QK].
+// run while the workers start the next unit; the workers read W back from TMEM and store it while
+// they wait for the next unit's [KK; QK], and four warps store Ut while two solve the next
+// unit's diagonal blocks.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -60,8 +61,9 @@ constexpr uint32_t TM_U = 128;    // Ut^T
 constexpr uint32_t TM_COLS = 256;
 
 constexpr int NWORK = 256;             // worker threads
-constexpr int NTHREADS = NWORK + 32;   // plus the issuer warp
+constexpr int NTHREADS = NWORK + 64;   // plus the issuer (MMAs) and producer (row copies) warps
 constexpr int ISSUER = NWORK;
+constexpr int PRODUCER = NWORK + 32;
 enum { HO_A = 0, HO_D = 1, HO_S = 2 };  // worker -> issuer handoffs of a unit (HO_S: staging read)
 
 constexpr float LOG2E = 1.4426950408889634f;
@@ -124,7 +126,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;          // TMEM lane quadrant, column half
-    const bool worker = tid < NWORK, issuer = tid == ISSUER;
+    const bool worker = tid < NWORK, issuer = tid == ISSUER, producer = tid == PRODUCER;
     const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar), gbar = smem_u32(&s_gbar);
 
     if (tid == 0) {
@@ -189,7 +191,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             rec_L = cr[2];
         }
     };
-    if (issuer && u_begin < u_end) {
+    if (producer && u_begin < u_end) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
@@ -206,7 +208,9 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         ++phase;
         fence_after();
     };
-    // Workers hand their shared-memory operands over to the issuer (see the state pass).
+    // Workers hand their shared-memory operands over to the issuer: every writer fences its
+    // generic-proxy stores for the tensor core, the workers meet on named barrier 1 (OR-reducing
+    // their wait failures), and one of them arrives.
     auto handoff = [&](int which) -> bool {
         fence_async_smem();
         fence_before();
@@ -215,8 +219,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         return ab;
     };
 
-    // W^T and Ut^T of a unit (already complete) from TMEM into its package, one at a time
-    auto store_w_ut = [&](long long u) {
+    // W^T of a unit (already complete) from TMEM into its package
+    auto store_w = [&](long long u) {
         unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
         {
             float x[32];
@@ -230,12 +234,20 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 *reinterpret_cast<uint4 *>(pk + PK_W + T64 + off) = lo;
             }
         }
-        {
+    };
+    // Ut^T by the threads of column half hw_of (all 32-column halves when one warp per quadrant
+    // does it: hw_of < 0)
+    auto store_ut = [&](long long u, int hw_of) {
+        unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            const int hh = hw_of < 0 ? half : hw_of;
+            if (hw_of >= 0 && half > 0) break;
             float x[32];
-            tmem_ld32(tl + TM_U + hw * 32, x);   // Ut^T[c = c_lane][r = hw*32 + j]
-            // Ut^T as [hw][m][c] float4 groups: a warp's store (and the state pass's load) of one
+            tmem_ld32(tl + TM_U + hh * 32, x);   // Ut^T[c = c_lane][r = hh*32 + j]
+            // Ut^T as [hh][m][c] float4 groups: a warp's store (and the state pass's load) of one
             // group covers 512 contiguous bytes
-            float4 *ut = reinterpret_cast<float4 *>(pk + PK_U) + hw * 8 * 128 + c_lane;
+            float4 *ut = reinterpret_cast<float4 *>(pk + PK_U) + hh * 8 * 128 + c_lane;
 #pragma unroll
             for (int m = 0; m < 8; ++m) ut[m * 128] = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
         }
@@ -339,7 +351,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 aborted = handoff(HO_A);   // -> [KK; QK]
             }
             if (aborted) break;
-            if (n > 0) store_w_ut(u - 1);   // while [KK; QK] runs
+            if (n > 0) store_w(u - 1);   // while [KK; QK] runs
 
             // ================= B: [KK; QK] = [Kt; Qt] Kh^T  (3-term split) =================
             wait_mma();
@@ -384,6 +396,9 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         // Diagonal blocks t_b by forward substitution; then each 32 x 32 half as
         // [t_0 0; -t_1 M_10 t_0  t_1], and the whole as [T_lo 0; -T_hi M_hi,lo T_lo  T_hi].
         {
+            // warps 4 - 7 (one per TMEM lane quadrant) store the previous unit's Ut^T meanwhile: its
+            // columns stay valid until this unit's T' is handed over
+            if (n > 0 && tid >= 128) store_ut(u - 1, -1);
             if (tid < 64) {   // column jj of diagonal block b; each solved entry updates all later rows
                 const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
                 float x[16], sacc[16];
@@ -477,27 +492,18 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
         }
         if (!aborted && n > 0) {   // the last unit's W / Ut
             wait_mma();
-            if (!bar_or1(NWORK, bad)) store_w_ut(u_end - 1);
+            if (!bar_or1(NWORK, bad)) {
+                store_w(u_end - 1);
+                store_ut(u_end - 1, hw);
+            }
             else aborted = true;
         }
     } else if (issuer) {
-        // Issuer: per unit, the next unit's rows once the staged rows are read, [KK; QK] once the
-        // operand tiles are in, then W and Ut once T' is.
+        // Issuer: per unit, [KK; QK] once the operand tiles are in, then W and Ut once T' is.
         bool ok = true;
         int n = 0;
-        int last_qkv = 0, last_g = 0;   // unit counts of the last staged copies
-        UnitPos ipos = pos_begin;
-        advance(ipos);   // the unit whose rows are staged next
         for (long long u = u_begin; u < u_end && ok; ++u, ++n) {
             const uint32_t par = n & 1;
-            const bool more = u + 1 < u_end;
-            const int t0_next = more ? chunk_tab[4 * ipos.ch + 1] : 0;   // read before the wait
-            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_S]), par))) break;
-            if (more) {   // this unit's rows are in registers: stage the next unit's
-                issue_rows(t0_next, ipos.h);
-                advance(ipos);
-                last_qkv = last_g = n + 1;
-            }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_A]), par))) break;
             fence_after();
             {
@@ -533,10 +539,26 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 commit(mbar);
             }
         }
-        if (!ok) {
-            atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
-            mbar_wait(ldbar, last_qkv & 1);   // bounded: let the last staged copies land
-            mbar_wait(gbar, last_g & 1);
+        if (!ok) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+    } else if (producer) {
+        // Producer: the next unit's rows once this unit's staged rows are read (a TMA unit busy with
+        // earlier boxes stalls the thread that issues more, which must not be the MMA issuer)
+        bool ok = true;
+        int n = 0;
+        int last = 0;   // unit count of the last staged copies
+        UnitPos ipos = pos_begin;
+        advance(ipos);   // the unit whose rows are staged next
+        for (long long u = u_begin; u + 1 < u_end && ok; ++u, ++n) {
+            const int t0_next = chunk_tab[4 * ipos.ch + 1];   // read before the wait
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_S]), n & 1))) break;
+            issue_rows(t0_next, ipos.h);
+            advance(ipos);
+            last = n + 1;
+        }
+        if (!ok) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+        if (u_begin < u_end) {   // bounded: every staged copy lands before the CTA exits
+            mbar_wait(ldbar, last & 1);
+            mbar_wait(gbar, last & 1);
         }
     }
     if (worker && aborted && tid == 0) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);

@@ -12,7 +12,9 @@
 // (cuLA PR #136, "feat(kda): add cuDNN concatenated-summary Kimi CP", §Summary:
 // preceding_transition).
 //
-// Mapping.  One CTA per (work item, head): 8 worker warps and an issuer warp.  The state lives
+// Mapping.  One CTA per (work item, head): 8 worker warps, an issuer warp (tcgen05 MMAs) and a
+// producer warp (package copies: a TMA unit busy with earlier copies stalls the thread that issues
+// the next one, which must not be the MMA issuer).  The state lives
 // transposed in TMEM (lane c, column k) twice: as an FP32 accumulator, and split into bf16 hi/lo
 // pairs as the A operand of W X and Qt X, which the tensor core reads from TMEM.  Per chunk the
 // chain is: (W X)^T = X^T W^T (3-term) -> workers form U^T = Ut^T - (W X)^T and split it into
@@ -55,8 +57,9 @@ constexpr uint32_t TM_O1 = 448;   // O^T of odd chunks (64 cols): a chunk's Qt X
 constexpr uint32_t TM_COLS = 512;
 
 constexpr int NWORK = 256;             // worker threads
-constexpr int NTHREADS = NWORK + 32;   // plus the issuer warp
+constexpr int NTHREADS = NWORK + 64;   // plus the issuer and producer warps
 constexpr int ISSUER = NWORK;
+constexpr int PRODUCER = NWORK + 32;
 enum { HO_X = 0, HO_U = 1 };           // worker -> issuer handoffs of a chunk
 
 __device__ int g_state_status;   // set to KDA_ERR_TIMEOUT when a bounded wait expires
@@ -85,6 +88,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     __shared__ __align__(8) uint64_t s_pbar1[2];  // package part 1 landed, per buffer
     __shared__ __align__(8) uint64_t s_pbar2[2];  // package part 2 landed, per buffer
     __shared__ __align__(8) uint64_t s_hbar[2];   // worker -> issuer handoffs
+    __shared__ __align__(8) uint64_t s_free[2];   // issuer -> producer: package buffer free
     __shared__ uint32_t s_tmem;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;   // 128-byte swizzle atoms
     unsigned char *const base = smem_raw + (sbase - smem_u32(smem_raw));
@@ -92,7 +96,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;          // TMEM lane quadrant, column half
-    const bool worker = tid < NWORK, issuer = tid == ISSUER;
+    const bool worker = tid < NWORK, issuer = tid == ISSUER, producer = tid == PRODUCER;
     const int item = blockIdx.x / H, h = blockIdx.x % H;
     const int32_t *it = pv.item(item);
     const int p = it[0], kind = it[1];
@@ -118,6 +122,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
             mbar_init(smem_u32(&s_pbar1[i]), 1);
             mbar_init(smem_u32(&s_pbar2[i]), 1);
             mbar_init(smem_u32(&s_hbar[i]), 1);
+            mbar_init(smem_u32(&s_free[i]), 1);
         }
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
@@ -128,7 +133,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
     const int c_lane = quad * 32 + lane;                                     // state column of this thread
 
-    // package parts by bulk copy (issuer thread)
+    // package parts by bulk copy (producer thread)
     auto load_p1 = [&](int ci) {
         const uint32_t bar = smem_u32(&s_pbar1[ci & 1]);
         mbar_arrive_expect_tx(bar, P1_BYTES);
@@ -139,7 +144,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         mbar_arrive_expect_tx(bar, P2_BYTES);
         bulk_g2s(sbase + OFF_P2 + (ci & 1) * P2_BYTES, pk_of(ci) + PK_QK, P2_BYTES, bar);
     };
-    if (issuer && nch > 0) {
+    if (producer && nch > 0) {
         load_p1(0);
         load_p2(0);
     }
@@ -289,13 +294,14 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         }
     } else if (issuer) {
         // Issuer: per chunk, W X and Qt X once the state split is in, the output / state products
-        // once U^T is; package parts are staged one chunk ahead.
+        // once U^T is.  Chunk ci's state handoff means every product of chunk ci - 1 has completed,
+        // so the producer may refill that chunk's package buffers with chunk ci + 1.
         bool ok = true;
-        int n_p1[2] = {nch > 0 ? 1 : 0, 0}, n_p2[2] = {nch > 0 ? 1 : 0, 0};
         for (int ci = 0; ci < nch && ok; ++ci) {
             const uint32_t par = ci & 1;
             const uint32_t t_o = tbase + ((ci & 1) ? TM_O1 : TM_O0);
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_X]), par))) break;
+            if (ci + 1 < nch) mbar_arrive(smem_u32(&s_free[(ci + 1) & 1]));
             if (!(ok = mbar_wait(smem_u32(&s_pbar1[ci & 1]), (ci >> 1) & 1))) break;
             fence_after();
             {
@@ -315,12 +321,6 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ta(t_o, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id, kk != 0);
-            }
-            if (ci + 1 < nch) {   // the buffers' previous chunk (ci - 1) is fully consumed
-                load_p1(ci + 1);
-                load_p2(ci + 1);
-                ++n_p1[(ci + 1) & 1];
-                ++n_p2[(ci + 1) & 1];
             }
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
             if (!(ok = mbar_wait(smem_u32(&s_pbar2[ci & 1]), (ci >> 1) & 1))) break;
@@ -345,12 +345,24 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 commit(mbar_o);
             }
         }
-        if (!ok) {   // a wait gave up: record it and let the staged copies land (bounded waits)
-            atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
-            for (int b = 0; b < 2; ++b) {
-                if (n_p1[b]) mbar_wait(smem_u32(&s_pbar1[b]), (n_p1[b] - 1) & 1);
-                if (n_p2[b]) mbar_wait(smem_u32(&s_pbar2[b]), (n_p2[b] - 1) & 1);
-            }
+        if (!ok) atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
+    } else if (producer) {
+        // Producer: chunk j's package parts once the issuer has freed their buffers (the free signal
+        // of buffer j & 1 cannot run a phase ahead: the next one needs chunk j's products).
+        bool ok = true;
+        int n_p1[2] = {nch > 0 ? 1 : 0, 0}, n_p2[2] = {nch > 0 ? 1 : 0, 0};
+        for (int j = 1; j < nch && ok; ++j) {
+            if (!(ok = mbar_wait(smem_u32(&s_free[j & 1]), ((j - 1) >> 1) & 1))) break;
+            load_p1(j);
+            load_p2(j);
+            ++n_p1[j & 1];
+            ++n_p2[j & 1];
+        }
+        if (!ok) atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
+        // every staged copy lands before the CTA exits (bounded waits)
+        for (int b = 0; b < 2; ++b) {
+            if (n_p1[b]) mbar_wait(smem_u32(&s_pbar1[b]), (n_p1[b] - 1) & 1);
+            if (n_p2[b]) mbar_wait(smem_u32(&s_pbar2[b]), (n_p2[b] - 1) & 1);
         }
     }
 
