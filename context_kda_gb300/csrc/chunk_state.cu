@@ -259,9 +259,11 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                     unsigned char *ob = base + OFF_OB + (c_lane >> 6) * 8192 + (c_lane & 7) * 2;
                     const int ch = (c_lane & 63) >> 3;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j, ch)) =
-                            f32_to_bf16_bits(__uint_as_float(od[j]));
+                    for (int j = 0; j < 32; j += 2) {   // one conversion per pair of rows
+                        const uint32_t w = bf16x2_bits(__uint_as_float(od[j]), __uint_as_float(od[j + 1]));
+                        *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j, ch)) = static_cast<uint16_t>(w);
+                        *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j + 1, ch)) = static_cast<uint16_t>(w >> 16);
+                    }
                 }
                 fence_async_smem();
                 bar_sync1(NWORK);
