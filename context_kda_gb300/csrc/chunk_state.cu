@@ -298,13 +298,13 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         // Issuer: per chunk, W X and Qt X once the state split is in, the output / state products
         // once U^T is.  Chunk ci's state handoff means every product of chunk ci - 1 has completed,
         // so the producer may refill that chunk's package buffers with chunk ci + 1.
-        bool ok = true;
+        // The package waits sit where the issuer idles anyway (while the workers run U and J).
+        bool ok = nch == 0 || mbar_wait(smem_u32(&s_pbar1[0]), 0);
         for (int ci = 0; ci < nch && ok; ++ci) {
             const uint32_t par = ci & 1;
             const uint32_t t_o = tbase + ((ci & 1) ? TM_O1 : TM_O0);
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_X]), par))) break;
             if (ci + 1 < nch) mbar_arrive(smem_u32(&s_free[(ci + 1) & 1]));
-            if (!(ok = mbar_wait(smem_u32(&s_pbar1[ci & 1]), (ci >> 1) & 1))) break;
             fence_after();
             {
                 const uint32_t p1 = sbase + OFF_P1 + (ci & 1) * P1_BYTES;
@@ -324,8 +324,8 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ta(t_o, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id, kk != 0);
             }
-            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
             if (!(ok = mbar_wait(smem_u32(&s_pbar2[ci & 1]), (ci >> 1) & 1))) break;
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
             fence_after();
             {
                 const unsigned char *p2 = base + OFF_P2 + (ci & 1) * P2_BYTES;
@@ -346,6 +346,8 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                     mma_bf16_ta(t_o, tbase + TM_UH + kk * 8, sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64, 1);
                 commit(mbar_o);
             }
+            // the next chunk's W and Qt (issued when this chunk began)
+            if (ci + 1 < nch && !(ok = mbar_wait(smem_u32(&s_pbar1[(ci + 1) & 1]), ((ci + 1) >> 1) & 1))) break;
         }
         if (!ok) atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
     } else if (producer) {
