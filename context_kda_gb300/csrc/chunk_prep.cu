@@ -42,6 +42,7 @@ constexpr uint32_t OFF_MISC = 163840;
 constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
 constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
 constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
+constexpr uint32_t OFF_NEXT = OFF_MISC + 1792;  // staged unit: beta (64 fp32), then its row count
 // Raw rows of a unit, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of 64 rows
 // x 128 bytes) into their own regions: q, k, v as two 64-column boxes each, g as four 32-column
 // boxes.  The next unit's copies are issued once this unit's rows are in registers.
@@ -52,7 +53,7 @@ constexpr uint32_t SMEM_BYTES = OFF_SQKV + 6 * BOX;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
 constexpr uint32_t T128 = 32768, T64 = 16384;
 constexpr uint32_t OFF_M32 = OFF_KH, OFF_T32 = OFF_KH + 16384;
-static_assert(OFF_MISC + 1792 <= OFF_SQKV && OFF_SQKV % 1024 == 0, "staging region");
+static_assert(OFF_NEXT + 260 <= OFF_SQKV && OFF_SQKV % 1024 == 0, "staging region");
 
 // ---- TMEM columns --------------------------------------------------------------------------
 constexpr uint32_t TM_D1 = 0;     // [KK; QK] (64 cols)
@@ -126,7 +127,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;          // TMEM lane quadrant, column half
-    const bool worker = tid < NWORK, issuer = tid == ISSUER, producer = tid == PRODUCER;
+    const bool worker = tid < NWORK, issuer = tid == ISSUER, producer_warp = warp == PRODUCER / 32;
     const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar), gbar = smem_u32(&s_gbar);
 
     if (tid == 0) {
@@ -173,32 +174,37 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
 #pragma unroll
         for (int qtr = 0; qtr < 4; ++qtr) tma_load_3d(sbase + STG_G + qtr * BOX, &tm_g, qtr * 32, h, t0, gbar);
     };
-    // the next unit's rows and beta, fetched while the current one is processed; its chunk record
-    // was read one call earlier, so no thread waits on the plan here
-    float beta_next = 0.f;
-    int L_next = 0;
-    UnitPos wpos = pos_begin;   // workers: the unit load_next fetches
-    int rec_t0 = chunk_tab[4 * pos_begin.ch + 1], rec_L = chunk_tab[4 * pos_begin.ch + 2];
-    auto load_next = [&](long long u) {
-        if (u >= u_end) return;
-        const int t0 = rec_t0, h = wpos.h;
-        L_next = rec_L;
-        if (tid < 64) beta_next = (tid < L_next) ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
-        advance(wpos);
-        if (u + 1 < u_end) {
-            const int32_t *cr = chunk_tab + 4 * wpos.ch;
-            rec_t0 = cr[1];
-            rec_L = cr[2];
+    // The producer warp stages a unit: its beta and row count into shared memory (all lanes), then
+    // (lane 0) arms the row barriers, whose release orders those writes before the workers' waits,
+    // and issues the row copies.
+    float *const s_beta_next = reinterpret_cast<float *>(base + OFF_NEXT);
+    int *const s_L_next = reinterpret_cast<int *>(base + OFF_NEXT + 256);
+    auto load_beta = [&](int t0, int L, int h, float (&b)[2]) {   // issued early, used at staging
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = lane + 32 * e;
+            b[e] = i < L ? beta[static_cast<size_t>(t0 + i) * H + h] : 0.f;
         }
     };
-    if (producer && u_begin < u_end) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_g) : "memory");
-        issue_rows(chunk_tab[4 * pos_begin.ch + 1], pos_begin.h);
+    auto stage_unit = [&](int t0, int L, int h, const float (&b)[2]) {
+        s_beta_next[lane] = b[0];
+        s_beta_next[lane + 32] = b[1];
+        if (lane == 0) *s_L_next = L;
+        __syncwarp();
+        if (lane == 0) issue_rows(t0, h);
+    };
+    if (producer_warp && u_begin < u_end) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_g) : "memory");
+        }
+        const int t0 = chunk_tab[4 * pos_begin.ch + 1], L = chunk_tab[4 * pos_begin.ch + 2];
+        float b[2];
+        load_beta(t0, L, pos_begin.h, b);
+        stage_unit(t0, L, pos_begin.h, b);
     }
-    load_next(u_begin);
 
     bool aborted = false;   // all workers agree on it (OR-reduced at barriers)
     bool bad = false;       // a bounded wait of this thread gave up
@@ -256,12 +262,13 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     if (worker) {
         int n = 0;
         for (long long u = u_begin; u < u_end && !aborted; ++u, ++n) {
-            const int L = L_next;
             unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
+            int L;
 
             // ================= A: staged rows -> decayed keys / queries / values =====================
             {
                 if (!mbar_wait_warp(gbar, n & 1)) bad = true;
+                L = *s_L_next;   // staged with the rows (read before this unit's staging handoff)
                 // A1: log2-scaled cumulative decay per key channel, in place over the staged g
                 //     (32 rows per thread: load all, scan in registers, store once)
                 {
@@ -278,7 +285,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                         gv[j] = acc;
                     }
                     s_gsum[hr * 128 + kc] = acc;
-                    if (tid < 64) s_beta[tid] = beta_next;
+                    if (tid < 64) s_beta[tid] = s_beta_next[tid];
                     bar_sync1(NWORK);
                     const float off = hr ? s_gsum[kc] : 0.f;
                     if (hr == 0) {
@@ -290,7 +297,6 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                     for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
                     bar_sync1(NWORK);
                 }
-                load_next(u + 1);   // s_beta holds this unit's values now
                 // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
                 //     the lanes of a warp hold consecutive rows of one piece column
                 if (!mbar_wait_warp(ldbar, n & 1)) bad = true;
@@ -540,23 +546,26 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             }
         }
         if (!ok) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
-    } else if (producer) {
-        // Producer: the next unit's rows once this unit's staged rows are read (a TMA unit busy with
-        // earlier boxes stalls the thread that issues more, which must not be the MMA issuer)
+    } else if (producer_warp) {
+        // Producer warp: the next unit once this unit's staged rows and metadata are read (a TMA unit
+        // busy with earlier boxes stalls the thread that issues more, which must not be the MMA
+        // issuer; the row count and beta loads ride along off the workers' path)
         bool ok = true;
         int n = 0;
         int last = 0;   // unit count of the last staged copies
         UnitPos ipos = pos_begin;
-        advance(ipos);   // the unit whose rows are staged next
+        advance(ipos);   // the unit staged next
         for (long long u = u_begin; u + 1 < u_end && ok; ++u, ++n) {
-            const int t0_next = chunk_tab[4 * ipos.ch + 1];   // read before the wait
-            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_S]), n & 1))) break;
-            issue_rows(t0_next, ipos.h);
+            const int t0_next = chunk_tab[4 * ipos.ch + 1], L_next = chunk_tab[4 * ipos.ch + 2];
+            float b[2];
+            load_beta(t0_next, L_next, ipos.h, b);   // in flight during the wait
+            if (!(ok = mbar_wait_warp(smem_u32(&s_hbar[HO_S]), n & 1))) break;
+            stage_unit(t0_next, L_next, ipos.h, b);
             advance(ipos);
             last = n + 1;
         }
-        if (!ok) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
-        if (u_begin < u_end) {   // bounded: every staged copy lands before the CTA exits
+        if (!ok && lane == 0) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+        if (lane == 0 && u_begin < u_end) {   // bounded: every staged copy lands before the CTA exits
             mbar_wait(ldbar, last & 1);
             mbar_wait(gbar, last & 1);
         }
