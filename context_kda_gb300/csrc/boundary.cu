@@ -8,20 +8,23 @@
 // (cuLA PR #110, "feat(cp): add opt-in NVSHMEM CP state handoff", §Motivation:
 // consumers assemble the final state from the producers' affine states).
 //
-// Work units are 128-row tiles (128 continuing tokens, or the 128 rows of a
-// final-state transition) of one head, numbered head-major so that consecutive
-// units share S_in[j].  The kernel is persistent: one CTA per SM takes a
-// contiguous run of units.  S_in[j] arrives by bulk copy and is split into a
-// bf16 hi/lo operand only when the run reaches a new (head, segment); each
-// qhat tile (bf16) arrives by bulk copy into a staging buffer and is laid out
-// as the A operand, and D = Qhat S_in is formed on the tcgen05 tensor cores
-// (M = N = K = 128; qhat hi * S hi + qhat hi * S lo, FP32 in TMEM).  A final-
-// state transition (fp32) is split into hi/lo and takes the third product too.  The copy of the next item is issued
-// as soon as the staging buffer has been read.  A full 128-row output tile
-// moves through a shared-memory buffer by tiled TMA (128-byte swizzle): loaded
-// one unit ahead, updated in place by the epilogue, written back with one TMA
-// store.  Ragged tail tiles and final states are read and written by the
-// threads directly, so nothing outside a record is ever stored.
+// Work units are 128-row tiles (128 continuing tokens, or the 128 rows of a final-state transition)
+// of one head, numbered head-major so that consecutive units share S_in[j]; a transition follows the
+// tiles of the continuing piece that ends its sequence, whose S_in[j] it needs.  The kernel is
+// persistent: one CTA per SM takes a contiguous run of units as a software pipeline.
+// - S_in[j] is read straight into registers and split into a bf16 hi/lo operand only when the run
+//   reaches a new (head, segment).
+// - A qhat tile (bf16) lands by tiled TMA (two 64-column boxes, 128-byte swizzle) directly in the
+//   layout the tensor core reads, in a ring of three buffers requested three units ahead.
+// - D = Qhat S_in is formed on the tcgen05 tensor cores (M = N = K = 128; qhat * S hi + qhat * S lo,
+//   FP32 in one of two TMEM accumulators).  The next unit's products are issued before this unit's
+//   epilogue whenever they share S_in and their qhat tile comes by TMA, so the epilogue of one unit
+//   overlaps the products of the next.  A final-state transition (fp32) is split into hi/lo by the
+//   threads and takes the third product too.
+// - A full 128-row output tile moves through one of two shared-memory buffers by tiled TMA: loaded a
+//   unit ahead, updated in place by the epilogue, written back with one TMA store.  Ragged tail tiles
+//   and final states are read and written by the threads directly, so nothing outside a record is
+//   ever stored.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -30,95 +33,106 @@ namespace {
 
 using namespace tc;
 
-constexpr int TR = 128;                   // rows per tile
-constexpr uint32_t LBO_B = 2048;          // S_in^T operand: rows c, cols k
-constexpr uint32_t LBO_A = 2064;          // Qhat operand: rows r, cols k (chunk stride padded off the bank period)
-constexpr uint32_t TILE_B = 32768, TILE_A = 16 * LBO_A;
-constexpr uint32_t OFF_B = 0;                      // S_in^T hi | lo
-constexpr uint32_t OFF_A = 2 * TILE_B;             // Qhat hi | lo
-constexpr uint32_t OFF_STG = OFF_A + 2 * TILE_A;   // fp32 staging: 128 rows x 512 bytes
-constexpr uint32_t OFF_OB = 197632;                // bf16 output tile: two swizzled 64-column boxes
-constexpr uint32_t SMEM_BYTES = OFF_OB + 32768;
+constexpr int TR = 128;                    // rows per tile
+constexpr uint32_t LBO_B = 2048;           // S_in^T operand: rows c, cols k (no swizzle)
+constexpr uint32_t TILE_B = 32768;
+constexpr uint32_t BOX = 16384;            // 128 rows x 128 bytes, 128-byte swizzle
+constexpr uint32_t OFF_B = 0;              // S_in^T hi | lo
+constexpr uint32_t OFF_A = 2 * TILE_B;     // three qhat tiles (ring), two boxes each
+constexpr uint32_t OFF_OB = OFF_A + 6 * BOX;   // two bf16 output tiles, two boxes each
+constexpr uint32_t SMEM_BYTES = OFF_OB + 4 * BOX;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
-static_assert(OFF_STG + 65536 <= OFF_OB && OFF_OB % 1024 == 0, "output tile buffer");
-constexpr uint32_t TM_COLS = 128;
+static_assert(OFF_A % 1024 == 0 && OFF_OB % 1024 == 0, "swizzled buffers");
+constexpr uint32_t TM_COLS = 256;          // two 128-column accumulators
 
 __device__ int g_boundary_status;
 
-// Position in the unit order: head h, record rec (continuing pieces first, then
-// final-state transitions), tile within the record.
+// Position in the unit order: head h, continuing record rec, unit within the record.  A record's
+// units are its 128-row qhat tiles, then, when its piece ends the sequence, the final-state
+// transition (which needs the same S_in[j]): transitions spread over the run with their records.
 struct Cursor {
     int h, rec, tile;
 };
 
+// One unit: segment, sequence (>= 0: a final-state transition), units in its record, rows, first
+// token and first qhat row (qhat tiles), element offset of its first row in qhat (bf16) or afin (fp32)
 struct Rec {
-    int seg, seq, nt, rows_total, t_first;   // seq >= 0: final-state record
-    size_t src;                              // element offset of row 0 in qhat (bf16) or afin (fp32), head h
+    int seg, seq, units, rows, tok, qrow;
+    size_t src;
 };
 
-__device__ __forceinline__ Rec rec_info(const PlanView &pv, int H, int h, int rec)
+__device__ __forceinline__ int record_units(const PlanView &pv, int rec)
+{
+    const int32_t *cr = pv.cont(rec);
+    return (cr[3] + TR - 1) / TR + ((pv.piece(cr[0])[PC_FLAGS] & KDA_PIECE_SEQ_END) ? 1 : 0);
+}
+
+__device__ __forceinline__ Rec rec_info(const PlanView &pv, int H, int h, int rec, int tile)
 {
     Rec r;
-    if (rec < pv.n_cont()) {
-        const int32_t *cr = pv.cont(rec);
-        r.seg = cr[1];
+    const int32_t *cr = pv.cont(rec);
+    const int32_t *pc = pv.piece(cr[0]);
+    const int nt = (cr[3] + TR - 1) / TR;
+    r.seg = cr[1];
+    r.units = nt + ((pc[PC_FLAGS] & KDA_PIECE_SEQ_END) ? 1 : 0);
+    if (tile < nt) {
         r.seq = -1;
-        r.rows_total = cr[3];
-        r.nt = (cr[3] + TR - 1) / TR;
-        r.t_first = pv.piece(cr[0])[PC_START];
-        r.src = (static_cast<size_t>(h) * pv.T_cont() + cr[2]) * KD;
+        r.rows = min(TR, cr[3] - tile * TR);
+        r.tok = pc[PC_START] + tile * TR;
+        r.qrow = h * pv.T_cont() + cr[2] + tile * TR;
+        r.src = static_cast<size_t>(r.qrow) * KD;
     } else {
-        const int f = rec - pv.n_cont();
-        const int32_t *fr = pv.fin(f);
-        r.seg = fr[2];
-        r.seq = fr[1];
-        r.rows_total = TR;
-        r.nt = 1;
-        r.t_first = 0;
+        const int f = pc[PC_FIN];
+        r.seq = pv.fin(f)[1];
+        r.rows = TR;
+        r.tok = 0;
+        r.qrow = 0;
         r.src = (static_cast<size_t>(f) * H + h) * KD * KD;
     }
     return r;
 }
 
-__device__ __forceinline__ void split_store4(unsigned char *base, uint32_t off_hi, uint32_t off_lo, float4 x)
+__device__ __forceinline__ void advance(Cursor &c, const Rec &r, int n_cont)
 {
-    uint32_t h0, h1, l0, l1;
-    split_bf16x2(x.x, x.y, h0, l0);
-    split_bf16x2(x.z, x.w, h1, l1);
-    *reinterpret_cast<uint2 *>(base + off_hi) = make_uint2(h0, h1);
-    *reinterpret_cast<uint2 *>(base + off_lo) = make_uint2(l0, l1);
+    if (++c.tile == r.units) {
+        c.tile = 0;
+        if (++c.rec == n_cont) {
+            c.rec = 0;
+            ++c.h;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(256, 1)
 boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long long n_units,
             const float *__restrict__ S_in, const uint16_t *__restrict__ qhat, const float *__restrict__ afin,
-            uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o)
+            uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o,
+            const __grid_constant__ CUtensorMap tm_q, int has_tq)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t s_mbar;
-    __shared__ __align__(8) uint64_t s_ldbar;
-    __shared__ __align__(8) uint64_t s_obar;   // output tile landed
+    __shared__ __align__(8) uint64_t s_mbar[2];   // products of a unit done, per TMEM accumulator
+    __shared__ __align__(8) uint64_t s_abar[3];   // qhat tile landed, per ring slot
+    __shared__ __align__(8) uint64_t s_obar[2];   // output tile landed, per buffer
     __shared__ uint32_t s_tmem;
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;
-    const int n_rec = pv.n_cont() + pv.n_fin();
+    const int n_cont = pv.n_cont();
     const long long u_begin = n_units * blockIdx.x / gridDim.x;
     const long long u_end = n_units * (blockIdx.x + 1) / gridDim.x;
     if (u_begin >= u_end) return;
+    const long long n_run = u_end - u_begin;
     unsigned char *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t mbar = smem_u32(&s_mbar), ldbar = smem_u32(&s_ldbar), obar = smem_u32(&s_obar);
-    const float *stg = reinterpret_cast<const float *>(smem + OFF_STG);
 
     // cursor of the first unit: each warp scans the records' tile counts 32 at a time (inclusive
     // prefix sums over the lanes) and takes the first record whose running count passes the unit
-    Cursor c{static_cast<int>(u_begin / units_per_head), 0, 0};
+    Cursor c0{static_cast<int>(u_begin / units_per_head), 0, 0};
     {
         int rem = static_cast<int>(u_begin % units_per_head);
-        for (int b = 0; b < n_rec; b += 32) {
+        for (int b = 0; b < n_cont; b += 32) {
             const int i = b + lane;
-            const int nt = i >= n_rec ? 0 : (i < pv.n_cont() ? (pv.cont(i)[3] + TR - 1) / TR : 1);
+            const int nt = i >= n_cont ? 0 : record_units(pv, i);
             int incl = nt;
 #pragma unroll
             for (int sh = 1; sh < 32; sh <<= 1) {
@@ -128,156 +142,186 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
             const int total = __shfl_sync(0xffffffffu, incl, 31);
             if (rem < total) {
                 const int l = __ffs(__ballot_sync(0xffffffffu, incl > rem)) - 1;
-                c.rec = b + l;
-                c.tile = rem - __shfl_sync(0xffffffffu, incl - nt, l);
+                c0.rec = b + l;
+                c0.tile = rem - __shfl_sync(0xffffffffu, incl - nt, l);
                 break;
             }
             rem -= total;
         }
     }
-    Rec ri = rec_info(pv, H, c.h, c.rec);
+    // units n .. n + 3 of the run (cursor and record; valid while inside the run)
+    Rec r0 = rec_info(pv, H, c0.h, c0.rec, c0.tile);
+    Cursor c1 = c0, c2, c3;
+    Rec r1 = r0, r2 = r0, r3 = r0;
+    if (n_run > 1) { advance(c1, r0, n_cont); r1 = rec_info(pv, H, c1.h, c1.rec, c1.tile); }
+    c2 = c1;
+    if (n_run > 2) { advance(c2, r1, n_cont); r2 = rec_info(pv, H, c2.h, c2.rec, c2.tile); }
+    c3 = c2;
+    if (n_run > 3) { advance(c3, r2, n_cont); r3 = rec_info(pv, H, c3.h, c3.rec, c3.tile); }
 
     if (tid == 0) {
-        mbar_init(mbar, 1);
-        mbar_init(ldbar, 1);
-        mbar_init(obar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s_mbar[i]), 1);
+            mbar_init(smem_u32(&s_obar[i]), 1);
+        }
+        for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&s_abar[i]), 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tbase = s_tmem;
-    uint32_t ld_phase = 0, mma_phase = 0, o_phase = 0;
-    bool ok = true, pending = false, o_pending = false;
+    uint32_t mph = 0, aph = 0, oph = 0;   // bit i: parity of the next wait on barrier i of each kind
+    bool ok = true;
+    bool a_pend[3] = {false, false, false}, o_pend[2] = {false, false};   // thread 0's copies in flight
+    uint32_t m_pend = 0;   // thread 0: bit t, products issued into accumulator t and not yet waited for
 
-    auto fetch_S = [&](int h, int seg) {
-        mbar_arrive_expect_tx(ldbar, 65536u);
-        bulk_g2s(sbase + OFF_STG, S_in + (static_cast<size_t>(seg) * H + h) * KD * VD, 65536u, ldbar);
+    // a continuing unit's qhat tile arrives by TMA (when the map exists)
+    auto via_tma = [&](const Rec &r) { return r.seq < 0 && has_tq != 0; };
+    // a unit whose output tile goes through a buffer: 128 continuing tokens
+    auto tiled = [&](const Rec &r) { return r.seq < 0 && r.rows == TR; };
+    auto fetch_q = [&](const Rec &r, int sl) {   // thread 0
+        const uint32_t bar = smem_u32(&s_abar[sl]);
+        mbar_arrive_expect_tx(bar, 2 * BOX);
+        const int row = r.qrow;
+        tma_load_3d(sbase + OFF_A + sl * 2 * BOX, &tm_q, 0, 0, row, bar);
+        tma_load_3d(sbase + OFF_A + sl * 2 * BOX + BOX, &tm_q, 64, 0, row, bar);
+        a_pend[sl] = true;
     };
-    // a unit whose output tile goes through the buffer: 128 continuing tokens
-    auto tiled = [&](const Rec &r, int tile) { return r.seq < 0 && r.rows_total - tile * TR >= TR; };
-    auto fetch_o = [&](const Rec &r, int tile, int h) {   // thread 0
-        mbar_arrive_expect_tx(obar, 32768u);
-        const int z = r.t_first + tile * TR;
-        tma_load_3d(sbase + OFF_OB, &tm_o, 0, h, z, obar);
-        tma_load_3d(sbase + OFF_OB + 16384, &tm_o, 64, h, z, obar);
+    auto fetch_o = [&](const Rec &r, int h, int t) {   // thread 0
+        const uint32_t bar = smem_u32(&s_obar[t]);
+        mbar_arrive_expect_tx(bar, 2 * BOX);
+        const int z = r.tok;
+        tma_load_3d(sbase + OFF_OB + t * 2 * BOX, &tm_o, 0, h, z, bar);
+        tma_load_3d(sbase + OFF_OB + t * 2 * BOX + BOX, &tm_o, 64, h, z, bar);
+        o_pend[t] = true;
     };
-    auto fetch_tile = [&](const Rec &r, int tile) {
-        const uint32_t rows = static_cast<uint32_t>(min(TR, r.rows_total - tile * TR));
-        const size_t e0 = r.src + static_cast<size_t>(tile) * TR * KD;
-        const void *base = r.seq < 0 ? static_cast<const void *>(qhat + e0) : static_cast<const void *>(afin + e0);
-        const uint32_t bytes = rows * KD * (r.seq < 0 ? 2u : 4u);
-        mbar_arrive_expect_tx(ldbar, bytes);
-        bulk_g2s(sbase + OFF_STG, base, bytes, ldbar);
+    // a unit's products into accumulator t (thread 0): qhat in ring slot sl, or a transition with its
+    // hi part in slot sl and its lo part in output buffer t
+    auto issue_mma = [&](const Rec &r, int sl, int t) {
+        if (via_tma(r)) {
+            ok &= mbar_wait(smem_u32(&s_abar[sl]), (aph >> sl) & 1u);
+            aph ^= 1u << sl;
+            a_pend[sl] = false;
+        }
+        fence_after();
+        const uint32_t id = idesc_bf16(128, 128);
+        const uint32_t a_hi = sbase + OFF_A + sl * 2 * BOX, a_lo = sbase + OFF_OB + t * 2 * BOX;
+        const uint32_t boff[3] = {0, TILE_B, 0};
+        const int terms = r.seq < 0 ? 2 : 3;   // qhat is exact in bf16: no lo * hi product
+        for (int ps = 0; ps < terms; ++ps) {
+            const uint32_t a = ps < 2 ? a_hi : a_lo;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tbase + t * 128, sdesc_sw128(a + (kk >> 2) * BOX + (kk & 3) * 32),
+                         sdesc(sbase + OFF_B + boff[ps] + kk * 2 * LBO_B, LBO_B), id, (ps | kk) != 0);
+        }
+        commit(smem_u32(&s_mbar[t]));
+        m_pend |= 1u << t;
     };
 
-    int key_h = -1, key_seg = -1;
-    if (tid == 0) fetch_S(c.h, ri.seg);
-    pending = true;
-    if (tiled(ri, c.tile)) {
-        if (tid == 0) fetch_o(ri, c.tile, c.h);
-        o_pending = true;
+    if (tid == 0) {
+        if (via_tma(r0)) fetch_q(r0, 0);
+        if (n_run > 1 && via_tma(r1)) fetch_q(r1, 1);
+        if (n_run > 2 && via_tma(r2)) fetch_q(r2, 2);
+        if (tiled(r0)) fetch_o(r0, c0.h, 0);
     }
 
-    for (long long u = u_begin; u < u_end; ++u) {
-        if (c.h != key_h || ri.seg != key_seg) {
-            // S_in[j] (rows k, cols c) -> S_in^T operand (rows c, cols k) as bf16 hi/lo
-            ok &= mbar_wait(ldbar, ld_phase++ & 1);
-            pending = false;
-            const int cc = tid & 127, kh = tid >> 7;
+    int key_h = -1, key_seg = -1;   // the S_in whose split is in the B operand
+    bool issued = false;            // unit n's products were issued during the previous unit
+    int sl = 0;                     // ring slot of unit n (n mod 3)
+    for (long long n = 0; n < n_run; ++n, sl = sl == 2 ? 0 : sl + 1) {
+        const int t = static_cast<int>(n & 1);
+        const int sl1 = sl == 2 ? 0 : sl + 1;
+        const int rows = r0.rows;
+        if (!issued) {
+            // operands of unit n by the threads; the previous unit's products have completed
+            if (c0.h != key_h || r0.seg != key_seg) {
+                // S_in[j] (rows k, cols c), read straight from HBM -> S_in^T operand (rows c, cols k)
+                // (all 64 loads of a thread in flight at once)
+                const float *src = S_in + (static_cast<size_t>(r0.seg) * H + c0.h) * KD * VD;
+                const int cc = tid & 127, kh = tid >> 7;
+                float xs[64];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float x[8];
+                for (int e = 0; e < 64; ++e) xs[e] = src[(kh * 64 + e) * VD + cc];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = stg[(kh * 64 + 8 * m + e) * VD + cc];
-                uint32_t hi[4], lo[4];
+                for (int m = 0; m < 8; ++m) {
+                    const float *x = xs + 8 * m;
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], hi[p], lo[p]);
-                const uint32_t off = cm_off(cc, kh * 64 + 8 * m, LBO_B);
-                *reinterpret_cast<uint4 *>(smem + OFF_B + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + OFF_B + TILE_B + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int p = 0; p < 4; ++p) split_bf16x2(x[2 * p], x[2 * p + 1], hi[p], lo[p]);
+                    const uint32_t off = cm_off(cc, kh * 64 + 8 * m, LBO_B);
+                    *reinterpret_cast<uint4 *>(smem + OFF_B + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(smem + OFF_B + TILE_B + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                key_h = c0.h;
+                key_seg = r0.seg;
+            }
+            if (r0.seq >= 0) {
+                // transition rows (fp32, rows r, cols k) -> hi in ring slot sl, lo in output buffer t
+                // (128-byte swizzle), once that buffer's last store has read it
+                if (tid == 0) bulk_wait_read_all();
+                __syncthreads();
+                const float *src = afin + r0.src;
+                float4 xa[16];   // all loads of a thread in flight at once
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int id = tid + 256 * i, r = id >> 5, k = (id & 31) * 4;
+                    xa[i] = *reinterpret_cast<const float4 *>(src + r * KD + k);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int id = tid + 256 * i, r = id >> 5, k = (id & 31) * 4;
+                    const float4 x = xa[i];
+                    uint32_t h0, h1, l0, l1;
+                    split_bf16x2(x.x, x.y, h0, l0);
+                    split_bf16x2(x.z, x.w, h1, l1);
+                    const uint32_t off = (k >> 6) * BOX + sw128(r, (k & 63) >> 3) + (k & 7) * 2;
+                    *reinterpret_cast<uint2 *>(smem + OFF_A + sl * 2 * BOX + off) = make_uint2(h0, h1);
+                    *reinterpret_cast<uint2 *>(smem + OFF_OB + t * 2 * BOX + off) = make_uint2(l0, l1);
+                }
+            } else if (!has_tq) {
+                // qhat rows (bf16) by the threads into ring slot sl; rows past the record are zero
+                const uint16_t *src = qhat + r0.src;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int id = tid + 256 * i, r = id >> 4, c8 = id & 15;
+                    const uint4 x = r < rows ? *reinterpret_cast<const uint4 *>(src + r * KD + c8 * 8)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(smem + OFF_A + sl * 2 * BOX + (c8 >> 3) * BOX + sw128(r, c8 & 7)) = x;
+                }
             }
             fence_async_smem();
-            __syncthreads();
-            if (tid == 0) fetch_tile(ri, c.tile);
-            pending = true;
-            key_h = c.h;
-            key_seg = ri.seg;
+            fence_before();
+            __syncthreads();   // operands written
+            if (tid == 0) issue_mma(r0, sl, t);
         }
-        const int rows = min(TR, ri.rows_total - c.tile * TR);
-        ok &= mbar_wait(ldbar, ld_phase++ & 1);
-        pending = false;
-        if (ri.seq < 0) {
-            // qhat tile (bf16 rows) -> operand (rows r, cols k); rows past the record are zero.  Lanes
-            // take consecutive 8-column pieces of a row.
-            const unsigned char *sb = smem + OFF_STG;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int id = tid + 256 * i, r = id >> 4, c8 = id & 15;
-                const uint4 x = r < rows ? *reinterpret_cast<const uint4 *>(sb + r * 256 + c8 * 16)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(smem + OFF_A + cm_off(r, c8 * 8, LBO_A)) = x;
-            }
-        } else {
-            // transition tile (fp32 rows) -> operand as bf16 hi/lo; lanes take consecutive 4-column pieces
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int id = tid + 256 * i, r = id >> 5, c4 = id & 31;
-                const float4 x = *reinterpret_cast<const float4 *>(stg + r * KD + c4 * 4);
-                const uint32_t off = cm_off(r, c4 * 4, LBO_A);
-                split_store4(smem, OFF_A + off, OFF_A + TILE_A + off, x);
-            }
-        }
-        fence_async_smem();
-        fence_before();
-        __syncthreads();   // staging read, operands written, previous epilogue done with TMEM
-
-        // the next unit, and the copy it needs first
-        Cursor nc = c;
-        if (++nc.tile == ri.nt) {
-            nc.tile = 0;
-            if (++nc.rec == n_rec) {
-                nc.rec = 0;
-                ++nc.h;
-            }
-        }
-        const bool more = u + 1 < u_end;
-        Rec nri = ri;
-        if (more) nri = rec_info(pv, H, nc.h, nc.rec);
+        // the next unit: its products now when they need nothing from the threads (same S_in, qhat
+        // tile by TMA), and its output tile once the store from that buffer (unit n - 1) has read it
+        const bool more1 = n + 1 < n_run;
+        const bool early = more1 && via_tma(r1) && c1.h == key_h && r1.seg == key_seg;
         if (tid == 0) {
-            fence_after();
-            if (more) {
-                if (nc.h != key_h || nri.seg != key_seg)
-                    fetch_S(nc.h, nri.seg);
-                else
-                    fetch_tile(nri, nc.tile);
+            if (early) issue_mma(r1, sl1, t ^ 1);
+            if (more1 && tiled(r1)) {
+                bulk_wait_read_all();
+                fetch_o(r1, c1.h, t ^ 1);
             }
-            const uint32_t id = idesc_bf16(128, 128);
-            const uint32_t aoff[3] = {0, 0, TILE_A}, boff[3] = {0, TILE_B, 0};
-            const int terms = ri.seq < 0 ? 2 : 3;   // qhat is exact in bf16: no lo * hi product
-            for (int ps = 0; ps < terms; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tbase, sdesc(sbase + OFF_A + aoff[ps] + kk * 2 * LBO_A, LBO_A),
-                             sdesc(sbase + OFF_B + boff[ps] + kk * 2 * LBO_B, LBO_B), id, (ps | kk) != 0);
-            commit(mbar);
         }
-        pending = more;
 
-        // fetch this thread's destination row piece while the tensor core works (units whose
-        // output tile is not in the buffer)
-        const bool tl_unit = tiled(ri, c.tile);
+        // epilogue of unit n: fetch this thread's destination row piece while the tensor core works
+        // (units whose output tile is not in a buffer)
+        const bool tl_unit = tiled(r0);
         const int r = quad * 32 + lane;
         const bool live = r < rows && !tl_unit;
         uint4 ow[8];
         float4 fw[16];
         uint4 *odst = nullptr;
         float4 *fdst = nullptr;
-        if (ri.seq < 0)
-            odst = reinterpret_cast<uint4 *>(o + (static_cast<size_t>(ri.t_first + c.tile * TR + r) * H + c.h) * VD +
+        if (r0.seq < 0)
+            odst = reinterpret_cast<uint4 *>(o + (static_cast<size_t>(r0.tok + r) * H + c0.h) * VD +
                                              hw * 64);
         else
-            fdst = reinterpret_cast<float4 *>(final_state + ((static_cast<size_t>(ri.seq) * H + c.h) * KD + r) * VD +
+            fdst = reinterpret_cast<float4 *>(final_state + ((static_cast<size_t>(r0.seq) * H + c0.h) * KD + r) * VD +
                                               hw * 64);
         if (live) {
             if (odst) {
@@ -288,12 +332,16 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
                 for (int m = 0; m < 16; ++m) fw[m] = fdst[m];
             }
         }
-        ok &= mbar_wait(mbar, mma_phase++ & 1);
+        ok &= mbar_wait(smem_u32(&s_mbar[t]), (mph >> t) & 1u);
+        mph ^= 1u << t;
+        m_pend &= ~(1u << t);
         fence_after();
+        // ring slot sl is free again: the qhat tile three units on
+        if (tid == 0 && n + 3 < n_run && via_tma(r3)) fetch_q(r3, sl);
         float d[64];
         {
             float d0[32], d1[32];
-            const uint32_t ta = tbase + (static_cast<uint32_t>(quad * 32) << 16) + hw * 64;
+            const uint32_t ta = tbase + t * 128 + (static_cast<uint32_t>(quad * 32) << 16) + hw * 64;
             tmem_ld32(ta, d0);
             tmem_ld32(ta + 32, d1);
 #pragma unroll
@@ -302,10 +350,11 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
                 d[32 + j] = d1[j];
             }
         }
-        if (tl_unit) {   // output tile in the buffer: update in place (row r, this half's box)
-            ok &= mbar_wait(obar, o_phase++ & 1);
-            o_pending = false;
-            unsigned char *box = smem + OFF_OB + hw * 16384;
+        if (tl_unit) {   // output tile in buffer t: update in place (row r, this half's box)
+            ok &= mbar_wait(smem_u32(&s_obar[t]), (oph >> t) & 1u);
+            oph ^= 1u << t;
+            if (tid == 0) o_pend[t] = false;
+            unsigned char *box = smem + OFF_OB + t * 2 * BOX + hw * BOX;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 uint4 *p = reinterpret_cast<uint4 *>(box + sw128(r, m));
@@ -341,28 +390,35 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
         }
         fence_before();
         if (!__syncthreads_and(ok)) break;
-        if (tid == 0 && (tl_unit || (more && tiled(nri, nc.tile)))) {
-            if (tl_unit) {   // write the tile back; the buffer is free once the store has read it
-                const int z = ri.t_first + c.tile * TR;
-                tma_store_3d(&tm_o, 0, c.h, z, sbase + OFF_OB);
-                tma_store_3d(&tm_o, 64, c.h, z, sbase + OFF_OB + 16384);
-                bulk_commit_group();
-                bulk_wait_read_all();
-            }
-            if (more && tiled(nri, nc.tile)) fetch_o(nri, nc.tile, nc.h);
+        if (tid == 0 && tl_unit) {   // write the tile back; its buffer is refilled two units on
+            const int z = r0.tok;
+            tma_store_3d(&tm_o, 0, c0.h, z, sbase + OFF_OB + t * 2 * BOX);
+            tma_store_3d(&tm_o, 64, c0.h, z, sbase + OFF_OB + t * 2 * BOX + BOX);
+            bulk_commit_group();
         }
-        if (more && tiled(nri, nc.tile)) o_pending = true;
-        c = nc;
-        ri = nri;
+        issued = early;
+        c0 = c1;
+        r0 = r1;
+        c1 = c2;
+        r1 = r2;
+        c2 = c3;
+        r2 = r3;
+        if (n + 4 < n_run) {
+            advance(c3, r3, n_cont);
+            r3 = rec_info(pv, H, c3.h, c3.rec, c3.tile);
+        }
     }
     if (tid == 0) bulk_wait_all();   // output tiles stored before the CTA exits
     if (!__syncthreads_and(ok)) {
-        // a wait gave up: record it, and let any copy still in flight land before the CTA exits
+        // a wait gave up: record it, and let any copy or product still in flight land (bounded waits)
         if (tid == 0) {
             atomicExch(&g_boundary_status, KDA_ERR_TIMEOUT);
-            if (pending) mbar_wait(ldbar, ld_phase & 1);
-            if (o_pending) mbar_wait(obar, o_phase & 1);
-            mbar_wait(mbar, mma_phase & 1);
+            for (int i = 0; i < 3; ++i)
+                if (a_pend[i]) mbar_wait(smem_u32(&s_abar[i]), (aph >> i) & 1u);
+            for (int i = 0; i < 2; ++i) {
+                if (o_pend[i]) mbar_wait(smem_u32(&s_obar[i]), (oph >> i) & 1u);
+                if ((m_pend >> i) & 1u) mbar_wait(smem_u32(&s_mbar[i]), (mph >> i) & 1u);
+            }
         }
         __syncthreads();
     }
@@ -379,20 +435,27 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
                             cudaStream_t stream)
 {
     const PlanView pv{plan_host};
-    long long per_head = pv.n_fin();
+    long long per_head = pv.n_fin();   // every transition belongs to a continuing record
     for (int i = 0; i < pv.n_cont(); ++i) per_head += (pv.cont(i)[3] + TR - 1) / TR;
     if (per_head == 0) return cudaSuccess;
     if (per_head > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const long long n_units = per_head * H;
     const long long grid = n_units < sm_count() ? n_units : sm_count();
-    CUtensorMap to{};   // only full 128-row tiles use it, so T < 128 never reads it
+    // full 128-row output tiles and every qhat tile go through tiled TMA; a tensor shorter than one
+    // tile never uses its map (qhat tiles are then read by the threads)
+    CUtensorMap to{}, tq{};
     if (pv.T() >= TR && !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, TR))
+        return cudaErrorInvalidValue;
+    const long long q_rows = static_cast<long long>(H) * pv.T_cont();
+    if (q_rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int has_tq = q_rows >= TR ? 1 : 0;
+    if (has_tq && !encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, TR))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(boundary_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     boundary_tc<<<static_cast<unsigned>(grid), 256, SMEM_ALLOC, stream>>>(
-        plan_dev, H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to);
+        plan_dev, H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
     return cudaGetLastError();
 }
 

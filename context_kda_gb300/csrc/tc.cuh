@@ -30,6 +30,15 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle layout (rows of
+// 128 bytes, 8-row atoms of 1024 bytes, as a 128-byte-swizzled TMA box lands): the K step of 16
+// bf16 advances the start address by 32 bytes within the atom.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
+{
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, M x N.  a_mn / b_mn
 // select an MN-major operand (the M / N index contiguous within a core-matrix row);
 // otherwise the operand is K-major.
