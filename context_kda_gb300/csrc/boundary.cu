@@ -220,6 +220,7 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
         m_pend |= 1u << t;
     };
 
+    grid_dep_wait();   // S_in, qhat and the outputs come from the previous kernels
     if (tid == 0) {
         if (via_tma(r0)) fetch_q(r0, 0);
         if (n_run > 1 && via_tma(r1)) fetch_q(r1, 1);
@@ -454,9 +455,8 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
     cudaError_t err = cudaFuncSetAttribute(boundary_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    boundary_tc<<<static_cast<unsigned>(grid), 256, SMEM_ALLOC, stream>>>(
-        plan_dev, H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
-    return cudaGetLastError();
+    return launch_dependent(boundary_tc, dim3(static_cast<unsigned>(grid)), dim3(256), SMEM_ALLOC, stream, plan_dev, H,
+                            static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
 }
 
 }  // namespace kda

@@ -96,6 +96,8 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
     __syncthreads();
     fence_after();
     const uint32_t tbase = s_tmem;
+    grid_dep_wait();     // the summaries come from the previous kernel
+    grid_dep_launch();   // the fix-up may be scheduled on SMs this kernel leaves
     uint32_t a_phase = 0, b_phase = 0, mma_phase = 0;
     bool ok = true, a_pending = false, b_pending = false;
     int n_conv = 0, n_mma = 0;   // transitions split so far / steps issued so far
@@ -288,8 +290,8 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
     cudaError_t err =
         cudaFuncSetAttribute(compose_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    compose_tc<<<H * (VD / NS), NT, SMEM_ALLOC, stream>>>(plan_dev, H, h0 ? 1 : 0, tA, tB, tH, tS);
-    return cudaGetLastError();
+    return launch_dependent(compose_tc, dim3(H * (VD / NS)), dim3(NT), SMEM_ALLOC, stream, plan_dev, H, h0 ? 1 : 0, tA,
+                            tB, tH, tS);
 }
 
 }  // namespace kda

@@ -76,6 +76,27 @@ void record_cuda_error(int err);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Launches a kernel that may begin while the previous kernel on the stream finishes (programmatic
+// dependent launch): its CTAs can be scheduled once every CTA of that kernel has signalled (or
+// exited), and the kernel itself waits (griddepcontrol.wait) before it touches anything the previous
+// kernel writes.  For kernels whose inputs come from the library's own previous kernel only.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 

@@ -303,6 +303,11 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t 
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Programmatic dependent launch: wait until the previous kernel on the stream has completed and its
+// memory operations are visible; allow the next kernel's CTAs to be scheduled.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 2^x by the SFU approximation (flushes subnormal inputs and results to zero).
 __device__ __forceinline__ float ex2_ftz(float x)
 {
