@@ -145,6 +145,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         bulk_g2s(sbase + OFF_P2 + (ci & 1) * P2_BYTES, pk_of(ci) + PK_QK, P2_BYTES, bar);
     };
     if (producer && nch > 0) {
+        grid_dep_wait();   // the packages come from the preparation kernel
         load_p1(0);
         load_p2(0);
     }
@@ -194,6 +195,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 tmem_st_split32(tl + TM_XH + k0 / 2, tl + TM_XL + k0 / 2, x);
             }
             tmem_wait_st();
+            grid_dep_wait();   // the packages come from the preparation kernel; every output write follows
             load_ut(0);
             aborted = handoff(HO_X);   // -> W X, Qt X
         }
@@ -434,9 +436,8 @@ cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev
     cudaError_t err = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    chunk_state_tc<<<static_cast<unsigned>(blocks), NTHREADS, SMEM_ALLOC, stream>>>(
-        plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, to, tq);
-    return cudaGetLastError();
+    return launch_dependent(chunk_state_tc, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC, stream,
+                            plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, to, tq);
 }
 
 // The local chunkwise forward: the chunk-parallel preparation, then the serial state pass.
