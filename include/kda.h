@@ -253,8 +253,9 @@ int kda_forward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t 
  *   - Arguments and results are those of kda_forward_segmented; the caller
  *     still passes every input and output buffer.
  *   - Returns KDA_ERR_WORKSPACE when kda_workspace_bytes(plan, H) exceeds
- *     KDA_NOALLOC_SCRATCH_BYTES (e.g. T = 4096, H = 8, S = 4 needs about 18 MiB
- *     and fits; T = 8192, H = 16, S = 4 does not).
+ *     KDA_NOALLOC_SCRATCH_BYTES (the workspace is dominated by the 123 KB chunk
+ *     packages of every chunk and head: T = 1024, H = 4, S = 2 needs about
+ *     10 MiB and fits; T = 4096, H = 8, S = 4 needs about 73 MiB and does not).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
