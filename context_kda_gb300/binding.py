@@ -35,6 +35,8 @@ def _load():
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_last_cuda_error.restype = ctypes.c_int
+    lib.kda_device_status.argtypes = []
+    lib.kda_device_status.restype = ctypes.c_int
     lib.kda_plan_segments.argtypes = [P, I32, I32, P, I32, P, ctypes.POINTER(SZ)]
     lib.kda_workspace_layout.argtypes = [P, I32, ctypes.POINTER(SZ)]
     lib.kda_workspace_bytes.argtypes = [P, I32]
@@ -59,6 +61,12 @@ def _check(fn: str, rc: int):
         if rc == KDA_ERR_CUDA:
             msg += f" (cudaError {_lib.kda_last_cuda_error()})"
         raise KDAError(fn, rc, msg)
+
+
+def kda_device_status() -> int:
+    """Synchronises the current device and returns (and clears) the kernels' device-side status:
+    KDA_OK, or KDA_ERR_TIMEOUT once a bounded wait inside a kernel expired."""
+    return int(_lib.kda_device_status())
 
 
 def _words(plan) -> np.ndarray:

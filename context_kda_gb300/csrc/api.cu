@@ -99,6 +99,20 @@ extern "C" const char *kda_status_string(int status)
 
 extern "C" int kda_last_cuda_error(void) { return g_last_cuda_error; }
 
+extern "C" int kda_device_status(void)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return KDA_ERR_CUDA;
+    }
+    int worst = KDA_OK;
+    for (int st : {kda::take_prep_status(), kda::take_state_status(), kda::take_compose_status(),
+                   kda::take_boundary_status()})
+        if (st != KDA_OK && worst == KDA_OK) worst = st;
+    return worst;
+}
+
 namespace kda {
 void record_cuda_error(int err) { g_last_cuda_error = err; }
 

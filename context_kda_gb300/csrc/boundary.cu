@@ -459,4 +459,13 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
                             static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
 }
 
+// The status word of this file's kernel: read and cleared (the caller has synchronised the device).
+int take_boundary_status()
+{
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_boundary_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_boundary_status, &z, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return v;
+}
+
 }  // namespace kda

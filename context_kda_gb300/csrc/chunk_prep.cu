@@ -602,4 +602,13 @@ cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev,
     return cudaGetLastError();
 }
 
+// The status word of this file's kernel: read and cleared (the caller has synchronised the device).
+int take_prep_status()
+{
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_prep_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_prep_status, &z, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return v;
+}
+
 }  // namespace kda

@@ -452,4 +452,13 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
     return launch_chunk_state(plan_host, plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, stream);
 }
 
+// The status word of this file's kernel: read and cleared (the caller has synchronised the device).
+int take_state_status()
+{
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_state_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_state_status, &z, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return v;
+}
+
 }  // namespace kda

@@ -294,4 +294,13 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
                             tB, tH, tS);
 }
 
+// The status word of this file's kernel: read and cleared (the caller has synchronised the device).
+int take_compose_status()
+{
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_compose_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_compose_status, &z, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return v;
+}
+
 }  // namespace kda

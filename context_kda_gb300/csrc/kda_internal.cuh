@@ -76,6 +76,13 @@ void record_cuda_error(int err);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Each kernel file's device status word (KDA_ERR_TIMEOUT once a bounded wait of its kernel expired),
+// read and cleared; the device must be synchronised first.
+int take_prep_status();
+int take_state_status();
+int take_compose_status();
+int take_boundary_status();
+
 // Launches a kernel that may begin while the previous kernel on the stream finishes (programmatic
 // dependent launch): its CTAs can be scheduled once every CTA of that kernel has signalled (or
 // exited), and the kernel itself waits (griddepcontrol.wait) before it touches anything the previous

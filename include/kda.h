@@ -120,6 +120,16 @@ const char *kda_status_string(int status);
 /* cudaError_t value behind the most recent KDA_ERR_CUDA on this thread (0 if none). */
 int kda_last_cuda_error(void);
 
+/* Device-side status of the kernels run so far on the current device: every wait
+ * inside a kernel (for a copy, a product or another thread's handoff) gives up
+ * after about two seconds, records KDA_ERR_TIMEOUT in a status word, lets its
+ * copies land, frees its tensor memory and returns, so the context stays
+ * usable but the results of that call are invalid.  This call synchronises the
+ * current device (the only entry point that does), reads every status word,
+ * clears them and returns KDA_OK, KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if the
+ * synchronisation or the read failed. */
+int kda_device_status(void);
+
 /*
  * kda_plan_segments -- packed-THD segment plan (host, integer work only).
  * PR #136 §Walkthrough: CPU-only plan construction and validation for balanced

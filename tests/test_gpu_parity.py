@@ -142,3 +142,13 @@ def test_wide_head_count_every_segment():
     res = gpu_forward(inp)
     _check_outputs(res, inp)
     _check_segments(res, inp, [(j, h) for j in range(9) for h in range(24)])
+
+
+def test_device_status_is_clear_after_every_kernel():
+    """No bounded device-side wait expired in the runs above and in a fresh one (kda_device_status
+    synchronises, reads and clears the kernels' status words)."""
+    from context_kda_gb300 import binding as kda
+    inp = make_workload(workloads()["t4096_h8_s4"])
+    gpu_forward(inp)
+    assert kda.kda_device_status() == kda.KDA_OK
+    assert kda.kda_device_status() == kda.KDA_OK
