@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -80,7 +81,8 @@ def _profile_values(kernel_srcs):
     for line in open(PROFILE_SUMMARY):
         if line.startswith("- ") and ":" in line:
             key, _, val = line[2:].partition(":")
-            vals[key.strip()] = val.strip().strip("`")
+            m = re.search(r"`([^`]*)`", val)   # the value is the first backticked token
+            vals[key.strip()] = m.group(1) if m else val.strip()
     return vals if vals.get("kernel_source_sha256_16") == sha else {}
 
 
