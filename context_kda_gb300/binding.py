@@ -37,6 +37,8 @@ def _load():
     lib.kda_last_cuda_error.restype = ctypes.c_int
     lib.kda_device_status.argtypes = []
     lib.kda_device_status.restype = ctypes.c_int
+    lib.kda_selftest_wait_expiry.argtypes = [P]
+    lib.kda_selftest_wait_expiry.restype = ctypes.c_int
     lib.kda_plan_segments.argtypes = [P, I32, I32, P, I32, P, ctypes.POINTER(SZ)]
     lib.kda_workspace_layout.argtypes = [P, I32, ctypes.POINTER(SZ)]
     lib.kda_workspace_bytes.argtypes = [P, I32]
@@ -67,6 +69,12 @@ def kda_device_status() -> int:
     """Synchronises the current device and returns (and clears) the kernels' device-side status:
     KDA_OK, or KDA_ERR_TIMEOUT once a bounded wait inside a kernel expired."""
     return int(_lib.kda_device_status())
+
+
+def kda_selftest_wait_expiry(stream=None):
+    """Enqueues a kernel whose bounded wait expires (about two seconds); kda_device_status() then
+    reports KDA_ERR_TIMEOUT."""
+    _check("kda_selftest_wait_expiry", _lib.kda_selftest_wait_expiry(_stream(stream)))
 
 
 def _words(plan) -> np.ndarray:

@@ -99,6 +99,11 @@ extern "C" const char *kda_status_string(int status)
 
 extern "C" int kda_last_cuda_error(void) { return g_last_cuda_error; }
 
+extern "C" int kda_selftest_wait_expiry(void *stream)
+{
+    return cuda_status(kda::launch_wait_expiry_probe(static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int kda_device_status(void)
 {
     cudaError_t e = cudaDeviceSynchronize();

@@ -459,6 +459,22 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
                             static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
 }
 
+// Self-test of the expiry path: one thread waits, bounded, on an mbarrier that nothing arrives on,
+// and records the expiry in this file's status word as any kernel of the library would.
+__global__ void wait_expiry_probe_tc()
+{
+    __shared__ __align__(8) uint64_t s_bar;
+    if (threadIdx.x == 0) mbar_init(smem_u32(&s_bar), 1);
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&s_bar), 0)) atomicExch(&g_boundary_status, KDA_ERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_expiry_probe(cudaStream_t stream)
+{
+    wait_expiry_probe_tc<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
 // The status word of this file's kernel: read and cleared (the caller has synchronised the device).
 int take_boundary_status()
 {

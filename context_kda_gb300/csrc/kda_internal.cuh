@@ -82,6 +82,7 @@ int take_prep_status();
 int take_state_status();
 int take_compose_status();
 int take_boundary_status();
+cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
 
 // Launches a kernel that may begin while the previous kernel on the stream finishes (programmatic
 // dependent launch): its CTAs can be scheduled once every CTA of that kernel has signalled (or

@@ -130,6 +130,12 @@ int kda_last_cuda_error(void);
  * synchronisation or the read failed. */
 int kda_device_status(void);
 
+/* Self-test of that path: enqueues a one-warp kernel whose bounded wait expires
+ * (nothing arrives on its barrier), about two seconds later; the next
+ * kda_device_status() then returns KDA_ERR_TIMEOUT and clears it.  Returns
+ * KDA_OK or KDA_ERR_CUDA (launch failure). */
+int kda_selftest_wait_expiry(void *stream);
+
 /*
  * kda_plan_segments -- packed-THD segment plan (host, integer work only).
  * PR #136 §Walkthrough: CPU-only plan construction and validation for balanced

@@ -152,3 +152,17 @@ def test_device_status_is_clear_after_every_kernel():
     gpu_forward(inp)
     assert kda.kda_device_status() == kda.KDA_OK
     assert kda.kda_device_status() == kda.KDA_OK
+
+
+def test_expired_wait_is_reported_and_the_context_survives():
+    """A kernel whose bounded wait runs out (nothing arrives on its barrier) records KDA_ERR_TIMEOUT;
+    kda_device_status reports it once, and the library keeps working afterwards."""
+    from context_kda_gb300 import binding as kda
+    assert kda.kda_device_status() == kda.KDA_OK
+    kda.kda_selftest_wait_expiry()
+    assert kda.kda_device_status() == kda.KDA_ERR_TIMEOUT
+    assert kda.kda_device_status() == kda.KDA_OK
+    inp = make_workload(workloads()["t1024_h4_s2"])
+    res = gpu_forward(inp)
+    _check_outputs(res, inp)
+    assert kda.kda_device_status() == kda.KDA_OK
