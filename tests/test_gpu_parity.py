@@ -110,6 +110,18 @@ def test_edge_cases_all_heads(seqlens, S, h0_std, scale):
     _check_segments(res, inp, [(j, h) for j in range(S) for h in range(2)])
 
 
+def test_long_ragged_pieces_with_few_chains():
+    """Few, long pieces of unequal length (ragged last chunks, a one-chunk sequence, continuing
+    pieces, chains of very different lengths side by side), every head and segment; a second
+    launch gives the same bits."""
+    inp = make_inputs([1800, 2300, 63, 1400], heads=4, segments=4, h0_std=0.1, seed=15, g_lo=-0.2)
+    res = gpu_forward(inp)
+    _check_outputs(res, inp)
+    _check_segments(res, inp, [(j, h) for j in range(4) for h in range(4)])
+    again = gpu_forward(inp)
+    assert np.array_equal(res["o"], again["o"]) and np.array_equal(res["final"], again["final"])
+
+
 def test_custom_segment_bounds():
     inp = make_inputs([130, 70, 300], heads=2, segments=4, h0_std=0.1, seed=12)
     bounds = [0, 1, 129, 333, 500]
