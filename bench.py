@@ -7,11 +7,14 @@ one batch of the synthetic workload, inputs resident in HBM.  The L2 cache is
 flushed (a 256 MiB write) before every step, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                  [--path fix_up|two_pass]
 
 N > 1 is launched with torch.distributed.run: every rank runs its own copy of
 the workload (independent problems, no collective on the data path), so the
 value is the tokens of all ranks over the slowest rank's time ("weak" scaling).
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+``--path two_pass`` times kda_forward_two_pass (the forward from preceding
+summaries, no fix-up) in place of the three calls, for comparison.
 """
 from __future__ import annotations
 
@@ -227,8 +230,20 @@ def run_ours(args, w, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     n_cont, n_fin = int(plan[8]), int(plan[10])
     launches_per_step = 3 + (1 if (n_cont + n_fin) > 0 else 0)   # prep, state, compose (+ fix-up)
+    two_pass = args.path == "two_pass"
+    if two_pass:
+        launches_per_step = 4   # prep, summary pass, compose, output pass
 
     def step(evs=None):
+        if two_pass:   # one call: the whole step is its first interval
+            if evs:
+                evs[0].record(stream)
+            kda.kda_forward_two_pass(plan, plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], h0, 1.0, o, fin,
+                                     ws, stream)
+            if evs:
+                for e in evs[1:]:
+                    e.record(stream)
+            return
         if evs:
             evs[0].record(stream)
         kda.kda_segment_forward(plan, plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], h0, 1.0, o, A, B,
@@ -293,8 +308,9 @@ def run_ours(args, w, rank, world, local_rank):
             dd = ln["d"]
             for k_ in pinned:
                 dd[k_].copy_(pinned[k_], non_blocking=True)
-            kda.kda_forward_segmented(plan, plan_dev, H, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd.get("h0"),
-                                      1.0, ln["o"], ln["fin"], ln["ws"], ln["stream"])
+            run = kda.kda_forward_two_pass if two_pass else kda.kda_forward_segmented
+            run(plan, plan_dev, H, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd.get("h0"), 1.0, ln["o"],
+                ln["fin"], ln["ws"], ln["stream"])
             ln["o_host"].copy_(ln["o"], non_blocking=True)
             ln["f_host"].copy_(ln["fin"], non_blocking=True)
 
@@ -341,26 +357,32 @@ def run_ours(args, w, rank, world, local_rank):
         ln = int(plan[pieces_off + 8 * pc + 1])
         issued += ((ln + CH - 1) // CH) * ISSUED_STATE_PER_CHUNK * H
     prof = _profile_values(CHUNK_KERNEL_SRCS)
-    traffic = float(prof["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in prof else None
+    traffic = float(prof["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in prof and not two_pass else None
     shares = (kern_ms / kern_ms.sum()).tolist()
+    kernel = "two_pass_forward" if two_pass else "chunk_forward"
+    if two_pass:   # the issued-flop count below is the fix-up path's
+        issued = None
     line = {
         "metric": METRIC, "value": world * T / (step_ms / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 state", "data": "synthetic",
-        "config": _config(w, world),
-        "kernels_ms": {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]},
-        "kernel_shares": {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]},
-        "roofline": ({"bound": "hbm", "kernel": "chunk_forward", "achieved": achieved_gbs,
+        "config": _config(w, world) | ({"path": "two_pass"} if two_pass else {}),
+        "kernels_ms": ({"two_pass_forward": kern_ms[0]} if two_pass else
+                       {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]}),
+        "kernel_shares": ({"two_pass_forward": 1.0} if two_pass else
+                          {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]}),
+        "roofline": ({"bound": "hbm", "kernel": kernel, "achieved": achieved_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
                       "peak_source": f"{peaks['source']} HBM copy"}
                      if t_hbm >= t_tensor else
-                     {"bound": "tensor", "kernel": "chunk_forward", "achieved": achieved_tflops,
+                     {"bound": "tensor", "kernel": kernel, "achieved": achieved_tflops,
                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved_tflops / peaks["bf16_tflops"],
                       "peak_source": f"{peaks['source']} bf16 dense (burst)"})
         | {"traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
            "algorithmic_flops_per_launch": flops, "tensor_frac": achieved_tflops / peaks["bf16_tflops"],
            "issued_tensor_flops_per_launch": issued,
-           "issued_frac": issued / sec / 1e12 / peaks["bf16_tflops"], "hbm_peak_gbs": peaks["hbm_gbs"],
+           "issued_frac": None if issued is None else issued / sec / 1e12 / peaks["bf16_tflops"],
+           "hbm_peak_gbs": peaks["hbm_gbs"],
            "bf16_peak_tflops": peaks["bf16_tflops"]},
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -383,6 +405,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-soak-s", type=float, default=1.0)
+    ap.add_argument("--path", default="fix_up", choices=["fix_up", "two_pass"],
+                    help="fix_up: the three calls (local forward, composition, fix-up); two_pass: "
+                         "kda_forward_two_pass (state pass from the preceding summaries, no fix-up)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     rank = int(os.environ.get("RANK", "0"))

@@ -48,8 +48,10 @@ def _load():
     lib.kda_apply_boundary.argtypes = [P, P, I32, P, P, SZ, P, P, P]
     lib.kda_forward_segmented.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.kda_forward_segmented_noalloc.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P]
+    lib.kda_forward_two_pass.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
     for name in ("kda_plan_segments", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
-                 "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc"):
+                 "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc",
+                 "kda_forward_two_pass"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -164,6 +166,16 @@ def kda_forward_segmented(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, fin
                                     _dp(h0), float(scale), _dp(o), _dp(final_state), _dp(ws), _nbytes(ws),
                                     _stream(stream))
     _check("kda_forward_segmented", rc)
+
+
+def kda_forward_two_pass(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, final_state, ws, stream=None):
+    """The segmented forward from preceding summaries (see include/kda.h): the same arguments and
+    results as kda_forward_segmented, with the state pass run twice and no fix-up."""
+    p = _words(plan)
+    rc = _lib.kda_forward_two_pass(_hp(p), _dp(plan_dev), int(H), _dp(q), _dp(k), _dp(v), _dp(g), _dp(beta),
+                                   _dp(h0), float(scale), _dp(o), _dp(final_state), _dp(ws), _nbytes(ws),
+                                   _stream(stream))
+    _check("kda_forward_two_pass", rc)
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

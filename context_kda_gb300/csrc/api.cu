@@ -256,3 +256,19 @@ extern "C" int kda_forward_segmented(const int32_t *plan, const int32_t *plan_de
     if (rc != KDA_OK) return rc;
     return cuda_status(kda::launch_boundary(plan, plan_dev, H, w.S_in, w.qhat, w.afin, o, final_state, s));
 }
+
+extern "C" int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                    const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                    const float *g, const float *beta, const float *h0, float scale,
+                                    kda_bf16 *o, float *final_state, void *ws, size_t ws_bytes, void *stream)
+{
+    size_t off[7];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
+    if (!o || !final_state || !aligned16(o) || !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < off[6]) return KDA_ERR_WORKSPACE;
+    const kda::Workspace w = carve(ws, off);
+    return cuda_status(kda::launch_two_pass(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, w.A, w.B, w.S_in,
+                                            final_state, w.pkg, static_cast<cudaStream_t>(stream)));
+}

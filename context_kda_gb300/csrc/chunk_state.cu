@@ -75,11 +75,20 @@ __device__ __forceinline__ void tmem_st_split32(uint32_t t_hi, uint32_t t_lo, co
     tmem_st16_nowait(t_lo, l);
 }
 
+// What a launch of the state pass produces.
+enum StateMode {
+    STATE_LOCAL = 0,     // every item: local outputs, qhat, summaries, local final states
+    STATE_SUMMARY = 1,   // only the last piece of each segment, only its summary (A, B)
+    STATE_OUTPUT = 2,    // the state-column item of every piece from its true incoming state (h0 or
+                         // S_in of its segment): exact outputs and final states, no summaries
+};
+
+template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ h0,
-               const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o, float *__restrict__ A,
-               float *__restrict__ B, float *__restrict__ fin_state, uint16_t *__restrict__ qhat,
-               float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
+               const float *__restrict__ s_in, const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o,
+               float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
+               uint16_t *__restrict__ qhat, float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
                const __grid_constant__ CUtensorMap tm_q)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -103,6 +112,12 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     const int32_t *pc = pv.piece(p);
     const int start = pc[PC_START], len = pc[PC_LEN], seq = pc[PC_SEQ], seg = pc[PC_SEG];
     const int flags = pc[PC_FLAGS], row0 = pc[PC_ROW], fin = pc[PC_FIN];
+    if constexpr (MODE == STATE_SUMMARY) {
+        if (!(flags & KDA_PIECE_SEG_LAST)) return;   // no part in a segment summary
+    }
+    if constexpr (MODE == STATE_OUTPUT) {
+        if (kind != 0) return;   // transitions are summaries
+    }
     const int64_t T_cont = pv.T_cont();
     const int nch = (len + CH - 1) / CH;
     // global index of the piece's first chunk (chunks are numbered piece by piece): each warp sums
@@ -180,8 +195,15 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     if (worker) {
         // ---- piece start: X^T into TMEM, fp32 and as its bf16 split
         {
-            const bool from_h0 = kind == 0 && (flags & KDA_PIECE_FIRST) && h0 != nullptr;
+            bool from_h0 = kind == 0 && (flags & KDA_PIECE_FIRST) && h0 != nullptr;
             const float *src = h0 + (static_cast<size_t>(seq) * H + h) * KD * VD;
+            if constexpr (MODE == STATE_OUTPUT) {
+                grid_dep_wait();   // S_in comes from the composition
+                if (flags & KDA_PIECE_CONT) {   // the true state entering the segment
+                    from_h0 = true;
+                    src = s_in + (static_cast<size_t>(seg) * H + h) * KD * VD;
+                }
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 float x[32];
@@ -247,51 +269,53 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                 tmem_wait_st();
                 aborted = handoff(HO_X);   // -> next chunk's W X, Qt X (they overlap the stores below)
                 if (aborted) break;
-                // O^T[c][r] -> bf16 tile of rows r in the TMA store layout (128-byte swizzle; the
-                // previous tile was read before the U^T handoff), then outputs (state columns) or
-                // qhat (transition columns) go out by tiled TMA stores; a ragged last chunk by 16-byte
-                // stores of its rows
-                if (!mbar_wait_warp(mbar_o, ci & 1)) bad = true;
-                fence_after();
-                {
-                    uint32_t od[32];
-                    tmem_ld32_nowait(tl + ((ci & 1) ? TM_O1 : TM_O0) + hw * 32, od);   // O^T[c][r = hw*32 + j]
-                    tmem_wait_ld();
-                    reg_fence32(od);
-                    unsigned char *ob = base + OFF_OB + (c_lane >> 6) * 8192 + (c_lane & 7) * 2;
-                    const int ch = (c_lane & 63) >> 3;
+                if constexpr (MODE != STATE_SUMMARY) {
+                    // O^T[c][r] -> bf16 tile of rows r in the TMA store layout (128-byte swizzle; the
+                    // previous tile was read before the U^T handoff), then outputs (state columns) or
+                    // qhat (transition columns) go out by tiled TMA stores; a ragged last chunk by 16-byte
+                    // stores of its rows
+                    if (!mbar_wait_warp(mbar_o, ci & 1)) bad = true;
+                    fence_after();
+                    {
+                        uint32_t od[32];
+                        tmem_ld32_nowait(tl + ((ci & 1) ? TM_O1 : TM_O0) + hw * 32, od);   // O^T[c][r = hw*32 + j]
+                        tmem_wait_ld();
+                        reg_fence32(od);
+                        unsigned char *ob = base + OFF_OB + (c_lane >> 6) * 8192 + (c_lane & 7) * 2;
+                        const int ch = (c_lane & 63) >> 3;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {   // one conversion per pair of rows
-                        const uint32_t w = bf16x2_bits(__uint_as_float(od[j]), __uint_as_float(od[j + 1]));
-                        *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j, ch)) = static_cast<uint16_t>(w);
-                        *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j + 1, ch)) = static_cast<uint16_t>(w >> 16);
-                    }
-                }
-                fence_async_smem();
-                bar_sync1(NWORK);
-                if (L == CH) {
-                    if (tid == 0) {
-                        if (kind == 0) {
-                            tma_store_3d(&tm_o, 0, h, t0, sbase + OFF_OB);
-                            tma_store_3d(&tm_o, 64, h, t0, sbase + OFF_OB + 8192);
-                        } else {
-                            const int row = static_cast<int>(static_cast<int64_t>(h) * T_cont + row0 + ci * CH);
-                            tma_store_3d(&tm_q, 0, 0, row, sbase + OFF_OB);
-                            tma_store_3d(&tm_q, 64, 0, row, sbase + OFF_OB + 8192);
+                        for (int j = 0; j < 32; j += 2) {   // one conversion per pair of rows
+                            const uint32_t w = bf16x2_bits(__uint_as_float(od[j]), __uint_as_float(od[j + 1]));
+                            *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j, ch)) = static_cast<uint16_t>(w);
+                            *reinterpret_cast<uint16_t *>(ob + sw128(hw * 32 + j + 1, ch)) = static_cast<uint16_t>(w >> 16);
                         }
-                        bulk_commit_group();
                     }
-                } else {
-                    uint16_t *const dst_row0 = kind == 0
-                                                   ? o + (static_cast<size_t>(t0) * H + h) * VD
-                                                   : qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH) * KD;
-                    const size_t row_stride = kind == 0 ? static_cast<size_t>(H) * VD : KD;
+                    fence_async_smem();
+                    bar_sync1(NWORK);
+                    if (L == CH) {
+                        if (tid == 0) {
+                            if (kind == 0) {
+                                tma_store_3d(&tm_o, 0, h, t0, sbase + OFF_OB);
+                                tma_store_3d(&tm_o, 64, h, t0, sbase + OFF_OB + 8192);
+                            } else {
+                                const int row = static_cast<int>(static_cast<int64_t>(h) * T_cont + row0 + ci * CH);
+                                tma_store_3d(&tm_q, 0, 0, row, sbase + OFF_OB);
+                                tma_store_3d(&tm_q, 64, 0, row, sbase + OFF_OB + 8192);
+                            }
+                            bulk_commit_group();
+                        }
+                    } else {
+                        uint16_t *const dst_row0 = kind == 0
+                                                       ? o + (static_cast<size_t>(t0) * H + h) * VD
+                                                       : qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH) * KD;
+                        const size_t row_stride = kind == 0 ? static_cast<size_t>(H) * VD : KD;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
-                        if (r < L)
-                            *reinterpret_cast<uint4 *>(dst_row0 + r * row_stride + c16 * 8) =
-                                *reinterpret_cast<const uint4 *>(base + OFF_OB + (c16 >> 3) * 8192 + sw128(r, c16 & 7));
+                        for (int i = 0; i < 4; ++i) {
+                            const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
+                            if (r < L)
+                                *reinterpret_cast<uint4 *>(dst_row0 + r * row_stride + c16 * 8) =
+                                    *reinterpret_cast<const uint4 *>(base + OFF_OB + (c16 >> 3) * 8192 + sw128(r, c16 & 7));
+                        }
                     }
                 }
             }
@@ -320,11 +344,12 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                         mma_bf16_ta(tbase + TM_WX, tbase + aoff[ps] + kk * 8,
                                     sdesc(p1 + PK_W + boff[ps] + kk * 256, 128, 2048), idw, (ps | kk) != 0);
                 commit(mbar);
-                // O^T = X^T Qt^T (1-term)
-                const uint32_t id = idesc_bf16(128, 64);
+                if constexpr (MODE != STATE_SUMMARY) {   // O^T = X^T Qt^T (1-term)
+                    const uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ta(t_o, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id, kk != 0);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ta(t_o, tbase + TM_XH + kk * 8, sdesc(p1 + PK_Q + kk * 2 * 1024, 1024), id, kk != 0);
+                }
             }
             if (!(ok = mbar_wait(smem_u32(&s_pbar2[ci & 1]), (ci >> 1) & 1))) break;
             if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
@@ -342,11 +367,12 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
                         mma_bf16_ta(tbase + TM_X, tbase + aoff[ps] + kk * 8,
                                     sdesc(s2 + P2_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
                 commit(mbar);
-                // O^T += U^T QK^T (1-term)
+                if constexpr (MODE != STATE_SUMMARY) {   // O^T += U^T QK^T (1-term)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ta(t_o, tbase + TM_UH + kk * 8, sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64, 1);
-                commit(mbar_o);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ta(t_o, tbase + TM_UH + kk * 8, sdesc(s2 + P2_QK + kk * 2 * 1024, 1024), id64, 1);
+                    commit(mbar_o);
+                }
             }
             // the next chunk's W and Qt (issued when this chunk began)
             if (ci + 1 < nch && !(ok = mbar_wait(smem_u32(&s_pbar1[(ci + 1) & 1]), ((ci + 1) >> 1) & 1))) break;
@@ -378,16 +404,16 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
         const bool seg_last = flags & KDA_PIECE_SEG_LAST, seq_end = flags & KDA_PIECE_SEQ_END;
         float *dst0 = nullptr, *dst1 = nullptr;
         if (kind == 0) {
-            if (seg_last) dst0 = B + (static_cast<size_t>(seg) * H + h) * mat;
-            if (seq_end) dst1 = fin_state + (static_cast<size_t>(seq) * H + h) * mat;
-            if (seg_last && (pv.seg(seg)[1] & KDA_SEG_HAS_RESET)) {
+            if (MODE != STATE_OUTPUT && seg_last) dst0 = B + (static_cast<size_t>(seg) * H + h) * mat;
+            if (MODE != STATE_SUMMARY && seq_end) dst1 = fin_state + (static_cast<size_t>(seq) * H + h) * mat;
+            if (MODE != STATE_OUTPUT && seg_last && (pv.seg(seg)[1] & KDA_SEG_HAS_RESET)) {
                 float *za = A + (static_cast<size_t>(seg) * H + h) * KD * KD;
                 for (int e = tid; e < KD * KD / 4; e += NWORK)
                     reinterpret_cast<float4 *>(za)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         } else {
             if (seg_last) dst0 = A + (static_cast<size_t>(seg) * H + h) * KD * KD;
-            if (seq_end) dst1 = afin + (static_cast<size_t>(fin) * H + h) * KD * KD;
+            if (MODE == STATE_LOCAL && seq_end) dst1 = afin + (static_cast<size_t>(fin) * H + h) * KD * KD;
         }
         if (dst0 || dst1) {
 #pragma unroll
@@ -412,11 +438,11 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     if (warp == 0) tmem_dealloc(tbase, TM_COLS);
 }
 
-}  // namespace
-
-cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
-                               const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
-                               uint16_t *qhat, float *afin, cudaStream_t stream)
+// The state pass in one of its modes, as a programmatic dependent of the kernel before it.
+template <int MODE>
+cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0, const float *s_in,
+                         const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
+                         uint16_t *qhat, float *afin, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
@@ -426,18 +452,29 @@ cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev
     // a tensor shorter than one chunk has no full chunk, so its map stays unused
     CUtensorMap to{}, tq{};
     const long long q_rows = static_cast<long long>(H) * pv.T_cont();
-    if (pv.T() >= CH && !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, CH))
+    if (MODE != STATE_SUMMARY && pv.T() >= CH &&
+        !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, CH))
         return cudaErrorInvalidValue;
-    if (q_rows >= CH) {
+    if (MODE == STATE_LOCAL && q_rows >= CH) {
         if (q_rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         if (!encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, CH))
             return cudaErrorInvalidValue;
     }
-    cudaError_t err = cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(chunk_state_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    return launch_dependent(chunk_state_tc, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC, stream,
-                            plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, to, tq);
+    return launch_dependent(chunk_state_tc<MODE>, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC,
+                            stream, plan_dev, H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
+                               const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
+                               uint16_t *qhat, float *afin, cudaStream_t stream)
+{
+    return launch_state<STATE_LOCAL>(plan_host, plan_dev, H, h0, nullptr, pkg, o, A, B, final_state, qhat, afin,
+                                     stream);
 }
 
 // The local chunkwise forward: the chunk-parallel preparation, then the serial state pass.
@@ -450,6 +487,26 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
     cudaError_t err = launch_chunk_prep(plan_host, plan_dev, H, q, k, v, g, beta, scale, pkg, stream);
     if (err != cudaSuccess) return err;
     return launch_chunk_state(plan_host, plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, stream);
+}
+
+// The forward from preceding summaries: the preparation; the segment summaries alone (the last piece of
+// each segment); their composition into S_in; then every piece's chain again from its true incoming
+// state, reading the same packages, which gives the outputs and final states directly.
+cudaError_t launch_two_pass(const int32_t *plan_host, const int32_t *plan_dev, int H,
+                            const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *g, const float *beta, const float *h0, float scale,
+                            uint16_t *o, float *A, float *B, float *S_in, float *final_state,
+                            unsigned char *pkg, cudaStream_t stream)
+{
+    cudaError_t err = launch_chunk_prep(plan_host, plan_dev, H, q, k, v, g, beta, scale, pkg, stream);
+    if (err != cudaSuccess) return err;
+    err = launch_state<STATE_SUMMARY>(plan_host, plan_dev, H, h0, nullptr, pkg, o, A, B, final_state, nullptr,
+                                      nullptr, stream);
+    if (err != cudaSuccess) return err;
+    err = launch_compose(plan_host, plan_dev, H, A, B, h0, S_in, stream);
+    if (err != cudaSuccess) return err;
+    return launch_state<STATE_OUTPUT>(plan_host, plan_dev, H, h0, S_in, pkg, o, A, B, final_state, nullptr, nullptr,
+                                      stream);
 }
 
 // The status word of this file's kernel: read and cleared (the caller has synchronised the device).

@@ -134,5 +134,10 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
                             const uint16_t *qhat, const float *afin, uint16_t *o, float *final_state,
                             cudaStream_t stream);
+cudaError_t launch_two_pass(const int32_t *plan_host, const int32_t *plan_dev, int H,
+                            const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *g, const float *beta, const float *h0, float scale,
+                            uint16_t *o, float *A, float *B, float *S_in, float *final_state,
+                            unsigned char *pkg, cudaStream_t stream);
 
 }  // namespace kda

@@ -256,6 +256,29 @@ int kda_forward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t 
                           void *stream);
 
 /*
+ * kda_forward_two_pass -- the segmented forward from preceding summaries: the
+ * forward run takes each segment's incoming state as an input instead of being
+ * fixed up afterwards (PR #136 §Summary: the cuDNN KDA forward takes the
+ * preceding state update and transition).  Same arguments, results and
+ * workspace as kda_forward_segmented; the workspace's qhat and fin regions
+ * are not used.  Four kernels run on 'stream':
+ *   1. the chunk-parallel preparation of every (chunk, head) package;
+ *   2. the state pass of the last piece of each segment only, writing that
+ *      segment's A and B and nothing else;
+ *   3. the composition into S_in (as kda_compose_summaries);
+ *   4. the state pass of every piece again, from its true incoming state
+ *      (h0 of its sequence, or S_in of its segment for a piece that continues
+ *      a sequence), reading the same packages and writing o and final_state.
+ * The state pass runs twice and the fix-up and qhat traffic disappear.
+ * Returns as kda_forward_segmented.
+ */
+int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                         const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                         const float *g, const float *beta, const float *h0, float scale,
+                         kda_bf16 *o, float *final_state, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/*
  * kda_forward_segmented_noalloc -- kda_forward_segmented without a caller
  * workspace.  The pages have no counterpart to this entry point.
  *

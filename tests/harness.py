@@ -45,7 +45,8 @@ def plan_bounds(plan, S):
 
 
 def gpu_forward(inp, scale=1.0, path="fused", seg_bounds=None, dev=None):
-    """Run the CUDA path; returns numpy o (fp32 of the bf16 bits), final, A, B, S_in."""
+    """Run the CUDA path ("fused": kda_forward_segmented; "split": its three calls; "two_pass":
+    kda_forward_two_pass); returns numpy o (fp32 of the bf16 bits), final, A, B, S_in."""
     import torch
     from context_kda_gb300 import binding as kda
     dev = dev or to_device(inp)
@@ -57,9 +58,9 @@ def gpu_forward(inp, scale=1.0, path="fused", seg_bounds=None, dev=None):
     ws = torch.empty(off[6], dtype=torch.uint8, device="cuda")
     o = torch.empty((T, H, V), dtype=torch.bfloat16, device="cuda")
     fin = torch.empty((N, H, K, V), dtype=torch.float32, device="cuda")
-    if path == "fused":
-        kda.kda_forward_segmented(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
-                                  dev["h0"], scale, o, fin, ws)
+    if path in ("fused", "two_pass"):
+        run = kda.kda_forward_segmented if path == "fused" else kda.kda_forward_two_pass
+        run(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"], scale, o, fin, ws)
         view = lambda a, shape: ws[a:a + 4 * int(np.prod(shape))].view(torch.float32).view(*shape)
         A = view(off[3], (S, H, K, K))
         B = view(off[4], (S, H, K, V))

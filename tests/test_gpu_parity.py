@@ -122,6 +122,51 @@ def test_long_ragged_pieces_with_few_chains():
     assert np.array_equal(res["o"], again["o"]) and np.array_equal(res["final"], again["final"])
 
 
+# ---- the forward from preceding summaries (cuLA PR #136 §Summary: the cuDNN KDA forward takes the
+# preceding state update and transition as inputs): same results, reached without a fix-up
+
+@pytest.mark.parametrize("name", ["t1024_h4_s2", "t4096_h8_s4"])
+def test_two_pass_single_sequence_all_heads(name):
+    inp = make_workload(workloads()[name])
+    res = gpu_forward(inp, path="two_pass")
+    _check_outputs(res, inp)
+    _check_segments(res, inp, [(j, h) for j in range(inp.segments) for h in range(inp.heads)])
+
+
+@pytest.mark.parametrize("seqlens,S,h0_std,scale", [
+    ([63, 1, 65, 130], 3, 0.1, 1.0),
+    ([200, 201, 50, 9, 300], 5, 0.3, 0.5),
+    ([700], 11, 0.0, 1.0),
+    ([5, 5, 5, 5], 20, 0.1, 1.0),
+    ([1800, 2300, 63, 1400], 4, 0.1, 1.0),
+])
+def test_two_pass_edge_cases_all_heads(seqlens, S, h0_std, scale):
+    inp = make_inputs(seqlens, heads=2, segments=S, h0_std=h0_std, seed=16, g_lo=-0.2)
+    res = gpu_forward(inp, scale=scale, path="two_pass")
+    _check_outputs(res, inp, scale=scale)
+    _check_segments(res, inp, [(j, h) for j in range(S) for h in range(2)])
+
+
+def test_two_pass_packed_sampled_heads():
+    inp = make_workload(workloads()["packed65536_h32_s64"])
+    res = gpu_forward(inp, path="two_pass")
+    _check_outputs(res, inp, heads=[0, 31])
+    _check_segments(res, inp, [(j, h) for j in (0, 1, 17, 40, 63) for h in (0, 31)])
+
+
+def test_two_pass_summaries_equal_the_fix_up_paths():
+    """The summaries and incoming states come from the same arithmetic in both paths (bit-equal);
+    outputs and final states differ only by rounding (the fix-up adds S_in^T qhat afterwards)."""
+    inp = make_workload(workloads()["t4096_h8_s4"])
+    dev = to_device(inp)
+    a = gpu_forward(inp, path="fused", dev=dev)
+    b = gpu_forward(inp, path="two_pass", dev=dev)
+    for key in ("A", "B", "S_in"):
+        assert np.array_equal(a[key], b[key]), key
+    assert float(np.max(np.abs(a["o"] - b["o"]))) <= O_TOL
+    assert rel_err(b["final"], a["final"]) <= REL_TOL
+
+
 def test_custom_segment_bounds():
     inp = make_inputs([130, 70, 300], heads=2, segments=4, h0_std=0.1, seed=12)
     bounds = [0, 1, 129, 333, 500]
