@@ -332,6 +332,19 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     e2e_ms = max(e_start.elapsed_time(ev) for ev in ends) / args.steps
 
+    # the host link alone: the step's input uploads with nothing else running (median of 5), which
+    # bounds the end-to-end rate from above
+    link = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k_ in pinned:
+            d[k_].copy_(pinned[k_], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        link.append(e0.elapsed_time(e1))
+    h2d_ms = float(statistics.median(link))
+
     t_step = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t_step, op=dist.ReduceOp.MAX)
@@ -385,7 +398,8 @@ def run_ours(args, w, rank, world, local_rank):
            "hbm_peak_gbs": peaks["hbm_gbs"],
            "bf16_peak_tflops": peaks["bf16_tflops"]},
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
+                "d2h_bytes_per_step": d2h, "h2d_gbs_alone": h2d / (h2d_ms / 1e3) / 1e9,
+                "upload_bound_value": world * T / (h2d_ms / 1e3),
                 "pipeline": "2 lanes: step i+1 uploads its inputs while step i computes and reads back"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": dict(clk.summary(), window=f"{args.clock_soak_s:g} s soak of identical steps + timed region"),

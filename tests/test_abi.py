@@ -152,6 +152,15 @@ def test_entry_points_reject_bad_arguments_before_any_device_work(kda):
     a = list(args)
     a[13] = ws_need - 1
     assert lib.kda_forward_segmented(*a) == kda.KDA_ERR_WORKSPACE
+    for i in (3, 4, 5, 6, 7, 10, 11, 12):   # the two-pass entry takes the same arguments
+        a = list(args)
+        a[i] = None
+        assert lib.kda_forward_two_pass(*a) == kda.KDA_ERR_INVALID_ARG
+        a[i] = odd
+        assert lib.kda_forward_two_pass(*a) == kda.KDA_ERR_INVALID_ARG
+    a = list(args)
+    a[13] = ws_need - 1
+    assert lib.kda_forward_two_pass(*a) == kda.KDA_ERR_WORKSPACE
     a = list(args)
     a[1] = None
     assert lib.kda_forward_segmented(*a) == kda.KDA_ERR_INVALID_ARG
