@@ -40,7 +40,7 @@ METRIC = "segmented KDA fwd tokens/sec (H=16,K=V=128) on 1 GB300; % of roofline"
 UNIT = "tokens/s"
 K_DIM = V_DIM = 128
 CH = 64
-# algorithmic work per token-head (minimal counts): the state columns of the
+# algorithmic work per token-head (minimal counts of the chunkwise algebra): the state columns of the
 # chunk forward, and the transition columns a continuing token adds
 FLOPS_STATE = 6 * CH * K_DIM + 4 * CH * V_DIM + 6 * K_DIM * V_DIM          # 180,224
 FLOPS_TRANSITION = 6 * K_DIM * K_DIM + 2 * CH * K_DIM                      # 114,688
@@ -59,7 +59,7 @@ BYTES_SEQ_STATE = K_DIM * V_DIM * 4                                      # 65,53
 ISSUED_PREP_PER_CHUNK = 2 * 128 * (3 * 64 * 128 + 3 * 64 * 64 + 2 * 64 * 64)
 ISSUED_STATE_PER_CHUNK = 2 * 128 * (3 * 64 * 128 + 64 * 128 + 64 * 64 + 3 * 128 * 64)
 CHUNK_KERNEL_SRCS = [os.path.join(ROOT, "context_kda_gb300", "csrc", f) for f in ("chunk_prep.cu", "chunk_state.cu")]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "chunk_forward_t8192_h16_s4.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "chunk_forward_t8192_h16_s4.txt")
 
 
 def _peaks():
