@@ -15,6 +15,9 @@ Contents
     sequential composition, and the fix-up of continuing outputs.
   * ``plan.py`` -- an independent Python planner producing the packed-THD
     segment plan word for word.
+  * ``backward.py`` -- gradients of q, k, v, g, beta and h0 by the chain rule
+    through the same recurrence (fp64, any K and V), and their segment-parallel
+    reading through the following summaries.  No CUDA path computes them yet.
 
 Parity pins (tests/test_oracle_*.py) tie the oracle to closed forms,
 brute-force dense products and invariants; see each function's docstring.
