@@ -30,6 +30,9 @@
  *   kda_compose_summaries      scan of the summaries -> S_in per segment
  *   kda_apply_boundary         fix-up of continuing outputs and final states
  *   kda_forward_segmented      the three device steps above, in order
+ *   kda_forward_two_pass       the same results from the preceding summaries:
+ *                              summaries, composition, then the forward from
+ *                              each segment's true incoming state (no fix-up)
  *
  * Conventions shared by every entry point
  *   - Fixed sizes: K = V = 128 (key and value head dimensions), chunk C = 64.
