@@ -134,6 +134,8 @@ def test_two_pass_single_sequence_all_heads(name):
 
 
 @pytest.mark.parametrize("seqlens,S,h0_std,scale", [
+    ([1], 1, 0.0, 1.0),                        # one token
+    ([300, 1, 77], 1, 0.2, 1.0),               # one segment: no continuing piece at all
     ([63, 1, 65, 130], 3, 0.1, 1.0),
     ([200, 201, 50, 9, 300], 5, 0.3, 0.5),
     ([700], 11, 0.0, 1.0),
