@@ -177,6 +177,23 @@ def _config(w, n):
             "h0_std": w.h0_std, "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas{n}"}
 
 
+def max_over_ranks(values, world, device=None):
+    """Each rank's timings (ms) -> the slowest rank's, element by element; every rank gets them.
+    With one rank the values come back unchanged."""
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def aggregate_rate(world, tokens_per_rank, ms):
+    """Whole-job tokens/s: every rank processes its own copy of the workload (weak scaling), and
+    the job takes the slowest rank's time."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 def run_reference(args, w, rank):
     if rank != 0:
         return
@@ -345,10 +362,7 @@ def run_ours(args, w, rank, world, local_rank):
         link.append(e0.elapsed_time(e1))
     h2d_ms = float(statistics.median(link))
 
-    t_step = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_step, op=dist.ReduceOp.MAX)
-    step_ms, e2e_ms = (float(x) for x in t_step.cpu())
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], world, dev)
     if rank != 0:
         return
     peaks = _peaks()
@@ -376,7 +390,7 @@ def run_ours(args, w, rank, world, local_rank):
     if two_pass:   # the issued-flop count below is the fix-up path's
         issued = None
     line = {
-        "metric": METRIC, "value": world * T / (step_ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": aggregate_rate(world, T, step_ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 state", "data": "synthetic",
         "config": _config(w, world) | ({"path": "two_pass"} if two_pass else {}),
@@ -397,9 +411,9 @@ def run_ours(args, w, rank, world, local_rank):
            "issued_frac": None if issued is None else issued / sec / 1e12 / peaks["bf16_tflops"],
            "hbm_peak_gbs": peaks["hbm_gbs"],
            "bf16_peak_tflops": peaks["bf16_tflops"]},
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": aggregate_rate(world, T, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "h2d_gbs_alone": h2d / (h2d_ms / 1e3) / 1e9,
-                "upload_bound_value": world * T / (h2d_ms / 1e3),
+                "upload_bound_value": aggregate_rate(world, T, h2d_ms),
                 "pipeline": "2 lanes: step i+1 uploads its inputs while step i computes and reads back"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": dict(clk.summary(), window=f"{args.clock_soak_s:g} s soak of identical steps + timed region"),
