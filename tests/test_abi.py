@@ -122,6 +122,23 @@ def test_summary_workspace_matches_the_pages(kda):
     assert all(o % 256 == 0 for o in off)
 
 
+@pytest.mark.parametrize("name", list(workloads().keys()))
+def test_workspace_regions_hold_what_the_header_documents(kda, name):
+    """qhat bf16 [H][T_cont][K], fin fp32 [n_fin][H][K][K], packages [H][n_chunks] of
+    KDA_PACKAGE_BYTES, then A, B, S_in; each region starts on a 256-byte boundary."""
+    w = workloads()[name]
+    plan = kda.kda_plan_segments(_cu(w.seqlens), w.segments)
+    H, K = w.heads, 128
+    off = kda.kda_workspace_layout(plan, H)
+    up = lambda x: (x + 255) // 256 * 256
+    T_cont, n_fin, n_chunks, S = int(plan[9]), int(plan[10]), int(plan[11]), int(plan[5])
+    sizes = [H * T_cont * K * 2, n_fin * H * K * K * 4, n_chunks * H * 123392, S * H * K * K * 4,
+             S * H * K * K * 4, S * H * K * K * 4]
+    assert off[0] == 0
+    for i, n in enumerate(sizes):
+        assert off[i + 1] - off[i] == up(n), i
+
+
 def test_layout_rejects_bad_plan_and_heads(kda):
     plan = kda.kda_plan_segments([0, 256], 2)
     with pytest.raises(kda.KDAError):
