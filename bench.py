@@ -218,65 +218,125 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, w, rank, world, local_rank):
-    import torch
-    import torch.distributed as dist
-    from context_kda_gb300 import binding as kda
+def kernel_bytes(plan, H, h0_given):
+    """Algorithmic HBM bytes of each kernel of one step:
+    chunk stage  q, k, v, g, beta read and o written per token-head, qhat written per continuing
+                 token-head, A and B written per segment-head, the final state written (and h0 read)
+                 per sequence-head;
+    composition  A and B read and S_in written per segment-head;
+    fix-up       qhat read and o read and written per continuing token-head, S_in read per
+                 (segment, head) with a continuing piece, and per final-state transition the
+                 transition and the final state read and the final state written."""
+    T, N, S, T_cont, n_fin = int(plan[3]), int(plan[4]), int(plan[5]), int(plan[9]), int(plan[10])
+    n_cont, cont_off = int(plan[8]), int(plan[20])
+    segs_with_cont = len({int(plan[cont_off + 4 * i + 1]) for i in range(n_cont)})
+    chunk = (T * H * BYTES_TOKEN + T_cont * H * BYTES_CONT + S * H * BYTES_SEGMENT
+             + N * H * BYTES_SEQ_STATE * (2 if h0_given else 1))
+    compose = S * H * (BYTES_SEGMENT + BYTES_SEQ_STATE)
+    fixup = T_cont * H * 3 * V_DIM * 2 + segs_with_cont * H * BYTES_SEQ_STATE + n_fin * H * 3 * BYTES_SEQ_STATE
+    return {"chunk_forward": chunk, "compose": compose, "boundary": fixup}
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    inp = make_workload(w)
-    T, H, N, S = inp.tokens, inp.heads, inp.num_seqs, inp.segments
-    to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt)
-    host = {"q": to(inp.q, torch.bfloat16), "k": to(inp.k, torch.bfloat16), "v": to(inp.v, torch.bfloat16),
-            "g": to(inp.g, torch.float32), "beta": to(inp.beta, torch.float32)}
-    if inp.h0 is not None:
-        host["h0"] = to(inp.h0, torch.float32)
-    d = {k_: v_.to(dev) for k_, v_ in host.items()}
-    h0 = d.get("h0")
-    plan = kda.kda_plan_segments(inp.cu_seqlens, S)
-    plan_dev = kda.upload_plan(plan, dev)
-    off = kda.kda_workspace_layout(plan, H)
-    ws = torch.empty(off[6], dtype=torch.uint8, device=dev)
-    A = ws[off[3]:off[4]].view(torch.float32)
-    B = ws[off[4]:off[5]].view(torch.float32)
-    S_in = ws[off[5]:off[6]].view(torch.float32)
-    o = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
-    fin = torch.empty((N, H, K_DIM, V_DIM), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    n_cont, n_fin = int(plan[8]), int(plan[10])
-    launches_per_step = 3 + (1 if (n_cont + n_fin) > 0 else 0)   # prep, state, compose (+ fix-up)
-    two_pass = args.path == "two_pass"
-    if two_pass:
-        launches_per_step = 4   # prep, summary pass, compose, output pass
 
-    def step(evs=None):
+class Problem:
+    """One workload resident on the device: inputs, plan, workspace and outputs."""
+
+    def __init__(self, w, dev, inp=None):
+        import torch
+        from context_kda_gb300 import binding as kda
+        self.kda = kda
+        self.w = w
+        self.inp = inp if inp is not None else make_workload(w)
+        inp = self.inp
+        self.T, self.H, self.N, self.S = inp.tokens, inp.heads, inp.num_seqs, inp.segments
+        to = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt)
+        self.host = {"q": to(inp.q, torch.bfloat16), "k": to(inp.k, torch.bfloat16),
+                     "v": to(inp.v, torch.bfloat16), "g": to(inp.g, torch.float32),
+                     "beta": to(inp.beta, torch.float32)}
+        if inp.h0 is not None:
+            self.host["h0"] = to(inp.h0, torch.float32)
+        self.d = {k_: v_.to(dev) for k_, v_ in self.host.items()}
+        self.h0 = self.d.get("h0")
+        self.plan = kda.kda_plan_segments(inp.cu_seqlens, self.S)
+        self.plan_dev = kda.upload_plan(self.plan, dev)
+        off = kda.kda_workspace_layout(self.plan, self.H)
+        self.ws = torch.empty(off[6], dtype=torch.uint8, device=dev)
+        self.A = self.ws[off[3]:off[4]].view(torch.float32)
+        self.B = self.ws[off[4]:off[5]].view(torch.float32)
+        self.S_in = self.ws[off[5]:off[6]].view(torch.float32)
+        self.o = torch.empty((self.T, self.H, V_DIM), dtype=torch.bfloat16, device=dev)
+        self.fin = torch.empty((self.N, self.H, K_DIM, V_DIM), dtype=torch.float32, device=dev)
+        n_cont, n_fin = int(self.plan[8]), int(self.plan[10])
+        self.launches_per_step = 3 + (1 if (n_cont + n_fin) > 0 else 0)   # prep, state, compose (+ fix-up)
+
+    def step(self, stream, evs=None, two_pass=False):
+        kda, d, H = self.kda, self.d, self.H
         if two_pass:   # one call: the whole step is its first interval
             if evs:
                 evs[0].record(stream)
-            kda.kda_forward_two_pass(plan, plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], h0, 1.0, o, fin,
-                                     ws, stream)
+            kda.kda_forward_two_pass(self.plan, self.plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                     self.h0, 1.0, self.o, self.fin, self.ws, stream)
             if evs:
                 for e in evs[1:]:
                     e.record(stream)
             return
         if evs:
             evs[0].record(stream)
-        kda.kda_segment_forward(plan, plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], h0, 1.0, o, A, B,
-                                fin, ws, stream)
+        kda.kda_segment_forward(self.plan, self.plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], self.h0,
+                                1.0, self.o, self.A, self.B, self.fin, self.ws, stream)
         if evs:
             evs[1].record(stream)
-        kda.kda_compose_summaries(plan, plan_dev, H, A, B, h0, S_in, stream)
+        kda.kda_compose_summaries(self.plan, self.plan_dev, H, self.A, self.B, self.h0, self.S_in, stream)
         if evs:
             evs[2].record(stream)
-        kda.kda_apply_boundary(plan, plan_dev, H, S_in, ws, o, fin, stream)
+        kda.kda_apply_boundary(self.plan, self.plan_dev, H, self.S_in, self.ws, self.o, self.fin, stream)
         if evs:
             evs[3].record(stream)
 
+    def time_steps(self, stream, flush, steps, warmup, two_pass=False):
+        """Per-kernel CUDA-event times (ms) of 'steps' steps after 'warmup' untimed ones, the L2
+        flushed (a 256 MiB write) before every step outside the events: array [steps, 3]."""
+        import torch
+        for _ in range(warmup):
+            flush.fill_(1)
+            self.step(stream, two_pass=two_pass)
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(1)
+            self.step(stream, evsets[i], two_pass=two_pass)
+        torch.cuda.synchronize()
+        return np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evsets])
+
+    def free(self):
+        for name in ("d", "ws", "A", "B", "S_in", "o", "fin", "plan_dev", "h0"):
+            setattr(self, name, None)
+
+
+def pages_protocol(prob, stream, flush, warmup=20, iters=60, repeats=5):
+    """The timing protocol of cuLA PR #110 §Performance: 20 warm-up iterations, then 5 repeats of 60
+    timed iterations; the median of each repeat, then the median of the repeats (one rank, so the
+    rank-max is the value itself).  The L2 is flushed before every iteration, outside the events."""
+    per = prob.time_steps(stream, flush, iters * repeats, warmup)
+    step = per.sum(axis=1).reshape(repeats, iters)
+    return float(np.median(np.median(step, axis=1)))
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    prob = Problem(w, dev)
+    inp, plan = prob.inp, prob.plan
+    T, H = prob.T, prob.H
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    two_pass = args.path == "two_pass"
+    launches_per_step = 4 if two_pass else prob.launches_per_step   # two-pass: prep, summary pass, compose, output pass
+
     for _ in range(args.warmup):
         flush.fill_(1)
-        step()
+        prob.step(stream, two_pass=two_pass)
     torch.cuda.synchronize(dev)
     evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
@@ -289,12 +349,12 @@ def run_ours(args, w, rank, world, local_rank):
         while time.perf_counter() - soak0 < args.clock_soak_s:
             for _ in range(8):
                 flush.fill_(1)
-                step()
+                prob.step(stream, two_pass=two_pass)
             torch.cuda.synchronize(dev)
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(1)
-            step(evsets[i])
+            prob.step(stream, evsets[i], two_pass=two_pass)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if world > 1:
@@ -302,12 +362,15 @@ def run_ours(args, w, rank, world, local_rank):
     per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evsets])  # ms
     step_ms = float(np.mean(per.sum(axis=1)))
     kern_ms = per.mean(axis=0)
+    protocol_ms = None if (two_pass or args.no_extra) else pages_protocol(prob, stream, flush)
 
     # end to end through the public entry point: every step uploads its inputs from pinned host
     # memory and reads its outputs and final states back.  Two lanes (own stream, device buffers
     # and workspace each) alternate steps, so one step's upload overlaps the previous step's
     # compute and read-back; the copies of every step stay inside the timed region.
-    pinned = {k_: v_.pin_memory() for k_, v_ in host.items()}
+    kda = prob.kda
+    d, o, fin, ws = prob.d, prob.o, prob.fin, prob.ws
+    pinned = {k_: v_.pin_memory() for k_, v_ in prob.host.items()}
     h2d = sum(v_.numel() * v_.element_size() for v_ in pinned.values())
     d2h = o.numel() * o.element_size() + fin.numel() * fin.element_size()
     lanes = []
@@ -326,8 +389,8 @@ def run_ours(args, w, rank, world, local_rank):
             for k_ in pinned:
                 dd[k_].copy_(pinned[k_], non_blocking=True)
             run = kda.kda_forward_two_pass if two_pass else kda.kda_forward_segmented
-            run(plan, plan_dev, H, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd.get("h0"), 1.0, ln["o"],
-                ln["fin"], ln["ws"], ln["stream"])
+            run(plan, prob.plan_dev, H, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd.get("h0"), 1.0,
+                ln["o"], ln["fin"], ln["ws"], ln["stream"])
             ln["o_host"].copy_(ln["o"], non_blocking=True)
             ln["f_host"].copy_(ln["fin"], non_blocking=True)
 
@@ -350,17 +413,23 @@ def run_ours(args, w, rank, world, local_rank):
     e2e_ms = max(e_start.elapsed_time(ev) for ev in ends) / args.steps
 
     # the host link alone: the step's input uploads with nothing else running (median of 5), which
-    # bounds the end-to-end rate from above
-    link = []
-    for _ in range(5):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for k_ in pinned:
-            d[k_].copy_(pinned[k_], non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        link.append(e0.elapsed_time(e1))
-    h2d_ms = float(statistics.median(link))
+    # bounds the end-to-end rate from above; and one 1 GiB pinned upload, the link's own rate
+    def timed_copies(pairs, reps=5):
+        out = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            out.append(e0.elapsed_time(e1))
+        return float(statistics.median(out))
+    h2d_ms = timed_copies([(d[k_], pinned[k_]) for k_ in pinned])
+    big_host = torch.empty(2 ** 30, dtype=torch.uint8).pin_memory()
+    big_dev = torch.empty(2 ** 30, dtype=torch.uint8, device=dev)
+    big_ms = timed_copies([(big_dev, big_host)])
+    del big_host, big_dev, lanes
 
     step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], world, dev)
     if rank != 0:
@@ -368,9 +437,8 @@ def run_ours(args, w, rank, world, local_rank):
     peaks = _peaks()
     T_cont = int(plan[9])
     flops = T * H * FLOPS_STATE + T_cont * H * FLOPS_TRANSITION
-    n_seq, n_seg = int(plan[4]), int(plan[5])
-    algo_bytes = (T * H * BYTES_TOKEN + T_cont * H * BYTES_CONT + n_seg * H * BYTES_SEGMENT
-                  + n_seq * H * BYTES_SEQ_STATE * (2 if w.h0_std > 0 else 1))
+    kb = kernel_bytes(plan, H, w.h0_std > 0)
+    algo_bytes = kb["chunk_forward"]
     # the binding roof is the larger of bytes / HBM bandwidth and flops / tensor peak
     t_hbm = algo_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
@@ -398,6 +466,9 @@ def run_ours(args, w, rank, world, local_rank):
                        {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]}),
         "kernel_shares": ({"two_pass_forward": 1.0} if two_pass else
                           {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]}),
+        "kernel_hbm_frac": (None if two_pass else
+                            {k_: kb[k_] / (kern_ms[i] / 1e3) / 1e9 / peaks["hbm_gbs"]
+                             for i, k_ in enumerate(("chunk_forward", "compose", "boundary"))}),
         "roofline": ({"bound": "hbm", "kernel": kernel, "achieved": achieved_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
                       "peak_source": f"{peaks['source']} HBM copy"}
@@ -411,17 +482,50 @@ def run_ours(args, w, rank, world, local_rank):
            "issued_frac": None if issued is None else issued / sec / 1e12 / peaks["bf16_tflops"],
            "hbm_peak_gbs": peaks["hbm_gbs"],
            "bf16_peak_tflops": peaks["bf16_tflops"]},
+        "pages_protocol_ms_per_step": protocol_ms,
         "e2e": {"value": aggregate_rate(world, T, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "h2d_gbs_alone": h2d / (h2d_ms / 1e3) / 1e9,
+                "h2d_gbs_one_1gib_copy": 2 ** 30 / (big_ms / 1e3) / 1e9,
                 "upload_bound_value": aggregate_rate(world, T, h2d_ms),
                 "pipeline": "2 lanes: step i+1 uploads its inputs while step i computes and reads back"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": dict(clk.summary(), window=f"{args.clock_soak_s:g} s soak of identical steps + timed region"),
         "wall_s_timed_region": wall,
     }
+    if world == 1 and not two_pass and not args.no_extra:
+        line["workloads"] = extra_workloads(args, dev, stream, flush, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
     print(json.dumps(line), flush=True)
+
+
+EXTRA_WORKLOADS = ("packed65536_h32_s64", "t131072_h32_s64")
+
+
+def extra_workloads(args, dev, stream, flush, peaks):
+    """The packed and long-context workloads, timed after the headline's timed region in the same
+    run: per-kernel CUDA-event times (mean of the timed steps), tokens/s and each kernel's fraction
+    of the measured HBM copy bandwidth on its algorithmic bytes."""
+    import torch
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        w = workloads()[name]
+        prob = Problem(w, dev)
+        per = prob.time_steps(stream, flush, args.extra_steps, 3)
+        kern = per.mean(axis=0)
+        ms = float(per.sum(axis=1).mean())
+        kb = kernel_bytes(prob.plan, prob.H, w.h0_std > 0)
+        names = ("chunk_forward", "compose", "boundary")
+        out[name] = {
+            "tokens_per_s": prob.T / (ms / 1e3), "ms_per_step": ms, "steps": args.extra_steps, "warmup": 3,
+            "kernels_ms": {n: float(kern[i]) for i, n in enumerate(names)},
+            "kernel_hbm_frac": {n: kb[n] / (kern[i] / 1e3) / 1e9 / peaks["hbm_gbs"] for i, n in enumerate(names)},
+            "algorithmic_bytes": kb, "config": _config(w, 1),
+        }
+        prob.free()
+        del prob
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -432,6 +536,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(workloads().keys()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the pages' timing protocol and the packed / long-context workloads")
+    ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--clock-soak-s", type=float, default=1.0)
     ap.add_argument("--path", default="fix_up", choices=["fix_up", "two_pass"],
                     help="fix_up: the three calls (local forward, composition, fix-up); two_pass: "

@@ -11,9 +11,10 @@ from __future__ import annotations
 
 import importlib
 
-_BINDING_NAMES = ("kda_status_string", "kda_plan_segments", "kda_workspace_layout", "kda_workspace_bytes",
-                  "kda_segment_forward", "kda_compose_summaries", "kda_apply_boundary", "kda_forward_segmented",
-                  "upload_plan", "KDAError", "LIB_PATH")
+_BINDING_NAMES = ("kda_status_string", "kda_plan_segments", "kda_plan_check", "kda_workspace_layout",
+                  "kda_workspace_bytes", "kda_segment_forward", "kda_compose_summaries", "kda_apply_boundary",
+                  "kda_forward_segmented", "kda_forward_two_pass", "kda_forward_segmented_noalloc",
+                  "kda_device_status", "kda_selftest_wait_expiry", "upload_plan", "KDAError", "LIB_PATH")
 
 
 def __getattr__(name):

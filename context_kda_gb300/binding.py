@@ -17,6 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+KDA_ERR_RANGE = -6
 HEAD_DIM_K = HEAD_DIM_V = 128
 CHUNK = 64
 
@@ -40,6 +41,7 @@ def _load():
     lib.kda_selftest_wait_expiry.argtypes = [P]
     lib.kda_selftest_wait_expiry.restype = ctypes.c_int
     lib.kda_plan_segments.argtypes = [P, I32, I32, P, I32, P, ctypes.POINTER(SZ)]
+    lib.kda_plan_check.argtypes = [P]
     lib.kda_workspace_layout.argtypes = [P, I32, ctypes.POINTER(SZ)]
     lib.kda_workspace_bytes.argtypes = [P, I32]
     lib.kda_workspace_bytes.restype = SZ
@@ -49,7 +51,7 @@ def _load():
     lib.kda_forward_segmented.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.kda_forward_segmented_noalloc.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P]
     lib.kda_forward_two_pass.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
-    for name in ("kda_plan_segments", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
+    for name in ("kda_plan_segments", "kda_plan_check", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
                  "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc",
                  "kda_forward_two_pass"):
         getattr(lib, name).restype = ctypes.c_int
@@ -69,7 +71,9 @@ def _check(fn: str, rc: int):
 
 def kda_device_status() -> int:
     """Synchronises the current device and returns (and clears) the kernels' device-side status:
-    KDA_OK, or KDA_ERR_TIMEOUT once a bounded wait inside a kernel expired."""
+    KDA_OK, or the first error a kernel recorded: KDA_ERR_TIMEOUT (a bounded wait expired),
+    KDA_ERR_RANGE (a chunk's summed decay out of range) or KDA_ERR_INVALID_ARG (a device plan
+    that is not the host plan's copy)."""
     return int(_lib.kda_device_status())
 
 
@@ -117,6 +121,11 @@ def kda_plan_segments(cu_seqlens, num_segments: int, seg_bounds=None, chunk: int
     out = np.zeros(n.value, dtype=np.int32)
     _check("kda_plan_segments", _lib.kda_plan_segments(*args, out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n)))
     return out
+
+
+def kda_plan_check(plan) -> int:
+    """Whole-plan validation (see include/kda.h): KDA_OK or KDA_ERR_INVALID_ARG."""
+    return int(_lib.kda_plan_check(_hp(_words(plan))))
 
 
 def kda_workspace_layout(plan, H: int):

@@ -22,18 +22,38 @@ int cuda_status(cudaError_t e)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Structural checks of a host plan (cheap, O(header)).
+// A host plan is accepted when kda_plan_check accepts it.  The check re-plans, so the plans
+// already accepted are remembered by (length, checksum, T, N, S); a plan whose words hash to a
+// remembered entry is accepted after the O(length) checksum pass alone.
+struct PlanKey {
+    int32_t total, checksum, T, N, S;
+    bool operator==(const PlanKey &o) const
+    {
+        return total == o.total && checksum == o.checksum && T == o.T && N == o.N && S == o.S;
+    }
+};
+std::mutex g_plan_mutex;
+PlanKey g_plan_seen[16];
+int g_plan_seen_n = 0, g_plan_seen_next = 0;
+
 bool plan_ok(const int32_t *plan)
 {
     if (!plan) return false;
     if (plan[KDA_PH_MAGIC] != KDA_PLAN_MAGIC || plan[KDA_PH_VERSION] != KDA_PLAN_VERSION) return false;
-    if (plan[KDA_PH_C] != KDA_CHUNK || plan[KDA_PH_T] < 1 || plan[KDA_PH_N] < 1 || plan[KDA_PH_S] < 1)
-        return false;
-    if (plan[KDA_PH_NPIECES] < plan[KDA_PH_S] || plan[KDA_PH_NCONT] < 0 || plan[KDA_PH_NFIN] < 0) return false;
-    if (plan[KDA_PH_TCONT] < 0 || plan[KDA_PH_TCONT] > plan[KDA_PH_T]) return false;
-    if (plan[KDA_PH_NITEMS] != plan[KDA_PH_NPIECES] + plan[KDA_PH_NCONT]) return false;
-    for (int i = KDA_PH_OFF_BOUNDS; i <= KDA_PH_OFF_FIN; ++i)
-        if (plan[i] < KDA_PLAN_HEADER_WORDS || plan[i] > plan[KDA_PH_TOTAL]) return false;
+    if (plan[KDA_PH_TOTAL] < KDA_PLAN_HEADER_WORDS) return false;
+    const uint32_t sum = kda::plan_checksum_words(plan, static_cast<size_t>(plan[KDA_PH_TOTAL]));
+    if (sum != static_cast<uint32_t>(plan[KDA_PH_CHECKSUM])) return false;
+    const PlanKey key{plan[KDA_PH_TOTAL], plan[KDA_PH_CHECKSUM], plan[KDA_PH_T], plan[KDA_PH_N], plan[KDA_PH_S]};
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mutex);
+        for (int i = 0; i < g_plan_seen_n; ++i)
+            if (g_plan_seen[i] == key) return true;
+    }
+    if (kda_plan_check(plan) != KDA_OK) return false;
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    g_plan_seen[g_plan_seen_next] = key;
+    g_plan_seen_next = (g_plan_seen_next + 1) % 16;
+    if (g_plan_seen_n < 16) ++g_plan_seen_n;
     return true;
 }
 
@@ -93,6 +113,7 @@ extern "C" const char *kda_status_string(int status)
     case KDA_ERR_WORKSPACE: return "buffer too small";
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "device wait timed out";
+    case KDA_ERR_RANGE: return "decay out of the chunkwise range";
     default: return "unknown status";
     }
 }

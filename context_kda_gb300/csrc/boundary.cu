@@ -104,7 +104,7 @@ __device__ __forceinline__ void advance(Cursor &c, const Rec &r, int n_cont)
 }
 
 __global__ void __launch_bounds__(256, 1)
-boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long long n_units,
+boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, int units_per_head, long long n_units,
             const float *__restrict__ S_in, const uint16_t *__restrict__ qhat, const float *__restrict__ afin,
             uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_q, int has_tq)
@@ -114,6 +114,10 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     __shared__ __align__(8) uint64_t s_abar[3];   // qhat tile landed, per ring slot
     __shared__ __align__(8) uint64_t s_obar[2];   // output tile landed, per buffer
     __shared__ uint32_t s_tmem;
+    if (!plan_matches(plan, sig)) {   // not the plan the launch was sized from: touch nothing
+        if (threadIdx.x == 0) record_status(&g_boundary_status, KDA_ERR_INVALID_ARG);
+        return;
+    }
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;
@@ -413,7 +417,7 @@ boundary_tc(const int32_t *__restrict__ plan, int H, int units_per_head, long lo
     if (!__syncthreads_and(ok)) {
         // a wait gave up: record it, and let any copy or product still in flight land (bounded waits)
         if (tid == 0) {
-            atomicExch(&g_boundary_status, KDA_ERR_TIMEOUT);
+            record_status(&g_boundary_status, KDA_ERR_TIMEOUT);
             for (int i = 0; i < 3; ++i)
                 if (a_pend[i]) mbar_wait(smem_u32(&s_abar[i]), (aph >> i) & 1u);
             for (int i = 0; i < 2; ++i) {
@@ -455,8 +459,8 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
     cudaError_t err = cudaFuncSetAttribute(boundary_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    return launch_dependent(boundary_tc, dim3(static_cast<unsigned>(grid)), dim3(256), SMEM_ALLOC, stream, plan_dev, H,
-                            static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
+    return launch_dependent(boundary_tc, dim3(static_cast<unsigned>(grid)), dim3(256), SMEM_ALLOC, stream, plan_dev,
+                            plan_sig(plan_host), H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
 }
 
 // Self-test of the expiry path: one thread waits, bounded, on an mbarrier that nothing arrives on,
@@ -466,7 +470,7 @@ __global__ void wait_expiry_probe_tc()
     __shared__ __align__(8) uint64_t s_bar;
     if (threadIdx.x == 0) mbar_init(smem_u32(&s_bar), 1);
     __syncthreads();
-    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&s_bar), 0)) atomicExch(&g_boundary_status, KDA_ERR_TIMEOUT);
+    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&s_bar), 0)) record_status(&g_boundary_status, KDA_ERR_TIMEOUT);
 }
 
 cudaError_t launch_wait_expiry_probe(cudaStream_t stream)

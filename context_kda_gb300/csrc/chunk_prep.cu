@@ -107,7 +107,7 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 w, float *x)
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const float *__restrict__ beta,
+chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_units, const float *__restrict__ beta,
               float scale, unsigned char *__restrict__ pkg, const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_g)
@@ -118,6 +118,10 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
     __shared__ __align__(8) uint64_t s_gbar;     // g rows landed
     __shared__ __align__(8) uint64_t s_hbar[3];
     __shared__ uint32_t s_tmem;
+    if (!plan_matches(plan, sig)) {   // not the plan the launch was sized from: touch nothing
+        if (threadIdx.x == 0) record_status(&g_prep_status, KDA_ERR_INVALID_ARG);
+        return;
+    }
     unsigned char *const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(base);
     float *const s_beta = reinterpret_cast<float *>(base + OFF_BETA);
@@ -289,7 +293,11 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                     bar_sync1(NWORK);
                     const float off = hr ? s_gsum[kc] : 0.f;
                     if (hr == 0) {
-                        const float gcv = ex2_ftz(s_gsum[kc] + s_gsum[128 + kc]);   // exp(Gamma_C)
+                        const float gsum = s_gsum[kc] + s_gsum[128 + kc];   // Gamma_C log2 e
+                        // below 2^-112 the decayed operands and their bf16 low parts leave the normal
+                        // fp32 range (NaN or inf in g lands here too)
+                        if (!(gsum >= -112.f)) record_status(&g_prep_status, KDA_ERR_RANGE);
+                        const float gcv = ex2_ftz(gsum);   // exp(Gamma_C)
                         s_gc[kc] = gcv;
                         reinterpret_cast<float *>(pk + PK_GC)[kc] = gcv;
                     }
@@ -545,7 +553,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
                 commit(mbar);
             }
         }
-        if (!ok) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+        if (!ok) record_status(&g_prep_status, KDA_ERR_TIMEOUT);
     } else if (producer_warp) {
         // Producer warp: the next unit once this unit's staged rows and metadata are read (a TMA unit
         // busy with earlier boxes stalls the thread that issues more, which must not be the MMA
@@ -564,13 +572,13 @@ chunk_prep_tc(const int32_t *__restrict__ plan, int H, long long n_units, const 
             advance(ipos);
             last = n + 1;
         }
-        if (!ok && lane == 0) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+        if (!ok && lane == 0) record_status(&g_prep_status, KDA_ERR_TIMEOUT);
         if (lane == 0 && u_begin < u_end) {   // bounded: every staged copy lands before the CTA exits
             mbar_wait(ldbar, last & 1);
             mbar_wait(gbar, last & 1);
         }
     }
-    if (worker && aborted && tid == 0) atomicExch(&g_prep_status, KDA_ERR_TIMEOUT);
+    if (worker && aborted && tid == 0) record_status(&g_prep_status, KDA_ERR_TIMEOUT);
     fence_before();
     __syncthreads();
     fence_after();
@@ -597,7 +605,8 @@ cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev,
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     const long long grid = n_units < sm_count() ? n_units : sm_count();
-    chunk_prep_tc<<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(plan_dev, H, n_units, beta, scale,
+    chunk_prep_tc<<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(plan_dev, plan_sig(plan_host), H, n_units,
+                                                                                 beta, scale,
                                                                                  pkg, tq, tk, tv, tg);
     return cudaGetLastError();
 }

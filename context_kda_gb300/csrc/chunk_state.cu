@@ -85,7 +85,7 @@ enum StateMode {
 
 template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
-chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict__ h0,
+chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float *__restrict__ h0,
                const float *__restrict__ s_in, const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o,
                float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
                uint16_t *__restrict__ qhat, float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
@@ -99,6 +99,10 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
     __shared__ __align__(8) uint64_t s_hbar[2];   // worker -> issuer handoffs
     __shared__ __align__(8) uint64_t s_free[2];   // issuer -> producer: package buffer free
     __shared__ uint32_t s_tmem;
+    if (!plan_matches(plan, sig)) {   // not the plan the launch was sized from: touch nothing
+        if (threadIdx.x == 0) record_status(&g_state_status, KDA_ERR_INVALID_ARG);
+        return;
+    }
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;   // 128-byte swizzle atoms
     unsigned char *const base = smem_raw + (sbase - smem_u32(smem_raw));
 
@@ -377,7 +381,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
             // the next chunk's W and Qt (issued when this chunk began)
             if (ci + 1 < nch && !(ok = mbar_wait(smem_u32(&s_pbar1[(ci + 1) & 1]), ((ci + 1) >> 1) & 1))) break;
         }
-        if (!ok) atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
+        if (!ok) record_status(&g_state_status, KDA_ERR_TIMEOUT);
     } else if (producer) {
         // Producer: chunk j's package parts once the issuer has freed their buffers (the free signal
         // of buffer j & 1 cannot run a phase ahead: the next one needs chunk j's products).
@@ -390,7 +394,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
             ++n_p1[j & 1];
             ++n_p2[j & 1];
         }
-        if (!ok) atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
+        if (!ok) record_status(&g_state_status, KDA_ERR_TIMEOUT);
         // every staged copy lands before the CTA exits (bounded waits)
         for (int b = 0; b < 2; ++b) {
             if (n_p1[b]) mbar_wait(smem_u32(&s_pbar1[b]), (n_p1[b] - 1) & 1);
@@ -429,7 +433,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, int H, const float *__restrict_
             }
         }
     } else if (worker && tid == 0) {
-        atomicExch(&g_state_status, KDA_ERR_TIMEOUT);
+        record_status(&g_state_status, KDA_ERR_TIMEOUT);
     }
     if (tid == 0) bulk_wait_all();   // the last O tiles are written before shared memory goes away
     fence_before();
@@ -464,7 +468,7 @@ cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int 
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(chunk_state_tc<MODE>, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC,
-                            stream, plan_dev, H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq);
+                            stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq);
 }
 
 }  // namespace

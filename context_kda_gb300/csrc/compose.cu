@@ -64,13 +64,17 @@ constexpr int NT = 320;                    // 8 worker warps + MMA warp + I/O wa
 constexpr int MMA_TID = 256, IO_TID = 288;
 
 __global__ void __launch_bounds__(NT, 1)
-compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_constant__ CUtensorMap tm_A,
+compose_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, int has_h0, const __grid_constant__ CUtensorMap tm_A,
            const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_h0,
            const __grid_constant__ CUtensorMap tm_S)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar, s_abar, s_bbar;
     __shared__ uint32_t s_tmem;
+    if (!plan_matches(plan, sig)) {   // not the plan the launch was sized from: touch nothing
+        if (threadIdx.x == 0) record_status(&g_compose_status, KDA_ERR_INVALID_ARG);
+        return;
+    }
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -256,7 +260,7 @@ compose_tc(const int32_t *__restrict__ plan, int H, int has_h0, const __grid_con
     if (!__syncthreads_and(ok)) {
         // a wait gave up: record it, and let copies and products still in flight land before the CTA exits
         if (issuer) {
-            atomicExch(&g_compose_status, KDA_ERR_TIMEOUT);
+            record_status(&g_compose_status, KDA_ERR_TIMEOUT);
             if (a_pending) mbar_wait(abar, a_phase & 1);
             mbar_wait(mbar, mma_phase & 1);
         }
@@ -290,7 +294,8 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
     cudaError_t err =
         cudaFuncSetAttribute(compose_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
-    return launch_dependent(compose_tc, dim3(H * (VD / NS)), dim3(NT), SMEM_ALLOC, stream, plan_dev, H, h0 ? 1 : 0, tA,
+    return launch_dependent(compose_tc, dim3(H * (VD / NS)), dim3(NT), SMEM_ALLOC, stream, plan_dev, plan_sig(plan_host), H,
+                            h0 ? 1 : 0, tA,
                             tB, tH, tS);
 }
 

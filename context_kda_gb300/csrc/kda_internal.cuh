@@ -38,6 +38,20 @@ struct PlanView {
     __host__ __device__ const int32_t *chunk(int i) const { return w + w[KDA_PH_OFF_CHUNKS] + 4 * i; }
 };
 
+// Identity of the host plan a launch was sized from: its length and checksum words.  Every kernel
+// compares them with its device plan before it reads anything else from it.
+struct PlanSig {
+    int32_t total, checksum;
+};
+inline PlanSig plan_sig(const int32_t *plan_host) { return PlanSig{plan_host[KDA_PH_TOTAL], plan_host[KDA_PH_CHECKSUM]}; }
+__device__ __forceinline__ bool plan_matches(const int32_t *plan_dev, PlanSig s)
+{
+    return plan_dev[KDA_PH_TOTAL] == s.total && plan_dev[KDA_PH_CHECKSUM] == s.checksum;
+}
+
+// Records an error code in a kernel's device status word unless an earlier one is there.
+__device__ __forceinline__ void record_status(int *word, int code) { atomicCAS(word, 0, code); }
+
 // Chunk package: the operands one (chunk, head) hands from the preparation kernel to the state
 // pass, each tile in the shared-memory layout its MMA reads (byte offsets; bf16 tiles in the
 // no-swizzle core-matrix layout, hi then lo where split).
@@ -69,6 +83,9 @@ struct Workspace {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+// Checksum of a plan's words by the rule of kda.h (the checksum word taken as 0).
+uint32_t plan_checksum_words(const int32_t *plan, size_t total);
 
 // Records a cudaError_t for kda_last_cuda_error() on the calling thread.
 void record_cuda_error(int err);

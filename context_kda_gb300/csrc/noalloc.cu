@@ -13,8 +13,10 @@
 // (32 MiB).  Every GPU that loads the library holds it until the process
 // exits.  Host code cannot use the array's name as a device address, so the
 // first call on each device looks the address up with cudaGetSymbolAddress
-// (with that device current) and caches it; later calls on that device reuse
-// the cached address.
+// (with that device current) and caches it.  The cache is keyed on the
+// context's unique id as well as the device: after cudaDeviceReset, or when the
+// primary context is destroyed and created again, the module is loaded anew and
+// the next call looks the address up again instead of reusing a stale one.
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -28,20 +30,58 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // id of the context the address belongs to
 
-// Device address of g_noalloc_scratch on the current device (looked up once per device).
+// Unique id of the calling thread's current context (driver entry points, looked up once).
+cudaError_t current_context_id(unsigned long long *id)
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    if (!get_current || !get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    if (!ctx) {   // nothing current yet on this thread: the runtime would use the primary context
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaSetDevice(dev);   // initialises and binds the primary context
+        if (e != cudaSuccess) return e;
+        if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+    }
+    if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
+
+// Device address of g_noalloc_scratch in the current context (looked up once per device and context).
 cudaError_t scratch_address(void **out)
 {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned long long ctx = 0;
+    e = current_context_id(&ctx);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;

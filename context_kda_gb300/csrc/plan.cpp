@@ -21,7 +21,23 @@ struct Piece {
     int32_t start, len, seq, seg, flags, cont, row, fin;
 };
 
+// FNV-1a over the plan's 32-bit words, the checksum word taken as 0 (the rule stated in kda.h).
+uint32_t checksum_words(const int32_t *plan, size_t total)
+{
+    uint32_t h = 2166136261u;
+    for (size_t i = 0; i < total; ++i) {
+        const uint32_t w = i == KDA_PH_CHECKSUM ? 0u : static_cast<uint32_t>(plan[i]);
+        h = (h ^ w) * 16777619u;
+    }
+    return h;
+}
+
 }  // namespace
+
+// Checksum of a plan of 'total' words, for the other translation units of the library.
+namespace kda {
+uint32_t plan_checksum_words(const int32_t *plan, size_t total) { return checksum_words(plan, total); }
+}  // namespace kda
 
 extern "C" int kda_plan_segments(const int32_t *cu, int32_t num_seqs, int32_t num_segments,
                                  const int32_t *seg_bounds, int32_t chunk, int32_t *plan,
@@ -162,5 +178,47 @@ extern "C" int kda_plan_segments(const int32_t *cu, int32_t num_seqs, int32_t nu
     if (!chunks.empty()) std::memcpy(plan + offs[5], chunks.data(), sizeof(int32_t) * sizes[5]);
     if (!cont.empty()) std::memcpy(plan + offs[6], cont.data(), sizeof(int32_t) * sizes[6]);
     if (!fin.empty()) std::memcpy(plan + offs[7], fin.data(), sizeof(int32_t) * sizes[7]);
+    plan[KDA_PH_CHECKSUM] = static_cast<int32_t>(checksum_words(plan, total));
     return KDA_OK;
+}
+
+// Whole-plan validation: the header must be self-consistent (sizes, section offsets in order and
+// of the sizes the counts imply), and every word must be what the planner gives for the plan's own
+// segment bounds and cu_seqlens.  Re-planning is the plainest complete check: the kernels index
+// pieces, chunks, items and records from these words, so any other content is rejected.
+extern "C" int kda_plan_check(const int32_t *plan)
+{
+    if (!plan) return KDA_ERR_INVALID_ARG;
+    if (plan[KDA_PH_MAGIC] != KDA_PLAN_MAGIC || plan[KDA_PH_VERSION] != KDA_PLAN_VERSION ||
+        plan[KDA_PH_C] != KDA_CHUNK)
+        return KDA_ERR_INVALID_ARG;
+    const int64_t total = plan[KDA_PH_TOTAL], T = plan[KDA_PH_T], N = plan[KDA_PH_N], S = plan[KDA_PH_S];
+    if (total < KDA_PLAN_HEADER_WORDS || T < 1 || N < 1 || S < 1 || S > T || N > T) return KDA_ERR_INVALID_ARG;
+    const int64_t counts[8] = {S + 1, N + 1, 4 * S, 8 * static_cast<int64_t>(plan[KDA_PH_NPIECES]),
+                               2 * static_cast<int64_t>(plan[KDA_PH_NITEMS]),
+                               4 * static_cast<int64_t>(plan[KDA_PH_NCHUNKS]),
+                               4 * static_cast<int64_t>(plan[KDA_PH_NCONT]),
+                               4 * static_cast<int64_t>(plan[KDA_PH_NFIN])};
+    int64_t pos = KDA_PLAN_HEADER_WORDS;
+    for (int i = 0; i < 8; ++i) {
+        if (counts[i] < 0 || plan[KDA_PH_OFF_BOUNDS + i] != pos) return KDA_ERR_INVALID_ARG;
+        pos += counts[i];
+    }
+    if (pos != total) return KDA_ERR_INVALID_ARG;
+    if (static_cast<uint32_t>(plan[KDA_PH_CHECKSUM]) != checksum_words(plan, static_cast<size_t>(total)))
+        return KDA_ERR_INVALID_ARG;
+    // the bounds and sequence sections as the planner's inputs (it checks them itself)
+    const int32_t *bounds = plan + plan[KDA_PH_OFF_BOUNDS];
+    const int32_t *cu = plan + plan[KDA_PH_OFF_CU];
+    if (cu[N] != T) return KDA_ERR_INVALID_ARG;
+    size_t len = 0;
+    if (kda_plan_segments(cu, static_cast<int32_t>(N), static_cast<int32_t>(S), bounds, KDA_CHUNK, nullptr, &len) !=
+            KDA_OK ||
+        len != static_cast<size_t>(total))
+        return KDA_ERR_INVALID_ARG;
+    std::vector<int32_t> again(len);
+    if (kda_plan_segments(cu, static_cast<int32_t>(N), static_cast<int32_t>(S), bounds, KDA_CHUNK, again.data(),
+                          &len) != KDA_OK)
+        return KDA_ERR_INVALID_ARG;
+    return std::memcmp(again.data(), plan, sizeof(int32_t) * len) == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
 }

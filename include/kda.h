@@ -45,8 +45,12 @@
  *           tensors, PR #136 §Latest cuDNN compatibility)
  *     bf16 is passed as its 16-bit pattern (kda_bf16).
  *   - The chunkwise form takes exp(+-Gamma), Gamma being the decay summed
- *     within a 64-token chunk; each channel's per-chunk sum must stay above
- *     about -80 (fp32 range), e.g. g >= -1.25 per token.
+ *     within a 64-token chunk.  g is a log-decay (g <= 0); each channel's
+ *     per-chunk sum must stay above -77 (2^-112 in fp32: e^{+-Gamma} and the
+ *     bf16 low parts of the split operands stay normal numbers), e.g.
+ *     g >= -1.2 per token.  The preparation checks every (chunk, head, channel)
+ *     and records KDA_ERR_RANGE for kda_device_status() when a sum falls
+ *     below; the outputs of that call are then not valid.
  *   - Device pointers must be 16-byte aligned.  The library never allocates
  *     or frees memory, never synchronises, and enqueues all device work on
  *     the caller's CUDA stream ('stream' is a cudaStream_t; NULL = legacy
@@ -60,7 +64,13 @@
  *     underlying cudaError_t value.
  *   - Each call takes the host plan (to size its grids without reading device
  *     memory) and a device copy of the same words (plan_dev), which the caller
- *     uploads once.
+ *     uploads once.  Every call validates the whole host plan (kda_plan_check:
+ *     each word must be what kda_plan_segments gives for its bounds; a plan
+ *     seen before is recognised by its checksum) and rejects any other with
+ *     KDA_ERR_INVALID_ARG.  Each kernel compares the device copy's length and
+ *     checksum words with the host plan's before it reads anything else; on a
+ *     mismatch it does nothing and records KDA_ERR_INVALID_ARG for
+ *     kda_device_status().
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -80,22 +90,28 @@ enum {
     KDA_ERR_UNSUPPORTED = -2,   /* valid request outside what is built (e.g. chunk != 64) */
     KDA_ERR_WORKSPACE = -3,     /* caller buffer too small */
     KDA_ERR_CUDA = -4,          /* a CUDA launch or API call failed */
-    KDA_ERR_TIMEOUT = -5        /* a bounded device-side wait expired */
+    KDA_ERR_TIMEOUT = -5,       /* a bounded device-side wait expired */
+    KDA_ERR_RANGE = -6          /* a chunk's summed decay is outside the range the chunkwise
+                                   form computes in fp32 (see the conventions above) */
 };
 
 enum { KDA_HEAD_DIM_K = 128, KDA_HEAD_DIM_V = 128, KDA_CHUNK = 64 };
 
-/* Plan format v1 (int32 words).  Header words: */
+/* Plan format v2 (int32 words).  Header words: */
 enum {
     KDA_PLAN_MAGIC = 0x4B444131,
-    KDA_PLAN_VERSION = 1,
+    KDA_PLAN_VERSION = 2,
     KDA_PLAN_HEADER_WORDS = 32,
     KDA_PH_MAGIC = 0, KDA_PH_VERSION = 1, KDA_PH_TOTAL = 2, KDA_PH_T = 3, KDA_PH_N = 4,
     KDA_PH_S = 5, KDA_PH_C = 6, KDA_PH_NPIECES = 7, KDA_PH_NCONT = 8, KDA_PH_TCONT = 9,
     KDA_PH_NFIN = 10, KDA_PH_NCHUNKS = 11, KDA_PH_NITEMS = 12, KDA_PH_MAXPIECE = 13,
     KDA_PH_OFF_BOUNDS = 14, KDA_PH_OFF_CU = 15, KDA_PH_OFF_SEGS = 16, KDA_PH_OFF_PIECES = 17,
-    KDA_PH_OFF_ITEMS = 18, KDA_PH_OFF_CHUNKS = 19, KDA_PH_OFF_CONT = 20, KDA_PH_OFF_FIN = 21
+    KDA_PH_OFF_ITEMS = 18, KDA_PH_OFF_CHUNKS = 19, KDA_PH_OFF_CONT = 20, KDA_PH_OFF_FIN = 21,
+    KDA_PH_CHECKSUM = 22
 };
+/* Word 22 is a checksum of the whole plan: FNV-1a over 32-bit words,
+ *     h = 2166136261; for every word w (word 22 taken as 0): h = (h ^ w) * 16777619 (mod 2^32),
+ * stored as its bit pattern.  Words 23..31 are zero. */
 /* Sections (in this order after the header):
  *   seg_bounds [S+1]; cu_seqlens [N+1];
  *   segs   [S][4]: sequence holding the segment's first token, flags
@@ -123,13 +139,18 @@ const char *kda_status_string(int status);
 /* cudaError_t value behind the most recent KDA_ERR_CUDA on this thread (0 if none). */
 int kda_last_cuda_error(void);
 
-/* Device-side status of the kernels run so far on the current device: every wait
- * inside a kernel (for a copy, a product or another thread's handoff) gives up
- * after about two seconds, records KDA_ERR_TIMEOUT in a status word, lets its
- * copies land, frees its tensor memory and returns, so the context stays
- * usable but the results of that call are invalid.  This call synchronises the
- * current device (the only entry point that does), reads every status word,
- * clears them and returns KDA_OK, KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if the
+/* Device-side status of the kernels run so far on the current device.  A kernel
+ * records, in its status word (the first error kept):
+ *   KDA_ERR_TIMEOUT      a wait inside it (for a copy, a product or another
+ *                        thread's handoff) gave up after about two seconds; it
+ *                        let its copies land, freed its tensor memory and
+ *                        returned, so the context stays usable;
+ *   KDA_ERR_RANGE        a chunk's summed decay was out of range (conventions);
+ *   KDA_ERR_INVALID_ARG  its device plan was not the host plan's copy, so it
+ *                        returned without touching memory.
+ * The results of such a call are invalid.  This call synchronises the current
+ * device (the only entry point that does), reads every status word, clears them
+ * and returns KDA_OK, the first error found, or KDA_ERR_CUDA if the
  * synchronisation or the read failed. */
 int kda_device_status(void);
 
@@ -160,6 +181,16 @@ int kda_selftest_wait_expiry(void *stream);
  */
 int kda_plan_segments(const int32_t *cu_seqlens, int32_t num_seqs, int32_t num_segments,
                       const int32_t *seg_bounds, int32_t chunk, int32_t *plan, size_t *plan_len);
+
+/*
+ * kda_plan_check -- validates a host plan word by word: the header's sizes and
+ * section offsets, then every section, by planning its segment bounds and
+ * cu_seqlens again and comparing all words (the checksum included).  The
+ * buffer must hold plan[KDA_PH_TOTAL] words.  Returns KDA_OK or
+ * KDA_ERR_INVALID_ARG.  Every entry point that takes a plan runs this check
+ * (a plan already accepted is recognised by its checksum and not re-planned).
+ */
+int kda_plan_check(const int32_t *plan);
 
 /* Bytes of one chunk package: the per-chunk operands that the chunk-parallel
  * preparation hands to the serial state pass (see kda_segment_forward). */
@@ -300,7 +331,10 @@ int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev, int32_t H
  *     10 MiB and fits; T = 4096, H = 8, S = 4 needs about 73 MiB and does not).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  The cached address belongs to the context it was looked
+ *     up in: after cudaDeviceReset, or once the primary context is destroyed
+ *     and created again, the next call finds a new context id and looks the
+ *     address up again (so that call, too, should come before any capture).
  *   - Nothing is allocated, freed or cleared: every workspace region is fully
  *     written before it is read within a call.
  *   - All calls on a device share the one array, which keeps the last call's

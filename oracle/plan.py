@@ -6,15 +6,18 @@ The rules follow cuLA PR #136 ("feat(kda): add cuDNN concatenated-summary
 Kimi CP", §Walkthrough, packed-shard planning): balanced or custom contiguous
 shards over a packed token stream, validated against sequence boundaries.
 
-Plan format v1 (int32 words)
+Plan format v2 (int32 words)
   header (32 words):
-     0 magic 0x4B444131        1 version 1            2 total words
+     0 magic 0x4B444131        1 version 2            2 total words
      3 T tokens                4 N sequences          5 S segments
      6 C chunk                 7 n_pieces             8 n_cont
      9 T_cont                 10 n_fin               11 n_chunks
     12 n_items                13 max piece length
     14..21 word offsets of: seg_bounds, cu_seqlens, segs, pieces, items,
-           chunks, cont, fin;   22..31 zero
+           chunks, cont, fin
+    22 checksum: FNV-1a over the 32-bit words of the whole plan (this word
+       taken as 0): h = 2166136261, then h = (h ^ w) * 16777619 mod 2^32 per
+       word, stored as a signed 32-bit value;   23..31 zero
   seg_bounds [S+1]; cu_seqlens [N+1]
   segs    [S][4]  (sequence containing the segment's first token, flags,
                    first piece, piece count); flags: 1 = segment starts a
@@ -37,7 +40,8 @@ Plan format v1 (int32 words)
 from __future__ import annotations
 
 MAGIC = 0x4B444131
-VERSION = 1
+VERSION = 2
+CHECKSUM_WORD = 22
 HEADER_WORDS = 32
 
 FIRST, CONT, SEG_LAST, SEQ_END = 1, 2, 4, 8
@@ -143,11 +147,21 @@ def plan_segments(cu_seqlens, num_segments, seg_bounds=None, chunk=64):
     for sec in sections:
         words = words + list(sec)
     assert len(words) == pos
+    words[CHECKSUM_WORD] = checksum(words)
     return words
 
 
+def checksum(words):
+    """FNV-1a over 32-bit words with the checksum word taken as 0, as a signed 32-bit value."""
+    h = 2166136261
+    for i, w in enumerate(words):
+        x = 0 if i == CHECKSUM_WORD else (int(w) & 0xFFFFFFFF)
+        h = ((h ^ x) * 16777619) & 0xFFFFFFFF
+    return h - (1 << 32) if h >= (1 << 31) else h
+
+
 def decode(words):
-    """Split a v1 plan into named Python lists (for tests)."""
+    """Split a v2 plan into named Python lists (for tests)."""
     h = list(words[:HEADER_WORDS])
     T, N, S = h[3], h[4], h[5]
     n_p, n_c, n_f, n_ch, n_it = h[7], h[8], h[10], h[11], h[12]

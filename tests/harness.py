@@ -112,3 +112,54 @@ def oracle_segment(inp, bounds, j, h, want_s_in=True):
         else:
             S_in = oracle.run_range(cu[s], a, h, q, k, v, g, b, S0=h0(s), want_o=False)["S"]
     return A, B, S_in
+
+
+def oracle_summaries(inp, bounds, heads=None, threads=None):
+    """A, B and S_in of every segment for the listed heads (default all), from the definitions,
+    one head per task on a thread pool (the oracle's C runner releases the GIL):
+      S_in[j]  the state of the monolithic run at b_j (h0 of a sequence starting there);
+      A_j, B_j the map of the segment: a zero-start run from a with the transition tracked when no
+               sequence starts inside [a, e); otherwise A_j = 0 and B_j is the monolithic state at e.
+    Returns arrays [S,H,K,K], [S,H,K,V], [S,H,K,V] (NaN for heads not listed)."""
+    import concurrent.futures as cf
+    import os
+    q, k, v, g, b = f32_inputs(inp)
+    cu = [int(x) for x in inp.cu_seqlens]
+    S = len(bounds) - 1
+    H = inp.heads
+    heads = list(range(H)) if heads is None else list(heads)
+    A = np.full((S, H, K, K), np.nan)
+    B = np.full((S, H, K, V), np.nan)
+    S_in = np.full((S, H, K, V), np.nan)
+    starts = set(cu[:-1])
+
+    def h0(s, h):
+        return np.zeros((K, V)) if inp.h0 is None else inp.h0[s, h].astype(np.float64)
+
+    def one_head(h):
+        # monolithic states at every segment bound, sequence by sequence
+        at = {}
+        for s in range(len(cu) - 1):
+            cuts = [x for x in bounds if cu[s] < x <= cu[s + 1]]
+            St, t = h0(s, h), cu[s]
+            for x in cuts:
+                St = oracle.run_range(t, x, h, q, k, v, g, b, S0=St, want_o=False)["S"]
+                t = x
+                at[(s, x)] = St
+        for j in range(S):
+            a, e = bounds[j], bounds[j + 1]
+            s_a = max(i for i in range(len(cu) - 1) if cu[i] <= a)
+            S_in[j, h] = h0(s_a, h) if cu[s_a] == a else at[(s_a, a)]
+            inside = [c for c in cu[:-1] if a <= c < e]
+            if inside:
+                s_e = max(i for i in range(len(cu) - 1) if cu[i] < e)
+                A[j, h] = 0.0
+                B[j, h] = at[(s_e, e)]
+            else:
+                r = oracle.run_range(a, e, h, q, k, v, g, b, S0=None, track_transition=True, want_o=False)
+                A[j, h], B[j, h] = r["P"], r["S"]
+
+    n = threads or max(1, min(len(heads), os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(one_head, heads))
+    return A, B, S_in

@@ -37,7 +37,8 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for want in ("kda_plan_segments", "kda_segment_forward", "kda_compose_summaries", "kda_apply_boundary",
                  "kda_forward_segmented", "kda_workspace_bytes", "kda_workspace_layout", "kda_status_string",
-                 "kda_last_cuda_error", "kda_device_status", "kda_selftest_wait_expiry", "kda_forward_two_pass"):
+                 "kda_last_cuda_error", "kda_device_status", "kda_selftest_wait_expiry", "kda_forward_two_pass",
+                 "kda_plan_check"):
         assert want in names
 
 

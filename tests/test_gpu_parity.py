@@ -4,15 +4,19 @@ Workloads are the seeded synthetic problems of context_kda_gb300.inputs (shapes
 of cuLA PR #110, "feat(cp): add opt-in NVSHMEM CP state handoff",
 §Correctness / §Performance, and the CP64 packed case of cuLA PR #136,
 "feat(kda): add cuDNN concatenated-summary Kimi CP", §Latest cuDNN
-compatibility).  Small workloads are compared element by element on every
-head; the large ones on sampled heads (every token and state of those heads)
-and sampled segments.  Tolerances are in tests/harness.py.
+compatibility).  Outputs and final states are compared element by element on
+every head of the single-sequence workloads, the packed 64-segment workload and
+the 32768-token long-context workloads, and A, B and S_in on every (segment,
+head) of them; the 131072-token workloads take four heads each (their oracle
+run on every head would dominate the suite).  Tolerances are in
+tests/harness.py.
 """
 import numpy as np
 import pytest
 
 from context_kda_gb300.inputs import bf16_to_f32, make_inputs, make_workload, workloads
-from harness import O_TOL, REL_TOL, gpu_forward, oracle_forward, oracle_segment, rel_err, to_device
+from harness import (O_TOL, REL_TOL, gpu_forward, oracle_forward, oracle_segment, oracle_summaries, rel_err,
+                     to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,20 +52,43 @@ def test_single_sequence_workloads_all_heads(name):
     _check_segments(res, inp, [(j, h) for j in range(inp.segments) for h in range(inp.heads)])
 
 
-def test_packed_varlen_64_segments_sampled_heads():
+def _check_all_segments(res, inp, heads=None):
+    """A, B and S_in of every segment of the listed heads (default all) against the oracle."""
+    b = res["bounds"]
+    A, B, S_in = oracle_summaries(inp, b, heads)
+    hs = list(range(inp.heads)) if heads is None else list(heads)
+    for h in hs:
+        for j in range(len(b) - 1):
+            if np.all(A[j, h] == 0):
+                assert np.all(res["A"][j, h] == 0), f"segment {j} head {h}: A must be exactly 0"
+    worst = max(rel_err(res["A"][:, hs], A[:, hs]), rel_err(res["B"][:, hs], B[:, hs]),
+                rel_err(res["S_in"][:, hs], S_in[:, hs]))
+    assert worst <= REL_TOL, f"summaries rel = {worst:.3e}"
+    return worst
+
+
+def test_packed_varlen_64_segments_every_head_and_segment():
     inp = make_workload(workloads()["packed65536_h32_s64"])
     res = gpu_forward(inp)
-    _check_outputs(res, inp, heads=[0, 31])
-    _check_segments(res, inp, [(j, h) for j in (0, 1, 17, 40, 63) for h in (0, 31)])
+    _check_outputs(res, inp)
+    _check_all_segments(res, inp)
 
 
-@pytest.mark.parametrize("name", ["t32768_h32_s8", "t32768_h32_s64", "t131072_h32_s8", "t131072_h32_s64"])
-def test_long_context_sampled(name):
-    w = workloads()[name]
-    inp = make_workload(w)
+@pytest.mark.parametrize("name", ["t32768_h32_s8", "t32768_h32_s64"])
+def test_long_context_every_head_and_segment(name):
+    inp = make_workload(workloads()[name])
     res = gpu_forward(inp)
-    _check_outputs(res, inp, heads=[5])
-    _check_segments(res, inp, [(1, 5), (w.segments - 1, 5)])
+    _check_outputs(res, inp)
+    _check_all_segments(res, inp)
+
+
+@pytest.mark.parametrize("name", ["t131072_h32_s8", "t131072_h32_s64"])
+def test_long_context_131072_four_heads(name):
+    inp = make_workload(workloads()[name])
+    res = gpu_forward(inp)
+    heads = [0, 5, 17, 31]
+    _check_outputs(res, inp, heads=heads)
+    _check_all_segments(res, inp, heads=heads)
 
 
 def test_three_call_path_matches_fused_bitwise():

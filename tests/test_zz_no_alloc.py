@@ -5,16 +5,17 @@ call cudaMalloc because an allocation can synchronise the device).  It uses the
 library's fixed 32 MiB device workspace instead of a caller buffer.
 
 The test calls it through the C ABI twice in a row, on two different problems
-and then on the first again, and checks every result against
-kda_forward_segmented with a caller-allocated workspace, using the tolerances
-of the other GPU tests.  This file is collected last on purpose, and it passes
-both on its own in a fresh process and after the rest of the suite.
+and then on the first again.  The forward is deterministic, so every result
+must equal, bit for bit, that of kda_forward_segmented with a caller-allocated
+workspace; both problems are also checked against the fp64 oracle with the
+tolerances of the other GPU tests.  This file is collected last on purpose, and
+it passes both on its own in a fresh process and after the rest of the suite.
 """
 import numpy as np
 import pytest
 
 from context_kda_gb300.inputs import make_inputs, make_workload, workloads
-from harness import O_TOL, REL_TOL, K, V, rel_err, to_device
+from harness import O_TOL, REL_TOL, K, V, oracle_forward, rel_err, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -34,15 +35,18 @@ def _run(inp, noalloc):
         ws = torch.empty(kda.kda_workspace_bytes(plan, inp.heads), dtype=torch.uint8, device="cuda")
         kda.kda_forward_segmented(*args, ws)
     torch.cuda.synchronize()
-    return o.float().cpu().numpy(), fin.cpu().numpy()
+    return o.view(torch.int16).cpu().numpy(), o.float().cpu().numpy(), fin.cpu().numpy()
 
 
 def _compare(inp):
-    o_ref, f_ref = _run(inp, noalloc=False)
-    o_na, f_na = _run(inp, noalloc=True)
+    bits_ref, _, f_ref = _run(inp, noalloc=False)
+    bits_na, o_na, f_na = _run(inp, noalloc=True)
     assert np.all(np.isfinite(o_na)) and np.all(np.isfinite(f_na))
-    assert float(np.max(np.abs(o_na - o_ref))) <= O_TOL
-    assert rel_err(f_na, f_ref) <= REL_TOL
+    assert np.array_equal(bits_na, bits_ref)
+    assert np.array_equal(f_na.view(np.int32), f_ref.view(np.int32))
+    o_or, f_or = oracle_forward(inp)
+    assert float(np.max(np.abs(o_na - o_or))) <= O_TOL
+    assert rel_err(f_na, f_or) <= REL_TOL
 
 
 def test_noalloc_matches_caller_workspace_on_consecutive_calls():
