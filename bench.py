@@ -499,7 +499,53 @@ def run_ours(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-EXTRA_WORKLOADS = ("packed65536_h32_s64", "t131072_h32_s64")
+EXTRA_WORKLOADS = ("packed65536_h32_s64", "t131072_h32_s64", "t32768_h2_s64")
+
+
+def time_scans(prob, stream, flush, steps=10, warmup=3):
+    """The composition alone, by the chain and by the two-level scan, from the summaries of one step:
+    mean CUDA-event ms of each (L2 flushed before every run)."""
+    import torch
+    kda = prob.kda
+    prob.step(stream)
+    scan_ws = torch.empty(max(1, kda.kda_scan_workspace_bytes(prob.plan, prob.H)), dtype=torch.uint8,
+                          device=prob.o.device)
+    out = {}
+    for name in ("chain", "blocked"):
+        def run():
+            if name == "chain":
+                kda.kda_compose_summaries(prob.plan, prob.plan_dev, prob.H, prob.A, prob.B, prob.h0, prob.S_in, stream)
+            else:
+                kda.kda_compose_summaries_blocked(prob.plan, prob.plan_dev, prob.H, prob.A, prob.B, prob.h0,
+                                                  prob.S_in, scan_ws, stream)
+        for _ in range(warmup):
+            flush.fill_(1)
+            run()
+        ms = []
+        for _ in range(steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        out[name] = float(np.mean(ms))
+    del scan_ws
+    return out
+
+
+def scan_bytes(S, H):
+    """Algorithmic HBM bytes of the two schedules of the composition: the chain reads A and B and writes
+    S_in per segment-head; the two-level scan adds the group totals (written, then read) and the group
+    incoming states (written, then read) and reads A and B twice."""
+    import math
+    m = math.isqrt(S - 1) + 1 if S > 1 else 1
+    G = (S + m - 1) // m
+    seg = S * H * (BYTES_SEGMENT + BYTES_SEQ_STATE)
+    totals = G * H * BYTES_SEGMENT
+    entry = G * H * BYTES_SEQ_STATE
+    return {"chain": seg, "blocked": seg + S * H * BYTES_SEGMENT + 2 * totals + 2 * entry}
 
 
 def extra_workloads(args, dev, stream, flush, peaks):
@@ -522,6 +568,11 @@ def extra_workloads(args, dev, stream, flush, peaks):
             "kernel_hbm_frac": {n: kb[n] / (kern[i] / 1e3) / 1e9 / peaks["hbm_gbs"] for i, n in enumerate(names)},
             "algorithmic_bytes": kb, "config": _config(w, 1),
         }
+        scans = time_scans(prob, stream, flush)
+        sb = scan_bytes(prob.S, prob.H)
+        out[name]["compose_schedules_ms"] = scans
+        out[name]["compose_schedules_hbm_frac"] = {k_: sb[k_] / (scans[k_] / 1e3) / 1e9 / peaks["hbm_gbs"]
+                                                   for k_ in scans}
         prob.free()
         del prob
         torch.cuda.empty_cache()

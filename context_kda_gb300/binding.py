@@ -47,12 +47,15 @@ def _load():
     lib.kda_workspace_bytes.restype = SZ
     lib.kda_segment_forward.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
     lib.kda_compose_summaries.argtypes = [P, P, I32, P, P, P, P, P]
+    lib.kda_compose_summaries_blocked.argtypes = [P, P, I32, P, P, P, P, P, SZ, P]
+    lib.kda_scan_workspace_bytes.argtypes = [P, I32]
+    lib.kda_scan_workspace_bytes.restype = SZ
     lib.kda_apply_boundary.argtypes = [P, P, I32, P, P, SZ, P, P, P]
     lib.kda_forward_segmented.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.kda_forward_segmented_noalloc.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P]
     lib.kda_forward_two_pass.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
     for name in ("kda_plan_segments", "kda_plan_check", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
-                 "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc",
+                 "kda_compose_summaries_blocked", "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc",
                  "kda_forward_two_pass"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -160,6 +163,18 @@ def kda_compose_summaries(plan, plan_dev, H, A, B, h0, S_in, stream=None):
     rc = _lib.kda_compose_summaries(_hp(p), _dp(plan_dev), int(H), _dp(A), _dp(B), _dp(h0), _dp(S_in),
                                     _stream(stream))
     _check("kda_compose_summaries", rc)
+
+
+def kda_scan_workspace_bytes(plan, H: int) -> int:
+    return int(_lib.kda_scan_workspace_bytes(_hp(_words(plan)), int(H)))
+
+
+def kda_compose_summaries_blocked(plan, plan_dev, H, A, B, h0, S_in, ws, stream=None):
+    """S_in by the two-level (log-depth across groups) scan; ws holds kda_scan_workspace_bytes."""
+    p = _words(plan)
+    rc = _lib.kda_compose_summaries_blocked(_hp(p), _dp(plan_dev), int(H), _dp(A), _dp(B), _dp(h0), _dp(S_in),
+                                            _dp(ws), _nbytes(ws), _stream(stream))
+    _check("kda_compose_summaries_blocked", rc)
 
 
 def kda_apply_boundary(plan, plan_dev, H, S_in, ws, o, final_state, stream=None):

@@ -59,6 +59,8 @@ bool plan_ok(const int32_t *plan)
 
 size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
+constexpr int kBlockedMinSegments = 16;   // fewer segments always compose by the chain
+
 bool layout(const int32_t *plan, int32_t H, size_t off[7])
 {
     if (!plan_ok(plan) || H < 1) return false;
@@ -76,8 +78,23 @@ bool layout(const int32_t *plan, int32_t H, size_t off[7])
         off[i] = pos;
         pos = round256(pos + sizes[i]);
     }
+    // from 16 segments on, room for the two-level scan's group totals and incoming states after S_in
+    if (plan[KDA_PH_S] >= kBlockedMinSegments) pos = round256(pos + kda::scan_scratch_bytes(plan, H));
     off[6] = pos;
     return true;
+}
+
+// The composition schedule of the fused entry points: the two-level scan where its estimated depth,
+// counted in products per CTA over the waves the device's SMs need, is below the chain's.
+bool use_blocked_scan(const int32_t *plan, int32_t H)
+{
+    const long long S = plan[KDA_PH_S];
+    if (S < kBlockedMinSegments) return false;
+    const long long sm = kda::sm_count(), m = kda::scan_group_size(static_cast<int>(S)), G = (S + m - 1) / m;
+    auto waves = [&](long long ctas) { return (ctas + sm - 1) / sm; };
+    const long long chain = waves(4LL * H) * S;
+    const long long blocked = waves(8LL * H * G) * (m + 1) + (G - 1) + waves(4LL * H * G) * (m + 1);
+    return blocked < chain;
 }
 
 bool inputs_ok(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -87,6 +104,11 @@ bool inputs_ok(const void *q, const void *k, const void *v, const float *g, cons
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta)) return false;
     if (h0 && !aligned16(h0)) return false;
     return true;
+}
+
+size_t S_in_bytes(const int32_t *plan, int32_t H)
+{
+    return static_cast<size_t>(plan[KDA_PH_S]) * static_cast<size_t>(H) * kda::KD * kda::VD * 4;
 }
 
 kda::Workspace carve(void *ws, const size_t off[7])
@@ -157,17 +179,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn()
     return fn;
 }
 
-bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows)
+bool encode_f32_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t cols, uint32_t box_rows)
 {
     auto fn = tmap_encode_fn();
     if (!fn || rows == 0) return false;
-    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {128ull * 4};
+    const cuuint64_t dims[2] = {cols, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
     const cuuint32_t box[2] = {32, box_rows};
     const cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows)
+{
+    return encode_f32_rows(m, ptr, rows, 128, box_rows);
 }
 
 bool encode_rows_3d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uint32_t elem, int H, int T,
@@ -241,6 +268,27 @@ extern "C" int kda_compose_summaries(const int32_t *plan, const int32_t *plan_de
     return cuda_status(kda::launch_compose(plan, plan_dev, H, A, B, h0, S_in, static_cast<cudaStream_t>(stream)));
 }
 
+extern "C" size_t kda_scan_workspace_bytes(const int32_t *plan, int32_t H)
+{
+    size_t off[7];
+    if (!layout(plan, H, off)) return 0;
+    return kda::scan_scratch_bytes(plan, H);
+}
+
+extern "C" int kda_compose_summaries_blocked(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                             const float *A, const float *B, const float *h0, float *S_in,
+                                             void *ws, size_t ws_bytes, void *stream)
+{
+    size_t off[7];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!A || !B || !S_in || !aligned16(A) || !aligned16(B) || !aligned16(S_in)) return KDA_ERR_INVALID_ARG;
+    if (h0 && !aligned16(h0)) return KDA_ERR_INVALID_ARG;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < kda::scan_scratch_bytes(plan, H)) return KDA_ERR_WORKSPACE;
+    return cuda_status(kda::launch_compose_blocked(plan, plan_dev, H, A, B, h0, S_in, ws,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int kda_apply_boundary(const int32_t *plan, const int32_t *plan_dev, int32_t H,
                                   const float *S_in, const void *ws, size_t ws_bytes, kda_bf16 *o,
                                   float *final_state, void *stream)
@@ -273,7 +321,10 @@ extern "C" int kda_forward_segmented(const int32_t *plan, const int32_t *plan_de
     int rc = cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, w.A, w.B,
                                                    final_state, w.qhat, w.afin, w.pkg, s));
     if (rc != KDA_OK) return rc;
-    rc = cuda_status(kda::launch_compose(plan, plan_dev, H, w.A, w.B, h0, w.S_in, s));
+    rc = cuda_status(use_blocked_scan(plan, H)
+                         ? kda::launch_compose_blocked(plan, plan_dev, H, w.A, w.B, h0, w.S_in,
+                                                       static_cast<char *>(ws) + round256(off[5] + S_in_bytes(plan, H)), s)
+                         : kda::launch_compose(plan, plan_dev, H, w.A, w.B, h0, w.S_in, s));
     if (rc != KDA_OK) return rc;
     return cuda_status(kda::launch_boundary(plan, plan_dev, H, w.S_in, w.qhat, w.afin, o, final_state, s));
 }

@@ -128,6 +128,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn();
 // Tensor map of a row-major [rows][128] fp32 matrix with a box of 32 columns x box_rows
 // rows and the 128-byte swizzle (16-byte chunk c of box row r lands at chunk c ^ (r % 8)).
 bool encode_f32_rows128(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t box_rows);
+// The same for a row-major [rows][cols] fp32 matrix (cols a multiple of 32).
+bool encode_f32_rows(CUtensorMap *m, const void *ptr, uint64_t rows, uint32_t cols, uint32_t box_rows);
 
 // Tensor map of a [T][H][128] tensor (inner dimension first) with a box of 'inner' columns x 1
 // head x box_rows rows and the 128-byte swizzle; elem = element bytes.
@@ -148,6 +150,13 @@ cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev
                                uint16_t *qhat, float *afin, cudaStream_t stream);
 cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
                            const float *B, const float *h0, float *S_in, cudaStream_t stream);
+// The two-level (blocked) scan: group totals, a chain over the groups, then every group from its
+// incoming state; 'scratch' holds scan_scratch_bytes(plan_host, H) bytes.
+cudaError_t launch_compose_blocked(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
+                                   const float *B, const float *h0, float *S_in, void *scratch, cudaStream_t stream);
+size_t scan_scratch_bytes(const int32_t *plan_host, int H);
+// Segments per group of the blocked scan (about sqrt(S)) and the number of groups.
+int scan_group_size(int S);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
                             const uint16_t *qhat, const float *afin, uint16_t *o, float *final_state,
                             cudaStream_t stream);

@@ -102,6 +102,8 @@ def workloads() -> Dict[str, Workload]:
         Workload("t32768_h32_s64", (32768,), 32, 64, note="long context"),
         Workload("t131072_h32_s8", (131072,), 32, 8, note="long context"),
         Workload("t131072_h32_s64", (131072,), 32, 64, note="long context"),
+        Workload("t32768_h2_s64", (32768,), 2, 64,
+                 note="few heads, many segments: the composition chain leaves most SMs idle"),
     ]
     return {x.name: x for x in w}
 

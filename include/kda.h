@@ -207,6 +207,8 @@ enum { KDA_PACKAGE_BYTES = 123392 };
  *   A      fp32 [S][H][K][K]      (used by kda_forward_segmented)
  *   B      fp32 [S][H][K][V]      (used by kda_forward_segmented)
  *   S_in   fp32 [S][H][K][V]      (used by kda_forward_segmented)
+ *   then, when S >= 16, kda_scan_workspace_bytes(plan, H) bytes of scratch for
+ *   the two-level scan (256-byte aligned, included in off[6]).
  * The three-call path uses the first off[3] bytes (qhat, fin, packages); A, B
  * and S_in are then caller tensors.  kda_apply_boundary reads only qhat and fin
  * (the first off[2] bytes).  Returns KDA_OK or KDA_ERR_INVALID_ARG.
@@ -264,6 +266,34 @@ int kda_compose_summaries(const int32_t *plan, const int32_t *plan_dev, int32_t 
                           void *stream);
 
 /*
+ * kda_compose_summaries_blocked -- the same S_in as kda_compose_summaries by a
+ * two-level scan that is log-depth across groups (PR #136 §Summary: affine
+ * summary composition in FP32; the maps F_j of the chain, S_in[j] =
+ * F_j(S_in[j-1]), composed as a prefix scan).  The segments are cut into
+ * groups of m = ceil(sqrt(S)); three kernels run on 'stream':
+ *   1. every group's total map C_g = F_last o ... o F_first, all groups and
+ *      heads in parallel, carried as the K x (K + V) state [A~ | B~] from the
+ *      identity;
+ *   2. the chain over the group totals, E_{g+1} = C_g(E_g): each group's
+ *      incoming state;
+ *   3. every group in parallel from E_g through its own maps, writing S_in.
+ * The depth is about 3 sqrt(S) products instead of S - 1, for about three
+ * times the tensor work and twice the memory traffic of the chain.
+ *   ws, ws_bytes  device scratch of at least kda_scan_workspace_bytes(plan, H)
+ *                 bytes, 256-byte aligned (group totals and incoming states).
+ * Other arguments and results as kda_compose_summaries; the outputs agree
+ * with it within rounding.  Returns KDA_ERR_WORKSPACE when ws_bytes is short.
+ */
+int kda_compose_summaries_blocked(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                  const float *A, const float *B, const float *h0, float *S_in,
+                                  void *ws, size_t ws_bytes, void *stream);
+
+/* Device scratch bytes kda_compose_summaries_blocked needs: G*H*K*(K+V)*4
+ * (group totals) + G*H*K*V*4 (incoming states), G = ceil(S / ceil(sqrt(S)));
+ * 0 if the plan or H is invalid. */
+size_t kda_scan_workspace_bytes(const int32_t *plan, int32_t H);
+
+/*
  * kda_apply_boundary -- fix-up from the incoming states: for every token t of
  * a continuing piece in segment j, o_t = bf16(o_local,t + S_in[j]^T qhat_t);
  * for every sequence that ends in a continuing piece of segment j,
@@ -278,8 +308,13 @@ int kda_apply_boundary(const int32_t *plan, const int32_t *plan_dev, int32_t H,
 
 /*
  * kda_forward_segmented -- the whole segmented forward: kda_segment_forward,
- * kda_compose_summaries and kda_apply_boundary in order on 'stream', with A,
- * B and S_in held in the workspace (kda_workspace_bytes(plan, H) bytes).
+ * the composition and kda_apply_boundary in order on 'stream', with A, B and
+ * S_in held in the workspace (kda_workspace_bytes(plan, H) bytes).  The
+ * composition takes the chain (kda_compose_summaries) or, from 16 segments
+ * on, the two-level scan (kda_compose_summaries_blocked) when its depth,
+ * counted in products per CTA over the waves this device's SMs need, is the
+ * smaller: with few heads and many segments, where the chain's CTAs leave
+ * most SMs idle.
  * Outputs o and final_state equal the monolithic recurrence of every sequence
  * (PR #136 §Walkthrough: compared with a monolithic reference).
  */

@@ -163,3 +163,32 @@ def oracle_summaries(inp, bounds, heads=None, threads=None):
     with cf.ThreadPoolExecutor(max_workers=n) as ex:
         list(ex.map(one_head, heads))
     return A, B, S_in
+
+
+def gpu_scan_both(inp, seg_bounds=None):
+    """The three-call path, with S_in computed both by the chain (kda_compose_summaries) and by the
+    two-level scan (kda_compose_summaries_blocked) from the same device summaries.  Returns numpy
+    S_in_chain, S_in_blocked, A, B and the segment bounds."""
+    import torch
+    from context_kda_gb300 import binding as kda
+    dev = to_device(inp)
+    T, H, N = inp.tokens, inp.heads, inp.num_seqs
+    S = inp.segments if seg_bounds is None else len(seg_bounds) - 1
+    plan = kda.kda_plan_segments(inp.cu_seqlens, S, seg_bounds)
+    plan_dev = kda.upload_plan(plan)
+    off = kda.kda_workspace_layout(plan, H)
+    ws = torch.empty(off[6], dtype=torch.uint8, device="cuda")
+    scan_ws = torch.empty(kda.kda_scan_workspace_bytes(plan, H), dtype=torch.uint8, device="cuda")
+    o = torch.empty((T, H, V), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((N, H, K, V), dtype=torch.float32, device="cuda")
+    A = torch.empty((S, H, K, K), dtype=torch.float32, device="cuda")
+    B = torch.empty((S, H, K, V), dtype=torch.float32, device="cuda")
+    S1 = torch.full((S, H, K, V), float("nan"), dtype=torch.float32, device="cuda")
+    S2 = torch.full((S, H, K, V), float("nan"), dtype=torch.float32, device="cuda")
+    kda.kda_segment_forward(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"],
+                            1.0, o, A, B, fin, ws)
+    kda.kda_compose_summaries(plan, plan_dev, H, A, B, dev["h0"], S1)
+    kda.kda_compose_summaries_blocked(plan, plan_dev, H, A, B, dev["h0"], S2, scan_ws)
+    torch.cuda.synchronize()
+    return {"S_in_chain": S1.cpu().numpy(), "S_in_blocked": S2.cpu().numpy(), "A": A.cpu().numpy(),
+            "B": B.cpu().numpy(), "bounds": plan_bounds(plan, S)}

@@ -126,7 +126,9 @@ def test_summary_workspace_matches_the_pages(kda):
 @pytest.mark.parametrize("name", list(workloads().keys()))
 def test_workspace_regions_hold_what_the_header_documents(kda, name):
     """qhat bf16 [H][T_cont][K], fin fp32 [n_fin][H][K][K], packages [H][n_chunks] of
-    KDA_PACKAGE_BYTES, then A, B, S_in; each region starts on a 256-byte boundary."""
+    KDA_PACKAGE_BYTES, then A, B, S_in, and from 16 segments on the two-level scan's scratch
+    (G H K (K + V) fp32 group totals, then G H K V fp32 incoming states, G = ceil(S / ceil(sqrt S)));
+    each region starts on a 256-byte boundary."""
     w = workloads()[name]
     plan = kda.kda_plan_segments(_cu(w.seqlens), w.segments)
     H, K = w.heads, 128
@@ -135,6 +137,11 @@ def test_workspace_regions_hold_what_the_header_documents(kda, name):
     T_cont, n_fin, n_chunks, S = int(plan[9]), int(plan[10]), int(plan[11]), int(plan[5])
     sizes = [H * T_cont * K * 2, n_fin * H * K * K * 4, n_chunks * H * 123392, S * H * K * K * 4,
              S * H * K * K * 4, S * H * K * K * 4]
+    if S >= 16:
+        m = next(x for x in range(1, S + 1) if x * x >= S)
+        G = (S + m - 1) // m
+        sizes[5] = up(sizes[5]) + up(G * H * K * 256 * 4) + G * H * K * K * 4
+        assert kda.kda_scan_workspace_bytes(plan, H) == up(G * H * K * 256 * 4) + G * H * K * K * 4
     assert off[0] == 0
     for i, n in enumerate(sizes):
         assert off[i + 1] - off[i] == up(n), i

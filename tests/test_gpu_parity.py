@@ -252,3 +252,50 @@ def test_expired_wait_is_reported_and_the_context_survives():
     res = gpu_forward(inp)
     _check_outputs(res, inp)
     assert kda.kda_device_status() == kda.KDA_OK
+
+
+# ---- the two-level (blocked, log-depth across groups) scan: the same S_in as the chain
+
+def _check_blocked(inp, heads=None, seg_bounds=None):
+    from harness import gpu_scan_both
+    res = gpu_scan_both(inp, seg_bounds)
+    assert np.all(np.isfinite(res["S_in_blocked"]))
+    hs = list(range(inp.heads)) if heads is None else list(heads)
+    _, _, S_ref = oracle_summaries(inp, res["bounds"], hs)
+    e_blocked = rel_err(res["S_in_blocked"][:, hs], S_ref[:, hs])
+    e_chain = rel_err(res["S_in_chain"][:, hs], S_ref[:, hs])
+    assert e_blocked <= REL_TOL, f"blocked scan S_in rel = {e_blocked:.3e}"
+    assert e_chain <= REL_TOL, f"chain S_in rel = {e_chain:.3e}"
+    assert rel_err(res["S_in_blocked"], res["S_in_chain"]) <= REL_TOL
+    return e_blocked
+
+
+def test_blocked_scan_packed_every_head_and_segment():
+    _check_blocked(make_workload(workloads()["packed65536_h32_s64"]))
+
+
+def test_blocked_scan_long_context_64_segments():
+    _check_blocked(make_workload(workloads()["t32768_h32_s64"]), heads=[0, 7, 31])
+
+
+@pytest.mark.parametrize("seqlens,S,h0_std", [
+    ([1], 1, 0.0),                              # one segment, one group
+    ([700], 2, 0.2),                            # two segments: groups of two
+    ([900, 40, 300], 5, 0.1),                   # groups of 3, the last one short
+    ([5, 5, 5, 5, 80], 20, 0.1),                # seeds and updates inside and at group starts
+    ([2000], 17, 0.0),                          # S just above a square: a one-segment last group
+    ([600, 1, 900], 50, 0.3),                   # a sequence starting exactly at a segment start
+])
+def test_blocked_scan_edge_cases(seqlens, S, h0_std):
+    inp = make_inputs(seqlens, heads=2, segments=S, h0_std=h0_std, seed=41, g_lo=-0.2)
+    _check_blocked(inp)
+
+
+def test_fused_path_with_the_blocked_scan_every_head_and_segment():
+    """Few heads and many segments: kda_forward_segmented composes by the two-level scan there (its
+    depth model picks it on this device); outputs, final states and every summary against the
+    oracle."""
+    inp = make_workload(workloads()["t32768_h2_s64"])
+    res = gpu_forward(inp)
+    _check_outputs(res, inp)
+    _check_all_segments(res, inp)
