@@ -14,7 +14,8 @@ import importlib
 _BINDING_NAMES = ("kda_status_string", "kda_plan_segments", "kda_plan_check", "kda_workspace_layout",
                   "kda_workspace_bytes", "kda_segment_forward", "kda_compose_summaries", "kda_apply_boundary",
                   "kda_forward_segmented", "kda_forward_two_pass", "kda_forward_segmented_noalloc",
-                  "kda_device_status", "kda_selftest_wait_expiry", "upload_plan", "KDAError", "LIB_PATH")
+                  "kda_device_status", "kda_selftest_wait_expiry", "kda_compose_summaries_blocked",
+                  "kda_scan_workspace_bytes", "kda_backward_segmented", "kda_backward_workspace_bytes", "upload_plan", "KDAError", "LIB_PATH")
 
 
 def __getattr__(name):

@@ -54,8 +54,12 @@ def _load():
     lib.kda_forward_segmented.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.kda_forward_segmented_noalloc.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P]
     lib.kda_forward_two_pass.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, SZ, P]
+    lib.kda_backward_segmented.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, P, P, P,
+                                           P, SZ, P]
+    lib.kda_backward_workspace_bytes.argtypes = [P, I32]
+    lib.kda_backward_workspace_bytes.restype = SZ
     for name in ("kda_plan_segments", "kda_plan_check", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
-                 "kda_compose_summaries_blocked", "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc",
+                 "kda_compose_summaries_blocked", "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc", "kda_backward_segmented",
                  "kda_forward_two_pass"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -200,6 +204,20 @@ def kda_forward_two_pass(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, fina
                                    _dp(h0), float(scale), _dp(o), _dp(final_state), _dp(ws), _nbytes(ws),
                                    _stream(stream))
     _check("kda_forward_two_pass", rc)
+
+
+def kda_backward_workspace_bytes(plan, H: int) -> int:
+    return int(_lib.kda_backward_workspace_bytes(_hp(_words(plan)), int(H)))
+
+
+def kda_backward_segmented(plan, plan_dev, H, q, k, v, g, beta, h0, scale, dout, dfinal, dq, dk, dv, dg, dbeta,
+                           dh0, ws, stream=None):
+    """Gradients of the segmented forward (see include/kda.h); dfinal and dh0 may be None."""
+    p = _words(plan)
+    rc = _lib.kda_backward_segmented(_hp(p), _dp(plan_dev), int(H), _dp(q), _dp(k), _dp(v), _dp(g), _dp(beta),
+                                     _dp(h0), float(scale), _dp(dout), _dp(dfinal), _dp(dq), _dp(dk), _dp(dv),
+                                     _dp(dg), _dp(dbeta), _dp(dh0), _dp(ws), _nbytes(ws), _stream(stream))
+    _check("kda_backward_segmented", rc)
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

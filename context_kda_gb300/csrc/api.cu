@@ -156,7 +156,7 @@ extern "C" int kda_device_status(void)
     }
     int worst = KDA_OK;
     for (int st : {kda::take_prep_status(), kda::take_state_status(), kda::take_compose_status(),
-                   kda::take_boundary_status()})
+                   kda::take_boundary_status(), kda::take_backward_status()})
         if (st != KDA_OK && worst == KDA_OK) worst = st;
     return worst;
 }
@@ -343,4 +343,75 @@ extern "C" int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev
     const kda::Workspace w = carve(ws, off);
     return cuda_status(kda::launch_two_pass(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, w.A, w.B, w.S_in,
                                             final_state, w.pkg, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+constexpr int kBackwardGrid = 152;   // CTAs of the backward's chunk and piece kernels (grid-stride)
+
+// Regions of the backward's workspace after the forward's: o and final states of the forward run it
+// needs (not returned), the chunk start states and end gradients, the segment end gradients and
+// continuing pieces' incoming-state gradients, and the CTAs' scratch.
+bool backward_layout(const int32_t *plan, int32_t H, size_t off[8])
+{
+    size_t fw[7];
+    if (!layout(plan, H, fw)) return false;
+    const size_t h = static_cast<size_t>(H), K = kda::KD, V = kda::VD;
+    const size_t T = static_cast<size_t>(plan[KDA_PH_T]), N = static_cast<size_t>(plan[KDA_PH_N]);
+    const size_t S = static_cast<size_t>(plan[KDA_PH_S]), C = static_cast<size_t>(plan[KDA_PH_NCHUNKS]);
+    const size_t sizes[7] = {T * h * V * 2, N * h * K * V * 4, h * C * K * V * 4, h * C * K * V * 4,
+                             S * h * K * V * 4, S * h * K * V * 4,
+                             static_cast<size_t>(kBackwardGrid) * kda::backward_scratch_floats() * 4};
+    size_t pos = fw[6];
+    for (int i = 0; i < 7; ++i) {
+        off[i] = pos;
+        pos = round256(pos + sizes[i]);
+    }
+    off[7] = pos;
+    return true;
+}
+
+}  // namespace
+
+extern "C" size_t kda_backward_workspace_bytes(const int32_t *plan, int32_t H)
+{
+    size_t off[8];
+    return backward_layout(plan, H, off) ? off[7] : 0;
+}
+
+extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                      const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const float *g,
+                                      const float *beta, const float *h0, float scale, const kda_bf16 *dout,
+                                      const float *dfinal, float *dq, float *dk, float *dv, float *dg,
+                                      float *dbeta, float *dh0, void *ws, size_t ws_bytes, void *stream)
+{
+    size_t fw[7], off[8];
+    if (!layout(plan, H, fw) || !backward_layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
+    if (!dout || !aligned16(dout) || (dfinal && !aligned16(dfinal)) || (dh0 && !aligned16(dh0)))
+        return KDA_ERR_INVALID_ARG;
+    if (!dq || !dk || !dv || !dg || !dbeta || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(dg) || !aligned16(dbeta))
+        return KDA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < off[7]) return KDA_ERR_WORKSPACE;
+    const kda::Workspace w = carve(ws, fw);
+    char *b = static_cast<char *>(ws);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the forward's local pass and composition: S_in, the segment transitions A and the final-state
+    // transitions of continuing pieces
+    int rc = cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale,
+                                                   reinterpret_cast<uint16_t *>(b + off[0]), w.A, w.B,
+                                                   reinterpret_cast<float *>(b + off[1]), w.qhat, w.afin, w.pkg, s));
+    if (rc != KDA_OK) return rc;
+    rc = cuda_status(use_blocked_scan(plan, H)
+                         ? kda::launch_compose_blocked(plan, plan_dev, H, w.A, w.B, h0, w.S_in,
+                                                       b + round256(fw[5] + S_in_bytes(plan, H)), s)
+                         : kda::launch_compose(plan, plan_dev, H, w.A, w.B, h0, w.S_in, s));
+    if (rc != KDA_OK) return rc;
+    return cuda_status(kda::launch_backward(
+        plan, plan_dev, H, q, k, v, g, beta, h0, scale, dout, dfinal, w.A, w.afin, w.S_in,
+        reinterpret_cast<float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
+        reinterpret_cast<float *>(b + off[4]), reinterpret_cast<float *>(b + off[5]),
+        reinterpret_cast<float *>(b + off[6]), kBackwardGrid, dq, dk, dv, dg, dbeta, dh0, s));
 }

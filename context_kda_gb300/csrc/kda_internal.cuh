@@ -99,6 +99,7 @@ int take_prep_status();
 int take_state_status();
 int take_compose_status();
 int take_boundary_status();
+int take_backward_status();
 cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
 
 // Launches a kernel that may begin while the previous kernel on the stream finishes (programmatic
@@ -155,6 +156,16 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
 cudaError_t launch_compose_blocked(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
                                    const float *B, const float *h0, float *S_in, void *scratch, cudaStream_t stream);
 size_t scan_scratch_bytes(const int32_t *plan_host, int H);
+// The backward (FP32 on the CUDA cores): see backward.cu.  'scratch' holds grid x
+// backward_scratch_floats() floats; xs and gs hold [H][n_chunks][K][V] floats each, G_end and Qd
+// [S][H][K][V] each.
+size_t backward_scratch_floats();
+cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
+                            const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
+                            const float *h0, float scale, const uint16_t *dout, const float *dfinal,
+                            const float *A, const float *afin, const float *S_in, float *xs, float *gs,
+                            float *G_end, float *Qd, float *scratch, int grid, float *dq, float *dk, float *dv,
+                            float *dg, float *dbeta, float *dh0, cudaStream_t stream);
 // Segments per group of the blocked scan (about sqrt(S)) and the number of groups.
 int scan_group_size(int S);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,

@@ -209,3 +209,15 @@ def make_workload(w: Workload, seed: Optional[int] = None) -> Inputs:
     return make_inputs(w.seqlens if w.lognormal_lengths is None else None, w.heads, w.segments,
                        w.g_lo, w.g_hi, w.h0_std, w.seed if seed is None else seed,
                        draw_lengths_spec=w.lognormal_lengths)
+
+
+def draw_output_grads(inp: Inputs, seed: int = 0, with_dfinal: bool = True):
+    """Seeded gradients of a problem's outputs for the backward: do ~ N(0,1) rounded to bf16
+    [T,H,V] (tensor id 7) and, when asked, dfinal ~ N(0,1) fp32 [N,H,K,V] (tensor id 8)."""
+    T, H, N = inp.tokens, inp.heads, inp.num_seqs
+    V, K = inp.v.shape[2], inp.q.shape[2]
+    do = _draw_rows(seed, 7, T * H, V, "bf16").reshape(T, H, V)
+    dfinal = None
+    if with_dfinal:
+        dfinal = _block_rng(seed, 8, 0).standard_normal((N, H, K, V), dtype=np.float32)
+    return do, dfinal

@@ -348,6 +348,46 @@ int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev, int32_t H
                          void *stream);
 
 /*
+ * kda_backward_segmented -- gradients of the segmented forward, segment-
+ * parallel through the following summaries (PR #136 §Summary and its
+ * walkthrough's sequence diagram: the following FP32 summaries are gathered
+ * during the backward; PR #110 §Correctness: output and Q/K/V/g/beta
+ * gradients).  The loss is L = sum_t <do_t, o_t> + sum_seq <dfinal, S_end>,
+ * o and S_end those of kda_forward_segmented on the same inputs.
+ *   q, k, v, g, beta, h0, scale   the forward's inputs (device), as above.
+ *   dout     device bf16 [T][H][V]: the gradient of the outputs.
+ *   dfinal   device fp32 [N][H][K][V] or NULL (zeros): of the final states.
+ *   dq, dk   out device fp32 [T][H][K];   dv out fp32 [T][H][V];
+ *   dg       out device fp32 [T][H][K];   dbeta out fp32 [T][H];
+ *   dh0      out device fp32 [N][H][K][V] (the gradient of the initial
+ *            states, defined also when h0 is NULL) or NULL (not written).
+ *   ws, ws_bytes  device workspace of at least kda_backward_workspace_bytes.
+ * Steps on 'stream': the forward's preparation, local state pass and
+ * composition (S_in, the segment transitions A and the final-state
+ * transitions of continuing pieces); every piece from its true incoming
+ * state, recording each chunk's start state; the incoming-state gradient of
+ * every continuing piece through its own outputs; the following summaries,
+ * last segment first, giving each segment's end-state gradient; every piece
+ * backwards from it, recording each chunk's end-state gradient and giving
+ * dh0; and every (chunk, head) in parallel for dq, dk, dv, dg and dbeta.
+ * Computed in FP32 on the CUDA cores.  Returns KDA_OK, KDA_ERR_INVALID_ARG,
+ * KDA_ERR_WORKSPACE or KDA_ERR_CUDA.
+ */
+int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                           const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                           const float *g, const float *beta, const float *h0, float scale,
+                           const kda_bf16 *dout, const float *dfinal,
+                           float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* Device workspace bytes kda_backward_segmented needs (0 if the plan or H is
+ * invalid): the forward's (kda_workspace_bytes), then scratch for the
+ * forward's outputs, the chunk start states and end-state gradients
+ * (2 * H * n_chunks * K * V * 4 bytes), the segment gradients
+ * (2 * S * H * K * V * 4 bytes) and the kernels' working areas. */
+size_t kda_backward_workspace_bytes(const int32_t *plan, int32_t H);
+
+/*
  * kda_forward_segmented_noalloc -- kda_forward_segmented without a caller
  * workspace.  The pages have no counterpart to this entry point.
  *

@@ -192,3 +192,46 @@ def gpu_scan_both(inp, seg_bounds=None):
     torch.cuda.synchronize()
     return {"S_in_chain": S1.cpu().numpy(), "S_in_blocked": S2.cpu().numpy(), "A": A.cpu().numpy(),
             "B": B.cpu().numpy(), "bounds": plan_bounds(plan, S)}
+
+
+def gpu_backward(inp, do_bits, dfinal, scale=1.0, want_dh0=True):
+    """kda_backward_segmented through the C ABI; returns numpy dq, dk, dv, dg, dbeta, dh0 (fp32)."""
+    import torch
+    from context_kda_gb300 import binding as kda
+    dev = to_device(inp)
+    T, H, N = inp.tokens, inp.heads, inp.num_seqs
+    plan = kda.kda_plan_segments(inp.cu_seqlens, inp.segments)
+    plan_dev = kda.upload_plan(plan)
+    ws = torch.empty(kda.kda_backward_workspace_bytes(plan, H), dtype=torch.uint8, device="cuda")
+    dout = torch.from_numpy(np.ascontiguousarray(do_bits)).view(torch.bfloat16).to("cuda")
+    df = None if dfinal is None else torch.from_numpy(np.ascontiguousarray(dfinal)).to("cuda")
+    nan = float("nan")
+    out = {"dq": torch.full((T, H, K), nan, device="cuda"), "dk": torch.full((T, H, K), nan, device="cuda"),
+           "dv": torch.full((T, H, V), nan, device="cuda"), "dg": torch.full((T, H, K), nan, device="cuda"),
+           "dbeta": torch.full((T, H), nan, device="cuda"),
+           "dh0": torch.full((N, H, K, V), nan, device="cuda") if want_dh0 else None}
+    kda.kda_backward_segmented(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"],
+                               scale, dout, df, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"],
+                               out["dh0"], ws)
+    torch.cuda.synchronize()
+    return {k_: (None if t is None else t.cpu().numpy()) for k_, t in out.items()}
+
+
+def oracle_backward(inp, do_bits, dfinal, scale=1.0, heads=None):
+    """The fp64 backward of the monolithic recurrence (oracle/backward.py) on the same values."""
+    from oracle import backward as bw
+    q, k, v, g, b = f32_inputs(inp)
+    return bw.backward(inp.cu_seqlens, q, k, v, g, b, bf16_to_f32(do_bits), dfinal=dfinal, h0=inp.h0,
+                       scale=scale, heads=heads)
+
+
+def grad_rel_err(x, y, axis_heads=1):
+    """Largest per-head relative Frobenius error of a gradient tensor (heads on axis 1)."""
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    worst = 0.0
+    for h in range(y.shape[axis_heads]):
+        xs, ys = np.take(x, h, axis=axis_heads), np.take(y, h, axis=axis_heads)
+        den = max(float(np.linalg.norm(ys)), 1e-30)
+        worst = max(worst, float(np.linalg.norm(xs - ys)) / den)
+    return worst

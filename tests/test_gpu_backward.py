@@ -1,0 +1,83 @@
+"""GPU parity of the segmented backward (kda_backward_segmented) against the fp64 oracle.
+
+The oracle is oracle/backward.py's chain rule through the token recurrence, the definition; it is
+pinned by finite differences in tests/test_oracle_backward.py.  The loss is
+L = sum_t <do_t, o_t> + sum_seq <dfinal, S_end> with do bf16 and dfinal fp32 drawn by
+context_kda_gb300.inputs.draw_output_grads.
+
+Tolerance.  The backward computes in fp32 from the exact values of the bf16/fp32 inputs, apart
+from the segments' incoming states, which come from the forward's tensor-core composition and
+carry up to the forward's state bar (relative 1e-4 per matrix).  Every gradient depends linearly
+on those states through the chunk products, so its error is that 1e-4 plus fp32 rounding of
+128-long dot products (about 1e-5).  The bar is ten times the state bar: per head and gradient
+tensor (dq, dk, dv, dg, dbeta, and dh0 per sequence and head),
+    ||x - y||_F <= 1e-3 ||y||_F.
+dg is the reverse cumulative sum of kt dkt - kh dkh + qt dqt, terms that cancel exactly where the
+decay meets a zero state (one token from h0 = 0 has dg = 0), so its error is measured against the
+size of those terms instead when that is larger: ||dg_x - dg_y||_F <= 1e-3 max(||dg_y||_F,
+||k dk_y||_F + ||q dq_y||_F) per head.
+"""
+import numpy as np
+import pytest
+
+from context_kda_gb300.inputs import draw_output_grads, make_inputs, make_workload, workloads
+from context_kda_gb300.inputs import bf16_to_f32
+from harness import gpu_backward, grad_rel_err, oracle_backward
+
+pytestmark = pytest.mark.gpu
+
+GRAD_TOL = 1e-3
+
+
+def _check(inp, scale=1.0, with_dfinal=True, seed=5):
+    do, dfinal = draw_output_grads(inp, seed=seed, with_dfinal=with_dfinal)
+    got = gpu_backward(inp, do, dfinal, scale=scale)
+    ref = oracle_backward(inp, do, dfinal, scale=scale)
+    errs = {}
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.all(np.isfinite(got[name])), name
+        errs[name] = grad_rel_err(got[name], ref[name])
+    k, q = bf16_to_f32(inp.k).astype(np.float64), bf16_to_f32(inp.q).astype(np.float64)
+    errs["dg"] = 0.0
+    for h in range(inp.heads):
+        terms = np.linalg.norm(k[:, h] * ref["dk"][:, h]) + np.linalg.norm(q[:, h] * ref["dq"][:, h])
+        den = max(float(np.linalg.norm(ref["dg"][:, h])), float(terms), 1e-30)
+        errs["dg"] = max(errs["dg"], float(np.linalg.norm(got["dg"][:, h] - ref["dg"][:, h])) / den)
+    errs["dh0"] = max(grad_rel_err(got["dh0"][s:s + 1], ref["dh0"][s:s + 1]) for s in range(inp.num_seqs))
+    for name, e in errs.items():
+        assert e <= GRAD_TOL, f"{name}: rel {e:.3e} ({errs})"
+    return errs
+
+
+def test_backward_t1024_h4_s2_all_heads():
+    _check(make_workload(workloads()["t1024_h4_s2"]))
+
+
+def test_backward_t4096_h8_s4_with_h0():
+    _check(make_workload(workloads()["t4096_h8_s4"]))
+
+
+@pytest.mark.parametrize("seqlens,S,h0_std,scale,with_dfinal", [
+    ([1], 1, 0.0, 1.0, True),                        # one token
+    ([63, 1, 65, 130], 3, 0.1, 1.0, True),          # ragged tails, a one-token sequence
+    ([200, 201, 50, 9, 300], 5, 0.3, 0.5, True),    # resets inside segments, pieces ending mid-segment
+    ([700], 11, 0.0, 1.0, False),                    # non-64-aligned cuts, no final-state gradient
+    ([5, 5, 5, 5], 20, 0.1, 1.0, True),              # one-token segments crossing sequence starts
+    ([300, 500, 77], 1, 0.2, 1.0, True),             # one segment: no following summaries at all
+])
+def test_backward_edge_cases(seqlens, S, h0_std, scale, with_dfinal):
+    inp = make_inputs(seqlens, heads=2, segments=S, h0_std=h0_std, seed=51, g_lo=-0.2)
+    _check(inp, scale=scale, with_dfinal=with_dfinal)
+
+
+def test_backward_segmentation_does_not_change_the_gradients():
+    """The following summaries carry exactly what a single segment computes in one piece: the
+    gradients with 1 and with 7 segments agree within the bar."""
+    one = make_inputs([900, 300], heads=2, segments=1, h0_std=0.1, seed=52)
+    seven = make_inputs([900, 300], heads=2, segments=7, h0_std=0.1, seed=52)
+    do, dfinal = draw_output_grads(one, seed=6)
+    a = gpu_backward(one, do, dfinal)
+    b = gpu_backward(seven, do, dfinal)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert grad_rel_err(b[name], a[name]) <= GRAD_TOL, name
+    assert grad_rel_err(b["dh0"], a["dh0"]) <= GRAD_TOL
