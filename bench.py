@@ -493,6 +493,7 @@ def run_ours(args, w, rank, world, local_rank):
         "wall_s_timed_region": wall,
     }
     if world == 1 and not two_pass and not args.no_extra:
+        line["backward"] = time_backward(prob, stream, flush)
         line["workloads"] = extra_workloads(args, dev, stream, flush, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
@@ -533,6 +534,43 @@ def time_scans(prob, stream, flush, steps=10, warmup=3):
         out[name] = float(np.mean(ms))
     del scan_ws
     return out
+
+
+def time_backward(prob, stream, flush, steps=5, warmup=2):
+    """kda_backward_segmented on the problem (seeded output gradients, inputs resident in HBM): mean
+    CUDA-event ms and tokens/s.  It includes the forward's local pass and composition it runs first."""
+    import torch
+    from context_kda_gb300.inputs import draw_output_grads
+    kda, dev = prob.kda, prob.o.device
+    do_bits, dfinal = draw_output_grads(prob.inp, seed=1)
+    dout = torch.from_numpy(np.ascontiguousarray(do_bits)).view(torch.bfloat16).to(dev)
+    df = torch.from_numpy(dfinal).to(dev)
+    T, H, N = prob.T, prob.H, prob.N
+    grads = [torch.empty((T, H, K_DIM), device=dev), torch.empty((T, H, K_DIM), device=dev),
+             torch.empty((T, H, V_DIM), device=dev), torch.empty((T, H, K_DIM), device=dev),
+             torch.empty((T, H), device=dev), torch.empty((N, H, K_DIM, V_DIM), device=dev)]
+    ws = torch.empty(kda.kda_backward_workspace_bytes(prob.plan, H), dtype=torch.uint8, device=dev)
+    d = prob.d
+
+    def run():
+        kda.kda_backward_segmented(prob.plan, prob.plan_dev, H, d["q"], d["k"], d["v"], d["g"], d["beta"], prob.h0,
+                                   1.0, dout, df, *grads, ws, stream)
+    for _ in range(warmup):
+        flush.fill_(1)
+        run()
+    ms = []
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    m = float(np.mean(ms))
+    del ws, grads
+    return {"ms_per_step": m, "tokens_per_s": T / (m / 1e3), "steps": steps, "warmup": warmup,
+            "note": "FP32 on the CUDA cores; includes the forward's local pass and composition"}
 
 
 def scan_bytes(S, H):
