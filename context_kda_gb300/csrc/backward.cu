@@ -27,9 +27,9 @@
 //     giving dh0 at a sequence start;
 //  5. every (chunk, head) in parallel: dq, dk, dv, dg, dbeta from (X_c, G_c, dO).
 //
-// This first implementation computes in FP32 on the CUDA cores: each CTA runs its chunk's products
-// through a small tiled matrix routine on a private scratch area in global memory (L2-resident),
-// which keeps every step a literal transcription of the formulas above.
+// This implementation computes in FP32 on the CUDA cores: each CTA keeps its chunk's matrices in a
+// private scratch area in global memory (L2-resident) and runs every product by staging both
+// operands in shared memory, which keeps every step a literal transcription of the formulas above.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -64,55 +64,74 @@ struct Mat {
 __device__ __forceinline__ Mat mat(const float *p, int ld) { return Mat{p, ld, false}; }
 __device__ __forceinline__ Mat tr(const float *p, int ld) { return Mat{p, ld, true}; }
 
-// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), for an M x N result and K-long sums,
-// by all threads of the CTA through 64 x 64 output tiles and 16-deep shared-memory slabs.
+// Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
+constexpr int SM_PAD = 4;
+constexpr int SM_LD = 128 + SM_PAD;
+constexpr size_t BWD_SMEM = 2ull * 128 * SM_LD * sizeof(float);
+
+// Micro-tile product over operands already in shared memory: As[k][m] (M x K), Bs[k][n] (K x N);
+// thread (ty, tx) of a 16 x 16 grid computes rows ty*MR .. +MR and columns tx*NR .. +NR.
+template <int MR, int NR>
+__device__ __forceinline__ void gemm_core(int K, const float *As, const float *Bs, float *C, int ldc, float alpha,
+                                          bool acc)
+{
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    float c[MR][NR];
+#pragma unroll
+    for (int i = 0; i < MR; ++i)
+#pragma unroll
+        for (int j = 0; j < NR; ++j) c[i][j] = 0.f;
+    for (int k = 0; k < K; ++k) {
+        float a[MR], b[NR];
+#pragma unroll
+        for (int i = 0; i < MR; i += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(As + k * SM_LD + ty * MR + i);
+            a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < NR; j += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(Bs + k * SM_LD + tx * NR + j);
+            b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < MR; ++i)
+#pragma unroll
+            for (int j = 0; j < NR; ++j) c[i][j] = fmaf(a[i], b[j], c[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < MR; ++i)
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+            float *d = C + (ty * MR + i) * ldc + tx * NR + j;
+            *d = alpha * c[i][j] + (acc ? *d : 0.f);
+        }
+}
+
+// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), for an M x N result (M, N in {64, 128})
+// and K-long sums (K <= 128), by all threads of the CTA: both operands are staged in shared memory
+// (k-major) in one pass, then every thread accumulates its micro-tile over the whole K.
 __device__ void gemm(int M, int N, int K, Mat A, Mat B, float *C, int ldc, float alpha, bool acc)
 {
-    __shared__ float As[16][68], Bs[16][68];
-    const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
+    extern __shared__ __align__(16) float bsm[];
+    float *As = bsm, *Bs = bsm + 128 * SM_LD;
+    const int tid = threadIdx.x;
     __syncthreads();
-    for (int m0 = 0; m0 < M; m0 += 64)
-        for (int n0 = 0; n0 < N; n0 += 64) {
-            float c[4][4] = {};
-            for (int k0 = 0; k0 < K; k0 += 16) {
-                for (int e = tid; e < 16 * 64; e += BT) {
-                    // the index that runs along contiguous memory is the fast one
-                    int kk, mm;
-                    if (A.t) { kk = e >> 6; mm = e & 63; } else { kk = e & 15; mm = e >> 4; }
-                    const int r = m0 + mm, x = k0 + kk;
-                    As[kk][mm] = (r < M && x < K) ? (A.t ? A.p[x * A.ld + r] : A.p[r * A.ld + x]) : 0.f;
-                    int kb, nb;
-                    if (B.t) { kb = e & 15; nb = e >> 4; } else { kb = e >> 6; nb = e & 63; }
-                    const int y = k0 + kb, cc = n0 + nb;
-                    Bs[kb][nb] = (y < K && cc < N) ? (B.t ? B.p[cc * B.ld + y] : B.p[y * B.ld + cc]) : 0.f;
-                }
-                __syncthreads();
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    float a[4], b[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        a[i] = As[kk][tm * 4 + i];
-                        b[i] = Bs[kk][tn * 4 + i];
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) c[i][j] = fmaf(a[i], b[j], c[i][j]);
-                }
-                __syncthreads();
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = m0 + tm * 4 + i, cc = n0 + tn * 4 + j;
-                    if (r < M && cc < N) {
-                        float *d = C + r * ldc + cc;
-                        *d = alpha * c[i][j] + (acc ? *d : 0.f);
-                    }
-                }
-        }
+    // the index that runs along contiguous memory is the fast one
+    if (A.t) {
+        for (int e = tid; e < K * M; e += BT) { const int k = e / M, m = e % M; As[k * SM_LD + m] = A.p[k * A.ld + m]; }
+    } else {
+        for (int e = tid; e < K * M; e += BT) { const int m = e / K, k = e % K; As[k * SM_LD + m] = A.p[m * A.ld + k]; }
+    }
+    if (B.t) {
+        for (int e = tid; e < K * N; e += BT) { const int n = e / K, k = e % K; Bs[k * SM_LD + n] = B.p[n * B.ld + k]; }
+    } else {
+        for (int e = tid; e < K * N; e += BT) { const int k = e / N, n = e % N; Bs[k * SM_LD + n] = B.p[k * B.ld + n]; }
+    }
+    __syncthreads();
+    if (M == 128 && N == 128) gemm_core<8, 8>(K, As, Bs, C, ldc, alpha, acc);
+    else if (M == 128) gemm_core<8, 4>(K, As, Bs, C, ldc, alpha, acc);
+    else if (N == 128) gemm_core<4, 8>(K, As, Bs, C, ldc, alpha, acc);
+    else gemm_core<4, 4>(K, As, Bs, C, ldc, alpha, acc);
     __syncthreads();
 }
 
@@ -170,18 +189,27 @@ __device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16
     }
     __syncthreads();
     // T = (I + M)^-1 by forward substitution, one column per thread: T[j][j] = 1,
-    // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]
-    if (tid < 64) {
-        const int j = tid;
-        float *T = sc + S_T;
-        const float *M = sc + S_M;
-        for (int r = 0; r < 64; ++r) {
-            float s = 0.f;
-            for (int i = j; i < r; ++i) s = fmaf(M[r * 64 + i], T[i * 64 + j], s);
-            T[r * 64 + j] = r < j ? 0.f : (r == j ? 1.f : -s);
+    // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]; M in shared memory (read by every thread alike),
+    // the column in registers
+    {
+        extern __shared__ __align__(16) float bsm[];
+        for (int e = tid; e < CC; e += BT) bsm[e] = sc[S_M + e];
+        __syncthreads();
+        if (tid < 64) {
+            const int j = tid;
+            float t[64];
+#pragma unroll
+            for (int r = 0; r < 64; ++r) {
+                float s = 0.f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) s = fmaf(bsm[r * 64 + i], t[i], s);
+                t[r] = r < j ? 0.f : (r == j ? 1.f : -s);
+            }
+#pragma unroll
+            for (int r = 0; r < 64; ++r) sc[S_T + r * 64 + j] = t[r];
         }
+        __syncthreads();
     }
-    __syncthreads();
     gemm(64, KD, 64, mat(sc + S_T, 64), mat(sc + S_BKT, KD), sc + S_W, KD, 1.f, false);
     gemm(64, VD, 64, mat(sc + S_T, 64), mat(sc + S_BV, VD), sc + S_UT, VD, 1.f, false);
 }
@@ -510,20 +538,26 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
 {
     const PlanView pv{plan_host};
     const PlanSig sig = plan_sig(plan_host);
-    bwd_states<<<grid, BT, 0, stream>>>(plan_dev, sig, H, q, k, v, g, beta, h0, S_in, scale, xs, scratch);
+    for (auto fn : {reinterpret_cast<const void *>(bwd_states), reinterpret_cast<const void *>(bwd_reverse<false>),
+                    reinterpret_cast<const void *>(bwd_reverse<true>), reinterpret_cast<const void *>(bwd_grads)}) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(BWD_SMEM));
+        if (e != cudaSuccess) return e;
+    }
+    bwd_states<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, h0, S_in, scale, xs, scratch);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (pv.n_cont() > 0) {
-        bwd_reverse<false><<<grid, BT, 0, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, dfinal, G_end,
+        bwd_reverse<false><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, dfinal, G_end,
                                                     Qd, gs, dh0, scratch);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     bwd_compose<<<H * 4, BT, 0, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    bwd_reverse<true><<<grid, BT, 0, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, dfinal, G_end, Qd,
+    bwd_reverse<true><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, dfinal, G_end, Qd,
                                                gs, dh0, scratch);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    bwd_grads<<<grid, BT, 0, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, dq, dk, dv, dg,
+    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, dq, dk, dv, dg,
                                        dbeta, scratch);
     return cudaGetLastError();
 }

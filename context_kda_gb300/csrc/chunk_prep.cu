@@ -17,7 +17,8 @@
 // tiles and solve the inverse on the CUDA cores; lane 0 of a ninth warp issues the tcgen05 MMAs
 // (M = 128, bf16 operands in shared memory, FP32 accumulators in TMEM) and lane 0 of a tenth the
 // TMA loads that stage the next unit's rows.  The products that feed the state (Kt Kh^T, W) use a three-term
-// bf16 split (hi*hi + hi*lo + lo*hi, ~2^-17 relative); Ut two terms (V is exact in bf16).
+// bf16 split (hi*hi + hi*lo + lo*hi, ~2^-17 relative); Ut two terms (V is exact in bf16); Qt Kh^T, an
+// output product, two (Qt's low part is zero).
 // Results go straight from registers to the unit's package in the workspace with 16-byte
 // stores, each tile already in the layout the state pass's MMAs read.  A unit's W and Ut products
 // run while the workers start the next unit; the workers read W back from TMEM and store it while
@@ -210,6 +211,14 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
         stage_unit(t0, L, pos_begin.h, b);
     }
 
+    // the bf16 low part of the Qt rows (64 .. 127) of the stacked [Kt; Qt] operand: zero for good
+    if (worker) {
+        for (int e = tid; e < 16 * 64; e += NWORK) {   // 16 column chunks x 64 rows x 16 bytes
+            const int ch = e >> 6, r = 64 + (e & 63);
+            *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + cm_off(r, ch * 8, 2048)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
     bool aborted = false;   // all workers agree on it (OR-reduced at barriers)
     bool bad = false;       // a bounded wait of this thread gave up
     uint32_t phase = 0;
@@ -351,9 +360,11 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                     split8(kt, hi, lo);
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + o_r) = hi;
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_r) = lo;
-                    split8(qt, hi, lo);
+                    // Qt only feeds the masked scores QK, single-term like every output product: its
+                    // bf16 low part stays zero (cleared once at the start), one conversion per pair
+                    hi = make_uint4(bf16x2_bits(qt[0], qt[1]), bf16x2_bits(qt[2], qt[3]), bf16x2_bits(qt[4], qt[5]),
+                                    bf16x2_bits(qt[6], qt[7]));
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + o_q) = hi;
-                    *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_q) = lo;
                     *reinterpret_cast<uint4 *>(pk + PK_Q + o_64) = hi;
                     split8(kh, hi, lo);
                     *reinterpret_cast<uint4 *>(base + OFF_KH + o_64) = hi;
