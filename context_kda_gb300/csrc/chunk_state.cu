@@ -60,7 +60,10 @@ constexpr int NWORK = 256;             // worker threads
 constexpr int NTHREADS = NWORK + 64;   // plus the issuer and producer warps
 constexpr int ISSUER = NWORK;
 constexpr int PRODUCER = NWORK + 32;
-enum { HO_X = 0, HO_U = 1 };           // worker -> issuer handoffs of a chunk
+// worker -> issuer handoffs of a chunk, each in two halves so that a product can start on the first:
+// the state split (XA: k in [0, 32) and [64, 96); XB: the rest) and U (UA: r in [0, 16) and [32, 48);
+// UB: the rest)
+enum { HO_XA = 0, HO_XB = 1, HO_UA = 2, HO_UB = 3 };
 
 __device__ int g_state_status;   // set to KDA_ERR_TIMEOUT when a bounded wait expires
 
@@ -96,7 +99,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
     __shared__ __align__(8) uint64_t s_mbar_o;    // the output products of a chunk
     __shared__ __align__(8) uint64_t s_pbar1[2];  // package part 1 landed, per buffer
     __shared__ __align__(8) uint64_t s_pbar2[2];  // package part 2 landed, per buffer
-    __shared__ __align__(8) uint64_t s_hbar[2];   // worker -> issuer handoffs
+    __shared__ __align__(8) uint64_t s_hbar[4];   // worker -> issuer handoffs
     __shared__ __align__(8) uint64_t s_free[2];   // issuer -> producer: package buffer free
     __shared__ uint32_t s_tmem;
     if (!plan_matches(plan, sig)) {   // not the plan the launch was sized from: touch nothing
@@ -140,9 +143,9 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_pbar1[i]), 1);
             mbar_init(smem_u32(&s_pbar2[i]), 1);
-            mbar_init(smem_u32(&s_hbar[i]), 1);
             mbar_init(smem_u32(&s_free[i]), 1);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&s_hbar[i]), 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
     fence_before();
@@ -223,34 +226,45 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
             tmem_wait_st();
             grid_dep_wait();   // the packages come from the preparation kernel; every output write follows
             load_ut(0);
-            aborted = handoff(HO_X);   // -> W X, Qt X
+            aborted = handoff(HO_XA);  // -> W X, Qt X
+            if (!aborted) aborted = handoff(HO_XB);
         }
         for (int ci = 0; ci < nch && !aborted; ++ci) {
             const int t0 = start + ci * CH;
             const int L = min(CH, len - ci * CH);
 
             // ================= U^T = Ut^T - (W X)^T, split into the A operand of the next products ===
+            // in two rounds of 16 rows r each (hw*32 + [0, 16), then + [16, 32)): the state product
+            // starts on the first
             wait_mma();
-            {
-                float d[32];
-                tmem_ld32(tl + TM_WX + hw * 32, d);   // (W X)^T[c = c_lane][r = hw*32 + j]
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float4 u4 = kind == 0 ? ut[m] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int rd = 0; rd < 2; ++rd) {
+                if (aborted) continue;   // (no break: the loop must unroll, ut is indexed by rd)
+                float d[16];
+                tmem_ld16(tl + TM_WX + hw * 32 + rd * 16, d);   // (W X)^T[c = c_lane][r = hw*32 + rd*16 + j]
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float4 u4 = kind == 0 ? ut[rd * 4 + m] : make_float4(0.f, 0.f, 0.f, 0.f);
                     d[4 * m] = u4.x - d[4 * m];
                     d[4 * m + 1] = u4.y - d[4 * m + 1];
                     d[4 * m + 2] = u4.z - d[4 * m + 2];
                     d[4 * m + 3] = u4.w - d[4 * m + 3];
                 }
-                tmem_st_split32(tl + TM_UH + hw * 16, tl + TM_UL + hw * 16, d);
+                uint32_t uh[8], ul[8];
+#pragma unroll
+                for (int p2 = 0; p2 < 8; ++p2) split_bf16x2(d[2 * p2], d[2 * p2 + 1], uh[p2], ul[p2]);
+                tmem_st8_nowait(tl + TM_UH + hw * 16 + rd * 8, uh);
+                tmem_st8_nowait(tl + TM_UL + hw * 16 + rd * 8, ul);
                 tmem_wait_st();
-                if (tid == 0) bulk_wait_read_all();   // the previous O tile has left shared memory
-                aborted = handoff(HO_U);   // -> O^T += U^T QK^T, X^T += U^T Kh
+                if (rd == 0 && tid == 0) bulk_wait_read_all();   // the previous O tile has left shared memory
+                aborted = handoff(rd == 0 ? HO_UA : HO_UB);   // -> X^T += U^T Kh (then O^T += U^T QK^T)
             }
             if (aborted) break;
             load_ut(ci + 1);
 
             // ================= new X^T and its split into TMEM; outputs (or qhat) to HBM ==============
+            // in two rounds of 32 columns k each (hw*64 + [0, 32), then + [32, 64)): the next chunk's
+            // W X starts on the first
             wait_mma();
             {
                 // this thread's half of X^T (X + Kh^T U) in one batch of TMEM reads
@@ -269,9 +283,10 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                     for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(half ? xb[j] : xa[j]) * gc[k0 + j];
                     tmem_st32_nowait(tl + TM_X + k0, reinterpret_cast<const uint32_t (&)[32]>(x));
                     tmem_st_split32(tl + TM_XH + k0 / 2, tl + TM_XL + k0 / 2, x);
+                    tmem_wait_st();
+                    aborted = handoff(half == 0 ? HO_XA : HO_XB);   // -> next chunk's W X, Qt X
+                    if (aborted) break;
                 }
-                tmem_wait_st();
-                aborted = handoff(HO_X);   // -> next chunk's W X, Qt X (they overlap the stores below)
                 if (aborted) break;
                 if constexpr (MODE != STATE_SUMMARY) {
                     // O^T[c][r] -> bf16 tile of rows r in the TMA store layout (128-byte swizzle; the
@@ -333,20 +348,32 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
         for (int ci = 0; ci < nch && ok; ++ci) {
             const uint32_t par = ci & 1;
             const uint32_t t_o = tbase + ((ci & 1) ? TM_O1 : TM_O0);
-            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_X]), par))) break;
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_XA]), par))) break;
             if (ci + 1 < nch) mbar_arrive(smem_u32(&s_free[(ci + 1) & 1]));
             fence_after();
             {
                 const uint32_t p1 = sbase + OFF_P1 + (ci & 1) * P1_BYTES;
-                // (W X)^T = X^T W^T (3-term; X^T from TMEM, W read MN-major)
+                // (W X)^T = X^T W^T (3-term; X^T from TMEM, W read MN-major): the K steps of the first
+                // half of the state split (k in [0, 32) and [64, 96)), then, once it is in, the rest
                 const uint32_t idw = idesc_bf16(128, 64, 0, 1);
                 const uint32_t aoff[3] = {TM_XH, TM_XH, TM_XL}, boff[3] = {0, T64, 0};
 #pragma unroll
-                for (int ps = 0; ps < 3; ++ps)
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (hf == 1) {
+                        if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_XB]), par))) break;
+                        fence_after();
+                    }
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ta(tbase + TM_WX, tbase + aoff[ps] + kk * 8,
-                                    sdesc(p1 + PK_W + boff[ps] + kk * 256, 128, 2048), idw, (ps | kk) != 0);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int kk = (q4 & 1) + 2 * hf + 4 * (q4 >> 1);   // hf 0: 0, 1, 4, 5; hf 1: 2, 3, 6, 7
+#pragma unroll
+                        for (int ps = 0; ps < 3; ++ps)
+                            mma_bf16_ta(tbase + TM_WX, tbase + aoff[ps] + kk * 8,
+                                        sdesc(p1 + PK_W + boff[ps] + kk * 256, 128, 2048), idw,
+                                        (hf | q4 | ps) != 0);
+                    }
+                }
+                if (!ok) break;
                 commit(mbar);
                 if constexpr (MODE != STATE_SUMMARY) {   // O^T = X^T Qt^T (1-term)
                     const uint32_t id = idesc_bf16(128, 64);
@@ -356,20 +383,31 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                 }
             }
             if (!(ok = mbar_wait(smem_u32(&s_pbar2[ci & 1]), (ci >> 1) & 1))) break;
-            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_U]), par))) break;
+            if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_UA]), par))) break;
             fence_after();
             {
                 const unsigned char *p2 = base + OFF_P2 + (ci & 1) * P2_BYTES;
                 const uint32_t s2 = smem_u32(p2);
                 const uint32_t id64 = idesc_bf16(128, 64), id128 = idesc_bf16(128, 128, 0, 1);
-                // X^T += U^T Kh (3-term; U^T from TMEM, Kh read MN-major): the next chunk waits on it
+                // X^T += U^T Kh (3-term; U^T from TMEM, Kh read MN-major): the next chunk waits on it.  The
+                // K steps of U's first half (r in [0, 16) and [32, 48)), then, once it is in, the rest
                 const uint32_t aoff[3] = {TM_UH, TM_UH, TM_UL}, boff[3] = {0, T64, 0};
 #pragma unroll
-                for (int ps = 0; ps < 3; ++ps)
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (hf == 1) {
+                        if (!(ok = mbar_wait(smem_u32(&s_hbar[HO_UB]), par))) break;
+                        fence_after();
+                    }
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ta(tbase + TM_X, tbase + aoff[ps] + kk * 8,
-                                    sdesc(s2 + P2_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const int kk = hf + 2 * q2;   // hf 0: 0, 2; hf 1: 1, 3
+#pragma unroll
+                        for (int ps = 0; ps < 3; ++ps)
+                            mma_bf16_ta(tbase + TM_X, tbase + aoff[ps] + kk * 8,
+                                        sdesc(s2 + P2_KH + boff[ps] + kk * 256, 128, 1024), id128, 1);
+                    }
+                }
+                if (!ok) break;
                 commit(mbar);
                 if constexpr (MODE != STATE_SUMMARY) {   // O^T += U^T QK^T (1-term)
 #pragma unroll
