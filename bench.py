@@ -240,7 +240,7 @@ def kernel_bytes(plan, H, h0_given):
 class Problem:
     """One workload resident on the device: inputs, plan, workspace and outputs."""
 
-    def __init__(self, w, dev, inp=None):
+    def __init__(self, w, dev, inp=None, refined=False):
         import torch
         from context_kda_gb300 import binding as kda
         self.kda = kda
@@ -256,7 +256,12 @@ class Problem:
             self.host["h0"] = to(inp.h0, torch.float32)
         self.d = {k_: v_.to(dev) for k_, v_ in self.host.items()}
         self.h0 = self.d.get("h0")
-        self.plan = kda.kda_plan_segments(inp.cu_seqlens, self.S)
+        if refined:   # the chunk-level split within the segments, sized for this device
+            sms = __import__("torch").cuda.get_device_properties(dev).multi_processor_count
+            self.plan = kda.kda_plan_segments_refined(inp.cu_seqlens, self.S, self.H, sms)
+            self.S = int(self.plan[5])
+        else:
+            self.plan = kda.kda_plan_segments(inp.cu_seqlens, self.S)
         self.plan_dev = kda.upload_plan(self.plan, dev)
         off = kda.kda_workspace_layout(self.plan, self.H)
         self.ws = torch.empty(off[6], dtype=torch.uint8, device=dev)
@@ -495,6 +500,7 @@ def run_ours(args, w, rank, world, local_rank):
     if world == 1 and not two_pass and not args.no_extra:
         line["backward"] = time_backward(prob, stream, flush)
         line["workloads"] = extra_workloads(args, dev, stream, flush, peaks)
+        line["chunk_level_split"] = refined_comparison(args, dev, stream, flush)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
     print(json.dumps(line), flush=True)
@@ -533,6 +539,32 @@ def time_scans(prob, stream, flush, steps=10, warmup=3):
             ms.append(e0.elapsed_time(e1))
         out[name] = float(np.mean(ms))
     del scan_ws
+    return out
+
+
+REFINED_WORKLOADS = ("t1024_h4_s2", "t8192_h16_s4", "t131072_h2_s1")
+
+
+def refined_comparison(args, dev, stream, flush):
+    """The chunk-level split within a segment: each workload's step on its own plan and on the refined
+    plan (kda_plan_segments_refined for this device), per-kernel ms and tokens/s of both."""
+    import torch
+    out = {}
+    for name in REFINED_WORKLOADS:
+        w = workloads()[name]
+        inp = make_workload(w)
+        row = {}
+        for label, refined in (("plan", False), ("refined", True)):
+            prob = Problem(w, dev, inp=inp, refined=refined)
+            per = prob.time_steps(stream, flush, args.extra_steps, 3)
+            kern = per.mean(axis=0)
+            ms = float(per.sum(axis=1).mean())
+            row[label] = {"segments": prob.S, "ms_per_step": ms, "tokens_per_s": prob.T / (ms / 1e3),
+                          "kernels_ms": {n: float(kern[i]) for i, n in enumerate(("chunk_forward", "compose", "boundary"))}}
+            prob.free()
+            del prob
+            torch.cuda.empty_cache()
+        out[name] = row
     return out
 
 

@@ -11,7 +11,7 @@ from __future__ import annotations
 
 import importlib
 
-_BINDING_NAMES = ("kda_status_string", "kda_plan_segments", "kda_plan_check", "kda_workspace_layout",
+_BINDING_NAMES = ("kda_status_string", "kda_plan_segments", "kda_plan_check", "kda_plan_segments_refined", "kda_workspace_layout",
                   "kda_workspace_bytes", "kda_segment_forward", "kda_compose_summaries", "kda_apply_boundary",
                   "kda_forward_segmented", "kda_forward_two_pass", "kda_forward_segmented_noalloc",
                   "kda_device_status", "kda_selftest_wait_expiry", "kda_compose_summaries_blocked",

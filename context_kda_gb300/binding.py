@@ -42,6 +42,7 @@ def _load():
     lib.kda_selftest_wait_expiry.restype = ctypes.c_int
     lib.kda_plan_segments.argtypes = [P, I32, I32, P, I32, P, ctypes.POINTER(SZ)]
     lib.kda_plan_check.argtypes = [P]
+    lib.kda_plan_segments_refined.argtypes = [P, I32, I32, P, I32, I32, I32, P, ctypes.POINTER(SZ)]
     lib.kda_workspace_layout.argtypes = [P, I32, ctypes.POINTER(SZ)]
     lib.kda_workspace_bytes.argtypes = [P, I32]
     lib.kda_workspace_bytes.restype = SZ
@@ -58,7 +59,7 @@ def _load():
                                            P, SZ, P]
     lib.kda_backward_workspace_bytes.argtypes = [P, I32]
     lib.kda_backward_workspace_bytes.restype = SZ
-    for name in ("kda_plan_segments", "kda_plan_check", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
+    for name in ("kda_plan_segments", "kda_plan_check", "kda_plan_segments_refined", "kda_workspace_layout", "kda_segment_forward", "kda_compose_summaries",
                  "kda_compose_summaries_blocked", "kda_apply_boundary", "kda_forward_segmented", "kda_forward_segmented_noalloc", "kda_backward_segmented",
                  "kda_forward_two_pass"):
         getattr(lib, name).restype = ctypes.c_int
@@ -127,6 +128,22 @@ def kda_plan_segments(cu_seqlens, num_segments: int, seg_bounds=None, chunk: int
     _check("kda_plan_segments", _lib.kda_plan_segments(*args, None, ctypes.byref(n)))
     out = np.zeros(n.value, dtype=np.int32)
     _check("kda_plan_segments", _lib.kda_plan_segments(*args, out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n)))
+    return out
+
+
+def kda_plan_segments_refined(cu_seqlens, num_segments: int, heads: int, num_sms: int, seg_bounds=None,
+                              chunk: int = CHUNK) -> np.ndarray:
+    """A plan whose segments refine ``num_segments`` into chunk-aligned sub-segments (see include/kda.h)."""
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    sb = None if seg_bounds is None else np.ascontiguousarray(seg_bounds, dtype=np.int32)
+    sbp = None if sb is None else sb.ctypes.data_as(ctypes.c_void_p)
+    n = ctypes.c_size_t(0)
+    args = (cu.ctypes.data_as(ctypes.c_void_p), cu.shape[0] - 1, int(num_segments), sbp, int(chunk), int(heads),
+            int(num_sms))
+    _check("kda_plan_segments_refined", _lib.kda_plan_segments_refined(*args, None, ctypes.byref(n)))
+    out = np.zeros(n.value, dtype=np.int32)
+    _check("kda_plan_segments_refined",
+           _lib.kda_plan_segments_refined(*args, out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n)))
     return out
 
 

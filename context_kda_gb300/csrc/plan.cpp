@@ -9,6 +9,7 @@
 // yields the pieces (segment x sequence intersections) in (segment, start)
 // order; everything else is derived from the piece list.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <vector>
@@ -221,4 +222,42 @@ extern "C" int kda_plan_check(const int32_t *plan)
                           &len) != KDA_OK)
         return KDA_ERR_INVALID_ARG;
     return std::memcmp(again.data(), plan, sizeof(int32_t) * len) == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+}
+
+// Refined plan for latency-bound problems: every segment cut into m chunk-aligned sub-segments so
+// that the serial chains are about m times shorter while the state pass still fits one wave of
+// chains on the device: m = min(floor(num_sms / (2 heads S)), floor(chunks per segment / 4)), at
+// least 1 (a piece that continues a sequence adds a transition chain to its state chain, hence the
+// 2).  Cuts fall on multiples of 64 tokens from the segment start, the chunk grid of the segment's
+// first piece.  The result is an ordinary plan of S m segments (custom bounds).
+extern "C" int kda_plan_segments_refined(const int32_t *cu, int32_t num_seqs, int32_t num_segments,
+                                         const int32_t *seg_bounds, int32_t chunk, int32_t heads, int32_t num_sms,
+                                         int32_t *plan, size_t *plan_len)
+{
+    if (!plan_len || !cu || num_seqs < 1 || num_segments < 1 || heads < 1 || num_sms < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (chunk != KDA_CHUNK) return KDA_ERR_UNSUPPORTED;
+    // the caller's segmentation, validated by planning it once
+    size_t len0 = 0;
+    int rc = kda_plan_segments(cu, num_seqs, num_segments, seg_bounds, chunk, nullptr, &len0);
+    if (rc != KDA_OK) return rc;
+    const int64_t T = cu[num_seqs];
+    const int32_t S = num_segments;
+    std::vector<int64_t> b(static_cast<size_t>(S) + 1);
+    for (int32_t j = 0; j <= S; ++j) b[j] = seg_bounds ? seg_bounds[j] : (int64_t)j * T / S;
+    int64_t min_chunks = INT64_MAX;
+    for (int32_t j = 0; j < S; ++j) min_chunks = std::min(min_chunks, (b[j + 1] - b[j]) / chunk);
+    const int64_t by_sms = num_sms / (2LL * heads * S);
+    const int64_t m = std::max<int64_t>(1, std::min(by_sms, min_chunks / 4));
+    std::vector<int32_t> nb;
+    nb.push_back(0);
+    for (int32_t j = 0; j < S; ++j) {
+        const int64_t a = b[j], e = b[j + 1], nch = (e - a + chunk - 1) / chunk;
+        for (int64_t i = 1; i < m; ++i) {
+            const int64_t cut = a + (nch * i / m) * chunk;
+            if (cut > nb.back() && cut < e) nb.push_back(static_cast<int32_t>(cut));
+        }
+        nb.push_back(static_cast<int32_t>(e));
+    }
+    return kda_plan_segments(cu, num_seqs, static_cast<int32_t>(nb.size()) - 1, nb.data(), chunk, plan, plan_len);
 }

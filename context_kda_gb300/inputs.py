@@ -104,6 +104,8 @@ def workloads() -> Dict[str, Workload]:
         Workload("t131072_h32_s64", (131072,), 32, 64, note="long context"),
         Workload("t32768_h2_s64", (32768,), 2, 64,
                  note="few heads, many segments: the composition chain leaves most SMs idle"),
+        Workload("t131072_h2_s1", (131072,), 2, 1,
+                 note="few heads, one long segment: two serial chains of 2048 chunks (the chunk-level split)"),
     ]
     return {x.name: x for x in w}
 

@@ -192,6 +192,28 @@ int kda_plan_segments(const int32_t *cu_seqlens, int32_t num_seqs, int32_t num_s
  */
 int kda_plan_check(const int32_t *plan);
 
+/*
+ * kda_plan_segments_refined -- the chunk-level split within a segment: a plan
+ * whose segments refine the caller's, each cut into m sub-segments of whole
+ * 64-token chunks (cuts on multiples of 64 from the segment start), so that
+ * the serial chunk chains are m times shorter.  The same affine summaries
+ * carry the state across the new cuts (PR #110 §Motivation: affine recurrence
+ * state; PR #136 §Summary: summary composition), so kda_forward_segmented on
+ * this plan gives the outputs and final states of the caller's segmentation
+ * (within rounding); its summaries are those of the sub-segments, which
+ * compose within each caller segment to that segment's summary.
+ *   m = max(1, min(floor(num_sms / (2 heads S)), floor(chunks per segment / 4))):
+ *   about one wave of state and transition chains on the device, and at least
+ *   four chunks per sub-segment.  It pays where few heads and long segments
+ *   leave most SMs idle (a single long sequence with a few heads); with
+ *   2 heads S >= num_sms it changes nothing.
+ *   heads, num_sms  the H the plan will run with and the device's SM count.
+ * Other arguments, results and errors as kda_plan_segments.
+ */
+int kda_plan_segments_refined(const int32_t *cu_seqlens, int32_t num_seqs, int32_t num_segments,
+                              const int32_t *seg_bounds, int32_t chunk, int32_t heads, int32_t num_sms,
+                              int32_t *plan, size_t *plan_len);
+
 /* Bytes of one chunk package: the per-chunk operands that the chunk-parallel
  * preparation hands to the serial state pass (see kda_segment_forward). */
 enum { KDA_PACKAGE_BYTES = 123392 };

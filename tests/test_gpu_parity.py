@@ -299,3 +299,47 @@ def test_fused_path_with_the_blocked_scan_every_head_and_segment():
     res = gpu_forward(inp)
     _check_outputs(res, inp)
     _check_all_segments(res, inp)
+
+
+# ---- the chunk-level split within a segment: refined plans give the same results
+
+def _refined(inp, sms=152):
+    from context_kda_gb300 import binding as kda
+    plan = kda.kda_plan_segments_refined(inp.cu_seqlens, inp.segments, inp.heads, sms)
+    S = int(plan[5])
+    return [int(x) for x in plan[int(plan[14]):int(plan[14]) + S + 1]]
+
+
+@pytest.mark.parametrize("seqlens,H,S,h0_std", [
+    ([16384], 2, 1, 0.1),               # one long sequence, two heads: 38 sub-segments
+    ([3000, 5000, 900], 1, 2, 0.2),     # packed, one head, resets inside the refined segments
+])
+def test_refined_plan_matches_the_oracle(seqlens, H, S, h0_std):
+    inp = make_inputs(seqlens, heads=H, segments=S, h0_std=h0_std, seed=61, g_lo=-0.1)
+    bounds = _refined(inp)
+    assert len(bounds) - 1 > S
+    res = gpu_forward(inp, seg_bounds=bounds)
+    _check_outputs(res, inp)
+    _check_all_segments(res, inp)
+
+
+def test_refined_summaries_compose_to_the_callers():
+    """Within each caller segment the sub-segment summaries compose, (A2,B2) o (A1,B1) =
+    (A2 A1, A2 B1 + B2), to that segment's summary from the unrefined plan."""
+    inp = make_inputs([6000], heads=2, segments=2, h0_std=0.1, seed=62, g_lo=-0.05)
+    coarse = gpu_forward(inp)
+    bounds = _refined(inp)
+    fine = gpu_forward(inp, seg_bounds=bounds)
+    assert float(np.max(np.abs(fine["o"] - coarse["o"]))) <= O_TOL
+    assert rel_err(fine["final"], coarse["final"]) <= REL_TOL
+    cb = coarse["bounds"]
+    for j in range(len(cb) - 1):
+        subs = [i for i in range(len(bounds) - 1) if cb[j] <= bounds[i] < cb[j + 1]]
+        for h in range(2):
+            A = np.eye(128)
+            B = np.zeros((128, 128))
+            for i in subs:
+                A2, B2 = fine["A"][i, h].astype(np.float64), fine["B"][i, h].astype(np.float64)
+                A, B = A2 @ A, A2 @ B + B2
+            assert rel_err(A, coarse["A"][j, h]) <= REL_TOL
+            assert rel_err(B, coarse["B"][j, h]) <= REL_TOL

@@ -131,3 +131,34 @@ def test_python_planner_writes_the_same_checksum(kda):
         want = np.array(plan_segments(cu, S), dtype=np.int32)
         assert np.array_equal(got, want)
         assert kda.kda_plan_check(got) == kda.KDA_OK
+
+
+# ---- the chunk-level split within a segment (kda_plan_segments_refined)
+
+@pytest.mark.parametrize("cu,S,H,sms", [([0, 131072], 1, 2, 152), ([0, 8192], 4, 16, 152), ([0, 1024], 2, 4, 152),
+                                         ([0, 300, 5000, 9000], 3, 1, 152), ([0, 4000], 2, 1, 8),
+                                         ([0, 100], 1, 1, 152)])
+def test_refined_plan_refines_on_the_chunk_grid(kda, cu, S, H, sms):
+    base = kda.kda_plan_segments(cu, S)
+    ref = kda.kda_plan_segments_refined(cu, S, H, sms)
+    assert kda.kda_plan_check(ref) == kda.KDA_OK
+    Sb, Sr = int(base[5]), int(ref[5])
+    bb = [int(x) for x in base[int(base[14]):int(base[14]) + Sb + 1]]
+    br = [int(x) for x in ref[int(ref[14]):int(ref[14]) + Sr + 1]]
+    assert set(bb) <= set(br)                                  # a refinement of the caller's segments
+    chunks = min((bb[j + 1] - bb[j]) // 64 for j in range(Sb))
+    m = max(1, min(sms // (2 * H * Sb), chunks // 4))
+    assert Sr <= Sb * m and (m == 1) == (Sr == Sb)
+    for j in range(Sb):                                        # cuts on the 64-token grid of each segment
+        for x in br:
+            if bb[j] < x < bb[j + 1]:
+                assert (x - bb[j]) % 64 == 0
+    # the refined plan is the ordinary plan of its bounds, word for word
+    assert np.array_equal(ref, np.array(plan_segments(cu, Sr, br), dtype=np.int32))
+
+
+def test_refined_plan_rejects_what_the_planner_rejects(kda):
+    with pytest.raises(kda.KDAError):
+        kda.kda_plan_segments_refined([0, 10, 10], 1, 2, 152)        # zero-length sequence
+    with pytest.raises(kda.KDAError):
+        kda.kda_plan_segments_refined([0, 100], 1, 0, 152)           # no heads
