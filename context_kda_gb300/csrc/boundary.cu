@@ -224,13 +224,16 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, int units_per_
         m_pend |= 1u << t;
     };
 
-    grid_dep_wait();   // S_in, qhat and the outputs come from the previous kernels
+    // qhat and the local outputs come from the state pass, which completed before the composition (this
+    // kernel's prerequisite) passed its own wait and let this kernel's CTAs start: the first tiles are
+    // requested while the composition still runs; S_in, the composition's result, only after the wait
     if (tid == 0) {
         if (via_tma(r0)) fetch_q(r0, 0);
         if (n_run > 1 && via_tma(r1)) fetch_q(r1, 1);
         if (n_run > 2 && via_tma(r2)) fetch_q(r2, 2);
         if (tiled(r0)) fetch_o(r0, c0.h, 0);
     }
+    grid_dep_wait();   // S_in comes from the composition
 
     int key_h = -1, key_seg = -1;   // the S_in whose split is in the B operand
     bool issued = false;            // unit n's products were issued during the previous unit
