@@ -40,6 +40,8 @@ def _load():
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_selftest_wait_expiry.argtypes = [P]
     lib.kda_selftest_wait_expiry.restype = ctypes.c_int
+    lib.kda_selftest_state_abort.argtypes = [P, P, I32, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
+    lib.kda_selftest_state_abort.restype = ctypes.c_int
     lib.kda_plan_segments.argtypes = [P, I32, I32, P, I32, P, ctypes.POINTER(SZ)]
     lib.kda_plan_check.argtypes = [P]
     lib.kda_plan_segments_refined.argtypes = [P, I32, I32, P, I32, I32, I32, P, ctypes.POINTER(SZ)]
@@ -83,6 +85,16 @@ def kda_device_status() -> int:
     KDA_ERR_RANGE (a chunk's summed decay out of range) or KDA_ERR_INVALID_ARG (a device plan
     that is not the host plan's copy)."""
     return int(_lib.kda_device_status())
+
+
+def kda_selftest_state_abort(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B, final_state, ws, stream=None):
+    """The state pass with the second chunk's package copies withheld (see include/kda.h): its waits run
+    out, it returns cleanly, and kda_device_status() then reports KDA_ERR_TIMEOUT."""
+    p = _words(plan)
+    _check("kda_selftest_state_abort",
+           _lib.kda_selftest_state_abort(_hp(p), _dp(plan_dev), int(H), _dp(q), _dp(k), _dp(v), _dp(g), _dp(beta),
+                                         _dp(h0), float(scale), _dp(o), _dp(A), _dp(B), _dp(final_state), _dp(ws),
+                                         _nbytes(ws), _stream(stream)))
 
 
 def kda_selftest_wait_expiry(stream=None):

@@ -147,6 +147,26 @@ extern "C" int kda_selftest_wait_expiry(void *stream)
     return cuda_status(kda::launch_wait_expiry_probe(static_cast<cudaStream_t>(stream)));
 }
 
+extern "C" int kda_selftest_state_abort(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                                        const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const float *g,
+                                        const float *beta, const float *h0, float scale, kda_bf16 *o, float *A,
+                                        float *B, float *final_state, void *ws, size_t ws_bytes, void *stream)
+{
+    size_t off[7];
+    if (!layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
+    if (plan[KDA_PH_MAXPIECE] <= KDA_CHUNK) return KDA_ERR_INVALID_ARG;   // needs a piece of two chunks
+    if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
+    if (!o || !A || !B || !final_state || !aligned16(o) || !aligned16(A) || !aligned16(B) ||
+        !aligned16(final_state))
+        return KDA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
+    if (ws_bytes < off[3]) return KDA_ERR_WORKSPACE;
+    const kda::Workspace w = carve(ws, off);
+    return cuda_status(kda::launch_state_abort_selftest(plan, plan_dev, H, q, k, v, g, beta, h0, scale, o, A, B,
+                                                        final_state, w.qhat, w.afin, w.pkg,
+                                                        static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int kda_device_status(void)
 {
     cudaError_t e = cudaDeviceSynchronize();

@@ -92,7 +92,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                const float *__restrict__ s_in, const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o,
                float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
                uint16_t *__restrict__ qhat, float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
-               const __grid_constant__ CUtensorMap tm_q)
+               const __grid_constant__ CUtensorMap tm_q, int withhold)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;      // W X, then the state product
@@ -427,6 +427,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
         int n_p1[2] = {nch > 0 ? 1 : 0, 0}, n_p2[2] = {nch > 0 ? 1 : 0, 0};
         for (int j = 1; j < nch && ok; ++j) {
             if (!(ok = mbar_wait(smem_u32(&s_free[j & 1]), ((j - 1) >> 1) & 1))) break;
+            if (j == withhold) continue;   // the abort-path self-test: this chunk's copies never come
             load_p1(j);
             load_p2(j);
             ++n_p1[j & 1];
@@ -484,7 +485,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
 template <int MODE>
 cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0, const float *s_in,
                          const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
-                         uint16_t *qhat, float *afin, cudaStream_t stream)
+                         uint16_t *qhat, float *afin, cudaStream_t stream, int withhold = -1)
 {
     const PlanView pv{plan_host};
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
@@ -506,7 +507,8 @@ cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int 
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(chunk_state_tc<MODE>, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC,
-                            stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq);
+                            stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq,
+                            withhold);
 }
 
 }  // namespace
@@ -549,6 +551,20 @@ cudaError_t launch_two_pass(const int32_t *plan_host, const int32_t *plan_dev, i
     if (err != cudaSuccess) return err;
     return launch_state<STATE_OUTPUT>(plan_host, plan_dev, H, h0, S_in, pkg, o, A, B, final_state, nullptr, nullptr,
                                       stream);
+}
+
+// Self-test of the state pass's abort path: the preparation, then the state pass with the package copies
+// of every piece's second chunk withheld, so that its waits run out.
+cudaError_t launch_state_abort_selftest(const int32_t *plan_host, const int32_t *plan_dev, int H,
+                                        const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                                        const float *beta, const float *h0, float scale, uint16_t *o, float *A,
+                                        float *B, float *final_state, uint16_t *qhat, float *afin,
+                                        unsigned char *pkg, cudaStream_t stream)
+{
+    cudaError_t err = launch_chunk_prep(plan_host, plan_dev, H, q, k, v, g, beta, scale, pkg, stream);
+    if (err != cudaSuccess) return err;
+    return launch_state<STATE_LOCAL>(plan_host, plan_dev, H, h0, nullptr, pkg, o, A, B, final_state, qhat, afin,
+                                     stream, 1);
 }
 
 // The status word of this file's kernel: read and cleared (the caller has synchronised the device).

@@ -101,6 +101,11 @@ int take_compose_status();
 int take_boundary_status();
 int take_backward_status();
 cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
+cudaError_t launch_state_abort_selftest(const int32_t *plan_host, const int32_t *plan_dev, int H,
+                                        const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                                        const float *beta, const float *h0, float scale, uint16_t *o, float *A,
+                                        float *B, float *final_state, uint16_t *qhat, float *afin,
+                                        unsigned char *pkg, cudaStream_t stream);
 
 // Launches a kernel that may begin while the previous kernel on the stream finishes (programmatic
 // dependent launch): its CTAs can be scheduled once every CTA of that kernel has signalled (or

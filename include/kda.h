@@ -160,6 +160,21 @@ int kda_device_status(void);
  * KDA_OK or KDA_ERR_CUDA (launch failure). */
 int kda_selftest_wait_expiry(void *stream);
 
+/* Self-test of a real kernel's abort path: kda_segment_forward's two kernels
+ * with the package copies of every piece's second chunk withheld inside the
+ * state pass, so that its waits for them (and for the products that need
+ * them) run out after about two seconds; the kernel then lets its issued
+ * copies and products land, frees its tensor memory and returns.  The next
+ * kda_device_status() returns KDA_ERR_TIMEOUT; the results of this call are
+ * invalid and the context stays usable.  Arguments as kda_segment_forward
+ * (the plan must have a piece of more than one chunk).  Returns KDA_OK,
+ * KDA_ERR_INVALID_ARG, KDA_ERR_WORKSPACE or KDA_ERR_CUDA. */
+int kda_selftest_state_abort(const int32_t *plan, const int32_t *plan_dev, int32_t H,
+                             const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                             const float *g, const float *beta, const float *h0, float scale,
+                             kda_bf16 *o, float *A, float *B, float *final_state,
+                             void *ws, size_t ws_bytes, void *stream);
+
 /*
  * kda_plan_segments -- packed-THD segment plan (host, integer work only).
  * PR #136 §Walkthrough: CPU-only plan construction and validation for balanced

@@ -197,3 +197,12 @@ def test_entry_points_reject_bad_arguments_before_any_device_work(kda):
     assert lib.kda_segment_forward(pp, fake, 2, fake, fake, fake, fake, fake, None, ctypes.c_float(1.0), fake,
                                    None, fake, fake, fake, ws_need, None) == kda.KDA_ERR_INVALID_ARG
     assert kda.kda_status_string(kda.KDA_ERR_WORKSPACE) == "buffer too small"
+
+
+def test_state_abort_selftest_refuses_plans_without_a_second_chunk(kda):
+    lib = kda._lib
+    plan = kda.kda_plan_segments([0, 64, 128], 2)       # every piece one chunk long
+    pp = plan.ctypes.data_as(ctypes.c_void_p)
+    fake = ctypes.c_void_p(1 << 20)                     # never dereferenced: validation fails first
+    assert lib.kda_selftest_state_abort(pp, fake, 2, fake, fake, fake, fake, fake, None, ctypes.c_float(1.0), fake,
+                                        fake, fake, fake, fake, 1 << 30, None) == kda.KDA_ERR_INVALID_ARG

@@ -8,7 +8,10 @@
   fp32 (g ~ U(-3, -0.5), about -112 per 64-token chunk): the preparation
   records KDA_ERR_RANGE;
 * a decay just inside that range (g ~ U(-1.15, -1.0), about -69 per chunk)
-  matches the oracle and records nothing.
+  matches the oracle and records nothing;
+* the state pass's own bounded waits running out (its package copies
+  withheld by the abort self-test): KDA_ERR_TIMEOUT, and the context stays
+  usable.
 
 Both error cases compute only finite or NaN/inf values without any
 value-dependent control flow in the kernels, and leave the context usable: a
@@ -67,5 +70,32 @@ def test_decay_just_inside_the_range_matches_the_oracle():
     from context_kda_gb300 import binding as kda
     assert kda.kda_device_status() == kda.KDA_OK
     inp = make_inputs([300, 70, 200], heads=2, segments=4, h0_std=0.1, seed=34, g_lo=-1.15, g_hi=-1.0)
+    _checked_forward(inp)
+    assert kda.kda_device_status() == kda.KDA_OK
+
+
+def test_state_pass_abort_path_reports_and_the_context_survives():
+    """A real kernel's waits run out: the state pass with the package copies of every piece's second
+    chunk withheld waits about two seconds for them, then lets its issued copies and products land,
+    frees its tensor memory and returns; kda_device_status reports KDA_ERR_TIMEOUT once, and a checked
+    forward follows."""
+    import torch
+    from context_kda_gb300 import binding as kda
+    assert kda.kda_device_status() == kda.KDA_OK
+    inp = make_inputs([300, 200], heads=2, segments=3, h0_std=0.1, seed=35)
+    plan = kda.kda_plan_segments(inp.cu_seqlens, inp.segments)
+    plan_dev = kda.upload_plan(plan)
+    dev = to_device(inp)
+    T, H, N, S = inp.tokens, inp.heads, inp.num_seqs, inp.segments
+    off = kda.kda_workspace_layout(plan, H)
+    ws = torch.empty(off[3], dtype=torch.uint8, device="cuda")
+    o = torch.empty((T, H, V), dtype=torch.bfloat16, device="cuda")
+    A = torch.empty((S, H, K, K), dtype=torch.float32, device="cuda")
+    B = torch.empty((S, H, K, V), dtype=torch.float32, device="cuda")
+    fin = torch.empty((N, H, K, V), dtype=torch.float32, device="cuda")
+    kda.kda_selftest_state_abort(plan, plan_dev, H, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["h0"],
+                                 1.0, o, A, B, fin, ws)
+    assert kda.kda_device_status() == kda.KDA_ERR_TIMEOUT
+    assert kda.kda_device_status() == kda.KDA_OK
     _checked_forward(inp)
     assert kda.kda_device_status() == kda.KDA_OK
