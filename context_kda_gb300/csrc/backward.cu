@@ -15,6 +15,7 @@
 //
 // Steps (after the forward's own preparation, state pass and composition, which give S_in, the
 // segment transitions A and the final-state transitions of continuing pieces):
+//  0. every (chunk, head) in parallel: the chunk's terms that the chains need (W, Ut, Kh, Qt, QK, Dc);
 //  1. every piece from its true incoming state (h0, or S_in of its segment), recording each chunk's
 //     start state X_c;
 //  2. every piece that continues a sequence, backwards from a zero end gradient: the gradient of its
@@ -54,6 +55,11 @@ enum : int {
     S_GC = S_T64 + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64, S_DBETA = S_DGC + KD,
     SCRATCH_FLOATS = S_DBETA + 64
 };
+
+// The terms a chain step needs, stored per (head, chunk) by the terms pass (floats): W, Ut, Kh, Qt
+// (64 x 128 each), QK (64 x 64), exp(Gamma_C) (128).
+enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * CK, TM_GC = 4 * CK + CC,
+             TERMS_FLOATS = TM_GC + KD };
 
 // A matrix operand in global scratch: element (r, c) = t ? p[c * ld + r] : p[r * ld + c].
 struct Mat {
@@ -108,7 +114,8 @@ __device__ __forceinline__ void gemm_core(int K, const float *As, const float *B
 }
 
 // C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), for an M x N result (M, N in {64, 128})
-// and K-long sums (K <= 128), by all threads of the CTA: both operands are staged in shared memory
+// and K-long sums (K in {64, 128}), operands 16-byte aligned with leading dimensions a multiple of 4, by
+// all threads of the CTA: both operands are staged in shared memory
 // (k-major) in one pass, then every thread accumulates its micro-tile over the whole K.
 __device__ void gemm(int M, int N, int K, Mat A, Mat B, float *C, int ldc, float alpha, bool acc)
 {
@@ -116,16 +123,40 @@ __device__ void gemm(int M, int N, int K, Mat A, Mat B, float *C, int ldc, float
     float *As = bsm, *Bs = bsm + 128 * SM_LD;
     const int tid = threadIdx.x;
     __syncthreads();
-    // the index that runs along contiguous memory is the fast one
-    if (A.t) {
-        for (int e = tid; e < K * M; e += BT) { const int k = e / M, m = e % M; As[k * SM_LD + m] = A.p[k * A.ld + m]; }
-    } else {
-        for (int e = tid; e < K * M; e += BT) { const int m = e / K, k = e % K; As[k * SM_LD + m] = A.p[m * A.ld + k]; }
+    // 16-byte loads along the contiguous index; M, N, K are powers of two (64 or 128, K >= 64)
+    const int lm = __ffs(M) - 1, ln = __ffs(N) - 1, lk = __ffs(K) - 1;
+    if (A.t) {            // A(m, k) = p[k * ld + m]: rows of m, stored as they come
+        for (int e = tid; e < (K * M) >> 2; e += BT) {
+            const int k = e >> (lm - 2), m4 = (e & ((M >> 2) - 1)) << 2;
+            *reinterpret_cast<float4 *>(As + k * SM_LD + m4) = *reinterpret_cast<const float4 *>(A.p + k * A.ld + m4);
+        }
+    } else {              // A(m, k) = p[m * ld + k]: rows of k, transposed into As; a warp takes 16 rows m
+                          // x 2 vectors, so its scattered stores fall in 32 distinct banks
+        for (int e = tid; e < (K * M) >> 2; e += BT) {
+            const int rest = e >> 4, kv = rest & ((K >> 2) - 1);
+            const int m = ((rest >> (lk - 2)) << 4) | (e & 15), k4 = kv << 2;
+            const float4 v = *reinterpret_cast<const float4 *>(A.p + m * A.ld + k4);
+            As[(k4 + 0) * SM_LD + m] = v.x;
+            As[(k4 + 1) * SM_LD + m] = v.y;
+            As[(k4 + 2) * SM_LD + m] = v.z;
+            As[(k4 + 3) * SM_LD + m] = v.w;
+        }
     }
-    if (B.t) {
-        for (int e = tid; e < K * N; e += BT) { const int n = e / K, k = e % K; Bs[k * SM_LD + n] = B.p[n * B.ld + k]; }
-    } else {
-        for (int e = tid; e < K * N; e += BT) { const int k = e / N, n = e % N; Bs[k * SM_LD + n] = B.p[k * B.ld + n]; }
+    if (B.t) {            // B(k, n) = p[n * ld + k]: rows of k, transposed into Bs (16 rows n x 2 vectors a warp)
+        for (int e = tid; e < (K * N) >> 2; e += BT) {
+            const int rest = e >> 4, kv = rest & ((K >> 2) - 1);
+            const int n = ((rest >> (lk - 2)) << 4) | (e & 15), k4 = kv << 2;
+            const float4 v = *reinterpret_cast<const float4 *>(B.p + n * B.ld + k4);
+            Bs[(k4 + 0) * SM_LD + n] = v.x;
+            Bs[(k4 + 1) * SM_LD + n] = v.y;
+            Bs[(k4 + 2) * SM_LD + n] = v.z;
+            Bs[(k4 + 3) * SM_LD + n] = v.w;
+        }
+    } else {              // B(k, n) = p[k * ld + n]: rows of n, stored as they come
+        for (int e = tid; e < (K * N) >> 2; e += BT) {
+            const int k = e >> (ln - 2), n4 = (e & ((N >> 2) - 1)) << 2;
+            *reinterpret_cast<float4 *>(Bs + k * SM_LD + n4) = *reinterpret_cast<const float4 *>(B.p + k * B.ld + n4);
+        }
     }
     __syncthreads();
     if (M == 128 && N == 128) gemm_core<8, 8>(K, As, Bs, C, ldc, alpha, acc);
@@ -224,29 +255,30 @@ __device__ void load_do(float *sc, int t0, int L, int h, int H, const uint16_t *
     __syncthreads();
 }
 
-// X <- Dc (X + Kh^T (Ut - W X))
-__device__ void forward_step(float *sc)
+// X <- Dc (X + Kh^T (Ut - W X)), the chunk's terms at tm
+__device__ void forward_step(float *sc, const float *tm)
 {
     float *X = sc + S_X, *U = sc + S_U;
-    for (int e = threadIdx.x; e < CK; e += BT) U[e] = sc[S_UT + e];
-    gemm(64, VD, KD, mat(sc + S_W, KD), mat(X, VD), U, VD, -1.f, true);
-    gemm(KD, VD, 64, tr(sc + S_KH, KD), mat(U, VD), X, VD, 1.f, true);
-    for (int e = threadIdx.x; e < SQ; e += BT) X[e] *= sc[S_GC + (e >> 7)];
+    for (int e = threadIdx.x; e < CK; e += BT) U[e] = tm[TM_UT + e];
+    gemm(64, VD, KD, mat(tm + TM_W, KD), mat(X, VD), U, VD, -1.f, true);
+    gemm(KD, VD, 64, tr(tm + TM_KH, KD), mat(U, VD), X, VD, 1.f, true);
+    for (int e = threadIdx.x; e < SQ; e += BT) X[e] *= tm[TM_GC + (e >> 7)];
     __syncthreads();
 }
 
-// G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start)
-__device__ void reverse_step(float *sc)
+// G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start), the chunk's
+// terms at tm
+__device__ void reverse_step(float *sc, const float *tm)
 {
     float *G = sc + S_G, *DG = sc + S_Y, *dU = sc + S_DU;
-    for (int e = threadIdx.x; e < SQ; e += BT) DG[e] = sc[S_GC + (e >> 7)] * G[e];
+    for (int e = threadIdx.x; e < SQ; e += BT) DG[e] = tm[TM_GC + (e >> 7)] * G[e];
     __syncthreads();
-    gemm(64, VD, KD, mat(sc + S_KH, KD), mat(DG, VD), dU, VD, 1.f, false);
-    gemm(64, VD, 64, tr(sc + S_QK, 64), mat(sc + S_DO, VD), dU, VD, 1.f, true);
+    gemm(64, VD, KD, mat(tm + TM_KH, KD), mat(DG, VD), dU, VD, 1.f, false);
+    gemm(64, VD, 64, tr(tm + TM_QK, 64), mat(sc + S_DO, VD), dU, VD, 1.f, true);
     for (int e = threadIdx.x; e < SQ; e += BT) G[e] = DG[e];
     __syncthreads();
-    gemm(KD, VD, 64, tr(sc + S_QT, KD), mat(sc + S_DO, VD), G, VD, 1.f, true);
-    gemm(KD, VD, 64, tr(sc + S_W, KD), mat(dU, VD), G, VD, -1.f, true);
+    gemm(KD, VD, 64, tr(tm + TM_QT, KD), mat(sc + S_DO, VD), G, VD, 1.f, true);
+    gemm(KD, VD, 64, tr(tm + TM_W, KD), mat(dU, VD), G, VD, -1.f, true);
 }
 
 // Plan helpers
@@ -269,11 +301,35 @@ __device__ PieceInfo piece_info(const PlanView &pv, int p)
         return;                                                                           \
     }
 
+// 0. every (chunk, head) in parallel: the terms the chains need, stored at terms[h][c]
+__global__ void __launch_bounds__(BT) bwd_terms(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
+                                                const uint16_t *k, const uint16_t *v, const float *g,
+                                                const float *beta, float scale, float *terms, float *scratch)
+{
+    BWD_PLAN_CHECK();
+    const PlanView pv{plan};
+    float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
+    const int n_chunks = pv.n_chunks();
+    for (int unit = blockIdx.x; unit < n_chunks * H; unit += gridDim.x) {
+        const int h = unit / n_chunks, c = unit % n_chunks;
+        const int32_t *cr = pv.chunk(c);
+        chunk_terms(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
+        float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;
+        for (int e = threadIdx.x; e < CK; e += BT) {
+            tm[TM_W + e] = sc[S_W + e];
+            tm[TM_UT + e] = sc[S_UT + e];
+            tm[TM_KH + e] = sc[S_KH + e];
+            tm[TM_QT + e] = sc[S_QT + e];
+        }
+        for (int e = threadIdx.x; e < CC; e += BT) tm[TM_QK + e] = sc[S_QK + e];
+        for (int e = threadIdx.x; e < KD; e += BT) tm[TM_GC + e] = sc[S_GC + e];
+        __syncthreads();
+    }
+}
+
 // 1. every piece from its true incoming state, recording X_c = xs[h][c] for each of its chunks
-__global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
-                                                 const uint16_t *k, const uint16_t *v, const float *g,
-                                                 const float *beta, const float *h0, const float *S_in, float scale,
-                                                 float *xs, float *scratch)
+__global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig sig, int H, const float *terms,
+                                                 const float *h0, const float *S_in, float *xs, float *scratch)
 {
     BWD_PLAN_CHECK();
     const PlanView pv{plan};
@@ -291,11 +347,10 @@ __global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig si
         for (int e = threadIdx.x; e < SQ; e += BT) sc[S_X + e] = src ? src[e] : 0.f;
         __syncthreads();
         for (int ci = 0; ci < pi.nch; ++ci) {
-            float *dst = xs + (static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci) * SQ;
+            const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
+            float *dst = xs + unit * SQ;
             for (int e = threadIdx.x; e < SQ; e += BT) dst[e] = sc[S_X + e];
-            const int t0 = pi.start + ci * CH, L = min(CH, pi.len - ci * CH);
-            chunk_terms(sc, t0, L, h, H, q, k, v, g, beta, scale);
-            forward_step(sc);
+            forward_step(sc, terms + unit * TERMS_FLOATS);
         }
         __syncthreads();
     }
@@ -306,11 +361,9 @@ __global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig si
 // its true end gradient (dfinal of its sequence when it ends it, else G_end[seg]); records G_c =
 // gs[h][c], the gradient of each chunk's end state, and gives dh0 at a sequence start.
 template <bool TRUE_PASS>
-__global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
-                                                  const uint16_t *k, const uint16_t *v, const float *g,
-                                                  const float *beta, float scale, const uint16_t *dout,
-                                                  const float *dfinal, const float *G_end, float *Qd, float *gs,
-                                                  float *dh0, float *scratch)
+__global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig sig, int H, const float *terms,
+                                                  const uint16_t *dout, const float *dfinal, const float *G_end,
+                                                  float *Qd, float *gs, float *dh0, float *scratch)
 {
     BWD_PLAN_CHECK();
     const PlanView pv{plan};
@@ -331,14 +384,14 @@ __global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig s
         for (int e = threadIdx.x; e < SQ; e += BT) sc[S_G + e] = src ? src[e] : 0.f;
         __syncthreads();
         for (int ci = pi.nch - 1; ci >= 0; --ci) {
+            const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
             if (TRUE_PASS) {
-                float *dst = gs + (static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci) * SQ;
+                float *dst = gs + unit * SQ;
                 for (int e = threadIdx.x; e < SQ; e += BT) dst[e] = sc[S_G + e];
             }
             const int t0 = pi.start + ci * CH, L = min(CH, pi.len - ci * CH);
-            chunk_terms(sc, t0, L, h, H, q, k, v, g, beta, scale);
             load_do(sc, t0, L, h, H, dout);
-            reverse_step(sc);
+            reverse_step(sc, terms + unit * TERMS_FLOATS);
         }
         __syncthreads();
         float *dst = nullptr;
@@ -528,34 +581,38 @@ __global__ void __launch_bounds__(BT) bwd_grads(const int32_t *plan, PlanSig sig
 }  // namespace
 
 size_t backward_scratch_floats() { return static_cast<size_t>(SCRATCH_FLOATS); }
+size_t backward_terms_floats() { return static_cast<size_t>(TERMS_FLOATS); }
 
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                             const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
                             const float *h0, float scale, const uint16_t *dout, const float *dfinal,
                             const float *A, const float *afin, const float *S_in, float *xs, float *gs,
-                            float *G_end, float *Qd, float *scratch, int grid, float *dq, float *dk, float *dv,
-                            float *dg, float *dbeta, float *dh0, cudaStream_t stream)
+                            float *G_end, float *Qd, float *terms, float *scratch, int grid, float *dq, float *dk,
+                            float *dv, float *dg, float *dbeta, float *dh0, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
     const PlanSig sig = plan_sig(plan_host);
-    for (auto fn : {reinterpret_cast<const void *>(bwd_states), reinterpret_cast<const void *>(bwd_reverse<false>),
+    for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_states),
+                    reinterpret_cast<const void *>(bwd_reverse<false>),
                     reinterpret_cast<const void *>(bwd_reverse<true>), reinterpret_cast<const void *>(bwd_grads)}) {
         const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(BWD_SMEM));
         if (e != cudaSuccess) return e;
     }
-    bwd_states<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, h0, S_in, scale, xs, scratch);
+    bwd_terms<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, terms, scratch);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    bwd_states<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, h0, S_in, xs, scratch);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (pv.n_cont() > 0) {
-        bwd_reverse<false><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, dfinal, G_end,
-                                                    Qd, gs, dh0, scratch);
+        bwd_reverse<false><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, dout, dfinal, G_end, Qd, gs, dh0,
+                                                           scratch);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     bwd_compose<<<H * 4, BT, 0, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    bwd_reverse<true><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, dfinal, G_end, Qd,
-                                               gs, dh0, scratch);
+    bwd_reverse<true><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, dout, dfinal, G_end, Qd, gs, dh0,
+                                                      scratch);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, dq, dk, dv, dg,
                                        dbeta, scratch);

@@ -165,12 +165,13 @@ size_t scan_scratch_bytes(const int32_t *plan_host, int H);
 // backward_scratch_floats() floats; xs and gs hold [H][n_chunks][K][V] floats each, G_end and Qd
 // [S][H][K][V] each.
 size_t backward_scratch_floats();
+size_t backward_terms_floats();   // per (head, chunk)
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                             const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
                             const float *h0, float scale, const uint16_t *dout, const float *dfinal,
                             const float *A, const float *afin, const float *S_in, float *xs, float *gs,
-                            float *G_end, float *Qd, float *scratch, int grid, float *dq, float *dk, float *dv,
-                            float *dg, float *dbeta, float *dh0, cudaStream_t stream);
+                            float *G_end, float *Qd, float *terms, float *scratch, int grid, float *dq, float *dk,
+                            float *dv, float *dg, float *dbeta, float *dh0, cudaStream_t stream);
 // Segments per group of the blocked scan (about sqrt(S)) and the number of groups.
 int scan_group_size(int S);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
