@@ -4,7 +4,11 @@
 A step is one pass of the whole hot path -- kda_segment_forward (chunk forward +
 summaries), kda_compose_summaries (scan) and kda_apply_boundary (fix-up) -- over
 one batch of the synthetic workload, inputs resident in HBM.  The L2 cache is
-flushed (a 256 MiB write) before every step, outside the timed events.
+flushed (a 256 MiB write) before every step, outside the timed events.  Each
+timed step is bracketed by one event pair, so its three calls run as they do
+for a user (each kernel a programmatic dependent of the one before); the
+per-kernel breakdown comes from a second pass of as many steps with events
+between the calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
                   [--path fix_up|two_pass]
@@ -311,6 +315,23 @@ class Problem:
         torch.cuda.synchronize()
         return np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evsets])
 
+    def time_whole(self, stream, flush, steps, warmup, two_pass=False):
+        """CUDA-event times (ms) of whole steps, one event pair around each step and none between its
+        kernels (so each kernel may launch as a programmatic dependent of the one before), after 'warmup'
+        untimed steps; the L2 flushed before every step outside the events."""
+        import torch
+        for _ in range(warmup):
+            flush.fill_(1)
+            self.step(stream, two_pass=two_pass)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            self.step(stream, two_pass=two_pass)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+
     def free(self):
         for name in ("d", "ws", "A", "B", "S_in", "o", "fin", "plan_dev", "h0"):
             setattr(self, name, None)
@@ -320,8 +341,7 @@ def pages_protocol(prob, stream, flush, warmup=20, iters=60, repeats=5):
     """The timing protocol of cuLA PR #110 §Performance: 20 warm-up iterations, then 5 repeats of 60
     timed iterations; the median of each repeat, then the median of the repeats (one rank, so the
     rank-max is the value itself).  The L2 is flushed before every iteration, outside the events."""
-    per = prob.time_steps(stream, flush, iters * repeats, warmup)
-    step = per.sum(axis=1).reshape(repeats, iters)
+    step = prob.time_whole(stream, flush, iters * repeats, warmup).reshape(repeats, iters)
     return float(np.median(np.median(step, axis=1)))
 
 
@@ -343,7 +363,7 @@ def run_ours(args, w, rank, world, local_rank):
         flush.fill_(1)
         prob.step(stream, two_pass=two_pass)
     torch.cuda.synchronize(dev)
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -357,15 +377,19 @@ def run_ours(args, w, rank, world, local_rank):
                 prob.step(stream, two_pass=two_pass)
             torch.cuda.synchronize(dev)
         wall0 = time.perf_counter()
-        for i in range(args.steps):
+        for e0, e1 in evs:
             flush.fill_(1)
-            prob.step(stream, evsets[i], two_pass=two_pass)
+            e0.record(stream)
+            prob.step(stream, two_pass=two_pass)
+            e1.record(stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
+        # the per-kernel breakdown: the same number of steps again, with events between the kernels
+        # (they serialise the programmatic dependent launches, so these sum to more than a step)
+        per = prob.time_steps(stream, flush, args.steps, 0, two_pass=two_pass)   # ms [steps, 3]
     if world > 1:
         dist.barrier()
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evsets])  # ms
-    step_ms = float(np.mean(per.sum(axis=1)))
+    step_ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
     kern_ms = per.mean(axis=0)
     protocol_ms = None if (two_pass or args.no_extra) else pages_protocol(prob, stream, flush)
 
@@ -469,6 +493,9 @@ def run_ours(args, w, rank, world, local_rank):
         "config": _config(w, world) | ({"path": "two_pass"} if two_pass else {}),
         "kernels_ms": ({"two_pass_forward": kern_ms[0]} if two_pass else
                        {"chunk_forward": kern_ms[0], "compose": kern_ms[1], "boundary": kern_ms[2]}),
+        "kernel_timing": ("ms_per_step: one event pair around each whole step; kernels_ms: a second pass of "
+                          "as many steps with events between the kernels, which serialises their "
+                          "programmatic dependent launches (sum %.4f ms)" % float(kern_ms.sum())),
         "kernel_shares": ({"two_pass_forward": 1.0} if two_pass else
                           {"chunk_forward": shares[0], "compose": shares[1], "boundary": shares[2]}),
         "kernel_hbm_frac": (None if two_pass else
@@ -558,7 +585,7 @@ def refined_comparison(args, dev, stream, flush):
             prob = Problem(w, dev, inp=inp, refined=refined)
             per = prob.time_steps(stream, flush, args.extra_steps, 3)
             kern = per.mean(axis=0)
-            ms = float(per.sum(axis=1).mean())
+            ms = float(prob.time_whole(stream, flush, args.extra_steps, 3).mean())
             row[label] = {"segments": prob.S, "ms_per_step": ms, "tokens_per_s": prob.T / (ms / 1e3),
                           "kernels_ms": {n: float(kern[i]) for i, n in enumerate(("chunk_forward", "compose", "boundary"))}}
             prob.free()
@@ -629,7 +656,7 @@ def extra_workloads(args, dev, stream, flush, peaks):
         prob = Problem(w, dev)
         per = prob.time_steps(stream, flush, args.extra_steps, 3)
         kern = per.mean(axis=0)
-        ms = float(per.sum(axis=1).mean())
+        ms = float(prob.time_whole(stream, flush, args.extra_steps, 3).mean())
         kb = kernel_bytes(prob.plan, prob.H, w.h0_std > 0)
         names = ("chunk_forward", "compose", "boundary")
         out[name] = {

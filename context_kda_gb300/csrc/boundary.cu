@@ -11,7 +11,9 @@
 // Work units are 128-row tiles (128 continuing tokens, or the 128 rows of a final-state transition)
 // of one head, numbered head-major so that consecutive units share S_in[j]; a transition follows the
 // tiles of the continuing piece that ends its sequence, whose S_in[j] it needs.  The kernel is
-// persistent: one CTA per SM takes a contiguous run of units as a software pipeline.
+// persistent: one CTA per SM takes a contiguous run of units as a software pipeline.  The runs are
+// cut by cost, not by count (the host computes each CTA's first unit): a transition moves twice a
+// tile's bytes through the threads and takes three products, and each new S_in is split once more.
 // - S_in[j] is read straight into registers and split into a bf16 hi/lo operand only when the run
 //   reaches a new (head, segment).
 // - A qhat tile (bf16) lands by tiled TMA (two 64-column boxes, 128-byte swizzle) directly in the
@@ -25,6 +27,9 @@
 //   unit ahead, updated in place by the epilogue, written back with one TMA store.  Ragged tail tiles
 //   and final states are read and written by the threads directly, so nothing outside a record is
 //   ever stored.
+#include <algorithm>
+#include <vector>
+
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -45,6 +50,16 @@ constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base t
 static_assert(OFF_A % 1024 == 0 && OFF_OB % 1024 == 0, "swizzled buffers");
 constexpr uint32_t TM_COLS = 256;          // two 128-column accumulators
 
+// Relative costs of the run partition, from clock stamps of full launches: a tile (full or ragged)
+// takes about 2.3 us, a final-state transition about 8 us, a new S_in split about 1.6 us.
+constexpr long long COST_TILE = 8, COST_TRANSITION = 28, COST_NEW_STATE = 5;
+constexpr int MAX_RUNS = 192;              // CTAs of one launch (one per SM)
+
+// Each CTA's run: the cursor of its first unit (head, record, unit within the record) and its length.
+struct Runs {
+    int4 c[MAX_RUNS];
+};
+
 __device__ int g_boundary_status;
 
 // Position in the unit order: head h, continuing record rec, unit within the record.  A record's
@@ -60,12 +75,6 @@ struct Rec {
     int seg, seq, units, rows, tok, qrow;
     size_t src;
 };
-
-__device__ __forceinline__ int record_units(const PlanView &pv, int rec)
-{
-    const int32_t *cr = pv.cont(rec);
-    return (cr[3] + TR - 1) / TR + ((pv.piece(cr[0])[PC_FLAGS] & KDA_PIECE_SEQ_END) ? 1 : 0);
-}
 
 __device__ __forceinline__ Rec rec_info(const PlanView &pv, int H, int h, int rec, int tile)
 {
@@ -104,7 +113,7 @@ __device__ __forceinline__ void advance(Cursor &c, const Rec &r, int n_cont)
 }
 
 __global__ void __launch_bounds__(256, 1)
-boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, int units_per_head, long long n_units,
+boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_constant__ Runs runs,
             const float *__restrict__ S_in, const uint16_t *__restrict__ qhat, const float *__restrict__ afin,
             uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_q, int has_tq)
@@ -122,38 +131,13 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, int units_per_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hw = warp >> 2;
     const int n_cont = pv.n_cont();
-    const long long u_begin = n_units * blockIdx.x / gridDim.x;
-    const long long u_end = n_units * (blockIdx.x + 1) / gridDim.x;
-    if (u_begin >= u_end) return;
-    const long long n_run = u_end - u_begin;
+    const int4 run = runs.c[blockIdx.x];
+    const long long n_run = run.w;
+    if (n_run <= 0) return;
     unsigned char *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-
-    // cursor of the first unit: each warp scans the records' tile counts 32 at a time (inclusive
-    // prefix sums over the lanes) and takes the first record whose running count passes the unit
-    Cursor c0{static_cast<int>(u_begin / units_per_head), 0, 0};
-    {
-        int rem = static_cast<int>(u_begin % units_per_head);
-        for (int b = 0; b < n_cont; b += 32) {
-            const int i = b + lane;
-            const int nt = i >= n_cont ? 0 : record_units(pv, i);
-            int incl = nt;
-#pragma unroll
-            for (int sh = 1; sh < 32; sh <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, sh);
-                if (lane >= sh) incl += y;
-            }
-            const int total = __shfl_sync(0xffffffffu, incl, 31);
-            if (rem < total) {
-                const int l = __ffs(__ballot_sync(0xffffffffu, incl > rem)) - 1;
-                c0.rec = b + l;
-                c0.tile = rem - __shfl_sync(0xffffffffu, incl - nt, l);
-                break;
-            }
-            rem -= total;
-        }
-    }
     // units n .. n + 3 of the run (cursor and record; valid while inside the run)
+    Cursor c0{run.x, run.y, run.z};
     Rec r0 = rec_info(pv, H, c0.h, c0.rec, c0.tile);
     Cursor c1 = c0, c2, c3;
     Rec r1 = r0, r2 = r0, r3 = r0;
@@ -443,12 +427,51 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
                             cudaStream_t stream)
 {
     const PlanView pv{plan_host};
-    long long per_head = pv.n_fin();   // every transition belongs to a continuing record
-    for (int i = 0; i < pv.n_cont(); ++i) per_head += (pv.cont(i)[3] + TR - 1) / TR;
+    // one head's units in order with their cumulative cost (every head has the same sequence)
+    std::vector<long long> pre(1, 0);
+    std::vector<long long> rec_first;
+    for (int i = 0; i < pv.n_cont(); ++i) {
+        const int32_t *cr = pv.cont(i);
+        const long long nt = (cr[3] + TR - 1) / TR;
+        const long long nu = nt + ((pv.piece(cr[0])[PC_FLAGS] & KDA_PIECE_SEQ_END) ? 1 : 0);
+        rec_first.push_back(static_cast<long long>(pre.size()) - 1);
+        for (long long t = 0; t < nu; ++t)
+            pre.push_back(pre.back() + (t < nt ? COST_TILE : COST_TRANSITION) + (t == 0 ? COST_NEW_STATE : 0));
+    }
+    const long long per_head = static_cast<long long>(pre.size()) - 1;
     if (per_head == 0) return cudaSuccess;
     if (per_head > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const long long n_units = per_head * H;
-    const long long grid = n_units < sm_count() ? n_units : sm_count();
+    const long long grid = std::min<long long>({n_units, static_cast<long long>(sm_count()), MAX_RUNS});
+    // CTA b starts at the unit boundary whose preceding cost is nearest to b/grid of the total
+    const long long w_head = pre.back();
+    const unsigned __int128 total = static_cast<unsigned __int128>(w_head) * static_cast<unsigned>(H);
+    auto cost_before = [&](long long u) {
+        return static_cast<unsigned __int128>(u / per_head) * static_cast<unsigned long long>(w_head) +
+               static_cast<unsigned long long>(pre[u % per_head]);
+    };
+    Runs runs{};
+    long long prev = 0;
+    for (long long b = 0; b < grid; ++b) {
+        long long next = n_units;
+        if (b + 1 < grid) {
+            const unsigned __int128 target = total * static_cast<unsigned long long>(b + 1) / static_cast<unsigned long long>(grid);
+            long long lo = prev, hi = n_units;   // first u in [prev, n_units] with cost_before(u) >= target
+            while (lo < hi) {
+                const long long mid = lo + (hi - lo) / 2;
+                if (cost_before(mid) >= target) hi = mid;
+                else lo = mid + 1;
+            }
+            if (lo > prev && target - cost_before(lo - 1) < cost_before(lo) - target) --lo;
+            next = lo;
+        }
+        if (next - prev > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        const long long w = prev % per_head;
+        const long long rec = std::upper_bound(rec_first.begin(), rec_first.end(), w) - rec_first.begin() - 1;
+        runs.c[b] = make_int4(static_cast<int>(prev / per_head), static_cast<int>(rec),
+                              static_cast<int>(w - rec_first[rec]), static_cast<int>(next - prev));
+        prev = next;
+    }
     // full 128-row output tiles and every qhat tile go through tiled TMA; a tensor shorter than one
     // tile never uses its map (qhat tiles are then read by the threads)
     CUtensorMap to{}, tq{};
@@ -463,7 +486,7 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
                                            static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(boundary_tc, dim3(static_cast<unsigned>(grid)), dim3(256), SMEM_ALLOC, stream, plan_dev,
-                            plan_sig(plan_host), H, static_cast<int>(per_head), n_units, S_in, qhat, afin, o, final_state, to, tq, has_tq);
+                            plan_sig(plan_host), H, runs, S_in, qhat, afin, o, final_state, to, tq, has_tq);
 }
 
 // Self-test of the expiry path: one thread waits, bounded, on an mbarrier that nothing arrives on,
