@@ -42,7 +42,6 @@ constexpr uint32_t OFF_TP = 147456;   // T': rows r, cols i, CS 1024, hi | lo   
 constexpr uint32_t OFF_MISC = 163840;
 constexpr uint32_t OFF_BETA = OFF_MISC;         // 64 fp32
 constexpr uint32_t OFF_GC = OFF_MISC + 256;     // 128 fp32: exp(Gamma_C)
-constexpr uint32_t OFF_GSUM = OFF_MISC + 768;   // 2 x 128 fp32: per-half decay sums
 constexpr uint32_t OFF_NEXT = OFF_MISC + 1792;  // staged unit: beta (64 fp32), then its row count
 // Raw rows of a unit, loaded by tiled TMA copies (128-byte swizzle, 1024-aligned boxes of 64 rows
 // x 128 bytes) into their own regions: q, k, v as two 64-column boxes each, g as four 32-column
@@ -127,7 +126,6 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
     const uint32_t sbase = smem_u32(base);
     float *const s_beta = reinterpret_cast<float *>(base + OFF_BETA);
     float *const s_gc = reinterpret_cast<float *>(base + OFF_GC);
-    float *const s_gsum = reinterpret_cast<float *>(base + OFF_GSUM);
 
     const PlanView pv{plan};
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -282,36 +280,56 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
             {
                 if (!mbar_wait_warp(gbar, n & 1)) bad = true;
                 L = *s_L_next;   // staged with the rows (read before this unit's staging handoff)
-                // A1: log2-scaled cumulative decay per key channel, in place over the staged g
-                //     (32 rows per thread: load all, scan in registers, store once)
+                // A1: log2-scaled cumulative decay per key channel, in place over the staged g: each
+                //     thread scans 8 rows x 4 channels (16-byte loads), the 8 row groups' totals meet
+                //     in the Kh region (free until A3 writes this unit's Kh), each thread adds the
+                //     totals of the groups above its own and stores its rows back
                 {
-                    const int kc = tid & 127, hr = tid >> 7;
-                    unsigned char *gq = base + STG_G + (kc >> 5) * BOX + (kc & 3) * 4;
-                    const int gch = (kc & 31) >> 2;
-                    float gv[32];
+                    const int cq = tid & 31, rg = tid >> 5;   // channels 4 cq .. 4 cq + 3, rows 8 rg .. 8 rg + 7
+                    unsigned char *gq = base + STG_G + (cq >> 3) * BOX;
+                    const int gch = cq & 7;
+                    float4 gv[8];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) gv[j] = *reinterpret_cast<const float *>(gq + sw128(hr * 32 + j, gch));
-                    float acc = 0.f;
+                    for (int j = 0; j < 8; ++j) gv[j] = *reinterpret_cast<const float4 *>(gq + sw128(rg * 8 + j, gch));
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        acc += (hr * 32 + j < L) ? gv[j] * LOG2E : 0.f;
+                    for (int j = 0; j < 8; ++j) {
+                        const bool ok = rg * 8 + j < L;
+                        acc.x += ok ? gv[j].x * LOG2E : 0.f;
+                        acc.y += ok ? gv[j].y * LOG2E : 0.f;
+                        acc.z += ok ? gv[j].z * LOG2E : 0.f;
+                        acc.w += ok ? gv[j].w * LOG2E : 0.f;
                         gv[j] = acc;
                     }
-                    s_gsum[hr * 128 + kc] = acc;
+                    float4 *const gtot = reinterpret_cast<float4 *>(base + OFF_KH);   // [row group][channel quad]
+                    gtot[rg * 32 + cq] = acc;
                     if (tid < 64) s_beta[tid] = s_beta_next[tid];
                     bar_sync1(NWORK);
-                    const float off = hr ? s_gsum[kc] : 0.f;
-                    if (hr == 0) {
-                        const float gsum = s_gsum[kc] + s_gsum[128 + kc];   // Gamma_C log2 e
-                        // below 2^-112 the decayed operands and their bf16 low parts leave the normal
-                        // fp32 range (NaN or inf in g lands here too)
-                        if (!(gsum >= -112.f)) record_status(&g_prep_status, KDA_ERR_RANGE);
-                        const float gcv = ex2_ftz(gsum);   // exp(Gamma_C)
-                        s_gc[kc] = gcv;
-                        reinterpret_cast<float *>(pk + PK_GC)[kc] = gcv;
+                    float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int g2 = 0; g2 < 7; ++g2) {
+                        const float4 t = gtot[g2 * 32 + cq];
+                        if (g2 < rg) {
+                            off.x += t.x;
+                            off.y += t.y;
+                            off.z += t.z;
+                            off.w += t.w;
+                        }
+                    }
+                    if (rg == 7) {
+                        // Gamma_C log2 e per channel; below 2^-112 the decayed operands and their bf16 low
+                        // parts leave the normal fp32 range (NaN or inf in g lands here too)
+                        const float4 gs = make_float4(off.x + acc.x, off.y + acc.y, off.z + acc.z, off.w + acc.w);
+                        if (!(gs.x >= -112.f && gs.y >= -112.f && gs.z >= -112.f && gs.w >= -112.f))
+                            record_status(&g_prep_status, KDA_ERR_RANGE);
+                        const float4 gcv = make_float4(ex2_ftz(gs.x), ex2_ftz(gs.y), ex2_ftz(gs.z), ex2_ftz(gs.w));
+                        reinterpret_cast<float4 *>(s_gc)[cq] = gcv;
+                        reinterpret_cast<float4 *>(pk + PK_GC)[cq] = gcv;
                     }
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(gq + sw128(hr * 32 + j, gch)) = gv[j] + off;
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4 *>(gq + sw128(rg * 8 + j, gch)) =
+                            make_float4(gv[j].x + off.x, gv[j].y + off.y, gv[j].z + off.z, gv[j].w + off.w);
                     bar_sync1(NWORK);
                 }
                 // A2: each thread takes four (row, 8-column) pieces of the staged rows into registers;
@@ -424,17 +442,28 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
             // warps 4 - 7 (one per TMEM lane quadrant) store the previous unit's Ut^T meanwhile: its
             // columns stay valid until this unit's T' is handed over
             if (n > 0 && tid >= 128) store_ut(u - 1, -1);
-            if (tid < 64) {   // column jj of diagonal block b; each solved entry updates all later rows
+            if (tid < 64) {   // column jj of diagonal block b, row by row: x_r = -sum_{i<r} M[r][i] x_i
                 const int b = tid >> 4, jj = tid & 15, r0 = 16 * b;
-                float x[16], sacc[16];
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) sacc[rr] = 0.f;
+                float x[16];
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
-                    x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -sacc[rr]);
+                    float s0 = 0.f, s1 = 0.f;   // two partial sums: half the dependent chain
 #pragma unroll
-                    for (int r2 = rr + 1; r2 < 16; ++r2)
-                        sacc[r2] = fmaf(*f32_at(base, OFF_M32, r0 + r2, r0 + rr), x[rr], sacc[r2]);
+                    for (int m4 = 0; m4 < 4; ++m4) {   // the block row's entries in 16-byte loads
+                        if (4 * m4 < rr) {
+                            const float4 mv =
+                                *reinterpret_cast<const float4 *>(f32_at(base, OFF_M32, r0 + rr, r0 + 4 * m4));
+                            const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (4 * m4 + e < rr) {
+                                    if (e & 1) s1 = fmaf(mm[e], x[4 * m4 + e], s1);
+                                    else s0 = fmaf(mm[e], x[4 * m4 + e], s0);
+                                }
+                            }
+                        }
+                    }
+                    x[rr] = (rr == jj) ? 1.f : ((rr < jj) ? 0.f : -(s0 + s1));
                 }
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) *f32_at(base, OFF_T32, r0 + rr, r0 + jj) = x[rr];
