@@ -61,25 +61,42 @@ enum : int {
 enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * CK, TM_GC = 4 * CK + CC,
              TERMS_FLOATS = TM_GC + KD };
 
-// A matrix operand in global scratch: element (r, c) = t ? p[c * ld + r] : p[r * ld + c].
-struct Mat {
-    const float *p;
-    int ld;
-    bool t;
-};
-__device__ __forceinline__ Mat mat(const float *p, int ld) { return Mat{p, ld, false}; }
-__device__ __forceinline__ Mat tr(const float *p, int ld) { return Mat{p, ld, true}; }
-
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
 constexpr int SM_PAD = 4;
 constexpr int SM_LD = 128 + SM_PAD;
 constexpr size_t BWD_SMEM = 2ull * 128 * SM_LD * sizeof(float);
 
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+__device__ __forceinline__ int warp_id() { return static_cast<int>(threadIdx.x) >> 5; }
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+__device__ __forceinline__ float4 scl4(float s, float4 a) { return make_float4(s * a.x, s * a.y, s * a.z, s * a.w); }
+__device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
+    return v;
+}
+
+// dst[e] = src[e] for n floats (n a multiple of 4 * BT), every thread's loads issued before its stores
+template <int N>
+__device__ __forceinline__ void copy_f(float *dst, const float *src)
+{
+    constexpr int P = N / 4 / BT;
+    float4 v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) v[i] = ld4(src + 4 * (threadIdx.x + i * BT));
+#pragma unroll
+    for (int i = 0; i < P; ++i) st4(dst + 4 * (threadIdx.x + i * BT), v[i]);
+}
+
 // Micro-tile product over operands already in shared memory: As[k][m] (M x K), Bs[k][n] (K x N);
 // thread (ty, tx) of a 16 x 16 grid computes rows ty*MR .. +MR and columns tx*NR .. +NR.
-template <int MR, int NR>
-__device__ __forceinline__ void gemm_core(int K, const float *As, const float *Bs, float *C, int ldc, float alpha,
-                                          bool acc)
+template <int MR, int NR, int K>
+__device__ __forceinline__ void gemm_core(const float *As, const float *Bs, float *C, int ldc, float alpha, bool acc)
 {
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     float c[MR][NR];
@@ -87,16 +104,17 @@ __device__ __forceinline__ void gemm_core(int K, const float *As, const float *B
     for (int i = 0; i < MR; ++i)
 #pragma unroll
         for (int j = 0; j < NR; ++j) c[i][j] = 0.f;
+#pragma unroll 4
     for (int k = 0; k < K; ++k) {
         float a[MR], b[NR];
 #pragma unroll
         for (int i = 0; i < MR; i += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(As + k * SM_LD + ty * MR + i);
+            const float4 v = ld4(As + k * SM_LD + ty * MR + i);
             a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
         }
 #pragma unroll
         for (int j = 0; j < NR; j += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(Bs + k * SM_LD + tx * NR + j);
+            const float4 v = ld4(Bs + k * SM_LD + tx * NR + j);
             b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
         }
 #pragma unroll
@@ -107,124 +125,223 @@ __device__ __forceinline__ void gemm_core(int K, const float *As, const float *B
 #pragma unroll
     for (int i = 0; i < MR; ++i)
 #pragma unroll
-        for (int j = 0; j < NR; ++j) {
+        for (int j = 0; j < NR; j += 4) {
             float *d = C + (ty * MR + i) * ldc + tx * NR + j;
-            *d = alpha * c[i][j] + (acc ? *d : 0.f);
+            const float4 old = acc ? ld4(d) : make_float4(0.f, 0.f, 0.f, 0.f);
+            st4(d, make_float4(alpha * c[i][j] + old.x, alpha * c[i][j + 1] + old.y, alpha * c[i][j + 2] + old.z,
+                               alpha * c[i][j + 3] + old.w));
         }
 }
 
-// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc), for an M x N result (M, N in {64, 128})
-// and K-long sums (K in {64, 128}), operands 16-byte aligned with leading dimensions a multiple of 4, by
-// all threads of the CTA: both operands are staged in shared memory
-// (k-major) in one pass, then every thread accumulates its micro-tile over the whole K.
-__device__ void gemm(int M, int N, int K, Mat A, Mat B, float *C, int ldc, float alpha, bool acc)
+// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc) for an M x N result and K-long sums
+// (M, N, K in {64, 128}), by all threads of the CTA, with A(m, k) = TA ? a[k * lda + m] : a[m * lda + k]
+// and B(k, n) = TB ? b[n * ldb + k] : b[k * ldb + n] (16-byte aligned, leading dimensions multiples of 4).
+// Every thread issues all its 16-byte operand loads at once, then both operands are stored k-major
+// in shared memory (a transposed operand by 16 rows x 2 vectors a warp, so that the scattered stores
+// fall in distinct banks), then each thread accumulates its micro-tile over the whole K.
+template <int M, int N, int K, bool TA, bool TB>
+__device__ void gemm(const float *a, int lda, const float *b, int ldb, float *C, int ldc, float alpha, bool acc)
 {
     extern __shared__ __align__(16) float bsm[];
     float *As = bsm, *Bs = bsm + 128 * SM_LD;
     const int tid = threadIdx.x;
-    __syncthreads();
-    // 16-byte loads along the contiguous index; M, N, K are powers of two (64 or 128, K >= 64)
-    const int lm = __ffs(M) - 1, ln = __ffs(N) - 1, lk = __ffs(K) - 1;
-    if (A.t) {            // A(m, k) = p[k * ld + m]: rows of m, stored as they come
-        for (int e = tid; e < (K * M) >> 2; e += BT) {
-            const int k = e >> (lm - 2), m4 = (e & ((M >> 2) - 1)) << 2;
-            *reinterpret_cast<float4 *>(As + k * SM_LD + m4) = *reinterpret_cast<const float4 *>(A.p + k * A.ld + m4);
-        }
-    } else {              // A(m, k) = p[m * ld + k]: rows of k, transposed into As; a warp takes 16 rows m
-                          // x 2 vectors, so its scattered stores fall in 32 distinct banks
-        for (int e = tid; e < (K * M) >> 2; e += BT) {
-            const int rest = e >> 4, kv = rest & ((K >> 2) - 1);
-            const int m = ((rest >> (lk - 2)) << 4) | (e & 15), k4 = kv << 2;
-            const float4 v = *reinterpret_cast<const float4 *>(A.p + m * A.ld + k4);
-            As[(k4 + 0) * SM_LD + m] = v.x;
-            As[(k4 + 1) * SM_LD + m] = v.y;
-            As[(k4 + 2) * SM_LD + m] = v.z;
-            As[(k4 + 3) * SM_LD + m] = v.w;
+    constexpr int NA = K * M / 4 / BT, NB = K * N / 4 / BT;
+    constexpr int LM = ilog2(M), LN = ilog2(N), LK = ilog2(K);
+    float4 va[NA], vb[NB];
+#pragma unroll
+    for (int i = 0; i < NA; ++i) {
+        const int e = tid + i * BT;
+        if (TA) {
+            va[i] = ld4(a + (e >> (LM - 2)) * lda + ((e & (M / 4 - 1)) << 2));
+        } else {
+            const int rest = e >> 4;
+            va[i] = ld4(a + (((rest >> (LK - 2)) << 4) | (e & 15)) * lda + ((rest & (K / 4 - 1)) << 2));
         }
     }
-    if (B.t) {            // B(k, n) = p[n * ld + k]: rows of k, transposed into Bs (16 rows n x 2 vectors a warp)
-        for (int e = tid; e < (K * N) >> 2; e += BT) {
-            const int rest = e >> 4, kv = rest & ((K >> 2) - 1);
-            const int n = ((rest >> (lk - 2)) << 4) | (e & 15), k4 = kv << 2;
-            const float4 v = *reinterpret_cast<const float4 *>(B.p + n * B.ld + k4);
-            Bs[(k4 + 0) * SM_LD + n] = v.x;
-            Bs[(k4 + 1) * SM_LD + n] = v.y;
-            Bs[(k4 + 2) * SM_LD + n] = v.z;
-            Bs[(k4 + 3) * SM_LD + n] = v.w;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        const int e = tid + i * BT;
+        if (TB) {
+            const int rest = e >> 4;
+            vb[i] = ld4(b + (((rest >> (LK - 2)) << 4) | (e & 15)) * ldb + ((rest & (K / 4 - 1)) << 2));
+        } else {
+            vb[i] = ld4(b + (e >> (LN - 2)) * ldb + ((e & (N / 4 - 1)) << 2));
         }
-    } else {              // B(k, n) = p[k * ld + n]: rows of n, stored as they come
-        for (int e = tid; e < (K * N) >> 2; e += BT) {
-            const int k = e >> (ln - 2), n4 = (e & ((N >> 2) - 1)) << 2;
-            *reinterpret_cast<float4 *>(Bs + k * SM_LD + n4) = *reinterpret_cast<const float4 *>(B.p + k * B.ld + n4);
+    }
+    __syncthreads();   // the operand buffers are free
+#pragma unroll
+    for (int i = 0; i < NA; ++i) {
+        const int e = tid + i * BT;
+        if (TA) {
+            st4(As + (e >> (LM - 2)) * SM_LD + ((e & (M / 4 - 1)) << 2), va[i]);
+        } else {
+            const int rest = e >> 4, k4 = (rest & (K / 4 - 1)) << 2, m = ((rest >> (LK - 2)) << 4) | (e & 15);
+            As[(k4 + 0) * SM_LD + m] = va[i].x;
+            As[(k4 + 1) * SM_LD + m] = va[i].y;
+            As[(k4 + 2) * SM_LD + m] = va[i].z;
+            As[(k4 + 3) * SM_LD + m] = va[i].w;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        const int e = tid + i * BT;
+        if (TB) {
+            const int rest = e >> 4, k4 = (rest & (K / 4 - 1)) << 2, n = ((rest >> (LK - 2)) << 4) | (e & 15);
+            Bs[(k4 + 0) * SM_LD + n] = vb[i].x;
+            Bs[(k4 + 1) * SM_LD + n] = vb[i].y;
+            Bs[(k4 + 2) * SM_LD + n] = vb[i].z;
+            Bs[(k4 + 3) * SM_LD + n] = vb[i].w;
+        } else {
+            st4(Bs + (e >> (LN - 2)) * SM_LD + ((e & (N / 4 - 1)) << 2), vb[i]);
         }
     }
     __syncthreads();
-    if (M == 128 && N == 128) gemm_core<8, 8>(K, As, Bs, C, ldc, alpha, acc);
-    else if (M == 128) gemm_core<8, 4>(K, As, Bs, C, ldc, alpha, acc);
-    else if (N == 128) gemm_core<4, 8>(K, As, Bs, C, ldc, alpha, acc);
-    else gemm_core<4, 4>(K, As, Bs, C, ldc, alpha, acc);
+    gemm_core<M / 16, N / 16, K>(As, Bs, C, ldc, alpha, acc);
     __syncthreads();
 }
 
-__device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+// 8 bf16 (one 16-byte word) as fp32
+__device__ __forceinline__ void bf8(uint4 w, float *x)
+{
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        x[2 * p] = __uint_as_float(ww[p] << 16);
+        x[2 * p + 1] = __uint_as_float(ww[p] & 0xFFFF0000u);
+    }
+}
 
 // The chunk's terms into scratch sc (rows past L are zero): Kt, Kh, Qt, V, E = e^Gamma, Ei = e^-Gamma,
 // gc = e^Gamma_C, beta, M, S = strictly_lower(Kt Kh^T), T, W, Ut, QK, and Diag(beta) Kt, Diag(beta) V.
 __device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16_t *q, const uint16_t *k,
                             const uint16_t *v, const float *g, const float *beta, float scale)
 {
+    extern __shared__ __align__(16) float bsm[];
     const int tid = threadIdx.x;
     float *Kt = sc + S_KT, *Kh = sc + S_KH, *Qt = sc + S_QT, *Vf = sc + S_VF, *E = sc + S_E, *Ei = sc + S_EI;
-    for (int e = tid; e < CK; e += BT) {
-        const int r = e >> 7, c = e & 127;
-        const bool ok = r < L;
-        const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + c;
-        Kt[e] = ok ? bf(k[gi]) : 0.f;       // raw k for now
-        Qt[e] = ok ? bf(q[gi]) : 0.f;       // raw q for now
-        Vf[e] = ok ? bf(v[gi]) : 0.f;
-        E[e] = ok ? g[gi] : 0.f;            // g for now
-    }
-    for (int r = tid; r < 64; r += BT) sc[S_BT + r] = r < L ? beta[static_cast<size_t>(t0 + r) * H + h] : 0.f;
-    __syncthreads();
-    if (tid < KD) {                           // Gamma: cumulative sum down the rows, per channel
-        float acc = 0.f;
-        for (int r = 0; r < 64; ++r) {
-            acc += E[r * KD + tid];
-            E[r * KD + tid] = acc;
+    if (tid < 64) sc[S_BT + tid] = tid < L ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
+    // V rows: 8 channels a piece, 4 pieces a thread
+    {
+        uint4 vw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + i * BT, r = e >> 4, c8 = (e & 15) << 3;
+            vw[i] = r < L ? *reinterpret_cast<const uint4 *>(v + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
+                          : make_uint4(0u, 0u, 0u, 0u);
         }
-        sc[S_GC + tid] = expf(acc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + i * BT, r = e >> 4, c8 = (e & 15) << 3;
+            float x[8];
+            bf8(vw[i], x);
+            st4(Vf + r * VD + c8, make_float4(x[0], x[1], x[2], x[3]));
+            st4(Vf + r * VD + c8 + 4, make_float4(x[4], x[5], x[6], x[7]));
+        }
+    }
+    // Gamma = cumulative g down the rows, per channel: each thread holds rows 8 rg .. 8 rg + 7 of
+    // channels 4 cq .. 4 cq + 3, scans them, and adds the totals of the row groups above (met in
+    // shared memory); then the decayed rows
+    {
+        const int cq = tid & 31, rg = tid >> 5;
+        float4 gv[8];
+        uint2 kw[8], qw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = rg * 8 + j;
+            const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
+            const bool ok = r < L;
+            gv[j] = ok ? ld4(g + gi) : make_float4(0.f, 0.f, 0.f, 0.f);
+            kw[j] = ok ? *reinterpret_cast<const uint2 *>(k + gi) : make_uint2(0u, 0u);
+            qw[j] = ok ? *reinterpret_cast<const uint2 *>(q + gi) : make_uint2(0u, 0u);
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc = add4(acc, gv[j]);
+            gv[j] = acc;
+        }
+        float4 *const tot = reinterpret_cast<float4 *>(bsm);   // [row group][channel quad]
+        __syncthreads();   // shared memory free
+        tot[rg * 32 + cq] = acc;
+        __syncthreads();
+        float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int g2 = 0; g2 < 7; ++g2) {
+            const float4 t = tot[g2 * 32 + cq];
+            if (g2 < rg) off = add4(off, t);
+        }
+        if (rg == 7) {
+            const float4 gs = add4(off, acc);
+            st4(sc + S_GC + 4 * cq, make_float4(expf(gs.x), expf(gs.y), expf(gs.z), expf(gs.w)));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = (rg * 8 + j) * KD + 4 * cq;
+            const float4 G = add4(gv[j], off);
+            const float4 ex = make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
+            const float4 exi = make_float4(expf(-G.x), expf(-G.y), expf(-G.z), expf(-G.w));
+            const float4 kf = make_float4(__uint_as_float(kw[j].x << 16), __uint_as_float(kw[j].x & 0xFFFF0000u),
+                                          __uint_as_float(kw[j].y << 16), __uint_as_float(kw[j].y & 0xFFFF0000u));
+            const float4 qf = make_float4(__uint_as_float(qw[j].x << 16), __uint_as_float(qw[j].x & 0xFFFF0000u),
+                                          __uint_as_float(qw[j].y << 16), __uint_as_float(qw[j].y & 0xFFFF0000u));
+            st4(Kt + e, mul4(ex, kf));
+            st4(Kh + e, mul4(exi, kf));
+            st4(Qt + e, scl4(scale, mul4(ex, qf)));
+            st4(E + e, ex);
+            st4(Ei + e, exi);
+        }
     }
     __syncthreads();
-    for (int e = tid; e < CK; e += BT) {
-        const float G = E[e], ex = expf(G), exi = expf(-G), kv = Kt[e];
-        Kt[e] = ex * kv;
-        Kh[e] = exi * kv;
-        Qt[e] = scale * ex * Qt[e];
-        E[e] = ex;
-        Ei[e] = exi;
+    gemm<64, 64, KD, false, true>(Kt, KD, Kh, KD, sc + S_S, 64, 1.f, false);
+    gemm<64, 64, KD, false, true>(Qt, KD, Kh, KD, sc + S_QK, 64, 1.f, false);
+    // S strictly lower, M = Diag(beta) S, QK lower with the diagonal
+    {
+        float4 sv[4], qv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = 4 * (tid + i * BT);
+            sv[i] = ld4(sc + S_S + e);
+            qv[i] = ld4(sc + S_QK + e);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = 4 * (tid + i * BT), r = e >> 6, c = e & 63;
+            const float br = sc[S_BT + r];
+            const float4 sm = make_float4(c + 0 < r ? sv[i].x : 0.f, c + 1 < r ? sv[i].y : 0.f, c + 2 < r ? sv[i].z : 0.f,
+                                          c + 3 < r ? sv[i].w : 0.f);
+            st4(sc + S_S + e, sm);
+            st4(sc + S_M + e, scl4(br, sm));
+            st4(sc + S_QK + e, make_float4(c + 0 <= r ? qv[i].x : 0.f, c + 1 <= r ? qv[i].y : 0.f,
+                                           c + 2 <= r ? qv[i].z : 0.f, c + 3 <= r ? qv[i].w : 0.f));
+        }
     }
-    __syncthreads();
-    gemm(64, 64, KD, mat(Kt, KD), tr(Kh, KD), sc + S_S, 64, 1.f, false);
-    gemm(64, 64, KD, mat(Qt, KD), tr(Kh, KD), sc + S_QK, 64, 1.f, false);
-    for (int e = tid; e < CC; e += BT) {
-        const int r = e >> 6, i = e & 63;
-        const float s = i < r ? sc[S_S + e] : 0.f;
-        sc[S_S + e] = s;
-        sc[S_M + e] = sc[S_BT + r] * s;
-        if (i > r) sc[S_QK + e] = 0.f;
-    }
-    for (int e = tid; e < CK; e += BT) {
-        const float b = sc[S_BT + (e >> 7)];
-        sc[S_BKT + e] = b * Kt[e];
-        sc[S_BV + e] = b * Vf[e];
+    // Diag(beta) Kt and Diag(beta) V
+    {
+        float4 kv[8], vv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 4 * (tid + i * BT);
+            kv[i] = ld4(Kt + e);
+            vv[i] = ld4(Vf + e);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 4 * (tid + i * BT);
+            const float b = sc[S_BT + (e >> 7)];
+            st4(sc + S_BKT + e, scl4(b, kv[i]));
+            st4(sc + S_BV + e, scl4(b, vv[i]));
+        }
     }
     __syncthreads();
     // T = (I + M)^-1 by forward substitution, one column per thread: T[j][j] = 1,
     // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]; M in shared memory (read by every thread alike),
     // the column in registers
     {
-        extern __shared__ __align__(16) float bsm[];
-        for (int e = tid; e < CC; e += BT) bsm[e] = sc[S_M + e];
+        float4 mv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mv[i] = ld4(sc + S_M + 4 * (tid + i * BT));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st4(bsm + 4 * (tid + i * BT), mv[i]);
         __syncthreads();
         if (tid < 64) {
             const int j = tid;
@@ -241,28 +358,53 @@ __device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16
         }
         __syncthreads();
     }
-    gemm(64, KD, 64, mat(sc + S_T, 64), mat(sc + S_BKT, KD), sc + S_W, KD, 1.f, false);
-    gemm(64, VD, 64, mat(sc + S_T, 64), mat(sc + S_BV, VD), sc + S_UT, VD, 1.f, false);
+    gemm<64, KD, 64, false, false>(sc + S_T, 64, sc + S_BKT, KD, sc + S_W, KD, 1.f, false);
+    gemm<64, VD, 64, false, false>(sc + S_T, 64, sc + S_BV, VD, sc + S_UT, VD, 1.f, false);
 }
 
-// The chunk's output gradients rows into scratch (zero past L), bf16 -> fp32.
+// The chunk's output gradient rows into scratch (zero past L), bf16 -> fp32.
 __device__ void load_do(float *sc, int t0, int L, int h, int H, const uint16_t *dout)
 {
-    for (int e = threadIdx.x; e < CK; e += BT) {
-        const int r = e >> 7, c = e & 127;
-        sc[S_DO + e] = r < L ? bf(dout[(static_cast<size_t>(t0 + r) * H + h) * VD + c]) : 0.f;
+    uint4 w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = threadIdx.x + i * BT, r = e >> 4, c8 = (e & 15) << 3;
+        w[i] = r < L ? *reinterpret_cast<const uint4 *>(dout + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = threadIdx.x + i * BT, r = e >> 4, c8 = (e & 15) << 3;
+        float x[8];
+        bf8(w[i], x);
+        st4(sc + S_DO + r * VD + c8, make_float4(x[0], x[1], x[2], x[3]));
+        st4(sc + S_DO + r * VD + c8 + 4, make_float4(x[4], x[5], x[6], x[7]));
     }
     __syncthreads();
+}
+
+// dst = Diag(d) src for a 128 x 128 state (d one value per row), every thread's loads first
+__device__ __forceinline__ void scale_rows(float *dst, const float *src, const float *d)
+{
+    constexpr int P = SQ / 4 / BT;
+    float4 v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) v[i] = ld4(src + 4 * (threadIdx.x + i * BT));
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = 4 * (threadIdx.x + i * BT);
+        st4(dst + e, scl4(d[e >> 7], v[i]));
+    }
 }
 
 // X <- Dc (X + Kh^T (Ut - W X)), the chunk's terms at tm
 __device__ void forward_step(float *sc, const float *tm)
 {
     float *X = sc + S_X, *U = sc + S_U;
-    for (int e = threadIdx.x; e < CK; e += BT) U[e] = tm[TM_UT + e];
-    gemm(64, VD, KD, mat(tm + TM_W, KD), mat(X, VD), U, VD, -1.f, true);
-    gemm(KD, VD, 64, tr(tm + TM_KH, KD), mat(U, VD), X, VD, 1.f, true);
-    for (int e = threadIdx.x; e < SQ; e += BT) X[e] *= tm[TM_GC + (e >> 7)];
+    copy_f<CK>(U, tm + TM_UT);
+    gemm<64, VD, KD, false, false>(tm + TM_W, KD, X, VD, U, VD, -1.f, true);
+    gemm<KD, VD, 64, true, false>(tm + TM_KH, KD, U, VD, X, VD, 1.f, true);
+    scale_rows(X, X, tm + TM_GC);
     __syncthreads();
 }
 
@@ -271,14 +413,13 @@ __device__ void forward_step(float *sc, const float *tm)
 __device__ void reverse_step(float *sc, const float *tm)
 {
     float *G = sc + S_G, *DG = sc + S_Y, *dU = sc + S_DU;
-    for (int e = threadIdx.x; e < SQ; e += BT) DG[e] = tm[TM_GC + (e >> 7)] * G[e];
+    scale_rows(DG, G, tm + TM_GC);
     __syncthreads();
-    gemm(64, VD, KD, mat(tm + TM_KH, KD), mat(DG, VD), dU, VD, 1.f, false);
-    gemm(64, VD, 64, tr(tm + TM_QK, 64), mat(sc + S_DO, VD), dU, VD, 1.f, true);
-    for (int e = threadIdx.x; e < SQ; e += BT) G[e] = DG[e];
-    __syncthreads();
-    gemm(KD, VD, 64, tr(tm + TM_QT, KD), mat(sc + S_DO, VD), G, VD, 1.f, true);
-    gemm(KD, VD, 64, tr(tm + TM_W, KD), mat(dU, VD), G, VD, -1.f, true);
+    gemm<64, VD, KD, false, false>(tm + TM_KH, KD, DG, VD, dU, VD, 1.f, false);
+    gemm<64, VD, 64, true, false>(tm + TM_QK, 64, sc + S_DO, VD, dU, VD, 1.f, true);
+    copy_f<SQ>(G, DG);
+    gemm<KD, VD, 64, true, false>(tm + TM_QT, KD, sc + S_DO, VD, G, VD, 1.f, true);
+    gemm<KD, VD, 64, true, false>(tm + TM_W, KD, dU, VD, G, VD, -1.f, true);
 }
 
 // Plan helpers
@@ -302,7 +443,7 @@ __device__ PieceInfo piece_info(const PlanView &pv, int p)
     }
 
 // 0. every (chunk, head) in parallel: the terms the chains need, stored at terms[h][c]
-__global__ void __launch_bounds__(BT) bwd_terms(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
+__global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
                                                 const uint16_t *k, const uint16_t *v, const float *g,
                                                 const float *beta, float scale, float *terms, float *scratch)
 {
@@ -315,20 +456,18 @@ __global__ void __launch_bounds__(BT) bwd_terms(const int32_t *plan, PlanSig sig
         const int32_t *cr = pv.chunk(c);
         chunk_terms(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
         float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;
-        for (int e = threadIdx.x; e < CK; e += BT) {
-            tm[TM_W + e] = sc[S_W + e];
-            tm[TM_UT + e] = sc[S_UT + e];
-            tm[TM_KH + e] = sc[S_KH + e];
-            tm[TM_QT + e] = sc[S_QT + e];
-        }
-        for (int e = threadIdx.x; e < CC; e += BT) tm[TM_QK + e] = sc[S_QK + e];
-        for (int e = threadIdx.x; e < KD; e += BT) tm[TM_GC + e] = sc[S_GC + e];
+        copy_f<CK>(tm + TM_W, sc + S_W);
+        copy_f<CK>(tm + TM_UT, sc + S_UT);
+        copy_f<CK>(tm + TM_KH, sc + S_KH);
+        copy_f<CK>(tm + TM_QT, sc + S_QT);
+        copy_f<CC>(tm + TM_QK, sc + S_QK);
+        if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
         __syncthreads();
     }
 }
 
 // 1. every piece from its true incoming state, recording X_c = xs[h][c] for each of its chunks
-__global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig sig, int H, const float *terms,
+__global__ void __launch_bounds__(BT, 1) bwd_states(const int32_t *plan, PlanSig sig, int H, const float *terms,
                                                  const float *h0, const float *S_in, float *xs, float *scratch)
 {
     BWD_PLAN_CHECK();
@@ -344,12 +483,13 @@ __global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig si
         } else {
             src = S_in + (static_cast<size_t>(pi.seg) * H + h) * SQ;
         }
-        for (int e = threadIdx.x; e < SQ; e += BT) sc[S_X + e] = src ? src[e] : 0.f;
+        if (src) copy_f<SQ>(sc + S_X, src);
+        else
+            for (int i = 0; i < SQ / 4 / BT; ++i) st4(sc + S_X + 4 * (threadIdx.x + i * BT), make_float4(0.f, 0.f, 0.f, 0.f));
         __syncthreads();
         for (int ci = 0; ci < pi.nch; ++ci) {
             const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
-            float *dst = xs + unit * SQ;
-            for (int e = threadIdx.x; e < SQ; e += BT) dst[e] = sc[S_X + e];
+            copy_f<SQ>(xs + unit * SQ, sc + S_X);
             forward_step(sc, terms + unit * TERMS_FLOATS);
         }
         __syncthreads();
@@ -361,7 +501,7 @@ __global__ void __launch_bounds__(BT) bwd_states(const int32_t *plan, PlanSig si
 // its true end gradient (dfinal of its sequence when it ends it, else G_end[seg]); records G_c =
 // gs[h][c], the gradient of each chunk's end state, and gives dh0 at a sequence start.
 template <bool TRUE_PASS>
-__global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig sig, int H, const float *terms,
+__global__ void __launch_bounds__(BT, 1) bwd_reverse(const int32_t *plan, PlanSig sig, int H, const float *terms,
                                                   const uint16_t *dout, const float *dfinal, const float *G_end,
                                                   float *Qd, float *gs, float *dh0, float *scratch)
 {
@@ -381,14 +521,13 @@ __global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig s
                 src = G_end + (static_cast<size_t>(pi.seg) * H + h) * SQ;
             }
         }
-        for (int e = threadIdx.x; e < SQ; e += BT) sc[S_G + e] = src ? src[e] : 0.f;
+        if (src) copy_f<SQ>(sc + S_G, src);
+        else
+            for (int i = 0; i < SQ / 4 / BT; ++i) st4(sc + S_G + 4 * (threadIdx.x + i * BT), make_float4(0.f, 0.f, 0.f, 0.f));
         __syncthreads();
         for (int ci = pi.nch - 1; ci >= 0; --ci) {
             const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
-            if (TRUE_PASS) {
-                float *dst = gs + unit * SQ;
-                for (int e = threadIdx.x; e < SQ; e += BT) dst[e] = sc[S_G + e];
-            }
+            if (TRUE_PASS) copy_f<SQ>(gs + unit * SQ, sc + S_G);
             const int t0 = pi.start + ci * CH, L = min(CH, pi.len - ci * CH);
             load_do(sc, t0, L, h, H, dout);
             reverse_step(sc, terms + unit * TERMS_FLOATS);
@@ -397,8 +536,7 @@ __global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig s
         float *dst = nullptr;
         if (!TRUE_PASS) dst = Qd + (static_cast<size_t>(pi.seg) * H + h) * SQ;
         else if ((pi.flags & KDA_PIECE_FIRST) && dh0) dst = dh0 + (static_cast<size_t>(pi.seq) * H + h) * SQ;
-        if (dst)
-            for (int e = threadIdx.x; e < SQ; e += BT) dst[e] = sc[S_G + e];
+        if (dst) copy_f<SQ>(dst, sc + S_G);
         __syncthreads();
     }
 }
@@ -407,7 +545,7 @@ __global__ void __launch_bounds__(BT) bwd_reverse(const int32_t *plan, PlanSig s
 //    G_end[j] = dfinal of the sequence ending at b_{j+1}, if one does; otherwise, with p the
 //    continuing piece that opens segment j+1,
 //    G_end[j] = Qd[j+1] + (P_end(p)^T dfinal[seq] if p ends its sequence, else A[j+1]^T G_end[j+1]).
-__global__ void __launch_bounds__(BT) bwd_compose(const int32_t *plan, PlanSig sig, int H, const float *A,
+__global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSig sig, int H, const float *A,
                                                   const float *afin, const float *dfinal, const float *Qd,
                                                   float *G_end)
 {
@@ -474,7 +612,7 @@ __global__ void __launch_bounds__(BT) bwd_compose(const int32_t *plan, PlanSig s
 }
 
 // 5. every (chunk, head): the input gradients of the chunk's rows from (X_c, G_c, dO)
-__global__ void __launch_bounds__(BT) bwd_grads(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
+__global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
                                                 const uint16_t *k, const uint16_t *v, const float *g,
                                                 const float *beta, float scale, const uint16_t *dout,
                                                 const float *xs, const float *gs, float *dq, float *dk, float *dv,
@@ -494,83 +632,166 @@ __global__ void __launch_bounds__(BT) bwd_grads(const int32_t *plan, PlanSig sig
         float *X = sc + S_X, *G = sc + S_G, *DG = sc + S_Y;
         const float *xsrc = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
         const float *gsrc = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
-        for (int e = tid; e < SQ; e += BT) {
-            X[e] = xsrc[e];
-            G[e] = gsrc[e];
-            DG[e] = sc[S_GC + (e >> 7)] * gsrc[e];
-        }
+        copy_f<SQ>(X, xsrc);
+        copy_f<SQ>(G, gsrc);
+        scale_rows(DG, gsrc, sc + S_GC);
         float *U = sc + S_U, *dU = sc + S_DU, *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dW = sc + S_DW;
         float *dQK = sc + S_DQK, *dT = sc + S_DT, *dM = sc + S_DM, *dKt = sc + S_DKT;
-        for (int e = tid; e < CK; e += BT) U[e] = sc[S_UT + e];
+        copy_f<CK>(U, sc + S_UT);
         __syncthreads();
-        gemm(64, VD, KD, mat(sc + S_W, KD), mat(X, VD), U, VD, -1.f, true);            // U = Ut - W X
-        gemm(64, VD, KD, mat(sc + S_KH, KD), mat(DG, VD), dU, VD, 1.f, false);         // dU = Kh DG
-        gemm(64, KD, VD, mat(U, VD), tr(DG, VD), dKh, KD, 1.f, false);                  // dKh = U DG^T
-        // dGamma_C[k] = sum_c G[k][c] gc[k] (X + Kh^T U)[k][c]: Y = X + Kh^T U in place of DG
-        for (int e = tid; e < SQ; e += BT) DG[e] = X[e];
+        gemm<64, VD, KD, false, false>(sc + S_W, KD, X, VD, U, VD, -1.f, true);     // U = Ut - W X
+        gemm<64, VD, KD, false, false>(sc + S_KH, KD, DG, VD, dU, VD, 1.f, false);  // dU = Kh DG
+        gemm<64, KD, VD, false, true>(U, VD, DG, VD, dKh, KD, 1.f, false);           // dKh = U DG^T
+        // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c]: Y = X + Kh^T U in place of DG
+        copy_f<SQ>(DG, X);
         __syncthreads();
-        gemm(KD, VD, 64, tr(sc + S_KH, KD), mat(U, VD), DG, VD, 1.f, true);
-        if (tid < KD) {
-            float s = 0.f;
-            for (int cc = 0; cc < VD; ++cc) s = fmaf(G[tid * VD + cc], DG[tid * VD + cc], s);
-            sc[S_DGC + tid] = s * sc[S_GC + tid];
-        }
-        __syncthreads();
-        gemm(64, KD, VD, mat(sc + S_DO, VD), tr(X, VD), dQt, KD, 1.f, false);          // dQt = dO X^T
-        gemm(64, 64, VD, mat(sc + S_DO, VD), tr(U, VD), dQK, 64, 1.f, false);          // dO U^T
-        for (int e = tid; e < CC; e += BT)
-            if ((e & 63) > (e >> 6)) dQK[e] = 0.f;                                      // lower incl. diagonal
-        __syncthreads();
-        gemm(64, VD, 64, tr(sc + S_QK, 64), mat(sc + S_DO, VD), dU, VD, 1.f, true);    // dU += QK^T dO
-        gemm(64, KD, 64, mat(dQK, 64), mat(sc + S_KH, KD), dQt, KD, 1.f, true);         // dQt += dQK Kh
-        gemm(64, KD, 64, tr(dQK, 64), mat(sc + S_QT, KD), dKh, KD, 1.f, true);          // dKh += dQK^T Qt
-        gemm(64, KD, VD, mat(dU, VD), tr(X, VD), dW, KD, -1.f, false);                  // dW = -dU X^T
-        gemm(64, 64, KD, mat(dW, KD), tr(sc + S_BKT, KD), dT, 64, 1.f, false);          // dT = dW (bKt)^T
-        gemm(64, 64, VD, mat(dU, VD), tr(sc + S_BV, VD), dT, 64, 1.f, true);            //    + dU (bV)^T
-        gemm(64, KD, 64, tr(sc + S_T, 64), mat(dW, KD), sc + S_DBKT, KD, 1.f, false);   // d(bKt) = T^T dW
-        gemm(64, VD, 64, tr(sc + S_T, 64), mat(dU, VD), sc + S_DBV, VD, 1.f, false);    // d(bV) = T^T dU
-        // dM = strictly_lower(-T^T dT T^T)
-        gemm(64, 64, 64, tr(sc + S_T, 64), mat(dT, 64), sc + S_T64, 64, 1.f, false);
-        gemm(64, 64, 64, mat(sc + S_T64, 64), tr(sc + S_T, 64), dM, 64, -1.f, false);
-        for (int e = tid; e < CC; e += BT)
-            if ((e & 63) >= (e >> 6)) dM[e] = 0.f;
-        __syncthreads();
-        // dKt = beta (d(bKt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(bV)
-        gemm(64, KD, 64, mat(dM, 64), mat(sc + S_KH, KD), dKt, KD, 1.f, false);
-        gemm(64, KD, 64, tr(dM, 64), mat(sc + S_BKT, KD), dKh, KD, 1.f, true);
-        // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S)
-        if (tid < 64) {
-            const int r = tid;
-            float s = 0.f;
-            for (int cc = 0; cc < KD; ++cc) s = fmaf(sc[S_DBKT + r * KD + cc], sc[S_KT + r * KD + cc], s);
-            for (int cc = 0; cc < VD; ++cc) s = fmaf(sc[S_DBV + r * VD + cc], sc[S_VF + r * VD + cc], s);
-            for (int i = 0; i < 64; ++i) s = fmaf(dM[r * 64 + i], sc[S_S + r * 64 + i], s);
-            sc[S_DBETA + r] = s;
-        }
-        for (int e = tid; e < CK; e += BT) {
-            const float b = sc[S_BT + (e >> 7)];
-            dKt[e] = b * (sc[S_DBKT + e] + dKt[e]);
-        }
-        __syncthreads();
-        // dGamma = Kt dKt - Kh dKh + Qt dQt (+ dGamma_C on the last row), dg its reverse cumulative sum;
-        // dq = scale E dQt, dk = E dKt + Ei dKh, dv = beta d(bV)
-        if (tid < KD) {
-            float acc = 0.f;
-            for (int r = 63; r >= 0; --r) {
-                const int e = r * KD + tid;
-                float dG = sc[S_KT + e] * dKt[e] - sc[S_KH + e] * dKh[e] + sc[S_QT + e] * dQt[e];
-                if (r == L - 1) dG += sc[S_DGC + tid];
-                acc += dG;
-                if (r < L) dg[(static_cast<size_t>(t0 + r) * H + h) * KD + tid] = acc;
+        gemm<KD, VD, 64, true, false>(sc + S_KH, KD, U, VD, DG, VD, 1.f, true);
+        {   // a warp per 16 rows k, 4 columns a lane, then a warp sum per row
+            float4 gv[16], yv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int e = (warp_id() * 16 + j) * VD + 4 * (tid & 31);
+                gv[j] = ld4(G + e);
+                yv[j] = ld4(DG + e);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float sum = warp_sum(dot4(gv[j], yv[j]));
+                const int kr = warp_id() * 16 + j;
+                if ((tid & 31) == 0) sc[S_DGC + kr] = sum * sc[S_GC + kr];
             }
         }
-        for (int e = tid; e < CK; e += BT) {
-            const int r = e >> 7, cc = e & 127;
+        __syncthreads();
+        gemm<64, KD, VD, false, true>(sc + S_DO, VD, X, VD, dQt, KD, 1.f, false);    // dQt = dO X^T
+        gemm<64, 64, VD, false, true>(sc + S_DO, VD, U, VD, dQK, 64, 1.f, false);    // dO U^T
+        {   // lower incl. diagonal
+            float4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = ld4(dQK + 4 * (tid + i * BT));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = 4 * (tid + i * BT), r = e >> 6, cc = e & 63;
+                st4(dQK + e, make_float4(cc + 0 <= r ? v[i].x : 0.f, cc + 1 <= r ? v[i].y : 0.f,
+                                         cc + 2 <= r ? v[i].z : 0.f, cc + 3 <= r ? v[i].w : 0.f));
+            }
+        }
+        __syncthreads();
+        gemm<64, VD, 64, true, false>(sc + S_QK, 64, sc + S_DO, VD, dU, VD, 1.f, true);   // dU += QK^T dO
+        gemm<64, KD, 64, false, false>(dQK, 64, sc + S_KH, KD, dQt, KD, 1.f, true);       // dQt += dQK Kh
+        gemm<64, KD, 64, true, false>(dQK, 64, sc + S_QT, KD, dKh, KD, 1.f, true);        // dKh += dQK^T Qt
+        gemm<64, KD, VD, false, true>(dU, VD, X, VD, dW, KD, -1.f, false);                // dW = -dU X^T
+        gemm<64, 64, KD, false, true>(dW, KD, sc + S_BKT, KD, dT, 64, 1.f, false);        // dT = dW (bKt)^T
+        gemm<64, 64, VD, false, true>(dU, VD, sc + S_BV, VD, dT, 64, 1.f, true);          //    + dU (bV)^T
+        gemm<64, KD, 64, true, false>(sc + S_T, 64, dW, KD, sc + S_DBKT, KD, 1.f, false); // d(bKt) = T^T dW
+        gemm<64, VD, 64, true, false>(sc + S_T, 64, dU, VD, sc + S_DBV, VD, 1.f, false);  // d(bV) = T^T dU
+        // dM = strictly_lower(-T^T dT T^T)
+        gemm<64, 64, 64, true, false>(sc + S_T, 64, dT, 64, sc + S_T64, 64, 1.f, false);
+        gemm<64, 64, 64, false, true>(sc + S_T64, 64, sc + S_T, 64, dM, 64, -1.f, false);
+        {
+            float4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = ld4(dM + 4 * (tid + i * BT));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = 4 * (tid + i * BT), r = e >> 6, cc = e & 63;
+                st4(dM + e, make_float4(cc + 0 < r ? v[i].x : 0.f, cc + 1 < r ? v[i].y : 0.f, cc + 2 < r ? v[i].z : 0.f,
+                                        cc + 3 < r ? v[i].w : 0.f));
+            }
+        }
+        __syncthreads();
+        // dKt = beta (d(bKt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(bV)
+        gemm<64, KD, 64, false, false>(dM, 64, sc + S_KH, KD, dKt, KD, 1.f, false);
+        gemm<64, KD, 64, true, false>(dM, 64, sc + S_BKT, KD, dKh, KD, 1.f, true);
+        // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S): a warp per 8 rows, then a warp sum
+        {
+            const int ln = tid & 31;
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j) {
+                const int r = warp_id() * 8 + j;
+                const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = ld4(sc + S_KT + r * KD + 4 * ln);
+                const float4 cv = ld4(sc + S_DBV + r * VD + 4 * ln), d = ld4(sc + S_VF + r * VD + 4 * ln);
+                const float2 m = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
+                const float2 sv = *reinterpret_cast<const float2 *>(sc + S_S + r * 64 + 2 * ln);
+                const float sum = warp_sum(dot4(a, b) + dot4(cv, d) + m.x * sv.x + m.y * sv.y);
+                if (ln == 0) sc[S_DBETA + r] = sum;
+            }
+        }
+        {
+            float4 a[8], b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = 4 * (tid + i * BT);
+                a[i] = ld4(sc + S_DBKT + e);
+                b[i] = ld4(dKt + e);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = 4 * (tid + i * BT);
+                st4(dKt + e, scl4(sc[S_BT + (e >> 7)], add4(a[i], b[i])));
+            }
+        }
+        __syncthreads();
+        // dGamma = Kt dKt - Kh dKh + Qt dQt (+ dGamma_C on the last row), dg its reverse cumulative sum:
+        // each thread holds rows 8 rg .. 8 rg + 7 of channels 4 cq .. 4 cq + 3, sums them from the bottom,
+        // and adds the totals of the row groups below (met in shared memory)
+        {
+            extern __shared__ __align__(16) float bsm[];
+            const int cq = tid & 31, rg = tid >> 5;
+            float4 suf[8];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float4 a[4], b[4], cv[4], d[4], e2[4], f[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = (rg * 8 + half * 4 + j) * KD + 4 * cq;
+                    a[j] = ld4(sc + S_KT + e);
+                    b[j] = ld4(dKt + e);
+                    cv[j] = ld4(sc + S_KH + e);
+                    d[j] = ld4(dKh + e);
+                    e2[j] = ld4(sc + S_QT + e);
+                    f[j] = ld4(dQt + e);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 kk = mul4(a[j], b[j]), hh = mul4(cv[j], d[j]), qq = mul4(e2[j], f[j]);
+                    suf[half * 4 + j] = make_float4(kk.x - hh.x + qq.x, kk.y - hh.y + qq.y, kk.z - hh.z + qq.z,
+                                                    kk.w - hh.w + qq.w);
+                }
+            }
+            if (L - 1 >= rg * 8 && L - 1 < rg * 8 + 8) {
+                const float4 dgc = ld4(sc + S_DGC + 4 * cq);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (rg * 8 + j == L - 1) suf[j] = add4(suf[j], dgc);
+            }
+#pragma unroll
+            for (int j = 6; j >= 0; --j) suf[j] = add4(suf[j], suf[j + 1]);
+            float4 *const tot = reinterpret_cast<float4 *>(bsm);   // [row group][channel quad]
+            tot[rg * 32 + cq] = suf[0];
+            __syncthreads();
+            float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int g2 = 1; g2 < 8; ++g2) {
+                const float4 t = tot[g2 * 32 + cq];
+                if (g2 > rg) off = add4(off, t);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = rg * 8 + j;
+                if (r < L) st4(dg + (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq, add4(suf[j], off));
+            }
+        }
+        // dq = scale E dQt, dk = E dKt + Ei dKh, dv = beta d(bV)
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+            const int e = 4 * (tid + i * BT), r = e >> 7, cc = e & 127;
             if (r < L) {
+                const float4 ex = ld4(sc + S_E + e), exi = ld4(sc + S_EI + e);
+                const float4 a = ld4(dQt + e), b = ld4(dKt + e), d = ld4(dKh + e), dvv = ld4(sc + S_DBV + e);
                 const size_t o = (static_cast<size_t>(t0 + r) * H + h) * KD + cc;
-                dq[o] = scale * sc[S_E + e] * dQt[e];
-                dk[o] = sc[S_E + e] * dKt[e] + sc[S_EI + e] * dKh[e];
-                dv[o] = sc[S_BT + r] * sc[S_DBV + e];
+                st4(dq + o, scl4(scale, mul4(ex, a)));
+                st4(dk + o, add4(mul4(ex, b), mul4(exi, d)));
+                st4(dv + o, scl4(sc[S_BT + r], dvv));
             }
         }
         for (int r = tid; r < L; r += BT) dbeta[static_cast<size_t>(t0 + r) * H + h] = sc[S_DBETA + r];
