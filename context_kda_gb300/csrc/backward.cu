@@ -383,7 +383,55 @@ __device__ void load_do(float *sc, int t0, int L, int h, int H, const uint16_t *
     __syncthreads();
 }
 
-// dst = Diag(d) src for a 128 x 128 state (d one value per row), every thread's loads first
+// The chains carry the state (or its gradient) in column slices: every product of a chain step
+// multiplies into the state's columns, so the NS slices of SW columns are independent chains.
+constexpr int NS = 2, SW = VD / NS;
+
+// dst = src on columns c0 .. c0 + SW of a 128-row state (row stride VD), every thread's loads first
+__device__ __forceinline__ void copy_slice(float *dst, const float *src, int c0)
+{
+    constexpr int P = KD * SW / 4 / BT;
+    float4 v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = threadIdx.x + i * BT;
+        v[i] = ld4(src + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)));
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = threadIdx.x + i * BT;
+        st4(dst + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)), v[i]);
+    }
+}
+
+// dst = 0 on columns c0 .. c0 + SW of a 128-row state
+__device__ __forceinline__ void zero_slice(float *dst, int c0)
+{
+#pragma unroll
+    for (int i = 0; i < KD * SW / 4 / BT; ++i) {
+        const int e = threadIdx.x + i * BT;
+        st4(dst + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)), make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+}
+
+// dst = Diag(d) src on columns c0 .. c0 + SW of a 128-row state (d one value per row)
+__device__ __forceinline__ void scale_slice(float *dst, const float *src, const float *d, int c0)
+{
+    constexpr int P = KD * SW / 4 / BT;
+    float4 v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = threadIdx.x + i * BT;
+        v[i] = ld4(src + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)));
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = threadIdx.x + i * BT, r = e / (SW / 4);
+        st4(dst + r * VD + c0 + 4 * (e % (SW / 4)), scl4(d[r], v[i]));
+    }
+}
+
+// dst = Diag(d) src for a whole 128 x 128 state, every thread's loads first
 __device__ __forceinline__ void scale_rows(float *dst, const float *src, const float *d)
 {
     constexpr int P = SQ / 4 / BT;
@@ -397,29 +445,64 @@ __device__ __forceinline__ void scale_rows(float *dst, const float *src, const f
     }
 }
 
-// X <- Dc (X + Kh^T (Ut - W X)), the chunk's terms at tm
-__device__ void forward_step(float *sc, const float *tm)
+// The chunk's output gradient rows, columns c0 .. c0 + SW, into scratch (zero past L), bf16 -> fp32.
+__device__ void load_do_slice(float *sc, int t0, int L, int h, int H, const uint16_t *dout, int c0)
 {
-    float *X = sc + S_X, *U = sc + S_U;
-    copy_f<CK>(U, tm + TM_UT);
-    gemm<64, VD, KD, false, false>(tm + TM_W, KD, X, VD, U, VD, -1.f, true);
-    gemm<KD, VD, 64, true, false>(tm + TM_KH, KD, U, VD, X, VD, 1.f, true);
-    scale_rows(X, X, tm + TM_GC);
+    constexpr int P = 64 * SW / 8 / BT;
+    uint4 w[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = threadIdx.x + i * BT, r = e / (SW / 8), c8 = c0 + 8 * (e % (SW / 8));
+        w[i] = r < L ? *reinterpret_cast<const uint4 *>(dout + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int e = threadIdx.x + i * BT, r = e / (SW / 8), c8 = c0 + 8 * (e % (SW / 8));
+        float x[8];
+        bf8(w[i], x);
+        st4(sc + S_DO + r * VD + c8, make_float4(x[0], x[1], x[2], x[3]));
+        st4(sc + S_DO + r * VD + c8 + 4, make_float4(x[4], x[5], x[6], x[7]));
+    }
     __syncthreads();
 }
 
-// G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start), the chunk's
-// terms at tm
-__device__ void reverse_step(float *sc, const float *tm)
+// X <- Dc (X + Kh^T (Ut - W X)) on columns c0 .. c0 + SW, the chunk's terms at tm
+__device__ void forward_step(float *sc, const float *tm, int c0)
+{
+    float *X = sc + S_X, *U = sc + S_U;
+    {   // U = Ut on the slice (64 rows)
+        constexpr int P = 64 * SW / 4 / BT;
+        float4 v[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            const int e = threadIdx.x + i * BT;
+            v[i] = ld4(tm + TM_UT + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)));
+        }
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            const int e = threadIdx.x + i * BT;
+            st4(U + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)), v[i]);
+        }
+    }
+    gemm<64, SW, KD, false, false>(tm + TM_W, KD, X + c0, VD, U + c0, VD, -1.f, true);
+    gemm<KD, SW, 64, true, false>(tm + TM_KH, KD, U + c0, VD, X + c0, VD, 1.f, true);
+    scale_slice(X, X, tm + TM_GC, c0);
+    __syncthreads();
+}
+
+// G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start), on
+// columns c0 .. c0 + SW, the chunk's terms at tm
+__device__ void reverse_step(float *sc, const float *tm, int c0)
 {
     float *G = sc + S_G, *DG = sc + S_Y, *dU = sc + S_DU;
-    scale_rows(DG, G, tm + TM_GC);
+    scale_slice(DG, G, tm + TM_GC, c0);
     __syncthreads();
-    gemm<64, VD, KD, false, false>(tm + TM_KH, KD, DG, VD, dU, VD, 1.f, false);
-    gemm<64, VD, 64, true, false>(tm + TM_QK, 64, sc + S_DO, VD, dU, VD, 1.f, true);
-    copy_f<SQ>(G, DG);
-    gemm<KD, VD, 64, true, false>(tm + TM_QT, KD, sc + S_DO, VD, G, VD, 1.f, true);
-    gemm<KD, VD, 64, true, false>(tm + TM_W, KD, dU, VD, G, VD, -1.f, true);
+    gemm<64, SW, KD, false, false>(tm + TM_KH, KD, DG + c0, VD, dU + c0, VD, 1.f, false);
+    gemm<64, SW, 64, true, false>(tm + TM_QK, 64, sc + S_DO + c0, VD, dU + c0, VD, 1.f, true);
+    copy_slice(G, DG, c0);
+    gemm<KD, SW, 64, true, false>(tm + TM_QT, KD, sc + S_DO + c0, VD, G + c0, VD, 1.f, true);
+    gemm<KD, SW, 64, true, false>(tm + TM_W, KD, dU + c0, VD, G + c0, VD, -1.f, true);
 }
 
 // Plan helpers
@@ -473,9 +556,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_states(const int32_t *plan, PlanSig
     BWD_PLAN_CHECK();
     const PlanView pv{plan};
     float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
-    const int n_items = pv.n_pieces() * H;
+    const int n_items = pv.n_pieces() * H * NS;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int p = item / H, h = item % H;
+        const int ph = item / NS, c0 = (item % NS) * SW;
+        const int p = ph / H, h = ph % H;
         const PieceInfo pi = piece_info(pv, p);
         const float *src = nullptr;
         if (pi.flags & KDA_PIECE_FIRST) {
@@ -483,14 +567,13 @@ __global__ void __launch_bounds__(BT, 1) bwd_states(const int32_t *plan, PlanSig
         } else {
             src = S_in + (static_cast<size_t>(pi.seg) * H + h) * SQ;
         }
-        if (src) copy_f<SQ>(sc + S_X, src);
-        else
-            for (int i = 0; i < SQ / 4 / BT; ++i) st4(sc + S_X + 4 * (threadIdx.x + i * BT), make_float4(0.f, 0.f, 0.f, 0.f));
+        if (src) copy_slice(sc + S_X, src, c0);
+        else zero_slice(sc + S_X, c0);
         __syncthreads();
         for (int ci = 0; ci < pi.nch; ++ci) {
             const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
-            copy_f<SQ>(xs + unit * SQ, sc + S_X);
-            forward_step(sc, terms + unit * TERMS_FLOATS);
+            copy_slice(xs + unit * SQ, sc + S_X, c0);
+            forward_step(sc, terms + unit * TERMS_FLOATS, c0);
         }
         __syncthreads();
     }
@@ -508,9 +591,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_reverse(const int32_t *plan, PlanSi
     BWD_PLAN_CHECK();
     const PlanView pv{plan};
     float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
-    const int n_items = pv.n_pieces() * H;
+    const int n_items = pv.n_pieces() * H * NS;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int p = item / H, h = item % H;
+        const int ph = item / NS, c0 = (item % NS) * SW;
+        const int p = ph / H, h = ph % H;
         const PieceInfo pi = piece_info(pv, p);
         if (!TRUE_PASS && !(pi.flags & KDA_PIECE_CONT)) continue;
         const float *src = nullptr;
@@ -521,22 +605,21 @@ __global__ void __launch_bounds__(BT, 1) bwd_reverse(const int32_t *plan, PlanSi
                 src = G_end + (static_cast<size_t>(pi.seg) * H + h) * SQ;
             }
         }
-        if (src) copy_f<SQ>(sc + S_G, src);
-        else
-            for (int i = 0; i < SQ / 4 / BT; ++i) st4(sc + S_G + 4 * (threadIdx.x + i * BT), make_float4(0.f, 0.f, 0.f, 0.f));
+        if (src) copy_slice(sc + S_G, src, c0);
+        else zero_slice(sc + S_G, c0);
         __syncthreads();
         for (int ci = pi.nch - 1; ci >= 0; --ci) {
             const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
-            if (TRUE_PASS) copy_f<SQ>(gs + unit * SQ, sc + S_G);
+            if (TRUE_PASS) copy_slice(gs + unit * SQ, sc + S_G, c0);
             const int t0 = pi.start + ci * CH, L = min(CH, pi.len - ci * CH);
-            load_do(sc, t0, L, h, H, dout);
-            reverse_step(sc, terms + unit * TERMS_FLOATS);
+            load_do_slice(sc, t0, L, h, H, dout, c0);
+            reverse_step(sc, terms + unit * TERMS_FLOATS, c0);
         }
         __syncthreads();
         float *dst = nullptr;
         if (!TRUE_PASS) dst = Qd + (static_cast<size_t>(pi.seg) * H + h) * SQ;
         else if ((pi.flags & KDA_PIECE_FIRST) && dh0) dst = dh0 + (static_cast<size_t>(pi.seq) * H + h) * SQ;
-        if (dst) copy_f<SQ>(dst, sc + S_G);
+        if (dst) copy_slice(dst, sc + S_G, c0);
         __syncthreads();
     }
 }
