@@ -32,9 +32,12 @@
 // private scratch area in global memory (L2-resident) and runs every product by staging both
 // operands in shared memory, which keeps every step a literal transcription of the formulas above.
 #include "kda_internal.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
+
+using namespace tc;
 
 constexpr int BT = 256;                      // threads per CTA
 constexpr int CK = 64 * KD;                  // a 64 x 128 chunk matrix
@@ -62,9 +65,7 @@ enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * C
              TERMS_FLOATS = TM_GC + KD };
 
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
-constexpr int SM_PAD = 4;
-constexpr int SM_LD = 128 + SM_PAD;
-constexpr size_t BWD_SMEM = 2ull * 128 * SM_LD * sizeof(float);
+constexpr size_t BWD_SMEM = 4ull * 32768 + 1024;   // the operand tiles of one product, aligned to 1024 bytes
 
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 __device__ __forceinline__ int warp_id() { return static_cast<int>(threadIdx.x) >> 5; }
@@ -93,111 +94,137 @@ __device__ __forceinline__ void copy_f(float *dst, const float *src)
     for (int i = 0; i < P; ++i) st4(dst + 4 * (threadIdx.x + i * BT), v[i]);
 }
 
-// Micro-tile product over operands already in shared memory: As[k][m] (M x K), Bs[k][n] (K x N);
-// thread (ty, tx) of a 16 x 16 grid computes rows ty*MR .. +MR and columns tx*NR .. +NR.
-template <int MR, int NR, int K>
-__device__ __forceinline__ void gemm_core(const float *As, const float *Bs, float *C, int ldc, float alpha, bool acc)
+// Tensor-core state of a CTA: the accumulator's TMEM columns, the products' mbarrier and the parity
+// of its next phase, and a flag raised when a bounded wait gave up (every later product of the CTA
+// is then skipped, and the kernel reports KDA_ERR_TIMEOUT).
+__shared__ __align__(8) uint64_t s_tc_bar;
+__shared__ uint32_t s_tc_tmem, s_tc_phase, s_tc_fail;
+constexpr uint32_t TC_COLS = 128;
+
+__device__ void tc_begin()
 {
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    float c[MR][NR];
-#pragma unroll
-    for (int i = 0; i < MR; ++i)
-#pragma unroll
-        for (int j = 0; j < NR; ++j) c[i][j] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[MR], b[NR];
-#pragma unroll
-        for (int i = 0; i < MR; i += 4) {
-            const float4 v = ld4(As + k * SM_LD + ty * MR + i);
-            a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
-        }
-#pragma unroll
-        for (int j = 0; j < NR; j += 4) {
-            const float4 v = ld4(Bs + k * SM_LD + tx * NR + j);
-            b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
-        }
-#pragma unroll
-        for (int i = 0; i < MR; ++i)
-#pragma unroll
-            for (int j = 0; j < NR; ++j) c[i][j] = fmaf(a[i], b[j], c[i][j]);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&s_tc_bar), 1);
+        s_tc_phase = 0;
+        s_tc_fail = 0;
     }
-#pragma unroll
-    for (int i = 0; i < MR; ++i)
-#pragma unroll
-        for (int j = 0; j < NR; j += 4) {
-            float *d = C + (ty * MR + i) * ldc + tx * NR + j;
-            const float4 old = acc ? ld4(d) : make_float4(0.f, 0.f, 0.f, 0.f);
-            st4(d, make_float4(alpha * c[i][j] + old.x, alpha * c[i][j + 1] + old.y, alpha * c[i][j + 2] + old.z,
-                               alpha * c[i][j + 3] + old.w));
-        }
+    if (threadIdx.x < 32) tmem_alloc(smem_u32(&s_tc_tmem), TC_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+}
+
+__device__ void tc_end()
+{
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (threadIdx.x == 0 && s_tc_fail) record_status(&g_bwd_status, KDA_ERR_TIMEOUT);
+    if (threadIdx.x < 32) tmem_dealloc(s_tc_tmem, TC_COLS);
+}
+
+// The operand tiles in dynamic shared memory (1024-byte aligned): A hi | lo (128 x K bf16 each), then
+// B hi | lo (N x K bf16 each).
+__device__ __forceinline__ unsigned char *tc_tiles()
+{
+    extern __shared__ __align__(16) unsigned char bsm_raw[];
+    return bsm_raw + ((1024u - (smem_u32(bsm_raw) & 1023u)) & 1023u);
 }
 
 // C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc) for an M x N result and K-long sums
 // (M, N, K in {64, 128}), by all threads of the CTA, with A(m, k) = TA ? a[k * lda + m] : a[m * lda + k]
-// and B(k, n) = TB ? b[n * ldb + k] : b[k * ldb + n] (16-byte aligned, leading dimensions multiples of 4).
-// Every thread issues all its 16-byte operand loads at once, then both operands are stored k-major
-// in shared memory (a transposed operand by 16 rows x 2 vectors a warp, so that the scattered stores
-// fall in distinct banks), then each thread accumulates its micro-tile over the whole K.
+// and B(k, n) = TB ? b[n * ldb + k] : b[k * ldb + n] (FP32, 16-byte aligned, leading dimensions
+// multiples of 8).  Each operand is copied as it lies (rows of its contiguous index) into the no-swizzle
+// canonical layout as a bf16 hi/lo pair, and read by the tensor core K-major or MN-major accordingly, so
+// nothing is transposed on the way; the product is the 3-term split hi*hi + hi*lo + lo*hi (~2^-16
+// relative, FP32 accumulation in TMEM) on tcgen05 with M = 128 (a 64-row A fills half the lanes, the
+// rest are never read).  The staging lanes take consecutive rows of one 8-column piece, so their
+// 16-byte stores land in distinct banks.
 template <int M, int N, int K, bool TA, bool TB>
 __device__ void gemm(const float *a, int lda, const float *b, int ldb, float *C, int ldc, float alpha, bool acc)
 {
-    extern __shared__ __align__(16) float bsm[];
-    float *As = bsm, *Bs = bsm + 128 * SM_LD;
+    static_assert((M == 64 || M == 128) && (N == 64 || N == 128) && (K == 64 || K == 128), "shapes");
+    if (s_tc_fail) return;   // uniform: written before the previous product's closing barrier
     const int tid = threadIdx.x;
-    constexpr int NA = K * M / 4 / BT, NB = K * N / 4 / BT;
-    constexpr int LM = ilog2(M), LN = ilog2(N), LK = ilog2(K);
-    float4 va[NA], vb[NB];
+    // tiles: A's rows are its contiguous index's partner (k when TA, else m), B's likewise (n when TB)
+    constexpr int RA = TA ? K : M, CA = TA ? M : K, RB = TB ? N : K, CB = TB ? K : N;
+    constexpr uint32_t CS_A = TA ? K * 16 : 128 * 16, CS_B = RB * 16;
+    constexpr uint32_t A_BYTES = 128 * K * 2, B_BYTES = N * K * 2;
+    constexpr int PA = RA * CA / 8 / BT, PB = RB * CB / 8 / BT;
+    unsigned char *const a_hi = tc_tiles(), *const a_lo = a_hi + A_BYTES;
+    unsigned char *const b_hi = a_lo + A_BYTES, *const b_lo = b_hi + B_BYTES;
+    float4 va[2 * PA], vb[2 * PB];
 #pragma unroll
-    for (int i = 0; i < NA; ++i) {
-        const int e = tid + i * BT;
-        if (TA) {
-            va[i] = ld4(a + (e >> (LM - 2)) * lda + ((e & (M / 4 - 1)) << 2));
-        } else {
-            const int rest = e >> 4;
-            va[i] = ld4(a + (((rest >> (LK - 2)) << 4) | (e & 15)) * lda + ((rest & (K / 4 - 1)) << 2));
-        }
+    for (int i = 0; i < PA; ++i) {
+        const int pc = tid + i * BT, r = pc % RA, c8 = (pc / RA) * 8;
+        va[2 * i] = ld4(a + r * lda + c8);
+        va[2 * i + 1] = ld4(a + r * lda + c8 + 4);
     }
 #pragma unroll
-    for (int i = 0; i < NB; ++i) {
-        const int e = tid + i * BT;
-        if (TB) {
-            const int rest = e >> 4;
-            vb[i] = ld4(b + (((rest >> (LK - 2)) << 4) | (e & 15)) * ldb + ((rest & (K / 4 - 1)) << 2));
-        } else {
-            vb[i] = ld4(b + (e >> (LN - 2)) * ldb + ((e & (N / 4 - 1)) << 2));
-        }
+    for (int i = 0; i < PB; ++i) {
+        const int pc = tid + i * BT, r = pc % RB, c8 = (pc / RB) * 8;
+        vb[2 * i] = ld4(b + r * ldb + c8);
+        vb[2 * i + 1] = ld4(b + r * ldb + c8 + 4);
     }
-    __syncthreads();   // the operand buffers are free
+    auto put = [](unsigned char *hi, unsigned char *lo, uint32_t off, float4 x0, float4 x1) {
+        uint32_t h[4], l[4];
+        split_bf16x2(x0.x, x0.y, h[0], l[0]);
+        split_bf16x2(x0.z, x0.w, h[1], l[1]);
+        split_bf16x2(x1.x, x1.y, h[2], l[2]);
+        split_bf16x2(x1.z, x1.w, h[3], l[3]);
+        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    };
 #pragma unroll
-    for (int i = 0; i < NA; ++i) {
-        const int e = tid + i * BT;
-        if (TA) {
-            st4(As + (e >> (LM - 2)) * SM_LD + ((e & (M / 4 - 1)) << 2), va[i]);
-        } else {
-            const int rest = e >> 4, k4 = (rest & (K / 4 - 1)) << 2, m = ((rest >> (LK - 2)) << 4) | (e & 15);
-            As[(k4 + 0) * SM_LD + m] = va[i].x;
-            As[(k4 + 1) * SM_LD + m] = va[i].y;
-            As[(k4 + 2) * SM_LD + m] = va[i].z;
-            As[(k4 + 3) * SM_LD + m] = va[i].w;
-        }
+    for (int i = 0; i < PA; ++i) {
+        const int pc = tid + i * BT, r = pc % RA, c8 = (pc / RA) * 8;
+        put(a_hi, a_lo, cm_off(r, c8, CS_A), va[2 * i], va[2 * i + 1]);
     }
 #pragma unroll
-    for (int i = 0; i < NB; ++i) {
-        const int e = tid + i * BT;
-        if (TB) {
-            const int rest = e >> 4, k4 = (rest & (K / 4 - 1)) << 2, n = ((rest >> (LK - 2)) << 4) | (e & 15);
-            Bs[(k4 + 0) * SM_LD + n] = vb[i].x;
-            Bs[(k4 + 1) * SM_LD + n] = vb[i].y;
-            Bs[(k4 + 2) * SM_LD + n] = vb[i].z;
-            Bs[(k4 + 3) * SM_LD + n] = vb[i].w;
-        } else {
-            st4(Bs + (e >> (LN - 2)) * SM_LD + ((e & (N / 4 - 1)) << 2), vb[i]);
-        }
+    for (int i = 0; i < PB; ++i) {
+        const int pc = tid + i * BT, r = pc % RB, c8 = (pc / RB) * 8;
+        put(b_hi, b_lo, cm_off(r, c8, CS_B), vb[2 * i], vb[2 * i + 1]);
     }
+    fence_async_smem();
     __syncthreads();
-    gemm_core<M / 16, N / 16, K>(As, Bs, C, ldc, alpha, acc);
+    fence_after();
+    const uint32_t ph = s_tc_phase, tmem = s_tc_tmem, bar = smem_u32(&s_tc_bar);
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16(128, N, TA ? 1 : 0, TB ? 0 : 1);
+        const uint32_t ah[3] = {smem_u32(a_hi), smem_u32(a_hi), smem_u32(a_lo)};
+        const uint32_t bh[3] = {smem_u32(b_hi), smem_u32(b_lo), smem_u32(b_hi)};
+#pragma unroll
+        for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+            for (int kk = 0; kk < K / 16; ++kk) {
+                const uint64_t ad = TA ? sdesc(ah[ps] + kk * 256, 128, CS_A) : sdesc(ah[ps] + kk * 2 * CS_A, CS_A, 128);
+                const uint64_t bd = TB ? sdesc(bh[ps] + kk * 2 * CS_B, CS_B, 128) : sdesc(bh[ps] + kk * 256, 128, CS_B);
+                mma_bf16(tmem, ad, bd, id, (ps | kk) != 0);
+            }
+        commit(bar);
+    }
+    const bool ok = mbar_wait_warp(bar, ph);
+    fence_after();
+    const int warp = tid >> 5, quad = warp & 3, hw = warp >> 2;
+    if (ok && quad * 32 < M) {   // row m = this thread's TMEM lane, columns hw * N/2 .. + N/2
+        const int m = quad * 32 + (tid & 31);
+#pragma unroll
+        for (int j0 = 0; j0 < N / 2; j0 += 32) {
+            float d[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + hw * (N / 2) + j0, d);
+            float *crow = C + m * ldc + hw * (N / 2) + j0;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 old = acc ? ld4(crow + 4 * q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                st4(crow + 4 * q4, make_float4(alpha * d[4 * q4] + old.x, alpha * d[4 * q4 + 1] + old.y,
+                                               alpha * d[4 * q4 + 2] + old.z, alpha * d[4 * q4 + 3] + old.w));
+            }
+        }
+    }
+    if (!ok) s_tc_fail = 1;
+    fence_before();
     __syncthreads();
+    if (tid == 0) s_tc_phase = ph ^ 1u;
 }
 
 // 8 bf16 (one 16-byte word) as fp32
@@ -531,6 +558,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
                                                 const float *beta, float scale, float *terms, float *scratch)
 {
     BWD_PLAN_CHECK();
+    tc_begin();
     const PlanView pv{plan};
     float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
     const int n_chunks = pv.n_chunks();
@@ -547,6 +575,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
         if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
         __syncthreads();
     }
+    tc_end();
 }
 
 // 1. every piece from its true incoming state, recording X_c = xs[h][c] for each of its chunks
@@ -554,6 +583,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_states(const int32_t *plan, PlanSig
                                                  const float *h0, const float *S_in, float *xs, float *scratch)
 {
     BWD_PLAN_CHECK();
+    tc_begin();
     const PlanView pv{plan};
     float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
     const int n_items = pv.n_pieces() * H * NS;
@@ -577,6 +607,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_states(const int32_t *plan, PlanSig
         }
         __syncthreads();
     }
+    tc_end();
 }
 
 // 2 (LOCAL) / 4 (TRUE). Pieces backwards over their chunks.  LOCAL: pieces that continue a sequence,
@@ -589,6 +620,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_reverse(const int32_t *plan, PlanSi
                                                   float *Qd, float *gs, float *dh0, float *scratch)
 {
     BWD_PLAN_CHECK();
+    tc_begin();
     const PlanView pv{plan};
     float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
     const int n_items = pv.n_pieces() * H * NS;
@@ -622,6 +654,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_reverse(const int32_t *plan, PlanSi
         if (dst) copy_slice(dst, sc + S_G, c0);
         __syncthreads();
     }
+    tc_end();
 }
 
 // 3. The following summaries, per (head, 32-column slice), last segment first:
@@ -702,6 +735,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                                                 float *dg, float *dbeta, float *scratch)
 {
     BWD_PLAN_CHECK();
+    tc_begin();
     const PlanView pv{plan};
     float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
     const int n_chunks = pv.n_chunks();
@@ -880,6 +914,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         for (int r = tid; r < L; r += BT) dbeta[static_cast<size_t>(t0 + r) * H + h] = sc[S_DBETA + r];
         __syncthreads();
     }
+    tc_end();
 }
 
 }  // namespace
