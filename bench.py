@@ -629,7 +629,7 @@ def time_backward(prob, stream, flush, steps=5, warmup=2):
     m = float(np.mean(ms))
     del ws, grads
     return {"ms_per_step": m, "tokens_per_s": T / (m / 1e3), "steps": steps, "warmup": warmup,
-            "note": "FP32 on the CUDA cores; includes the forward's local pass and composition"}
+            "note": "FP32 matrices, products on tcgen05 as a 3-term bf16 split; includes the forward's local pass and composition"}
 
 
 def scan_bytes(S, H):

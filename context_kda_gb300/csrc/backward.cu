@@ -28,9 +28,10 @@
 //     giving dh0 at a sequence start;
 //  5. every (chunk, head) in parallel: dq, dk, dv, dg, dbeta from (X_c, G_c, dO).
 //
-// This implementation computes in FP32 on the CUDA cores: each CTA keeps its chunk's matrices in a
-// private scratch area in global memory (L2-resident) and runs every product by staging both
-// operands in shared memory, which keeps every step a literal transcription of the formulas above.
+// Each CTA keeps its chunk's matrices in FP32 in a private scratch area in global memory and runs every
+// product on the tensor cores (both operands staged in shared memory as bf16 hi/lo pairs, a three-term
+// split accumulated in FP32 in TMEM), which keeps every step a literal transcription of the formulas
+// above.  The chains carry the state and its gradient in two 64-column slices per (piece, head).
 #include "kda_internal.cuh"
 #include "tc.cuh"
 

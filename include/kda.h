@@ -407,8 +407,10 @@ int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev, int32_t H
  * last segment first, giving each segment's end-state gradient; every piece
  * backwards from it, recording each chunk's end-state gradient and giving
  * dh0; and every (chunk, head) in parallel for dq, dk, dv, dg and dbeta.
- * Computed in FP32 on the CUDA cores.  Returns KDA_OK, KDA_ERR_INVALID_ARG,
- * KDA_ERR_WORKSPACE or KDA_ERR_CUDA.
+ * Matrices are kept in FP32; every product runs on the tensor cores as a
+ * three-term bf16 split (about 2^-16 relative, FP32 accumulation).  Returns
+ * KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_WORKSPACE or KDA_ERR_CUDA; a bounded
+ * wait that gave up is reported by kda_device_status() as KDA_ERR_TIMEOUT.
  */
 int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t H,
                            const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
