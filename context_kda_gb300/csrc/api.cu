@@ -231,6 +231,69 @@ bool encode_rows_3d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, uin
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Unique id of the calling thread's current context (driver entry points, looked up once).
+cudaError_t current_context_id(unsigned long long *id)
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    if (!get_current || !get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    if (!ctx) {   // nothing current yet on this thread: the runtime would use the primary context
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaSetDevice(dev);   // initialises and binds the primary context
+        if (e != cudaSuccess) return e;
+        if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+    }
+    if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
+
+// The dynamic shared-memory limit of a kernel, set once per (kernel, context): the attribute
+// belongs to the function in the current context, so after cudaDeviceReset (a new context id) it
+// is set again.
+cudaError_t set_dynamic_smem(const void *fn, int bytes)
+{
+    unsigned long long ctx = 0;
+    cudaError_t e = current_context_id(&ctx);
+    if (e != cudaSuccess) return e;
+    struct Done {
+        const void *fn;
+        unsigned long long ctx;
+        int bytes;
+    };
+    static std::mutex mu;
+    static Done done[64];
+    static int n_done = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_done; ++i)
+            if (done[i].fn == fn && done[i].ctx == ctx && done[i].bytes >= bytes) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    done[next] = Done{fn, ctx, bytes};
+    next = (next + 1) % 64;
+    if (n_done < 64) ++n_done;
+    return cudaSuccess;
+}
+
 int sm_count()
 {
     static int cached[64] = {0};

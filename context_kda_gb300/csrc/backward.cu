@@ -935,8 +935,7 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
     for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_states),
                     reinterpret_cast<const void *>(bwd_reverse<false>),
                     reinterpret_cast<const void *>(bwd_reverse<true>), reinterpret_cast<const void *>(bwd_grads)}) {
-        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(BWD_SMEM));
+        const cudaError_t e = set_dynamic_smem(fn, static_cast<int>(BWD_SMEM));
         if (e != cudaSuccess) return e;
     }
     bwd_terms<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, terms, scratch);

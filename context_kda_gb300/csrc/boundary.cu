@@ -443,27 +443,24 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
     if (per_head > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const long long n_units = per_head * H;
     const long long grid = std::min<long long>({n_units, static_cast<long long>(sm_count()), MAX_RUNS});
-    // CTA b starts at the unit boundary whose preceding cost is nearest to b/grid of the total
-    const long long w_head = pre.back();
-    const unsigned __int128 total = static_cast<unsigned __int128>(w_head) * static_cast<unsigned>(H);
-    auto cost_before = [&](long long u) {
-        return static_cast<unsigned __int128>(u / per_head) * static_cast<unsigned long long>(w_head) +
-               static_cast<unsigned long long>(pre[u % per_head]);
-    };
+    // CTA b starts at the unit boundary whose preceding cost is nearest to b/grid of the total: the
+    // head from one division, the unit within it from a search of the head's cumulative costs
+    const unsigned long long w_head = static_cast<unsigned long long>(pre.back());
+    const unsigned long long total = w_head * static_cast<unsigned long long>(H);
+    if (total / static_cast<unsigned long long>(H) != w_head || total > (1ull << 54)) return cudaErrorInvalidConfiguration;
     Runs runs{};
     long long prev = 0;
     for (long long b = 0; b < grid; ++b) {
         long long next = n_units;
         if (b + 1 < grid) {
-            const unsigned __int128 target = total * static_cast<unsigned long long>(b + 1) / static_cast<unsigned long long>(grid);
-            long long lo = prev, hi = n_units;   // first u in [prev, n_units] with cost_before(u) >= target
-            while (lo < hi) {
-                const long long mid = lo + (hi - lo) / 2;
-                if (cost_before(mid) >= target) hi = mid;
-                else lo = mid + 1;
-            }
-            if (lo > prev && target - cost_before(lo - 1) < cost_before(lo) - target) --lo;
-            next = lo;
+            const unsigned long long target = total * static_cast<unsigned long long>(b + 1) / static_cast<unsigned long long>(grid);
+            const long long h = static_cast<long long>(target / w_head);
+            const long long rem = static_cast<long long>(target - static_cast<unsigned long long>(h) * w_head);
+            // first unit boundary within head h at or past rem, or the nearer one before it
+            const long long i = std::lower_bound(pre.begin(), pre.end(), rem) - pre.begin();
+            next = std::min(n_units, h * per_head + i);
+            if (i > 0 && rem - pre[i - 1] < pre[i] - rem && next - 1 > prev) --next;
+            next = std::max(prev, next);
         }
         if (next - prev > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         const long long w = prev % per_head;
@@ -482,8 +479,8 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
     const int has_tq = q_rows >= TR ? 1 : 0;
     if (has_tq && !encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, TR))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(boundary_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_ALLOC));
+    cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(boundary_tc),
+                                       static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(boundary_tc, dim3(static_cast<unsigned>(grid)), dim3(256), SMEM_ALLOC, stream, plan_dev,
                             plan_sig(plan_host), H, runs, S_in, qhat, afin, o, final_state, to, tq, has_tq);

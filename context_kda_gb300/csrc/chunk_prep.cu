@@ -641,8 +641,8 @@ cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev,
         !encode_rows_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
         !encode_rows_3d(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, 32))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(chunk_prep_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_ALLOC));
+    cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(chunk_prep_tc),
+                                       static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     const long long grid = n_units < sm_count() ? n_units : sm_count();
     chunk_prep_tc<<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(plan_dev, plan_sig(plan_host), H, n_units,

@@ -503,8 +503,8 @@ cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int 
         if (!encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, CH))
             return cudaErrorInvalidValue;
     }
-    cudaError_t err = cudaFuncSetAttribute(chunk_state_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_ALLOC));
+    cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(chunk_state_tc<MODE>),
+                                       static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(chunk_state_tc<MODE>, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC,
                             stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq,

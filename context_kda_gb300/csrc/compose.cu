@@ -495,8 +495,8 @@ template <int MODE>
 cudaError_t launch_mode(const int32_t *plan_host, const int32_t *plan_dev, int H, int has_h0, int m, int G,
                         const float *A, const Maps &mp, cudaStream_t stream)
 {
-    cudaError_t err = cudaFuncSetAttribute(compose_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(SMEM_ALLOC));
+    cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(compose_tc<MODE>),
+                                       static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     const int per_head = MODE == MODE_TOTALS ? 8 * G : MODE == MODE_APPLY ? 4 * G : 4;
     return launch_dependent(compose_tc<MODE>, dim3(static_cast<unsigned>(H * per_head)), dim3(NT), SMEM_ALLOC,

@@ -92,6 +92,8 @@ void record_cuda_error(int err);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+cudaError_t current_context_id(unsigned long long *id);   // unique id of the current context
+cudaError_t set_dynamic_smem(const void *fn, int bytes);   // once per (kernel, context)
 
 // Each kernel file's device status word (KDA_ERR_TIMEOUT once a bounded wait of its kernel expired),
 // read and cleared; the device must be synchronised first.

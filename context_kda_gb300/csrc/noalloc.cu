@@ -32,39 +32,6 @@ std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 unsigned long long g_scratch_ctx[kMaxDevices] = {};   // id of the context the address belongs to
 
-// Unique id of the calling thread's current context (driver entry points, looked up once).
-cudaError_t current_context_id(unsigned long long *id)
-{
-    using GetCurrent = CUresult (*)(CUcontext *);
-    using GetId = CUresult (*)(CUcontext, unsigned long long *);
-    static GetCurrent get_current = nullptr;
-    static GetId get_id = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<GetCurrent>(p);
-        p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<GetId>(p);
-    });
-    if (!get_current || !get_id) return cudaErrorNotSupported;
-    CUcontext ctx = nullptr;
-    if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
-    if (!ctx) {   // nothing current yet on this thread: the runtime would use the primary context
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaSetDevice(dev);   // initialises and binds the primary context
-        if (e != cudaSuccess) return e;
-        if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
-    }
-    if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
-    return cudaSuccess;
-}
-
 // Device address of g_noalloc_scratch in the current context (looked up once per device and context).
 cudaError_t scratch_address(void **out)
 {
@@ -73,7 +40,7 @@ cudaError_t scratch_address(void **out)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     unsigned long long ctx = 0;
-    e = current_context_id(&ctx);
+    e = kda::current_context_id(&ctx);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
