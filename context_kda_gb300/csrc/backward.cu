@@ -60,10 +60,10 @@ enum : int {
     SCRATCH_FLOATS = S_DBETA + 64
 };
 
-// The terms a chain step needs, stored per (head, chunk) by the terms pass (floats): W, Ut, Kh, Qt
-// (64 x 128 each), QK (64 x 64), exp(Gamma_C) (128).
-enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * CK, TM_GC = 4 * CK + CC,
-             TERMS_FLOATS = TM_GC + KD };
+// The chunk's terms the chains and the gradient pass read, stored per (head, chunk) by the terms pass
+// (floats): W, Ut, Kh, Qt (64 x 128 each), QK, S, T (64 x 64 each), exp(Gamma_C) (128).
+enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * CK, TM_S = TM_QK + CC,
+             TM_T = TM_S + CC, TM_GC = TM_T + CC, TERMS_FLOATS = TM_GC + KD };
 
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
 constexpr size_t BWD_SMEM = 4ull * 32768 + 1024;   // the operand tiles of one product, aligned to 1024 bytes
@@ -239,9 +239,9 @@ __device__ __forceinline__ void bf8(uint4 w, float *x)
     }
 }
 
-// The chunk's terms into scratch sc (rows past L are zero): Kt, Kh, Qt, V, E = e^Gamma, Ei = e^-Gamma,
-// gc = e^Gamma_C, beta, M, S = strictly_lower(Kt Kh^T), T, W, Ut, QK, and Diag(beta) Kt, Diag(beta) V.
-__device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16_t *q, const uint16_t *k,
+// The chunk's element-wise terms into scratch sc (rows past L are zero): Kt, Kh, Qt, V, E = e^Gamma,
+// Ei = e^-Gamma, gc = e^Gamma_C, beta, Diag(beta) Kt and Diag(beta) V.
+__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_t *q, const uint16_t *k,
                             const uint16_t *v, const float *g, const float *beta, float scale)
 {
     extern __shared__ __align__(16) float bsm[];
@@ -320,6 +320,32 @@ __device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16
         }
     }
     __syncthreads();
+    // Diag(beta) Kt and Diag(beta) V
+    {
+        float4 kv[8], vv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 4 * (tid + i * BT);
+            kv[i] = ld4(Kt + e);
+            vv[i] = ld4(Vf + e);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 4 * (tid + i * BT);
+            const float b = sc[S_BT + (e >> 7)];
+            st4(sc + S_BKT + e, scl4(b, kv[i]));
+            st4(sc + S_BV + e, scl4(b, vv[i]));
+        }
+    }
+    __syncthreads();
+}
+
+// The chunk's products into scratch: S, QK (masked), M, T = (I + M)^-1, W and Ut, from the rows above.
+__device__ void chunk_products(float *sc)
+{
+    extern __shared__ __align__(16) float bsm[];
+    const int tid = threadIdx.x;
+    const float *Kt = sc + S_KT, *Kh = sc + S_KH, *Qt = sc + S_QT;
     gemm<64, 64, KD, false, true>(Kt, KD, Kh, KD, sc + S_S, 64, 1.f, false);
     gemm<64, 64, KD, false, true>(Qt, KD, Kh, KD, sc + S_QK, 64, 1.f, false);
     // S strictly lower, M = Diag(beta) S, QK lower with the diagonal
@@ -341,23 +367,6 @@ __device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16
             st4(sc + S_M + e, scl4(br, sm));
             st4(sc + S_QK + e, make_float4(c + 0 <= r ? qv[i].x : 0.f, c + 1 <= r ? qv[i].y : 0.f,
                                            c + 2 <= r ? qv[i].z : 0.f, c + 3 <= r ? qv[i].w : 0.f));
-        }
-    }
-    // Diag(beta) Kt and Diag(beta) V
-    {
-        float4 kv[8], vv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = 4 * (tid + i * BT);
-            kv[i] = ld4(Kt + e);
-            vv[i] = ld4(Vf + e);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = 4 * (tid + i * BT);
-            const float b = sc[S_BT + (e >> 7)];
-            st4(sc + S_BKT + e, scl4(b, kv[i]));
-            st4(sc + S_BV + e, scl4(b, vv[i]));
         }
     }
     __syncthreads();
@@ -388,6 +397,15 @@ __device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16
     }
     gemm<64, KD, 64, false, false>(sc + S_T, 64, sc + S_BKT, KD, sc + S_W, KD, 1.f, false);
     gemm<64, VD, 64, false, false>(sc + S_T, 64, sc + S_BV, VD, sc + S_UT, VD, 1.f, false);
+}
+
+// All of the chunk's terms (rows past L are zero): the rows, then S = strictly_lower(Kt Kh^T), QK, M,
+// T, W and Ut.
+__device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16_t *q, const uint16_t *k,
+                            const uint16_t *v, const float *g, const float *beta, float scale)
+{
+    chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
+    chunk_products(sc);
 }
 
 // The chunk's output gradient rows into scratch (zero past L), bf16 -> fp32.
@@ -573,6 +591,8 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
         copy_f<CK>(tm + TM_KH, sc + S_KH);
         copy_f<CK>(tm + TM_QT, sc + S_QT);
         copy_f<CC>(tm + TM_QK, sc + S_QK);
+        copy_f<CC>(tm + TM_S, sc + S_S);
+        copy_f<CC>(tm + TM_T, sc + S_T);
         if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
         __syncthreads();
     }
@@ -732,8 +752,8 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
 __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
                                                 const uint16_t *k, const uint16_t *v, const float *g,
                                                 const float *beta, float scale, const uint16_t *dout,
-                                                const float *xs, const float *gs, float *dq, float *dk, float *dv,
-                                                float *dg, float *dbeta, float *scratch)
+                                                const float *xs, const float *gs, const float *terms, float *dq,
+                                                float *dk, float *dv, float *dg, float *dbeta, float *scratch)
 {
     BWD_PLAN_CHECK();
     tc_begin();
@@ -745,7 +765,8 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const int h = unit / n_chunks, c = unit % n_chunks;
         const int32_t *cr = pv.chunk(c);
         const int t0 = cr[1], L = cr[2];
-        chunk_terms(sc, t0, L, h, H, q, k, v, g, beta, scale);
+        chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
+        const float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;   // W, Ut, QK, S, T
         load_do(sc, t0, L, h, H, dout);
         float *X = sc + S_X, *G = sc + S_G, *DG = sc + S_Y;
         const float *xsrc = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
@@ -755,9 +776,9 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         scale_rows(DG, gsrc, sc + S_GC);
         float *U = sc + S_U, *dU = sc + S_DU, *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dW = sc + S_DW;
         float *dQK = sc + S_DQK, *dT = sc + S_DT, *dM = sc + S_DM, *dKt = sc + S_DKT;
-        copy_f<CK>(U, sc + S_UT);
+        copy_f<CK>(U, tm + TM_UT);
         __syncthreads();
-        gemm<64, VD, KD, false, false>(sc + S_W, KD, X, VD, U, VD, -1.f, true);     // U = Ut - W X
+        gemm<64, VD, KD, false, false>(tm + TM_W, KD, X, VD, U, VD, -1.f, true);     // U = Ut - W X
         gemm<64, VD, KD, false, false>(sc + S_KH, KD, DG, VD, dU, VD, 1.f, false);  // dU = Kh DG
         gemm<64, KD, VD, false, true>(U, VD, DG, VD, dKh, KD, 1.f, false);           // dKh = U DG^T
         // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c]: Y = X + Kh^T U in place of DG
@@ -794,17 +815,17 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
             }
         }
         __syncthreads();
-        gemm<64, VD, 64, true, false>(sc + S_QK, 64, sc + S_DO, VD, dU, VD, 1.f, true);   // dU += QK^T dO
+        gemm<64, VD, 64, true, false>(tm + TM_QK, 64, sc + S_DO, VD, dU, VD, 1.f, true);   // dU += QK^T dO
         gemm<64, KD, 64, false, false>(dQK, 64, sc + S_KH, KD, dQt, KD, 1.f, true);       // dQt += dQK Kh
         gemm<64, KD, 64, true, false>(dQK, 64, sc + S_QT, KD, dKh, KD, 1.f, true);        // dKh += dQK^T Qt
         gemm<64, KD, VD, false, true>(dU, VD, X, VD, dW, KD, -1.f, false);                // dW = -dU X^T
         gemm<64, 64, KD, false, true>(dW, KD, sc + S_BKT, KD, dT, 64, 1.f, false);        // dT = dW (bKt)^T
         gemm<64, 64, VD, false, true>(dU, VD, sc + S_BV, VD, dT, 64, 1.f, true);          //    + dU (bV)^T
-        gemm<64, KD, 64, true, false>(sc + S_T, 64, dW, KD, sc + S_DBKT, KD, 1.f, false); // d(bKt) = T^T dW
-        gemm<64, VD, 64, true, false>(sc + S_T, 64, dU, VD, sc + S_DBV, VD, 1.f, false);  // d(bV) = T^T dU
+        gemm<64, KD, 64, true, false>(tm + TM_T, 64, dW, KD, sc + S_DBKT, KD, 1.f, false); // d(bKt) = T^T dW
+        gemm<64, VD, 64, true, false>(tm + TM_T, 64, dU, VD, sc + S_DBV, VD, 1.f, false);  // d(bV) = T^T dU
         // dM = strictly_lower(-T^T dT T^T)
-        gemm<64, 64, 64, true, false>(sc + S_T, 64, dT, 64, sc + S_T64, 64, 1.f, false);
-        gemm<64, 64, 64, false, true>(sc + S_T64, 64, sc + S_T, 64, dM, 64, -1.f, false);
+        gemm<64, 64, 64, true, false>(tm + TM_T, 64, dT, 64, sc + S_T64, 64, 1.f, false);
+        gemm<64, 64, 64, false, true>(sc + S_T64, 64, tm + TM_T, 64, dM, 64, -1.f, false);
         {
             float4 v[4];
 #pragma unroll
@@ -829,7 +850,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = ld4(sc + S_KT + r * KD + 4 * ln);
                 const float4 cv = ld4(sc + S_DBV + r * VD + 4 * ln), d = ld4(sc + S_VF + r * VD + 4 * ln);
                 const float2 m = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
-                const float2 sv = *reinterpret_cast<const float2 *>(sc + S_S + r * 64 + 2 * ln);
+                const float2 sv = *reinterpret_cast<const float2 *>(tm + TM_S + r * 64 + 2 * ln);
                 const float sum = warp_sum(dot4(a, b) + dot4(cv, d) + m.x * sv.x + m.y * sv.y);
                 if (ln == 0) sc[S_DBETA + r] = sum;
             }
@@ -953,8 +974,8 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
     bwd_reverse<true><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, dout, dfinal, G_end, Qd, gs, dh0,
                                                       scratch);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, dq, dk, dv, dg,
-                                       dbeta, scratch);
+    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, terms, dq, dk,
+                                              dv, dg, dbeta, scratch);
     return cudaGetLastError();
 }
 
