@@ -66,7 +66,7 @@ enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * C
              TM_T = TM_S + CC, TM_GC = TM_T + CC, TERMS_FLOATS = TM_GC + KD };
 
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
-constexpr size_t BWD_SMEM = 4ull * 32768 + 1024;   // the operand tiles of one product, aligned to 1024 bytes
+constexpr size_t BWD_SMEM = 6ull * 32768 + 1024;   // the operand tiles of a two-term product, aligned to 1024 bytes
 
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 __device__ __forceinline__ int warp_id() { return static_cast<int>(threadIdx.x) >> 5; }
@@ -132,93 +132,184 @@ __device__ __forceinline__ unsigned char *tc_tiles()
     return bsm_raw + ((1024u - (smem_u32(bsm_raw) & 1023u)) & 1023u);
 }
 
-// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc) for an M x N result and K-long sums
-// (M, N, K in {64, 128}), by all threads of the CTA, with A(m, k) = TA ? a[k * lda + m] : a[m * lda + k]
-// and B(k, n) = TB ? b[n * ldb + k] : b[k * ldb + n] (FP32, 16-byte aligned, leading dimensions
-// multiples of 8).  Each operand is copied as it lies (rows of its contiguous index) into the no-swizzle
-// canonical layout as a bf16 hi/lo pair, and read by the tensor core K-major or MN-major accordingly, so
-// nothing is transposed on the way; the product is the 3-term split hi*hi + hi*lo + lo*hi (~2^-16
-// relative, FP32 accumulation in TMEM) on tcgen05 with M = 128 (a 64-row A fills half the lanes, the
-// rest are never read).  The staging lanes take consecutive rows of one 8-column piece, so their
-// 16-byte stores land in distinct banks.
-template <int M, int N, int K, bool TA, bool TB>
-__device__ void gemm(const float *a, int lda, const float *b, int ldb, float *C, int ldc, float alpha, bool acc)
+// Staging of one operand for the tensor core: the source is a row-major FP32 array of R rows and C
+// contiguous columns (leading dimension ld), stored as it lies into the no-swizzle canonical layout as
+// a bf16 hi/lo pair (chunk stride CS); rows_scale, when set, multiplies source row r, and s the whole
+// operand.  The lanes of a warp take consecutive rows of one 8-column piece, so their 16-byte stores
+// land in distinct banks.
+template <int R, int C>
+struct Stage {
+    static constexpr int P = R * C / 8 / BT;   // 8-column pieces per thread
+    float4 v[2 * P];
+    __device__ __forceinline__ void load(const float *src, int ld)
+    {
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            const int pc = threadIdx.x + i * BT, r = pc % R, c8 = (pc / R) * 8;
+            v[2 * i] = ld4(src + r * ld + c8);
+            v[2 * i + 1] = ld4(src + r * ld + c8 + 4);
+        }
+    }
+    __device__ __forceinline__ void store(unsigned char *hi, unsigned char *lo, uint32_t cs, const float *rows_scale,
+                                          float s)
+    {
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            const int pc = threadIdx.x + i * BT, r = pc % R, c8 = (pc / R) * 8;
+            const float f = rows_scale ? s * rows_scale[r] : s;
+            const float4 x0 = scl4(f, v[2 * i]), x1 = scl4(f, v[2 * i + 1]);
+            uint32_t h[4], l[4];
+            split_bf16x2(x0.x, x0.y, h[0], l[0]);
+            split_bf16x2(x0.z, x0.w, h[1], l[1]);
+            split_bf16x2(x1.x, x1.y, h[2], l[2]);
+            split_bf16x2(x1.z, x1.w, h[3], l[3]);
+            const uint32_t off = cm_off(r, c8, cs);
+            *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+    }
+};
+
+// One term A B of a product: A(m, k) = TA ? a[k * lda + m] : a[m * lda + k], B(k, n) = TB ? b[n * ldb + k]
+// : b[k * ldb + n], scaled by s; b_rows, when set (only with !TB), multiplies B's row k.
+struct Term {
+    const float *a;
+    int lda;
+    const float *b;
+    int ldb;
+    float s;
+    const float *b_rows;
+};
+__device__ __forceinline__ Term term(const float *a, int lda, const float *b, int ldb, float s = 1.f,
+                                     const float *b_rows = nullptr)
 {
-    static_assert((M == 64 || M == 128) && (N == 64 || N == 128) && (K == 64 || K == 128), "shapes");
+    return Term{a, lda, b, ldb, s, b_rows};
+}
+
+// The output of a product: C[m][n] = out_rows[m] * (alpha * sum of the terms + in_rows[m] * cin[m][n]),
+// each factor or input omitted when its pointer is null; MASK 1 keeps n <= m, MASK 2 n < m (zero
+// elsewhere).
+struct Out {
+    float *c;
+    int ldc;
+    float alpha;
+    const float *cin;
+    int ldcin;
+    const float *in_rows;
+    const float *out_rows;
+};
+__device__ __forceinline__ Out out(float *c, int ldc, float alpha = 1.f, const float *cin = nullptr, int ldcin = 0,
+                                   const float *in_rows = nullptr, const float *out_rows = nullptr)
+{
+    return Out{c, ldc, alpha, cin, ldcin, in_rows, out_rows};
+}
+
+// An M x N product of one or two terms (K1- and K2-long sums; K2 = 0: one term; M, N, K in {64, 128})
+// by all threads of the CTA.  Every operand is copied as it lies (rows of its contiguous index) into the
+// no-swizzle canonical layout as a bf16 hi/lo pair and read by the tensor core K-major or MN-major
+// accordingly, so nothing is transposed on the way; each term is the 3-term split hi*hi + hi*lo + lo*hi
+// (~2^-16 relative), both terms accumulate in FP32 in one TMEM accumulator, M = 128 (a 64-row A fills
+// half the lanes, the rest are never read).  All operand loads are issued before the first staging
+// store, and the accumulated input is loaded while the tensor core works.
+template <int M, int N, int K1, bool TA1, bool TB1, int K2 = 0, bool TA2 = false, bool TB2 = false, int MASK = 0>
+__device__ void product(const Term t1, const Term t2, const Out o)
+{
+    static_assert((M == 64 || M == 128) && (N == 64 || N == 128) && (K1 == 64 || K1 == 128) &&
+                      (K2 == 0 || K2 == 64 || K2 == 128), "shapes");
     if (s_tc_fail) return;   // uniform: written before the previous product's closing barrier
     const int tid = threadIdx.x;
-    // tiles: A's rows are its contiguous index's partner (k when TA, else m), B's likewise (n when TB)
-    constexpr int RA = TA ? K : M, CA = TA ? M : K, RB = TB ? N : K, CB = TB ? K : N;
-    constexpr uint32_t CS_A = TA ? K * 16 : 128 * 16, CS_B = RB * 16;
-    constexpr uint32_t A_BYTES = 128 * K * 2, B_BYTES = N * K * 2;
-    constexpr int PA = RA * CA / 8 / BT, PB = RB * CB / 8 / BT;
-    unsigned char *const a_hi = tc_tiles(), *const a_lo = a_hi + A_BYTES;
-    unsigned char *const b_hi = a_lo + A_BYTES, *const b_lo = b_hi + B_BYTES;
-    float4 va[2 * PA], vb[2 * PB];
-#pragma unroll
-    for (int i = 0; i < PA; ++i) {
-        const int pc = tid + i * BT, r = pc % RA, c8 = (pc / RA) * 8;
-        va[2 * i] = ld4(a + r * lda + c8);
-        va[2 * i + 1] = ld4(a + r * lda + c8 + 4);
-    }
-#pragma unroll
-    for (int i = 0; i < PB; ++i) {
-        const int pc = tid + i * BT, r = pc % RB, c8 = (pc / RB) * 8;
-        vb[2 * i] = ld4(b + r * ldb + c8);
-        vb[2 * i + 1] = ld4(b + r * ldb + c8 + 4);
-    }
-    auto put = [](unsigned char *hi, unsigned char *lo, uint32_t off, float4 x0, float4 x1) {
-        uint32_t h[4], l[4];
-        split_bf16x2(x0.x, x0.y, h[0], l[0]);
-        split_bf16x2(x0.z, x0.w, h[1], l[1]);
-        split_bf16x2(x1.x, x1.y, h[2], l[2]);
-        split_bf16x2(x1.z, x1.w, h[3], l[3]);
-        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    };
-#pragma unroll
-    for (int i = 0; i < PA; ++i) {
-        const int pc = tid + i * BT, r = pc % RA, c8 = (pc / RA) * 8;
-        put(a_hi, a_lo, cm_off(r, c8, CS_A), va[2 * i], va[2 * i + 1]);
-    }
-#pragma unroll
-    for (int i = 0; i < PB; ++i) {
-        const int pc = tid + i * BT, r = pc % RB, c8 = (pc / RB) * 8;
-        put(b_hi, b_lo, cm_off(r, c8, CS_B), vb[2 * i], vb[2 * i + 1]);
+    constexpr int K2E = K2 ? K2 : 64;   // shapes of the (unused when K2 = 0) second term
+    constexpr int RA1 = TA1 ? K1 : M, CA1 = TA1 ? M : K1, RB1 = TB1 ? N : K1, CB1 = TB1 ? K1 : N;
+    constexpr int RA2 = TA2 ? K2E : M, CA2 = TA2 ? M : K2E, RB2 = TB2 ? N : K2E, CB2 = TB2 ? K2E : N;
+    constexpr uint32_t CSA1 = TA1 ? K1 * 16 : 128 * 16, CSB1 = RB1 * 16;
+    constexpr uint32_t CSA2 = TA2 ? K2E * 16 : 128 * 16, CSB2 = RB2 * 16;
+    constexpr uint32_t A1B = 128 * K1 * 2, B1B = N * K1 * 2, A2B = 128 * K2E * 2, B2B = N * K2E * 2;
+    static_assert(2 * (A1B + B1B + (K2 ? A2B + B2B : 0)) <= BWD_SMEM - 1024, "the operand tiles fit");
+    unsigned char *const a1h = tc_tiles(), *const a1l = a1h + A1B, *const b1h = a1l + A1B, *const b1l = b1h + B1B;
+    unsigned char *const a2h = b1l + B1B, *const a2l = a2h + A2B, *const b2h = a2l + A2B, *const b2l = b2h + B2B;
+    {
+        Stage<RA1, CA1> sa1;
+        Stage<RB1, CB1> sb1;
+        sa1.load(t1.a, t1.lda);
+        sb1.load(t1.b, t1.ldb);
+        if constexpr (K2 != 0) {
+            Stage<RA2, CA2> sa2;
+            Stage<RB2, CB2> sb2;
+            sa2.load(t2.a, t2.lda);
+            sb2.load(t2.b, t2.ldb);
+            sa2.store(a2h, a2l, CSA2, nullptr, t2.s);
+            sb2.store(b2h, b2l, CSB2, TB2 ? nullptr : t2.b_rows, 1.f);
+        }
+        sa1.store(a1h, a1l, CSA1, nullptr, t1.s);
+        sb1.store(b1h, b1l, CSB1, TB1 ? nullptr : t1.b_rows, 1.f);
     }
     fence_async_smem();
     __syncthreads();
     fence_after();
     const uint32_t ph = s_tc_phase, tmem = s_tc_tmem, bar = smem_u32(&s_tc_bar);
     if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, N, TA ? 1 : 0, TB ? 0 : 1);
-        const uint32_t ah[3] = {smem_u32(a_hi), smem_u32(a_hi), smem_u32(a_lo)};
-        const uint32_t bh[3] = {smem_u32(b_hi), smem_u32(b_lo), smem_u32(b_hi)};
+        const uint32_t ah[3] = {smem_u32(a1h), smem_u32(a1h), smem_u32(a1l)};
+        const uint32_t bh[3] = {smem_u32(b1h), smem_u32(b1l), smem_u32(b1h)};
+        const uint32_t id1 = idesc_bf16(128, N, TA1 ? 1 : 0, TB1 ? 0 : 1);
 #pragma unroll
         for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
-            for (int kk = 0; kk < K / 16; ++kk) {
-                const uint64_t ad = TA ? sdesc(ah[ps] + kk * 256, 128, CS_A) : sdesc(ah[ps] + kk * 2 * CS_A, CS_A, 128);
-                const uint64_t bd = TB ? sdesc(bh[ps] + kk * 2 * CS_B, CS_B, 128) : sdesc(bh[ps] + kk * 256, 128, CS_B);
-                mma_bf16(tmem, ad, bd, id, (ps | kk) != 0);
+            for (int kk = 0; kk < K1 / 16; ++kk) {
+                const uint64_t ad = TA1 ? sdesc(ah[ps] + kk * 256, 128, CSA1) : sdesc(ah[ps] + kk * 2 * CSA1, CSA1, 128);
+                const uint64_t bd = TB1 ? sdesc(bh[ps] + kk * 2 * CSB1, CSB1, 128) : sdesc(bh[ps] + kk * 256, 128, CSB1);
+                mma_bf16(tmem, ad, bd, id1, (ps | kk) != 0);
             }
+        if constexpr (K2 != 0) {
+            const uint32_t ah2[3] = {smem_u32(a2h), smem_u32(a2h), smem_u32(a2l)};
+            const uint32_t bh2[3] = {smem_u32(b2h), smem_u32(b2l), smem_u32(b2h)};
+            const uint32_t id2 = idesc_bf16(128, N, TA2 ? 1 : 0, TB2 ? 0 : 1);
+#pragma unroll
+            for (int ps = 0; ps < 3; ++ps)
+#pragma unroll
+                for (int kk = 0; kk < K2 / 16; ++kk) {
+                    const uint64_t ad =
+                        TA2 ? sdesc(ah2[ps] + kk * 256, 128, CSA2) : sdesc(ah2[ps] + kk * 2 * CSA2, CSA2, 128);
+                    const uint64_t bd =
+                        TB2 ? sdesc(bh2[ps] + kk * 2 * CSB2, CSB2, 128) : sdesc(bh2[ps] + kk * 256, 128, CSB2);
+                    mma_bf16(tmem, ad, bd, id2, 1u);
+                }
+        }
         commit(bar);
     }
+    // row m = this thread's TMEM lane, columns hw * N/2 .. + N/2; the accumulated input is loaded
+    // while the tensor core works
+    const int warp = tid >> 5, quad = warp & 3, hw = warp >> 2;
+    const int m = quad * 32 + (tid & 31), n0 = hw * (N / 2);
+    const bool live = quad * 32 < M;
+    float4 old[N / 8];
+    {
+        const float f = (o.cin && live) ? (o.in_rows ? o.in_rows[m] : 1.f) : 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < N / 8; ++q4)
+            old[q4] = (o.cin && live) ? scl4(f, ld4(o.cin + m * o.ldcin + n0 + 4 * q4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float fo = (o.out_rows && live) ? o.out_rows[m] : 1.f;
     const bool ok = mbar_wait_warp(bar, ph);
     fence_after();
-    const int warp = tid >> 5, quad = warp & 3, hw = warp >> 2;
-    if (ok && quad * 32 < M) {   // row m = this thread's TMEM lane, columns hw * N/2 .. + N/2
-        const int m = quad * 32 + (tid & 31);
+    if (ok && live) {
+        float *const crow = o.c + m * o.ldc + n0;
 #pragma unroll
         for (int j0 = 0; j0 < N / 2; j0 += 32) {
             float d[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + hw * (N / 2) + j0, d);
-            float *crow = C + m * ldc + hw * (N / 2) + j0;
+            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + n0 + j0, d);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 old = acc ? ld4(crow + 4 * q4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                st4(crow + 4 * q4, make_float4(alpha * d[4 * q4] + old.x, alpha * d[4 * q4 + 1] + old.y,
-                                               alpha * d[4 * q4 + 2] + old.z, alpha * d[4 * q4 + 3] + old.w));
+                const float4 o4 = old[j0 / 4 + q4];
+                float r[4] = {fo * (o.alpha * d[4 * q4] + o4.x), fo * (o.alpha * d[4 * q4 + 1] + o4.y),
+                              fo * (o.alpha * d[4 * q4 + 2] + o4.z), fo * (o.alpha * d[4 * q4 + 3] + o4.w)};
+                if constexpr (MASK != 0) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int n = n0 + j0 + 4 * q4 + e;
+                        if (MASK == 1 ? n > m : n >= m) r[e] = 0.f;
+                    }
+                }
+                st4(crow + j0 + 4 * q4, make_float4(r[0], r[1], r[2], r[3]));
             }
         }
     }
@@ -226,6 +317,14 @@ __device__ void gemm(const float *a, int lda, const float *b, int ldb, float *C,
     fence_before();
     __syncthreads();
     if (tid == 0) s_tc_phase = ph ^ 1u;
+}
+
+// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc): a one-term product.
+template <int M, int N, int K, bool TA, bool TB>
+__device__ __forceinline__ void gemm(const float *a, int lda, const float *b, int ldb, float *C, int ldc, float alpha,
+                                     bool acc)
+{
+    product<M, N, K, TA, TB>(term(a, lda, b, ldb), term(nullptr, 0, nullptr, 0), out(C, ldc, alpha, acc ? C : nullptr, ldc));
 }
 
 // 8 bf16 (one 16-byte word) as fp32
@@ -460,23 +559,6 @@ __device__ __forceinline__ void zero_slice(float *dst, int c0)
     }
 }
 
-// dst = Diag(d) src on columns c0 .. c0 + SW of a 128-row state (d one value per row)
-__device__ __forceinline__ void scale_slice(float *dst, const float *src, const float *d, int c0)
-{
-    constexpr int P = KD * SW / 4 / BT;
-    float4 v[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int e = threadIdx.x + i * BT;
-        v[i] = ld4(src + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)));
-    }
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int e = threadIdx.x + i * BT, r = e / (SW / 4);
-        st4(dst + r * VD + c0 + 4 * (e % (SW / 4)), scl4(d[r], v[i]));
-    }
-}
-
 // dst = Diag(d) src for a whole 128 x 128 state, every thread's loads first
 __device__ __forceinline__ void scale_rows(float *dst, const float *src, const float *d)
 {
@@ -517,38 +599,24 @@ __device__ void load_do_slice(float *sc, int t0, int L, int h, int H, const uint
 __device__ void forward_step(float *sc, const float *tm, int c0)
 {
     float *X = sc + S_X, *U = sc + S_U;
-    {   // U = Ut on the slice (64 rows)
-        constexpr int P = 64 * SW / 4 / BT;
-        float4 v[P];
-#pragma unroll
-        for (int i = 0; i < P; ++i) {
-            const int e = threadIdx.x + i * BT;
-            v[i] = ld4(tm + TM_UT + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)));
-        }
-#pragma unroll
-        for (int i = 0; i < P; ++i) {
-            const int e = threadIdx.x + i * BT;
-            st4(U + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)), v[i]);
-        }
-    }
-    gemm<64, SW, KD, false, false>(tm + TM_W, KD, X + c0, VD, U + c0, VD, -1.f, true);
-    gemm<KD, SW, 64, true, false>(tm + TM_KH, KD, U + c0, VD, X + c0, VD, 1.f, true);
-    scale_slice(X, X, tm + TM_GC, c0);
-    __syncthreads();
+    product<64, SW, KD, false, false>(term(tm + TM_W, KD, X + c0, VD), Term{},
+                                      out(U + c0, VD, -1.f, tm + TM_UT + c0, VD));                 // U = Ut - W X
+    product<KD, SW, 64, true, false>(term(tm + TM_KH, KD, U + c0, VD), Term{},
+                                     out(X + c0, VD, 1.f, X + c0, VD, nullptr, tm + TM_GC));       // Dc (X + Kh^T U)
 }
 
 // G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start), on
 // columns c0 .. c0 + SW, the chunk's terms at tm
 __device__ void reverse_step(float *sc, const float *tm, int c0)
 {
-    float *G = sc + S_G, *DG = sc + S_Y, *dU = sc + S_DU;
-    scale_slice(DG, G, tm + TM_GC, c0);
-    __syncthreads();
-    gemm<64, SW, KD, false, false>(tm + TM_KH, KD, DG + c0, VD, dU + c0, VD, 1.f, false);
-    gemm<64, SW, 64, true, false>(tm + TM_QK, 64, sc + S_DO + c0, VD, dU + c0, VD, 1.f, true);
-    copy_slice(G, DG, c0);
-    gemm<KD, SW, 64, true, false>(tm + TM_QT, KD, sc + S_DO + c0, VD, G + c0, VD, 1.f, true);
-    gemm<KD, SW, 64, true, false>(tm + TM_W, KD, dU + c0, VD, G + c0, VD, -1.f, true);
+    float *G = sc + S_G, *dU = sc + S_DU;
+    const float *dO = sc + S_DO;
+    product<64, SW, KD, false, false, 64, true, false>(
+        term(tm + TM_KH, KD, G + c0, VD, 1.f, tm + TM_GC), term(tm + TM_QK, 64, dO + c0, VD),
+        out(dU + c0, VD));                                                                          // Kh DG + QK^T dO
+    product<KD, SW, 64, true, false, 64, true, false>(
+        term(tm + TM_QT, KD, dO + c0, VD), term(tm + TM_W, KD, dU + c0, VD, -1.f),
+        out(G + c0, VD, 1.f, G + c0, VD, tm + TM_GC));                                              // DG + Qt^T dO - W^T dU
 }
 
 // Plan helpers
@@ -768,23 +836,22 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
         const float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;   // W, Ut, QK, S, T
         load_do(sc, t0, L, h, H, dout);
-        float *X = sc + S_X, *G = sc + S_G, *DG = sc + S_Y;
-        const float *xsrc = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
-        const float *gsrc = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
-        copy_f<SQ>(X, xsrc);
-        copy_f<SQ>(G, gsrc);
-        scale_rows(DG, gsrc, sc + S_GC);
-        float *U = sc + S_U, *dU = sc + S_DU, *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dW = sc + S_DW;
-        float *dQK = sc + S_DQK, *dT = sc + S_DT, *dM = sc + S_DM, *dKt = sc + S_DKT;
-        copy_f<CK>(U, tm + TM_UT);
+        // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them
+        const float *X = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
+        const float *G = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
+        float *DG = sc + S_Y, *U = sc + S_U, *dU = sc + S_DU, *dKh = sc + S_DKH, *dQt = sc + S_DQT;
+        float *dW = sc + S_DW, *dQK = sc + S_DQK, *dT = sc + S_DT, *dM = sc + S_DM, *dKt = sc + S_DKT;
+        const float *dO = sc + S_DO, *Kh = sc + S_KH, *Qt = sc + S_QT, *bKt = sc + S_BKT, *bV = sc + S_BV;
+        scale_rows(DG, G, sc + S_GC);   // DG = Dc G
         __syncthreads();
-        gemm<64, VD, KD, false, false>(tm + TM_W, KD, X, VD, U, VD, -1.f, true);     // U = Ut - W X
-        gemm<64, VD, KD, false, false>(sc + S_KH, KD, DG, VD, dU, VD, 1.f, false);  // dU = Kh DG
-        gemm<64, KD, VD, false, true>(U, VD, DG, VD, dKh, KD, 1.f, false);           // dKh = U DG^T
+        product<64, VD, KD, false, false>(term(tm + TM_W, KD, X, VD), Term{}, out(U, VD, -1.f, tm + TM_UT, VD));  // U = Ut - W X
+        product<64, 64, VD, false, true, 0, false, false, 1>(term(dO, VD, U, VD), Term{}, out(dQK, 64));          // lower(dO U^T)
+        product<64, VD, KD, false, false, 64, true, false>(term(Kh, KD, DG, VD), term(tm + TM_QK, 64, dO, VD),
+                                                           out(dU, VD));                                  // dU = Kh DG + QK^T dO
+        product<64, KD, VD, false, true, 64, true, false>(term(U, VD, DG, VD), term(dQK, 64, Qt, KD),
+                                                          out(dKh, KD));                                  // dKh = U DG^T + dQK^T Qt
         // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c]: Y = X + Kh^T U in place of DG
-        copy_f<SQ>(DG, X);
-        __syncthreads();
-        gemm<KD, VD, 64, true, false>(sc + S_KH, KD, U, VD, DG, VD, 1.f, true);
+        product<KD, VD, 64, true, false>(term(Kh, KD, U, VD), Term{}, out(DG, VD, 1.f, X, VD));
         {   // a warp per 16 rows k, 4 columns a lane, then a warp sum per row
             float4 gv[16], yv[16];
 #pragma unroll
@@ -800,47 +867,21 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 if ((tid & 31) == 0) sc[S_DGC + kr] = sum * sc[S_GC + kr];
             }
         }
-        __syncthreads();
-        gemm<64, KD, VD, false, true>(sc + S_DO, VD, X, VD, dQt, KD, 1.f, false);    // dQt = dO X^T
-        gemm<64, 64, VD, false, true>(sc + S_DO, VD, U, VD, dQK, 64, 1.f, false);    // dO U^T
-        {   // lower incl. diagonal
-            float4 v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = ld4(dQK + 4 * (tid + i * BT));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = 4 * (tid + i * BT), r = e >> 6, cc = e & 63;
-                st4(dQK + e, make_float4(cc + 0 <= r ? v[i].x : 0.f, cc + 1 <= r ? v[i].y : 0.f,
-                                         cc + 2 <= r ? v[i].z : 0.f, cc + 3 <= r ? v[i].w : 0.f));
-            }
-        }
-        __syncthreads();
-        gemm<64, VD, 64, true, false>(tm + TM_QK, 64, sc + S_DO, VD, dU, VD, 1.f, true);   // dU += QK^T dO
-        gemm<64, KD, 64, false, false>(dQK, 64, sc + S_KH, KD, dQt, KD, 1.f, true);       // dQt += dQK Kh
-        gemm<64, KD, 64, true, false>(dQK, 64, sc + S_QT, KD, dKh, KD, 1.f, true);        // dKh += dQK^T Qt
-        gemm<64, KD, VD, false, true>(dU, VD, X, VD, dW, KD, -1.f, false);                // dW = -dU X^T
-        gemm<64, 64, KD, false, true>(dW, KD, sc + S_BKT, KD, dT, 64, 1.f, false);        // dT = dW (bKt)^T
-        gemm<64, 64, VD, false, true>(dU, VD, sc + S_BV, VD, dT, 64, 1.f, true);          //    + dU (bV)^T
-        gemm<64, KD, 64, true, false>(tm + TM_T, 64, dW, KD, sc + S_DBKT, KD, 1.f, false); // d(bKt) = T^T dW
-        gemm<64, VD, 64, true, false>(tm + TM_T, 64, dU, VD, sc + S_DBV, VD, 1.f, false);  // d(bV) = T^T dU
+        product<64, KD, VD, false, true, 64, false, false>(term(dO, VD, X, VD), term(dQK, 64, Kh, KD),
+                                                           out(dQt, KD));                                 // dQt = dO X^T + dQK Kh
+        product<64, KD, VD, false, true>(term(dU, VD, X, VD), Term{}, out(dW, KD, -1.f));               // dW = -dU X^T
+        product<64, 64, KD, false, true, VD, false, true>(term(dW, KD, bKt, KD), term(dU, VD, bV, VD),
+                                                          out(dT, 64));                                   // dT = dW bKt^T + dU bV^T
+        product<64, KD, 64, true, false>(term(tm + TM_T, 64, dW, KD), Term{}, out(sc + S_DBKT, KD));      // d(bKt) = T^T dW
+        product<64, VD, 64, true, false>(term(tm + TM_T, 64, dU, VD), Term{}, out(sc + S_DBV, VD));       // d(bV) = T^T dU
         // dM = strictly_lower(-T^T dT T^T)
-        gemm<64, 64, 64, true, false>(tm + TM_T, 64, dT, 64, sc + S_T64, 64, 1.f, false);
-        gemm<64, 64, 64, false, true>(sc + S_T64, 64, tm + TM_T, 64, dM, 64, -1.f, false);
-        {
-            float4 v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = ld4(dM + 4 * (tid + i * BT));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = 4 * (tid + i * BT), r = e >> 6, cc = e & 63;
-                st4(dM + e, make_float4(cc + 0 < r ? v[i].x : 0.f, cc + 1 < r ? v[i].y : 0.f, cc + 2 < r ? v[i].z : 0.f,
-                                        cc + 3 < r ? v[i].w : 0.f));
-            }
-        }
-        __syncthreads();
+        product<64, 64, 64, true, false>(term(tm + TM_T, 64, dT, 64), Term{}, out(sc + S_T64, 64));
+        product<64, 64, 64, false, true, 0, false, false, 2>(term(sc + S_T64, 64, tm + TM_T, 64), Term{},
+                                                             out(dM, 64, -1.f));
         // dKt = beta (d(bKt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(bV)
-        gemm<64, KD, 64, false, false>(dM, 64, sc + S_KH, KD, dKt, KD, 1.f, false);
-        gemm<64, KD, 64, true, false>(dM, 64, sc + S_BKT, KD, dKh, KD, 1.f, true);
+        product<64, KD, 64, false, false>(term(dM, 64, Kh, KD), Term{},
+                                          out(dKt, KD, 1.f, sc + S_DBKT, KD, nullptr, sc + S_BT));
+        product<64, KD, 64, true, false>(term(dM, 64, bKt, KD), Term{}, out(dKh, KD, 1.f, dKh, KD));
         // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S): a warp per 8 rows, then a warp sum
         {
             const int ln = tid & 31;
@@ -849,24 +890,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 const int r = warp_id() * 8 + j;
                 const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = ld4(sc + S_KT + r * KD + 4 * ln);
                 const float4 cv = ld4(sc + S_DBV + r * VD + 4 * ln), d = ld4(sc + S_VF + r * VD + 4 * ln);
-                const float2 m = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
+                const float2 mm = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
                 const float2 sv = *reinterpret_cast<const float2 *>(tm + TM_S + r * 64 + 2 * ln);
-                const float sum = warp_sum(dot4(a, b) + dot4(cv, d) + m.x * sv.x + m.y * sv.y);
+                const float sum = warp_sum(dot4(a, b) + dot4(cv, d) + mm.x * sv.x + mm.y * sv.y);
                 if (ln == 0) sc[S_DBETA + r] = sum;
-            }
-        }
-        {
-            float4 a[8], b[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = 4 * (tid + i * BT);
-                a[i] = ld4(sc + S_DBKT + e);
-                b[i] = ld4(dKt + e);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = 4 * (tid + i * BT);
-                st4(dKt + e, scl4(sc[S_BT + (e >> 7)], add4(a[i], b[i])));
             }
         }
         __syncthreads();
