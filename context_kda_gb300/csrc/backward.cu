@@ -47,15 +47,14 @@ constexpr int SQ = KD * VD;                  // a 128 x 128 state
 
 __device__ int g_bwd_status;
 
-// Per-CTA scratch (floats): three states, twenty 64 x 128 and eight 64 x 64 matrices, vectors.
+// Per-CTA scratch (floats): three states, seventeen 64 x 128 and four 64 x 64 matrices, vectors.
 enum : int {
     S_X = 0, S_G = S_X + SQ, S_Y = S_G + SQ,
     S_KT = S_Y + SQ, S_KH = S_KT + CK, S_QT = S_KH + CK, S_VF = S_QT + CK, S_E = S_VF + CK, S_EI = S_E + CK,
-    S_W = S_EI + CK, S_UT = S_W + CK, S_U = S_UT + CK, S_DO = S_U + CK, S_DU = S_DO + CK, S_DKH = S_DU + CK,
+    S_U = S_EI + CK, S_DO = S_U + CK, S_DU = S_DO + CK, S_DKH = S_DU + CK,
     S_DQT = S_DKH + CK, S_DW = S_DQT + CK, S_DKT = S_DW + CK, S_BKT = S_DKT + CK, S_BV = S_BKT + CK,
-    S_DBKT = S_BV + CK, S_DBV = S_DBKT + CK, S_TMP = S_DBV + CK,
-    S_M = S_TMP + CK, S_S = S_M + CC, S_T = S_S + CC, S_QK = S_T + CC, S_DQK = S_QK + CC, S_DT = S_DQK + CC,
-    S_DM = S_DT + CC, S_T64 = S_DM + CC,
+    S_DBKT = S_BV + CK, S_DBV = S_DBKT + CK,
+    S_DQK = S_DBV + CK, S_DT = S_DQK + CC, S_DM = S_DT + CC, S_T64 = S_DM + CC,
     S_GC = S_T64 + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64, S_DBETA = S_DGC + KD,
     SCRATCH_FLOATS = S_DBETA + 64
 };
@@ -439,72 +438,45 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
     __syncthreads();
 }
 
-// The chunk's products into scratch: S, QK (masked), M, T = (I + M)^-1, W and Ut, from the rows above.
-__device__ void chunk_products(float *sc)
+// The chunk's products, from the rows above, straight into its stored terms tm: S = strictly_lower(Kt Kh^T),
+// QK = lower(Qt Kh^T), T = (I + M)^-1 with M = Diag(beta) S, W = T Diag(beta) Kt and Ut = T Diag(beta) V.
+__device__ void chunk_products(const float *sc, float *tm)
 {
     extern __shared__ __align__(16) float bsm[];
     const int tid = threadIdx.x;
     const float *Kt = sc + S_KT, *Kh = sc + S_KH, *Qt = sc + S_QT;
-    gemm<64, 64, KD, false, true>(Kt, KD, Kh, KD, sc + S_S, 64, 1.f, false);
-    gemm<64, 64, KD, false, true>(Qt, KD, Kh, KD, sc + S_QK, 64, 1.f, false);
-    // S strictly lower, M = Diag(beta) S, QK lower with the diagonal
-    {
-        float4 sv[4], qv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = 4 * (tid + i * BT);
-            sv[i] = ld4(sc + S_S + e);
-            qv[i] = ld4(sc + S_QK + e);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = 4 * (tid + i * BT), r = e >> 6, c = e & 63;
-            const float br = sc[S_BT + r];
-            const float4 sm = make_float4(c + 0 < r ? sv[i].x : 0.f, c + 1 < r ? sv[i].y : 0.f, c + 2 < r ? sv[i].z : 0.f,
-                                          c + 3 < r ? sv[i].w : 0.f);
-            st4(sc + S_S + e, sm);
-            st4(sc + S_M + e, scl4(br, sm));
-            st4(sc + S_QK + e, make_float4(c + 0 <= r ? qv[i].x : 0.f, c + 1 <= r ? qv[i].y : 0.f,
-                                           c + 2 <= r ? qv[i].z : 0.f, c + 3 <= r ? qv[i].w : 0.f));
-        }
-    }
-    __syncthreads();
+    product<64, 64, KD, false, true, 0, false, false, 2>(term(Kt, KD, Kh, KD), Term{}, out(tm + TM_S, 64));
+    product<64, 64, KD, false, true, 0, false, false, 1>(term(Qt, KD, Kh, KD), Term{}, out(tm + TM_QK, 64));
     // T = (I + M)^-1 by forward substitution, one column per thread: T[j][j] = 1,
-    // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]; M in shared memory (read by every thread alike),
-    // the column in registers
+    // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]; M = Diag(beta) S in shared memory (read by every
+    // thread alike), the column in registers
     {
         float4 mv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) mv[i] = ld4(sc + S_M + 4 * (tid + i * BT));
+        for (int i = 0; i < 4; ++i) mv[i] = ld4(tm + TM_S + 4 * (tid + i * BT));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) st4(bsm + 4 * (tid + i * BT), mv[i]);
+        for (int i = 0; i < 4; ++i) {
+            const int e = 4 * (tid + i * BT);
+            st4(bsm + e, scl4(sc[S_BT + (e >> 6)], mv[i]));
+        }
         __syncthreads();
         if (tid < 64) {
             const int j = tid;
             float t[64];
 #pragma unroll
             for (int r = 0; r < 64; ++r) {
-                float s = 0.f;
+                float acc = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) s = fmaf(bsm[r * 64 + i], t[i], s);
-                t[r] = r < j ? 0.f : (r == j ? 1.f : -s);
+                for (int i = 0; i < r; ++i) acc = fmaf(bsm[r * 64 + i], t[i], acc);
+                t[r] = r < j ? 0.f : (r == j ? 1.f : -acc);
             }
 #pragma unroll
-            for (int r = 0; r < 64; ++r) sc[S_T + r * 64 + j] = t[r];
+            for (int r = 0; r < 64; ++r) tm[TM_T + r * 64 + j] = t[r];
         }
         __syncthreads();
     }
-    gemm<64, KD, 64, false, false>(sc + S_T, 64, sc + S_BKT, KD, sc + S_W, KD, 1.f, false);
-    gemm<64, VD, 64, false, false>(sc + S_T, 64, sc + S_BV, VD, sc + S_UT, VD, 1.f, false);
-}
-
-// All of the chunk's terms (rows past L are zero): the rows, then S = strictly_lower(Kt Kh^T), QK, M,
-// T, W and Ut.
-__device__ void chunk_terms(float *sc, int t0, int L, int h, int H, const uint16_t *q, const uint16_t *k,
-                            const uint16_t *v, const float *g, const float *beta, float scale)
-{
-    chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
-    chunk_products(sc);
+    product<64, KD, 64, false, false>(term(tm + TM_T, 64, sc + S_BKT, KD), Term{}, out(tm + TM_W, KD));
+    product<64, VD, 64, false, false>(term(tm + TM_T, 64, sc + S_BV, VD), Term{}, out(tm + TM_UT, VD));
 }
 
 // The chunk's output gradient rows into scratch (zero past L), bf16 -> fp32.
@@ -652,15 +624,11 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
     for (int unit = blockIdx.x; unit < n_chunks * H; unit += gridDim.x) {
         const int h = unit / n_chunks, c = unit % n_chunks;
         const int32_t *cr = pv.chunk(c);
-        chunk_terms(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
         float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;
-        copy_f<CK>(tm + TM_W, sc + S_W);
-        copy_f<CK>(tm + TM_UT, sc + S_UT);
+        chunk_rows(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
+        chunk_products(sc, tm);
         copy_f<CK>(tm + TM_KH, sc + S_KH);
         copy_f<CK>(tm + TM_QT, sc + S_QT);
-        copy_f<CC>(tm + TM_QK, sc + S_QK);
-        copy_f<CC>(tm + TM_S, sc + S_S);
-        copy_f<CC>(tm + TM_T, sc + S_T);
         if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
         __syncthreads();
     }
