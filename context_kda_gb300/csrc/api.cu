@@ -493,6 +493,12 @@ extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_d
                                                        b + round256(fw[5] + S_in_bytes(plan, H)), s)
                          : kda::launch_compose(plan, plan_dev, H, w.A, w.B, h0, w.S_in, s));
     if (rc != KDA_OK) return rc;
+    // every piece again from its true incoming state, recording each chunk's start state
+    rc = cuda_status(kda::launch_state_record(plan, plan_dev, H, h0, w.S_in, w.pkg,
+                                              reinterpret_cast<uint16_t *>(b + off[0]),
+                                              reinterpret_cast<float *>(b + off[1]),
+                                              reinterpret_cast<float *>(b + off[2]), s));
+    if (rc != KDA_OK) return rc;
     return cuda_status(kda::launch_backward(
         plan, plan_dev, H, q, k, v, g, beta, h0, scale, dout, dfinal, w.A, w.afin, w.S_in,
         reinterpret_cast<float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),

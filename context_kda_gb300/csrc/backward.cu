@@ -17,7 +17,7 @@
 // segment transitions A and the final-state transitions of continuing pieces):
 //  0. every (chunk, head) in parallel: the chunk's terms that the chains need (W, Ut, Kh, Qt, QK, Dc);
 //  1. every piece from its true incoming state (h0, or S_in of its segment), recording each chunk's
-//     start state X_c;
+//     start state X_c: the forward's state pass in its output mode (the caller launches it);
 //  2. every piece that continues a sequence, backwards from a zero end gradient: the gradient of its
 //     incoming state through its own outputs, Qd (the qhat do^T sum of the pages' summaries);
 //  3. the following summaries, last segment first: the gradient of the state crossing the end of
@@ -567,16 +567,6 @@ __device__ void load_do_slice(float *sc, int t0, int L, int h, int H, const uint
     __syncthreads();
 }
 
-// X <- Dc (X + Kh^T (Ut - W X)) on columns c0 .. c0 + SW, the chunk's terms at tm
-__device__ void forward_step(float *sc, const float *tm, int c0)
-{
-    float *X = sc + S_X, *U = sc + S_U;
-    product<64, SW, KD, false, false>(term(tm + TM_W, KD, X + c0, VD), Term{},
-                                      out(U + c0, VD, -1.f, tm + TM_UT + c0, VD));                 // U = Ut - W X
-    product<KD, SW, 64, true, false>(term(tm + TM_KH, KD, U + c0, VD), Term{},
-                                     out(X + c0, VD, 1.f, X + c0, VD, nullptr, tm + TM_GC));       // Dc (X + Kh^T U)
-}
-
 // G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start), on
 // columns c0 .. c0 + SW, the chunk's terms at tm
 __device__ void reverse_step(float *sc, const float *tm, int c0)
@@ -630,38 +620,6 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
         copy_f<CK>(tm + TM_KH, sc + S_KH);
         copy_f<CK>(tm + TM_QT, sc + S_QT);
         if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
-        __syncthreads();
-    }
-    tc_end();
-}
-
-// 1. every piece from its true incoming state, recording X_c = xs[h][c] for each of its chunks
-__global__ void __launch_bounds__(BT, 1) bwd_states(const int32_t *plan, PlanSig sig, int H, const float *terms,
-                                                 const float *h0, const float *S_in, float *xs, float *scratch)
-{
-    BWD_PLAN_CHECK();
-    tc_begin();
-    const PlanView pv{plan};
-    float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
-    const int n_items = pv.n_pieces() * H * NS;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int ph = item / NS, c0 = (item % NS) * SW;
-        const int p = ph / H, h = ph % H;
-        const PieceInfo pi = piece_info(pv, p);
-        const float *src = nullptr;
-        if (pi.flags & KDA_PIECE_FIRST) {
-            if (h0) src = h0 + (static_cast<size_t>(pi.seq) * H + h) * SQ;
-        } else {
-            src = S_in + (static_cast<size_t>(pi.seg) * H + h) * SQ;
-        }
-        if (src) copy_slice(sc + S_X, src, c0);
-        else zero_slice(sc + S_X, c0);
-        __syncthreads();
-        for (int ci = 0; ci < pi.nch; ++ci) {
-            const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
-            copy_slice(xs + unit * SQ, sc + S_X, c0);
-            forward_step(sc, terms + unit * TERMS_FLOATS, c0);
-        }
         __syncthreads();
     }
     tc_end();
@@ -948,8 +906,7 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
 {
     const PlanView pv{plan_host};
     const PlanSig sig = plan_sig(plan_host);
-    for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_states),
-                    reinterpret_cast<const void *>(bwd_reverse<false>),
+    for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_reverse<false>),
                     reinterpret_cast<const void *>(bwd_reverse<true>), reinterpret_cast<const void *>(bwd_grads)}) {
         const cudaError_t e = set_dynamic_smem(fn, static_cast<int>(BWD_SMEM));
         if (e != cudaSuccess) return e;
@@ -957,8 +914,6 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
     bwd_terms<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, terms, scratch);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    bwd_states<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, h0, S_in, xs, scratch);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (pv.n_cont() > 0) {
         bwd_reverse<false><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, dout, dfinal, G_end, Qd, gs, dh0,
                                                            scratch);

@@ -92,7 +92,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                const float *__restrict__ s_in, const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o,
                float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
                uint16_t *__restrict__ qhat, float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
-               const __grid_constant__ CUtensorMap tm_q, int withhold)
+               const __grid_constant__ CUtensorMap tm_q, int withhold, float *__restrict__ xs)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;      // W X, then the state product
@@ -154,6 +154,16 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
     const uint32_t tbase = s_tmem;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
     const int c_lane = quad * 32 + lane;                                     // state column of this thread
+    // (STATE_OUTPUT with xs) the start state of the piece's chunk ci, rows k0 .. k0 + 31 of this
+    // thread's column, into xs[h][chunk] (fp32 K x V, row-major): a warp's store covers 128 bytes of a row
+    auto record_x = [&](int ci, int k0, const float (&x)[32]) {
+        if constexpr (MODE == STATE_OUTPUT) {
+            if (!xs) return;
+            float *dst = xs + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KD * VD + c_lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[(k0 + j) * VD] = x[j];
+        }
+    };
 
     // package parts by bulk copy (producer thread)
     auto load_p1 = [&](int ci) {
@@ -222,6 +232,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                 }
                 tmem_st32(tl + TM_X + k0, x);
                 tmem_st_split32(tl + TM_XH + k0 / 2, tl + TM_XL + k0 / 2, x);
+                if (nch > 0) record_x(0, k0, x);
             }
             tmem_wait_st();
             grid_dep_wait();   // the packages come from the preparation kernel; every output write follows
@@ -286,6 +297,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                     tmem_wait_st();
                     aborted = handoff(half == 0 ? HO_XA : HO_XB);   // -> next chunk's W X, Qt X
                     if (aborted) break;
+                    if (ci + 1 < nch) record_x(ci + 1, k0, x);
                 }
                 if (aborted) break;
                 if constexpr (MODE != STATE_SUMMARY) {
@@ -485,7 +497,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
 template <int MODE>
 cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0, const float *s_in,
                          const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
-                         uint16_t *qhat, float *afin, cudaStream_t stream, int withhold = -1)
+                         uint16_t *qhat, float *afin, cudaStream_t stream, int withhold = -1, float *xs = nullptr)
 {
     const PlanView pv{plan_host};
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
@@ -508,7 +520,7 @@ cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int 
     if (err != cudaSuccess) return err;
     return launch_dependent(chunk_state_tc<MODE>, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC,
                             stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq,
-                            withhold);
+                            withhold, xs);
 }
 
 }  // namespace
@@ -551,6 +563,17 @@ cudaError_t launch_two_pass(const int32_t *plan_host, const int32_t *plan_dev, i
     if (err != cudaSuccess) return err;
     return launch_state<STATE_OUTPUT>(plan_host, plan_dev, H, h0, S_in, pkg, o, A, B, final_state, nullptr, nullptr,
                                       stream);
+}
+
+// Every piece's state chain from its true incoming state (h0, or S_in of its segment), recording the
+// start state of each chunk into xs[h][chunk] (fp32 K x V); the outputs and final states go to o and
+// final_state.  The packages and S_in come from the kernels before it on the stream.
+cudaError_t launch_state_record(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
+                                const float *S_in, const unsigned char *pkg, uint16_t *o, float *final_state,
+                                float *xs, cudaStream_t stream)
+{
+    return launch_state<STATE_OUTPUT>(plan_host, plan_dev, H, h0, S_in, pkg, o, nullptr, nullptr, final_state,
+                                      nullptr, nullptr, stream, -1, xs);
 }
 
 // Self-test of the state pass's abort path: the preparation, then the state pass with the package copies

@@ -103,6 +103,9 @@ int take_compose_status();
 int take_boundary_status();
 int take_backward_status();
 cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
+cudaError_t launch_state_record(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
+                                const float *S_in, const unsigned char *pkg, uint16_t *o, float *final_state,
+                                float *xs, cudaStream_t stream);
 cudaError_t launch_state_abort_selftest(const int32_t *plan_host, const int32_t *plan_dev, int H,
                                         const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
                                         const float *beta, const float *h0, float scale, uint16_t *o, float *A,
