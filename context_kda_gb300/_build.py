@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkda.so")
 ROOT = os.path.dirname(PKG)
 
-CUDA_SOURCES = ["api.cu", "chunk_prep.cu", "chunk_state.cu", "compose.cu", "boundary.cu", "noalloc.cu", "backward.cu"]
+CUDA_SOURCES = ["api.cu", "chunk_prep.cu", "chunk_state.cu", "compose.cu", "boundary.cu", "noalloc.cu", "backward.cu", "reverse.cu"]
 CXX_SOURCES = ["plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

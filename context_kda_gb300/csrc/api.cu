@@ -176,7 +176,7 @@ extern "C" int kda_device_status(void)
     }
     int worst = KDA_OK;
     for (int st : {kda::take_prep_status(), kda::take_state_status(), kda::take_compose_status(),
-                   kda::take_boundary_status(), kda::take_backward_status()})
+                   kda::take_boundary_status(), kda::take_backward_status(), kda::take_reverse_status()})
         if (st != KDA_OK && worst == KDA_OK) worst = st;
     return worst;
 }
@@ -435,23 +435,23 @@ constexpr int kBackwardGrid = 152;   // CTAs of the backward's chunk and piece k
 // Regions of the backward's workspace after the forward's: o and final states of the forward run it
 // needs (not returned), the chunk start states and end gradients, the segment end gradients and
 // continuing pieces' incoming-state gradients, the CTAs' scratch, and each chunk's terms for the chains.
-bool backward_layout(const int32_t *plan, int32_t H, size_t off[9])
+bool backward_layout(const int32_t *plan, int32_t H, size_t off[10])
 {
     size_t fw[7];
     if (!layout(plan, H, fw)) return false;
     const size_t h = static_cast<size_t>(H), K = kda::KD, V = kda::VD;
     const size_t T = static_cast<size_t>(plan[KDA_PH_T]), N = static_cast<size_t>(plan[KDA_PH_N]);
     const size_t S = static_cast<size_t>(plan[KDA_PH_S]), C = static_cast<size_t>(plan[KDA_PH_NCHUNKS]);
-    const size_t sizes[8] = {T * h * V * 2, N * h * K * V * 4, h * C * K * V * 4, h * C * K * V * 4,
+    const size_t sizes[9] = {T * h * V * 2, N * h * K * V * 4, h * C * K * V * 4, h * C * K * V * 4,
                              S * h * K * V * 4, S * h * K * V * 4,
                              static_cast<size_t>(kBackwardGrid) * kda::backward_scratch_floats() * 4,
-                             h * C * kda::backward_terms_floats() * 4};
+                             h * C * kda::backward_terms_floats() * 4, h * C * kda::RIMG_UNIT};
     size_t pos = fw[6];
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 9; ++i) {
         off[i] = pos;
         pos = round256(pos + sizes[i]);
     }
-    off[8] = pos;
+    off[9] = pos;
     return true;
 }
 
@@ -459,8 +459,8 @@ bool backward_layout(const int32_t *plan, int32_t H, size_t off[9])
 
 extern "C" size_t kda_backward_workspace_bytes(const int32_t *plan, int32_t H)
 {
-    size_t off[9];
-    return backward_layout(plan, H, off) ? off[8] : 0;
+    size_t off[10];
+    return backward_layout(plan, H, off) ? off[9] : 0;
 }
 
 extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t H,
@@ -469,7 +469,7 @@ extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_d
                                       const float *dfinal, float *dq, float *dk, float *dv, float *dg,
                                       float *dbeta, float *dh0, void *ws, size_t ws_bytes, void *stream)
 {
-    size_t fw[7], off[9];
+    size_t fw[7], off[10];
     if (!layout(plan, H, fw) || !backward_layout(plan, H, off) || !plan_dev) return KDA_ERR_INVALID_ARG;
     if (!inputs_ok(q, k, v, g, beta, h0)) return KDA_ERR_INVALID_ARG;
     if (!dout || !aligned16(dout) || (dfinal && !aligned16(dfinal)) || (dh0 && !aligned16(dh0)))
@@ -478,7 +478,7 @@ extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_d
         !aligned16(dg) || !aligned16(dbeta))
         return KDA_ERR_INVALID_ARG;
     if (!ws || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
-    if (ws_bytes < off[8]) return KDA_ERR_WORKSPACE;
+    if (ws_bytes < off[9]) return KDA_ERR_WORKSPACE;
     const kda::Workspace w = carve(ws, fw);
     char *b = static_cast<char *>(ws);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -500,9 +500,9 @@ extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_d
                                               reinterpret_cast<float *>(b + off[2]), s));
     if (rc != KDA_OK) return rc;
     return cuda_status(kda::launch_backward(
-        plan, plan_dev, H, q, k, v, g, beta, h0, scale, dout, dfinal, w.A, w.afin, w.S_in,
-        reinterpret_cast<float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
+        plan, plan_dev, H, q, k, v, g, beta, scale, dout, dfinal, w.A, w.afin,
+        reinterpret_cast<const float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
         reinterpret_cast<float *>(b + off[4]), reinterpret_cast<float *>(b + off[5]),
-        reinterpret_cast<float *>(b + off[7]), reinterpret_cast<float *>(b + off[6]), kBackwardGrid, dq, dk, dv, dg,
-        dbeta, dh0, s));
+        reinterpret_cast<float *>(b + off[7]), reinterpret_cast<unsigned char *>(b + off[8]),
+        reinterpret_cast<float *>(b + off[6]), kBackwardGrid, dq, dk, dv, dg, dbeta, dh0, s));
 }

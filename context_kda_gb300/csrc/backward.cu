@@ -500,37 +500,6 @@ __device__ void load_do(float *sc, int t0, int L, int h, int H, const uint16_t *
     __syncthreads();
 }
 
-// The chains carry the state (or its gradient) in column slices: every product of a chain step
-// multiplies into the state's columns, so the NS slices of SW columns are independent chains.
-constexpr int NS = 2, SW = VD / NS;
-
-// dst = src on columns c0 .. c0 + SW of a 128-row state (row stride VD), every thread's loads first
-__device__ __forceinline__ void copy_slice(float *dst, const float *src, int c0)
-{
-    constexpr int P = KD * SW / 4 / BT;
-    float4 v[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int e = threadIdx.x + i * BT;
-        v[i] = ld4(src + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)));
-    }
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int e = threadIdx.x + i * BT;
-        st4(dst + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)), v[i]);
-    }
-}
-
-// dst = 0 on columns c0 .. c0 + SW of a 128-row state
-__device__ __forceinline__ void zero_slice(float *dst, int c0)
-{
-#pragma unroll
-    for (int i = 0; i < KD * SW / 4 / BT; ++i) {
-        const int e = threadIdx.x + i * BT;
-        st4(dst + (e / (SW / 4)) * VD + c0 + 4 * (e % (SW / 4)), make_float4(0.f, 0.f, 0.f, 0.f));
-    }
-}
-
 // dst = Diag(d) src for a whole 128 x 128 state, every thread's loads first
 __device__ __forceinline__ void scale_rows(float *dst, const float *src, const float *d)
 {
@@ -545,54 +514,57 @@ __device__ __forceinline__ void scale_rows(float *dst, const float *src, const f
     }
 }
 
-// The chunk's output gradient rows, columns c0 .. c0 + SW, into scratch (zero past L), bf16 -> fp32.
-__device__ void load_do_slice(float *sc, int t0, int L, int h, int H, const uint16_t *dout, int c0)
+// Rows 0..63 of an FP32 array (row stride ld) of C columns as a bf16 hi/lo image in the reverse chains'
+// layout (8-column chunks of 64 rows x 16 bytes, RIMG_CS apart); the lanes of a warp take consecutive
+// rows of one piece, so each store instruction writes 512 contiguous bytes.
+template <int C>
+__device__ __forceinline__ void put_image(unsigned char *hi, unsigned char *lo, const float *src, int ld)
 {
-    constexpr int P = 64 * SW / 8 / BT;
-    uint4 w[P];
+    constexpr int P = 64 * C / 8 / BT;
+    float4 x[2 * P];
 #pragma unroll
     for (int i = 0; i < P; ++i) {
-        const int e = threadIdx.x + i * BT, r = e / (SW / 8), c8 = c0 + 8 * (e % (SW / 8));
+        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
+        x[2 * i] = ld4(src + r * ld + c8);
+        x[2 * i + 1] = ld4(src + r * ld + c8 + 4);
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
+        uint32_t hh[4], ll[4];
+        split_bf16x2(x[2 * i].x, x[2 * i].y, hh[0], ll[0]);
+        split_bf16x2(x[2 * i].z, x[2 * i].w, hh[1], ll[1]);
+        split_bf16x2(x[2 * i + 1].x, x[2 * i + 1].y, hh[2], ll[2]);
+        split_bf16x2(x[2 * i + 1].z, x[2 * i + 1].w, hh[3], ll[3]);
+        const uint32_t off = cm_off(r, c8, RIMG_CS);
+        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+    }
+}
+
+// The chunk's images for the reverse chains: Kh, QK, Qt and W as bf16 pairs, dO (bf16, rows past L
+// zero) and exp(Gamma_C), from the rows in scratch and the products in the stored terms.
+__device__ void put_reverse_images(unsigned char *im, const float *sc, const float *tm, const uint16_t *dout, int t0,
+                                   int L, int h, int H)
+{
+    put_image<KD>(im + RIMG_KH, im + RIMG_KH + 16384, sc + S_KH, KD);
+    put_image<64>(im + RIMG_QK, im + RIMG_QK + 8192, tm + TM_QK, 64);
+    put_image<KD>(im + RIMG_QT, im + RIMG_QT + 16384, sc + S_QT, KD);
+    put_image<KD>(im + RIMG_W, im + RIMG_W + 16384, tm + TM_W, KD);
+    uint4 w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
         w[i] = r < L ? *reinterpret_cast<const uint4 *>(dout + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
                      : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int e = threadIdx.x + i * BT, r = e / (SW / 8), c8 = c0 + 8 * (e % (SW / 8));
-        float x[8];
-        bf8(w[i], x);
-        st4(sc + S_DO + r * VD + c8, make_float4(x[0], x[1], x[2], x[3]));
-        st4(sc + S_DO + r * VD + c8 + 4, make_float4(x[4], x[5], x[6], x[7]));
+    for (int i = 0; i < 4; ++i) {
+        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
+        *reinterpret_cast<uint4 *>(im + RIMG_DO + cm_off(r, c8, RIMG_CS)) = w[i];
     }
-    __syncthreads();
-}
-
-// G <- DG + Qt^T dO - W^T (Kh DG + QK^T dO), DG = Dc G (the gradient reaching the chunk start), on
-// columns c0 .. c0 + SW, the chunk's terms at tm
-__device__ void reverse_step(float *sc, const float *tm, int c0)
-{
-    float *G = sc + S_G, *dU = sc + S_DU;
-    const float *dO = sc + S_DO;
-    product<64, SW, KD, false, false, 64, true, false>(
-        term(tm + TM_KH, KD, G + c0, VD, 1.f, tm + TM_GC), term(tm + TM_QK, 64, dO + c0, VD),
-        out(dU + c0, VD));                                                                          // Kh DG + QK^T dO
-    product<KD, SW, 64, true, false, 64, true, false>(
-        term(tm + TM_QT, KD, dO + c0, VD), term(tm + TM_W, KD, dU + c0, VD, -1.f),
-        out(G + c0, VD, 1.f, G + c0, VD, tm + TM_GC));                                              // DG + Qt^T dO - W^T dU
-}
-
-// Plan helpers
-struct PieceInfo {
-    int start, len, seq, seg, flags, nch, c0;   // c0: global index of the piece's first chunk
-};
-__device__ PieceInfo piece_info(const PlanView &pv, int p)
-{
-    const int32_t *pc = pv.piece(p);
-    PieceInfo pi{pc[PC_START], pc[PC_LEN], pc[PC_SEQ], pc[PC_SEG], pc[PC_FLAGS], (pc[PC_LEN] + CH - 1) / CH, 0};
-    int c0 = 0;
-    for (int i = 0; i < p; ++i) c0 += (pv.piece(i)[PC_LEN] + CH - 1) / CH;
-    pi.c0 = c0;
-    return pi;
+    if (threadIdx.x < KD / 4)
+        st4(reinterpret_cast<float *>(im + RIMG_GC) + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
 }
 
 #define BWD_PLAN_CHECK()                                                                  \
@@ -604,7 +576,8 @@ __device__ PieceInfo piece_info(const PlanView &pv, int p)
 // 0. every (chunk, head) in parallel: the terms the chains need, stored at terms[h][c]
 __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
                                                 const uint16_t *k, const uint16_t *v, const float *g,
-                                                const float *beta, float scale, float *terms, float *scratch)
+                                                const float *beta, float scale, const uint16_t *dout, float *terms,
+                                                unsigned char *img, float *scratch)
 {
     BWD_PLAN_CHECK();
     tc_begin();
@@ -617,56 +590,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
         float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;
         chunk_rows(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
         chunk_products(sc, tm);
+        put_reverse_images(img + static_cast<size_t>(unit) * RIMG_UNIT, sc, tm, dout, cr[1], cr[2], h, H);
         copy_f<CK>(tm + TM_KH, sc + S_KH);
         copy_f<CK>(tm + TM_QT, sc + S_QT);
         if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
-        __syncthreads();
-    }
-    tc_end();
-}
-
-// 2 (LOCAL) / 4 (TRUE). Pieces backwards over their chunks.  LOCAL: pieces that continue a sequence,
-// from a zero end gradient; the gradient reaching the piece start is Qd[seg].  TRUE: every piece from
-// its true end gradient (dfinal of its sequence when it ends it, else G_end[seg]); records G_c =
-// gs[h][c], the gradient of each chunk's end state, and gives dh0 at a sequence start.
-template <bool TRUE_PASS>
-__global__ void __launch_bounds__(BT, 1) bwd_reverse(const int32_t *plan, PlanSig sig, int H, const float *terms,
-                                                  const uint16_t *dout, const float *dfinal, const float *G_end,
-                                                  float *Qd, float *gs, float *dh0, float *scratch)
-{
-    BWD_PLAN_CHECK();
-    tc_begin();
-    const PlanView pv{plan};
-    float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
-    const int n_items = pv.n_pieces() * H * NS;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int ph = item / NS, c0 = (item % NS) * SW;
-        const int p = ph / H, h = ph % H;
-        const PieceInfo pi = piece_info(pv, p);
-        if (!TRUE_PASS && !(pi.flags & KDA_PIECE_CONT)) continue;
-        const float *src = nullptr;
-        if (TRUE_PASS) {
-            if (pi.flags & KDA_PIECE_SEQ_END) {
-                if (dfinal) src = dfinal + (static_cast<size_t>(pi.seq) * H + h) * SQ;
-            } else {
-                src = G_end + (static_cast<size_t>(pi.seg) * H + h) * SQ;
-            }
-        }
-        if (src) copy_slice(sc + S_G, src, c0);
-        else zero_slice(sc + S_G, c0);
-        __syncthreads();
-        for (int ci = pi.nch - 1; ci >= 0; --ci) {
-            const size_t unit = static_cast<size_t>(h) * pv.n_chunks() + pi.c0 + ci;
-            if (TRUE_PASS) copy_slice(gs + unit * SQ, sc + S_G, c0);
-            const int t0 = pi.start + ci * CH, L = min(CH, pi.len - ci * CH);
-            load_do_slice(sc, t0, L, h, H, dout, c0);
-            reverse_step(sc, terms + unit * TERMS_FLOATS, c0);
-        }
-        __syncthreads();
-        float *dst = nullptr;
-        if (!TRUE_PASS) dst = Qd + (static_cast<size_t>(pi.seg) * H + h) * SQ;
-        else if ((pi.flags & KDA_PIECE_FIRST) && dh0) dst = dh0 + (static_cast<size_t>(pi.seq) * H + h) * SQ;
-        if (dst) copy_slice(dst, sc + S_G, c0);
         __syncthreads();
     }
     tc_end();
@@ -898,32 +825,29 @@ size_t backward_scratch_floats() { return static_cast<size_t>(SCRATCH_FLOATS); }
 size_t backward_terms_floats() { return static_cast<size_t>(TERMS_FLOATS); }
 
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
-                            const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
-                            const float *h0, float scale, const uint16_t *dout, const float *dfinal,
-                            const float *A, const float *afin, const float *S_in, float *xs, float *gs,
-                            float *G_end, float *Qd, float *terms, float *scratch, int grid, float *dq, float *dk,
-                            float *dv, float *dg, float *dbeta, float *dh0, cudaStream_t stream)
+                            const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
+                            const uint16_t *dout, const float *dfinal, const float *A, const float *afin,
+                            const float *xs, float *gs, float *G_end, float *Qd, float *terms, unsigned char *img,
+                            float *scratch, int grid, float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                            float *dh0, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
     const PlanSig sig = plan_sig(plan_host);
-    for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_reverse<false>),
-                    reinterpret_cast<const void *>(bwd_reverse<true>), reinterpret_cast<const void *>(bwd_grads)}) {
+    for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_grads)}) {
         const cudaError_t e = set_dynamic_smem(fn, static_cast<int>(BWD_SMEM));
         if (e != cudaSuccess) return e;
     }
-    bwd_terms<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, terms, scratch);
+    bwd_terms<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, terms, img, scratch);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (pv.n_cont() > 0) {
-        bwd_reverse<false><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, dout, dfinal, G_end, Qd, gs, dh0,
-                                                           scratch);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = launch_reverse_tc(plan_host, plan_dev, H, false, img, dfinal, G_end, Qd, gs, dh0, stream);
+        if (err != cudaSuccess) return err;
     }
     bwd_compose<<<H * 4, BT, 0, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    bwd_reverse<true><<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, terms, dout, dfinal, G_end, Qd, gs, dh0,
-                                                      scratch);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_reverse_tc(plan_host, plan_dev, H, true, img, dfinal, G_end, Qd, gs, dh0, stream);
+    if (err != cudaSuccess) return err;
     bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, terms, dq, dk,
                                               dv, dg, dbeta, scratch);
     return cudaGetLastError();

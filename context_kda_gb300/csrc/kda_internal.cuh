@@ -171,12 +171,26 @@ size_t scan_scratch_bytes(const int32_t *plan_host, int H);
 // [S][H][K][V] each.
 size_t backward_scratch_floats();
 size_t backward_terms_floats();   // per (head, chunk)
+// Per-(chunk, head) operand images of the backward's reverse chains, written by its terms pass (bytes):
+// bf16 tiles of 64 rows in the no-swizzle canonical layout (8-column chunks of 64 rows x 16 bytes,
+// chunk stride RIMG_CS), hi then lo where split.  The part the first product of a chain step reads
+// (Kh rows r x cols k, QK rows r' x cols r, dO rows r x cols v, exp(Gamma_C) as 128 fp32) comes
+// first, then the part the second reads (Qt and W, rows r x cols k).
+constexpr uint32_t RIMG_CS = 1024;
+constexpr uint32_t RIMG_KH = 0, RIMG_QK = 32768, RIMG_DO = 49152, RIMG_GC = 65536, RIMG_A_BYTES = 66048;
+constexpr uint32_t RIMG_QT = 66560, RIMG_W = RIMG_QT + 32768, RIMG_B_BYTES = 65536;
+constexpr uint32_t RIMG_UNIT = RIMG_QT + RIMG_B_BYTES;
+static_assert(RIMG_UNIT % 1024 == 0 && RIMG_QT % 1024 == 0 && RIMG_A_BYTES % 16 == 0, "image layout");
+cudaError_t launch_reverse_tc(const int32_t *plan_host, const int32_t *plan_dev, int H, bool true_pass,
+                              const unsigned char *img, const float *dfinal, const float *G_end, float *Qd,
+                              float *gs, float *dh0, cudaStream_t stream);
+int take_reverse_status();
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
-                            const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
-                            const float *h0, float scale, const uint16_t *dout, const float *dfinal,
-                            const float *A, const float *afin, const float *S_in, float *xs, float *gs,
-                            float *G_end, float *Qd, float *terms, float *scratch, int grid, float *dq, float *dk,
-                            float *dv, float *dg, float *dbeta, float *dh0, cudaStream_t stream);
+                            const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
+                            const uint16_t *dout, const float *dfinal, const float *A, const float *afin,
+                            const float *xs, float *gs, float *G_end, float *Qd, float *terms, unsigned char *img,
+                            float *scratch, int grid, float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                            float *dh0, cudaStream_t stream);
 // Segments per group of the blocked scan (about sqrt(S)) and the number of groups.
 int scan_group_size(int S);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
