@@ -15,23 +15,24 @@
 //
 // Steps (after the forward's own preparation, state pass and composition, which give S_in, the
 // segment transitions A and the final-state transitions of continuing pieces):
-//  0. every (chunk, head) in parallel: the chunk's terms that the chains need (W, Ut, Kh, Qt, QK, Dc);
+//  0. every (chunk, head) in parallel: the chunk's terms (W, Ut, Kh, Qt, QK, S, T, Dc) for the gradient
+//     pass, and the reverse chains' bf16 operand images;
 //  1. every piece from its true incoming state (h0, or S_in of its segment), recording each chunk's
 //     start state X_c: the forward's state pass in its output mode (the caller launches it);
-//  2. every piece that continues a sequence, backwards from a zero end gradient: the gradient of its
+//  2. (reverse.cu) every piece that continues a sequence, backwards from a zero end gradient: the gradient of its
 //     incoming state through its own outputs, Qd (the qhat do^T sum of the pages' summaries);
 //  3. the following summaries, last segment first: the gradient of the state crossing the end of
 //     segment j is dfinal of a sequence that ends there, or Qd[j+1] plus the transposed map of the
 //     continuing piece of segment j+1 (A[j+1]^T, or P_end^T of a piece that ends its sequence
 //     there, on dfinal) applied to the gradient at that piece's end;
-//  4. every piece backwards from its true end gradient, recording each chunk's end gradient G_c and
+//  4. (reverse.cu) every piece backwards from its true end gradient, recording each chunk's end gradient G_c and
 //     giving dh0 at a sequence start;
 //  5. every (chunk, head) in parallel: dq, dk, dv, dg, dbeta from (X_c, G_c, dO).
 //
-// Each CTA keeps its chunk's matrices in FP32 in a private scratch area in global memory and runs every
-// product on the tensor cores (both operands staged in shared memory as bf16 hi/lo pairs, a three-term
-// split accumulated in FP32 in TMEM), which keeps every step a literal transcription of the formulas
-// above.  The chains carry the state and its gradient in two 64-column slices per (piece, head).
+// The terms and gradient passes here keep a chunk's matrices in FP32 in a private scratch area in global
+// memory and run every product on the tensor cores (both operands staged in shared memory as bf16 hi/lo
+// pairs, a three-term split accumulated in FP32 in TMEM), which keeps every step a literal transcription
+// of the formulas above.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
