@@ -57,7 +57,12 @@ enum : int {
     S_DBKT = S_BV + CK, S_DBV = S_DBKT + CK,
     S_DQK = S_DBV + CK, S_DT = S_DQK + CC, S_DM = S_DT + CC, S_T64 = S_DM + CC,
     S_GC = S_T64 + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64, S_DBETA = S_DGC + KD,
-    SCRATCH_FLOATS = S_DBETA + 64
+    // bf16 hi/lo images of the gradient pass's operands (bytes / 4): X and DG (128 x 128), T (64 x 64),
+    // beta Kt (64 x 128), and the products U, dQK, dU, dW, dT, T^T dT, dM
+    S_IMG = (S_DBETA + 64 + 255) & ~255, S_XI = S_IMG, S_DGI = S_XI + SQ, S_TI = S_DGI + SQ, S_BKTI = S_TI + CC,
+    S_UI = S_BKTI + CK, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
+    S_T64I = S_DTI + CC, S_DMI = S_T64I + CC, S_IMG_END = S_DMI + CC,
+    SCRATCH_FLOATS = S_IMG_END
 };
 
 // The chunk's terms the chains and the gradient pass read, stored per (head, chunk) by the terms pass
@@ -71,6 +76,8 @@ constexpr size_t BWD_SMEM = 6ull * 32768 + 1024;   // the operand tiles of a two
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 __device__ __forceinline__ int warp_id() { return static_cast<int>(threadIdx.x) >> 5; }
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+// Orders this thread's generic-proxy global writes before later bulk (async-proxy) reads of them.
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
@@ -99,15 +106,18 @@ __device__ __forceinline__ void copy_f(float *dst, const float *src)
 // of its next phase, and a flag raised when a bounded wait gave up (every later product of the CTA
 // is then skipped, and the kernel reports KDA_ERR_TIMEOUT).
 __shared__ __align__(8) uint64_t s_tc_bar;
-__shared__ uint32_t s_tc_tmem, s_tc_phase, s_tc_fail;
+__shared__ __align__(8) uint64_t s_tc_ld;   // a product's operand images landed (bulk copies)
+__shared__ uint32_t s_tc_tmem, s_tc_phase, s_tc_fail, s_tc_ldph;
 constexpr uint32_t TC_COLS = 128;
 
 __device__ void tc_begin()
 {
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&s_tc_bar), 1);
+        mbar_init(smem_u32(&s_tc_ld), 1);
         s_tc_phase = 0;
         s_tc_fail = 0;
+        s_tc_ldph = 0;
     }
     if (threadIdx.x < 32) tmem_alloc(smem_u32(&s_tc_tmem), TC_COLS);
     fence_before();
@@ -150,8 +160,9 @@ struct Stage {
             v[2 * i + 1] = ld4(src + r * ld + c8 + 4);
         }
     }
+    // save, when set: the same split also into a global image (hi, then lo R * C * 2 bytes on)
     __device__ __forceinline__ void store(unsigned char *hi, unsigned char *lo, uint32_t cs, const float *rows_scale,
-                                          float s)
+                                          float s, unsigned char *save)
     {
 #pragma unroll
         for (int i = 0; i < P; ++i) {
@@ -164,14 +175,23 @@ struct Stage {
             split_bf16x2(x1.x, x1.y, h[2], l[2]);
             split_bf16x2(x1.z, x1.w, h[3], l[3]);
             const uint32_t off = cm_off(r, c8, cs);
-            *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+            const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]), lv = make_uint4(l[0], l[1], l[2], l[3]);
+            *reinterpret_cast<uint4 *>(hi + off) = hv;
+            *reinterpret_cast<uint4 *>(lo + off) = lv;
+            if (save) {
+                *reinterpret_cast<uint4 *>(save + off) = hv;
+                *reinterpret_cast<uint4 *>(save + R * C * 2 + off) = lv;
+            }
         }
     }
 };
 
 // One term A B of a product: A(m, k) = TA ? a[k * lda + m] : a[m * lda + k], B(k, n) = TB ? b[n * ldb + k]
-// : b[k * ldb + n], scaled by s; b_rows, when set (only with !TB), multiplies B's row k.
+// : b[k * ldb + n], scaled by s; b_rows, when set (only with !TB), multiplies B's row k.  An operand may
+// instead come as an image in global memory (ia / ib): the bf16 hi/lo split of its source as it lies
+// (R rows of its contiguous index, chunk stride R * 16, lo R * C * 2 bytes after hi; a single image
+// holds only hi, the operand being exact in bf16, and the products with its lo part are skipped),
+// brought in by a bulk copy; a staged operand may leave its split in such an image (sa / sb).
 struct Term {
     const float *a;
     int lda;
@@ -179,16 +199,41 @@ struct Term {
     int ldb;
     float s;
     const float *b_rows;
+    const unsigned char *ia, *ib;
+    unsigned char *sa, *sb;
+    bool a_single, b_single;
 };
 __device__ __forceinline__ Term term(const float *a, int lda, const float *b, int ldb, float s = 1.f,
                                      const float *b_rows = nullptr)
 {
-    return Term{a, lda, b, ldb, s, b_rows};
+    return Term{a, lda, b, ldb, s, b_rows, nullptr, nullptr, nullptr, nullptr, false, false};
+}
+__device__ __forceinline__ Term img_a(Term t, const unsigned char *p, bool single = false)
+{
+    t.ia = p;
+    t.a_single = single;
+    return t;
+}
+__device__ __forceinline__ Term img_b(Term t, const unsigned char *p, bool single = false)
+{
+    t.ib = p;
+    t.b_single = single;
+    return t;
+}
+__device__ __forceinline__ Term save_a(Term t, unsigned char *p)
+{
+    t.sa = p;
+    return t;
+}
+__device__ __forceinline__ Term save_b(Term t, unsigned char *p)
+{
+    t.sb = p;
+    return t;
 }
 
 // The output of a product: C[m][n] = out_rows[m] * (alpha * sum of the terms + in_rows[m] * cin[m][n]),
 // each factor or input omitted when its pointer is null; MASK 1 keeps n <= m, MASK 2 n < m (zero
-// elsewhere).
+// elsewhere).  c may be null; img, when set, receives the result's bf16 hi/lo image as it lies (M rows).
 struct Out {
     float *c;
     int ldc;
@@ -197,20 +242,28 @@ struct Out {
     int ldcin;
     const float *in_rows;
     const float *out_rows;
+    unsigned char *img;
 };
 __device__ __forceinline__ Out out(float *c, int ldc, float alpha = 1.f, const float *cin = nullptr, int ldcin = 0,
                                    const float *in_rows = nullptr, const float *out_rows = nullptr)
 {
-    return Out{c, ldc, alpha, cin, ldcin, in_rows, out_rows};
+    return Out{c, ldc, alpha, cin, ldcin, in_rows, out_rows, nullptr};
+}
+__device__ __forceinline__ Out out_img(Out o, unsigned char *img)
+{
+    o.img = img;
+    return o;
 }
 
 // An M x N product of one or two terms (K1- and K2-long sums; K2 = 0: one term; M, N, K in {64, 128})
 // by all threads of the CTA.  Every operand is copied as it lies (rows of its contiguous index) into the
-// no-swizzle canonical layout as a bf16 hi/lo pair and read by the tensor core K-major or MN-major
-// accordingly, so nothing is transposed on the way; each term is the 3-term split hi*hi + hi*lo + lo*hi
-// (~2^-16 relative), both terms accumulate in FP32 in one TMEM accumulator, M = 128 (a 64-row A fills
-// half the lanes, the rest are never read).  All operand loads are issued before the first staging
-// store, and the accumulated input is loaded while the tensor core works.
+// no-swizzle canonical layout as a bf16 hi/lo pair (chunk stride: its rows x 16) and read by the tensor
+// core K-major or MN-major accordingly, so nothing is transposed on the way; each term is the split
+// hi*hi + hi*lo + lo*hi (~2^-16 relative; without the products of a single operand's absent lo part),
+// both terms accumulate in FP32 in one TMEM accumulator, M = 128 (a 64-row A fills half the lanes: the
+// rows the tensor core reads past it land in lanes that are never read).  Image operands arrive by bulk
+// copies issued first; every staged operand's loads are issued before its first store; the accumulated
+// input is loaded while the tensor core works.
 template <int M, int N, int K1, bool TA1, bool TB1, int K2 = 0, bool TA2 = false, bool TB2 = false, int MASK = 0>
 __device__ void product(const Term t1, const Term t2, const Out o)
 {
@@ -221,60 +274,90 @@ __device__ void product(const Term t1, const Term t2, const Out o)
     constexpr int K2E = K2 ? K2 : 64;   // shapes of the (unused when K2 = 0) second term
     constexpr int RA1 = TA1 ? K1 : M, CA1 = TA1 ? M : K1, RB1 = TB1 ? N : K1, CB1 = TB1 ? K1 : N;
     constexpr int RA2 = TA2 ? K2E : M, CA2 = TA2 ? M : K2E, RB2 = TB2 ? N : K2E, CB2 = TB2 ? K2E : N;
-    constexpr uint32_t CSA1 = TA1 ? K1 * 16 : 128 * 16, CSB1 = RB1 * 16;
-    constexpr uint32_t CSA2 = TA2 ? K2E * 16 : 128 * 16, CSB2 = RB2 * 16;
+    constexpr uint32_t CSA1 = RA1 * 16, CSB1 = RB1 * 16, CSA2 = RA2 * 16, CSB2 = RB2 * 16;
     constexpr uint32_t A1B = 128 * K1 * 2, B1B = N * K1 * 2, A2B = 128 * K2E * 2, B2B = N * K2E * 2;
     static_assert(2 * (A1B + B1B + (K2 ? A2B + B2B : 0)) <= BWD_SMEM - 1024, "the operand tiles fit");
     unsigned char *const a1h = tc_tiles(), *const a1l = a1h + A1B, *const b1h = a1l + A1B, *const b1l = b1h + B1B;
     unsigned char *const a2h = b1l + B1B, *const a2l = a2h + A2B, *const b2h = a2l + A2B, *const b2l = b2h + B2B;
+    const bool any_img = t1.ia || t1.ib || (K2 != 0 && (t2.ia || t2.ib));
+    if (tid == 0 && any_img) {   // image operands: bulk copies into the tiles, counted on s_tc_ld
+        const uint32_t ld = smem_u32(&s_tc_ld);
+        uint32_t bytes = 0;
+        auto part = [&](const unsigned char *img, bool single, uint32_t nbytes) {
+            if (img) bytes += single ? nbytes : 2 * nbytes;
+        };
+        part(t1.ia, t1.a_single, RA1 * CA1 * 2);
+        part(t1.ib, t1.b_single, RB1 * CB1 * 2);
+        if (K2 != 0) {
+            part(t2.ia, t2.a_single, RA2 * CA2 * 2);
+            part(t2.ib, t2.b_single, RB2 * CB2 * 2);
+        }
+        mbar_arrive_expect_tx(ld, bytes);
+        auto copy = [&](const unsigned char *img, bool single, uint32_t nbytes, unsigned char *hi, unsigned char *lo) {
+            if (!img) return;
+            bulk_g2s(smem_u32(hi), img, nbytes, ld);
+            if (!single) bulk_g2s(smem_u32(lo), img + nbytes, nbytes, ld);
+        };
+        copy(t1.ia, t1.a_single, RA1 * CA1 * 2, a1h, a1l);
+        copy(t1.ib, t1.b_single, RB1 * CB1 * 2, b1h, b1l);
+        if (K2 != 0) {
+            copy(t2.ia, t2.a_single, RA2 * CA2 * 2, a2h, a2l);
+            copy(t2.ib, t2.b_single, RB2 * CB2 * 2, b2h, b2l);
+        }
+    }
     {
         Stage<RA1, CA1> sa1;
         Stage<RB1, CB1> sb1;
-        sa1.load(t1.a, t1.lda);
-        sb1.load(t1.b, t1.ldb);
+        if (!t1.ia) sa1.load(t1.a, t1.lda);
+        if (!t1.ib) sb1.load(t1.b, t1.ldb);
         if constexpr (K2 != 0) {
             Stage<RA2, CA2> sa2;
             Stage<RB2, CB2> sb2;
-            sa2.load(t2.a, t2.lda);
-            sb2.load(t2.b, t2.ldb);
-            sa2.store(a2h, a2l, CSA2, nullptr, t2.s);
-            sb2.store(b2h, b2l, CSB2, TB2 ? nullptr : t2.b_rows, 1.f);
+            if (!t2.ia) sa2.load(t2.a, t2.lda);
+            if (!t2.ib) sb2.load(t2.b, t2.ldb);
+            if (!t2.ia) sa2.store(a2h, a2l, CSA2, nullptr, t2.s, t2.sa);
+            if (!t2.ib) sb2.store(b2h, b2l, CSB2, TB2 ? nullptr : t2.b_rows, 1.f, t2.sb);
         }
-        sa1.store(a1h, a1l, CSA1, nullptr, t1.s);
-        sb1.store(b1h, b1l, CSB1, TB1 ? nullptr : t1.b_rows, 1.f);
+        if (!t1.ia) sa1.store(a1h, a1l, CSA1, nullptr, t1.s, t1.sa);
+        if (!t1.ib) sb1.store(b1h, b1l, CSB1, TB1 ? nullptr : t1.b_rows, 1.f, t1.sb);
     }
     fence_async_smem();
+    if (t1.sa || t1.sb || (K2 != 0 && (t2.sa || t2.sb))) fence_async_global();
     __syncthreads();
     fence_after();
     const uint32_t ph = s_tc_phase, tmem = s_tc_tmem, bar = smem_u32(&s_tc_bar);
     if (tid == 0) {
-        const uint32_t ah[3] = {smem_u32(a1h), smem_u32(a1h), smem_u32(a1l)};
-        const uint32_t bh[3] = {smem_u32(b1h), smem_u32(b1l), smem_u32(b1h)};
-        const uint32_t id1 = idesc_bf16(128, N, TA1 ? 1 : 0, TB1 ? 0 : 1);
-#pragma unroll
-        for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-            for (int kk = 0; kk < K1 / 16; ++kk) {
-                const uint64_t ad = TA1 ? sdesc(ah[ps] + kk * 256, 128, CSA1) : sdesc(ah[ps] + kk * 2 * CSA1, CSA1, 128);
-                const uint64_t bd = TB1 ? sdesc(bh[ps] + kk * 2 * CSB1, CSB1, 128) : sdesc(bh[ps] + kk * 256, 128, CSB1);
-                mma_bf16(tmem, ad, bd, id1, (ps | kk) != 0);
-            }
-        if constexpr (K2 != 0) {
-            const uint32_t ah2[3] = {smem_u32(a2h), smem_u32(a2h), smem_u32(a2l)};
-            const uint32_t bh2[3] = {smem_u32(b2h), smem_u32(b2l), smem_u32(b2h)};
-            const uint32_t id2 = idesc_bf16(128, N, TA2 ? 1 : 0, TB2 ? 0 : 1);
-#pragma unroll
-            for (int ps = 0; ps < 3; ++ps)
-#pragma unroll
-                for (int kk = 0; kk < K2 / 16; ++kk) {
-                    const uint64_t ad =
-                        TA2 ? sdesc(ah2[ps] + kk * 256, 128, CSA2) : sdesc(ah2[ps] + kk * 2 * CSA2, CSA2, 128);
-                    const uint64_t bd =
-                        TB2 ? sdesc(bh2[ps] + kk * 2 * CSB2, CSB2, 128) : sdesc(bh2[ps] + kk * 256, 128, CSB2);
-                    mma_bf16(tmem, ad, bd, id2, 1u);
-                }
+        bool ld_ok = true;
+        if (any_img) {
+            ld_ok = mbar_wait(smem_u32(&s_tc_ld), s_tc_ldph);
+            s_tc_ldph ^= 1u;
+            if (!ld_ok) s_tc_fail = 1;
         }
-        commit(bar);
+        bool first = true;
+        // the split terms of one A B pair: hi hi, hi lo (unless B is single), lo hi (unless A is single)
+        auto issue = [&](int K, bool ta, bool tb, uint32_t ah_, uint32_t al_, uint32_t bh_, uint32_t bl_, uint32_t csa,
+                         uint32_t csb, bool a_single, bool b_single) {
+            const uint32_t id = idesc_bf16(128, N, ta ? 1 : 0, tb ? 0 : 1);
+            const uint32_t ah[3] = {ah_, ah_, al_}, bh[3] = {bh_, bl_, bh_};
+            const bool use[3] = {true, !b_single, !a_single};
+            for (int ps = 0; ps < 3; ++ps) {
+                if (!use[ps]) continue;
+                for (int kk = 0; kk < K / 16; ++kk) {
+                    const uint64_t ad = ta ? sdesc(ah[ps] + kk * 256, 128, csa) : sdesc(ah[ps] + kk * 2 * csa, csa, 128);
+                    const uint64_t bd = tb ? sdesc(bh[ps] + kk * 2 * csb, csb, 128) : sdesc(bh[ps] + kk * 256, 128, csb);
+                    mma_bf16(tmem, ad, bd, id, first ? 0u : 1u);
+                    first = false;
+                }
+            }
+        };
+        if (ld_ok) {
+            issue(K1, TA1, TB1, smem_u32(a1h), smem_u32(a1l), smem_u32(b1h), smem_u32(b1l), CSA1, CSB1, t1.ia && t1.a_single,
+                  t1.ib && t1.b_single);
+            if constexpr (K2 != 0)
+                issue(K2, TA2, TB2, smem_u32(a2h), smem_u32(a2l), smem_u32(b2h), smem_u32(b2l), CSA2, CSB2,
+                      t2.ia && t2.a_single, t2.ib && t2.b_single);
+        }
+        commit(bar);   // (with nothing issued, it arrives at once: the readers see the failure flag)
     }
     // row m = this thread's TMEM lane, columns hw * N/2 .. + N/2; the accumulated input is loaded
     // while the tensor core works
@@ -292,28 +375,41 @@ __device__ void product(const Term t1, const Term t2, const Out o)
     const bool ok = mbar_wait_warp(bar, ph);
     fence_after();
     if (ok && live) {
-        float *const crow = o.c + m * o.ldc + n0;
+        float *const crow = o.c ? o.c + m * o.ldc + n0 : nullptr;
 #pragma unroll
         for (int j0 = 0; j0 < N / 2; j0 += 32) {
             float d[32];
             tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + n0 + j0, d);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 o4 = old[j0 / 4 + q4];
-                float r[4] = {fo * (o.alpha * d[4 * q4] + o4.x), fo * (o.alpha * d[4 * q4 + 1] + o4.y),
-                              fo * (o.alpha * d[4 * q4 + 2] + o4.z), fo * (o.alpha * d[4 * q4 + 3] + o4.w)};
-                if constexpr (MASK != 0) {
+            for (int q8 = 0; q8 < 4; ++q8) {
+                float r[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int n = n0 + j0 + 4 * q4 + e;
+                for (int e = 0; e < 8; ++e) {
+                    const float4 o4 = old[(j0 + 8 * q8 + e) / 4];
+                    const float ov = (e & 3) == 0 ? o4.x : (e & 3) == 1 ? o4.y : (e & 3) == 2 ? o4.z : o4.w;
+                    r[e] = fo * (o.alpha * d[8 * q8 + e] + ov);
+                    if constexpr (MASK != 0) {
+                        const int n = n0 + j0 + 8 * q8 + e;
                         if (MASK == 1 ? n > m : n >= m) r[e] = 0.f;
                     }
                 }
-                st4(crow + j0 + 4 * q4, make_float4(r[0], r[1], r[2], r[3]));
+                if (crow) {
+                    st4(crow + j0 + 8 * q8, make_float4(r[0], r[1], r[2], r[3]));
+                    st4(crow + j0 + 8 * q8 + 4, make_float4(r[4], r[5], r[6], r[7]));
+                }
+                if (o.img) {   // the result's image as it lies: rows m (M of them), chunk stride M * 16
+                    uint32_t hh[4], ll[4];
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) split_bf16x2(r[2 * pp], r[2 * pp + 1], hh[pp], ll[pp]);
+                    const uint32_t off = cm_off(m, n0 + j0 + 8 * q8, M * 16);
+                    *reinterpret_cast<uint4 *>(o.img + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                    *reinterpret_cast<uint4 *>(o.img + M * N * 2 + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                }
             }
         }
     }
     if (!ok) s_tc_fail = 1;
+    if (o.img) fence_async_global();
     fence_before();
     __syncthreads();
     if (tid == 0) s_tc_phase = ph ^ 1u;
@@ -480,40 +576,6 @@ __device__ void chunk_products(const float *sc, float *tm)
     product<64, VD, 64, false, false>(term(tm + TM_T, 64, sc + S_BV, VD), Term{}, out(tm + TM_UT, VD));
 }
 
-// The chunk's output gradient rows into scratch (zero past L), bf16 -> fp32.
-__device__ void load_do(float *sc, int t0, int L, int h, int H, const uint16_t *dout)
-{
-    uint4 w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int e = threadIdx.x + i * BT, r = e >> 4, c8 = (e & 15) << 3;
-        w[i] = r < L ? *reinterpret_cast<const uint4 *>(dout + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
-                     : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int e = threadIdx.x + i * BT, r = e >> 4, c8 = (e & 15) << 3;
-        float x[8];
-        bf8(w[i], x);
-        st4(sc + S_DO + r * VD + c8, make_float4(x[0], x[1], x[2], x[3]));
-        st4(sc + S_DO + r * VD + c8 + 4, make_float4(x[4], x[5], x[6], x[7]));
-    }
-    __syncthreads();
-}
-
-// dst = Diag(d) src for a whole 128 x 128 state, every thread's loads first
-__device__ __forceinline__ void scale_rows(float *dst, const float *src, const float *d)
-{
-    constexpr int P = SQ / 4 / BT;
-    float4 v[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) v[i] = ld4(src + 4 * (threadIdx.x + i * BT));
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int e = 4 * (threadIdx.x + i * BT);
-        st4(dst + e, scl4(d[e >> 7], v[i]));
-    }
-}
 
 // Rows 0..63 of an FP32 array (row stride ld) of C columns as a bf16 hi/lo image in the reverse chains'
 // layout (8-column chunks of 64 rows x 16 bytes, RIMG_CS apart); the lanes of a warp take consecutive
@@ -674,8 +736,9 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
 __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
                                                 const uint16_t *k, const uint16_t *v, const float *g,
                                                 const float *beta, float scale, const uint16_t *dout,
-                                                const float *xs, const float *gs, const float *terms, float *dq,
-                                                float *dk, float *dv, float *dg, float *dbeta, float *scratch)
+                                                const float *xs, const float *gs, const float *terms,
+                                                const unsigned char *img, float *dq, float *dk, float *dv, float *dg,
+                                                float *dbeta, float *scratch)
 {
     BWD_PLAN_CHECK();
     tc_begin();
@@ -688,31 +751,45 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const int32_t *cr = pv.chunk(c);
         const int t0 = cr[1], L = cr[2];
         chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
-        const float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;   // W, Ut, QK, S, T
-        load_do(sc, t0, L, h, H, dout);
-        // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them
+        const float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;   // Ut, S, T
+        // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them;
+        // Kh, QK, Qt, W and dO come as the chunk's operand images; X, DG = Dc G, T and beta Kt leave their
+        // split in an image where they are first staged, and every product whose result feeds another
+        // leaves its result as an image, so later products bring their operands in by bulk copies
         const float *X = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
         const float *G = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
-        float *DG = sc + S_Y, *U = sc + S_U, *dU = sc + S_DU, *dKh = sc + S_DKH, *dQt = sc + S_DQT;
-        float *dW = sc + S_DW, *dQK = sc + S_DQK, *dT = sc + S_DT, *dM = sc + S_DM, *dKt = sc + S_DKT;
-        const float *dO = sc + S_DO, *Kh = sc + S_KH, *Qt = sc + S_QT, *bKt = sc + S_BKT, *bV = sc + S_BV;
-        scale_rows(DG, G, sc + S_GC);   // DG = Dc G
+        const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
+        unsigned char *const sci = reinterpret_cast<unsigned char *>(sc);
+        unsigned char *const xi = sci + 4 * S_XI, *const dgi = sci + 4 * S_DGI, *const ti = sci + 4 * S_TI;
+        unsigned char *const bkti = sci + 4 * S_BKTI, *const ui = sci + 4 * S_UI, *const dqki = sci + 4 * S_DQKI;
+        unsigned char *const dui = sci + 4 * S_DUI, *const dwi = sci + 4 * S_DWI, *const dti = sci + 4 * S_DTI;
+        unsigned char *const t64i = sci + 4 * S_T64I, *const dmi = sci + 4 * S_DMI;
+        float *Y = sc + S_Y, *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dM = sc + S_DM, *dKt = sc + S_DKT;
+        const float *bKt = sc + S_BKT, *bV = sc + S_BV;
+        const Term none = term(nullptr, 0, nullptr, 0);
         __syncthreads();
-        product<64, VD, KD, false, false>(term(tm + TM_W, KD, X, VD), Term{}, out(U, VD, -1.f, tm + TM_UT, VD));  // U = Ut - W X
-        product<64, 64, VD, false, true, 0, false, false, 1>(term(dO, VD, U, VD), Term{}, out(dQK, 64));          // lower(dO U^T)
-        product<64, VD, KD, false, false, 64, true, false>(term(Kh, KD, DG, VD), term(tm + TM_QK, 64, dO, VD),
-                                                           out(dU, VD));                                  // dU = Kh DG + QK^T dO
-        product<64, KD, VD, false, true, 64, true, false>(term(U, VD, DG, VD), term(dQK, 64, Qt, KD),
-                                                          out(dKh, KD));                                  // dKh = U DG^T + dQK^T Qt
-        // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c]: Y = X + Kh^T U in place of DG
-        product<KD, VD, 64, true, false>(term(Kh, KD, U, VD), Term{}, out(DG, VD, 1.f, X, VD));
+        // U = Ut - W X
+        product<64, VD, KD, false, false>(save_b(img_a(term(nullptr, 0, X, VD), im + RIMG_W), xi), none,
+                                          out_img(out(nullptr, 0, -1.f, tm + TM_UT, VD), ui));
+        // dQK = lower(dO U^T)
+        product<64, 64, VD, false, true, 0, false, false, 1>(img_b(img_a(none, im + RIMG_DO, true), ui), none,
+                                                             out_img(out(nullptr, 0), dqki));
+        // dU = Kh DG + QK^T dO (DG = Dc G staged from G)
+        product<64, VD, KD, false, false, 64, true, false>(
+            save_b(img_a(term(nullptr, 0, G, VD, 1.f, sc + S_GC), im + RIMG_KH), dgi),
+            img_b(img_a(none, im + RIMG_QK), im + RIMG_DO, true), out_img(out(nullptr, 0), dui));
+        // dKh = U DG^T + dQK^T Qt
+        product<64, KD, VD, false, true, 64, true, false>(img_b(img_a(none, ui), dgi), img_b(img_a(none, dqki), im + RIMG_QT),
+                                                          out(dKh, KD));
+        // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c]: Y = X + Kh^T U
+        product<KD, VD, 64, true, false>(img_b(img_a(none, im + RIMG_KH), ui), none, out(Y, VD, 1.f, X, VD));
         {   // a warp per 16 rows k, 4 columns a lane, then a warp sum per row
             float4 gv[16], yv[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int e = (warp_id() * 16 + j) * VD + 4 * (tid & 31);
                 gv[j] = ld4(G + e);
-                yv[j] = ld4(DG + e);
+                yv[j] = ld4(Y + e);
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -721,21 +798,26 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 if ((tid & 31) == 0) sc[S_DGC + kr] = sum * sc[S_GC + kr];
             }
         }
-        product<64, KD, VD, false, true, 64, false, false>(term(dO, VD, X, VD), term(dQK, 64, Kh, KD),
-                                                           out(dQt, KD));                                 // dQt = dO X^T + dQK Kh
-        product<64, KD, VD, false, true>(term(dU, VD, X, VD), Term{}, out(dW, KD, -1.f));               // dW = -dU X^T
-        product<64, 64, KD, false, true, VD, false, true>(term(dW, KD, bKt, KD), term(dU, VD, bV, VD),
-                                                          out(dT, 64));                                   // dT = dW bKt^T + dU bV^T
-        product<64, KD, 64, true, false>(term(tm + TM_T, 64, dW, KD), Term{}, out(sc + S_DBKT, KD));      // d(bKt) = T^T dW
-        product<64, VD, 64, true, false>(term(tm + TM_T, 64, dU, VD), Term{}, out(sc + S_DBV, VD));       // d(bV) = T^T dU
+        // dQt = dO X^T + dQK Kh
+        product<64, KD, VD, false, true, 64, false, false>(img_b(img_a(none, im + RIMG_DO, true), xi),
+                                                           img_b(img_a(none, dqki), im + RIMG_KH), out(dQt, KD));
+        // dW = -dU X^T
+        product<64, KD, VD, false, true>(img_b(img_a(none, dui), xi), none, out_img(out(nullptr, 0, -1.f), dwi));
+        // dT = dW (beta Kt)^T + dU (beta V)^T
+        product<64, 64, KD, false, true, VD, false, true>(save_b(img_a(term(nullptr, 0, bKt, KD), dwi), bkti),
+                                                          img_a(term(nullptr, 0, bV, VD), dui), out_img(out(nullptr, 0), dti));
+        // d(beta Kt) = T^T dW, d(beta V) = T^T dU
+        product<64, KD, 64, true, false>(save_a(img_b(term(tm + TM_T, 64, nullptr, 0), dwi), ti), none,
+                                         out(sc + S_DBKT, KD));
+        product<64, VD, 64, true, false>(img_b(img_a(none, ti), dui), none, out(sc + S_DBV, VD));
         // dM = strictly_lower(-T^T dT T^T)
-        product<64, 64, 64, true, false>(term(tm + TM_T, 64, dT, 64), Term{}, out(sc + S_T64, 64));
-        product<64, 64, 64, false, true, 0, false, false, 2>(term(sc + S_T64, 64, tm + TM_T, 64), Term{},
-                                                             out(dM, 64, -1.f));
-        // dKt = beta (d(bKt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(bV)
-        product<64, KD, 64, false, false>(term(dM, 64, Kh, KD), Term{},
+        product<64, 64, 64, true, false>(img_b(img_a(none, ti), dti), none, out_img(out(nullptr, 0), t64i));
+        product<64, 64, 64, false, true, 0, false, false, 2>(img_b(img_a(none, t64i), ti), none,
+                                                             out_img(out(dM, 64, -1.f), dmi));
+        // dKt = beta (d(beta Kt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(beta V)
+        product<64, KD, 64, false, false>(img_b(img_a(none, dmi), im + RIMG_KH), none,
                                           out(dKt, KD, 1.f, sc + S_DBKT, KD, nullptr, sc + S_BT));
-        product<64, KD, 64, true, false>(term(dM, 64, bKt, KD), Term{}, out(dKh, KD, 1.f, dKh, KD));
+        product<64, KD, 64, true, false>(img_b(img_a(none, dmi), bkti), none, out(dKh, KD, 1.f, dKh, KD));
         // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S): a warp per 8 rows, then a warp sum
         {
             const int ln = tid & 31;
@@ -849,8 +931,8 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     err = launch_reverse_tc(plan_host, plan_dev, H, true, img, dfinal, G_end, Qd, gs, dh0, stream);
     if (err != cudaSuccess) return err;
-    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, terms, dq, dk,
-                                              dv, dg, dbeta, scratch);
+    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, terms, img,
+                                              dq, dk, dv, dg, dbeta, scratch);
     return cudaGetLastError();
 }
 
