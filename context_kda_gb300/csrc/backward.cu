@@ -65,10 +65,9 @@ enum : int {
     SCRATCH_FLOATS = S_IMG_END
 };
 
-// The chunk's terms the chains and the gradient pass read, stored per (head, chunk) by the terms pass
-// (floats): W, Ut, Kh, Qt (64 x 128 each), QK, S, T (64 x 64 each), exp(Gamma_C) (128).
-enum : int { TM_W = 0, TM_UT = CK, TM_KH = 2 * CK, TM_QT = 3 * CK, TM_QK = 4 * CK, TM_S = TM_QK + CC,
-             TM_T = TM_S + CC, TM_GC = TM_T + CC, TERMS_FLOATS = TM_GC + KD };
+// The chunk's FP32 terms the gradient pass reads, stored per (head, chunk) by the terms pass (floats): Ut
+// (64 x 128), S and T (64 x 64 each).  Everything a product reads comes as a bf16 image instead.
+enum : int { TM_UT = 0, TM_S = CK, TM_T = TM_S + CC, TERMS_FLOATS = TM_T + CC };
 
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
 constexpr size_t BWD_SMEM = 6ull * 32768 + 1024;   // the operand tiles of a two-term product, aligned to 1024 bytes
@@ -88,18 +87,6 @@ __device__ __forceinline__ float warp_sum(float v)
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
     return v;
-}
-
-// dst[e] = src[e] for n floats (n a multiple of 4 * BT), every thread's loads issued before its stores
-template <int N>
-__device__ __forceinline__ void copy_f(float *dst, const float *src)
-{
-    constexpr int P = N / 4 / BT;
-    float4 v[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) v[i] = ld4(src + 4 * (threadIdx.x + i * BT));
-#pragma unroll
-    for (int i = 0; i < P; ++i) st4(dst + 4 * (threadIdx.x + i * BT), v[i]);
 }
 
 // Tensor-core state of a CTA: the accumulator's TMEM columns, the products' mbarrier and the parity
@@ -535,15 +522,16 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
     __syncthreads();
 }
 
-// The chunk's products, from the rows above, straight into its stored terms tm: S = strictly_lower(Kt Kh^T),
-// QK = lower(Qt Kh^T), T = (I + M)^-1 with M = Diag(beta) S, W = T Diag(beta) Kt and Ut = T Diag(beta) V.
-__device__ void chunk_products(const float *sc, float *tm)
+// The chunk's products, from the rows above: S = strictly_lower(Kt Kh^T), T = (I + M)^-1 with
+// M = Diag(beta) S and Ut = T Diag(beta) V into its stored terms tm; QK = lower(Qt Kh^T) and
+// W = T Diag(beta) Kt as bf16 images into its image unit im.
+__device__ void chunk_products(const float *sc, float *tm, unsigned char *im)
 {
     extern __shared__ __align__(16) float bsm[];
     const int tid = threadIdx.x;
     const float *Kt = sc + S_KT, *Kh = sc + S_KH, *Qt = sc + S_QT;
     product<64, 64, KD, false, true, 0, false, false, 2>(term(Kt, KD, Kh, KD), Term{}, out(tm + TM_S, 64));
-    product<64, 64, KD, false, true, 0, false, false, 1>(term(Qt, KD, Kh, KD), Term{}, out(tm + TM_QK, 64));
+    product<64, 64, KD, false, true, 0, false, false, 1>(term(Qt, KD, Kh, KD), Term{}, out_img(out(nullptr, 0), im + RIMG_QK));
     // T = (I + M)^-1 by forward substitution, one column per thread: T[j][j] = 1,
     // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]; M = Diag(beta) S in shared memory (read by every
     // thread alike), the column in registers
@@ -572,7 +560,7 @@ __device__ void chunk_products(const float *sc, float *tm)
         }
         __syncthreads();
     }
-    product<64, KD, 64, false, false>(term(tm + TM_T, 64, sc + S_BKT, KD), Term{}, out(tm + TM_W, KD));
+    product<64, KD, 64, false, false>(term(tm + TM_T, 64, sc + S_BKT, KD), Term{}, out_img(out(nullptr, 0), im + RIMG_W));
     product<64, VD, 64, false, false>(term(tm + TM_T, 64, sc + S_BV, VD), Term{}, out(tm + TM_UT, VD));
 }
 
@@ -605,15 +593,12 @@ __device__ __forceinline__ void put_image(unsigned char *hi, unsigned char *lo, 
     }
 }
 
-// The chunk's images for the reverse chains: Kh, QK, Qt and W as bf16 pairs, dO (bf16, rows past L
-// zero) and exp(Gamma_C), from the rows in scratch and the products in the stored terms.
-__device__ void put_reverse_images(unsigned char *im, const float *sc, const float *tm, const uint16_t *dout, int t0,
-                                   int L, int h, int H)
+// The chunk's images of its rows: Kh and Qt as bf16 pairs, dO (bf16, rows past L zero) and exp(Gamma_C),
+// from the rows in scratch (the products leave QK's and W's images themselves).
+__device__ void put_row_images(unsigned char *im, const float *sc, const uint16_t *dout, int t0, int L, int h, int H)
 {
     put_image<KD>(im + RIMG_KH, im + RIMG_KH + 16384, sc + S_KH, KD);
-    put_image<64>(im + RIMG_QK, im + RIMG_QK + 8192, tm + TM_QK, 64);
     put_image<KD>(im + RIMG_QT, im + RIMG_QT + 16384, sc + S_QT, KD);
-    put_image<KD>(im + RIMG_W, im + RIMG_W + 16384, tm + TM_W, KD);
     uint4 w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -651,12 +636,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig 
         const int h = unit / n_chunks, c = unit % n_chunks;
         const int32_t *cr = pv.chunk(c);
         float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;
+        unsigned char *const im = img + static_cast<size_t>(unit) * RIMG_UNIT;
         chunk_rows(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
-        chunk_products(sc, tm);
-        put_reverse_images(img + static_cast<size_t>(unit) * RIMG_UNIT, sc, tm, dout, cr[1], cr[2], h, H);
-        copy_f<CK>(tm + TM_KH, sc + S_KH);
-        copy_f<CK>(tm + TM_QT, sc + S_QT);
-        if (threadIdx.x < KD / 4) st4(tm + TM_GC + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
+        put_row_images(im, sc, dout, cr[1], cr[2], h, H);
+        chunk_products(sc, tm, im);
         __syncthreads();
     }
     tc_end();

@@ -424,7 +424,7 @@ int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t
  * forward's outputs, the chunk start states and end-state gradients
  * (2 * H * n_chunks * K * V * 4 bytes), the segment gradients
  * (2 * S * H * K * V * 4 bytes), the kernels' working areas, each chunk's
- * terms for the gradient pass (180,736 bytes per chunk and head), and each
+ * terms for the gradient pass (65,536 bytes per chunk and head), and each
  * chunk's bf16 operand images for the reverse chains (132,096 bytes per
  * chunk and head). */
 size_t kda_backward_workspace_bytes(const int32_t *plan, int32_t H);
