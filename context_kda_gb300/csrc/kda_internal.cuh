@@ -166,7 +166,7 @@ cudaError_t launch_compose(const int32_t *plan_host, const int32_t *plan_dev, in
 cudaError_t launch_compose_blocked(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *A,
                                    const float *B, const float *h0, float *S_in, void *scratch, cudaStream_t stream);
 size_t scan_scratch_bytes(const int32_t *plan_host, int H);
-// The backward (FP32 on the CUDA cores): see backward.cu.  'scratch' holds grid x
+// The backward (FP32 matrices, products on tcgen05): see backward.cu.  'scratch' holds grid x
 // backward_scratch_floats() floats; xs and gs hold [H][n_chunks][K][V] floats each, G_end and Qd
 // [S][H][K][V] each.
 size_t backward_scratch_floats();
