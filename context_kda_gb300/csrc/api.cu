@@ -445,7 +445,7 @@ bool backward_layout(const int32_t *plan, int32_t H, size_t off[10])
     const size_t sizes[9] = {T * h * V * 2, N * h * K * V * 4, h * C * K * V * 4, h * C * K * V * 4,
                              S * h * K * V * 4, S * h * K * V * 4,
                              static_cast<size_t>(kBackwardGrid) * kda::backward_scratch_floats() * 4,
-                             h * C * kda::backward_terms_floats() * 4, h * C * kda::RIMG_UNIT};
+                             h * C * kda::BT_FLOATS * 4, h * C * kda::RIMG_UNIT};
     size_t pos = fw[6];
     for (int i = 0; i < 9; ++i) {
         off[i] = pos;
@@ -484,9 +484,12 @@ extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_d
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the forward's local pass and composition: S_in, the segment transitions A and the final-state
     // transitions of continuing pieces
+    // (its preparation in backward mode also leaves each chunk's FP32 terms and operand images)
     int rc = cuda_status(kda::launch_chunk_forward(plan, plan_dev, H, q, k, v, g, beta, h0, scale,
                                                    reinterpret_cast<uint16_t *>(b + off[0]), w.A, w.B,
-                                                   reinterpret_cast<float *>(b + off[1]), w.qhat, w.afin, w.pkg, s));
+                                                   reinterpret_cast<float *>(b + off[1]), w.qhat, w.afin, w.pkg, s,
+                                                   reinterpret_cast<unsigned char *>(b + off[8]),
+                                                   reinterpret_cast<float *>(b + off[7])));
     if (rc != KDA_OK) return rc;
     rc = cuda_status(use_blocked_scan(plan, H)
                          ? kda::launch_compose_blocked(plan, plan_dev, H, w.A, w.B, h0, w.S_in,

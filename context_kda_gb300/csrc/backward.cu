@@ -15,8 +15,9 @@
 //
 // Steps (after the forward's own preparation, state pass and composition, which give S_in, the
 // segment transitions A and the final-state transitions of continuing pieces):
-//  0. every (chunk, head) in parallel: the chunk's terms (W, Ut, Kh, Qt, QK, S, T, Dc) for the gradient
-//     pass, and the reverse chains' bf16 operand images;
+//  0. every (chunk, head) in parallel: the chunk's FP32 terms (Ut, S, T) for the gradient pass and the
+//     bf16 operand images (Kh, Qt, QK, W, Dc) of the reverse chains and the gradient pass, which the
+//     forward's preparation writes in its backward mode (the caller launches it), and dO's image;
 //  1. every piece from its true incoming state (h0, or S_in of its segment), recording each chunk's
 //     start state X_c: the forward's state pass in its output mode (the caller launches it);
 //  2. (reverse.cu) every piece that continues a sequence, backwards from a zero end gradient: the gradient of its
@@ -29,8 +30,8 @@
 //     giving dh0 at a sequence start;
 //  5. every (chunk, head) in parallel: dq, dk, dv, dg, dbeta from (X_c, G_c, dO).
 //
-// The terms and gradient passes here keep a chunk's matrices in FP32 in a private scratch area in global
-// memory and run every product on the tensor cores (both operands staged in shared memory as bf16 hi/lo
+// The gradient pass here keeps a chunk's matrices in FP32 in a private scratch area in global
+// memory and runs every product on the tensor cores (both operands staged in shared memory as bf16 hi/lo
 // pairs, a three-term split accumulated in FP32 in TMEM), which keeps every step a literal transcription
 // of the formulas above.
 #include "kda_internal.cuh"
@@ -65,9 +66,7 @@ enum : int {
     SCRATCH_FLOATS = S_IMG_END
 };
 
-// The chunk's FP32 terms the gradient pass reads, stored per (head, chunk) by the terms pass (floats): Ut
-// (64 x 128), S and T (64 x 64 each).  Everything a product reads comes as a bf16 image instead.
-enum : int { TM_UT = 0, TM_S = CK, TM_T = TM_S + CC, TERMS_FLOATS = TM_T + CC };
+static_assert(BT_UT == 0 && BT_S == CK && BT_T == BT_S + CC && BT_FLOATS == BT_T + CC, "the chunk terms' layout");
 
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
 constexpr size_t BWD_SMEM = 6ull * 32768 + 1024;   // the operand tiles of a two-term product, aligned to 1024 bytes
@@ -522,127 +521,38 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
     __syncthreads();
 }
 
-// The chunk's products, from the rows above: S = strictly_lower(Kt Kh^T), T = (I + M)^-1 with
-// M = Diag(beta) S and Ut = T Diag(beta) V into its stored terms tm; QK = lower(Qt Kh^T) and
-// W = T Diag(beta) Kt as bf16 images into its image unit im.
-__device__ void chunk_products(const float *sc, float *tm, unsigned char *im)
-{
-    extern __shared__ __align__(16) float bsm[];
-    const int tid = threadIdx.x;
-    const float *Kt = sc + S_KT, *Kh = sc + S_KH, *Qt = sc + S_QT;
-    product<64, 64, KD, false, true, 0, false, false, 2>(term(Kt, KD, Kh, KD), Term{}, out(tm + TM_S, 64));
-    product<64, 64, KD, false, true, 0, false, false, 1>(term(Qt, KD, Kh, KD), Term{}, out_img(out(nullptr, 0), im + RIMG_QK));
-    // T = (I + M)^-1 by forward substitution, one column per thread: T[j][j] = 1,
-    // T[r][j] = -sum_{j <= i < r} M[r][i] T[i][j]; M = Diag(beta) S in shared memory (read by every
-    // thread alike), the column in registers
-    {
-        float4 mv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mv[i] = ld4(tm + TM_S + 4 * (tid + i * BT));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = 4 * (tid + i * BT);
-            st4(bsm + e, scl4(sc[S_BT + (e >> 6)], mv[i]));
-        }
-        __syncthreads();
-        if (tid < 64) {
-            const int j = tid;
-            float t[64];
-#pragma unroll
-            for (int r = 0; r < 64; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i) acc = fmaf(bsm[r * 64 + i], t[i], acc);
-                t[r] = r < j ? 0.f : (r == j ? 1.f : -acc);
-            }
-#pragma unroll
-            for (int r = 0; r < 64; ++r) tm[TM_T + r * 64 + j] = t[r];
-        }
-        __syncthreads();
-    }
-    product<64, KD, 64, false, false>(term(tm + TM_T, 64, sc + S_BKT, KD), Term{}, out_img(out(nullptr, 0), im + RIMG_W));
-    product<64, VD, 64, false, false>(term(tm + TM_T, 64, sc + S_BV, VD), Term{}, out(tm + TM_UT, VD));
-}
-
-
-// Rows 0..63 of an FP32 array (row stride ld) of C columns as a bf16 hi/lo image in the reverse chains'
-// layout (8-column chunks of 64 rows x 16 bytes, RIMG_CS apart); the lanes of a warp take consecutive
-// rows of one piece, so each store instruction writes 512 contiguous bytes.
-template <int C>
-__device__ __forceinline__ void put_image(unsigned char *hi, unsigned char *lo, const float *src, int ld)
-{
-    constexpr int P = 64 * C / 8 / BT;
-    float4 x[2 * P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
-        x[2 * i] = ld4(src + r * ld + c8);
-        x[2 * i + 1] = ld4(src + r * ld + c8 + 4);
-    }
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
-        uint32_t hh[4], ll[4];
-        split_bf16x2(x[2 * i].x, x[2 * i].y, hh[0], ll[0]);
-        split_bf16x2(x[2 * i].z, x[2 * i].w, hh[1], ll[1]);
-        split_bf16x2(x[2 * i + 1].x, x[2 * i + 1].y, hh[2], ll[2]);
-        split_bf16x2(x[2 * i + 1].z, x[2 * i + 1].w, hh[3], ll[3]);
-        const uint32_t off = cm_off(r, c8, RIMG_CS);
-        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-    }
-}
-
-// The chunk's images of its rows: Kh and Qt as bf16 pairs, dO (bf16, rows past L zero) and exp(Gamma_C),
-// from the rows in scratch (the products leave QK's and W's images themselves).
-__device__ void put_row_images(unsigned char *im, const float *sc, const uint16_t *dout, int t0, int L, int h, int H)
-{
-    put_image<KD>(im + RIMG_KH, im + RIMG_KH + 16384, sc + S_KH, KD);
-    put_image<KD>(im + RIMG_QT, im + RIMG_QT + 16384, sc + S_QT, KD);
-    uint4 w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
-        w[i] = r < L ? *reinterpret_cast<const uint4 *>(dout + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
-                     : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
-        *reinterpret_cast<uint4 *>(im + RIMG_DO + cm_off(r, c8, RIMG_CS)) = w[i];
-    }
-    if (threadIdx.x < KD / 4)
-        st4(reinterpret_cast<float *>(im + RIMG_GC) + 4 * threadIdx.x, ld4(sc + S_GC + 4 * threadIdx.x));
-}
-
 #define BWD_PLAN_CHECK()                                                                  \
     if (!plan_matches(plan, sig)) {                                                       \
         if (threadIdx.x == 0 && blockIdx.x == 0) record_status(&g_bwd_status, KDA_ERR_INVALID_ARG); \
         return;                                                                           \
     }
 
-// 0. every (chunk, head) in parallel: the terms the chains need, stored at terms[h][c]
-__global__ void __launch_bounds__(BT, 1) bwd_terms(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
-                                                const uint16_t *k, const uint16_t *v, const float *g,
-                                                const float *beta, float scale, const uint16_t *dout, float *terms,
-                                                unsigned char *img, float *scratch)
+// 0. every (chunk, head): dO's bf16 image (rows r x cols v, rows past the chunk zero) into the unit's images;
+//    the lanes of a warp take consecutive rows of one 8-column piece, so each store writes 512 contiguous bytes
+__global__ void __launch_bounds__(BT) bwd_do_images(const int32_t *plan, PlanSig sig, int H, const uint16_t *dout,
+                                                    unsigned char *img)
 {
     BWD_PLAN_CHECK();
-    tc_begin();
     const PlanView pv{plan};
-    float *sc = scratch + static_cast<size_t>(blockIdx.x) * SCRATCH_FLOATS;
     const int n_chunks = pv.n_chunks();
-    for (int unit = blockIdx.x; unit < n_chunks * H; unit += gridDim.x) {
-        const int h = unit / n_chunks, c = unit % n_chunks;
+    for (long long unit = blockIdx.x; unit < static_cast<long long>(n_chunks) * H; unit += gridDim.x) {
+        const int h = static_cast<int>(unit / n_chunks), c = static_cast<int>(unit % n_chunks);
         const int32_t *cr = pv.chunk(c);
-        float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;
-        unsigned char *const im = img + static_cast<size_t>(unit) * RIMG_UNIT;
-        chunk_rows(sc, cr[1], cr[2], h, H, q, k, v, g, beta, scale);
-        put_row_images(im, sc, dout, cr[1], cr[2], h, H);
-        chunk_products(sc, tm, im);
-        __syncthreads();
+        const int t0 = cr[1], L = cr[2];
+        unsigned char *const dst = img + static_cast<size_t>(unit) * RIMG_UNIT + RIMG_DO;
+        uint4 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
+            w[i] = r < L ? *reinterpret_cast<const uint4 *>(dout + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int pc = threadIdx.x + i * BT, r = pc & 63, c8 = (pc >> 6) * 8;
+            *reinterpret_cast<uint4 *>(dst + cm_off(r, c8, RIMG_CS)) = w[i];
+        }
     }
-    tc_end();
 }
 
 // 3. The following summaries, per (head, 32-column slice), last segment first:
@@ -734,9 +644,9 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const int32_t *cr = pv.chunk(c);
         const int t0 = cr[1], L = cr[2];
         chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
-        const float *tm = terms + static_cast<size_t>(unit) * TERMS_FLOATS;   // Ut, S, T
+        const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S, T
         // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them;
-        // Kh, QK, Qt, W and dO come as the chunk's operand images; X, DG = Dc G, T and beta Kt leave their
+        // Kh, QK, Qt, W (as W^T) and dO come as the chunk's operand images; X, DG = Dc G, T and beta Kt leave their
         // split in an image where they are first staged, and every product whose result feeds another
         // leaves its result as an image, so later products bring their operands in by bulk copies
         const float *X = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
@@ -751,9 +661,9 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const float *bKt = sc + S_BKT, *bV = sc + S_BV;
         const Term none = term(nullptr, 0, nullptr, 0);
         __syncthreads();
-        // U = Ut - W X
-        product<64, VD, KD, false, false>(save_b(img_a(term(nullptr, 0, X, VD), im + RIMG_W), xi), none,
-                                          out_img(out(nullptr, 0, -1.f, tm + TM_UT, VD), ui));
+        // U = Ut - W X (W from the image of W^T as it lies)
+        product<64, VD, KD, true, false>(save_b(img_a(term(nullptr, 0, X, VD), im + RIMG_W), xi), none,
+                                         out_img(out(nullptr, 0, -1.f, tm + BT_UT, VD), ui));
         // dQK = lower(dO U^T)
         product<64, 64, VD, false, true, 0, false, false, 1>(img_b(img_a(none, im + RIMG_DO, true), ui), none,
                                                              out_img(out(nullptr, 0), dqki));
@@ -790,7 +700,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         product<64, 64, KD, false, true, VD, false, true>(save_b(img_a(term(nullptr, 0, bKt, KD), dwi), bkti),
                                                           img_a(term(nullptr, 0, bV, VD), dui), out_img(out(nullptr, 0), dti));
         // d(beta Kt) = T^T dW, d(beta V) = T^T dU
-        product<64, KD, 64, true, false>(save_a(img_b(term(tm + TM_T, 64, nullptr, 0), dwi), ti), none,
+        product<64, KD, 64, true, false>(save_a(img_b(term(tm + BT_T, 64, nullptr, 0), dwi), ti), none,
                                          out(sc + S_DBKT, KD));
         product<64, VD, 64, true, false>(img_b(img_a(none, ti), dui), none, out(sc + S_DBV, VD));
         // dM = strictly_lower(-T^T dT T^T)
@@ -810,7 +720,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = ld4(sc + S_KT + r * KD + 4 * ln);
                 const float4 cv = ld4(sc + S_DBV + r * VD + 4 * ln), d = ld4(sc + S_VF + r * VD + 4 * ln);
                 const float2 mm = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
-                const float2 sv = *reinterpret_cast<const float2 *>(tm + TM_S + r * 64 + 2 * ln);
+                const float2 sv = *reinterpret_cast<const float2 *>(tm + BT_S + r * 64 + 2 * ln);
                 const float sum = warp_sum(dot4(a, b) + dot4(cv, d) + mm.x * sv.x + mm.y * sv.y);
                 if (ln == 0) sc[S_DBETA + r] = sum;
             }
@@ -888,7 +798,6 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
 }  // namespace
 
 size_t backward_scratch_floats() { return static_cast<size_t>(SCRATCH_FLOATS); }
-size_t backward_terms_floats() { return static_cast<size_t>(TERMS_FLOATS); }
 
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                             const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
@@ -899,12 +808,14 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
 {
     const PlanView pv{plan_host};
     const PlanSig sig = plan_sig(plan_host);
-    for (auto fn : {reinterpret_cast<const void *>(bwd_terms), reinterpret_cast<const void *>(bwd_grads)}) {
-        const cudaError_t e = set_dynamic_smem(fn, static_cast<int>(BWD_SMEM));
-        if (e != cudaSuccess) return e;
+    cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(bwd_grads), static_cast<int>(BWD_SMEM));
+    if (err != cudaSuccess) return err;
+    const long long n_units = static_cast<long long>(pv.n_chunks()) * H;
+    if (n_units > 0) {
+        const unsigned blocks = static_cast<unsigned>(n_units < 4096 ? n_units : 4096);
+        bwd_do_images<<<blocks, BT, 0, stream>>>(plan_dev, sig, H, dout, img);
+        err = cudaGetLastError();
     }
-    bwd_terms<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, terms, img, scratch);
-    cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (pv.n_cont() > 0) {
         err = launch_reverse_tc(plan_host, plan_dev, H, false, img, dfinal, G_end, Qd, gs, dh0, stream);

@@ -24,6 +24,11 @@
 // run while the workers start the next unit; the workers read W back from TMEM and store it while
 // they wait for the next unit's [KK; QK], and four warps store Ut while two solve the next
 // unit's diagonal blocks.
+//
+// Backward mode (BWD): the same pass also leaves what the backward reads of each unit, in the layouts
+// its kernels use: the FP32 terms Ut (row-major), S = strictly_lower(Kt Kh^T) and T = (I + M)^-1
+// (lower), and the bf16 hi/lo images of Kh, Qt, the masked QK, W (as W^T: rows k, cols r) and
+// exp(Gamma_C).  Qt then enters [KK; QK] with its low part too, so QK is a full three-term product.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -106,11 +111,12 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 w, float *x)
     }
 }
 
+template <bool BWD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_units, const float *__restrict__ beta,
               float scale, unsigned char *__restrict__ pkg, const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_g)
+              const __grid_constant__ CUtensorMap tm_g, unsigned char *__restrict__ bimg, float *__restrict__ bterms)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;
@@ -239,6 +245,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
     // W^T of a unit (already complete) from TMEM into its package
     auto store_w = [&](long long u) {
         unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
+        unsigned char *const im = BWD ? bimg + static_cast<size_t>(u) * RIMG_UNIT : nullptr;
         {
             float x[32];
             tmem_ld32(tl + TM_W + hw * 32, x);   // W^T[k = c_lane][r = hw*32 + j]
@@ -249,6 +256,10 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                 const uint32_t off = cm_off(c_lane, hw * 32 + 8 * m, 2048);
                 *reinterpret_cast<uint4 *>(pk + PK_W + off) = hi;
                 *reinterpret_cast<uint4 *>(pk + PK_W + T64 + off) = lo;
+                if constexpr (BWD) {
+                    *reinterpret_cast<uint4 *>(im + RIMG_W + off) = hi;
+                    *reinterpret_cast<uint4 *>(im + RIMG_W + T64 + off) = lo;
+                }
             }
         }
     };
@@ -267,6 +278,11 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
             float4 *ut = reinterpret_cast<float4 *>(pk + PK_U) + hh * 8 * 128 + c_lane;
 #pragma unroll
             for (int m = 0; m < 8; ++m) ut[m * 128] = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+            if constexpr (BWD) {   // Ut row-major: a warp's store covers 128 contiguous bytes of a row
+                float *const ur = bterms + static_cast<size_t>(u) * BT_FLOATS + BT_UT + (hh * 32) * VD + c_lane;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ur[j * VD] = x[j];
+            }
         }
     };
 
@@ -274,6 +290,8 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
         int n = 0;
         for (long long u = u_begin; u < u_end && !aborted; ++u, ++n) {
             unsigned char *const pk = pkg + static_cast<size_t>(u) * KDA_PACKAGE_BYTES;
+            unsigned char *const im = BWD ? bimg + static_cast<size_t>(u) * RIMG_UNIT : nullptr;
+            float *const bt = BWD ? bterms + static_cast<size_t>(u) * BT_FLOATS : nullptr;
             int L;
 
             // ================= A: staged rows -> decayed keys / queries / values =====================
@@ -325,6 +343,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                         const float4 gcv = make_float4(ex2_ftz(gs.x), ex2_ftz(gs.y), ex2_ftz(gs.z), ex2_ftz(gs.w));
                         reinterpret_cast<float4 *>(s_gc)[cq] = gcv;
                         reinterpret_cast<float4 *>(pk + PK_GC)[cq] = gcv;
+                        if constexpr (BWD) reinterpret_cast<float4 *>(im + RIMG_GC)[cq] = gcv;
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
@@ -378,17 +397,31 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                     split8(kt, hi, lo);
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + o_r) = hi;
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_r) = lo;
-                    // Qt only feeds the masked scores QK, single-term like every output product: its
-                    // bf16 low part stays zero (cleared once at the start), one conversion per pair
-                    hi = make_uint4(bf16x2_bits(qt[0], qt[1]), bf16x2_bits(qt[2], qt[3]), bf16x2_bits(qt[4], qt[5]),
-                                    bf16x2_bits(qt[6], qt[7]));
-                    *reinterpret_cast<uint4 *>(base + OFF_KQ + o_q) = hi;
-                    *reinterpret_cast<uint4 *>(pk + PK_Q + o_64) = hi;
+                    if constexpr (BWD) {
+                        // the backward's QK and Qt take the full split
+                        split8(qt, hi, lo);
+                        *reinterpret_cast<uint4 *>(base + OFF_KQ + o_q) = hi;
+                        *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_q) = lo;
+                        *reinterpret_cast<uint4 *>(pk + PK_Q + o_64) = hi;
+                        *reinterpret_cast<uint4 *>(im + RIMG_QT + o_64) = hi;
+                        *reinterpret_cast<uint4 *>(im + RIMG_QT + T64 + o_64) = lo;
+                    } else {
+                        // Qt only feeds the masked scores QK, single-term like every output product: its
+                        // bf16 low part stays zero (cleared once at the start), one conversion per pair
+                        hi = make_uint4(bf16x2_bits(qt[0], qt[1]), bf16x2_bits(qt[2], qt[3]),
+                                        bf16x2_bits(qt[4], qt[5]), bf16x2_bits(qt[6], qt[7]));
+                        *reinterpret_cast<uint4 *>(base + OFF_KQ + o_q) = hi;
+                        *reinterpret_cast<uint4 *>(pk + PK_Q + o_64) = hi;
+                    }
                     split8(kh, hi, lo);
                     *reinterpret_cast<uint4 *>(base + OFF_KH + o_64) = hi;
                     *reinterpret_cast<uint4 *>(base + OFF_KH + T64 + o_64) = lo;
                     *reinterpret_cast<uint4 *>(pk + PK_KH + o_64) = hi;
                     *reinterpret_cast<uint4 *>(pk + PK_KH + T64 + o_64) = lo;
+                    if constexpr (BWD) {
+                        *reinterpret_cast<uint4 *>(im + RIMG_KH + o_64) = hi;
+                        *reinterpret_cast<uint4 *>(im + RIMG_KH + T64 + o_64) = lo;
+                    }
                     *reinterpret_cast<uint4 *>(base + OFF_VT + o_64) = vw[i];
                 }
                 aborted = handoff(HO_A);   // -> [KK; QK]
@@ -408,26 +441,40 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                     const float br = s_beta[r];
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        float4 m4;
+                        float4 s4, m4;
                         const int i0 = hw * 32 + 4 * j4;
-                        m4.x = (i0 + 0 < r) ? br * d[4 * j4 + 0] : 0.f;
-                        m4.y = (i0 + 1 < r) ? br * d[4 * j4 + 1] : 0.f;
-                        m4.z = (i0 + 2 < r) ? br * d[4 * j4 + 2] : 0.f;
-                        m4.w = (i0 + 3 < r) ? br * d[4 * j4 + 3] : 0.f;
+                        s4.x = (i0 + 0 < r) ? d[4 * j4 + 0] : 0.f;
+                        s4.y = (i0 + 1 < r) ? d[4 * j4 + 1] : 0.f;
+                        s4.z = (i0 + 2 < r) ? d[4 * j4 + 2] : 0.f;
+                        s4.w = (i0 + 3 < r) ? d[4 * j4 + 3] : 0.f;
+                        m4 = make_float4(br * s4.x, br * s4.y, br * s4.z, br * s4.w);
                         *reinterpret_cast<float4 *>(f32_at(base, OFF_M32, r, i0)) = m4;
+                        if constexpr (BWD) *reinterpret_cast<float4 *>(bt + BT_S + r * 64 + i0) = s4;
                     }
                 } else {
                     const int r = c_lane - 64;
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        uint32_t w[4];
+                        const uint32_t off = cm_off(r, hw * 32 + 8 * m, 1024);
+                        if constexpr (BWD) {
+                            float qk[8];
 #pragma unroll
-                        for (int p2 = 0; p2 < 4; ++p2) {
-                            const int i0 = hw * 32 + 8 * m + 2 * p2;
-                            w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f, i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                            for (int e = 0; e < 8; ++e) qk[e] = hw * 32 + 8 * m + e <= r ? d[8 * m + e] : 0.f;
+                            uint4 hi, lo;
+                            split8(qk, hi, lo);
+                            *reinterpret_cast<uint4 *>(pk + PK_QK + off) = hi;
+                            *reinterpret_cast<uint4 *>(im + RIMG_QK + off) = hi;
+                            *reinterpret_cast<uint4 *>(im + RIMG_QK + 8192 + off) = lo;
+                        } else {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int p2 = 0; p2 < 4; ++p2) {
+                                const int i0 = hw * 32 + 8 * m + 2 * p2;
+                                w[p2] = bf16x2_bits(i0 <= r ? d[8 * m + 2 * p2] : 0.f,
+                                                    i0 + 1 <= r ? d[8 * m + 2 * p2 + 1] : 0.f);
+                            }
+                            *reinterpret_cast<uint4 *>(pk + PK_QK + off) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        *reinterpret_cast<uint4 *>(pk + PK_QK + cm_off(r, hw * 32 + 8 * m, 1024)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
                 fence_before();
@@ -530,11 +577,16 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                 for (int m4 = 0; m4 < 4; ++m4) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
                     const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+                    float tl4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i = i0 + 4 * m4 + e;
-                        tv[4 * m4 + e] = (i <= r) ? tt[e] * s_beta[i] : 0.f;
+                        tl4[e] = (i <= r) ? tt[e] : 0.f;   // T, zero above the diagonal
+                        tv[4 * m4 + e] = tl4[e] * s_beta[i];
                     }
+                    if constexpr (BWD)
+                        *reinterpret_cast<float4 *>(bt + BT_T + r * 64 + i0 + 4 * m4) =
+                            make_float4(tl4[0], tl4[1], tl4[2], tl4[3]);
                 }
                 st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
                 st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),
@@ -629,7 +681,7 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
 
 cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                               const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
-                              unsigned char *pkg, cudaStream_t stream)
+                              unsigned char *pkg, cudaStream_t stream, unsigned char *bimg, float *bterms)
 {
     const PlanView pv{plan_host};
     const long long n_units = static_cast<long long>(pv.n_chunks()) * H;
@@ -641,13 +693,20 @@ cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev,
         !encode_rows_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64) ||
         !encode_rows_3d(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, 32))
         return cudaErrorInvalidValue;
-    cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(chunk_prep_tc),
-                                       static_cast<int>(SMEM_ALLOC));
+    const bool bwd = bimg != nullptr && bterms != nullptr;
+    if ((bimg != nullptr) != (bterms != nullptr)) return cudaErrorInvalidValue;
+    const void *fn = bwd ? reinterpret_cast<const void *>(chunk_prep_tc<true>)
+                         : reinterpret_cast<const void *>(chunk_prep_tc<false>);
+    cudaError_t err = set_dynamic_smem(fn, static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     const long long grid = n_units < sm_count() ? n_units : sm_count();
-    chunk_prep_tc<<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(plan_dev, plan_sig(plan_host), H, n_units,
-                                                                                 beta, scale,
-                                                                                 pkg, tq, tk, tv, tg);
+    const PlanSig sig = plan_sig(plan_host);
+    if (bwd)
+        chunk_prep_tc<true><<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(
+            plan_dev, sig, H, n_units, beta, scale, pkg, tq, tk, tv, tg, bimg, bterms);
+    else
+        chunk_prep_tc<false><<<static_cast<unsigned>(grid), NTHREADS, SMEM_ALLOC, stream>>>(
+            plan_dev, sig, H, n_units, beta, scale, pkg, tq, tk, tv, tg, nullptr, nullptr);
     return cudaGetLastError();
 }
 

@@ -533,14 +533,16 @@ cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev
                                      stream);
 }
 
-// The local chunkwise forward: the chunk-parallel preparation, then the serial state pass.
+// The local chunkwise forward: the chunk-parallel preparation (in its backward mode when bimg and bterms
+// are given), then the serial state pass.
 cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_dev, int H,
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const float *g, const float *beta, const float *h0, float scale,
                                  uint16_t *o, float *A, float *B, float *final_state,
-                                 uint16_t *qhat, float *afin, unsigned char *pkg, cudaStream_t stream)
+                                 uint16_t *qhat, float *afin, unsigned char *pkg, cudaStream_t stream,
+                                 unsigned char *bimg, float *bterms)
 {
-    cudaError_t err = launch_chunk_prep(plan_host, plan_dev, H, q, k, v, g, beta, scale, pkg, stream);
+    cudaError_t err = launch_chunk_prep(plan_host, plan_dev, H, q, k, v, g, beta, scale, pkg, stream, bimg, bterms);
     if (err != cudaSuccess) return err;
     return launch_chunk_state(plan_host, plan_dev, H, h0, pkg, o, A, B, final_state, qhat, afin, stream);
 }

@@ -152,10 +152,14 @@ cudaError_t launch_chunk_forward(const int32_t *plan_host, const int32_t *plan_d
                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const float *g, const float *beta, const float *h0, float scale,
                                  uint16_t *o, float *A, float *B, float *final_state,
-                                 uint16_t *qhat, float *afin, unsigned char *pkg, cudaStream_t stream);
+                                 uint16_t *qhat, float *afin, unsigned char *pkg, cudaStream_t stream,
+                                 unsigned char *bimg = nullptr, float *bterms = nullptr);
+// With bimg and bterms (the backward's per-unit images and FP32 terms), the preparation also writes
+// those: its backward mode.
 cudaError_t launch_chunk_prep(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                               const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
-                              unsigned char *pkg, cudaStream_t stream);
+                              unsigned char *pkg, cudaStream_t stream, unsigned char *bimg = nullptr,
+                              float *bterms = nullptr);
 cudaError_t launch_chunk_state(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
                                const unsigned char *pkg, uint16_t *o, float *A, float *B, float *final_state,
                                uint16_t *qhat, float *afin, cudaStream_t stream);
@@ -170,12 +174,16 @@ size_t scan_scratch_bytes(const int32_t *plan_host, int H);
 // backward_scratch_floats() floats; xs and gs hold [H][n_chunks][K][V] floats each, G_end and Qd
 // [S][H][K][V] each.
 size_t backward_scratch_floats();
-size_t backward_terms_floats();   // per (head, chunk)
-// Per-(chunk, head) operand images of the backward's reverse chains, written by its terms pass (bytes):
-// bf16 tiles of 64 rows in the no-swizzle canonical layout (8-column chunks of 64 rows x 16 bytes,
-// chunk stride RIMG_CS), hi then lo where split.  The part the first product of a chain step reads
-// (Kh rows r x cols k, QK rows r' x cols r, dO rows r x cols v, exp(Gamma_C) as 128 fp32) comes
-// first, then the part the second reads (Qt and W, rows r x cols k).
+// The FP32 chunk terms the backward's gradient pass reads, per (head, chunk) (floats, row-major): Ut
+// (64 x 128), S = strictly_lower(Kt Kh^T) and T = (I + Diag(beta) S)^-1 (64 x 64 each).  The preparation
+// kernel writes them in its backward mode.
+constexpr int BT_UT = 0, BT_S = 64 * 128, BT_T = BT_S + 64 * 64, BT_FLOATS = BT_T + 64 * 64;
+// Per-(chunk, head) operand images of the backward (bytes), written by the preparation kernel's
+// backward mode (dO by its own small kernel): bf16 tiles in the no-swizzle canonical layout (8-column
+// chunks of the tile's rows x 16 bytes), hi then lo where split.  The part the first product of a
+// reverse chain step reads (Kh rows r x cols k, QK rows r' x cols r, dO rows r x cols v, each with
+// chunk stride RIMG_CS, and exp(Gamma_C) as 128 fp32) comes first, then the part the second reads (Qt
+// rows r x cols k, chunk stride RIMG_CS; W as its transpose, rows k x cols r, chunk stride 2048).
 constexpr uint32_t RIMG_CS = 1024;
 constexpr uint32_t RIMG_KH = 0, RIMG_QK = 32768, RIMG_DO = 49152, RIMG_GC = 65536, RIMG_A_BYTES = 66048;
 constexpr uint32_t RIMG_QT = 66560, RIMG_W = RIMG_QT + 32768, RIMG_B_BYTES = 65536;

@@ -18,9 +18,10 @@
 //   dU^T = DG^T Kh^T (3-term) + dO^T QK (2-term)                       -> workers:
 //   -dU^T split into TMEM                                              -> issuer:
 //   G^T += dO^T Qt (2-term) - dU^T W (3-term)
-// The operands come as ready bf16 images (written once per chunk by the terms pass) by bulk copies: the
-// part the first product reads is double-buffered and arrives a chunk ahead, the part the second
-// reads is single-buffered and arrives once the previous chunk's second product is done.
+// The operands come as ready bf16 images (written once per chunk by the forward's preparation in its
+// backward mode, dO's by a small kernel) by bulk copies: the part the first product reads is
+// double-buffered and arrives a chunk ahead, the part the second reads is single-buffered and arrives
+// once the previous chunk's second product is done.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -261,15 +262,16 @@ reverse_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const unsigned 
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16(tbase + TG, sdesc(pa + RIMG_DO + kk * 256, 128, RIMG_CS),
                                  sdesc(pb + ps * 16384 + kk * 256, 128, RIMG_CS), id3, 1u);
-                // G^T += (-dU^T) W: A from TMEM (K = r), B(k, r) = W[r][k] (rows r, read MN-major)
-                const uint32_t id4 = idesc_bf16(128, 128, 0, 1);
+                // G^T += (-dU^T) W: A from TMEM (K = r), B(k, r) = W^T[k][r] (the image of W^T: rows k,
+                // chunk stride 2048, read K-major)
+                const uint32_t id4 = idesc_bf16(128, 128, 0, 0);
                 const uint32_t aof[3] = {TUH, TUH, TUL}, bof[3] = {0, 16384, 0};
 #pragma unroll
                 for (int ps = 0; ps < 3; ++ps)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16_ta(tbase + TG, tbase + aof[ps] + kk * 8,
-                                    sdesc(pb + (RIMG_W - RIMG_QT) + bof[ps] + kk * 256, 128, RIMG_CS), id4, 1u);
+                                    sdesc(pb + (RIMG_W - RIMG_QT) + bof[ps] + kk * 2 * 2048, 2048), id4, 1u);
                 commit(m2);
                 ++n2;
             }

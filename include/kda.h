@@ -399,9 +399,10 @@ int kda_forward_two_pass(const int32_t *plan, const int32_t *plan_dev, int32_t H
  *   dh0      out device fp32 [N][H][K][V] (the gradient of the initial
  *            states, defined also when h0 is NULL) or NULL (not written).
  *   ws, ws_bytes  device workspace of at least kda_backward_workspace_bytes.
- * Steps on 'stream': the forward's preparation, local state pass and
- * composition (S_in, the segment transitions A and the final-state
- * transitions of continuing pieces); every piece from its true incoming
+ * Steps on 'stream': the forward's preparation (which also leaves each
+ * chunk's terms for the backward), local state pass and composition (S_in,
+ * the segment transitions A and the final-state transitions of continuing
+ * pieces); every piece from its true incoming
  * state, recording each chunk's start state; the incoming-state gradient of
  * every continuing piece through its own outputs; the following summaries,
  * last segment first, giving each segment's end-state gradient; every piece
@@ -424,9 +425,9 @@ int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t
  * forward's outputs, the chunk start states and end-state gradients
  * (2 * H * n_chunks * K * V * 4 bytes), the segment gradients
  * (2 * S * H * K * V * 4 bytes), the kernels' working areas, each chunk's
- * terms for the gradient pass (65,536 bytes per chunk and head), and each
- * chunk's bf16 operand images for the reverse chains (132,096 bytes per
- * chunk and head). */
+ * FP32 terms for the gradient pass (65,536 bytes per chunk and head), and
+ * each chunk's bf16 operand images for the reverse chains and the gradient
+ * pass (132,096 bytes per chunk and head). */
 size_t kda_backward_workspace_bytes(const int32_t *plan, int32_t H);
 
 /*
