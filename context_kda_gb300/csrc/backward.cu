@@ -78,6 +78,13 @@ __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast
 __device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 sub4(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+// 4 bf16 (8 bytes) as fp32
+__device__ __forceinline__ float4 bf4(uint2 w)
+{
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xFFFF0000u));
+}
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
 __device__ __forceinline__ float4 scl4(float s, float4 a) { return make_float4(s * a.x, s * a.y, s * a.z, s * a.w); }
 __device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
@@ -420,14 +427,15 @@ __device__ __forceinline__ void bf8(uint4 w, float *x)
     }
 }
 
-// The chunk's element-wise terms into scratch sc (rows past L are zero): Kt, Kh, Qt, V, E = e^Gamma,
-// Ei = e^-Gamma, gc = e^Gamma_C, beta, Diag(beta) Kt and Diag(beta) V.
-__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_t *q, const uint16_t *k,
-                            const uint16_t *v, const float *g, const float *beta, float scale)
+// The chunk's element-wise terms into scratch sc (rows past L are zero where they carry k or v): V,
+// E = e^Gamma, Ei = e^-Gamma, gc = e^Gamma_C, beta, Diag(beta) Kt and Diag(beta) V.  (Kt = E k, Kh = Ei k
+// and Qt = scale E q are formed where they are used, from E, Ei and the bf16 rows.)
+__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_t *k, const uint16_t *v,
+                            const float *g, const float *beta)
 {
     extern __shared__ __align__(16) float bsm[];
     const int tid = threadIdx.x;
-    float *Kt = sc + S_KT, *Kh = sc + S_KH, *Qt = sc + S_QT, *Vf = sc + S_VF, *E = sc + S_E, *Ei = sc + S_EI;
+    float *Vf = sc + S_VF, *E = sc + S_E, *Ei = sc + S_EI;
     if (tid < 64) sc[S_BT + tid] = tid < L ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
     // V rows: 8 channels a piece, 4 pieces a thread
     {
@@ -453,7 +461,7 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
     {
         const int cq = tid & 31, rg = tid >> 5;
         float4 gv[8];
-        uint2 kw[8], qw[8];
+        uint2 kw[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int r = rg * 8 + j;
@@ -461,7 +469,6 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
             const bool ok = r < L;
             gv[j] = ok ? ld4(g + gi) : make_float4(0.f, 0.f, 0.f, 0.f);
             kw[j] = ok ? *reinterpret_cast<const uint2 *>(k + gi) : make_uint2(0u, 0u);
-            qw[j] = ok ? *reinterpret_cast<const uint2 *>(q + gi) : make_uint2(0u, 0u);
         }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -489,33 +496,21 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
             const float4 G = add4(gv[j], off);
             const float4 ex = make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
             const float4 exi = make_float4(expf(-G.x), expf(-G.y), expf(-G.z), expf(-G.w));
-            const float4 kf = make_float4(__uint_as_float(kw[j].x << 16), __uint_as_float(kw[j].x & 0xFFFF0000u),
-                                          __uint_as_float(kw[j].y << 16), __uint_as_float(kw[j].y & 0xFFFF0000u));
-            const float4 qf = make_float4(__uint_as_float(qw[j].x << 16), __uint_as_float(qw[j].x & 0xFFFF0000u),
-                                          __uint_as_float(qw[j].y << 16), __uint_as_float(qw[j].y & 0xFFFF0000u));
-            st4(Kt + e, mul4(ex, kf));
-            st4(Kh + e, mul4(exi, kf));
-            st4(Qt + e, scl4(scale, mul4(ex, qf)));
             st4(E + e, ex);
             st4(Ei + e, exi);
+            st4(sc + S_BKT + e, scl4(sc[S_BT + rg * 8 + j], mul4(ex, bf4(kw[j]))));   // Diag(beta) Kt
         }
     }
     __syncthreads();
-    // Diag(beta) Kt and Diag(beta) V
+    // Diag(beta) V
     {
-        float4 kv[8], vv[8];
+        float4 vv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vv[i] = ld4(Vf + 4 * (tid + i * BT));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = 4 * (tid + i * BT);
-            kv[i] = ld4(Kt + e);
-            vv[i] = ld4(Vf + e);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = 4 * (tid + i * BT);
-            const float b = sc[S_BT + (e >> 7)];
-            st4(sc + S_BKT + e, scl4(b, kv[i]));
-            st4(sc + S_BV + e, scl4(b, vv[i]));
+            st4(sc + S_BV + e, scl4(sc[S_BT + (e >> 7)], vv[i]));
         }
     }
     __syncthreads();
@@ -643,7 +638,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const int h = unit / n_chunks, c = unit % n_chunks;
         const int32_t *cr = pv.chunk(c);
         const int t0 = cr[1], L = cr[2];
-        chunk_rows(sc, t0, L, h, H, q, k, v, g, beta, scale);
+        chunk_rows(sc, t0, L, h, H, k, v, g, beta);
         const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S, T
         // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them;
         // Kh, QK, Qt, W (as W^T) and dO come as the chunk's operand images; X, DG = Dc G, T and beta Kt leave their
@@ -711,13 +706,16 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         product<64, KD, 64, false, false>(img_b(img_a(none, dmi), im + RIMG_KH), none,
                                           out(dKt, KD, 1.f, sc + S_DBKT, KD, nullptr, sc + S_BT));
         product<64, KD, 64, true, false>(img_b(img_a(none, dmi), bkti), none, out(dKh, KD, 1.f, dKh, KD));
-        // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S): a warp per 8 rows, then a warp sum
+        // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S) (Kt = E k): a warp per 8 rows, then a
+        // warp sum
         {
             const int ln = tid & 31;
 #pragma unroll 2
             for (int j = 0; j < 8; ++j) {
                 const int r = warp_id() * 8 + j;
-                const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = ld4(sc + S_KT + r * KD + 4 * ln);
+                const uint2 kw = r < L ? *reinterpret_cast<const uint2 *>(k + (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * ln)
+                                       : make_uint2(0u, 0u);
+                const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = mul4(ld4(sc + S_E + r * KD + 4 * ln), bf4(kw));
                 const float4 cv = ld4(sc + S_DBV + r * VD + 4 * ln), d = ld4(sc + S_VF + r * VD + 4 * ln);
                 const float2 mm = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
                 const float2 sv = *reinterpret_cast<const float2 *>(tm + BT_S + r * 64 + 2 * ln);
@@ -726,31 +724,42 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
             }
         }
         __syncthreads();
-        // dGamma = Kt dKt - Kh dKh + Qt dQt (+ dGamma_C on the last row), dg its reverse cumulative sum:
-        // each thread holds rows 8 rg .. 8 rg + 7 of channels 4 cq .. 4 cq + 3, sums them from the bottom,
-        // and adds the totals of the row groups below (met in shared memory)
+        // dq = scale E dQt and dk = E dKt + Ei dKh, and with them dGamma = Kt dKt - Kh dKh + Qt dQt
+        // = k (E dKt - Ei dKh) + q dq (+ dGamma_C on the last row), dg its reverse cumulative sum: each thread
+        // holds rows 8 rg .. 8 rg + 7 of channels 4 cq .. 4 cq + 3, sums them from the bottom, and adds the
+        // totals of the row groups below (met in shared memory)
         {
             extern __shared__ __align__(16) float bsm[];
             const int cq = tid & 31, rg = tid >> 5;
             float4 suf[8];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float4 a[4], b[4], cv[4], d[4], e2[4], f[4];
+                float4 ea[4], ei[4], dkt[4], dkh[4], dqt[4];
+                uint2 kw[4], qw[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int e = (rg * 8 + half * 4 + j) * KD + 4 * cq;
-                    a[j] = ld4(sc + S_KT + e);
-                    b[j] = ld4(dKt + e);
-                    cv[j] = ld4(sc + S_KH + e);
-                    d[j] = ld4(dKh + e);
-                    e2[j] = ld4(sc + S_QT + e);
-                    f[j] = ld4(dQt + e);
+                    const int r = rg * 8 + half * 4 + j;
+                    const int e = r * KD + 4 * cq;
+                    const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
+                    ea[j] = ld4(sc + S_E + e);
+                    ei[j] = ld4(sc + S_EI + e);
+                    dkt[j] = ld4(dKt + e);
+                    dkh[j] = ld4(dKh + e);
+                    dqt[j] = ld4(dQt + e);
+                    kw[j] = r < L ? *reinterpret_cast<const uint2 *>(k + gi) : make_uint2(0u, 0u);
+                    qw[j] = r < L ? *reinterpret_cast<const uint2 *>(q + gi) : make_uint2(0u, 0u);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 kk = mul4(a[j], b[j]), hh = mul4(cv[j], d[j]), qq = mul4(e2[j], f[j]);
-                    suf[half * 4 + j] = make_float4(kk.x - hh.x + qq.x, kk.y - hh.y + qq.y, kk.z - hh.z + qq.z,
-                                                    kk.w - hh.w + qq.w);
+                    const int r = rg * 8 + half * 4 + j;
+                    const float4 a = mul4(ea[j], dkt[j]), b = mul4(ei[j], dkh[j]);
+                    const float4 dqv = scl4(scale, mul4(ea[j], dqt[j]));
+                    if (r < L) {
+                        const size_t o = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
+                        st4(dq + o, dqv);
+                        st4(dk + o, add4(a, b));
+                    }
+                    suf[half * 4 + j] = add4(mul4(bf4(kw[j]), sub4(a, b)), mul4(bf4(qw[j]), dqv));
                 }
             }
             if (L - 1 >= rg * 8 && L - 1 < rg * 8 + 8) {
@@ -776,18 +785,11 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 if (r < L) st4(dg + (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq, add4(suf[j], off));
             }
         }
-        // dq = scale E dQt, dk = E dKt + Ei dKh, dv = beta d(bV)
+        // dv = beta d(beta V)
 #pragma unroll 2
         for (int i = 0; i < 8; ++i) {
             const int e = 4 * (tid + i * BT), r = e >> 7, cc = e & 127;
-            if (r < L) {
-                const float4 ex = ld4(sc + S_E + e), exi = ld4(sc + S_EI + e);
-                const float4 a = ld4(dQt + e), b = ld4(dKt + e), d = ld4(dKh + e), dvv = ld4(sc + S_DBV + e);
-                const size_t o = (static_cast<size_t>(t0 + r) * H + h) * KD + cc;
-                st4(dq + o, scl4(scale, mul4(ex, a)));
-                st4(dk + o, add4(mul4(ex, b), mul4(exi, d)));
-                st4(dv + o, scl4(sc[S_BT + r], dvv));
-            }
+            if (r < L) st4(dv + (static_cast<size_t>(t0 + r) * H + h) * VD + cc, scl4(sc[S_BT + r], ld4(sc + S_DBV + e)));
         }
         for (int r = tid; r < L; r += BT) dbeta[static_cast<size_t>(t0 + r) * H + h] = sc[S_DBETA + r];
         __syncthreads();

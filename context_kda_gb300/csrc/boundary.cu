@@ -136,17 +136,6 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
     if (n_run <= 0) return;
     unsigned char *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    // units n .. n + 3 of the run (cursor and record; valid while inside the run)
-    Cursor c0{run.x, run.y, run.z};
-    Rec r0 = rec_info(pv, H, c0.h, c0.rec, c0.tile);
-    Cursor c1 = c0, c2, c3;
-    Rec r1 = r0, r2 = r0, r3 = r0;
-    if (n_run > 1) { advance(c1, r0, n_cont); r1 = rec_info(pv, H, c1.h, c1.rec, c1.tile); }
-    c2 = c1;
-    if (n_run > 2) { advance(c2, r1, n_cont); r2 = rec_info(pv, H, c2.h, c2.rec, c2.tile); }
-    c3 = c2;
-    if (n_run > 3) { advance(c3, r2, n_cont); r3 = rec_info(pv, H, c3.h, c3.rec, c3.tile); }
-
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_mbar[i]), 1);
@@ -208,14 +197,34 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
         m_pend |= 1u << t;
     };
 
-    // qhat and the local outputs come from the state pass, which completed before the composition (this
-    // kernel's prerequisite) passed its own wait and let this kernel's CTAs start: the first tiles are
-    // requested while the composition still runs; S_in, the composition's result, only after the wait
+    // Units n .. n + 3 of the run (cursor and record; valid while inside the run).  qhat and the local
+    // outputs come from the state pass, which completed before the composition (this kernel's
+    // prerequisite) passed its own wait and let this kernel's CTAs start: each of the first tiles is
+    // requested as soon as its unit's record is known, while the composition still runs; S_in, the
+    // composition's result, only after the wait.
+    Cursor c0{run.x, run.y, run.z};
+    Rec r0 = rec_info(pv, H, c0.h, c0.rec, c0.tile);
     if (tid == 0) {
         if (via_tma(r0)) fetch_q(r0, 0);
-        if (n_run > 1 && via_tma(r1)) fetch_q(r1, 1);
-        if (n_run > 2 && via_tma(r2)) fetch_q(r2, 2);
         if (tiled(r0)) fetch_o(r0, c0.h, 0);
+    }
+    Cursor c1 = c0, c2, c3;
+    Rec r1 = r0, r2 = r0, r3 = r0;
+    if (n_run > 1) {
+        advance(c1, r0, n_cont);
+        r1 = rec_info(pv, H, c1.h, c1.rec, c1.tile);
+        if (tid == 0 && via_tma(r1)) fetch_q(r1, 1);
+    }
+    c2 = c1;
+    if (n_run > 2) {
+        advance(c2, r1, n_cont);
+        r2 = rec_info(pv, H, c2.h, c2.rec, c2.tile);
+        if (tid == 0 && via_tma(r2)) fetch_q(r2, 2);
+    }
+    c3 = c2;
+    if (n_run > 3) {
+        advance(c3, r2, n_cont);
+        r3 = rec_info(pv, H, c3.h, c3.rec, c3.tile);
     }
     grid_dep_wait();   // S_in comes from the composition
 
