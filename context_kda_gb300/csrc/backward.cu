@@ -554,10 +554,13 @@ __global__ void __launch_bounds__(BT) bwd_do_images(const int32_t *plan, PlanSig
 //    G_end[j] = dfinal of the sequence ending at b_{j+1}, if one does; otherwise, with p the
 //    continuing piece that opens segment j+1,
 //    G_end[j] = Qd[j+1] + (P_end(p)^T dfinal[seq] if p ends its sequence, else A[j+1]^T G_end[j+1]).
+constexpr int CMP_SMEM = (KD * KD + KD * 32) * 4;   // the map's matrix and the gradient's column slice
+
 __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSig sig, int H, const float *A,
                                                   const float *afin, const float *dfinal, const float *Qd,
                                                   float *G_end)
 {
+    extern __shared__ __align__(16) float csm[];
     BWD_PLAN_CHECK();
     const PlanView pv{plan};
     const int h = blockIdx.x / 4, col0 = (blockIdx.x % 4) * 32;
@@ -591,31 +594,51 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
             Mt = A + (static_cast<size_t>(j + 1) * H + h) * KD * KD;
             gin = G_end + (static_cast<size_t>(j + 1) * H + h) * SQ;
         }
-        // out[r][c] = qd[r][c] + sum_i Mt[i][r] gin[i][c]  (4 rows x 4 columns per thread)
+        // out[r][c] = qd[r][c] + sum_i Mt[i][r] gin[i][c]  (4 rows x 4 columns per thread), with Mt and this
+        // CTA's column slice of gin staged in shared memory first (every 16-byte load of a thread in flight)
         const int rr = (tid >> 3) * 4, cc = col0 + (tid & 7) * 4;
+        float *const sM = csm, *const sG = csm + KD * KD;
+        if (gin) {
+            float4 mv[16], gv[4];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mv[i] = ld4(Mt + 4 * (tid + i * BT));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = tid + i * BT;
+                gv[i] = ld4(gin + (e >> 3) * VD + col0 + 4 * (e & 7));
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) st4(sM + 4 * (tid + i * BT), mv[i]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = tid + i * BT;
+                st4(sG + (e >> 3) * 32 + 4 * (e & 7), gv[i]);
+            }
+        }
         float acc[4][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) acc[a][bb] = qd[(rr + a) * VD + cc + bb];
-        if (gin)
+        for (int a = 0; a < 4; ++a) {
+            const float4 q4 = ld4(qd + (rr + a) * VD + cc);
+            acc[a][0] = q4.x;
+            acc[a][1] = q4.y;
+            acc[a][2] = q4.z;
+            acc[a][3] = q4.w;
+        }
+        __syncthreads();   // the staged operands are in; every read of G_end[j + 1] is done before G_end[j]
+                           // is written (other slices of the same rows belong to other CTAs)
+        if (gin) {
+#pragma unroll 8
             for (int i = 0; i < KD; ++i) {
-                float m[4], x[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) m[a] = Mt[i * KD + rr + a];
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) x[bb] = gin[i * VD + cc + bb];
+                const float4 m4 = ld4(sM + i * KD + rr), x4 = ld4(sG + i * 32 + (cc - col0));
+                const float m[4] = {m4.x, m4.y, m4.z, m4.w}, x[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
                     for (int bb = 0; bb < 4; ++bb) acc[a][bb] = fmaf(m[a], x[bb], acc[a][bb]);
             }
-        __syncthreads();   // every read of G_end[j + 1] is done before G_end[j] is written (other slices
-                           // of the same rows belong to other CTAs and are not touched here)
+        }
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) out[(rr + a) * VD + cc + bb] = acc[a][bb];
+        for (int a = 0; a < 4; ++a) st4(out + (rr + a) * VD + cc, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
         __syncthreads();
     }
 }
@@ -823,7 +846,8 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
         err = launch_reverse_tc(plan_host, plan_dev, H, false, img, dfinal, G_end, Qd, gs, dh0, stream);
         if (err != cudaSuccess) return err;
     }
-    bwd_compose<<<H * 4, BT, 0, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
+    if ((err = set_dynamic_smem(reinterpret_cast<const void *>(bwd_compose), CMP_SMEM)) != cudaSuccess) return err;
+    bwd_compose<<<H * 4, BT, CMP_SMEM, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     err = launch_reverse_tc(plan_host, plan_dev, H, true, img, dfinal, G_end, Qd, gs, dh0, stream);
     if (err != cudaSuccess) return err;

@@ -15,9 +15,9 @@
 // (lane v, column k) as an FP32 accumulator, and DG next to it split into bf16 hi/lo pairs, the A
 // operand of the first product.  Per chunk:
 //   workers: DG = Dc G (FP32 back into the accumulator, and split)   -> issuer:
-//   dU^T = DG^T Kh^T (3-term) + dO^T QK (2-term)                       -> workers:
-//   -dU^T split into TMEM                                              -> issuer:
-//   G^T += dO^T Qt (2-term) - dU^T W (3-term)
+//   dU^T = dO^T QK (2-term, issued while the workers form DG) + DG^T Kh^T (3-term) -> workers:
+//   -dU^T split into TMEM (meanwhile the issuer adds G^T += dO^T Qt, 2-term)       -> issuer:
+//   G^T -= dU^T W (3-term)
 // The operands come as ready bf16 images (written once per chunk by the forward's preparation in its
 // backward mode, dO's by a small kernel) by bulk copies: the part the first product reads is
 // double-buffered and arrives a chunk ahead, the part the second reads is single-buffered and arrives
@@ -227,10 +227,28 @@ reverse_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const unsigned 
             const int b = i & 1;
             const uint32_t pa = sbase + OFF_A + b * A_STRIDE, pb = sbase + OFF_B;
             if (!(ok = mbar_wait(smem_u32(&s_pa[b]), (i >> 1) & 1))) break;
-            if (!(ok = mbar_wait(smem_u32(&s_hdg), i & 1))) break;
+            fence_after();
+            // dU^T = dO^T QK + DG^T Kh^T.  The first term needs only the chunk's images: it goes in while the
+            // workers form DG (the accumulator is free: the workers read the previous chunk's dU before
+            // handing its split over, and that chunk's second product was issued after it).
+            {
+                // dO^T QK: A = dO^T (rows r, cols v, read MN-major), B(r, r') = QK[r'][r] (rows r', read MN-major)
+                const uint32_t id2 = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tbase + TU, sdesc(pa + RIMG_DO + kk * 256, 128, RIMG_CS),
+                                 sdesc(pa + RIMG_QK + ps * 8192 + kk * 256, 128, RIMG_CS), id2, (ps | kk) != 0);
+            }
+            if (!(ok = mbar_wait(smem_u32(&s_hdg), i & 1))) {
+                commit(m1);   // the first term is in flight: it lands before the CTA frees its tensor memory
+                ++n1;
+                break;
+            }
             fence_after();
             {
-                // dU^T = DG^T Kh^T: A = DG^T from TMEM (K = k), B = Kh read K-major (rows r, cols k)
+                // + DG^T Kh^T: A = DG^T from TMEM (K = k), B = Kh read K-major (rows r, cols k)
                 const uint32_t id = idesc_bf16(128, 64);
                 const uint32_t aof[3] = {TDGH, TDGH, TDGL}, bof[3] = {0, 16384, 0};
 #pragma unroll
@@ -238,23 +256,15 @@ reverse_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const unsigned 
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_bf16_ta(tbase + TU, tbase + aof[ps] + kk * 8,
-                                    sdesc(pa + RIMG_KH + bof[ps] + kk * 2 * RIMG_CS, RIMG_CS), id, (ps | kk) != 0);
-                // + dO^T QK: A = dO^T (rows r, cols v, read MN-major), B(r, r') = QK[r'][r] (rows r', read MN-major)
-                const uint32_t id2 = idesc_bf16(128, 64, 1, 1);
-#pragma unroll
-                for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tbase + TU, sdesc(pa + RIMG_DO + kk * 256, 128, RIMG_CS),
-                                 sdesc(pa + RIMG_QK + ps * 8192 + kk * 256, 128, RIMG_CS), id2, 1u);
+                                    sdesc(pa + RIMG_KH + bof[ps] + kk * 2 * RIMG_CS, RIMG_CS), id, 1u);
                 commit(m1);
                 ++n1;
             }
             if (!(ok = mbar_wait(smem_u32(&s_pb), i & 1))) break;
-            if (!(ok = mbar_wait(smem_u32(&s_hu), i & 1))) break;
             fence_after();
             {
-                // G^T += dO^T Qt: B(k, r) = Qt[r][k] (rows r, read MN-major)
+                // G^T += dO^T Qt: B(k, r) = Qt[r][k] (rows r, read MN-major).  DG is in the accumulator: this
+                // term goes in while the workers split -dU.
                 const uint32_t id3 = idesc_bf16(128, 128, 1, 1);
 #pragma unroll
                 for (int ps = 0; ps < 2; ++ps)
@@ -262,6 +272,14 @@ reverse_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const unsigned 
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16(tbase + TG, sdesc(pa + RIMG_DO + kk * 256, 128, RIMG_CS),
                                  sdesc(pb + ps * 16384 + kk * 256, 128, RIMG_CS), id3, 1u);
+            }
+            if (!(ok = mbar_wait(smem_u32(&s_hu), i & 1))) {
+                commit(m2);   // the term in flight lands before the CTA frees its tensor memory
+                ++n2;
+                break;
+            }
+            fence_after();
+            {
                 // G^T += (-dU^T) W: A from TMEM (K = r), B(k, r) = W^T[k][r] (the image of W^T: rows k,
                 // chunk stride 2048, read K-major)
                 const uint32_t id4 = idesc_bf16(128, 128, 0, 0);
