@@ -505,7 +505,8 @@ extern "C" int kda_backward_segmented(const int32_t *plan, const int32_t *plan_d
     return cuda_status(kda::launch_backward(
         plan, plan_dev, H, q, k, v, g, beta, scale, dout, dfinal, w.A, w.afin,
         reinterpret_cast<const float *>(b + off[2]), reinterpret_cast<float *>(b + off[3]),
-        reinterpret_cast<float *>(b + off[4]), reinterpret_cast<float *>(b + off[5]),
-        reinterpret_cast<float *>(b + off[7]), reinterpret_cast<unsigned char *>(b + off[8]),
+        reinterpret_cast<float *>(b + off[4]), reinterpret_cast<float *>(b + off[5]), w.S_in,
+        reinterpret_cast<const float *>(b + off[1]), reinterpret_cast<float *>(b + off[7]),
+        reinterpret_cast<unsigned char *>(b + off[8]),
         reinterpret_cast<float *>(b + off[6]), kBackwardGrid, dq, dk, dv, dg, dbeta, dh0, s));
 }

@@ -647,9 +647,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
 __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig sig, int H, const uint16_t *q,
                                                 const uint16_t *k, const uint16_t *v, const float *g,
                                                 const float *beta, float scale, const uint16_t *dout,
-                                                const float *xs, const float *gs, const float *terms,
-                                                const unsigned char *img, float *dq, float *dk, float *dv, float *dg,
-                                                float *dbeta, float *scratch)
+                                                const float *xs, const float *gs, const float *S_in,
+                                                const float *fin_out, const float *terms, const unsigned char *img,
+                                                float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                                                float *scratch)
 {
     BWD_PLAN_CHECK();
     tc_begin();
@@ -669,13 +670,22 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         // leaves its result as an image, so later products bring their operands in by bulk copies
         const float *X = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
         const float *G = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
+        // the state after the chunk: the next chunk's recorded start state, or the piece's end state (the
+        // final state of a sequence that ends there, else the state entering the next segment)
+        const float *Xn;
+        {
+            const int32_t *pc = pv.piece(cr[0]);
+            if (cr[3] + 1 < (pc[PC_LEN] + CH - 1) / CH) Xn = X + SQ;
+            else if (pc[PC_FLAGS] & KDA_PIECE_SEQ_END) Xn = fin_out + (static_cast<size_t>(pc[PC_SEQ]) * H + h) * SQ;
+            else Xn = S_in + (static_cast<size_t>(pc[PC_SEG] + 1) * H + h) * SQ;
+        }
         const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
         unsigned char *const sci = reinterpret_cast<unsigned char *>(sc);
         unsigned char *const xi = sci + 4 * S_XI, *const dgi = sci + 4 * S_DGI, *const ti = sci + 4 * S_TI;
         unsigned char *const bkti = sci + 4 * S_BKTI, *const ui = sci + 4 * S_UI, *const dqki = sci + 4 * S_DQKI;
         unsigned char *const dui = sci + 4 * S_DUI, *const dwi = sci + 4 * S_DWI, *const dti = sci + 4 * S_DTI;
         unsigned char *const t64i = sci + 4 * S_T64I, *const dmi = sci + 4 * S_DMI;
-        float *Y = sc + S_Y, *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dM = sc + S_DM, *dKt = sc + S_DKT;
+        float *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dM = sc + S_DM, *dKt = sc + S_DKT;
         const float *bKt = sc + S_BKT, *bV = sc + S_BV;
         const Term none = term(nullptr, 0, nullptr, 0);
         __syncthreads();
@@ -692,21 +702,20 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         // dKh = U DG^T + dQK^T Qt
         product<64, KD, VD, false, true, 64, true, false>(img_b(img_a(none, ui), dgi), img_b(img_a(none, dqki), im + RIMG_QT),
                                                           out(dKh, KD));
-        // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c]: Y = X + Kh^T U
-        product<KD, VD, 64, true, false>(img_b(img_a(none, im + RIMG_KH), ui), none, out(Y, VD, 1.f, X, VD));
-        {   // a warp per 16 rows k, 4 columns a lane, then a warp sum per row
+        // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c] = sum_c G[k][c] X'[k][c], X' = Diag(gc) (X + Kh^T U)
+        // the state after the chunk: a warp per 16 rows k, 4 columns a lane, then a warp sum per row
+        {
             float4 gv[16], yv[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int e = (warp_id() * 16 + j) * VD + 4 * (tid & 31);
                 gv[j] = ld4(G + e);
-                yv[j] = ld4(Y + e);
+                yv[j] = ld4(Xn + e);
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float sum = warp_sum(dot4(gv[j], yv[j]));
-                const int kr = warp_id() * 16 + j;
-                if ((tid & 31) == 0) sc[S_DGC + kr] = sum * sc[S_GC + kr];
+                if ((tid & 31) == 0) sc[S_DGC + warp_id() * 16 + j] = sum;
             }
         }
         // dQt = dO X^T + dQK Kh
@@ -827,9 +836,9 @@ size_t backward_scratch_floats() { return static_cast<size_t>(SCRATCH_FLOATS); }
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                             const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
                             const uint16_t *dout, const float *dfinal, const float *A, const float *afin,
-                            const float *xs, float *gs, float *G_end, float *Qd, float *terms, unsigned char *img,
-                            float *scratch, int grid, float *dq, float *dk, float *dv, float *dg, float *dbeta,
-                            float *dh0, cudaStream_t stream)
+                            const float *xs, float *gs, float *G_end, float *Qd, const float *S_in,
+                            const float *fin_out, float *terms, unsigned char *img, float *scratch, int grid, float *dq,
+                            float *dk, float *dv, float *dg, float *dbeta, float *dh0, cudaStream_t stream)
 {
     const PlanView pv{plan_host};
     const PlanSig sig = plan_sig(plan_host);
@@ -851,8 +860,8 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     err = launch_reverse_tc(plan_host, plan_dev, H, true, img, dfinal, G_end, Qd, gs, dh0, stream);
     if (err != cudaSuccess) return err;
-    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, terms, img,
-                                              dq, dk, dv, dg, dbeta, scratch);
+    bwd_grads<<<grid, BT, BWD_SMEM, stream>>>(plan_dev, sig, H, q, k, v, g, beta, scale, dout, xs, gs, S_in, fin_out,
+                                              terms, img, dq, dk, dv, dg, dbeta, scratch);
     return cudaGetLastError();
 }
 

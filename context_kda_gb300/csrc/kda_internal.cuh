@@ -196,9 +196,9 @@ int take_reverse_status();
 cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, int H, const uint16_t *q,
                             const uint16_t *k, const uint16_t *v, const float *g, const float *beta, float scale,
                             const uint16_t *dout, const float *dfinal, const float *A, const float *afin,
-                            const float *xs, float *gs, float *G_end, float *Qd, float *terms, unsigned char *img,
-                            float *scratch, int grid, float *dq, float *dk, float *dv, float *dg, float *dbeta,
-                            float *dh0, cudaStream_t stream);
+                            const float *xs, float *gs, float *G_end, float *Qd, const float *S_in,
+                            const float *fin_out, float *terms, unsigned char *img, float *scratch, int grid, float *dq,
+                            float *dk, float *dv, float *dg, float *dbeta, float *dh0, cudaStream_t stream);
 // Segments per group of the blocked scan (about sqrt(S)) and the number of groups.
 int scan_group_size(int S);
 cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *S_in,
