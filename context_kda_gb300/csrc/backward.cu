@@ -54,19 +54,19 @@ enum : int {
     S_X = 0, S_G = S_X + SQ, S_Y = S_G + SQ,
     S_KT = S_Y + SQ, S_KH = S_KT + CK, S_QT = S_KH + CK, S_VF = S_QT + CK, S_E = S_VF + CK, S_EI = S_E + CK,
     S_U = S_EI + CK, S_DO = S_U + CK, S_DU = S_DO + CK, S_DKH = S_DU + CK,
-    S_DQT = S_DKH + CK, S_DW = S_DQT + CK, S_DKT = S_DW + CK, S_BKT = S_DKT + CK, S_BV = S_BKT + CK,
-    S_DBKT = S_BV + CK, S_DBV = S_DBKT + CK,
+    S_DQT = S_DKH + CK, S_DW = S_DQT + CK, S_DKT = S_DW + CK,
+    S_DBKT = S_DKT + CK, S_DBV = S_DBKT + CK,
     S_DQK = S_DBV + CK, S_DT = S_DQK + CC, S_DM = S_DT + CC, S_T64 = S_DM + CC,
     S_GC = S_T64 + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64, S_DBETA = S_DGC + KD,
     // bf16 hi/lo images of the gradient pass's operands (bytes / 4): X and DG (128 x 128), T (64 x 64),
     // beta Kt (64 x 128), and the products U, dQK, dU, dW, dT, T^T dT, dM
-    S_IMG = (S_DBETA + 64 + 255) & ~255, S_XI = S_IMG, S_DGI = S_XI + SQ, S_TI = S_DGI + SQ, S_BKTI = S_TI + CC,
-    S_UI = S_BKTI + CK, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
+    S_IMG = (S_DBETA + 64 + 255) & ~255, S_XI = S_IMG, S_DGI = S_XI + SQ,
+    S_UI = S_DGI + SQ, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
     S_T64I = S_DTI + CC, S_DMI = S_T64I + CC, S_IMG_END = S_DMI + CC,
     SCRATCH_FLOATS = S_IMG_END
 };
 
-static_assert(BT_UT == 0 && BT_S == CK && BT_T == BT_S + CC && BT_FLOATS == BT_T + CC, "the chunk terms' layout");
+static_assert(BT_UT == 0 && BT_S == CK && BT_FLOATS == BT_S + CC, "the chunk terms' layout");
 
 // Dynamic shared memory of the backward's kernels: both operands of one product, k-major.
 constexpr size_t BWD_SMEM = 6ull * 32768 + 1024;   // the operand tiles of a two-term product, aligned to 1024 bytes
@@ -211,11 +211,6 @@ __device__ __forceinline__ Term img_b(Term t, const unsigned char *p, bool singl
 {
     t.ib = p;
     t.b_single = single;
-    return t;
-}
-__device__ __forceinline__ Term save_a(Term t, unsigned char *p)
-{
-    t.sa = p;
     return t;
 }
 __device__ __forceinline__ Term save_b(Term t, unsigned char *p)
@@ -427,11 +422,11 @@ __device__ __forceinline__ void bf8(uint4 w, float *x)
     }
 }
 
-// The chunk's element-wise terms into scratch sc (rows past L are zero where they carry k or v): V,
-// E = e^Gamma, Ei = e^-Gamma, gc = e^Gamma_C, beta, Diag(beta) Kt and Diag(beta) V.  (Kt = E k, Kh = Ei k
-// and Qt = scale E q are formed where they are used, from E, Ei and the bf16 rows.)
-__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_t *k, const uint16_t *v,
-                            const float *g, const float *beta)
+// The chunk's element-wise terms into scratch sc (rows past L are zero where they carry v): V,
+// E = e^Gamma, Ei = e^-Gamma, gc = e^Gamma_C and beta.  (Kt = E k, Kh = Ei k and Qt = scale E q are formed
+// where they are used, from E, Ei and the bf16 rows; Diag(beta) Kt and Diag(beta) V come as images.)
+__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_t *v, const float *g,
+                            const float *beta)
 {
     extern __shared__ __align__(16) float bsm[];
     const int tid = threadIdx.x;
@@ -461,14 +456,11 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
     {
         const int cq = tid & 31, rg = tid >> 5;
         float4 gv[8];
-        uint2 kw[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int r = rg * 8 + j;
             const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
-            const bool ok = r < L;
-            gv[j] = ok ? ld4(g + gi) : make_float4(0.f, 0.f, 0.f, 0.f);
-            kw[j] = ok ? *reinterpret_cast<const uint2 *>(k + gi) : make_uint2(0u, 0u);
+            gv[j] = r < L ? ld4(g + gi) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -498,19 +490,6 @@ __device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_
             const float4 exi = make_float4(expf(-G.x), expf(-G.y), expf(-G.z), expf(-G.w));
             st4(E + e, ex);
             st4(Ei + e, exi);
-            st4(sc + S_BKT + e, scl4(sc[S_BT + rg * 8 + j], mul4(ex, bf4(kw[j]))));   // Diag(beta) Kt
-        }
-    }
-    __syncthreads();
-    // Diag(beta) V
-    {
-        float4 vv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vv[i] = ld4(Vf + 4 * (tid + i * BT));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = 4 * (tid + i * BT);
-            st4(sc + S_BV + e, scl4(sc[S_BT + (e >> 7)], vv[i]));
         }
     }
     __syncthreads();
@@ -662,12 +641,13 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const int h = unit / n_chunks, c = unit % n_chunks;
         const int32_t *cr = pv.chunk(c);
         const int t0 = cr[1], L = cr[2];
-        chunk_rows(sc, t0, L, h, H, k, v, g, beta);
-        const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S, T
+        chunk_rows(sc, t0, L, h, H, v, g, beta);
+        const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S
         // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them;
-        // Kh, QK, Qt, W (as W^T) and dO come as the chunk's operand images; X, DG = Dc G, T and beta Kt leave their
-        // split in an image where they are first staged, and every product whose result feeds another
-        // leaves its result as an image, so later products bring their operands in by bulk copies
+        // Kh, QK, Qt, W (as W^T), dO, T, Diag(beta) Kt and Diag(beta) V come as the chunk's operand images; X
+        // and DG = Dc G leave their split in an image where they are first staged, and every product whose
+        // result feeds another leaves its result as an image, so later products bring their operands in by
+        // bulk copies
         const float *X = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
         const float *G = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
         // the state after the chunk: the next chunk's recorded start state, or the piece's end state (the
@@ -681,12 +661,12 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         }
         const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
         unsigned char *const sci = reinterpret_cast<unsigned char *>(sc);
-        unsigned char *const xi = sci + 4 * S_XI, *const dgi = sci + 4 * S_DGI, *const ti = sci + 4 * S_TI;
-        unsigned char *const bkti = sci + 4 * S_BKTI, *const ui = sci + 4 * S_UI, *const dqki = sci + 4 * S_DQKI;
+        unsigned char *const xi = sci + 4 * S_XI, *const dgi = sci + 4 * S_DGI;
+        unsigned char *const ui = sci + 4 * S_UI, *const dqki = sci + 4 * S_DQKI;
+        const unsigned char *const ti = im + RIMG_T, *const bkti = im + RIMG_BKT;   // T, Diag(beta) Kt
         unsigned char *const dui = sci + 4 * S_DUI, *const dwi = sci + 4 * S_DWI, *const dti = sci + 4 * S_DTI;
         unsigned char *const t64i = sci + 4 * S_T64I, *const dmi = sci + 4 * S_DMI;
         float *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dM = sc + S_DM, *dKt = sc + S_DKT;
-        const float *bKt = sc + S_BKT, *bV = sc + S_BV;
         const Term none = term(nullptr, 0, nullptr, 0);
         __syncthreads();
         // U = Ut - W X (W from the image of W^T as it lies)
@@ -724,10 +704,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         // dW = -dU X^T
         product<64, KD, VD, false, true>(img_b(img_a(none, dui), xi), none, out_img(out(nullptr, 0, -1.f), dwi));
         // dT = dW (beta Kt)^T + dU (beta V)^T
-        product<64, 64, KD, false, true, VD, false, true>(save_b(img_a(term(nullptr, 0, bKt, KD), dwi), bkti),
-                                                          img_a(term(nullptr, 0, bV, VD), dui), out_img(out(nullptr, 0), dti));
+        product<64, 64, KD, false, true, VD, false, true>(img_b(img_a(none, dwi), bkti),
+                                                          img_b(img_a(none, dui), im + RIMG_BV), out_img(out(nullptr, 0), dti));
         // d(beta Kt) = T^T dW, d(beta V) = T^T dU
-        product<64, KD, 64, true, false>(save_a(img_b(term(tm + BT_T, 64, nullptr, 0), dwi), ti), none,
+        product<64, KD, 64, true, false>(img_b(img_a(none, ti), dwi), none,
                                          out(sc + S_DBKT, KD));
         product<64, VD, 64, true, false>(img_b(img_a(none, ti), dui), none, out(sc + S_DBV, VD));
         // dM = strictly_lower(-T^T dT T^T)

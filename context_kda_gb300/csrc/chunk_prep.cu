@@ -26,9 +26,10 @@
 // unit's diagonal blocks.
 //
 // Backward mode (BWD): the same pass also leaves what the backward reads of each unit, in the layouts
-// its kernels use: the FP32 terms Ut (row-major), S = strictly_lower(Kt Kh^T) and T = (I + M)^-1
-// (lower), and the bf16 hi/lo images of Kh, Qt, the masked QK, W (as W^T: rows k, cols r) and
-// exp(Gamma_C).  Qt then enters [KK; QK] with its low part too, so QK is a full three-term product.
+// its kernels use: the FP32 terms Ut (row-major) and S = strictly_lower(Kt Kh^T), and the bf16 hi/lo
+// images of Kh, Qt, the masked QK, W (as W^T: rows k, cols r), exp(Gamma_C), T = (I + M)^-1 (lower),
+// Diag(beta) Kt and Diag(beta) V.  Qt then enters [KK; QK] with its low part too, so QK is a full
+// three-term product.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -397,6 +398,21 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                     split8(kt, hi, lo);
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + o_r) = hi;
                     *reinterpret_cast<uint4 *>(base + OFF_KQ + T128 + o_r) = lo;
+                    if constexpr (BWD) {   // Diag(beta) Kt and Diag(beta) V for the gradient pass
+                        const float br = s_beta[r];
+                        float bx[8], vf[8];
+#pragma unroll
+                        for (int e8 = 0; e8 < 8; ++e8) bx[e8] = br * kt[e8];
+                        split8(bx, hi, lo);
+                        *reinterpret_cast<uint4 *>(im + RIMG_BKT + o_64) = hi;
+                        *reinterpret_cast<uint4 *>(im + RIMG_BKT + T64 + o_64) = lo;
+                        bf16x8_to_f32(vw[i], vf);
+#pragma unroll
+                        for (int e8 = 0; e8 < 8; ++e8) bx[e8] = br * vf[e8];
+                        split8(bx, hi, lo);
+                        *reinterpret_cast<uint4 *>(im + RIMG_BV + o_64) = hi;
+                        *reinterpret_cast<uint4 *>(im + RIMG_BV + T64 + o_64) = lo;
+                    }
                     if constexpr (BWD) {
                         // the backward's QK and Qt take the full split
                         split8(qt, hi, lo);
@@ -573,20 +589,27 @@ chunk_prep_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, long long n_
                 // lanes: 8 consecutive rows x four 16-column groups (conflict-free row-piece reads)
                 const int r = ((tid >> 5) << 3) | (tid & 7), i0 = ((tid >> 3) & 3) * 16;
                 float tv[16];
+                float tfull[BWD ? 16 : 1];   // (backward mode) T itself, for its image
 #pragma unroll
                 for (int m4 = 0; m4 < 4; ++m4) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(f32_at(base, OFF_T32, r, i0 + 4 * m4));
                     const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
-                    float tl4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i = i0 + 4 * m4 + e;
-                        tl4[e] = (i <= r) ? tt[e] : 0.f;   // T, zero above the diagonal
-                        tv[4 * m4 + e] = tl4[e] * s_beta[i];
+                        const float t = (i <= r) ? tt[e] : 0.f;   // T, zero above the diagonal
+                        tv[4 * m4 + e] = t * s_beta[i];
+                        if constexpr (BWD) tfull[4 * m4 + e] = t;
                     }
-                    if constexpr (BWD)
-                        *reinterpret_cast<float4 *>(bt + BT_T + r * 64 + i0 + 4 * m4) =
-                            make_float4(tl4[0], tl4[1], tl4[2], tl4[3]);
+                }
+                if constexpr (BWD) {   // T's image for the gradient pass (rows r, cols i)
+                    uint4 hi, lo;
+                    split8(tfull, hi, lo);
+                    *reinterpret_cast<uint4 *>(im + RIMG_T + cm_off(r, i0, 1024)) = hi;
+                    *reinterpret_cast<uint4 *>(im + RIMG_T + 8192 + cm_off(r, i0, 1024)) = lo;
+                    split8(tfull + 8, hi, lo);
+                    *reinterpret_cast<uint4 *>(im + RIMG_T + cm_off(r, i0 + 8, 1024)) = hi;
+                    *reinterpret_cast<uint4 *>(im + RIMG_T + 8192 + cm_off(r, i0 + 8, 1024)) = lo;
                 }
                 st_split8(base + OFF_TP + cm_off(r, i0, 1024), base + OFF_TP + 8192 + cm_off(r, i0, 1024), tv);
                 st_split8(base + OFF_TP + cm_off(r, i0 + 8, 1024), base + OFF_TP + 8192 + cm_off(r, i0 + 8, 1024),

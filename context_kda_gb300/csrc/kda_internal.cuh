@@ -174,20 +174,23 @@ size_t scan_scratch_bytes(const int32_t *plan_host, int H);
 // backward_scratch_floats() floats; xs and gs hold [H][n_chunks][K][V] floats each, G_end and Qd
 // [S][H][K][V] each.
 size_t backward_scratch_floats();
-// The FP32 chunk terms the backward's gradient pass reads, per (head, chunk) (floats, row-major): Ut
-// (64 x 128), S = strictly_lower(Kt Kh^T) and T = (I + Diag(beta) S)^-1 (64 x 64 each).  The preparation
-// kernel writes them in its backward mode.
-constexpr int BT_UT = 0, BT_S = 64 * 128, BT_T = BT_S + 64 * 64, BT_FLOATS = BT_T + 64 * 64;
+// The FP32 chunk terms the backward's gradient pass reads element-wise or as an accumulated input, per
+// (head, chunk) (floats, row-major): Ut (64 x 128) and S = strictly_lower(Kt Kh^T) (64 x 64).  The
+// preparation kernel writes them in its backward mode.
+constexpr int BT_UT = 0, BT_S = 64 * 128, BT_FLOATS = BT_S + 64 * 64;
 // Per-(chunk, head) operand images of the backward (bytes), written by the preparation kernel's
 // backward mode (dO by its own small kernel): bf16 tiles in the no-swizzle canonical layout (8-column
 // chunks of the tile's rows x 16 bytes), hi then lo where split.  The part the first product of a
 // reverse chain step reads (Kh rows r x cols k, QK rows r' x cols r, dO rows r x cols v, each with
 // chunk stride RIMG_CS, and exp(Gamma_C) as 128 fp32) comes first, then the part the second reads (Qt
-// rows r x cols k, chunk stride RIMG_CS; W as its transpose, rows k x cols r, chunk stride 2048).
+// rows r x cols k, chunk stride RIMG_CS; W as its transpose, rows k x cols r, chunk stride 2048), then
+// what only the gradient pass reads: Diag(beta) Kt (rows r x cols k), Diag(beta) V (rows r x cols v) and
+// T (rows r x cols i), chunk stride RIMG_CS.
 constexpr uint32_t RIMG_CS = 1024;
 constexpr uint32_t RIMG_KH = 0, RIMG_QK = 32768, RIMG_DO = 49152, RIMG_GC = 65536, RIMG_A_BYTES = 66048;
 constexpr uint32_t RIMG_QT = 66560, RIMG_W = RIMG_QT + 32768, RIMG_B_BYTES = 65536;
-constexpr uint32_t RIMG_UNIT = RIMG_QT + RIMG_B_BYTES;
+constexpr uint32_t RIMG_BKT = RIMG_QT + RIMG_B_BYTES, RIMG_BV = RIMG_BKT + 32768, RIMG_T = RIMG_BV + 32768;
+constexpr uint32_t RIMG_UNIT = RIMG_T + 16384;
 static_assert(RIMG_UNIT % 1024 == 0 && RIMG_QT % 1024 == 0 && RIMG_A_BYTES % 16 == 0, "image layout");
 cudaError_t launch_reverse_tc(const int32_t *plan_host, const int32_t *plan_dev, int H, bool true_pass,
                               const unsigned char *img, const float *dfinal, const float *G_end, float *Qd,

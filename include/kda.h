@@ -425,9 +425,9 @@ int kda_backward_segmented(const int32_t *plan, const int32_t *plan_dev, int32_t
  * forward's outputs, the chunk start states and end-state gradients
  * (2 * H * n_chunks * K * V * 4 bytes), the segment gradients
  * (2 * S * H * K * V * 4 bytes), the kernels' working areas, each chunk's
- * FP32 terms for the gradient pass (65,536 bytes per chunk and head), and
+ * FP32 terms for the gradient pass (49,152 bytes per chunk and head), and
  * each chunk's bf16 operand images for the reverse chains and the gradient
- * pass (132,096 bytes per chunk and head). */
+ * pass (214,016 bytes per chunk and head). */
 size_t kda_backward_workspace_bytes(const int32_t *plan, int32_t H);
 
 /*
