@@ -49,18 +49,14 @@ constexpr int SQ = KD * VD;                  // a 128 x 128 state
 
 __device__ int g_bwd_status;
 
-// Per-CTA scratch (floats): three states, seventeen 64 x 128 and four 64 x 64 matrices, vectors.
+// Per-CTA scratch (floats): the FP32 product results an element-wise step reads (dKh, dQt, dKt, d(beta Kt),
+// d(beta V): 64 x 128; dM: 64 x 64), row vectors (gc, beta, dGamma_C), then bf16 hi/lo images (bytes / 4) of
+// the operands the threads stage (X and DG, 128 x 128) and of the products' results that later products read
+// (U, dQK, dU, dW, dT, T^T dT, dM).  About 0.47 MB: the working areas of all CTAs fit in the L2.
 enum : int {
-    S_X = 0, S_G = S_X + SQ, S_Y = S_G + SQ,
-    S_KT = S_Y + SQ, S_KH = S_KT + CK, S_QT = S_KH + CK, S_VF = S_QT + CK, S_E = S_VF + CK, S_EI = S_E + CK,
-    S_U = S_EI + CK, S_DO = S_U + CK, S_DU = S_DO + CK, S_DKH = S_DU + CK,
-    S_DQT = S_DKH + CK, S_DW = S_DQT + CK, S_DKT = S_DW + CK,
-    S_DBKT = S_DKT + CK, S_DBV = S_DBKT + CK,
-    S_DQK = S_DBV + CK, S_DT = S_DQK + CC, S_DM = S_DT + CC, S_T64 = S_DM + CC,
-    S_GC = S_T64 + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64, S_DBETA = S_DGC + KD,
-    // bf16 hi/lo images of the gradient pass's operands (bytes / 4): X and DG (128 x 128), T (64 x 64),
-    // beta Kt (64 x 128), and the products U, dQK, dU, dW, dT, T^T dT, dM
-    S_IMG = (S_DBETA + 64 + 255) & ~255, S_XI = S_IMG, S_DGI = S_XI + SQ,
+    S_DKH = 0, S_DQT = S_DKH + CK, S_DKT = S_DQT + CK, S_DBKT = S_DKT + CK, S_DBV = S_DBKT + CK,
+    S_DM = S_DBV + CK, S_GC = S_DM + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64,
+    S_IMG = (S_DGC + KD + 255) & ~255, S_XI = S_IMG, S_DGI = S_XI + SQ,
     S_UI = S_DGI + SQ, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
     S_T64I = S_DTI + CC, S_DMI = S_T64I + CC, S_IMG_END = S_DMI + CC,
     SCRATCH_FLOATS = S_IMG_END
@@ -403,95 +399,14 @@ __device__ void product(const Term t1, const Term t2, const Out o)
     if (tid == 0) s_tc_phase = ph ^ 1u;
 }
 
-// C(m, n) = alpha * sum_k A(m, k) B(k, n) (+ C(m, n) when acc): a one-term product.
-template <int M, int N, int K, bool TA, bool TB>
-__device__ __forceinline__ void gemm(const float *a, int lda, const float *b, int ldb, float *C, int ldc, float alpha,
-                                     bool acc)
+// The chunk's row scalars into scratch sc: beta (rows past L zero) and gc = e^Gamma_C (from the chunk's
+// image, the values the reverse chains decayed with).
+__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const float *beta, const unsigned char *im)
 {
-    product<M, N, K, TA, TB>(term(a, lda, b, ldb), term(nullptr, 0, nullptr, 0), out(C, ldc, alpha, acc ? C : nullptr, ldc));
-}
-
-// 8 bf16 (one 16-byte word) as fp32
-__device__ __forceinline__ void bf8(uint4 w, float *x)
-{
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        x[2 * p] = __uint_as_float(ww[p] << 16);
-        x[2 * p + 1] = __uint_as_float(ww[p] & 0xFFFF0000u);
-    }
-}
-
-// The chunk's element-wise terms into scratch sc (rows past L are zero where they carry v): V,
-// E = e^Gamma, Ei = e^-Gamma, gc = e^Gamma_C and beta.  (Kt = E k, Kh = Ei k and Qt = scale E q are formed
-// where they are used, from E, Ei and the bf16 rows; Diag(beta) Kt and Diag(beta) V come as images.)
-__device__ void chunk_rows(float *sc, int t0, int L, int h, int H, const uint16_t *v, const float *g,
-                            const float *beta)
-{
-    extern __shared__ __align__(16) float bsm[];
     const int tid = threadIdx.x;
-    float *Vf = sc + S_VF, *E = sc + S_E, *Ei = sc + S_EI;
     if (tid < 64) sc[S_BT + tid] = tid < L ? beta[static_cast<size_t>(t0 + tid) * H + h] : 0.f;
-    // V rows: 8 channels a piece, 4 pieces a thread
-    {
-        uint4 vw[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = tid + i * BT, r = e >> 4, c8 = (e & 15) << 3;
-            vw[i] = r < L ? *reinterpret_cast<const uint4 *>(v + (static_cast<size_t>(t0 + r) * H + h) * VD + c8)
-                          : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = tid + i * BT, r = e >> 4, c8 = (e & 15) << 3;
-            float x[8];
-            bf8(vw[i], x);
-            st4(Vf + r * VD + c8, make_float4(x[0], x[1], x[2], x[3]));
-            st4(Vf + r * VD + c8 + 4, make_float4(x[4], x[5], x[6], x[7]));
-        }
-    }
-    // Gamma = cumulative g down the rows, per channel: each thread holds rows 8 rg .. 8 rg + 7 of
-    // channels 4 cq .. 4 cq + 3, scans them, and adds the totals of the row groups above (met in
-    // shared memory); then the decayed rows
-    {
-        const int cq = tid & 31, rg = tid >> 5;
-        float4 gv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = rg * 8 + j;
-            const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
-            gv[j] = r < L ? ld4(g + gi) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            acc = add4(acc, gv[j]);
-            gv[j] = acc;
-        }
-        float4 *const tot = reinterpret_cast<float4 *>(bsm);   // [row group][channel quad]
-        __syncthreads();   // shared memory free
-        tot[rg * 32 + cq] = acc;
-        __syncthreads();
-        float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int g2 = 0; g2 < 7; ++g2) {
-            const float4 t = tot[g2 * 32 + cq];
-            if (g2 < rg) off = add4(off, t);
-        }
-        if (rg == 7) {
-            const float4 gs = add4(off, acc);
-            st4(sc + S_GC + 4 * cq, make_float4(expf(gs.x), expf(gs.y), expf(gs.z), expf(gs.w)));
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = (rg * 8 + j) * KD + 4 * cq;
-            const float4 G = add4(gv[j], off);
-            const float4 ex = make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
-            const float4 exi = make_float4(expf(-G.x), expf(-G.y), expf(-G.z), expf(-G.w));
-            st4(E + e, ex);
-            st4(Ei + e, exi);
-        }
-    }
+    else if (tid < 64 + KD / 4)
+        st4(sc + S_GC + 4 * (tid - 64), ld4(reinterpret_cast<const float *>(im + RIMG_GC) + 4 * (tid - 64)));
     __syncthreads();
 }
 
@@ -641,7 +556,8 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const int h = unit / n_chunks, c = unit % n_chunks;
         const int32_t *cr = pv.chunk(c);
         const int t0 = cr[1], L = cr[2];
-        chunk_rows(sc, t0, L, h, H, v, g, beta);
+        const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
+        chunk_rows(sc, t0, L, h, H, beta, im);
         const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S
         // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them;
         // Kh, QK, Qt, W (as W^T), dO, T, Diag(beta) Kt and Diag(beta) V come as the chunk's operand images; X
@@ -659,7 +575,6 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
             else if (pc[PC_FLAGS] & KDA_PIECE_SEQ_END) Xn = fin_out + (static_cast<size_t>(pc[PC_SEQ]) * H + h) * SQ;
             else Xn = S_in + (static_cast<size_t>(pc[PC_SEG] + 1) * H + h) * SQ;
         }
-        const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
         unsigned char *const sci = reinterpret_cast<unsigned char *>(sc);
         unsigned char *const xi = sci + 4 * S_XI, *const dgi = sci + 4 * S_DGI;
         unsigned char *const ui = sci + 4 * S_UI, *const dqki = sci + 4 * S_DQKI;
@@ -718,61 +633,76 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         product<64, KD, 64, false, false>(img_b(img_a(none, dmi), im + RIMG_KH), none,
                                           out(dKt, KD, 1.f, sc + S_DBKT, KD, nullptr, sc + S_BT));
         product<64, KD, 64, true, false>(img_b(img_a(none, dmi), bkti), none, out(dKh, KD, 1.f, dKh, KD));
-        // dbeta = rowsum(d(bKt) Kt) + rowsum(d(bV) V) + rowsum(dM S) (Kt = E k): a warp per 8 rows, then a
-        // warp sum
-        {
-            const int ln = tid & 31;
-#pragma unroll 2
-            for (int j = 0; j < 8; ++j) {
-                const int r = warp_id() * 8 + j;
-                const uint2 kw = r < L ? *reinterpret_cast<const uint2 *>(k + (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * ln)
-                                       : make_uint2(0u, 0u);
-                const float4 a = ld4(sc + S_DBKT + r * KD + 4 * ln), b = mul4(ld4(sc + S_E + r * KD + 4 * ln), bf4(kw));
-                const float4 cv = ld4(sc + S_DBV + r * VD + 4 * ln), d = ld4(sc + S_VF + r * VD + 4 * ln);
-                const float2 mm = *reinterpret_cast<const float2 *>(dM + r * 64 + 2 * ln);
-                const float2 sv = *reinterpret_cast<const float2 *>(tm + BT_S + r * 64 + 2 * ln);
-                const float sum = warp_sum(dot4(a, b) + dot4(cv, d) + mm.x * sv.x + mm.y * sv.y);
-                if (ln == 0) sc[S_DBETA + r] = sum;
-            }
-        }
         __syncthreads();
-        // dq = scale E dQt and dk = E dKt + Ei dKh, and with them dGamma = Kt dKt - Kh dKh + Qt dQt
-        // = k (E dKt - Ei dKh) + q dq (+ dGamma_C on the last row), dg its reverse cumulative sum: each thread
-        // holds rows 8 rg .. 8 rg + 7 of channels 4 cq .. 4 cq + 3, sums them from the bottom, and adds the
-        // totals of the row groups below (met in shared memory)
+        // The rows' input gradients in one pass.  Each thread holds rows 8 rg .. 8 rg + 7 and columns
+        // 4 cq .. 4 cq + 3 (of K, and of V for v and d(beta V); of the 64-wide dM and S rows on lanes cq < 16).
+        // Gamma = cumulative g down the rows (the row groups' totals met in shared memory); per row, with
+        // E = e^Gamma and Ei = e^-Gamma:
+        //   dq = scale E dQt,  dk = E dKt + Ei dKh,  dv = beta d(beta V),
+        //   dbeta = rowsum(d(beta Kt) E k) + rowsum(d(beta V) v) + rowsum(dM S)  (a warp sum per row),
+        //   dGamma = Kt dKt - Kh dKh + Qt dQt = k (E dKt - Ei dKh) + q dq  (+ dGamma_C on the last row),
+        // and dg is its reverse cumulative sum (the row groups' totals met in shared memory again).
         {
             extern __shared__ __align__(16) float bsm[];
+            float4 *const tot = reinterpret_cast<float4 *>(bsm);   // [row group][channel quad]
             const int cq = tid & 31, rg = tid >> 5;
+            float4 gam[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = rg * 8 + j;
+                gam[j] = r < L ? ld4(g + (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc = add4(acc, gam[j]);
+                    gam[j] = acc;
+                }
+                tot[rg * 32 + cq] = acc;
+                __syncthreads();
+                float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int g2 = 0; g2 < 7; ++g2) {
+                    const float4 t = tot[g2 * 32 + cq];
+                    if (g2 < rg) off = add4(off, t);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gam[j] = add4(gam[j], off);
+                __syncthreads();   // the totals are read: the suffix sums below reuse the array
+            }
             float4 suf[8];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float4 ea[4], ei[4], dkt[4], dkh[4], dqt[4];
-                uint2 kw[4], qw[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = rg * 8 + half * 4 + j;
-                    const int e = r * KD + 4 * cq;
-                    const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
-                    ea[j] = ld4(sc + S_E + e);
-                    ei[j] = ld4(sc + S_EI + e);
-                    dkt[j] = ld4(dKt + e);
-                    dkh[j] = ld4(dKh + e);
-                    dqt[j] = ld4(dQt + e);
-                    kw[j] = r < L ? *reinterpret_cast<const uint2 *>(k + gi) : make_uint2(0u, 0u);
-                    qw[j] = r < L ? *reinterpret_cast<const uint2 *>(q + gi) : make_uint2(0u, 0u);
+            for (int j = 0; j < 8; ++j) {
+                const int r = rg * 8 + j;
+                const bool live = r < L;
+                const size_t gi = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;   // (V = K columns)
+                const int e = r * KD + 4 * cq;
+                const uint2 kw = live ? *reinterpret_cast<const uint2 *>(k + gi) : make_uint2(0u, 0u);
+                const uint2 qw = live ? *reinterpret_cast<const uint2 *>(q + gi) : make_uint2(0u, 0u);
+                const uint2 vw = live ? *reinterpret_cast<const uint2 *>(v + gi) : make_uint2(0u, 0u);
+                const float4 dkt = ld4(dKt + e), dkh = ld4(dKh + e), dqt = ld4(dQt + e);
+                const float4 dbk = ld4(sc + S_DBKT + e), dbv = ld4(sc + S_DBV + e);
+                float4 ms = make_float4(0.f, 0.f, 0.f, 0.f), sv = ms;
+                if (cq < 16) {
+                    ms = ld4(dM + r * 64 + 4 * cq);
+                    sv = ld4(tm + BT_S + r * 64 + 4 * cq);
                 }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = rg * 8 + half * 4 + j;
-                    const float4 a = mul4(ea[j], dkt[j]), b = mul4(ei[j], dkh[j]);
-                    const float4 dqv = scl4(scale, mul4(ea[j], dqt[j]));
-                    if (r < L) {
-                        const size_t o = (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq;
-                        st4(dq + o, dqv);
-                        st4(dk + o, add4(a, b));
-                    }
-                    suf[half * 4 + j] = add4(mul4(bf4(kw[j]), sub4(a, b)), mul4(bf4(qw[j]), dqv));
+                const float4 G = gam[j];
+                const float4 ea = make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
+                const float4 ei = make_float4(expf(-G.x), expf(-G.y), expf(-G.z), expf(-G.w));
+                const float4 a = mul4(ea, dkt), b = mul4(ei, dkh);
+                const float4 dqv = scl4(scale, mul4(ea, dqt));
+                const float4 kf = bf4(kw);
+                const float br = sc[S_BT + r];
+                if (live) {
+                    st4(dq + gi, dqv);
+                    st4(dk + gi, add4(a, b));
+                    st4(dv + gi, scl4(br, dbv));
                 }
+                suf[j] = add4(mul4(kf, sub4(a, b)), mul4(bf4(qw), dqv));
+                const float part = warp_sum(dot4(dbk, mul4(ea, kf)) + dot4(dbv, bf4(vw)) + dot4(ms, sv));
+                if (cq == 0 && live) dbeta[static_cast<size_t>(t0 + r) * H + h] = part;
             }
             if (L - 1 >= rg * 8 && L - 1 < rg * 8 + 8) {
                 const float4 dgc = ld4(sc + S_DGC + 4 * cq);
@@ -782,7 +712,6 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
             }
 #pragma unroll
             for (int j = 6; j >= 0; --j) suf[j] = add4(suf[j], suf[j + 1]);
-            float4 *const tot = reinterpret_cast<float4 *>(bsm);   // [row group][channel quad]
             tot[rg * 32 + cq] = suf[0];
             __syncthreads();
             float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -797,13 +726,6 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 if (r < L) st4(dg + (static_cast<size_t>(t0 + r) * H + h) * KD + 4 * cq, add4(suf[j], off));
             }
         }
-        // dv = beta d(beta V)
-#pragma unroll 2
-        for (int i = 0; i < 8; ++i) {
-            const int e = 4 * (tid + i * BT), r = e >> 7, cc = e & 127;
-            if (r < L) st4(dv + (static_cast<size_t>(t0 + r) * H + h) * VD + cc, scl4(sc[S_BT + r], ld4(sc + S_DBV + e)));
-        }
-        for (int r = tid; r < L; r += BT) dbeta[static_cast<size_t>(t0 + r) * H + h] = sc[S_DBETA + r];
         __syncthreads();
     }
     tc_end();
