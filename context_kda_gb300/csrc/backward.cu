@@ -51,13 +51,13 @@ __device__ int g_bwd_status;
 
 // Per-CTA scratch (floats): the FP32 product results an element-wise step reads (dKh, dQt, dKt, d(beta Kt),
 // d(beta V): 64 x 128; dM: 64 x 64), row vectors (gc, beta, dGamma_C), then bf16 hi/lo images (bytes / 4) of
-// the operands the threads stage (X and DG, 128 x 128) and of the products' results that later products read
-// (U, dQK, dU, dW, dT, T^T dT, dM).  About 0.47 MB: the working areas of all CTAs fit in the L2.
+// the products' results that later products read (U, dQK, dU, dW, dT, T^T dT, dM).  About 0.34 MB: the
+// working areas of all CTAs fit in the L2.
 enum : int {
     S_DKH = 0, S_DQT = S_DKH + CK, S_DKT = S_DQT + CK, S_DBKT = S_DKT + CK, S_DBV = S_DBKT + CK,
     S_DM = S_DBV + CK, S_GC = S_DM + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64,
-    S_IMG = (S_DGC + KD + 255) & ~255, S_XI = S_IMG, S_DGI = S_XI + SQ,
-    S_UI = S_DGI + SQ, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
+    S_IMG = (S_DGC + KD + 255) & ~255,
+    S_UI = S_IMG, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
     S_T64I = S_DTI + CC, S_DMI = S_T64I + CC, S_IMG_END = S_DMI + CC,
     SCRATCH_FLOATS = S_IMG_END
 };
@@ -68,13 +68,22 @@ static_assert(BT_UT == 0 && BT_S == CK && BT_FLOATS == BT_S + CC, "the chunk ter
 constexpr size_t BWD_SMEM = 6ull * 32768 + 1024;   // the operand tiles of a two-term product, aligned to 1024 bytes
 
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
-__device__ __forceinline__ int warp_id() { return static_cast<int>(threadIdx.x) >> 5; }
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 // Orders this thread's generic-proxy global writes before later bulk (async-proxy) reads of them.
 __device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 __device__ __forceinline__ float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
 __device__ __forceinline__ float4 sub4(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+// 8 bf16 (16 bytes) as fp32
+__device__ __forceinline__ void bf16x8(uint4 w, float *x)
+{
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        x[2 * p] = __uint_as_float(ww[p] << 16);
+        x[2 * p + 1] = __uint_as_float(ww[p] & 0xFFFF0000u);
+    }
+}
 // 4 bf16 (8 bytes) as fp32
 __device__ __forceinline__ float4 bf4(uint2 w)
 {
@@ -207,11 +216,6 @@ __device__ __forceinline__ Term img_b(Term t, const unsigned char *p, bool singl
 {
     t.ib = p;
     t.b_single = single;
-    return t;
-}
-__device__ __forceinline__ Term save_b(Term t, unsigned char *p)
-{
-    t.sb = p;
     return t;
 }
 
@@ -559,24 +563,24 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
         chunk_rows(sc, t0, L, h, H, beta, im);
         const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S
-        // X (the chunk's start state) and G (its end-state gradient) are read where the chains left them;
-        // Kh, QK, Qt, W (as W^T), dO, T, Diag(beta) Kt and Diag(beta) V come as the chunk's operand images; X
-        // and DG = Dc G leave their split in an image where they are first staged, and every product whose
-        // result feeds another leaves its result as an image, so later products bring their operands in by
-        // bulk copies
-        const float *X = xs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
-        const float *G = gs + (static_cast<size_t>(h) * n_chunks + c) * SQ;
-        // the state after the chunk: the next chunk's recorded start state, or the piece's end state (the
+        // Every operand comes as a bf16 hi/lo image by bulk copies: X^T and DG^T as the chains recorded them;
+        // Kh, QK, Qt, W (as W^T), dO, T, Diag(beta) Kt and Diag(beta) V as the chunk's operand images; and every
+        // product whose result feeds another leaves its result as an image
+        // X (the chunk's start state) and DG = Dc G (G its end-state gradient) as the chains recorded them:
+        // the bf16 hi/lo images of X^T and DG^T as they lie (rows v, cols k)
+        const unsigned char *const xt = reinterpret_cast<const unsigned char *>(xs + (static_cast<size_t>(h) * n_chunks + c) * SQ);
+        const unsigned char *const dgt = reinterpret_cast<const unsigned char *>(gs + (static_cast<size_t>(h) * n_chunks + c) * SQ);
+        // the state after the chunk: the next chunk's recorded image, or the piece's end state (FP32 K x V: the
         // final state of a sequence that ends there, else the state entering the next segment)
-        const float *Xn;
+        const unsigned char *xn_img = nullptr;
+        const float *xn = nullptr;
         {
             const int32_t *pc = pv.piece(cr[0]);
-            if (cr[3] + 1 < (pc[PC_LEN] + CH - 1) / CH) Xn = X + SQ;
-            else if (pc[PC_FLAGS] & KDA_PIECE_SEQ_END) Xn = fin_out + (static_cast<size_t>(pc[PC_SEQ]) * H + h) * SQ;
-            else Xn = S_in + (static_cast<size_t>(pc[PC_SEG] + 1) * H + h) * SQ;
+            if (cr[3] + 1 < (pc[PC_LEN] + CH - 1) / CH) xn_img = xt + SQ * 4;
+            else if (pc[PC_FLAGS] & KDA_PIECE_SEQ_END) xn = fin_out + (static_cast<size_t>(pc[PC_SEQ]) * H + h) * SQ;
+            else xn = S_in + (static_cast<size_t>(pc[PC_SEG] + 1) * H + h) * SQ;
         }
         unsigned char *const sci = reinterpret_cast<unsigned char *>(sc);
-        unsigned char *const xi = sci + 4 * S_XI, *const dgi = sci + 4 * S_DGI;
         unsigned char *const ui = sci + 4 * S_UI, *const dqki = sci + 4 * S_DQKI;
         const unsigned char *const ti = im + RIMG_T, *const bkti = im + RIMG_BKT;   // T, Diag(beta) Kt
         unsigned char *const dui = sci + 4 * S_DUI, *const dwi = sci + 4 * S_DWI, *const dti = sci + 4 * S_DTI;
@@ -585,39 +589,60 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const Term none = term(nullptr, 0, nullptr, 0);
         __syncthreads();
         // U = Ut - W X (W from the image of W^T as it lies)
-        product<64, VD, KD, true, false>(save_b(img_a(term(nullptr, 0, X, VD), im + RIMG_W), xi), none,
-                                         out_img(out(nullptr, 0, -1.f, tm + BT_UT, VD), ui));
+        product<64, VD, KD, true, true>(img_b(img_a(none, im + RIMG_W), xt), none,
+                                        out_img(out(nullptr, 0, -1.f, tm + BT_UT, VD), ui));
         // dQK = lower(dO U^T)
         product<64, 64, VD, false, true, 0, false, false, 1>(img_b(img_a(none, im + RIMG_DO, true), ui), none,
                                                              out_img(out(nullptr, 0), dqki));
-        // dU = Kh DG + QK^T dO (DG = Dc G staged from G)
-        product<64, VD, KD, false, false, 64, true, false>(
-            save_b(img_a(term(nullptr, 0, G, VD, 1.f, sc + S_GC), im + RIMG_KH), dgi),
-            img_b(img_a(none, im + RIMG_QK), im + RIMG_DO, true), out_img(out(nullptr, 0), dui));
+        // dU = Kh DG + QK^T dO
+        product<64, VD, KD, false, true, 64, true, false>(img_b(img_a(none, im + RIMG_KH), dgt),
+                                                          img_b(img_a(none, im + RIMG_QK), im + RIMG_DO, true),
+                                                          out_img(out(nullptr, 0), dui));
         // dKh = U DG^T + dQK^T Qt
-        product<64, KD, VD, false, true, 64, true, false>(img_b(img_a(none, ui), dgi), img_b(img_a(none, dqki), im + RIMG_QT),
-                                                          out(dKh, KD));
-        // dGamma_C[k] = gc[k] sum_c G[k][c] (X + Kh^T U)[k][c] = sum_c G[k][c] X'[k][c], X' = Diag(gc) (X + Kh^T U)
-        // the state after the chunk: a warp per 16 rows k, 4 columns a lane, then a warp sum per row
+        product<64, KD, VD, false, false, 64, true, false>(img_b(img_a(none, ui), dgt), img_b(img_a(none, dqki), im + RIMG_QT),
+                                                           out(dKh, KD));
+        // dGamma_C[k] = gc[k] sum_v G[k][v] (X + Kh^T U)[k][v] = sum_v DG[k][v] X'[k][v] / gc[k], with
+        // X' = Diag(gc) (X + Kh^T U) the state after the chunk (images read as hi + lo): each thread takes the 8
+        // columns k of chunk kc for 8 rows v of group vg, then the 16 groups of a half-warp are summed
         {
-            float4 gv[16], yv[16];
+            const int kc = tid >> 4, vg = tid & 15;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+            for (int i = 0; i < 8; ++i) {
+                const int vv = vg * 8 + i;
+                const uint32_t o = cm_off(vv, kc * 8, 2048);
+                const uint4 dh = *reinterpret_cast<const uint4 *>(dgt + o), dl = *reinterpret_cast<const uint4 *>(dgt + 32768 + o);
+                float d[8], dlo[8], xv[8];
+                bf16x8(dh, d);
+                bf16x8(dl, dlo);
+                if (xn_img) {
+                    float xlo[8];
+                    bf16x8(*reinterpret_cast<const uint4 *>(xn_img + o), xv);
+                    bf16x8(*reinterpret_cast<const uint4 *>(xn_img + 32768 + o), xlo);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int e = (warp_id() * 16 + j) * VD + 4 * (tid & 31);
-                gv[j] = ld4(G + e);
-                yv[j] = ld4(Xn + e);
+                    for (int e = 0; e < 8; ++e) xv[e] += xlo[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xv[e] = xn[(kc * 8 + e) * VD + vv];
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(d[e] + dlo[e], xv[e], acc[e]);
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float sum = warp_sum(dot4(gv[j], yv[j]));
-                if ((tid & 31) == 0) sc[S_DGC + warp_id() * 16 + j] = sum;
+            for (int e = 0; e < 8; ++e) {
+#pragma unroll
+                for (int sh = 8; sh > 0; sh >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], sh);
+            }
+            if (vg == 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sc[S_DGC + kc * 8 + e] = acc[e] / sc[S_GC + kc * 8 + e];
             }
         }
         // dQt = dO X^T + dQK Kh
-        product<64, KD, VD, false, true, 64, false, false>(img_b(img_a(none, im + RIMG_DO, true), xi),
-                                                           img_b(img_a(none, dqki), im + RIMG_KH), out(dQt, KD));
+        product<64, KD, VD, false, false, 64, false, false>(img_b(img_a(none, im + RIMG_DO, true), xt),
+                                                            img_b(img_a(none, dqki), im + RIMG_KH), out(dQt, KD));
         // dW = -dU X^T
-        product<64, KD, VD, false, true>(img_b(img_a(none, dui), xi), none, out_img(out(nullptr, 0, -1.f), dwi));
+        product<64, KD, VD, false, false>(img_b(img_a(none, dui), xt), none, out_img(out(nullptr, 0, -1.f), dwi));
         // dT = dW (beta Kt)^T + dU (beta V)^T
         product<64, 64, KD, false, true, VD, false, true>(img_b(img_a(none, dwi), bkti),
                                                           img_b(img_a(none, dui), im + RIMG_BV), out_img(out(nullptr, 0), dti));

@@ -154,14 +154,25 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
     const uint32_t tbase = s_tmem;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's lane quadrant
     const int c_lane = quad * 32 + lane;                                     // state column of this thread
-    // (STATE_OUTPUT with xs) the start state of the piece's chunk ci, rows k0 .. k0 + 31 of this
-    // thread's column, into xs[h][chunk] (fp32 K x V, row-major): a warp's store covers 128 bytes of a row
+    // (STATE_OUTPUT with xs) the start state of the piece's chunk ci: this thread's row c of X^T, columns
+    // k0 .. k0 + 31, into xs[h][chunk] as the bf16 hi/lo image of X^T as it lies (rows c, cols k: 8-column
+    // chunks of 128 rows x 16 bytes, chunk stride 2048; lo 32 KiB after hi), the backward's operand; a
+    // warp's 16-byte stores cover 512 contiguous bytes
     auto record_x = [&](int ci, int k0, const float (&x)[32]) {
         if constexpr (MODE == STATE_OUTPUT) {
             if (!xs) return;
-            float *dst = xs + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KD * VD + c_lane;
+            unsigned char *const dst = reinterpret_cast<unsigned char *>(
+                                           xs + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KD * VD) +
+                                       cm_off(c_lane, k0, 2048);
+            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dst[(k0 + j) * VD] = x[j];
+            for (int p2 = 0; p2 < 16; ++p2) split_bf16x2(x[2 * p2], x[2 * p2 + 1], hi[p2], lo[p2]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                *reinterpret_cast<uint4 *>(dst + q * 2048) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+                *reinterpret_cast<uint4 *>(dst + 32768 + q * 2048) =
+                    make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+            }
         }
     };
 

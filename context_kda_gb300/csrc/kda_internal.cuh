@@ -171,8 +171,9 @@ cudaError_t launch_compose_blocked(const int32_t *plan_host, const int32_t *plan
                                    const float *B, const float *h0, float *S_in, void *scratch, cudaStream_t stream);
 size_t scan_scratch_bytes(const int32_t *plan_host, int H);
 // The backward (FP32 matrices, products on tcgen05): see backward.cu.  'scratch' holds grid x
-// backward_scratch_floats() floats; xs and gs hold [H][n_chunks][K][V] floats each, G_end and Qd
-// [S][H][K][V] each.
+// backward_scratch_floats() floats; xs and gs hold, per (head, chunk), K x V x 4 bytes: the bf16 hi/lo
+// images (rows v, cols k, 8-column chunks of 128 rows x 16 bytes, lo 32 KiB after hi) of X^T (the chunk's
+// start state) and of DG^T (DG = Dc G, G its end-state gradient); G_end and Qd are [S][H][K][V] floats.
 size_t backward_scratch_floats();
 // The FP32 chunk terms the backward's gradient pass reads element-wise or as an accumulated input, per
 // (head, chunk) (floats, row-major): Ut (64 x 128) and S = strictly_lower(Kt Kh^T) (64 x 64).  The

@@ -7,7 +7,8 @@
 // over a piece's chunks; the local pass starts from a zero gradient at the end of every piece that
 // continues a sequence and gives the gradient of its incoming state through its own outputs (the
 // backward summary Qd of the segment), the true pass starts from dfinal or from the segment's
-// end-state gradient, records G for every chunk and gives dh0 at a sequence start (cuLA PR #136,
+// end-state gradient, records DG = Dc G for every chunk (as the gradient pass's bf16 operand image) and
+// gives dh0 at a sequence start (cuLA PR #136,
 // "feat(kda): add cuDNN concatenated-summary Kimi CP", §Summary: the following summaries are
 // gathered during the backward).
 //
@@ -151,8 +152,8 @@ reverse_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const unsigned 
             }
             if (!mbar_wait_warp(smem_u32(&s_pa[b]), (i >> 1) & 1)) bad = true;   // exp(Gamma_C) of the chunk
             const float *gc = reinterpret_cast<const float *>(base + OFF_A + b * A_STRIDE + RIMG_GC);
-            // ---- G of the chunk's end (recorded by the true pass), then DG = Dc G: FP32 into the
-            //      accumulator (the second product adds onto it) and split into the A operand
+            // ---- G of the chunk's end, then DG = Dc G: FP32 into the accumulator (the second product adds
+            //      onto it) and split into the A operand (and, in the true pass, recorded as an image)
             {
                 uint32_t ga[32], gb[32];
                 tmem_ld32_nowait(tl + TG + hw * 64, ga);
@@ -160,22 +161,33 @@ reverse_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const unsigned 
                 tmem_wait_ld();
                 reg_fence32(ga);
                 reg_fence32(gb);
-                float *rec = TRUE_PASS ? gs + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KD * VD + v : nullptr;
+                // (true pass) DG's record: this thread's row v of DG^T as the bf16 hi/lo image of DG^T as it lies
+                // (rows v, cols k: 8-column chunks of 128 rows x 16 bytes, chunk stride 2048; lo 32 KiB after
+                // hi), the words of its split into TMEM; a warp's 16-byte stores cover 512 contiguous bytes
+                unsigned char *const rec =
+                    TRUE_PASS ? reinterpret_cast<unsigned char *>(gs + (static_cast<size_t>(h) * pv.n_chunks() + c0 + ci) * KD * VD)
+                              : nullptr;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int k0 = hw * 64 + half * 32;
                     float x[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float gv = __uint_as_float(half ? gb[j] : ga[j]);
-                        if (TRUE_PASS) rec[(k0 + j) * VD] = gv;
-                        x[j] = gv * gc[k0 + j];
-                    }
+                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(half ? gb[j] : ga[j]) * gc[k0 + j];
                     tmem_st32(tl + TG + k0, x);
                     uint32_t hi[16], lo[16];
                     split_pairs32(x, hi, lo);
                     tmem_st16_nowait(tl + TDGH + k0 / 2, hi);
                     tmem_st16_nowait(tl + TDGL + k0 / 2, lo);
+                    if (TRUE_PASS) {
+                        unsigned char *const dst = rec + cm_off(v, k0, 2048);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            *reinterpret_cast<uint4 *>(dst + q * 2048) =
+                                make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+                            *reinterpret_cast<uint4 *>(dst + 32768 + q * 2048) =
+                                make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+                        }
+                    }
                 }
                 tmem_wait_st();
             }
