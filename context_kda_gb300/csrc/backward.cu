@@ -140,83 +140,19 @@ __device__ __forceinline__ unsigned char *tc_tiles()
     return bsm_raw + ((1024u - (smem_u32(bsm_raw) & 1023u)) & 1023u);
 }
 
-// Staging of one operand for the tensor core: the source is a row-major FP32 array of R rows and C
-// contiguous columns (leading dimension ld), stored as it lies into the no-swizzle canonical layout as
-// a bf16 hi/lo pair (chunk stride CS); rows_scale, when set, multiplies source row r, and s the whole
-// operand.  The lanes of a warp take consecutive rows of one 8-column piece, so their 16-byte stores
-// land in distinct banks.
-template <int R, int C>
-struct Stage {
-    static constexpr int P = R * C / 8 / BT;   // 8-column pieces per thread
-    float4 v[2 * P];
-    __device__ __forceinline__ void load(const float *src, int ld)
-    {
-#pragma unroll
-        for (int i = 0; i < P; ++i) {
-            const int pc = threadIdx.x + i * BT, r = pc % R, c8 = (pc / R) * 8;
-            v[2 * i] = ld4(src + r * ld + c8);
-            v[2 * i + 1] = ld4(src + r * ld + c8 + 4);
-        }
-    }
-    // save, when set: the same split also into a global image (hi, then lo R * C * 2 bytes on)
-    __device__ __forceinline__ void store(unsigned char *hi, unsigned char *lo, uint32_t cs, const float *rows_scale,
-                                          float s, unsigned char *save)
-    {
-#pragma unroll
-        for (int i = 0; i < P; ++i) {
-            const int pc = threadIdx.x + i * BT, r = pc % R, c8 = (pc / R) * 8;
-            const float f = rows_scale ? s * rows_scale[r] : s;
-            const float4 x0 = scl4(f, v[2 * i]), x1 = scl4(f, v[2 * i + 1]);
-            uint32_t h[4], l[4];
-            split_bf16x2(x0.x, x0.y, h[0], l[0]);
-            split_bf16x2(x0.z, x0.w, h[1], l[1]);
-            split_bf16x2(x1.x, x1.y, h[2], l[2]);
-            split_bf16x2(x1.z, x1.w, h[3], l[3]);
-            const uint32_t off = cm_off(r, c8, cs);
-            const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]), lv = make_uint4(l[0], l[1], l[2], l[3]);
-            *reinterpret_cast<uint4 *>(hi + off) = hv;
-            *reinterpret_cast<uint4 *>(lo + off) = lv;
-            if (save) {
-                *reinterpret_cast<uint4 *>(save + off) = hv;
-                *reinterpret_cast<uint4 *>(save + R * C * 2 + off) = lv;
-            }
-        }
-    }
-};
-
-// One term A B of a product: A(m, k) = TA ? a[k * lda + m] : a[m * lda + k], B(k, n) = TB ? b[n * ldb + k]
-// : b[k * ldb + n], scaled by s; b_rows, when set (only with !TB), multiplies B's row k.  An operand may
-// instead come as an image in global memory (ia / ib): the bf16 hi/lo split of its source as it lies
-// (R rows of its contiguous index, chunk stride R * 16, lo R * C * 2 bytes after hi; a single image
-// holds only hi, the operand being exact in bf16, and the products with its lo part are skipped),
-// brought in by a bulk copy; a staged operand may leave its split in such an image (sa / sb).
+// One term A B of a product, both operands as images in global memory: the bf16 hi/lo split of the
+// operand as it lies (R rows of its contiguous index, chunk stride R * 16, lo R * C * 2 bytes after hi; a
+// single image holds only hi, the operand being exact in bf16, and the products with its lo part are
+// skipped), brought in by bulk copies.  A(m, k) is the image's [k][m] when the product transposes A (rows k),
+// else [m][k]; B(k, n) likewise [n][k] or [k][n].
 struct Term {
-    const float *a;
-    int lda;
-    const float *b;
-    int ldb;
-    float s;
-    const float *b_rows;
-    const unsigned char *ia, *ib;
-    unsigned char *sa, *sb;
+    const unsigned char *a, *b;
     bool a_single, b_single;
 };
-__device__ __forceinline__ Term term(const float *a, int lda, const float *b, int ldb, float s = 1.f,
-                                     const float *b_rows = nullptr)
+__device__ __forceinline__ Term term(const unsigned char *a, const unsigned char *b, bool a_single = false,
+                                     bool b_single = false)
 {
-    return Term{a, lda, b, ldb, s, b_rows, nullptr, nullptr, nullptr, nullptr, false, false};
-}
-__device__ __forceinline__ Term img_a(Term t, const unsigned char *p, bool single = false)
-{
-    t.ia = p;
-    t.a_single = single;
-    return t;
-}
-__device__ __forceinline__ Term img_b(Term t, const unsigned char *p, bool single = false)
-{
-    t.ib = p;
-    t.b_single = single;
-    return t;
+    return Term{a, b, a_single, b_single};
 }
 
 // The output of a product: C[m][n] = out_rows[m] * (alpha * sum of the terms + in_rows[m] * cin[m][n]),
@@ -244,13 +180,12 @@ __device__ __forceinline__ Out out_img(Out o, unsigned char *img)
 }
 
 // An M x N product of one or two terms (K1- and K2-long sums; K2 = 0: one term; M, N, K in {64, 128})
-// by all threads of the CTA.  Every operand is copied as it lies (rows of its contiguous index) into the
-// no-swizzle canonical layout as a bf16 hi/lo pair (chunk stride: its rows x 16) and read by the tensor
-// core K-major or MN-major accordingly, so nothing is transposed on the way; each term is the split
-// hi*hi + hi*lo + lo*hi (~2^-16 relative; without the products of a single operand's absent lo part),
-// both terms accumulate in FP32 in one TMEM accumulator, M = 128 (a 64-row A fills half the lanes: the
-// rows the tensor core reads past it land in lanes that are never read).  Image operands arrive by bulk
-// copies issued first; every staged operand's loads are issued before its first store; the accumulated
+// by all threads of the CTA.  Every operand is an image of its bf16 hi/lo split as it lies (rows of its
+// contiguous index, chunk stride: its rows x 16), brought into the no-swizzle canonical tiles by bulk copies
+// and read by the tensor core K-major or MN-major accordingly, so nothing is transposed on the way; each
+// term is the split hi*hi + hi*lo + lo*hi (~2^-16 relative; without the products of a single operand's
+// absent lo part), both terms accumulate in FP32 in one TMEM accumulator, M = 128 (a 64-row A fills half
+// the lanes: the rows the tensor core reads past it land in lanes that are never read).  The accumulated
 // input is loaded while the tensor core works.
 template <int M, int N, int K1, bool TA1, bool TB1, int K2 = 0, bool TA2 = false, bool TB2 = false, int MASK = 0>
 __device__ void product(const Term t1, const Term t2, const Out o)
@@ -267,60 +202,35 @@ __device__ void product(const Term t1, const Term t2, const Out o)
     static_assert(2 * (A1B + B1B + (K2 ? A2B + B2B : 0)) <= BWD_SMEM - 1024, "the operand tiles fit");
     unsigned char *const a1h = tc_tiles(), *const a1l = a1h + A1B, *const b1h = a1l + A1B, *const b1l = b1h + B1B;
     unsigned char *const a2h = b1l + B1B, *const a2l = a2h + A2B, *const b2h = a2l + A2B, *const b2l = b2h + B2B;
-    const bool any_img = t1.ia || t1.ib || (K2 != 0 && (t2.ia || t2.ib));
-    if (tid == 0 && any_img) {   // image operands: bulk copies into the tiles, counted on s_tc_ld
+    if (tid == 0) {   // the operands: bulk copies into the tiles, counted on s_tc_ld
         const uint32_t ld = smem_u32(&s_tc_ld);
         uint32_t bytes = 0;
-        auto part = [&](const unsigned char *img, bool single, uint32_t nbytes) {
-            if (img) bytes += single ? nbytes : 2 * nbytes;
-        };
-        part(t1.ia, t1.a_single, RA1 * CA1 * 2);
-        part(t1.ib, t1.b_single, RB1 * CB1 * 2);
+        auto part = [&](bool single, uint32_t nbytes) { bytes += single ? nbytes : 2 * nbytes; };
+        part(t1.a_single, RA1 * CA1 * 2);
+        part(t1.b_single, RB1 * CB1 * 2);
         if (K2 != 0) {
-            part(t2.ia, t2.a_single, RA2 * CA2 * 2);
-            part(t2.ib, t2.b_single, RB2 * CB2 * 2);
+            part(t2.a_single, RA2 * CA2 * 2);
+            part(t2.b_single, RB2 * CB2 * 2);
         }
         mbar_arrive_expect_tx(ld, bytes);
         auto copy = [&](const unsigned char *img, bool single, uint32_t nbytes, unsigned char *hi, unsigned char *lo) {
-            if (!img) return;
             bulk_g2s(smem_u32(hi), img, nbytes, ld);
             if (!single) bulk_g2s(smem_u32(lo), img + nbytes, nbytes, ld);
         };
-        copy(t1.ia, t1.a_single, RA1 * CA1 * 2, a1h, a1l);
-        copy(t1.ib, t1.b_single, RB1 * CB1 * 2, b1h, b1l);
+        copy(t1.a, t1.a_single, RA1 * CA1 * 2, a1h, a1l);
+        copy(t1.b, t1.b_single, RB1 * CB1 * 2, b1h, b1l);
         if (K2 != 0) {
-            copy(t2.ia, t2.a_single, RA2 * CA2 * 2, a2h, a2l);
-            copy(t2.ib, t2.b_single, RB2 * CB2 * 2, b2h, b2l);
+            copy(t2.a, t2.a_single, RA2 * CA2 * 2, a2h, a2l);
+            copy(t2.b, t2.b_single, RB2 * CB2 * 2, b2h, b2l);
         }
     }
-    {
-        Stage<RA1, CA1> sa1;
-        Stage<RB1, CB1> sb1;
-        if (!t1.ia) sa1.load(t1.a, t1.lda);
-        if (!t1.ib) sb1.load(t1.b, t1.ldb);
-        if constexpr (K2 != 0) {
-            Stage<RA2, CA2> sa2;
-            Stage<RB2, CB2> sb2;
-            if (!t2.ia) sa2.load(t2.a, t2.lda);
-            if (!t2.ib) sb2.load(t2.b, t2.ldb);
-            if (!t2.ia) sa2.store(a2h, a2l, CSA2, nullptr, t2.s, t2.sa);
-            if (!t2.ib) sb2.store(b2h, b2l, CSB2, TB2 ? nullptr : t2.b_rows, 1.f, t2.sb);
-        }
-        if (!t1.ia) sa1.store(a1h, a1l, CSA1, nullptr, t1.s, t1.sa);
-        if (!t1.ib) sb1.store(b1h, b1l, CSB1, TB1 ? nullptr : t1.b_rows, 1.f, t1.sb);
-    }
-    fence_async_smem();
-    if (t1.sa || t1.sb || (K2 != 0 && (t2.sa || t2.sb))) fence_async_global();
-    __syncthreads();
+    __syncthreads();   // every thread reads the phase of this product's barrier after the previous one's update
     fence_after();
     const uint32_t ph = s_tc_phase, tmem = s_tc_tmem, bar = smem_u32(&s_tc_bar);
     if (tid == 0) {
-        bool ld_ok = true;
-        if (any_img) {
-            ld_ok = mbar_wait(smem_u32(&s_tc_ld), s_tc_ldph);
-            s_tc_ldph ^= 1u;
-            if (!ld_ok) s_tc_fail = 1;
-        }
+        const bool ld_ok = mbar_wait(smem_u32(&s_tc_ld), s_tc_ldph);
+        s_tc_ldph ^= 1u;
+        if (!ld_ok) s_tc_fail = 1;
         bool first = true;
         // the split terms of one A B pair: hi hi, hi lo (unless B is single), lo hi (unless A is single)
         auto issue = [&](int K, bool ta, bool tb, uint32_t ah_, uint32_t al_, uint32_t bh_, uint32_t bl_, uint32_t csa,
@@ -339,11 +249,11 @@ __device__ void product(const Term t1, const Term t2, const Out o)
             }
         };
         if (ld_ok) {
-            issue(K1, TA1, TB1, smem_u32(a1h), smem_u32(a1l), smem_u32(b1h), smem_u32(b1l), CSA1, CSB1, t1.ia && t1.a_single,
-                  t1.ib && t1.b_single);
+            issue(K1, TA1, TB1, smem_u32(a1h), smem_u32(a1l), smem_u32(b1h), smem_u32(b1l), CSA1, CSB1, t1.a_single,
+                  t1.b_single);
             if constexpr (K2 != 0)
                 issue(K2, TA2, TB2, smem_u32(a2h), smem_u32(a2l), smem_u32(b2h), smem_u32(b2l), CSA2, CSB2,
-                      t2.ia && t2.a_single, t2.ib && t2.b_single);
+                      t2.a_single, t2.b_single);
         }
         commit(bar);   // (with nothing issued, it arrives at once: the readers see the failure flag)
     }
@@ -586,20 +496,20 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         unsigned char *const dui = sci + 4 * S_DUI, *const dwi = sci + 4 * S_DWI, *const dti = sci + 4 * S_DTI;
         unsigned char *const t64i = sci + 4 * S_T64I, *const dmi = sci + 4 * S_DMI;
         float *dKh = sc + S_DKH, *dQt = sc + S_DQT, *dM = sc + S_DM, *dKt = sc + S_DKT;
-        const Term none = term(nullptr, 0, nullptr, 0);
+        const Term none = term(nullptr, nullptr);
         __syncthreads();
         // U = Ut - W X (W from the image of W^T as it lies)
-        product<64, VD, KD, true, true>(img_b(img_a(none, im + RIMG_W), xt), none,
+        product<64, VD, KD, true, true>(term(im + RIMG_W, xt), none,
                                         out_img(out(nullptr, 0, -1.f, tm + BT_UT, VD), ui));
         // dQK = lower(dO U^T)
-        product<64, 64, VD, false, true, 0, false, false, 1>(img_b(img_a(none, im + RIMG_DO, true), ui), none,
+        product<64, 64, VD, false, true, 0, false, false, 1>(term(im + RIMG_DO, ui, true, false), none,
                                                              out_img(out(nullptr, 0), dqki));
         // dU = Kh DG + QK^T dO
-        product<64, VD, KD, false, true, 64, true, false>(img_b(img_a(none, im + RIMG_KH), dgt),
-                                                          img_b(img_a(none, im + RIMG_QK), im + RIMG_DO, true),
+        product<64, VD, KD, false, true, 64, true, false>(term(im + RIMG_KH, dgt),
+                                                          term(im + RIMG_QK, im + RIMG_DO, false, true),
                                                           out_img(out(nullptr, 0), dui));
         // dKh = U DG^T + dQK^T Qt
-        product<64, KD, VD, false, false, 64, true, false>(img_b(img_a(none, ui), dgt), img_b(img_a(none, dqki), im + RIMG_QT),
+        product<64, KD, VD, false, false, 64, true, false>(term(ui, dgt), term(dqki, im + RIMG_QT),
                                                            out(dKh, KD));
         // dGamma_C[k] = gc[k] sum_v G[k][v] (X + Kh^T U)[k][v] = sum_v DG[k][v] X'[k][v] / gc[k], with
         // X' = Diag(gc) (X + Kh^T U) the state after the chunk (images read as hi + lo): each thread takes the 8
@@ -639,25 +549,25 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
             }
         }
         // dQt = dO X^T + dQK Kh
-        product<64, KD, VD, false, false, 64, false, false>(img_b(img_a(none, im + RIMG_DO, true), xt),
-                                                            img_b(img_a(none, dqki), im + RIMG_KH), out(dQt, KD));
+        product<64, KD, VD, false, false, 64, false, false>(term(im + RIMG_DO, xt, true, false),
+                                                            term(dqki, im + RIMG_KH), out(dQt, KD));
         // dW = -dU X^T
-        product<64, KD, VD, false, false>(img_b(img_a(none, dui), xt), none, out_img(out(nullptr, 0, -1.f), dwi));
+        product<64, KD, VD, false, false>(term(dui, xt), none, out_img(out(nullptr, 0, -1.f), dwi));
         // dT = dW (beta Kt)^T + dU (beta V)^T
-        product<64, 64, KD, false, true, VD, false, true>(img_b(img_a(none, dwi), bkti),
-                                                          img_b(img_a(none, dui), im + RIMG_BV), out_img(out(nullptr, 0), dti));
+        product<64, 64, KD, false, true, VD, false, true>(term(dwi, bkti),
+                                                          term(dui, im + RIMG_BV), out_img(out(nullptr, 0), dti));
         // d(beta Kt) = T^T dW, d(beta V) = T^T dU
-        product<64, KD, 64, true, false>(img_b(img_a(none, ti), dwi), none,
+        product<64, KD, 64, true, false>(term(ti, dwi), none,
                                          out(sc + S_DBKT, KD));
-        product<64, VD, 64, true, false>(img_b(img_a(none, ti), dui), none, out(sc + S_DBV, VD));
+        product<64, VD, 64, true, false>(term(ti, dui), none, out(sc + S_DBV, VD));
         // dM = strictly_lower(-T^T dT T^T)
-        product<64, 64, 64, true, false>(img_b(img_a(none, ti), dti), none, out_img(out(nullptr, 0), t64i));
-        product<64, 64, 64, false, true, 0, false, false, 2>(img_b(img_a(none, t64i), ti), none,
+        product<64, 64, 64, true, false>(term(ti, dti), none, out_img(out(nullptr, 0), t64i));
+        product<64, 64, 64, false, true, 0, false, false, 2>(term(t64i, ti), none,
                                                              out_img(out(dM, 64, -1.f), dmi));
         // dKt = beta (d(beta Kt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(beta V)
-        product<64, KD, 64, false, false>(img_b(img_a(none, dmi), im + RIMG_KH), none,
+        product<64, KD, 64, false, false>(term(dmi, im + RIMG_KH), none,
                                           out(dKt, KD, 1.f, sc + S_DBKT, KD, nullptr, sc + S_BT));
-        product<64, KD, 64, true, false>(img_b(img_a(none, dmi), bkti), none, out(dKh, KD, 1.f, dKh, KD));
+        product<64, KD, 64, true, false>(term(dmi, bkti), none, out(dKh, KD, 1.f, dKh, KD));
         __syncthreads();
         // The rows' input gradients in one pass.  Each thread holds rows 8 rg .. 8 rg + 7 and columns
         // 4 cq .. 4 cq + 3 (of K, and of V for v and d(beta V); of the 64-wide dM and S rows on lanes cq < 16).
