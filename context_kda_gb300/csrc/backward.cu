@@ -358,11 +358,12 @@ __global__ void __launch_bounds__(BT) bwd_do_images(const int32_t *plan, PlanSig
     }
 }
 
-// 3. The following summaries, per (head, 32-column slice), last segment first:
+// 3. The following summaries, per (head, 16-column slice), last segment first:
 //    G_end[j] = dfinal of the sequence ending at b_{j+1}, if one does; otherwise, with p the
 //    continuing piece that opens segment j+1,
 //    G_end[j] = Qd[j+1] + (P_end(p)^T dfinal[seq] if p ends its sequence, else A[j+1]^T G_end[j+1]).
-constexpr int CMP_SMEM = (KD * KD + KD * 32) * 4;   // the map's matrix and the gradient's column slice
+constexpr int CMP_COLS = 16;                               // gradient columns per CTA
+constexpr int CMP_SMEM = (KD * KD + KD * CMP_COLS) * 4;   // the map's matrix and the gradient's column slice
 
 __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSig sig, int H, const float *A,
                                                   const float *afin, const float *dfinal, const float *Qd,
@@ -371,7 +372,8 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
     extern __shared__ __align__(16) float csm[];
     BWD_PLAN_CHECK();
     const PlanView pv{plan};
-    const int h = blockIdx.x / 4, col0 = (blockIdx.x % 4) * 32;
+    constexpr int NSL = VD / CMP_COLS;   // slices per head
+    const int h = blockIdx.x / NSL, col0 = (blockIdx.x % NSL) * CMP_COLS;
     const int S = pv.S(), N = pv.N(), T = pv.T();
     const int32_t *cu = pv.cu();
     const int tid = threadIdx.x;
@@ -383,8 +385,8 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
             if (cu[s + 1] == b) ends = s;
         if (ends >= 0 || b == T) {
             const float *df = (dfinal && ends >= 0) ? dfinal + (static_cast<size_t>(ends) * H + h) * SQ : nullptr;
-            for (int e = tid; e < KD * 32; e += BT) {
-                const int r = e >> 5, c = col0 + (e & 31);
+            for (int e = tid; e < KD * CMP_COLS; e += BT) {
+                const int r = e / CMP_COLS, c = col0 + e % CMP_COLS;
                 out[r * VD + c] = df ? df[r * VD + c] : 0.f;
             }
             __syncthreads();
@@ -402,30 +404,30 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
             Mt = A + (static_cast<size_t>(j + 1) * H + h) * KD * KD;
             gin = G_end + (static_cast<size_t>(j + 1) * H + h) * SQ;
         }
-        // out[r][c] = qd[r][c] + sum_i Mt[i][r] gin[i][c]  (4 rows x 4 columns per thread), with Mt and this
+        // out[r][c] = qd[r][c] + sum_i Mt[i][r] gin[i][c]  (2 rows x 4 columns per thread), with Mt and this
         // CTA's column slice of gin staged in shared memory first (every 16-byte load of a thread in flight)
-        const int rr = (tid >> 3) * 4, cc = col0 + (tid & 7) * 4;
+        const int rr = (tid >> 2) * 2, cc = col0 + (tid & 3) * 4;
         float *const sM = csm, *const sG = csm + KD * KD;
         if (gin) {
-            float4 mv[16], gv[4];
+            float4 mv[16], gv[2];
 #pragma unroll
             for (int i = 0; i < 16; ++i) mv[i] = ld4(Mt + 4 * (tid + i * BT));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = tid + i * BT;
-                gv[i] = ld4(gin + (e >> 3) * VD + col0 + 4 * (e & 7));
+            for (int i = 0; i < 2; ++i) {
+                const int e = tid + i * BT;   // row e / 4, columns 4 (e % 4) .. + 3 of the slice
+                gv[i] = ld4(gin + (e >> 2) * VD + col0 + 4 * (e & 3));
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) st4(sM + 4 * (tid + i * BT), mv[i]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 const int e = tid + i * BT;
-                st4(sG + (e >> 3) * 32 + 4 * (e & 7), gv[i]);
+                st4(sG + (e >> 2) * CMP_COLS + 4 * (e & 3), gv[i]);
             }
         }
-        float acc[4][4];
+        float acc[2][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < 2; ++a) {
             const float4 q4 = ld4(qd + (rr + a) * VD + cc);
             acc[a][0] = q4.x;
             acc[a][1] = q4.y;
@@ -437,16 +439,17 @@ __global__ void __launch_bounds__(BT, 1) bwd_compose(const int32_t *plan, PlanSi
         if (gin) {
 #pragma unroll 8
             for (int i = 0; i < KD; ++i) {
-                const float4 m4 = ld4(sM + i * KD + rr), x4 = ld4(sG + i * 32 + (cc - col0));
-                const float m[4] = {m4.x, m4.y, m4.z, m4.w}, x[4] = {x4.x, x4.y, x4.z, x4.w};
+                const float2 m2 = *reinterpret_cast<const float2 *>(sM + i * KD + rr);
+                const float4 x4 = ld4(sG + i * CMP_COLS + (cc - col0));
+                const float m[2] = {m2.x, m2.y}, x[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
+                for (int a = 0; a < 2; ++a)
 #pragma unroll
                     for (int bb = 0; bb < 4; ++bb) acc[a][bb] = fmaf(m[a], x[bb], acc[a][bb]);
             }
         }
 #pragma unroll
-        for (int a = 0; a < 4; ++a) st4(out + (rr + a) * VD + cc, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
+        for (int a = 0; a < 2; ++a) st4(out + (rr + a) * VD + cc, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
         __syncthreads();
     }
 }
@@ -693,7 +696,7 @@ cudaError_t launch_backward(const int32_t *plan_host, const int32_t *plan_dev, i
         if (err != cudaSuccess) return err;
     }
     if ((err = set_dynamic_smem(reinterpret_cast<const void *>(bwd_compose), CMP_SMEM)) != cudaSuccess) return err;
-    bwd_compose<<<H * 4, BT, CMP_SMEM, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
+    bwd_compose<<<H * (VD / CMP_COLS), BT, CMP_SMEM, stream>>>(plan_dev, sig, H, A, afin, dfinal, Qd, G_end);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     err = launch_reverse_tc(plan_host, plan_dev, H, true, img, dfinal, G_end, Qd, gs, dh0, stream);
     if (err != cudaSuccess) return err;
