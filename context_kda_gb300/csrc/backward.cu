@@ -50,12 +50,12 @@ constexpr int SQ = KD * VD;                  // a 128 x 128 state
 __device__ int g_bwd_status;
 
 // Per-CTA scratch (floats): the FP32 product results an element-wise step reads (dKh, dQt, dKt, d(beta Kt),
-// d(beta V): 64 x 128; dM: 64 x 64), row vectors (gc, beta, dGamma_C), then bf16 hi/lo images (bytes / 4) of
+// d(beta V), side by side in one 64 x 256 array; dM: 64 x 64), row vectors (gc, beta, dGamma_C), then bf16 hi/lo images (bytes / 4) of
 // the products' results that later products read (U, dQK, dU, dW, dT, T^T dT, dM).  About 0.34 MB: the
 // working areas of all CTAs fit in the L2.
 enum : int {
-    S_DKH = 0, S_DQT = S_DKH + CK, S_DKT = S_DQT + CK, S_DBKT = S_DKT + CK, S_DBV = S_DBKT + CK,
-    S_DM = S_DBV + CK, S_GC = S_DM + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64,
+    S_DKH = 0, S_DQT = S_DKH + CK, S_DKT = S_DQT + CK, S_DBKV = S_DKT + CK,   // [d(beta Kt) | d(beta V)]: 64 x 256
+    S_DM = S_DBKV + 2 * CK, S_GC = S_DM + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64,
     S_IMG = (S_DGC + KD + 255) & ~255,
     S_UI = S_IMG, S_DQKI = S_UI + CK, S_DUI = S_DQKI + CC, S_DWI = S_DUI + CK, S_DTI = S_DWI + CK,
     S_T64I = S_DTI + CC, S_DMI = S_T64I + CC, S_IMG_END = S_DMI + CC,
@@ -106,7 +106,7 @@ __device__ __forceinline__ float warp_sum(float v)
 __shared__ __align__(8) uint64_t s_tc_bar;
 __shared__ __align__(8) uint64_t s_tc_ld;   // a product's operand images landed (bulk copies)
 __shared__ uint32_t s_tc_tmem, s_tc_phase, s_tc_fail, s_tc_ldph;
-constexpr uint32_t TC_COLS = 128;
+constexpr uint32_t TC_COLS = 256;
 
 __device__ void tc_begin()
 {
@@ -144,15 +144,16 @@ __device__ __forceinline__ unsigned char *tc_tiles()
 // operand as it lies (R rows of its contiguous index, chunk stride R * 16, lo R * C * 2 bytes after hi; a
 // single image holds only hi, the operand being exact in bf16, and the products with its lo part are
 // skipped), brought in by bulk copies.  A(m, k) is the image's [k][m] when the product transposes A (rows k),
-// else [m][k]; B(k, n) likewise [n][k] or [k][n].
+// else [m][k]; B(k, n) likewise [n][k] or [k][n].  b2, when set (untransposed B only), is a second image whose
+// columns follow b's: B = [b | b2].
 struct Term {
-    const unsigned char *a, *b;
+    const unsigned char *a, *b, *b2;
     bool a_single, b_single;
 };
 __device__ __forceinline__ Term term(const unsigned char *a, const unsigned char *b, bool a_single = false,
-                                     bool b_single = false)
+                                     bool b_single = false, const unsigned char *b2 = nullptr)
 {
-    return Term{a, b, a_single, b_single};
+    return Term{a, b, b2, a_single, b_single};
 }
 
 // The output of a product: C[m][n] = out_rows[m] * (alpha * sum of the terms + in_rows[m] * cin[m][n]),
@@ -179,7 +180,8 @@ __device__ __forceinline__ Out out_img(Out o, unsigned char *img)
     return o;
 }
 
-// An M x N product of one or two terms (K1- and K2-long sums; K2 = 0: one term; M, N, K in {64, 128})
+// An M x N product of one or two terms (K1- and K2-long sums; K2 = 0: one term; M, K in {64, 128}, N in
+// {64, 128}, or 256 for a one-term product with no accumulated input)
 // by all threads of the CTA.  Every operand is an image of its bf16 hi/lo split as it lies (rows of its
 // contiguous index, chunk stride: its rows x 16), brought into the no-swizzle canonical tiles by bulk copies
 // and read by the tensor core K-major or MN-major accordingly, so nothing is transposed on the way; each
@@ -190,8 +192,8 @@ __device__ __forceinline__ Out out_img(Out o, unsigned char *img)
 template <int M, int N, int K1, bool TA1, bool TB1, int K2 = 0, bool TA2 = false, bool TB2 = false, int MASK = 0>
 __device__ void product(const Term t1, const Term t2, const Out o)
 {
-    static_assert((M == 64 || M == 128) && (N == 64 || N == 128) && (K1 == 64 || K1 == 128) &&
-                      (K2 == 0 || K2 == 64 || K2 == 128), "shapes");
+    static_assert((M == 64 || M == 128) && (N == 64 || N == 128 || (N == 256 && K2 == 0 && !TB1)) &&
+                      (K1 == 64 || K1 == 128) && (K2 == 0 || K2 == 64 || K2 == 128), "shapes");
     if (s_tc_fail) return;   // uniform: written before the previous product's closing barrier
     const int tid = threadIdx.x;
     constexpr int K2E = K2 ? K2 : 64;   // shapes of the (unused when K2 = 0) second term
@@ -218,7 +220,12 @@ __device__ void product(const Term t1, const Term t2, const Out o)
             if (!single) bulk_g2s(smem_u32(lo), img + nbytes, nbytes, ld);
         };
         copy(t1.a, t1.a_single, RA1 * CA1 * 2, a1h, a1l);
-        copy(t1.b, t1.b_single, RB1 * CB1 * 2, b1h, b1l);
+        if (t1.b2) {   // B = [b | b2]: each image fills half of the tile's column chunks
+            copy(t1.b, t1.b_single, RB1 * CB1, b1h, b1l);
+            copy(t1.b2, t1.b_single, RB1 * CB1, b1h + RB1 * CB1, b1l + RB1 * CB1);
+        } else {
+            copy(t1.b, t1.b_single, RB1 * CB1 * 2, b1h, b1l);
+        }
         if (K2 != 0) {
             copy(t2.a, t2.a_single, RA2 * CA2 * 2, a2h, a2l);
             copy(t2.b, t2.b_single, RB2 * CB2 * 2, b2h, b2l);
@@ -262,8 +269,9 @@ __device__ void product(const Term t1, const Term t2, const Out o)
     const int warp = tid >> 5, quad = warp & 3, hw = warp >> 2;
     const int m = quad * 32 + (tid & 31), n0 = hw * (N / 2);
     const bool live = quad * 32 < M;
-    float4 old[N / 8];
-    {
+    constexpr int NOLD = N <= 128 ? N / 8 : 1;   // (N = 256: no accumulated input)
+    float4 old[NOLD];
+    if constexpr (N <= 128) {
         const float f = (o.cin && live) ? (o.in_rows ? o.in_rows[m] : 1.f) : 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < N / 8; ++q4)
@@ -283,8 +291,11 @@ __device__ void product(const Term t1, const Term t2, const Out o)
                 float r[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float4 o4 = old[(j0 + 8 * q8 + e) / 4];
-                    const float ov = (e & 3) == 0 ? o4.x : (e & 3) == 1 ? o4.y : (e & 3) == 2 ? o4.z : o4.w;
+                    float ov = 0.f;
+                    if constexpr (N <= 128) {
+                        const float4 o4 = old[(j0 + 8 * q8 + e) / 4];
+                        ov = (e & 3) == 0 ? o4.x : (e & 3) == 1 ? o4.y : (e & 3) == 2 ? o4.z : o4.w;
+                    }
                     r[e] = fo * (o.alpha * d[8 * q8 + e] + ov);
                     if constexpr (MASK != 0) {
                         const int n = n0 + j0 + 8 * q8 + e;
@@ -560,16 +571,15 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         product<64, 64, KD, false, true, VD, false, true>(term(dwi, bkti),
                                                           term(dui, im + RIMG_BV), out_img(out(nullptr, 0), dti));
         // d(beta Kt) = T^T dW, d(beta V) = T^T dU
-        product<64, KD, 64, true, false>(term(ti, dwi), none,
-                                         out(sc + S_DBKT, KD));
-        product<64, VD, 64, true, false>(term(ti, dui), none, out(sc + S_DBV, VD));
+        // (one product: B = [dW | dU], N = 256)
+        product<64, KD + VD, 64, true, false>(term(ti, dwi, false, false, dui), none, out(sc + S_DBKV, KD + VD));
         // dM = strictly_lower(-T^T dT T^T)
         product<64, 64, 64, true, false>(term(ti, dti), none, out_img(out(nullptr, 0), t64i));
         product<64, 64, 64, false, true, 0, false, false, 2>(term(t64i, ti), none,
                                                              out_img(out(dM, 64, -1.f), dmi));
         // dKt = beta (d(beta Kt) + dM Kh);  dKh += dM^T (beta Kt);  dv = beta d(beta V)
         product<64, KD, 64, false, false>(term(dmi, im + RIMG_KH), none,
-                                          out(dKt, KD, 1.f, sc + S_DBKT, KD, nullptr, sc + S_BT));
+                                          out(dKt, KD, 1.f, sc + S_DBKV, KD + VD, nullptr, sc + S_BT));
         product<64, KD, 64, true, false>(term(dmi, bkti), none, out(dKh, KD, 1.f, dKh, KD));
         __syncthreads();
         // The rows' input gradients in one pass.  Each thread holds rows 8 rg .. 8 rg + 7 and columns
@@ -620,7 +630,7 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
                 const uint2 qw = live ? *reinterpret_cast<const uint2 *>(q + gi) : make_uint2(0u, 0u);
                 const uint2 vw = live ? *reinterpret_cast<const uint2 *>(v + gi) : make_uint2(0u, 0u);
                 const float4 dkt = ld4(dKt + e), dkh = ld4(dKh + e), dqt = ld4(dQt + e);
-                const float4 dbk = ld4(sc + S_DBKT + e), dbv = ld4(sc + S_DBV + e);
+                const float4 dbk = ld4(sc + S_DBKV + r * (KD + VD) + 4 * cq), dbv = ld4(sc + S_DBKV + r * (KD + VD) + KD + 4 * cq);
                 float4 ms = make_float4(0.f, 0.f, 0.f, 0.f), sv = ms;
                 if (cq < 16) {
                     ms = ld4(dM + r * 64 + 4 * cq);
