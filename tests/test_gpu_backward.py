@@ -112,3 +112,14 @@ def test_backward_headline_sampled_heads():
         den = max(float(np.linalg.norm(ref["dg"][:, h])), float(terms), 1e-30)
         assert float(np.linalg.norm(got["dg"][:, h] - ref["dg"][:, h])) / den <= GRAD_TOL, f"head {h} dg"
         assert grad_rel_err(got["dh0"][:, h:h + 1], ref["dh0"][:, h:h + 1]) <= GRAD_TOL, f"head {h} dh0"
+
+
+def test_backward_is_deterministic():
+    """No atomics and a fixed order of every sum: three calls on the same inputs give bitwise equal
+    gradients."""
+    inp = make_inputs([700, 300, 130], heads=2, segments=5, h0_std=0.1, seed=53, g_lo=-0.2)
+    do, dfinal = draw_output_grads(inp, seed=8)
+    runs = [gpu_backward(inp, do, dfinal) for _ in range(3)]
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        for other in runs[1:]:
+            assert np.array_equal(runs[0][name], other[name]), name
