@@ -15,25 +15,28 @@
 //
 // Steps (after the forward's own preparation, state pass and composition, which give S_in, the
 // segment transitions A and the final-state transitions of continuing pieces):
-//  0. every (chunk, head) in parallel: the chunk's FP32 terms (Ut, S, T) for the gradient pass and the
-//     bf16 operand images (Kh, Qt, QK, W, Dc) of the reverse chains and the gradient pass, which the
-//     forward's preparation writes in its backward mode (the caller launches it), and dO's image;
+//  0. every (chunk, head) in parallel: the chunk's FP32 terms (Ut, S) for the gradient pass and the bf16
+//     operand images (Kh, Qt, QK, W, Dc, T, Diag(beta) Kt, Diag(beta) V) of the reverse chains and the
+//     gradient pass, which the forward's preparation writes in its backward mode (the caller launches
+//     it), and dO's image;
 //  1. every piece from its true incoming state (h0, or S_in of its segment), recording each chunk's
-//     start state X_c: the forward's state pass in its output mode (the caller launches it);
+//     start state X_c as the image of X_c^T: the forward's state pass in its output mode (the caller
+//     launches it);
 //  2. (reverse.cu) every piece that continues a sequence, backwards from a zero end gradient: the gradient of its
 //     incoming state through its own outputs, Qd (the qhat do^T sum of the pages' summaries);
 //  3. the following summaries, last segment first: the gradient of the state crossing the end of
 //     segment j is dfinal of a sequence that ends there, or Qd[j+1] plus the transposed map of the
 //     continuing piece of segment j+1 (A[j+1]^T, or P_end^T of a piece that ends its sequence
 //     there, on dfinal) applied to the gradient at that piece's end;
-//  4. (reverse.cu) every piece backwards from its true end gradient, recording each chunk's end gradient G_c and
-//     giving dh0 at a sequence start;
-//  5. every (chunk, head) in parallel: dq, dk, dv, dg, dbeta from (X_c, G_c, dO).
+//  4. (reverse.cu) every piece backwards from its true end gradient, recording each chunk's DG_c = Dc G_c
+//     (G_c its end gradient) as the image of DG_c^T and giving dh0 at a sequence start;
+//  5. every (chunk, head) in parallel: dq, dk, dv, dg, dbeta from (X_c, DG_c, dO).
 //
-// The gradient pass here keeps a chunk's matrices in FP32 in a private scratch area in global
-// memory and runs every product on the tensor cores (both operands staged in shared memory as bf16 hi/lo
-// pairs, a three-term split accumulated in FP32 in TMEM), which keeps every step a literal transcription
-// of the formulas above.
+// The gradient pass here runs every product on the tensor cores, its operands bf16 hi/lo images brought
+// into shared memory by bulk copies (a three-term split accumulated in FP32 in TMEM), and keeps the
+// results that later steps read in a private scratch area in global memory (FP32 where an element-wise
+// step reads them, as images where a product does), which keeps every step a literal transcription of
+// the formulas above.
 #include "kda_internal.cuh"
 #include "tc.cuh"
 
@@ -49,10 +52,10 @@ constexpr int SQ = KD * VD;                  // a 128 x 128 state
 
 __device__ int g_bwd_status;
 
-// Per-CTA scratch (floats): the FP32 product results an element-wise step reads (dKh, dQt, dKt, d(beta Kt),
-// d(beta V), side by side in one 64 x 256 array; dM: 64 x 64), row vectors (gc, beta, dGamma_C), then bf16 hi/lo images (bytes / 4) of
-// the products' results that later products read (U, dQK, dU, dW, dT, T^T dT, dM).  About 0.34 MB: the
-// working areas of all CTAs fit in the L2.
+// Per-CTA scratch (floats): the FP32 product results an element-wise step reads (dKh, dQt, dKt: 64 x 128;
+// d(beta Kt) and d(beta V) side by side in one 64 x 256 array; dM: 64 x 64), row vectors (gc, beta,
+// dGamma_C), then bf16 hi/lo images (bytes / 4) of the products' results that later products read (U, dQK,
+// dU, dW, dT, T^T dT, dM).  About 0.34 MB: the working areas of all CTAs fit in the L2.
 enum : int {
     S_DKH = 0, S_DQT = S_DKH + CK, S_DKT = S_DQT + CK, S_DBKV = S_DKT + CK,   // [d(beta Kt) | d(beta V)]: 64 x 256
     S_DM = S_DBKV + 2 * CK, S_GC = S_DM + CC, S_BT = S_GC + KD, S_DGC = S_BT + 64,
@@ -487,11 +490,10 @@ __global__ void __launch_bounds__(BT, 1) bwd_grads(const int32_t *plan, PlanSig 
         const unsigned char *im = img + static_cast<size_t>(unit) * RIMG_UNIT;
         chunk_rows(sc, t0, L, h, H, beta, im);
         const float *tm = terms + static_cast<size_t>(unit) * BT_FLOATS;   // Ut, S
-        // Every operand comes as a bf16 hi/lo image by bulk copies: X^T and DG^T as the chains recorded them;
-        // Kh, QK, Qt, W (as W^T), dO, T, Diag(beta) Kt and Diag(beta) V as the chunk's operand images; and every
+        // Every operand comes as a bf16 hi/lo image by bulk copies: X (the chunk's start state) and DG = Dc G
+        // (G its end-state gradient) as the images of X^T and DG^T the chains recorded (rows v, cols k); Kh,
+        // QK, Qt, W (as W^T), dO, T, Diag(beta) Kt and Diag(beta) V as the chunk's operand images; and every
         // product whose result feeds another leaves its result as an image
-        // X (the chunk's start state) and DG = Dc G (G its end-state gradient) as the chains recorded them:
-        // the bf16 hi/lo images of X^T and DG^T as they lie (rows v, cols k)
         const unsigned char *const xt = reinterpret_cast<const unsigned char *>(xs + (static_cast<size_t>(h) * n_chunks + c) * SQ);
         const unsigned char *const dgt = reinterpret_cast<const unsigned char *>(gs + (static_cast<size_t>(h) * n_chunks + c) * SQ);
         // the state after the chunk: the next chunk's recorded image, or the piece's end state (FP32 K x V: the
