@@ -579,8 +579,9 @@ cudaError_t launch_two_pass(const int32_t *plan_host, const int32_t *plan_dev, i
 }
 
 // Every piece's state chain from its true incoming state (h0, or S_in of its segment), recording the
-// start state of each chunk into xs[h][chunk] (fp32 K x V); the outputs and final states go to o and
-// final_state.  The packages and S_in come from the kernels before it on the stream.
+// start state X of each chunk into xs[h][chunk] as the bf16 hi/lo image of X^T (K x V x 4 bytes); the
+// outputs and final states go to o and final_state.  The packages and S_in come from the kernels before
+// it on the stream.
 cudaError_t launch_state_record(const int32_t *plan_host, const int32_t *plan_dev, int H, const float *h0,
                                 const float *S_in, const unsigned char *pkg, uint16_t *o, float *final_state,
                                 float *xs, cudaStream_t stream)
