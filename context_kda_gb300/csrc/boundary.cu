@@ -23,10 +23,11 @@
 //   epilogue whenever they share S_in and their qhat tile comes by TMA, so the epilogue of one unit
 //   overlaps the products of the next.  A final-state transition (fp32) is split into hi/lo by the
 //   threads and takes the third product too.
-// - A full 128-row output tile moves through one of two shared-memory buffers by tiled TMA: loaded a
-//   unit ahead, updated in place by the epilogue, written back with one TMA store.  Ragged tail tiles
-//   and final states are read and written by the threads directly, so nothing outside a record is
-//   ever stored.
+// - A full 128-row tile's correction D is rounded to bf16 into one of two shared-memory buffers and
+//   added into the outputs in memory by a tiled TMA reduce-add (bf16): the outputs never pass through
+//   the SM, so a tile costs the tensor-copy unit 512 rows of 128 bytes (qhat in, D out) instead of 768
+//   (the copy unit's row rate bounds this kernel).  Ragged tail tiles and final states are read and
+//   written by the threads directly (o + D rounded once), so nothing outside a record is ever touched.
 #include <algorithm>
 #include <vector>
 
@@ -44,7 +45,7 @@ constexpr uint32_t TILE_B = 32768;
 constexpr uint32_t BOX = 16384;            // 128 rows x 128 bytes, 128-byte swizzle
 constexpr uint32_t OFF_B = 0;              // S_in^T hi | lo
 constexpr uint32_t OFF_A = 2 * TILE_B;     // three qhat tiles (ring), two boxes each
-constexpr uint32_t OFF_OB = OFF_A + 6 * BOX;   // two bf16 output tiles, two boxes each
+constexpr uint32_t OFF_OB = OFF_A + 6 * BOX;   // two bf16 correction tiles, two boxes each
 constexpr uint32_t SMEM_BYTES = OFF_OB + 4 * BOX;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base to 1024 bytes
 static_assert(OFF_A % 1024 == 0 && OFF_OB % 1024 == 0, "swizzled buffers");
@@ -61,6 +62,15 @@ struct Runs {
 };
 
 __device__ int g_boundary_status;
+
+// D (bf16, a 64-column box in the 128-byte swizzled layout of the map) added element-wise into the
+// outputs at (x, y, z) of the map by the memory system; completes in this thread's bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, int x, int y, int z, uint32_t src_smem)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(tmap), "r"(x), "r"(y), "r"(z), "r"(src_smem)
+                 : "memory");
+}
 
 // Position in the unit order: head h, continuing record rec, unit within the record.  A record's
 // units are its 128-row qhat tiles, then, when its piece ends the sequence, the final-state
@@ -121,7 +131,6 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar[2];   // products of a unit done, per TMEM accumulator
     __shared__ __align__(8) uint64_t s_abar[3];   // qhat tile landed, per ring slot
-    __shared__ __align__(8) uint64_t s_obar[2];   // output tile landed, per buffer
     __shared__ uint32_t s_tmem;
     if (!plan_matches(plan, sig)) {   // not the plan the launch was sized from: touch nothing
         if (threadIdx.x == 0) record_status(&g_boundary_status, KDA_ERR_INVALID_ARG);
@@ -137,10 +146,7 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
     unsigned char *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&s_mbar[i]), 1);
-            mbar_init(smem_u32(&s_obar[i]), 1);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s_mbar[i]), 1);
         for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&s_abar[i]), 1);
     }
     if (warp == 0) tmem_alloc(smem_u32(&s_tmem), TM_COLS);
@@ -148,14 +154,14 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
     __syncthreads();
     fence_after();
     const uint32_t tbase = s_tmem;
-    uint32_t mph = 0, aph = 0, oph = 0;   // bit i: parity of the next wait on barrier i of each kind
+    uint32_t mph = 0, aph = 0;   // bit i: parity of the next wait on barrier i of each kind
     bool ok = true;
-    bool a_pend[3] = {false, false, false}, o_pend[2] = {false, false};   // thread 0's copies in flight
+    bool a_pend[3] = {false, false, false};   // thread 0's copies in flight
     uint32_t m_pend = 0;   // thread 0: bit t, products issued into accumulator t and not yet waited for
 
     // a continuing unit's qhat tile arrives by TMA (when the map exists)
     auto via_tma = [&](const Rec &r) { return r.seq < 0 && has_tq != 0; };
-    // a unit whose output tile goes through a buffer: 128 continuing tokens
+    // a unit whose correction goes out by TMA reduce-add: 128 continuing tokens
     auto tiled = [&](const Rec &r) { return r.seq < 0 && r.rows == TR; };
     auto fetch_q = [&](const Rec &r, int sl) {   // thread 0
         const uint32_t bar = smem_u32(&s_abar[sl]);
@@ -164,14 +170,6 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
         tma_load_3d(sbase + OFF_A + sl * 2 * BOX, &tm_q, 0, 0, row, bar);
         tma_load_3d(sbase + OFF_A + sl * 2 * BOX + BOX, &tm_q, 64, 0, row, bar);
         a_pend[sl] = true;
-    };
-    auto fetch_o = [&](const Rec &r, int h, int t) {   // thread 0
-        const uint32_t bar = smem_u32(&s_obar[t]);
-        mbar_arrive_expect_tx(bar, 2 * BOX);
-        const int z = r.tok;
-        tma_load_3d(sbase + OFF_OB + t * 2 * BOX, &tm_o, 0, h, z, bar);
-        tma_load_3d(sbase + OFF_OB + t * 2 * BOX + BOX, &tm_o, 64, h, z, bar);
-        o_pend[t] = true;
     };
     // a unit's products into accumulator t (thread 0): qhat in ring slot sl, or a transition with its
     // hi part in slot sl and its lo part in output buffer t
@@ -197,17 +195,14 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
         m_pend |= 1u << t;
     };
 
-    // Units n .. n + 3 of the run (cursor and record; valid while inside the run).  qhat and the local
-    // outputs come from the state pass, which completed before the composition (this kernel's
-    // prerequisite) passed its own wait and let this kernel's CTAs start: each of the first tiles is
-    // requested as soon as its unit's record is known, while the composition still runs; S_in, the
-    // composition's result, only after the wait.
+    // Units n .. n + 3 of the run (cursor and record; valid while inside the run).  qhat comes from
+    // the state pass, which completed before the composition (this kernel's prerequisite) passed its
+    // own wait and let this kernel's CTAs start: each of the first tiles is requested as soon as its
+    // unit's record is known, while the composition still runs; S_in, the composition's result, only
+    // after the wait.  The local outputs, also the state pass's, are only read and written after it.
     Cursor c0{run.x, run.y, run.z};
     Rec r0 = rec_info(pv, H, c0.h, c0.rec, c0.tile);
-    if (tid == 0) {
-        if (via_tma(r0)) fetch_q(r0, 0);
-        if (tiled(r0)) fetch_o(r0, c0.h, 0);
-    }
+    if (tid == 0 && via_tma(r0)) fetch_q(r0, 0);
     Cursor c1 = c0, c2, c3;
     Rec r1 = r0, r2 = r0, r3 = r0;
     if (n_run > 1) {
@@ -298,19 +293,13 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
             if (tid == 0) issue_mma(r0, sl, t);
         }
         // the next unit: its products now when they need nothing from the threads (same S_in, qhat
-        // tile by TMA), and its output tile once the store from that buffer (unit n - 1) has read it
+        // tile by TMA)
         const bool more1 = n + 1 < n_run;
         const bool early = more1 && via_tma(r1) && c1.h == key_h && r1.seg == key_seg;
-        if (tid == 0) {
-            if (early) issue_mma(r1, sl1, t ^ 1);
-            if (more1 && tiled(r1)) {
-                bulk_wait_read_all();
-                fetch_o(r1, c1.h, t ^ 1);
-            }
-        }
+        if (tid == 0 && early) issue_mma(r1, sl1, t ^ 1);
 
         // epilogue of unit n: fetch this thread's destination row piece while the tensor core works
-        // (units whose output tile is not in a buffer)
+        // (units whose correction is not added by the copy unit)
         const bool tl_unit = tiled(r0);
         const int r = quad * 32 + lane;
         const bool live = r < rows && !tl_unit;
@@ -351,22 +340,14 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
                 d[32 + j] = d1[j];
             }
         }
-        if (tl_unit) {   // output tile in buffer t: update in place (row r, this half's box)
-            ok &= mbar_wait(smem_u32(&s_obar[t]), (oph >> t) & 1u);
-            oph ^= 1u << t;
-            if (tid == 0) o_pend[t] = false;
+        if (tl_unit) {   // D as bf16 into buffer t (row r, this half's box), free since the unit before last
             unsigned char *box = smem + OFF_OB + t * 2 * BOX + hw * BOX;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                uint4 *p = reinterpret_cast<uint4 *>(box + sw128(r, m));
-                const uint4 w4 = *p;
-                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
                 uint32_t nw[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    nw[q] = bf16x2_bits(__uint_as_float(ww[q] << 16) + d[8 * m + 2 * q],
-                                        __uint_as_float(ww[q] & 0xFFFF0000u) + d[8 * m + 2 * q + 1]);
-                *p = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+                for (int q = 0; q < 4; ++q) nw[q] = bf16x2_bits(d[8 * m + 2 * q], d[8 * m + 2 * q + 1]);
+                *reinterpret_cast<uint4 *>(box + sw128(r, m)) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
             }
             fence_async_smem();
         }
@@ -389,12 +370,14 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
                                           fw[m].w + d[4 * m + 3]);
             }
         }
+        // the previous unit's reduce has read its buffer, which the next unit fills
+        if (tid == 0) bulk_wait_read_all();
         fence_before();
         if (!__syncthreads_and(ok)) break;
-        if (tid == 0 && tl_unit) {   // write the tile back; its buffer is refilled two units on
+        if (tid == 0 && tl_unit) {   // o += D for the tile's 128 tokens of head h, in memory
             const int z = r0.tok;
-            tma_store_3d(&tm_o, 0, c0.h, z, sbase + OFF_OB + t * 2 * BOX);
-            tma_store_3d(&tm_o, 64, c0.h, z, sbase + OFF_OB + t * 2 * BOX + BOX);
+            tma_reduce_add_3d(&tm_o, 0, c0.h, z, sbase + OFF_OB + t * 2 * BOX);
+            tma_reduce_add_3d(&tm_o, 64, c0.h, z, sbase + OFF_OB + t * 2 * BOX + BOX);
             bulk_commit_group();
         }
         issued = early;
@@ -409,17 +392,15 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
             r3 = rec_info(pv, H, c3.h, c3.rec, c3.tile);
         }
     }
-    if (tid == 0) bulk_wait_all();   // output tiles stored before the CTA exits
+    if (tid == 0) bulk_wait_all();   // corrections added before the CTA exits
     if (!__syncthreads_and(ok)) {
         // a wait gave up: record it, and let any copy or product still in flight land (bounded waits)
         if (tid == 0) {
             record_status(&g_boundary_status, KDA_ERR_TIMEOUT);
             for (int i = 0; i < 3; ++i)
                 if (a_pend[i]) mbar_wait(smem_u32(&s_abar[i]), (aph >> i) & 1u);
-            for (int i = 0; i < 2; ++i) {
-                if (o_pend[i]) mbar_wait(smem_u32(&s_obar[i]), (oph >> i) & 1u);
+            for (int i = 0; i < 2; ++i)
                 if ((m_pend >> i) & 1u) mbar_wait(smem_u32(&s_mbar[i]), (mph >> i) & 1u);
-            }
         }
         __syncthreads();
     }
