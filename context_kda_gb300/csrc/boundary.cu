@@ -16,8 +16,10 @@
 // tile's bytes through the threads and takes three products, and each new S_in is split once more.
 // - S_in[j] is read straight into registers and split into a bf16 hi/lo operand only when the run
 //   reaches a new (head, segment).
-// - A qhat tile (bf16) lands by tiled TMA (two 64-column boxes, 128-byte swizzle) directly in the
-//   layout the tensor core reads, in a ring of three buffers requested three units ahead.
+// - A qhat tile (bf16) lands by two plain bulk copies directly in the layout the tensor core reads
+//   (two 64-column boxes, 128-byte swizzle): the state pass wrote it as that image, box b of a tile of
+//   R rows holding row r at (b R + r) 128 bytes from the tile's start.  A ring of three buffers,
+//   requested three units ahead.
 // - D = Qhat S_in is formed on the tcgen05 tensor cores (M = N = K = 128; qhat * S hi + qhat * S lo,
 //   FP32 in one of two TMEM accumulators).  The next unit's products are issued before this unit's
 //   epilogue whenever they share S_in and their qhat tile comes by TMA, so the epilogue of one unit
@@ -125,8 +127,7 @@ __device__ __forceinline__ void advance(Cursor &c, const Rec &r, int n_cont)
 __global__ void __launch_bounds__(256, 1)
 boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_constant__ Runs runs,
             const float *__restrict__ S_in, const uint16_t *__restrict__ qhat, const float *__restrict__ afin,
-            uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o,
-            const __grid_constant__ CUtensorMap tm_q, int has_tq)
+            uint16_t *__restrict__ o, float *__restrict__ final_state, const __grid_constant__ CUtensorMap tm_o)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar[2];   // products of a unit done, per TMEM accumulator
@@ -159,22 +160,22 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
     bool a_pend[3] = {false, false, false};   // thread 0's copies in flight
     uint32_t m_pend = 0;   // thread 0: bit t, products issued into accumulator t and not yet waited for
 
-    // a continuing unit's qhat tile arrives by TMA (when the map exists)
-    auto via_tma = [&](const Rec &r) { return r.seq < 0 && has_tq != 0; };
+    // a continuing unit's qhat tile arrives by bulk copy
+    auto by_copy = [&](const Rec &r) { return r.seq < 0; };
     // a unit whose correction goes out by TMA reduce-add: 128 continuing tokens
     auto tiled = [&](const Rec &r) { return r.seq < 0 && r.rows == TR; };
-    auto fetch_q = [&](const Rec &r, int sl) {   // thread 0
-        const uint32_t bar = smem_u32(&s_abar[sl]);
-        mbar_arrive_expect_tx(bar, 2 * BOX);
-        const int row = r.qrow;
-        tma_load_3d(sbase + OFF_A + sl * 2 * BOX, &tm_q, 0, 0, row, bar);
-        tma_load_3d(sbase + OFF_A + sl * 2 * BOX + BOX, &tm_q, 64, 0, row, bar);
+    auto fetch_q = [&](const Rec &r, int sl) {   // thread 0: the tile's two box images, r.rows rows each
+        const uint32_t bar = smem_u32(&s_abar[sl]), bytes = static_cast<uint32_t>(r.rows) * 128u;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(qhat + r.src);
+        bulk_g2s(sbase + OFF_A + sl * 2 * BOX, src, bytes, bar);
+        bulk_g2s(sbase + OFF_A + sl * 2 * BOX + BOX, src + bytes, bytes, bar);
         a_pend[sl] = true;
     };
     // a unit's products into accumulator t (thread 0): qhat in ring slot sl, or a transition with its
     // hi part in slot sl and its lo part in output buffer t
     auto issue_mma = [&](const Rec &r, int sl, int t) {
-        if (via_tma(r)) {
+        if (by_copy(r)) {
             ok &= mbar_wait(smem_u32(&s_abar[sl]), (aph >> sl) & 1u);
             aph ^= 1u << sl;
             a_pend[sl] = false;
@@ -202,19 +203,19 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
     // after the wait.  The local outputs, also the state pass's, are only read and written after it.
     Cursor c0{run.x, run.y, run.z};
     Rec r0 = rec_info(pv, H, c0.h, c0.rec, c0.tile);
-    if (tid == 0 && via_tma(r0)) fetch_q(r0, 0);
+    if (tid == 0 && by_copy(r0)) fetch_q(r0, 0);
     Cursor c1 = c0, c2, c3;
     Rec r1 = r0, r2 = r0, r3 = r0;
     if (n_run > 1) {
         advance(c1, r0, n_cont);
         r1 = rec_info(pv, H, c1.h, c1.rec, c1.tile);
-        if (tid == 0 && via_tma(r1)) fetch_q(r1, 1);
+        if (tid == 0 && by_copy(r1)) fetch_q(r1, 1);
     }
     c2 = c1;
     if (n_run > 2) {
         advance(c2, r1, n_cont);
         r2 = rec_info(pv, H, c2.h, c2.rec, c2.tile);
-        if (tid == 0 && via_tma(r2)) fetch_q(r2, 2);
+        if (tid == 0 && by_copy(r2)) fetch_q(r2, 2);
     }
     c3 = c2;
     if (n_run > 3) {
@@ -276,16 +277,6 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
                     *reinterpret_cast<uint2 *>(smem + OFF_A + sl * 2 * BOX + off) = make_uint2(h0, h1);
                     *reinterpret_cast<uint2 *>(smem + OFF_OB + t * 2 * BOX + off) = make_uint2(l0, l1);
                 }
-            } else if (!has_tq) {
-                // qhat rows (bf16) by the threads into ring slot sl; rows past the record are zero
-                const uint16_t *src = qhat + r0.src;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int id = tid + 256 * i, r = id >> 4, c8 = id & 15;
-                    const uint4 x = r < rows ? *reinterpret_cast<const uint4 *>(src + r * KD + c8 * 8)
-                                             : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4 *>(smem + OFF_A + sl * 2 * BOX + (c8 >> 3) * BOX + sw128(r, c8 & 7)) = x;
-                }
             }
             fence_async_smem();
             fence_before();
@@ -295,7 +286,7 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
         // the next unit: its products now when they need nothing from the threads (same S_in, qhat
         // tile by TMA)
         const bool more1 = n + 1 < n_run;
-        const bool early = more1 && via_tma(r1) && c1.h == key_h && r1.seg == key_seg;
+        const bool early = more1 && by_copy(r1) && c1.h == key_h && r1.seg == key_seg;
         if (tid == 0 && early) issue_mma(r1, sl1, t ^ 1);
 
         // epilogue of unit n: fetch this thread's destination row piece while the tensor core works
@@ -327,7 +318,7 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
         m_pend &= ~(1u << t);
         fence_after();
         // ring slot sl is free again: the qhat tile three units on
-        if (tid == 0 && n + 3 < n_run && via_tma(r3)) fetch_q(r3, sl);
+        if (tid == 0 && n + 3 < n_run && by_copy(r3)) fetch_q(r3, sl);
         float d[64];
         {
             float d0[32], d1[32];
@@ -459,21 +450,16 @@ cudaError_t launch_boundary(const int32_t *plan_host, const int32_t *plan_dev, i
                               static_cast<int>(w - rec_first[rec]), static_cast<int>(next - prev));
         prev = next;
     }
-    // full 128-row output tiles and every qhat tile go through tiled TMA; a tensor shorter than one
-    // tile never uses its map (qhat tiles are then read by the threads)
-    CUtensorMap to{}, tq{};
+    // full 128-row tiles add their corrections by tiled TMA; a tensor shorter than one tile never
+    // uses the map
+    CUtensorMap to{};
     if (pv.T() >= TR && !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, TR))
-        return cudaErrorInvalidValue;
-    const long long q_rows = static_cast<long long>(H) * pv.T_cont();
-    if (q_rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int has_tq = q_rows >= TR ? 1 : 0;
-    if (has_tq && !encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, TR))
         return cudaErrorInvalidValue;
     cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(boundary_tc),
                                        static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(boundary_tc, dim3(static_cast<unsigned>(grid)), dim3(256), SMEM_ALLOC, stream, plan_dev,
-                            plan_sig(plan_host), H, runs, S_in, qhat, afin, o, final_state, to, tq, has_tq);
+                            plan_sig(plan_host), H, runs, S_in, qhat, afin, o, final_state, to);
 }
 
 // Self-test of the expiry path: one thread waits, bounded, on an mbarrier that nothing arrives on,

@@ -92,7 +92,7 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                const float *__restrict__ s_in, const unsigned char *__restrict__ pkg, uint16_t *__restrict__ o,
                float *__restrict__ A, float *__restrict__ B, float *__restrict__ fin_state,
                uint16_t *__restrict__ qhat, float *__restrict__ afin, const __grid_constant__ CUtensorMap tm_o,
-               const __grid_constant__ CUtensorMap tm_q, int withhold, float *__restrict__ xs)
+               int withhold, float *__restrict__ xs)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t s_mbar;      // W X, then the state product
@@ -313,9 +313,9 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                 if (aborted) break;
                 if constexpr (MODE != STATE_SUMMARY) {
                     // O^T[c][r] -> bf16 tile of rows r in the TMA store layout (128-byte swizzle; the
-                    // previous tile was read before the U^T handoff), then outputs (state columns) or
-                    // qhat (transition columns) go out by tiled TMA stores; a ragged last chunk by 16-byte
-                    // stores of its rows
+                    // previous tile was read before the U^T handoff), then outputs (state columns) go out
+                    // by tiled TMA stores, a ragged last chunk by 16-byte stores of its rows; qhat
+                    // (transition columns) leaves as the two boxes lie, into the piece's qhat image
                     if (!mbar_wait_warp(mbar_o, ci & 1)) bad = true;
                     fence_after();
                     {
@@ -334,23 +334,40 @@ chunk_state_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const float
                     }
                     fence_async_smem();
                     bar_sync1(NWORK);
-                    if (L == CH) {
-                        if (tid == 0) {
-                            if (kind == 0) {
-                                tma_store_3d(&tm_o, 0, h, t0, sbase + OFF_OB);
-                                tma_store_3d(&tm_o, 64, h, t0, sbase + OFF_OB + 8192);
-                            } else {
-                                const int row = static_cast<int>(static_cast<int64_t>(h) * T_cont + row0 + ci * CH);
-                                tma_store_3d(&tm_q, 0, 0, row, sbase + OFF_OB);
-                                tma_store_3d(&tm_q, 64, 0, row, sbase + OFF_OB + 8192);
+                    if (kind != 0) {
+                        // qhat image of the piece: its rows in tiles of 2 CH (the last one R_t < 2 CH rows);
+                        // box b (columns 64 b ..) of a tile holds its rows r at (b R_t + r) 128 bytes from the
+                        // tile's start, each row's 16-byte groups in the swizzled order of the box, so that
+                        // the fix-up brings a tile in with two plain bulk copies
+                        const int tq = ci >> 1, r_in = (ci & 1) * CH;
+                        const int R_t = min(2 * CH, len - tq * 2 * CH);
+                        unsigned char *const tile = reinterpret_cast<unsigned char *>(
+                            qhat + (static_cast<size_t>(h) * T_cont + row0 + tq * 2 * CH) * KD);
+                        if (L == CH) {
+                            if (tid == 0) {
+                                bulk_s2g(tile + static_cast<size_t>(r_in) * 128, sbase + OFF_OB, 8192);
+                                bulk_s2g(tile + static_cast<size_t>(R_t + r_in) * 128, sbase + OFF_OB + 8192, 8192);
+                                bulk_commit_group();
                             }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int id = tid + 256 * i, r = id >> 4, c16 = id & 15, b = c16 >> 3;
+                                if (r < L)
+                                    *reinterpret_cast<uint4 *>(tile + static_cast<size_t>(b * R_t + r_in + r) * 128 +
+                                                               (c16 & 7) * 16) =
+                                        *reinterpret_cast<const uint4 *>(base + OFF_OB + b * 8192 + r * 128 + (c16 & 7) * 16);
+                            }
+                        }
+                    } else if (L == CH) {
+                        if (tid == 0) {
+                            tma_store_3d(&tm_o, 0, h, t0, sbase + OFF_OB);
+                            tma_store_3d(&tm_o, 64, h, t0, sbase + OFF_OB + 8192);
                             bulk_commit_group();
                         }
                     } else {
-                        uint16_t *const dst_row0 = kind == 0
-                                                       ? o + (static_cast<size_t>(t0) * H + h) * VD
-                                                       : qhat + (static_cast<size_t>(h) * T_cont + row0 + ci * CH) * KD;
-                        const size_t row_stride = kind == 0 ? static_cast<size_t>(H) * VD : KD;
+                        uint16_t *const dst_row0 = o + (static_cast<size_t>(t0) * H + h) * VD;
+                        const size_t row_stride = static_cast<size_t>(H) * VD;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int id = tid + 256 * i, r = id >> 4, c16 = id & 15;
@@ -514,23 +531,17 @@ cudaError_t launch_state(const int32_t *plan_host, const int32_t *plan_dev, int 
     const long long blocks = static_cast<long long>(pv.n_items()) * H;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // full 64-row chunks leave by tiled TMA stores: outputs [T][H][V] and qhat rows [H * T_cont][K];
-    // a tensor shorter than one chunk has no full chunk, so its map stays unused
-    CUtensorMap to{}, tq{};
-    const long long q_rows = static_cast<long long>(H) * pv.T_cont();
+    // full 64-row output chunks leave by tiled TMA stores ([T][H][V]); a tensor shorter than one chunk
+    // has no full chunk, so its map stays unused
+    CUtensorMap to{};
     if (MODE != STATE_SUMMARY && pv.T() >= CH &&
         !encode_rows_3d(&to, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, pv.T(), 64, CH))
         return cudaErrorInvalidValue;
-    if (MODE == STATE_LOCAL && q_rows >= CH) {
-        if (q_rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        if (!encode_rows_3d(&tq, qhat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 1, static_cast<int>(q_rows), 64, CH))
-            return cudaErrorInvalidValue;
-    }
     cudaError_t err = set_dynamic_smem(reinterpret_cast<const void *>(chunk_state_tc<MODE>),
                                        static_cast<int>(SMEM_ALLOC));
     if (err != cudaSuccess) return err;
     return launch_dependent(chunk_state_tc<MODE>, dim3(static_cast<unsigned>(blocks)), dim3(NTHREADS), SMEM_ALLOC,
-                            stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to, tq,
+                            stream, plan_dev, plan_sig(plan_host), H, h0, s_in, pkg, o, A, B, final_state, qhat, afin, to,
                             withhold, xs);
 }
 

@@ -153,6 +153,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void *src, uin
         : "memory");
 }
 
+// Bulk (TMA) copy of 'bytes' (multiple of 16, 16-byte aligned ends) shared -> global, completing in
+// this thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
 // Tiled (tensor-map) TMA load of one 3-D box at coordinates (x, y, z) into shared memory,
 // completing its byte count on the mbarrier.  x * element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void *tmap, int x, int y, int z, uint32_t mbar)

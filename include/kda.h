@@ -237,8 +237,13 @@ enum { KDA_PACKAGE_BYTES = 123392 };
  * kda_workspace_layout -- byte offsets of the regions of the device workspace
  * for a plan and head count.  off[0..6] = qhat, fin transitions, packages, A,
  * B, S_in, total.  Each region starts on a 256-byte boundary.
- *   qhat   bf16 [H][T_cont][K]    transition-seen queries of continuing tokens
- *                                  (they only complete bf16 outputs)
+ *   qhat   bf16, H*T_cont*K       transition-seen queries of continuing tokens
+ *                                  (they only complete bf16 outputs); per head and
+ *                                  continuing piece, its rows (from the piece's qhat
+ *                                  row) in tiles of 128, the last one R rows: box b
+ *                                  (k in [64b, 64b+64)) of a tile holds row r at
+ *                                  byte (b*R + r)*128 from the tile's start, the
+ *                                  row's 16-byte groups j at ((j ^ (r & 7)) * 16)
  *   fin    fp32 [n_fin][H][K][K]  transitions of continuing pieces that end a sequence
  *   pkg    [H][n_chunks][KDA_PACKAGE_BYTES]  per-chunk operands (scratch)
  *   A      fp32 [S][H][K][K]      (used by kda_forward_segmented)

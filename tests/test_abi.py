@@ -125,7 +125,7 @@ def test_summary_workspace_matches_the_pages(kda):
 
 @pytest.mark.parametrize("name", list(workloads().keys()))
 def test_workspace_regions_hold_what_the_header_documents(kda, name):
-    """qhat bf16 [H][T_cont][K], fin fp32 [n_fin][H][K][K], packages [H][n_chunks] of
+    """qhat H*T_cont*K bf16 (per piece, 128-row tile images), fin fp32 [n_fin][H][K][K], packages [H][n_chunks] of
     KDA_PACKAGE_BYTES, then A, B, S_in, and from 16 segments on the two-level scan's scratch
     (G H K (K + V) fp32 group totals, then G H K V fp32 incoming states, G = ceil(S / ceil(sqrt S)));
     each region starts on a 256-byte boundary."""
