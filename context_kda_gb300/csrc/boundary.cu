@@ -53,9 +53,12 @@ constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // room to align the base t
 static_assert(OFF_A % 1024 == 0 && OFF_OB % 1024 == 0, "swizzled buffers");
 constexpr uint32_t TM_COLS = 256;          // two 128-column accumulators
 
-// Relative costs of the run partition, from clock stamps of full launches: a tile (full or ragged)
-// takes about 2.3 us, a final-state transition about 8 us, a new S_in split about 1.6 us.
-constexpr long long COST_TILE = 8, COST_TRANSITION = 28, COST_NEW_STATE = 5;
+// Relative costs of the run partition, fitted to the global-timer end of every CTA on a packed
+// 64-segment launch (65536 tokens, 32 heads), where the stream runs at the HBM roof: a tile about
+// 1.45 us, a final-state transition about 11.6 us, the load and split of a new S_in about 5.9 us.
+// On shorter launches, whose data stay in L2, the last two weigh less; these weights are the
+// compromise that keeps the slowest CTA nearest the mean on both.
+constexpr long long COST_TILE = 8, COST_TRANSITION = 64, COST_NEW_STATE = 24;
 constexpr int MAX_RUNS = 192;              // CTAs of one launch (one per SM)
 
 // Each CTA's run: the cursor of its first unit (head, record, unit within the record) and its length.
