@@ -28,8 +28,10 @@
 // - A full 128-row tile's correction D is rounded to bf16 into one of two shared-memory buffers and
 //   added into the outputs in memory by a tiled TMA reduce-add (bf16): the outputs never pass through
 //   the SM, so a tile costs the tensor-copy unit 512 rows of 128 bytes (qhat in, D out) instead of 768
-//   (the copy unit's row rate bounds this kernel).  Ragged tail tiles and final states are read and
-//   written by the threads directly (o + D rounded once), so nothing outside a record is ever touched.
+//   (the copy unit's row rate bounds this kernel).  Ragged tail tiles are read and written by the
+//   threads directly (o + D rounded once), so nothing outside a record is ever touched.  A final
+//   state's D (fp32) is staged in both correction buffers and added one 512-byte row per warp
+//   instruction.
 #include <algorithm>
 #include <vector>
 
@@ -292,29 +294,16 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
         const bool early = more1 && by_copy(r1) && c1.h == key_h && r1.seg == key_seg;
         if (tid == 0 && early) issue_mma(r1, sl1, t ^ 1);
 
-        // epilogue of unit n: fetch this thread's destination row piece while the tensor core works
-        // (units whose correction is not added by the copy unit)
-        const bool tl_unit = tiled(r0);
+        // epilogue of unit n: a ragged tile fetches this thread's destination row piece while the tensor
+        // core works
+        const bool tl_unit = tiled(r0), fin_unit = r0.seq >= 0;
         const int r = quad * 32 + lane;
-        const bool live = r < rows && !tl_unit;
+        const bool live = r < rows && !tl_unit && !fin_unit;
         uint4 ow[8];
-        float4 fw[16];
-        uint4 *odst = nullptr;
-        float4 *fdst = nullptr;
-        if (r0.seq < 0)
-            odst = reinterpret_cast<uint4 *>(o + (static_cast<size_t>(r0.tok + r) * H + c0.h) * VD +
-                                             hw * 64);
-        else
-            fdst = reinterpret_cast<float4 *>(final_state + ((static_cast<size_t>(r0.seq) * H + c0.h) * KD + r) * VD +
-                                              hw * 64);
+        uint4 *const odst = reinterpret_cast<uint4 *>(o + (static_cast<size_t>(r0.tok + r) * H + c0.h) * VD + hw * 64);
         if (live) {
-            if (odst) {
 #pragma unroll
-                for (int m = 0; m < 8; ++m) ow[m] = odst[m];
-            } else {
-#pragma unroll
-                for (int m = 0; m < 16; ++m) fw[m] = fdst[m];
-            }
+            for (int m = 0; m < 8; ++m) ow[m] = odst[m];
         }
         ok &= mbar_wait(smem_u32(&s_mbar[t]), (mph >> t) & 1u);
         mph ^= 1u << t;
@@ -346,22 +335,46 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
             fence_async_smem();
         }
         if (live && ok) {
-            if (odst) {
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const uint32_t ww[4] = {ow[m].x, ow[m].y, ow[m].z, ow[m].w};
-                    uint32_t nw[4];
+            for (int m = 0; m < 8; ++m) {
+                const uint32_t ww[4] = {ow[m].x, ow[m].y, ow[m].z, ow[m].w};
+                uint32_t nw[4];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        nw[p] = bf16x2_bits(__uint_as_float(ww[p] << 16) + d[8 * m + 2 * p],
-                                            __uint_as_float(ww[p] & 0xFFFF0000u) + d[8 * m + 2 * p + 1]);
-                    odst[m] = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+                for (int p = 0; p < 4; ++p)
+                    nw[p] = bf16x2_bits(__uint_as_float(ww[p] << 16) + d[8 * m + 2 * p],
+                                        __uint_as_float(ww[p] & 0xFFFF0000u) + d[8 * m + 2 * p + 1]);
+                odst[m] = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+            }
+        }
+        if (fin_unit) {
+            // D (fp32, rows r, cols c) into both correction buffers as four 32-column boxes with the
+            // 128-byte swizzle: both are free (every reduce had read its buffer before this unit's split,
+            // and the lo operand in buffer t has been read by the products)
+#pragma unroll
+            for (int qb = 0; qb < 2; ++qb) {
+                unsigned char *box = smem + OFF_OB + (2 * hw + qb) * BOX;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float *x = d + qb * 32 + 4 * j;
+                    *reinterpret_cast<float4 *>(box + sw128(r, j)) = make_float4(x[0], x[1], x[2], x[3]);
                 }
-            } else {
+            }
+            __syncthreads();
+            // final += D, one 512-byte row per warp instruction: warp w takes rows 16 w .. 16 w + 15, lane l
+            // the 16 bytes of columns 32 (l / 8) + 4 (l % 8) ..
+            const int qb = lane >> 3, j = lane & 7;
+            float4 *const frow = reinterpret_cast<float4 *>(final_state + (static_cast<size_t>(r0.seq) * H + c0.h) * KD * VD) +
+                                 (qb * 32 + 4 * j) / 4;
+            float4 fw[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    fdst[m] = make_float4(fw[m].x + d[4 * m], fw[m].y + d[4 * m + 1], fw[m].z + d[4 * m + 2],
-                                          fw[m].w + d[4 * m + 3]);
+            for (int i = 0; i < 16; ++i) fw[i] = frow[(warp * 16 + i) * (VD / 4)];
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int rr = warp * 16 + i;
+                    const float4 x = *reinterpret_cast<const float4 *>(smem + OFF_OB + qb * BOX + sw128(rr, j));
+                    frow[rr * (VD / 4)] = make_float4(fw[i].x + x.x, fw[i].y + x.y, fw[i].z + x.z, fw[i].w + x.w);
+                }
             }
         }
         // the previous unit's reduce has read its buffer, which the next unit fills
