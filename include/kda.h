@@ -337,9 +337,13 @@ size_t kda_scan_workspace_bytes(const int32_t *plan, int32_t H);
 
 /*
  * kda_apply_boundary -- fix-up from the incoming states: for every token t of
- * a continuing piece in segment j, o_t = bf16(o_local,t + S_in[j]^T qhat_t);
- * for every sequence that ends in a continuing piece of segment j,
- * final = P_end S_in[j] + final_local.
+ * a continuing piece in segment j, o_t = o_local,t + S_in[j]^T qhat_t,
+ * rounded to bf16 (in 128-token tiles the correction is rounded to bf16 and
+ * added by the memory system's bf16 add; in a shorter last tile the sum is
+ * rounded once); for every sequence that ends in a continuing piece of
+ * segment j, final = P_end S_in[j] + final_local (fp32).  Every output and
+ * final-state element receives exactly one addition, so results are
+ * deterministic.
  *   S_in        device fp32 [S][H][K][V] from kda_compose_summaries.
  *   ws          the workspace kda_segment_forward wrote (qhat and fin regions).
  *   o           in/out bf16 [T][H][V].   final_state in/out fp32 [N][H][K][V].
