@@ -22,7 +22,7 @@
 //   requested three units ahead.
 // - D = Qhat S_in is formed on the tcgen05 tensor cores (M = N = K = 128; qhat * S hi + qhat * S lo,
 //   FP32 in one of two TMEM accumulators).  The next unit's products are issued before this unit's
-//   epilogue whenever they share S_in and their qhat tile comes by TMA, so the epilogue of one unit
+//   epilogue whenever they share S_in and their qhat tile comes by copy, so the epilogue of one unit
 //   overlaps the products of the next.  A final-state transition (fp32) is split into hi/lo by the
 //   threads and takes the third product too.
 // - A full 128-row tile's correction D is rounded to bf16 into one of two shared-memory buffers and
@@ -289,7 +289,7 @@ boundary_tc(const int32_t *__restrict__ plan, PlanSig sig, int H, const __grid_c
             if (tid == 0) issue_mma(r0, sl, t);
         }
         // the next unit: its products now when they need nothing from the threads (same S_in, qhat
-        // tile by TMA)
+        // tile by copy)
         const bool more1 = n + 1 < n_run;
         const bool early = more1 && by_copy(r1) && c1.h == key_h && r1.seg == key_seg;
         if (tid == 0 && early) issue_mma(r1, sl1, t ^ 1);
