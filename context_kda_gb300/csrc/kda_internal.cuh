@@ -73,7 +73,7 @@ enum { PC_START = 0, PC_LEN = 1, PC_SEQ = 2, PC_SEG = 3, PC_FLAGS = 4, PC_CONT =
 
 // Workspace regions resolved to typed device pointers.
 struct Workspace {
-    uint16_t *qhat;       // [H][T_cont][K] bf16
+    uint16_t *qhat;       // H * T_cont * K bf16: per continuing piece, 128-row tile images
     float *afin;          // [n_fin][H][K][K]
     unsigned char *pkg;   // [H][n_chunks][KDA_PACKAGE_BYTES]
     float *A;             // [S][H][K][K]
